@@ -1,0 +1,128 @@
+/*
+ * gma.h -- C ABI of libgma.so: the forward pass of Gaussian Mixture Attention
+ * (GMA) on one NVIDIA GB300 (sm_103a).
+ *
+ * Method: "Gaussian Mixture Attention: Linear-Time Sequence Mixing via
+ * Probabilistic Latent Routing" (Huang & Raza, arXiv 2606.18283), as described
+ * on the gist.science technical summaries ("Core mechanism" items 1-2,
+ * "Variants and training" item 3) and in the English abstract on fugumt.com.
+ *
+ *   gamma_ik = p(z = k | x_i)             GMM posterior over K diagonal Gaussians
+ *                                         with means mu_k, variances sigma2_k and
+ *                                         priors pi_k, shared by queries and keys
+ *   Vt = Gamma_K^T V,  Z = Gamma_K^T 1    write phase (K-slot latent memory)
+ *   O  = Gamma_Q Vt / (Gamma_Q Z + eps)   read phase
+ *   causal: Vt, Z replaced by inclusive prefix sums over key positions j <= i.
+ *
+ * Conventions shared by every entry point:
+ *   - Every pointer argument except `p` is a DEVICE pointer (cudaMalloc'd or
+ *     equivalent) owned by the caller.  The library allocates and frees
+ *     nothing; scratch memory is the caller's workspace `ws`.
+ *   - Tensors are dense, row-major, innermost dimension last:
+ *       Q, K, X : [B, H, N, d]      V, O : [B, H, N, dv]
+ *       mu, sigma2 : [H, K, d] float32      log_pi : [H, K] float32
+ *     Q, K, X, V, O use the I/O dtype `p->dtype`; every base pointer must be
+ *     16-byte aligned, ws 256-byte aligned.
+ *   - sigma2 is the variance after the caller's reparametrisation and floor
+ *     (softplus + lower bound), must be > 0; log_pi is the log prior (any
+ *     constant offset per head cancels).  One component set per head routes
+ *     both queries and keys.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *     asynchronous on it; argument errors are returned before anything is
+ *     launched.  No C++ exception crosses this interface.
+ *   - A device-side wait that runs out of time sets an error word in `ws`
+ *     (never a trap); gma_check_device_error() reports it.
+ *   - Supported in this version: d == dv == 64, 1 <= K <= 256, N >= 0
+ *     (N == 0 is a no-op), B, H >= 1, B*H*N < 2^31.
+ *   - Precision: dtype GMA_F32 computes in float32 on the CUDA cores;
+ *     GMA_BF16 runs the log-density contraction with fp16 operands and the
+ *     write/read contractions with bf16 operands on the tcgen05 tensor cores,
+ *     all accumulated in float32; the output is rounded to bf16 (RNE).
+ *     For GMA_BF16, |q|, |k| must stay below 255 (fp16 range of q^2).
+ */
+#ifndef GMA_H_
+#define GMA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GMA_OK = 0,
+  GMA_ERR_INVALID_ARG = 1, /* null pointer, bad shape, misalignment, eps < 0 */
+  GMA_ERR_UNSUPPORTED = 2, /* d, dv, K or dtype outside what this build runs */
+  GMA_ERR_WORKSPACE = 3,   /* ws_bytes smaller than gma_workspace_bytes() */
+  GMA_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
+  GMA_ERR_TIMEOUT = 5      /* a bounded device wait gave up (see ws error word) */
+} gma_status_t;
+
+typedef enum { GMA_F32 = 0, GMA_BF16 = 1 } gma_dtype_t;
+
+typedef enum { GMA_OP_RESPONSIBILITIES = 0, GMA_OP_BIDIR = 1, GMA_OP_CAUSAL = 2 } gma_op_t;
+
+typedef struct {
+  int B, H, N; /* batch, heads, sequence length */
+  int d, dv;   /* routing (query/key) width and value width; both 64 */
+  int K;       /* mixture components per head */
+  gma_dtype_t dtype;
+  float eps;   /* read-phase denominator offset, >= 0 */
+} gma_problem_t;
+
+/* Bytes of device workspace `op` needs for problem `p` (0 if p is invalid). */
+size_t gma_workspace_bytes(const gma_problem_t *p, gma_op_t op);
+
+/*
+ * Responsibilities Gamma = p(z | x) of routing vectors X.
+ * Passage: gist.science summary, "Core mechanism" item 1 (standard GMM
+ * posterior with learned mu_k, diagonal Sigma_k, prior pi_k).
+ *   X      [B,H,N,d] in p->dtype        gamma_out [B,H,N,K] float32 (written)
+ * Rows of gamma_out are non-negative and sum to 1.
+ */
+gma_status_t gma_responsibilities(const gma_problem_t *p, const void *X, const float *mu, const float *sigma2,
+                                  const float *log_pi, float *gamma_out, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Bidirectional GMA forward: O = Gamma_Q (Gamma_K^T V) / (Gamma_Q (Gamma_K^T 1) + eps).
+ * Passage: gist.science summary, "Core mechanism" item 2 (write phase, read
+ * phase); "Variants and training" item 3 (bidirectional form).
+ *   Q, K [B,H,N,d], V [B,H,N,dv] in p->dtype;  O [B,H,N,dv] in p->dtype (written).
+ * O may not alias any input.
+ */
+gma_status_t gma_forward_bidir(const gma_problem_t *p, const void *Q, const void *K, const void *V, const float *mu,
+                               const float *sigma2, const float *log_pi, void *O, void *ws, size_t ws_bytes,
+                               void *stream);
+
+/*
+ * Causal GMA forward: row i uses the inclusive prefix sums over keys j <= i,
+ *   O_i = gamma_Qi . (sum_{j<=i} gamma_Kj v_j^T) / (gamma_Qi . sum_{j<=i} gamma_Kj + eps).
+ * Passage: gist.science summary, "Variants and training" item 3 (prefix sums
+ * of the latent memory and normaliser; O at position i depends on j <= i only).
+ * Same arguments and layouts as gma_forward_bidir.
+ */
+gma_status_t gma_forward_causal(const gma_problem_t *p, const void *Q, const void *K, const void *V, const float *mu,
+                                const float *sigma2, const float *log_pi, void *O, void *ws, size_t ws_bytes,
+                                void *stream);
+
+/*
+ * Synchronises `stream`, then reads the error word kept at the start of `ws`:
+ * GMA_OK if no device wait timed out since the word was last cleared (every
+ * forward/responsibilities call clears it when it starts), GMA_ERR_TIMEOUT if
+ * one did, GMA_ERR_CUDA if the synchronisation itself failed.  `ws` must be a
+ * workspace previously passed to one of the calls above.
+ */
+gma_status_t gma_check_device_error(void *ws, void *stream);
+
+/* Static, NUL-terminated description of a status code. */
+const char *gma_status_string(gma_status_t s);
+
+/* ABI version of this library: (major << 16) | minor. */
+int gma_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GMA_H_ */

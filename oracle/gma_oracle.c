@@ -1,0 +1,232 @@
+/*
+ * gma_oracle.c -- plain float64 CPU oracle for the Gaussian Mixture Attention
+ * (GMA) forward pass.  TEST INFRASTRUCTURE ONLY: the tests, the package's
+ * smoke check and the CPU-baseline leg of the benchmark call it; the product
+ * path never does.  It shares no source with the CUDA library.
+ *
+ * Source: "Gaussian Mixture Attention: Linear-Time Sequence Mixing via
+ * Probabilistic Latent Routing" (Huang & Raza, arXiv 2606.18283), as summarised
+ * on gist.science (ja / de technical summaries) and in the English abstract on
+ * fugumt.com.  Citations below name the page and its section.
+ *
+ *   [R]  Responsibilities: gist.science summary, "Core mechanism" item 1
+ *        (probabilistic latent routing): gamma_{i,k} = p(z = k | x) from the
+ *        standard GMM posterior with means mu_k, diagonal covariances Sigma_k and
+ *        priors pi_k; queries and keys share one set of components (abstract:
+ *        "shared latent routing space").
+ *   [W]  Write phase: same section, item 2: Vt = Gamma_K^T V, Z = Gamma_K^T 1.
+ *   [Rd] Read phase: same section, item 2: O = Gamma_Q Vt / (Gamma_Q Z + eps).
+ *   [C]  Causal variant: "Variants and training" item 3: prefix sums of the
+ *        latent memory and the normaliser so that O_i depends on j <= i only.
+ *
+ * Readings where the pages leave a step open:
+ *   - The log-density keeps every term of the diagonal Gaussian, including
+ *     -1/2 sum_d log sigma2_kd and -(d/2) log(2 pi); the last one cancels in
+ *     the posterior but is kept so the formula reads like the textbook one.
+ *   - The routing vector x is the head's query / key row itself.
+ *   - eps is added once to the scalar denominator of each output row.
+ *   - The causal sum is inclusive: position i sees keys j = 0..i.
+ *
+ * Everything is computed in the centered form sum_d (x_d - mu_kd)^2 / sigma2_kd,
+ * with a max-subtracted log-sum-exp over the K components.  Work is split over
+ * (batch, head) units across threads; each unit is computed by the plain
+ * sequential code below, so threading does not change any arithmetic.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define GMA_ORACLE_LOG_2PI 1.8378770664093454835606594728112
+
+/* [R] posterior responsibilities of one routing vector x (length d) over the
+ * K components of one head.  mu, sigma2: [K][d]; log_pi: [K]; out: [K]. */
+static void posterior(int d, int K, const double *x, const double *mu, const double *sigma2,
+                      const double *log_pi, double *out) {
+  double m = -INFINITY;
+  for (int k = 0; k < K; ++k) {
+    double quad = 0.0, logdet = 0.0;
+    for (int j = 0; j < d; ++j) {
+      double diff = x[j] - mu[(size_t)k * d + j];
+      quad += diff * diff / sigma2[(size_t)k * d + j];
+      logdet += log(sigma2[(size_t)k * d + j]);
+    }
+    /* log pi_k + log N(x; mu_k, diag(sigma2_k)) */
+    double l = log_pi[k] - 0.5 * (quad + logdet) - 0.5 * d * GMA_ORACLE_LOG_2PI;
+    out[k] = l;
+    if (l > m) m = l;
+  }
+  double s = 0.0;
+  for (int k = 0; k < K; ++k) {
+    out[k] = exp(out[k] - m);
+    s += out[k];
+  }
+  for (int k = 0; k < K; ++k) out[k] /= s;
+}
+
+typedef struct {
+  int mode; /* 0 = responsibilities, 1 = bidirectional, 2 = causal */
+  int B, H, N, d, dv, K;
+  const double *Q, *Kx, *V, *mu, *sigma2, *log_pi;
+  double eps;
+  const int64_t *rows; /* sorted ascending, or NULL for every row */
+  int64_t nrows;
+  double *out;
+  int nthreads;
+  int next_unit;
+  pthread_mutex_t lock;
+} job_t;
+
+/* One (b, h) unit. */
+static void run_unit(job_t *J, int unit) {
+  const int H = J->H, N = J->N, d = J->d, dv = J->dv, K = J->K;
+  const int h = unit % H;
+  const double *mu = J->mu + (size_t)h * K * d;
+  const double *s2 = J->sigma2 + (size_t)h * K * d;
+  const double *lp = J->log_pi + (size_t)h * K;
+  const int64_t nout = J->rows ? J->nrows : N;
+  double *g = (double *)malloc(sizeof(double) * K);
+
+  if (J->mode == 0) {
+    const double *X = J->Q + (size_t)unit * N * d;
+    double *G = J->out + (size_t)unit * nout * K;
+    for (int64_t r = 0; r < nout; ++r) {
+      int64_t i = J->rows ? J->rows[r] : r;
+      posterior(d, K, X + i * d, mu, s2, lp, G + r * K);
+    }
+    free(g);
+    return;
+  }
+
+  const double *Q = J->Q + (size_t)unit * N * d;
+  const double *Kx = J->Kx + (size_t)unit * N * d;
+  const double *V = J->V + (size_t)unit * N * dv;
+  double *O = J->out + (size_t)unit * nout * dv;
+  double *Vt = (double *)calloc((size_t)K * dv, sizeof(double)); /* latent memory, K x dv */
+  double *Z = (double *)calloc((size_t)K, sizeof(double));       /* normaliser, K */
+
+  if (J->mode == 1) {
+    /* [W] write phase over all N keys */
+    for (int j = 0; j < N; ++j) {
+      posterior(d, K, Kx + (size_t)j * d, mu, s2, lp, g);
+      for (int k = 0; k < K; ++k) {
+        Z[k] += g[k];
+        for (int c = 0; c < dv; ++c) Vt[(size_t)k * dv + c] += g[k] * V[(size_t)j * dv + c];
+      }
+    }
+    /* [Rd] read phase for the requested query rows */
+    for (int64_t r = 0; r < nout; ++r) {
+      int64_t i = J->rows ? J->rows[r] : r;
+      posterior(d, K, Q + i * d, mu, s2, lp, g);
+      double den = 0.0;
+      for (int k = 0; k < K; ++k) den += g[k] * Z[k];
+      den += J->eps;
+      for (int c = 0; c < dv; ++c) {
+        double num = 0.0;
+        for (int k = 0; k < K; ++k) num += g[k] * Vt[(size_t)k * dv + c];
+        O[r * dv + c] = num / den;
+      }
+    }
+  } else {
+    /* [C] running prefix sums, inclusive of the current position */
+    int64_t r = 0;
+    for (int64_t i = 0; i < N && r < nout; ++i) {
+      posterior(d, K, Kx + i * d, mu, s2, lp, g);
+      for (int k = 0; k < K; ++k) {
+        Z[k] += g[k];
+        for (int c = 0; c < dv; ++c) Vt[(size_t)k * dv + c] += g[k] * V[i * dv + c];
+      }
+      int64_t want = J->rows ? J->rows[r] : i;
+      if (want != i) continue;
+      posterior(d, K, Q + i * d, mu, s2, lp, g);
+      double den = 0.0;
+      for (int k = 0; k < K; ++k) den += g[k] * Z[k];
+      den += J->eps;
+      for (int c = 0; c < dv; ++c) {
+        double num = 0.0;
+        for (int k = 0; k < K; ++k) num += g[k] * Vt[(size_t)k * dv + c];
+        O[r * dv + c] = num / den;
+      }
+      ++r;
+    }
+  }
+  free(Vt);
+  free(Z);
+  free(g);
+}
+
+static void *worker(void *arg) {
+  job_t *J = (job_t *)arg;
+  for (;;) {
+    pthread_mutex_lock(&J->lock);
+    int u = J->next_unit++;
+    pthread_mutex_unlock(&J->lock);
+    if (u >= J->B * J->H) break;
+    run_unit(J, u);
+  }
+  return NULL;
+}
+
+static int run_job(job_t *J) {
+  int nt = J->nthreads < 1 ? 1 : J->nthreads;
+  if (nt > J->B * J->H) nt = J->B * J->H;
+  if (nt < 1) return 0;
+  J->next_unit = 0;
+  pthread_mutex_init(&J->lock, NULL);
+  pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * nt);
+  int started = 0;
+  for (int t = 0; t < nt; ++t)
+    if (pthread_create(&th[t], NULL, worker, J) == 0) ++started;
+  if (started == 0) worker(J);
+  for (int t = 0; t < started; ++t) pthread_join(th[t], NULL);
+  free(th);
+  pthread_mutex_destroy(&J->lock);
+  return 0;
+}
+
+/* Gamma [B,H,nrows or N,K] of routing vectors X [B,H,N,d]. */
+int gma_oracle_responsibilities(int B, int H, int N, int d, int K, const double *X, const double *mu,
+                                const double *sigma2, const double *log_pi, const int64_t *rows, int64_t nrows,
+                                double *gamma, int nthreads) {
+  job_t J;
+  memset(&J, 0, sizeof J);
+  J.mode = 0; J.B = B; J.H = H; J.N = N; J.d = d; J.dv = 0; J.K = K;
+  J.Q = X; J.mu = mu; J.sigma2 = sigma2; J.log_pi = log_pi;
+  J.rows = rows; J.nrows = nrows; J.out = gamma; J.nthreads = nthreads;
+  return run_job(&J);
+}
+
+/* O [B,H,nrows or N,dv]; causal = 0 bidirectional, 1 causal. */
+int gma_oracle_forward(int causal, int B, int H, int N, int d, int dv, int K, const double *Q, const double *Kx,
+                       const double *V, const double *mu, const double *sigma2, const double *log_pi, double eps,
+                       const int64_t *rows, int64_t nrows, double *O, int nthreads) {
+  job_t J;
+  memset(&J, 0, sizeof J);
+  J.mode = causal ? 2 : 1; J.B = B; J.H = H; J.N = N; J.d = d; J.dv = dv; J.K = K;
+  J.Q = Q; J.Kx = Kx; J.V = V; J.mu = mu; J.sigma2 = sigma2; J.log_pi = log_pi; J.eps = eps;
+  J.rows = rows; J.nrows = nrows; J.out = O; J.nthreads = nthreads;
+  return run_job(&J);
+}
+
+/* Latent memory Vt [B,H,K,dv] and normaliser Z [B,H,K] over all N keys ([W]). */
+int gma_oracle_state(int B, int H, int N, int d, int dv, int K, const double *Kx, const double *V, const double *mu,
+                     const double *sigma2, const double *log_pi, double *Vt, double *Z) {
+  double *g = (double *)malloc(sizeof(double) * (K > 0 ? K : 1));
+  for (int u = 0; u < B * H; ++u) {
+    int h = u % H;
+    double *vt = Vt + (size_t)u * K * dv, *z = Z + (size_t)u * K;
+    memset(vt, 0, sizeof(double) * K * dv);
+    memset(z, 0, sizeof(double) * K);
+    for (int j = 0; j < N; ++j) {
+      posterior(d, K, Kx + ((size_t)u * N + j) * d, mu + (size_t)h * K * d, sigma2 + (size_t)h * K * d,
+                log_pi + (size_t)h * K, g);
+      for (int k = 0; k < K; ++k) {
+        z[k] += g[k];
+        for (int c = 0; c < dv; ++c) vt[(size_t)k * dv + c] += g[k] * V[((size_t)u * N + j) * dv + c];
+      }
+    }
+  }
+  free(g);
+  return 0;
+}

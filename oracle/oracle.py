@@ -1,0 +1,138 @@
+"""Python face of the float64 CPU oracle (``gma_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY.  The tests, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may call this module; the library path never
+does, and this module imports nothing from the CUDA package.
+
+What it computes follows the Gaussian Mixture Attention pages (gist.science
+technical summaries, "Core mechanism" items 1-2 and "Variants and training"
+item 3; fugumt.com English abstract):
+
+* ``responsibilities``: gamma_ik = p(z=k | x_i) under a K-component diagonal
+  GMM with priors pi_k (standard GMM posterior).
+* ``forward(causal=False)``: Vt = Gamma_K^T V, Z = Gamma_K^T 1,
+  O = Gamma_Q Vt / (Gamma_Q Z + eps).
+* ``forward(causal=True)``: the same with inclusive prefix sums over keys.
+* ``state``: Vt and Z alone.
+
+All inputs are converted to float64 here; the C code is plain sequential
+float64 arithmetic per (batch, head) unit.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gma_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libgma_oracle.so")
+_lib = None
+
+
+def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH) -> str:
+    """Compile the C oracle with gcc (-O2, no fast-math) into ``out``."""
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src):
+        return out
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    tmp = out + ".tmp%d" % os.getpid()
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math", "-ffp-contract=off",
+           "-o", tmp, src, "-lm", "-lpthread"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def _load(path: str | None = None):
+    global _lib
+    if path is not None:
+        lib = ctypes.CDLL(path)
+    else:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+    dp = ctypes.POINTER(ctypes.c_double)
+    i64p = ctypes.POINTER(ctypes.c_int64)
+    ci, cl = ctypes.c_int, ctypes.c_int64
+    lib.gma_oracle_responsibilities.argtypes = [ci, ci, ci, ci, ci, dp, dp, dp, dp, i64p, cl, dp, ci]
+    lib.gma_oracle_responsibilities.restype = ci
+    lib.gma_oracle_forward.argtypes = [ci, ci, ci, ci, ci, ci, ci, dp, dp, dp, dp, dp, dp, ctypes.c_double,
+                                       i64p, cl, dp, ci]
+    lib.gma_oracle_forward.restype = ci
+    lib.gma_oracle_state.argtypes = [ci, ci, ci, ci, ci, ci, dp, dp, dp, dp, dp, dp, dp]
+    lib.gma_oracle_state.restype = ci
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def default_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _rows(rows, N):
+    if rows is None:
+        return None, 0, None
+    r = np.unique(np.asarray(rows, dtype=np.int64))
+    if r.size and (r[0] < 0 or r[-1] >= N):
+        raise ValueError("row index out of range")
+    return r, r.size, r.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
+
+
+def responsibilities(X, mu, sigma2, log_pi, rows=None, nthreads=None, lib=None):
+    """Gamma [B,H,N|len(rows),K] for X [B,H,N,d] with per-head mu, sigma2 [H,K,d], log_pi [H,K]."""
+    X, mu, sigma2, log_pi = _f64(X), _f64(mu), _f64(sigma2), _f64(log_pi)
+    B, H, N, d = X.shape
+    K = mu.shape[1]
+    assert mu.shape == (H, K, d) and sigma2.shape == (H, K, d) and log_pi.shape == (H, K)
+    r, nr, rp = _rows(rows, N)
+    out = np.empty((B, H, nr if r is not None else N, K), dtype=np.float64)
+    lib = lib or _load()
+    lib.gma_oracle_responsibilities(B, H, N, d, K, _ptr(X), _ptr(mu), _ptr(sigma2), _ptr(log_pi), rp, nr,
+                                    _ptr(out), nthreads or default_threads())
+    return out
+
+
+def forward(Q, Kx, V, mu, sigma2, log_pi, eps, causal=False, rows=None, nthreads=None, lib=None):
+    """O [B,H,N|len(rows),dv].  ``rows`` (sorted unique indices) limits which outputs are formed."""
+    Q, Kx, V = _f64(Q), _f64(Kx), _f64(V)
+    mu, sigma2, log_pi = _f64(mu), _f64(sigma2), _f64(log_pi)
+    B, H, N, d = Q.shape
+    dv = V.shape[-1]
+    K = mu.shape[1]
+    assert Kx.shape == Q.shape and V.shape[:3] == (B, H, N)
+    assert mu.shape == (H, K, d) and sigma2.shape == (H, K, d) and log_pi.shape == (H, K)
+    r, nr, rp = _rows(rows, N)
+    out = np.empty((B, H, nr if r is not None else N, dv), dtype=np.float64)
+    lib = lib or _load()
+    lib.gma_oracle_forward(1 if causal else 0, B, H, N, d, dv, K, _ptr(Q), _ptr(Kx), _ptr(V), _ptr(mu),
+                           _ptr(sigma2), _ptr(log_pi), float(eps), rp, nr, _ptr(out), nthreads or default_threads())
+    return out
+
+
+def state(Kx, V, mu, sigma2, log_pi, lib=None):
+    """(Vt [B,H,K,dv], Z [B,H,K]) summed over all keys."""
+    Kx, V = _f64(Kx), _f64(V)
+    mu, sigma2, log_pi = _f64(mu), _f64(sigma2), _f64(log_pi)
+    B, H, N, d = Kx.shape
+    dv = V.shape[-1]
+    K = mu.shape[1]
+    Vt = np.empty((B, H, K, dv), dtype=np.float64)
+    Z = np.empty((B, H, K), dtype=np.float64)
+    lib = lib or _load()
+    lib.gma_oracle_state(B, H, N, d, dv, K, _ptr(Kx), _ptr(V), _ptr(mu), _ptr(sigma2), _ptr(log_pi), _ptr(Vt), _ptr(Z))
+    return Vt, Z
