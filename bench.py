@@ -1,0 +1,408 @@
+#!/usr/bin/env python
+"""GMA forward throughput on one GB300: tokens*heads/s at K=256, bidirectional + causal.
+
+One step = one bidirectional and one causal forward over the workload (both forms of the hot
+path).  Prints ONE JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gma|reference]
+
+--impl reference times the float64 CPU oracle (the only baseline that exists for this method)
+on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gaussian_mixture_sequence_gma_gb300.inputs import bf16_bits, make_workload, workloads  # noqa: E402
+
+WORKLOAD = "sweep_bf16_B1H8N131072K256"
+METRIC = "GMA fwd tokens*heads/s at K=256 (bidir & causal)"
+UNIT = "tokens*heads/s"
+SWEEP = (4096, 16384, 65536, 131072)
+MUFU_EX2_PER_S = 9.58e12  # measured ex2.approx.f32 throughput on this machine's GB300 (profiles/peaks_probe.md)
+CPU_SAMPLE_N = 8192       # positions of the workload the oracle baseline processes
+
+
+def flop_per_tokhead(K, d=64, dv=64):
+    """Algorithmic FLOPs per token*head for both forms' shared work: logits for q and k
+    (2 * 2*(2d)*K) plus write and read contractions with the normaliser column (2 * 2*K*(dv+1))."""
+    return 8 * d * K + 4 * K * (dv + 1)
+
+
+# Algorithmic FLOPs per token*head assigned to each kernel (every algorithmic op counted once;
+# recomputation and the causal intra-chunk term are kernel overhead).
+def kernel_flops(name, K, d=64, dv=64):
+    half = 2 * 2 * d * K + 2 * K * (dv + 1)  # one side's logits + one of write/read
+    table = {
+        "simt_write": half, "simt_read": half, "simt_causal": half,
+        "tc_bidir_write": half, "tc_bidir_read": half, "tc_causal_aggregate": half, "tc_causal_chunk": half,
+    }
+    return table.get(name, 0)
+
+
+def kernel_bound(name):
+    return "tensor" if name.startswith("tc_") else "alu"
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return dict(hbm=j["hbm_gbs"], bf16=j["bf16_tflops"], bf16_sus=j.get("bf16_tflops_sustained"),
+                    sm_max_mhz=j.get("sm_max_mhz", 2070.0), source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, sm_max_mhz=2070.0, source="fallback")
+
+
+def traffic_for(name):
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current source."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(p):
+        return None
+    src = os.path.join(ROOT, "gaussian_mixture_sequence_gma_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(src)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(src, f), "rb").read())
+    sha = h.hexdigest()[:16]
+    for line in open(p):
+        parts = line.split()
+        if len(parts) >= 3 and not line.startswith("#") and parts[0] == name and parts[2] == sha:
+            return float(parts[1])
+    return None
+
+
+class ClockSampler:
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.windows = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def mark(self, t0, t1):
+        self.windows.append((t0, t1))
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = []
+        for line in out.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[4:]))
+            except (ValueError, IndexError):
+                continue
+        inside = [r for r in rows if any(t0 - 0.06 <= r[0] <= t1 + 0.06 for t0, t1 in self.windows)]
+        use = inside if inside else rows
+        if not use:
+            return None
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in use:
+            for n, v in zip(names[1:], r[3][1:]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median([r[1] for r in use])), "sm_max_mhz": float(max(r[2] for r in use)),
+                "reasons": sorted(reasons), "samples": len(use), "in_window": bool(inside)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def oracle_sample(inp, n_pos):
+    """Float64 oracle over the first n_pos positions of every (b, h): bidir + causal.  Returns
+    (seconds, token*heads processed, threads used)."""
+    from oracle import oracle as orc
+    sl = {k: np.ascontiguousarray(inp[k][:, :, :n_pos]) for k in ("Q", "K", "V")}
+    B, H = sl["Q"].shape[:2]
+    threads = orc.default_threads()
+    t0 = time.perf_counter()
+    for causal in (False, True):
+        orc.forward(sl["Q"], sl["K"], sl["V"], inp["mu"], inp["sigma2"], inp["log_pi"], 1e-6, causal=causal,
+                    nthreads=threads)
+    dt = time.perf_counter() - t0
+    return dt, 2 * B * H * n_pos, min(threads, B * H)
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    w = workloads()[args.workload]
+    inp = make_workload(w)
+    n_pos = min(args.ref_positions, w.N)
+    for _ in range(args.warmup):
+        oracle_sample(inp, n_pos)
+    total_t, total_units, cores = 0.0, 0, 1
+    for _ in range(args.steps):
+        dt, units, cores = oracle_sample(inp, n_pos)
+        total_t += dt
+        total_units += units
+    value = total_units / total_t
+    sample = "first %d positions of every (b,h) of %s, bidirectional + causal, float64 oracle" % (n_pos, w.name)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded; shapes and distributions of the workload)",
+            "config": config_dict(w),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_dict(w):
+    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "K": w.K, "d": w.d, "dv": w.dv,
+            "forms": "bidirectional + causal per step", "io_dtype": w.dtype,
+            "l2": "inputs larger than L2 (Q,K,V = %.0f MB > 129 MB); no flush" % (3 * w.B * w.H * w.N * 64 * 2 / 1e6),
+            "parallelism": "one process per GPU, independent replicas of the workload"}
+
+
+def to_dev(inp, dev):
+    import torch
+    t = {k: torch.from_numpy(inp[k]).to(dev) for k in ("mu", "sigma2", "log_pi")}
+    for k in ("Q", "K", "V"):
+        t[k] = torch.from_numpy(bf16_bits(inp[k]).view(np.int16)).to(dev).view(torch.bfloat16)
+    return t
+
+
+def run_gma(args, world, rank, local):
+    import torch
+    import torch.distributed as dist
+
+    from gaussian_mixture_sequence_gma_gb300 import gma
+
+    if world > 1:
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peaks = load_peaks()
+    w = workloads()[args.workload]
+    B, H, N, K = w.B, w.H, w.N, w.K
+    inp = make_workload(w)
+    t = to_dev(inp, dev)
+    stream = torch.cuda.current_stream(dev)
+    prob_b = gma.problem(B, H, N, K, torch.bfloat16, w.eps)
+    ws_b = gma.alloc_workspace(prob_b, gma.OP_BIDIR, dev)
+    ws_c = gma.alloc_workspace(prob_b, gma.OP_CAUSAL, dev)
+    Ob = torch.empty((B, H, N, w.dv), dtype=torch.bfloat16, device=dev)
+    Oc = torch.empty_like(Ob)
+
+    def step(q, k, v):
+        gma.forward_bidir(q, k, v, t["mu"], t["sigma2"], t["log_pi"], w.eps, out=Ob, workspace=ws_b)
+        gma.forward_causal(q, k, v, t["mu"], t["sigma2"], t["log_pi"], w.eps, out=Oc, workspace=ws_c)
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    def timed(fn, n):
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        w0 = time.time()
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        barrier()
+        w1 = time.time()
+        ms = e0.elapsed_time(e1)
+        if world > 1:
+            x = torch.tensor([ms], device=dev)
+            dist.all_reduce(x, op=dist.ReduceOp.MAX)
+            ms = float(x.item())
+        return ms, (w0, w1)
+
+    clocks = ClockSampler(local)
+    for _ in range(args.warmup):
+        step(t["Q"], t["K"], t["V"])
+    if gma.check_device_error(ws_b) != gma.GMA_OK or gma.check_device_error(ws_c) != gma.GMA_OK:
+        raise RuntimeError("device wait timed out during warm-up")
+    clocks.start()
+    n0 = gma.launch_count()
+    ms, win = timed(lambda: step(t["Q"], t["K"], t["V"]), args.steps)
+    launches = gma.launch_count() - n0
+    clocks.mark(*win)
+    ms_per_step = ms / args.steps
+    units_per_step = 2 * B * H * N
+    value = world * units_per_step / (ms_per_step * 1e-3)
+
+    # per-kernel durations (events on the launch stream), same step loop
+    gma.profile_enable(True)
+    _, win = timed(lambda: step(t["Q"], t["K"], t["V"]), args.steps)
+    gma.profile_enable(False)
+    clocks.mark(*win)
+    prof = gma.profile_read()
+
+    # end to end through the public API with host buffers: H2D of Q,K,V and D2H of both outputs per step
+    host = {k: torch.from_numpy(bf16_bits(inp[k]).view(np.int16)).view(torch.bfloat16).pin_memory()
+            for k in ("Q", "K", "V")}
+    dq, dk, dv_ = (torch.empty_like(t["Q"]), torch.empty_like(t["K"]), torch.empty_like(t["V"]))
+    hb = torch.empty(Ob.shape, dtype=torch.bfloat16).pin_memory()
+    hc = torch.empty(Oc.shape, dtype=torch.bfloat16).pin_memory()
+
+    def e2e_step():
+        dq.copy_(host["Q"], non_blocking=True)
+        dk.copy_(host["K"], non_blocking=True)
+        dv_.copy_(host["V"], non_blocking=True)
+        step(dq, dk, dv_)
+        hb.copy_(Ob, non_blocking=True)
+        hc.copy_(Oc, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    e2e_ms, win = timed(e2e_step, args.steps)
+    clocks.mark(*win)
+    clk = clocks.stop()
+    e2e_value = world * units_per_step / (e2e_ms / args.steps * 1e-3)
+    h2d = sum(host[k].numel() * 2 for k in ("Q", "K", "V"))
+    d2h = (hb.numel() + hc.numel()) * 2
+
+    if gma.check_device_error(ws_b) != gma.GMA_OK or gma.check_device_error(ws_c) != gma.GMA_OK:
+        raise RuntimeError("device wait timed out in the timed region")
+
+    # roofline of the dominant kernel
+    dom = max(prof.items(), key=lambda kv: kv[1][1]) if prof else None
+    roof = None
+    if dom:
+        name, (cnt, tot_ms) = dom
+        avg_s = tot_ms / cnt * 1e-3
+        bound = kernel_bound(name)
+        fl = kernel_flops(name, K) * B * H * N
+        achieved = fl / avg_s / 1e12
+        if bound == "tensor":
+            peak, unit, src = peaks["bf16"], "TFLOP/s", "bf16 dense, %s (burst)" % peaks["source"]
+        else:
+            peak = 152 * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
+            unit, src = "TFLOP/s", "fp32 FFMA: 152 SMs x 128 lanes x 2 flop x max SM clock (derived)"
+        tr = traffic_for(name)
+        roof = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+                "traffic": tr, "kernel": name, "avg_launch_us": avg_s * 1e6, "peak_source": src}
+        if bound == "tensor" and peaks.get("bf16_sus"):
+            roof["frac_of_sustained"] = achieved / peaks["bf16_sus"]
+
+    # whole-path roofline (spec definition): slowest of tensor, MUFU and HBM per token*head
+    t_tensor = flop_per_tokhead(K) / (peaks["bf16"] * 1e12)
+    t_mufu = 2 * K / MUFU_EX2_PER_S
+    t_hbm = 4 * 64 * 2 / (peaks["hbm"] * 1e9)
+    bound_rate = 1.0 / max(t_tensor, t_mufu, t_hbm)
+    path = {"bound_tok_heads_per_s": bound_rate, "frac": value / world / bound_rate,
+            "binding": ["tensor", "mufu", "hbm"][int(np.argmax([t_tensor, t_mufu, t_hbm]))],
+            "per_form_ms": {}}
+    kernels = {k: {"launches": c, "total_ms": m, "avg_us": 1e3 * m / c} for k, (c, m) in prof.items()}
+
+    # per-form times and the long-context sweep (time and peak memory vs N)
+    sweep = {}
+    if args.sweep and rank == 0 and world == 1:
+        for n in SWEEP:
+            wi = workloads()["sweep_bf16_B1H8N%dK256" % n]
+            ii = make_workload(wi) if n != N else inp
+            ti = to_dev(ii, dev) if n != N else t
+            pb = gma.problem(wi.B, wi.H, n, wi.K, torch.bfloat16, wi.eps)
+            entry = {}
+            for form, op, fn in (("bidir", gma.OP_BIDIR, gma.forward_bidir), ("causal", gma.OP_CAUSAL, gma.forward_causal)):
+                ws = gma.alloc_workspace(pb, op, dev)
+                out = torch.empty((wi.B, wi.H, n, 64), dtype=torch.bfloat16, device=dev)
+                for _ in range(3):
+                    fn(ti["Q"], ti["K"], ti["V"], ti["mu"], ti["sigma2"], ti["log_pi"], wi.eps, out=out, workspace=ws)
+                reps = max(3, min(50, int(2e6 // n)))
+                m, _ = timed(lambda: fn(ti["Q"], ti["K"], ti["V"], ti["mu"], ti["sigma2"], ti["log_pi"], wi.eps,
+                                        out=out, workspace=ws), reps)
+                torch.cuda.synchronize(dev)
+                torch.cuda.reset_peak_memory_stats(dev)
+                base = torch.cuda.memory_allocated(dev)
+                ws2 = gma.alloc_workspace(pb, op, dev)
+                out2 = torch.empty_like(out)
+                fn(ti["Q"], ti["K"], ti["V"], ti["mu"], ti["sigma2"], ti["log_pi"], wi.eps, out=out2, workspace=ws2)
+                torch.cuda.synchronize(dev)
+                peak_call = torch.cuda.max_memory_allocated(dev) - base
+                inputs_b = 3 * wi.B * wi.H * n * 64 * 2
+                entry[form] = {"ms": m / reps, "tok_heads_per_s": wi.B * wi.H * n / (m / reps * 1e-3),
+                               "workspace_bytes": ws.numel(), "call_peak_bytes_beyond_inputs": peak_call,
+                               "inputs_bytes": inputs_b}
+                del ws, out, ws2, out2
+            sweep[str(n)] = entry
+            if n == N:
+                path["per_form_ms"] = {f: entry[f]["ms"] for f in entry}
+
+    # CPU baseline: the oracle as it stands on a bounded sample of the same workload (rank 0 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n_pos = min(CPU_SAMPLE_N, N)
+        dt, units, cores = oracle_sample(inp, n_pos)
+        cpu = {"value": units / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": "first %d positions of each of the %d (b,h) units, bidirectional + causal (%.1f s)"
+                         % (n_pos, B * H, dt)}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; shapes and distributions of the workload)",
+                "config": config_dict(w),
+                "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "gpu_launches": int(launches), "roofline": roof, "cpu_baseline": cpu, "clocks": clk,
+                "roofline_path": path, "kernels": kernels, "sweep": sweep or None,
+                "mufu_ex2_per_s": MUFU_EX2_PER_S}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gma", "reference"], default="gma")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-sweep", dest="sweep", action="store_false")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-positions", type=int, default=2048)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    return run_gma(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

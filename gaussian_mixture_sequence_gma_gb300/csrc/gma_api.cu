@@ -1,0 +1,122 @@
+// gma_api.cu -- the extern "C" boundary of libgma.so: argument validation, workspace sizing,
+// dispatch to the float32 CUDA-core path or the bf16 tensor-core path, and status mapping.
+#include <cuda_runtime.h>
+
+#include <mutex>
+#include <vector>
+
+#include "gma_internal.h"
+
+namespace gma {
+
+gma_status_t set_smem_optin(const void* func, int bytes, int /*slot*/) {
+  if (bytes <= 48 * 1024) return GMA_OK;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GMA_ERR_CUDA;
+  struct Entry { const void* f; int dev; int bytes; };
+  static std::mutex mu;
+  static std::vector<Entry> done;
+  std::lock_guard<std::mutex> lock(mu);
+  for (auto& e : done)
+    if (e.f == func && e.dev == dev && e.bytes >= bytes) return GMA_OK;
+  if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+    return GMA_ERR_CUDA;
+  done.push_back({func, dev, bytes});
+  return GMA_OK;
+}
+
+namespace {
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+gma_status_t validate_problem(const gma_problem_t* p) {
+  if (!p) return GMA_ERR_INVALID_ARG;
+  if (p->B < 1 || p->H < 1 || p->N < 0 || p->K < 1 || p->d < 1 || p->dv < 1) return GMA_ERR_INVALID_ARG;
+  if (!(p->eps >= 0.0f) || p->eps == INFINITY) return GMA_ERR_INVALID_ARG;
+  if (p->dtype != GMA_F32 && p->dtype != GMA_BF16) return GMA_ERR_UNSUPPORTED;
+  if (p->d != kD || p->dv != kDv || p->K > kMaxK) return GMA_ERR_UNSUPPORTED;
+  if ((long long)p->B * p->H * (long long)p->N >= (1LL << 31)) return GMA_ERR_UNSUPPORTED;
+  return GMA_OK;
+}
+
+size_t required_bytes(const gma_problem_t& p, gma_op_t op) {
+  if (p.dtype == GMA_BF16) return tc_plan(p, op).total;
+  return simt_plan(p, op).total;
+}
+
+gma_status_t run(const gma_problem_t* p, gma_op_t op, const void* Q, const void* K, const void* V, const float* mu,
+                 const float* sigma2, const float* log_pi, void* out, void* ws, size_t ws_bytes, void* stream) {
+  gma_status_t s = validate_problem(p);
+  if (s != GMA_OK) return s;
+  if (!mu || !sigma2 || !log_pi || !ws) return GMA_ERR_INVALID_ARG;
+  if (p->N > 0) {  // with N == 0 nothing is read or written, so empty tensors may be null
+    if (!Q || !out) return GMA_ERR_INVALID_ARG;
+    if (op != GMA_OP_RESPONSIBILITIES && (!K || !V)) return GMA_ERR_INVALID_ARG;
+    if (op != GMA_OP_RESPONSIBILITIES && (out == Q || out == K || out == V)) return GMA_ERR_INVALID_ARG;
+  }
+  const void* ptrs[] = {Q, K, V, mu, sigma2, log_pi, out};
+  for (const void* q : ptrs)
+    if (q && !aligned(q, 16)) return GMA_ERR_INVALID_ARG;
+  if (!aligned(ws, kAlign)) return GMA_ERR_INVALID_ARG;
+  if (ws_bytes < required_bytes(*p, op)) return GMA_ERR_WORKSPACE;
+  if (p->N == 0) return GMA_OK;
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaGetLastError();  // a stale error from earlier caller work is not ours to report
+  if (p->dtype == GMA_BF16) return tc_run(*p, op, Q, K, V, mu, sigma2, log_pi, out, ws, st);
+  return simt_run(*p, op, Q, K, V, mu, sigma2, log_pi, out, ws, st);
+}
+
+}  // namespace
+}  // namespace gma
+
+using namespace gma;
+
+extern "C" {
+
+size_t gma_workspace_bytes(const gma_problem_t* p, gma_op_t op) {
+  if (validate_problem(p) != GMA_OK) return 0;
+  if (op != GMA_OP_RESPONSIBILITIES && op != GMA_OP_BIDIR && op != GMA_OP_CAUSAL) return 0;
+  return required_bytes(*p, op);
+}
+
+gma_status_t gma_responsibilities(const gma_problem_t* p, const void* X, const float* mu, const float* sigma2,
+                                  const float* log_pi, float* gamma_out, void* ws, size_t ws_bytes, void* stream) {
+  return run(p, GMA_OP_RESPONSIBILITIES, X, nullptr, nullptr, mu, sigma2, log_pi, gamma_out, ws, ws_bytes, stream);
+}
+
+gma_status_t gma_forward_bidir(const gma_problem_t* p, const void* Q, const void* K, const void* V, const float* mu,
+                               const float* sigma2, const float* log_pi, void* O, void* ws, size_t ws_bytes,
+                               void* stream) {
+  return run(p, GMA_OP_BIDIR, Q, K, V, mu, sigma2, log_pi, O, ws, ws_bytes, stream);
+}
+
+gma_status_t gma_forward_causal(const gma_problem_t* p, const void* Q, const void* K, const void* V, const float* mu,
+                                const float* sigma2, const float* log_pi, void* O, void* ws, size_t ws_bytes,
+                                void* stream) {
+  return run(p, GMA_OP_CAUSAL, Q, K, V, mu, sigma2, log_pi, O, ws, ws_bytes, stream);
+}
+
+gma_status_t gma_check_device_error(void* ws, void* stream) {
+  if (!ws || !aligned(ws, kAlign)) return GMA_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  Ctrl c;
+  if (cudaMemcpyAsync(&c, ws, sizeof(Ctrl), cudaMemcpyDeviceToHost, st) != cudaSuccess) return GMA_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return GMA_ERR_CUDA;
+  return c.err == kErrNone ? GMA_OK : GMA_ERR_TIMEOUT;
+}
+
+const char* gma_status_string(gma_status_t s) {
+  switch (s) {
+    case GMA_OK: return "ok";
+    case GMA_ERR_INVALID_ARG: return "invalid argument";
+    case GMA_ERR_UNSUPPORTED: return "unsupported problem (d, dv, K or dtype)";
+    case GMA_ERR_WORKSPACE: return "workspace too small";
+    case GMA_ERR_CUDA: return "CUDA runtime error";
+    case GMA_ERR_TIMEOUT: return "a bounded device wait timed out";
+  }
+  return "unknown status";
+}
+
+int gma_version(void) { return (0 << 16) | 1; }
+
+}  // extern "C"

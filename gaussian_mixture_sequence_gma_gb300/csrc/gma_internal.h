@@ -1,0 +1,76 @@
+// gma_internal.h -- host-side plumbing shared by the translation units of libgma.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "gma.h"
+
+namespace gma {
+
+constexpr int kD = 64;          // routing width d supported by this build
+constexpr int kDv = 64;         // value width dv supported by this build
+constexpr int kMaxK = 256;      // largest mixture size
+constexpr int kStateCols = 65;  // CUDA-core path: [Vt | Z] row width (dv + 1)
+constexpr size_t kAlign = 256;  // alignment of every workspace section
+constexpr int kTargetUnits = 304;  // work units the split heuristics aim for (2 per SM on 152 SMs)
+
+// Control block at the start of every workspace.
+struct Ctrl {
+  uint32_t err;       // non-zero: a bounded device wait gave up
+  uint32_t err_site;  // which wait (kernel-defined code)
+  uint32_t pad[62];
+};
+static_assert(sizeof(Ctrl) == 256, "control block is one aligned section");
+
+// Device error codes written into Ctrl::err.
+enum : uint32_t { kErrNone = 0, kErrTimeout = 1 };
+
+inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
+inline int cdiv(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+// ---- CUDA-core (float32) path -------------------------------------------------------------------
+constexpr int kSimtTile = 32;  // tokens per tile
+
+struct SimtPlan {
+  int tiles;       // ceil(N / tile)
+  int splits;      // CTAs per (b,h) for the write phase (bidir) or segments (causal)
+  int seg_tiles;   // tiles per segment / split
+  size_t off_params, off_state, total;
+};
+SimtPlan simt_plan(const gma_problem_t& p, gma_op_t op);
+gma_status_t simt_run(const gma_problem_t& p, gma_op_t op, const void* Q, const void* K, const void* V,
+                      const float* mu, const float* sigma2, const float* log_pi, void* out, void* ws,
+                      cudaStream_t stream);
+
+// ---- tensor-core (bf16 I/O) path ----------------------------------------------------------------
+struct TcPlan {
+  int Kp;          // K rounded up to a multiple of 16 (MMA N granularity)
+  int tiles;       // ceil(N / 128)
+  int splits;      // CTAs per (b,h) in the write phase / segments in the causal path
+  int seg_tiles;   // tiles per split or segment
+  size_t off_w, off_c, off_state, total;
+};
+TcPlan tc_plan(const gma_problem_t& p, gma_op_t op);
+gma_status_t tc_run(const gma_problem_t& p, gma_op_t op, const void* Q, const void* K, const void* V,
+                    const float* mu, const float* sigma2, const float* log_pi, void* out, void* ws,
+                    cudaStream_t stream);
+bool tc_available();
+
+// Launch bookkeeping: counts every kernel launch and, while profiling is on, brackets it with a
+// CUDA event pair on the launch stream.
+void* prof_before(cudaStream_t st, const char* name);
+void prof_after(cudaStream_t st, void* token);
+
+#define GMA_LAUNCH(name, kernel, grid, block, smem, stream, ...)    \
+  do {                                                              \
+    void* gma_prof_token_ = ::gma::prof_before((stream), (name));   \
+    kernel<<<(grid), (block), (smem), (stream)>>>(__VA_ARGS__);     \
+    ::gma::prof_after((stream), gma_prof_token_);                   \
+  } while (0)
+
+// Sets the dynamic shared-memory opt-in of a kernel once per device.
+gma_status_t set_smem_optin(const void* func, int bytes, int slot);
+
+}  // namespace gma

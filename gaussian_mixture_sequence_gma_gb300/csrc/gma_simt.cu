@@ -1,0 +1,401 @@
+// gma_simt.cu -- float32 CUDA-core path of the GMA forward pass (dtype GMA_F32).
+//
+// This is the precision path: float32 I/O asks for float32-level agreement, which
+// the 16-bit tensor-core operands cannot give, and at the small K this dtype is
+// used with the work is memory- and launch-bound rather than tensor-bound.
+//
+// Method (Gaussian Mixture Attention pages, gist.science summaries):
+//   "Core mechanism" item 1  gamma_ik = softmax_k( log pi_k + log N(x_i; mu_k, diag sigma2_k) )
+//   "Core mechanism" item 2  Vt = Gamma_K^T V, Z = Gamma_K^T 1, O = Gamma_Q Vt / (Gamma_Q Z + eps)
+//   "Variants and training" item 3  causal: inclusive prefix sums over key positions.
+// The log-density is evaluated in centered form, c_k - 1/2 sum_d (x_d - mu_kd)^2 / sigma2_kd with
+// c_k = log pi_k - 1/2 sum_d log sigma2_kd; the -(d/2) log 2pi term is common to all k and
+// cancels in the softmax.
+#include <cuda_bf16.h>
+
+#include "gma_internal.h"
+
+namespace gma {
+namespace {
+
+constexpr int T = kSimtTile;
+constexpr int kThreads = 256;
+
+template <typename IO>
+__device__ __forceinline__ float ld_io(const IO* p);
+template <>
+__device__ __forceinline__ float ld_io<float>(const float* p) { return __ldg(p); }
+template <>
+__device__ __forceinline__ float ld_io<__nv_bfloat16>(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+
+template <typename IO>
+__device__ __forceinline__ void st_io(IO* p, float v);
+template <>
+__device__ __forceinline__ void st_io<float>(float* p, float v) { *p = v; }
+template <>
+__device__ __forceinline__ void st_io<__nv_bfloat16>(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+
+// Prepared parameters, per head: mu_t[d][K], w_t[d][K] = 1/sigma2 (component index fastest so that a
+// warp of consecutive components reads consecutive addresses), c[K].
+struct SimtParams {
+  float* mu_t;
+  float* w_t;
+  float* c;
+};
+
+__device__ __forceinline__ SimtParams params_at(float* base, int H, int K) {
+  SimtParams P;
+  P.mu_t = base;
+  P.w_t = base + (size_t)H * kD * K;
+  P.c = base + (size_t)2 * H * kD * K;
+  return P;
+}
+
+// Folds (mu, sigma2, log_pi) into the prepared layout, clears the error word and zeroes `zero_n`
+// floats at `zero` (the write-phase accumulator).
+__global__ void simt_prep_kernel(const float* __restrict__ mu, const float* __restrict__ sigma2,
+                                 const float* __restrict__ log_pi, int H, int K, float* params, Ctrl* ctrl,
+                                 float* zero, size_t zero_n) {
+  SimtParams P = params_at(params, H, K);
+  const size_t tid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const size_t nth = (size_t)gridDim.x * blockDim.x;
+  if (tid == 0) { ctrl->err = kErrNone; ctrl->err_site = 0; }
+  const size_t nkd = (size_t)H * K * kD;
+  for (size_t i = tid; i < nkd; i += nth) {
+    const int j = (int)(i % kD);
+    const int k = (int)((i / kD) % K);
+    const int h = (int)(i / ((size_t)kD * K));
+    const size_t o = ((size_t)h * kD + j) * K + k;
+    P.mu_t[o] = mu[i];
+    P.w_t[o] = 1.0f / sigma2[i];
+  }
+  for (size_t i = tid; i < (size_t)H * K; i += nth) {
+    float s = 0.f;
+    for (int j = 0; j < kD; ++j) s += logf(sigma2[i * kD + j]);
+    P.c[i] = log_pi[i] - 0.5f * s;
+  }
+  for (size_t i = tid; i < zero_n; i += nth) zero[i] = 0.f;
+}
+
+// Loads `n` valid rows (of 64) starting at row `r0` of a [rows][64] matrix into smem as float32;
+// rows past `n` are zero.
+template <typename IO>
+__device__ __forceinline__ void load_rows(const IO* __restrict__ src, int r0, int n, float* dst) {
+  for (int i = threadIdx.x; i < T * kD; i += blockDim.x) {
+    const int r = i / kD;
+    dst[i] = r < n ? ld_io<IO>(src + (size_t)(r0 + r) * kD + (i % kD)) : 0.f;
+  }
+}
+
+// Responsibilities of the T rows in xs (first `nvalid` valid) into G[T][K]; invalid rows are zero.
+__device__ void gamma_tile(const float* xs, int nvalid, const SimtParams& P, int h, int K, float* G) {
+  const float* mu_t = P.mu_t + (size_t)h * kD * K;
+  const float* w_t = P.w_t + (size_t)h * kD * K;
+  const float* c = P.c + (size_t)h * K;
+  for (int p = threadIdx.x; p < K * (T / 8); p += blockDim.x) {
+    const int k = p % K, tg = p / K;
+    float acc[8];
+#pragma unroll
+    for (int ii = 0; ii < 8; ++ii) acc[ii] = 0.f;
+    for (int j = 0; j < kD; ++j) {
+      const float m = __ldg(mu_t + (size_t)j * K + k);
+      const float w = __ldg(w_t + (size_t)j * K + k);
+#pragma unroll
+      for (int ii = 0; ii < 8; ++ii) {
+        const float diff = xs[(tg * 8 + ii) * kD + j] - m;
+        acc[ii] = fmaf(diff * w, diff, acc[ii]);
+      }
+    }
+    const float ck = __ldg(c + k);
+#pragma unroll
+    for (int ii = 0; ii < 8; ++ii) G[(tg * 8 + ii) * K + k] = ck - 0.5f * acc[ii];
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  for (int i = warp; i < T; i += nwarps) {
+    float* row = G + i * K;
+    if (i >= nvalid) {
+      for (int k = lane; k < K; k += 32) row[k] = 0.f;
+      continue;
+    }
+    float m = -INFINITY;
+    for (int k = lane; k < K; k += 32) m = fmaxf(m, row[k]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float s = 0.f;
+    for (int k = lane; k < K; k += 32) {
+      const float e = expf(row[k] - m);
+      row[k] = e;
+      s += e;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    const float inv = 1.0f / s;
+    for (int k = lane; k < K; k += 32) row[k] *= inv;
+  }
+  __syncthreads();
+}
+
+// sacc[(k, c)] += sum_i G[i][k] * [v_i | 1]_c over one tile; each pair is owned by one thread.
+__device__ __forceinline__ void accumulate_state(const float* G, const float* vs, int K, float* sacc) {
+  const int npairs = K * kStateCols;
+  for (int p = threadIdx.x; p < npairs; p += blockDim.x) {
+    const int k = p / kStateCols, c = p % kStateCols;
+    float s = 0.f;
+    if (c < kDv) {
+      for (int i = 0; i < T; ++i) s = fmaf(G[i * K + k], vs[i * kDv + c], s);
+    } else {
+      for (int i = 0; i < T; ++i) s += G[i * K + k];
+    }
+    sacc[p] += s;
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Responsibilities export: grid (tiles, B*H).
+template <typename IO>
+__global__ void __launch_bounds__(kThreads) simt_resp_kernel(const IO* __restrict__ X, float* params, int H, int N,
+                                                             int K, float* __restrict__ gamma) {
+  extern __shared__ float sm[];
+  float* xs = sm;
+  float* G = xs + T * kD;
+  const int unit = blockIdx.y, h = unit % H;
+  const int t0 = blockIdx.x * T;
+  const int nvalid = min(T, N - t0);
+  const SimtParams P = params_at(params, H, K);
+  load_rows<IO>(X + (size_t)unit * N * kD, t0, nvalid, xs);
+  __syncthreads();
+  gamma_tile(xs, nvalid, P, h, K, G);
+  float* out = gamma + ((size_t)unit * N + t0) * K;
+  for (int i = threadIdx.x; i < nvalid * K; i += blockDim.x) out[i] = G[i];
+}
+
+// Write phase (bidirectional) or segment aggregate (causal): grid (splits, B*H).  Each CTA covers
+// tiles [split * seg_tiles, ...) of its (b,h).  atomic != 0: add into state[unit][K][65];
+// atomic == 0: store into state[unit][split][K][65].
+template <typename IO>
+__global__ void __launch_bounds__(kThreads) simt_write_kernel(const IO* __restrict__ Kx, const IO* __restrict__ V,
+                                                              float* params, int H, int N, int K, int seg_tiles,
+                                                              int splits, float* state, int atomic) {
+  extern __shared__ float sm[];
+  float* xs = sm;
+  float* vs = xs + T * kD;
+  float* G = vs + T * kDv;
+  float* sacc = G + T * K;  // [K][65] partial state of this CTA
+  const int unit = blockIdx.y, h = unit % H, split = blockIdx.x;
+  const SimtParams P = params_at(params, H, K);
+  const int npairs = K * kStateCols;
+  for (int p = threadIdx.x; p < npairs; p += blockDim.x) sacc[p] = 0.f;
+  const int tiles = (N + T - 1) / T;
+  const int tb = split * seg_tiles, te = min(tiles, tb + seg_tiles);
+  for (int t = tb; t < te; ++t) {
+    const int t0 = t * T, nvalid = min(T, N - t0);
+    load_rows<IO>(Kx + (size_t)unit * N * kD, t0, nvalid, xs);
+    load_rows<IO>(V + (size_t)unit * N * kDv, t0, nvalid, vs);
+    __syncthreads();
+    gamma_tile(xs, nvalid, P, h, K, G);
+    accumulate_state(G, vs, K, sacc);
+    __syncthreads();
+  }
+  float* dst = atomic ? state + (size_t)unit * npairs : state + ((size_t)unit * splits + split) * npairs;
+  for (int p = threadIdx.x; p < npairs; p += blockDim.x) {
+    if (atomic) atomicAdd(dst + p, sacc[p]); else dst[p] = sacc[p];
+  }
+}
+
+// Read phase (bidirectional): grid (tiles, B*H).
+template <typename IO>
+__global__ void __launch_bounds__(kThreads) simt_read_kernel(const IO* __restrict__ Q, float* params, int H, int N,
+                                                             int K, const float* __restrict__ state, float eps,
+                                                             IO* __restrict__ O) {
+  extern __shared__ float sm[];
+  float* xs = sm;
+  float* G = xs + T * kD;
+  float* num = G + T * K;
+  const int unit = blockIdx.y, h = unit % H;
+  const int t0 = blockIdx.x * T, nvalid = min(T, N - t0);
+  const SimtParams P = params_at(params, H, K);
+  load_rows<IO>(Q + (size_t)unit * N * kD, t0, nvalid, xs);
+  __syncthreads();
+  gamma_tile(xs, nvalid, P, h, K, G);
+  const float* S = state + (size_t)unit * K * kStateCols;
+  for (int p = threadIdx.x; p < T * kStateCols; p += blockDim.x) {
+    const int i = p / kStateCols, c = p % kStateCols;
+    float s = 0.f;
+    for (int k = 0; k < K; ++k) s = fmaf(G[i * K + k], __ldg(S + k * kStateCols + c), s);
+    num[p] = s;
+  }
+  __syncthreads();
+  IO* out = O + ((size_t)unit * N + t0) * kDv;
+  for (int p = threadIdx.x; p < nvalid * kDv; p += blockDim.x) {
+    const int i = p / kDv, c = p % kDv;
+    st_io<IO>(out + p, num[i * kStateCols + c] / (num[i * kStateCols + kDv] + eps));
+  }
+}
+
+// Exclusive scan over segments: agg[unit][p][e] <- sum_{p' < p} agg[unit][p'][e].  grid (ceil(K*65/256), B*H).
+__global__ void simt_scan_kernel(float* agg, int P, int npairs) {
+  const int unit = blockIdx.y;
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= npairs) return;
+  float* base = agg + (size_t)unit * P * npairs + e;
+  float run = 0.f;
+  for (int p = 0; p < P; ++p) {
+    const float t = base[(size_t)p * npairs];
+    base[(size_t)p * npairs] = run;
+    run += t;
+  }
+}
+
+// Causal sweep: grid (segments, B*H).  Starts from the exclusive prefix state of its segment and walks
+// the segment tile by tile: O_i = [gQ_i . S + sum_{j in tile, j <= i} (gQ_i . gK_j) [v_j|1]] normalised,
+// then S += Gamma_K(tile)^T [V|1].
+template <typename IO>
+__global__ void __launch_bounds__(kThreads) simt_causal_kernel(const IO* __restrict__ Q, const IO* __restrict__ Kx,
+                                                               const IO* __restrict__ V, float* params, int H, int N,
+                                                               int K, int seg_tiles, int P, const float* agg,
+                                                               float eps, IO* __restrict__ O) {
+  extern __shared__ float sm[];
+  const int npairs = K * kStateCols;
+  float* S = sm;                 // [K][65]
+  float* xs = S + npairs;        // [T][64]
+  float* vs = xs + T * kD;       // [T][64]
+  float* GQ = vs + T * kDv;      // [T][K]
+  float* GK = GQ + T * K;        // [T][K]
+  float* A = GK + T * K;         // [T][T]
+  float* num = A + T * T;        // [T][65]
+  const int unit = blockIdx.y, h = unit % H, seg = blockIdx.x;
+  const SimtParams Pp = params_at(params, H, K);
+  const float* S0 = agg + ((size_t)unit * P + seg) * npairs;
+  for (int p = threadIdx.x; p < npairs; p += blockDim.x) S[p] = S0[p];
+  const int tiles = (N + T - 1) / T;
+  const int tb = seg * seg_tiles, te = min(tiles, tb + seg_tiles);
+  for (int t = tb; t < te; ++t) {
+    const int t0 = t * T, nvalid = min(T, N - t0);
+    __syncthreads();
+    load_rows<IO>(Q + (size_t)unit * N * kD, t0, nvalid, xs);
+    __syncthreads();
+    gamma_tile(xs, nvalid, Pp, h, K, GQ);
+    load_rows<IO>(Kx + (size_t)unit * N * kD, t0, nvalid, xs);
+    load_rows<IO>(V + (size_t)unit * N * kDv, t0, nvalid, vs);
+    __syncthreads();
+    gamma_tile(xs, nvalid, Pp, h, K, GK);
+    // masked intra-tile affinity, j <= i inclusive
+    for (int p = threadIdx.x; p < T * T; p += blockDim.x) {
+      const int i = p / T, j = p % T;
+      float s = 0.f;
+      if (j <= i)
+        for (int k = 0; k < K; ++k) s = fmaf(GQ[i * K + k], GK[j * K + k], s);
+      A[p] = s;
+    }
+    __syncthreads();
+    for (int p = threadIdx.x; p < T * kStateCols; p += blockDim.x) {
+      const int i = p / kStateCols, c = p % kStateCols;
+      float s = 0.f;
+      for (int k = 0; k < K; ++k) s = fmaf(GQ[i * K + k], S[k * kStateCols + c], s);
+      if (c < kDv) {
+        for (int j = 0; j <= i; ++j) s = fmaf(A[i * T + j], vs[j * kDv + c], s);
+      } else {
+        for (int j = 0; j <= i; ++j) s += A[i * T + j];
+      }
+      num[p] = s;
+    }
+    __syncthreads();
+    IO* out = O + ((size_t)unit * N + t0) * kDv;
+    for (int p = threadIdx.x; p < nvalid * kDv; p += blockDim.x) {
+      const int i = p / kDv, c = p % kDv;
+      st_io<IO>(out + p, num[i * kStateCols + c] / (num[i * kStateCols + kDv] + eps));
+    }
+    for (int p = threadIdx.x; p < npairs; p += blockDim.x) {
+      const int k = p / kStateCols, c = p % kStateCols;
+      float s = 0.f;
+      if (c < kDv) {
+        for (int j = 0; j < T; ++j) s = fmaf(GK[j * K + k], vs[j * kDv + c], s);
+      } else {
+        for (int j = 0; j < T; ++j) s += GK[j * K + k];
+      }
+      S[p] += s;
+    }
+  }
+}
+
+template <typename IO>
+gma_status_t run_typed(const gma_problem_t& p, gma_op_t op, const IO* Q, const IO* Kx, const IO* V,
+                       const float* mu, const float* sigma2, const float* log_pi, void* out, void* ws,
+                       cudaStream_t st) {
+  const SimtPlan pl = simt_plan(p, op);
+  char* base = (char*)ws;
+  Ctrl* ctrl = (Ctrl*)base;
+  float* params = (float*)(base + pl.off_params);
+  float* state = (float*)(base + pl.off_state);
+  const int BH = p.B * p.H, K = p.K;
+  const int npairs = K * kStateCols;
+  const size_t zero_n = op == GMA_OP_BIDIR ? (size_t)BH * npairs : 0;
+  GMA_LAUNCH("simt_prep", simt_prep_kernel, 148, 256, 0, st, mu, sigma2, log_pi, p.H, K, params, ctrl, state, zero_n);
+  if (cudaGetLastError() != cudaSuccess) return GMA_ERR_CUDA;
+  if (p.N == 0) return GMA_OK;
+  const size_t sm_gamma = (size_t)(T * kD + T * K) * sizeof(float);
+  if (op == GMA_OP_RESPONSIBILITIES) {
+    if (set_smem_optin((const void*)simt_resp_kernel<IO>, (int)sm_gamma, 0) != GMA_OK) return GMA_ERR_CUDA;
+    GMA_LAUNCH("simt_resp", simt_resp_kernel<IO>, dim3(pl.tiles, BH), kThreads, sm_gamma, st, Q, params, p.H, p.N, K, (float*)out);
+    return cudaGetLastError() == cudaSuccess ? GMA_OK : GMA_ERR_CUDA;
+  }
+  const size_t sm_write = (size_t)(T * kD + T * kDv + T * K + npairs) * sizeof(float);
+  if (set_smem_optin((const void*)simt_write_kernel<IO>, (int)sm_write, 1) != GMA_OK) return GMA_ERR_CUDA;
+  if (op == GMA_OP_BIDIR) {
+    GMA_LAUNCH("simt_write", simt_write_kernel<IO>, dim3(pl.splits, BH), kThreads, sm_write, st, Kx, V, params, p.H, p.N, K, pl.seg_tiles,
+                                                                           pl.splits, state, 1);
+    if (cudaGetLastError() != cudaSuccess) return GMA_ERR_CUDA;
+    const size_t sm_read = (size_t)(T * kD + T * K + T * kStateCols) * sizeof(float);
+    if (set_smem_optin((const void*)simt_read_kernel<IO>, (int)sm_read, 2) != GMA_OK) return GMA_ERR_CUDA;
+    GMA_LAUNCH("simt_read", simt_read_kernel<IO>, dim3(pl.tiles, BH), kThreads, sm_read, st, Q, params, p.H, p.N, K, state, p.eps,
+                                                                        (IO*)out);
+    return cudaGetLastError() == cudaSuccess ? GMA_OK : GMA_ERR_CUDA;
+  }
+  // causal
+  GMA_LAUNCH("simt_write", simt_write_kernel<IO>, dim3(pl.splits, BH), kThreads, sm_write, st, Kx, V, params, p.H, p.N, K, pl.seg_tiles,
+                                                                         pl.splits, state, 0);
+  if (cudaGetLastError() != cudaSuccess) return GMA_ERR_CUDA;
+  GMA_LAUNCH("simt_scan", simt_scan_kernel, dim3(cdiv(npairs, 256), BH), 256, 0, st, state, pl.splits, npairs);
+  if (cudaGetLastError() != cudaSuccess) return GMA_ERR_CUDA;
+  const size_t sm_causal = (size_t)(npairs + T * kD + T * kDv + 2 * T * K + T * T + T * kStateCols) * sizeof(float);
+  if (set_smem_optin((const void*)simt_causal_kernel<IO>, (int)sm_causal, 3) != GMA_OK) return GMA_ERR_CUDA;
+  GMA_LAUNCH("simt_causal", simt_causal_kernel<IO>, dim3(pl.splits, BH), kThreads, sm_causal, st, Q, Kx, V, params, p.H, p.N, K,
+                                                                           pl.seg_tiles, pl.splits, state, p.eps,
+                                                                           (IO*)out);
+  return cudaGetLastError() == cudaSuccess ? GMA_OK : GMA_ERR_CUDA;
+}
+
+}  // namespace
+
+SimtPlan simt_plan(const gma_problem_t& p, gma_op_t op) {
+  SimtPlan pl{};
+  const int BH = p.B * p.H;
+  pl.tiles = cdiv(p.N, T);
+  int want = cdiv(kTargetUnits, BH);
+  if (want < 1) want = 1;
+  if (want > pl.tiles) want = pl.tiles;
+  if (want < 1) want = 1;
+  pl.seg_tiles = cdiv(pl.tiles > 0 ? pl.tiles : 1, want);
+  pl.splits = cdiv(pl.tiles > 0 ? pl.tiles : 1, pl.seg_tiles);
+  pl.off_params = align_up(sizeof(Ctrl));
+  const size_t params_bytes = ((size_t)2 * p.H * kD * p.K + (size_t)p.H * p.K) * sizeof(float);
+  pl.off_state = align_up(pl.off_params + params_bytes);
+  size_t state_bytes = 0;
+  if (op == GMA_OP_BIDIR) state_bytes = (size_t)BH * p.K * kStateCols * sizeof(float);
+  if (op == GMA_OP_CAUSAL) state_bytes = (size_t)BH * pl.splits * p.K * kStateCols * sizeof(float);
+  pl.total = align_up(pl.off_state + state_bytes);
+  return pl;
+}
+
+gma_status_t simt_run(const gma_problem_t& p, gma_op_t op, const void* Q, const void* K, const void* V,
+                      const float* mu, const float* sigma2, const float* log_pi, void* out, void* ws,
+                      cudaStream_t stream) {
+  if (p.dtype == GMA_F32)
+    return run_typed<float>(p, op, (const float*)Q, (const float*)K, (const float*)V, mu, sigma2, log_pi, out, ws,
+                            stream);
+  return run_typed<__nv_bfloat16>(p, op, (const __nv_bfloat16*)Q, (const __nv_bfloat16*)K, (const __nv_bfloat16*)V,
+                                  mu, sigma2, log_pi, out, ws, stream);
+}
+
+}  // namespace gma

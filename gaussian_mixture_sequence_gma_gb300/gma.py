@@ -1,0 +1,219 @@
+"""Thin Python binding over libgma.so (ctypes).
+
+Argument marshalling only: PyTorch provides device memory, the current stream
+and the workspace; every step of the GMA forward pass runs in the library's
+CUDA kernels.  If ``libgma.so`` has not been built this module raises; there is
+no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libgma.so")
+
+GMA_OK, GMA_ERR_INVALID_ARG, GMA_ERR_UNSUPPORTED, GMA_ERR_WORKSPACE, GMA_ERR_CUDA, GMA_ERR_TIMEOUT = range(6)
+GMA_F32, GMA_BF16 = 0, 1
+OP_RESPONSIBILITIES, OP_BIDIR, OP_CAUSAL = 0, 1, 2
+
+EXPORTED = ("gma_workspace_bytes", "gma_responsibilities", "gma_forward_bidir", "gma_forward_causal",
+            "gma_check_device_error", "gma_status_string", "gma_version", "gma_launch_count", "gma_profile_enable",
+            "gma_profile_read")
+
+
+class GmaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s failed: %s (status %d)" % (where, status_string(status), status))
+
+
+class Problem(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("N", ctypes.c_int), ("d", ctypes.c_int),
+                ("dv", ctypes.c_int), ("K", ctypes.c_int), ("dtype", ctypes.c_int), ("eps", ctypes.c_float)]
+
+
+_lib = None
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def lib():
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError("libgma.so is not built (expected at %s); run "
+                           "gaussian_mixture_sequence_gma_gb300.build.build()" % _LIB_PATH)
+    L = ctypes.CDLL(_LIB_PATH)
+    vp, fp, sz = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t
+    pp = ctypes.POINTER(Problem)
+    L.gma_workspace_bytes.argtypes = [pp, ctypes.c_int]
+    L.gma_workspace_bytes.restype = sz
+    L.gma_responsibilities.argtypes = [pp, vp, fp, fp, fp, fp, vp, sz, vp]
+    L.gma_responsibilities.restype = ctypes.c_int
+    for name in ("gma_forward_bidir", "gma_forward_causal"):
+        f = getattr(L, name)
+        f.argtypes = [pp, vp, vp, vp, fp, fp, fp, vp, vp, sz, vp]
+        f.restype = ctypes.c_int
+    L.gma_check_device_error.argtypes = [vp, vp]
+    L.gma_check_device_error.restype = ctypes.c_int
+    L.gma_status_string.argtypes = [ctypes.c_int]
+    L.gma_status_string.restype = ctypes.c_char_p
+    L.gma_version.argtypes = []
+    L.gma_version.restype = ctypes.c_int
+    L.gma_launch_count.argtypes = []
+    L.gma_launch_count.restype = ctypes.c_ulonglong
+    L.gma_profile_enable.argtypes = [ctypes.c_int]
+    L.gma_profile_enable.restype = ctypes.c_int
+    L.gma_profile_read.argtypes = [ctypes.c_char_p, ctypes.c_size_t]
+    L.gma_profile_read.restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def status_string(s: int) -> str:
+    try:
+        return lib().gma_status_string(int(s)).decode()
+    except RuntimeError:
+        return "status %d" % s
+
+
+def _dtype_code(t: torch.dtype) -> int:
+    if t == torch.float32:
+        return GMA_F32
+    if t == torch.bfloat16:
+        return GMA_BF16
+    raise TypeError("GMA I/O dtype must be float32 or bfloat16, got %s" % t)
+
+
+def problem(B, H, N, K, dtype, eps=1e-6, d=64, dv=64) -> Problem:
+    code = dtype if isinstance(dtype, int) else _dtype_code(dtype)
+    return Problem(int(B), int(H), int(N), int(d), int(dv), int(K), int(code), float(eps))
+
+
+def workspace_bytes(prob: Problem, op: int) -> int:
+    return int(lib().gma_workspace_bytes(ctypes.byref(prob), int(op)))
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _check_cuda(*ts):
+    dev = None
+    for t in ts:
+        if not t.is_cuda:
+            raise ValueError("GMA tensors must live on a CUDA device")
+        if not t.is_contiguous():
+            raise ValueError("GMA tensors must be contiguous")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError("GMA tensors must share one device")
+    return dev
+
+
+def _stream_handle(stream, device) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return s.cuda_stream
+
+
+def alloc_workspace(prob: Problem, op: int, device) -> torch.Tensor:
+    n = workspace_bytes(prob, op)
+    if n == 0:
+        raise GmaError(GMA_ERR_INVALID_ARG, "gma_workspace_bytes")
+    # torch's caching allocator returns 512-byte aligned blocks, above the 256 the ABI needs
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def _params(mu, sigma2, log_pi):
+    for t in (mu, sigma2, log_pi):
+        if t.dtype != torch.float32:
+            raise TypeError("mu, sigma2 and log_pi must be float32")
+    return mu, sigma2, log_pi
+
+
+def responsibilities(X, mu, sigma2, log_pi, out=None, workspace=None, stream=None):
+    """Gamma [B,H,N,K] float32 of routing vectors X [B,H,N,64] (float32 or bf16)."""
+    B, H, N, d = X.shape
+    K = mu.shape[1]
+    _params(mu, sigma2, log_pi)
+    dev = _check_cuda(X, mu, sigma2, log_pi)
+    prob = problem(B, H, N, K, X.dtype, 0.0, d=d)
+    if out is None:
+        out = torch.empty((B, H, N, K), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(prob, OP_RESPONSIBILITIES, dev)
+    with torch.cuda.device(dev):
+        s = lib().gma_responsibilities(ctypes.byref(prob), _ptr(X), _ptr(mu), _ptr(sigma2), _ptr(log_pi), _ptr(out),
+                                       _ptr(workspace), workspace.numel(), _stream_handle(stream, dev))
+    if s != GMA_OK:
+        raise GmaError(s, "gma_responsibilities")
+    return out
+
+
+def _forward(name, op, Q, K, V, mu, sigma2, log_pi, eps, out, workspace, stream):
+    B, H, N, d = Q.shape
+    dv = V.shape[-1]
+    Kc = mu.shape[1]
+    _params(mu, sigma2, log_pi)
+    dev = _check_cuda(Q, K, V, mu, sigma2, log_pi)
+    if K.dtype != Q.dtype or V.dtype != Q.dtype:
+        raise TypeError("Q, K and V must share one dtype")
+    prob = problem(B, H, N, Kc, Q.dtype, eps, d=d, dv=dv)
+    if out is None:
+        out = torch.empty((B, H, N, dv), dtype=Q.dtype, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(prob, op, dev)
+    with torch.cuda.device(dev):
+        s = getattr(lib(), name)(ctypes.byref(prob), _ptr(Q), _ptr(K), _ptr(V), _ptr(mu), _ptr(sigma2), _ptr(log_pi),
+                                 _ptr(out), _ptr(workspace), workspace.numel(), _stream_handle(stream, dev))
+    if s != GMA_OK:
+        raise GmaError(s, name)
+    return out
+
+
+def forward_bidir(Q, K, V, mu, sigma2, log_pi, eps=1e-6, out=None, workspace=None, stream=None):
+    """Bidirectional GMA forward: O [B,H,N,64] in the dtype of Q."""
+    return _forward("gma_forward_bidir", OP_BIDIR, Q, K, V, mu, sigma2, log_pi, eps, out, workspace, stream)
+
+
+def forward_causal(Q, K, V, mu, sigma2, log_pi, eps=1e-6, out=None, workspace=None, stream=None):
+    """Causal GMA forward (inclusive prefix over key positions): O [B,H,N,64]."""
+    return _forward("gma_forward_causal", OP_CAUSAL, Q, K, V, mu, sigma2, log_pi, eps, out, workspace, stream)
+
+
+def check_device_error(workspace, stream=None) -> int:
+    """Synchronises the stream and returns the status held in the workspace's error word."""
+    dev = workspace.device
+    with torch.cuda.device(dev):
+        return int(lib().gma_check_device_error(_ptr(workspace), _stream_handle(stream, dev)))
+
+
+def launch_count() -> int:
+    """Kernels launched by libgma.so so far in this process."""
+    return int(lib().gma_launch_count())
+
+
+def profile_enable(on: bool) -> None:
+    s = lib().gma_profile_enable(1 if on else 0)
+    if s != GMA_OK:
+        raise GmaError(s, "gma_profile_enable")
+
+
+def profile_read() -> dict:
+    """{kernel name: (launches, total ms)} of the launches recorded while profiling was on."""
+    buf = ctypes.create_string_buffer(1 << 16)
+    n = lib().gma_profile_read(buf, len(buf))
+    if n < 0:
+        raise GmaError(GMA_ERR_CUDA, "gma_profile_read")
+    out = {}
+    for line in buf.value.decode().splitlines():
+        name, cnt, ms = line.split()
+        out[name] = (int(cnt), float(ms))
+    return out

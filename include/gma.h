@@ -46,6 +46,12 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#if defined(__GNUC__)
+#define GMA_API __attribute__((visibility("default")))
+#else
+#define GMA_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -72,7 +78,7 @@ typedef struct {
 } gma_problem_t;
 
 /* Bytes of device workspace `op` needs for problem `p` (0 if p is invalid). */
-size_t gma_workspace_bytes(const gma_problem_t *p, gma_op_t op);
+GMA_API size_t gma_workspace_bytes(const gma_problem_t *p, gma_op_t op);
 
 /*
  * Responsibilities Gamma = p(z | x) of routing vectors X.
@@ -81,7 +87,7 @@ size_t gma_workspace_bytes(const gma_problem_t *p, gma_op_t op);
  *   X      [B,H,N,d] in p->dtype        gamma_out [B,H,N,K] float32 (written)
  * Rows of gamma_out are non-negative and sum to 1.
  */
-gma_status_t gma_responsibilities(const gma_problem_t *p, const void *X, const float *mu, const float *sigma2,
+GMA_API gma_status_t gma_responsibilities(const gma_problem_t *p, const void *X, const float *mu, const float *sigma2,
                                   const float *log_pi, float *gamma_out, void *ws, size_t ws_bytes, void *stream);
 
 /*
@@ -91,7 +97,7 @@ gma_status_t gma_responsibilities(const gma_problem_t *p, const void *X, const f
  *   Q, K [B,H,N,d], V [B,H,N,dv] in p->dtype;  O [B,H,N,dv] in p->dtype (written).
  * O may not alias any input.
  */
-gma_status_t gma_forward_bidir(const gma_problem_t *p, const void *Q, const void *K, const void *V, const float *mu,
+GMA_API gma_status_t gma_forward_bidir(const gma_problem_t *p, const void *Q, const void *K, const void *V, const float *mu,
                                const float *sigma2, const float *log_pi, void *O, void *ws, size_t ws_bytes,
                                void *stream);
 
@@ -102,7 +108,7 @@ gma_status_t gma_forward_bidir(const gma_problem_t *p, const void *Q, const void
  * of the latent memory and normaliser; O at position i depends on j <= i only).
  * Same arguments and layouts as gma_forward_bidir.
  */
-gma_status_t gma_forward_causal(const gma_problem_t *p, const void *Q, const void *K, const void *V, const float *mu,
+GMA_API gma_status_t gma_forward_causal(const gma_problem_t *p, const void *Q, const void *K, const void *V, const float *mu,
                                 const float *sigma2, const float *log_pi, void *O, void *ws, size_t ws_bytes,
                                 void *stream);
 
@@ -113,13 +119,13 @@ gma_status_t gma_forward_causal(const gma_problem_t *p, const void *Q, const voi
  * one did, GMA_ERR_CUDA if the synchronisation itself failed.  `ws` must be a
  * workspace previously passed to one of the calls above.
  */
-gma_status_t gma_check_device_error(void *ws, void *stream);
+GMA_API gma_status_t gma_check_device_error(void *ws, void *stream);
 
 /* Static, NUL-terminated description of a status code. */
-const char *gma_status_string(gma_status_t s);
+GMA_API const char *gma_status_string(gma_status_t s);
 
 /* ABI version of this library: (major << 16) | minor. */
-int gma_version(void);
+GMA_API int gma_version(void);
 
 #ifdef __cplusplus
 }

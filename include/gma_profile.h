@@ -1,0 +1,41 @@
+/*
+ * gma_profile.h -- instrumentation entry points of libgma.so (not part of the GMA method).
+ *
+ * They let a benchmark count the library's kernel launches and time each kernel with CUDA
+ * events recorded on the stream the kernel is launched on.  The method itself is described
+ * in gma.h; nothing here changes what the forward pass computes.
+ */
+#ifndef GMA_PROFILE_H_
+#define GMA_PROFILE_H_
+
+#include <stddef.h>
+
+#include "gma.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Number of kernels libgma.so has launched in this process (all devices, all streams). */
+GMA_API unsigned long long gma_launch_count(void);
+
+/*
+ * on != 0: start recording a CUDA event pair around every kernel the library launches (the
+ * previous records are dropped); on == 0: stop recording (records are kept for reading).
+ * Recording adds two event records per launch on the launch stream.  Returns GMA_ERR_CUDA if
+ * an event could not be created.
+ */
+GMA_API gma_status_t gma_profile_enable(int on);
+
+/*
+ * Waits for every recorded event, then writes one line per kernel kind into `buf`:
+ *   "<kernel name> <launches> <total milliseconds>\n"
+ * NUL-terminated, truncated to `len` bytes.  Returns the number of lines, or -1 on a CUDA error.
+ */
+GMA_API int gma_profile_read(char *buf, size_t len);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GMA_PROFILE_H_ */

@@ -40,20 +40,29 @@
 
 #define GMA_ORACLE_LOG_2PI 1.8378770664093454835606594728112
 
+/* sum_d log sigma2_kd for each of the K components of one head (the Gaussian's log-determinant). */
+static void log_determinants(int d, int K, const double *sigma2, double *logdet) {
+  for (int k = 0; k < K; ++k) {
+    double s = 0.0;
+    for (int j = 0; j < d; ++j) s += log(sigma2[(size_t)k * d + j]);
+    logdet[k] = s;
+  }
+}
+
 /* [R] posterior responsibilities of one routing vector x (length d) over the
- * K components of one head.  mu, sigma2: [K][d]; log_pi: [K]; out: [K]. */
-static void posterior(int d, int K, const double *x, const double *mu, const double *sigma2,
+ * K components of one head.  mu, sigma2: [K][d]; logdet: [K] from
+ * log_determinants(); log_pi: [K]; out: [K]. */
+static void posterior(int d, int K, const double *x, const double *mu, const double *sigma2, const double *logdet,
                       const double *log_pi, double *out) {
   double m = -INFINITY;
   for (int k = 0; k < K; ++k) {
-    double quad = 0.0, logdet = 0.0;
+    double quad = 0.0;
     for (int j = 0; j < d; ++j) {
       double diff = x[j] - mu[(size_t)k * d + j];
       quad += diff * diff / sigma2[(size_t)k * d + j];
-      logdet += log(sigma2[(size_t)k * d + j]);
     }
     /* log pi_k + log N(x; mu_k, diag(sigma2_k)) */
-    double l = log_pi[k] - 0.5 * (quad + logdet) - 0.5 * d * GMA_ORACLE_LOG_2PI;
+    double l = log_pi[k] - 0.5 * (quad + logdet[k]) - 0.5 * d * GMA_ORACLE_LOG_2PI;
     out[k] = l;
     if (l > m) m = l;
   }
@@ -87,15 +96,18 @@ static void run_unit(job_t *J, int unit) {
   const double *lp = J->log_pi + (size_t)h * K;
   const int64_t nout = J->rows ? J->nrows : N;
   double *g = (double *)malloc(sizeof(double) * K);
+  double *ld = (double *)malloc(sizeof(double) * K);
+  log_determinants(d, K, s2, ld);
 
   if (J->mode == 0) {
     const double *X = J->Q + (size_t)unit * N * d;
     double *G = J->out + (size_t)unit * nout * K;
     for (int64_t r = 0; r < nout; ++r) {
       int64_t i = J->rows ? J->rows[r] : r;
-      posterior(d, K, X + i * d, mu, s2, lp, G + r * K);
+      posterior(d, K, X + i * d, mu, s2, ld, lp, G + r * K);
     }
     free(g);
+    free(ld);
     return;
   }
 
@@ -109,7 +121,7 @@ static void run_unit(job_t *J, int unit) {
   if (J->mode == 1) {
     /* [W] write phase over all N keys */
     for (int j = 0; j < N; ++j) {
-      posterior(d, K, Kx + (size_t)j * d, mu, s2, lp, g);
+      posterior(d, K, Kx + (size_t)j * d, mu, s2, ld, lp, g);
       for (int k = 0; k < K; ++k) {
         Z[k] += g[k];
         for (int c = 0; c < dv; ++c) Vt[(size_t)k * dv + c] += g[k] * V[(size_t)j * dv + c];
@@ -118,7 +130,7 @@ static void run_unit(job_t *J, int unit) {
     /* [Rd] read phase for the requested query rows */
     for (int64_t r = 0; r < nout; ++r) {
       int64_t i = J->rows ? J->rows[r] : r;
-      posterior(d, K, Q + i * d, mu, s2, lp, g);
+      posterior(d, K, Q + i * d, mu, s2, ld, lp, g);
       double den = 0.0;
       for (int k = 0; k < K; ++k) den += g[k] * Z[k];
       den += J->eps;
@@ -132,14 +144,14 @@ static void run_unit(job_t *J, int unit) {
     /* [C] running prefix sums, inclusive of the current position */
     int64_t r = 0;
     for (int64_t i = 0; i < N && r < nout; ++i) {
-      posterior(d, K, Kx + i * d, mu, s2, lp, g);
+      posterior(d, K, Kx + i * d, mu, s2, ld, lp, g);
       for (int k = 0; k < K; ++k) {
         Z[k] += g[k];
         for (int c = 0; c < dv; ++c) Vt[(size_t)k * dv + c] += g[k] * V[i * dv + c];
       }
       int64_t want = J->rows ? J->rows[r] : i;
       if (want != i) continue;
-      posterior(d, K, Q + i * d, mu, s2, lp, g);
+      posterior(d, K, Q + i * d, mu, s2, ld, lp, g);
       double den = 0.0;
       for (int k = 0; k < K; ++k) den += g[k] * Z[k];
       den += J->eps;
@@ -154,6 +166,7 @@ static void run_unit(job_t *J, int unit) {
   free(Vt);
   free(Z);
   free(g);
+  free(ld);
 }
 
 static void *worker(void *arg) {
@@ -213,13 +226,15 @@ int gma_oracle_forward(int causal, int B, int H, int N, int d, int dv, int K, co
 int gma_oracle_state(int B, int H, int N, int d, int dv, int K, const double *Kx, const double *V, const double *mu,
                      const double *sigma2, const double *log_pi, double *Vt, double *Z) {
   double *g = (double *)malloc(sizeof(double) * (K > 0 ? K : 1));
+  double *ld = (double *)malloc(sizeof(double) * (K > 0 ? K : 1));
   for (int u = 0; u < B * H; ++u) {
     int h = u % H;
+    log_determinants(d, K, sigma2 + (size_t)h * K * d, ld);
     double *vt = Vt + (size_t)u * K * dv, *z = Z + (size_t)u * K;
     memset(vt, 0, sizeof(double) * K * dv);
     memset(z, 0, sizeof(double) * K);
     for (int j = 0; j < N; ++j) {
-      posterior(d, K, Kx + ((size_t)u * N + j) * d, mu + (size_t)h * K * d, sigma2 + (size_t)h * K * d,
+      posterior(d, K, Kx + ((size_t)u * N + j) * d, mu + (size_t)h * K * d, sigma2 + (size_t)h * K * d, ld,
                 log_pi + (size_t)h * K, g);
       for (int k = 0; k < K; ++k) {
         z[k] += g[k];
@@ -228,5 +243,6 @@ int gma_oracle_state(int B, int H, int N, int d, int dv, int K, const double *Kx
     }
   }
   free(g);
+  free(ld);
   return 0;
 }

@@ -1,0 +1,141 @@
+"""Host-only checks of the C ABI: the library loads, exports every declared entry point, and
+rejects bad arguments with the documented status before touching the GPU."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from gaussian_mixture_sequence_gma_gb300 import build as gbuild
+from gaussian_mixture_sequence_gma_gb300 import gma
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in sorted(os.listdir(os.path.join(ROOT, "include"))) if f.endswith(".h")]
+
+
+@pytest.fixture(scope="module")
+def L():
+    gbuild.build()
+    return gma.lib()
+
+
+def declared_symbols():
+    names = []
+    for h in HEADERS:
+        src = open(h).read()
+        names += re.findall(r"GMA_API\s+[\w\s\*]+?\b(gma_\w+)\s*\(", src)
+    return names
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_symbols()
+    assert set(gma.EXPORTED) <= set(names)
+    out = subprocess.run(["nm", "-D", "--defined-only", gma.lib_path()], capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT\s+(gma_\w+)", out))
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+    for n in names:
+        getattr(L, n)
+
+
+def test_status_strings_and_version(L):
+    for s in range(6):
+        assert len(gma.status_string(s)) > 0
+    assert L.gma_version() >= 1
+
+
+def P(**kw):
+    base = dict(B=1, H=2, N=256, K=16, dtype=gma.GMA_BF16, eps=1e-6, d=64, dv=64)
+    base.update(kw)
+    return gma.problem(base["B"], base["H"], base["N"], base["K"], base["dtype"], base["eps"], base["d"], base["dv"])
+
+
+def test_workspace_bytes(L):
+    for op in (gma.OP_RESPONSIBILITIES, gma.OP_BIDIR, gma.OP_CAUSAL):
+        for dt in (gma.GMA_F32, gma.GMA_BF16):
+            assert gma.workspace_bytes(P(dtype=dt), op) > 0
+            assert gma.workspace_bytes(P(dtype=dt), op) % 256 == 0
+    assert gma.workspace_bytes(P(d=32), gma.OP_BIDIR) == 0
+    assert gma.workspace_bytes(P(K=257), gma.OP_BIDIR) == 0
+    assert gma.workspace_bytes(P(B=0), gma.OP_BIDIR) == 0
+    assert gma.workspace_bytes(P(dtype=7), gma.OP_BIDIR) == 0
+    assert gma.workspace_bytes(P(), 9) == 0
+    # workspace does not grow with N for the bidirectional write state beyond the fixed split
+    assert gma.workspace_bytes(P(N=1 << 20), gma.OP_BIDIR) == gma.workspace_bytes(P(N=1 << 16), gma.OP_BIDIR)
+
+
+# Fake, 256-aligned "device" addresses: every call below must fail (or no-op) before any CUDA call.
+A = 1 << 20
+
+
+def call(L, name, prob, ptrs=None, ws_bytes=1 << 30):
+    p = [A + i * (1 << 16) for i in range(8)] if ptrs is None else ptrs
+    if name == "gma_responsibilities":
+        return L.gma_responsibilities(ctypes.byref(prob), p[0], p[3], p[4], p[5], p[6], p[7], ws_bytes, None)
+    return getattr(L, name)(ctypes.byref(prob), p[0], p[1], p[2], p[3], p[4], p[5], p[6], p[7], ws_bytes, None)
+
+
+@pytest.mark.parametrize("name", ["gma_responsibilities", "gma_forward_bidir", "gma_forward_causal"])
+def test_argument_errors(L, name):
+    assert call(L, name, P(d=32)) == gma.GMA_ERR_UNSUPPORTED
+    assert call(L, name, P(dv=128)) == gma.GMA_ERR_UNSUPPORTED
+    assert call(L, name, P(K=300)) == gma.GMA_ERR_UNSUPPORTED
+    assert call(L, name, P(dtype=5)) == gma.GMA_ERR_UNSUPPORTED
+    assert call(L, name, P(B=0)) == gma.GMA_ERR_INVALID_ARG
+    assert call(L, name, P(K=0)) == gma.GMA_ERR_INVALID_ARG
+    assert call(L, name, P(N=-1)) == gma.GMA_ERR_INVALID_ARG
+    assert call(L, name, P(eps=-1.0)) == gma.GMA_ERR_INVALID_ARG
+    assert call(L, name, P(eps=float("nan"))) == gma.GMA_ERR_INVALID_ARG
+    assert call(L, name, P(B=1 << 16, H=1 << 8, N=1 << 8)) == gma.GMA_ERR_UNSUPPORTED
+    ptrs = [A + i * (1 << 16) for i in range(8)]
+    for i in (0, 3, 4, 5, 6, 7):
+        bad = list(ptrs); bad[i] = None
+        assert call(L, name, P(), bad) == gma.GMA_ERR_INVALID_ARG
+    for i in (0, 3, 4, 5, 6):
+        bad = list(ptrs); bad[i] += 2
+        assert call(L, name, P(), bad) == gma.GMA_ERR_INVALID_ARG
+    bad = list(ptrs); bad[7] += 16  # workspace must be 256-aligned
+    assert call(L, name, P(), bad) == gma.GMA_ERR_INVALID_ARG
+    op = {"gma_responsibilities": 0, "gma_forward_bidir": 1, "gma_forward_causal": 2}[name]
+    need = gma.workspace_bytes(P(), op)
+    assert call(L, name, P(), ws_bytes=need - 1) == gma.GMA_ERR_WORKSPACE
+    # N == 0 is a no-op that launches nothing; the (empty) tensors may then be null
+    assert call(L, name, P(N=0), ws_bytes=gma.workspace_bytes(P(N=0), op)) == gma.GMA_OK
+    nul = [None, None, None, A + 3 * (1 << 16), A + 4 * (1 << 16), A + 5 * (1 << 16), None, A + 7 * (1 << 16)]
+    assert call(L, name, P(N=0), nul, ws_bytes=gma.workspace_bytes(P(N=0), op)) == gma.GMA_OK
+
+
+@pytest.mark.parametrize("name", ["gma_forward_bidir", "gma_forward_causal"])
+def test_forward_specific_errors(L, name):
+    ptrs = [A + i * (1 << 16) for i in range(8)]
+    for i in (1, 2):
+        bad = list(ptrs); bad[i] = None
+        assert call(L, name, P(), bad) == gma.GMA_ERR_INVALID_ARG
+        bad = list(ptrs); bad[i] += 8
+        assert call(L, name, P(), bad) == gma.GMA_ERR_INVALID_ARG
+    for i in (0, 1, 2):  # output aliasing an input
+        bad = list(ptrs); bad[6] = bad[i]
+        assert call(L, name, P(), bad) == gma.GMA_ERR_INVALID_ARG
+
+
+def test_check_device_error_rejects_bad_workspace(L):
+    assert L.gma_check_device_error(None, None) == gma.GMA_ERR_INVALID_ARG
+    assert L.gma_check_device_error(A + 16, None) == gma.GMA_ERR_INVALID_ARG
+
+
+def test_product_never_imports_the_oracle():
+    pkg = os.path.join(ROOT, "gaussian_mixture_sequence_gma_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(from|import)\s+oracle\b", src, re.M), f
+                assert "gma_oracle" not in src and "liboracle" not in src, f
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(gma, "_lib", None)
+    monkeypatch.setattr(gma, "_LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        gma.lib()

@@ -1,0 +1,201 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle on the same seeded inputs.
+
+Bar (max |O_gpu - O_ref| / max |O_ref|): 1e-3 for float32 I/O, 2e-2 for bf16 I/O.
+Full-size workloads are compared on every output where the oracle finishes in seconds, and on
+sampled rows (ends, tile boundaries, random rows) otherwise.
+"""
+import numpy as np
+import pytest
+
+from gaussian_mixture_sequence_gma_gb300.inputs import make_inputs, make_workload, workloads
+from oracle import oracle as orc
+from tests.helpers import TOL, rel_err, sample_rows, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def gma():
+    import torch  # noqa: F401
+    from gaussian_mixture_sequence_gma_gb300 import gma as g
+    g.lib()
+    return g
+
+
+def run(gma, t, causal, eps=1e-6):
+    f = gma.forward_causal if causal else gma.forward_bidir
+    return f(t["Q"], t["K"], t["V"], t["mu"], t["sigma2"], t["log_pi"], eps=eps)
+
+
+def ref(inp, causal, eps=1e-6, rows=None):
+    return orc.forward(inp["Q"], inp["K"], inp["V"], inp["mu"], inp["sigma2"], inp["log_pi"], eps, causal=causal,
+                       rows=rows)
+
+
+def check(gma, inp, causal, eps=1e-6, rows=None, tol=None):
+    t = to_device(inp)
+    O = run(gma, t, causal, eps).float().cpu().numpy()
+    R = ref(inp, causal, eps, rows)
+    if rows is not None:
+        O = O[:, :, rows]
+    err = rel_err(O, R)
+    assert np.isfinite(O).all()
+    assert err <= (tol or TOL[inp["dtype"]]), "max rel err %.3e" % err
+    return err
+
+
+# ------------------------------------------------------------------------------------ workloads
+
+W = workloads()
+
+
+def test_bidir_f32_B1H1N1024K16_full(gma):
+    w = W["bidir_f32_B1H1N1024K16"]
+    check(gma, make_workload(w), causal=False)
+
+
+def test_bidir_bf16_B4H8N4096K128_full(gma):
+    w = W["bidir_bf16_B4H8N4096K128"]
+    check(gma, make_workload(w), causal=False)
+
+
+def test_causal_bf16_B4H8N4096K128_full(gma):
+    w = W["causal_bf16_B4H8N4096K128"]
+    check(gma, make_workload(w), causal=True)
+
+
+def test_causal_lm_bf16_B8H12N2048K256_sampled(gma):
+    w = W["causal_lm_bf16_B8H12N2048K256"]
+    inp = make_workload(w)
+    check(gma, inp, causal=True, rows=sample_rows(w.N, seed=3))
+
+
+@pytest.mark.parametrize("N", [4096, 16384, 65536, 131072])
+@pytest.mark.parametrize("causal", [False, True])
+def test_sweep_bf16_B1H8K256(gma, N, causal):
+    w = W["sweep_bf16_B1H8N%dK256" % N]
+    inp = make_workload(w)
+    rows = None if N == 4096 else sample_rows(N, seed=N)
+    check(gma, inp, causal=causal, rows=rows)
+
+
+# ------------------------------------------------------------------------------------ shapes and edges
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("K", [1, 3, 16, 17, 256])
+@pytest.mark.parametrize("causal", [False, True])
+def test_ragged_small(gma, dtype, K, causal):
+    inp = make_inputs(2, 3, 300, K, dtype=dtype, seed=100 + K)
+    check(gma, inp, causal)
+
+
+@pytest.mark.parametrize("N", [1, 2, 31, 32, 33, 127, 128, 129, 1000])
+@pytest.mark.parametrize("causal", [False, True])
+def test_lengths(gma, N, causal):
+    inp = make_inputs(1, 2, N, 64, dtype="bf16", seed=N)
+    check(gma, inp, causal)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_large_eps_placement(gma, dtype):
+    inp = make_inputs(1, 2, 200, 16, dtype=dtype, seed=7)
+    for causal in (False, True):
+        check(gma, inp, causal, eps=3.0)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("K", [17, 256])
+def test_responsibilities_parity(gma, dtype, K):
+    import torch
+    inp = make_inputs(2, 2, 333, K, dtype=dtype, seed=K)
+    t = to_device(inp)
+    G = gma.responsibilities(t["Q"], t["mu"], t["sigma2"], t["log_pi"]).cpu().numpy()
+    R = orc.responsibilities(inp["Q"], inp["mu"], inp["sigma2"], inp["log_pi"])
+    # float32 path: the log-density sums 64 terms (x-mu)^2/sigma2 of size up to ~600 for these
+    # distributions, each with relative rounding ~1.2e-7, so logits carry up to ~5e-3 absolute error
+    # in the worst case (typically ~1e-4) and |d gamma| <= gamma (1 - gamma) |d logit| stays below 1e-4
+    # for typical rows; bf16 path: 11-bit operands of the log-density contraction.
+    tol = 1e-4 if dtype == "f32" else 2e-2
+    assert np.abs(G - R).max() <= tol
+    assert G.min() >= 0
+    assert np.abs(G.sum(-1) - 1).max() <= (1e-5 if dtype == "f32" else 1e-2)
+    torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_single_component_is_mean(gma, dtype):
+    inp = make_inputs(1, 2, 777, 1, dtype=dtype, seed=3)
+    t = to_device(inp)
+    V = inp["V"].astype(np.float64)
+    Ob = run(gma, t, False, eps=0.5).float().cpu().numpy()
+    assert rel_err(Ob, np.broadcast_to(V.sum(2, keepdims=True) / (777 + 0.5), V.shape)) <= TOL[dtype]
+    Oc = run(gma, t, True, eps=0.5).float().cpu().numpy()
+    run_mean = np.cumsum(V, axis=2) / (np.arange(1, 778)[None, None, :, None] + 0.5)
+    assert rel_err(Oc, run_mean) <= TOL[dtype]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_isotropic_uniform_is_distance_softmax(gma, dtype):
+    import scipy.special
+    from scipy.spatial.distance import cdist
+    inp = make_inputs(1, 1, 256, 32, dtype=dtype, seed=9)
+    inp["sigma2"][:] = 0.9
+    inp["log_pi"][:] = -np.log(32.0)
+    t = to_device(inp)
+    G = gma.responsibilities(t["Q"], t["mu"], t["sigma2"], t["log_pi"]).cpu().numpy()[0, 0]
+    R = scipy.special.softmax(-cdist(inp["Q"][0, 0].astype(np.float64), inp["mu"][0].astype(np.float64),
+                                     "sqeuclidean") / (2 * 0.9), axis=-1)
+    assert np.abs(G - R).max() <= (1e-4 if dtype == "f32" else 2e-2)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_output_fully_written_and_guards_intact(gma, causal):
+    import torch
+    inp = make_inputs(2, 2, 257, 48, dtype="bf16", seed=5)
+    t = to_device(inp)
+    n = 2 * 2 * 257 * 64
+    guard = 4096
+    buf = torch.full((n + 2 * guard,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    out = buf[guard:guard + n].view(2, 2, 257, 64)
+    f = gma.forward_causal if causal else gma.forward_bidir
+    f(t["Q"], t["K"], t["V"], t["mu"], t["sigma2"], t["log_pi"], out=out)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out.float()).all()
+    assert torch.isnan(buf[:guard].float()).all() and torch.isnan(buf[guard + n:].float()).all()
+    assert rel_err(out.float().cpu().numpy(), ref(inp, causal)) <= TOL["bf16"]
+
+
+def test_zero_length_is_a_noop(gma):
+    import torch
+    inp = make_inputs(1, 1, 8, 16, dtype="bf16", seed=1)
+    t = to_device(inp)
+    q = t["Q"][:, :, :0]
+    out = torch.full((1, 1, 0, 64), 1.0, dtype=torch.bfloat16, device="cuda")
+    gma.forward_bidir(q, q, q, t["mu"], t["sigma2"], t["log_pi"], out=out)
+    gma.forward_causal(q, q, q, t["mu"], t["sigma2"], t["log_pi"], out=out)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_repeatable_and_error_word_clean(gma, causal):
+    import torch
+    inp = make_inputs(1, 8, 4096, 256, dtype="bf16", seed=11)
+    t = to_device(inp)
+    prob = gma.problem(1, 8, 4096, 256, torch.bfloat16, 1e-6)
+    ws = gma.alloc_workspace(prob, gma.OP_CAUSAL if causal else gma.OP_BIDIR, "cuda")
+    f = gma.forward_causal if causal else gma.forward_bidir
+    O1 = f(t["Q"], t["K"], t["V"], t["mu"], t["sigma2"], t["log_pi"], workspace=ws).float()
+    O2 = f(t["Q"], t["K"], t["V"], t["mu"], t["sigma2"], t["log_pi"], workspace=ws).float()
+    assert gma.check_device_error(ws) == gma.GMA_OK
+    assert (O1 - O2).abs().max().item() <= 1e-2 * O1.abs().max().item()
+
+
+def test_small_workspace_rejected(gma):
+    import torch
+    inp = make_inputs(1, 2, 64, 16, dtype="bf16", seed=2)
+    t = to_device(inp)
+    prob = gma.problem(1, 2, 64, 16, torch.bfloat16, 1e-6)
+    need = gma.workspace_bytes(prob, gma.OP_BIDIR)
+    ws = torch.empty(need - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(gma.GmaError) as e:
+        gma.forward_bidir(t["Q"], t["K"], t["V"], t["mu"], t["sigma2"], t["log_pi"], workspace=ws)
+    assert e.value.status == gma.GMA_ERR_WORKSPACE

@@ -274,8 +274,8 @@ def test_causal_endpoints():
 # ----------------------------------------------------------------------------- planted mistakes
 
 MUTANTS = {
-    "drop_logdet": ("- 0.5 * (quad + logdet)", "- 0.5 * (quad)"),
-    "sign_flip": ("- 0.5 * (quad + logdet)", "+ 0.5 * (quad + logdet)"),
+    "drop_logdet": ("- 0.5 * (quad + logdet[k])", "- 0.5 * (quad)"),
+    "sign_flip": ("- 0.5 * (quad + logdet[k])", "+ 0.5 * (quad + logdet[k])"),
     "drop_prior": ("double l = log_pi[k]", "double l = 0.0 * log_pi[k]"),
     "drop_eps": ("den += J->eps;", "den += 0.0;"),
     "value_index": ("g[k] * V[(size_t)j * dv + c]", "g[k] * V[(size_t)j * dv + (dv - 1 - c)]"),
