@@ -20,7 +20,7 @@ OP_RESPONSIBILITIES, OP_BIDIR, OP_CAUSAL = 0, 1, 2
 
 EXPORTED = ("gma_workspace_bytes", "gma_responsibilities", "gma_forward_bidir", "gma_forward_causal",
             "gma_check_device_error", "gma_status_string", "gma_version", "gma_launch_count", "gma_profile_enable",
-            "gma_profile_read")
+            "gma_profile_read", "gma_forward_bidir_static_ws", "gma_static_ws_capacity")
 
 
 class GmaError(RuntimeError):
@@ -66,6 +66,10 @@ def lib():
     L.gma_status_string.restype = ctypes.c_char_p
     L.gma_version.argtypes = []
     L.gma_version.restype = ctypes.c_int
+    L.gma_forward_bidir_static_ws.argtypes = [pp, vp, vp, vp, fp, fp, fp, vp, vp]
+    L.gma_forward_bidir_static_ws.restype = ctypes.c_int
+    L.gma_static_ws_capacity.argtypes = []
+    L.gma_static_ws_capacity.restype = sz
     L.gma_launch_count.argtypes = []
     L.gma_launch_count.restype = ctypes.c_ulonglong
     L.gma_profile_enable.argtypes = [ctypes.c_int]
@@ -186,6 +190,28 @@ def forward_bidir(Q, K, V, mu, sigma2, log_pi, eps=1e-6, out=None, workspace=Non
 def forward_causal(Q, K, V, mu, sigma2, log_pi, eps=1e-6, out=None, workspace=None, stream=None):
     """Causal GMA forward (inclusive prefix over key positions): O [B,H,N,64]."""
     return _forward("gma_forward_causal", OP_CAUSAL, Q, K, V, mu, sigma2, log_pi, eps, out, workspace, stream)
+
+
+def forward_bidir_static_ws(Q, K, V, mu, sigma2, log_pi, eps=1e-6, out=None, stream=None):
+    """Bidirectional forward whose scratch is the library's own static device array (no workspace
+    is allocated anywhere); see gma_forward_bidir_static_ws in gma.h for its limits."""
+    B, H, N, d = Q.shape
+    dv = V.shape[-1]
+    _params(mu, sigma2, log_pi)
+    dev = _check_cuda(Q, K, V, mu, sigma2, log_pi)
+    prob = problem(B, H, N, mu.shape[1], Q.dtype, eps, d=d, dv=dv)
+    if out is None:
+        out = torch.empty((B, H, N, dv), dtype=Q.dtype, device=dev)
+    with torch.cuda.device(dev):
+        s = lib().gma_forward_bidir_static_ws(ctypes.byref(prob), _ptr(Q), _ptr(K), _ptr(V), _ptr(mu), _ptr(sigma2),
+                                              _ptr(log_pi), _ptr(out), _stream_handle(stream, dev))
+    if s != GMA_OK:
+        raise GmaError(s, "gma_forward_bidir_static_ws")
+    return out
+
+
+def static_ws_capacity() -> int:
+    return int(lib().gma_static_ws_capacity())
 
 
 def check_device_error(workspace, stream=None) -> int:

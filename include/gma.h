@@ -102,6 +102,31 @@ GMA_API gma_status_t gma_forward_bidir(const gma_problem_t *p, const void *Q, co
                                void *stream);
 
 /*
+ * Bidirectional forward for callers that cannot allocate device memory (for example a plugin
+ * whose host framework forbids allocation on its execute path, a runtime that plans every
+ * device byte ahead of time, or a C program without a device allocator).  The method itself
+ * has no counterpart to this entry point: it computes exactly what gma_forward_bidir computes,
+ * but its scratch memory is a 16 MiB array inside the library (a file-scope __device__ array,
+ * held by every GPU that loads the library until the process exits) instead of a caller
+ * workspace.  Allocates nothing and calls no allocating routine.
+ *   - Problems whose gma_workspace_bytes(p, GMA_OP_BIDIR) exceeds gma_static_ws_capacity()
+ *     return GMA_ERR_WORKSPACE before launching anything.
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress
+ *     with that device current) and caches it; make that first call before any stream capture.
+ *   - Every call shares the one array; each call clears what must start at zero.  Calls whose
+ *     GPU work overlaps (several streams or host threads) race on it and must be serialised.
+ *   - gma_check_device_error() cannot be pointed at this array; timeouts surface as a status
+ *     only through the regular entry points.
+ * Arguments and layouts as gma_forward_bidir, without ws / ws_bytes.
+ */
+GMA_API gma_status_t gma_forward_bidir_static_ws(const gma_problem_t *p, const void *Q, const void *K, const void *V,
+                                                 const float *mu, const float *sigma2, const float *log_pi, void *O,
+                                                 void *stream);
+
+/* Size in bytes of the library-held scratch array used by gma_forward_bidir_static_ws(). */
+GMA_API size_t gma_static_ws_capacity(void);
+
+/*
  * Causal GMA forward: row i uses the inclusive prefix sums over keys j <= i,
  *   O_i = gamma_Qi . (sum_{j<=i} gamma_Kj v_j^T) / (gamma_Qi . sum_{j<=i} gamma_Kj + eps).
  * Passage: gist.science summary, "Variants and training" item 3 (prefix sums
