@@ -2,12 +2,34 @@
 // dispatch to the float32 CUDA-core path or the bf16 tensor-core path, and status mapping.
 #include <cuda_runtime.h>
 
+#include <cstdio>
 #include <mutex>
 #include <vector>
 
 #include "gma_internal.h"
 
 namespace gma {
+
+namespace {
+thread_local char g_detail[256] = "";
+}
+
+void set_error_detail(const char* msg) { snprintf(g_detail, sizeof g_detail, "%s", msg); }
+
+gma_status_t cuda_fail(const char* step, cudaError_t err, const void* func) {
+  const cudaError_t e = err != cudaSuccess ? err : cudaGetLastError();
+  int n = snprintf(g_detail, sizeof g_detail, "%s: %s", step, e == cudaSuccess ? "failed" : cudaGetErrorString(e));
+  cudaFuncAttributes fa;
+  if (func && n > 0 && n < (int)sizeof g_detail && cudaFuncGetAttributes(&fa, func) == cudaSuccess)
+    snprintf(g_detail + n, sizeof g_detail - n, " (kernel: %d registers, max %d threads, %zu B static smem, %d B max dynamic)",
+             fa.numRegs, fa.maxThreadsPerBlock, fa.sharedSizeBytes, fa.maxDynamicSharedSizeBytes);
+  return GMA_ERR_CUDA;
+}
+
+gma_status_t check_launch(const char* step, const void* func) {
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? GMA_OK : cuda_fail(step, e, func);
+}
 
 gma_status_t set_smem_optin(const void* func, int bytes, int /*slot*/) {
   if (bytes <= 48 * 1024) return GMA_OK;
@@ -20,7 +42,7 @@ gma_status_t set_smem_optin(const void* func, int bytes, int /*slot*/) {
   for (auto& e : done)
     if (e.f == func && e.dev == dev && e.bytes >= bytes) return GMA_OK;
   if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
-    return GMA_ERR_CUDA;
+    return cuda_fail("cudaFuncSetAttribute(max dynamic shared memory)");
   done.push_back({func, dev, bytes});
   return GMA_OK;
 }
@@ -118,5 +140,7 @@ const char* gma_status_string(gma_status_t s) {
 }
 
 int gma_version(void) { return (0 << 16) | 1; }
+
+const char* gma_last_error(void) { return g_detail; }
 
 }  // extern "C"

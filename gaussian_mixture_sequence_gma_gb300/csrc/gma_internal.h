@@ -57,6 +57,9 @@ gma_status_t tc_run(const gma_problem_t& p, gma_op_t op, const void* Q, const vo
                     const float* mu, const float* sigma2, const float* log_pi, void* out, void* ws,
                     cudaStream_t stream);
 bool tc_available();
+// Test hook: bit 0 makes the next bidirectional write launch skip its first X-tile load, so that a
+// bounded device wait runs out and reports GMA_ERR_TIMEOUT.
+void tc_set_fault_injection(uint32_t mask);
 
 // Launch bookkeeping: counts every kernel launch and, while profiling is on, brackets it with a
 // CUDA event pair on the launch stream.
@@ -69,6 +72,14 @@ void prof_after(cudaStream_t st, void* token);
     kernel<<<(grid), (block), (smem), (stream)>>>(__VA_ARGS__);     \
     ::gma::prof_after((stream), gma_prof_token_);                   \
   } while (0)
+
+// Records a description of the failing step (and the pending CUDA error, if any) for
+// gma_last_error(); returns GMA_ERR_CUDA.
+gma_status_t cuda_fail(const char* step, cudaError_t err = cudaSuccess, const void* func = nullptr);
+// cudaGetLastError() after a launch; on failure records the step, CUDA's message and the kernel's
+// attributes.
+gma_status_t check_launch(const char* step, const void* func);
+void set_error_detail(const char* msg);
 
 // Sets the dynamic shared-memory opt-in of a kernel once per device.
 gma_status_t set_smem_optin(const void* func, int bytes, int slot);

@@ -66,6 +66,8 @@ extern "C" {
 
 unsigned long long gma_launch_count(void) { return g_launches.load(); }
 
+void gma_debug_withhold_first_load(void) { gma::tc_set_fault_injection(1u); }
+
 gma_status_t gma_profile_enable(int on) {
   std::lock_guard<std::mutex> lock(g_mu);
   if (on) {

@@ -1,21 +1,839 @@
-// gma_tc.cu -- bf16 I/O path.  Placeholder that routes to the CUDA-core kernels until the
-// tcgen05 kernels land.
-#include "gma_internal.h"
+// gma_tc.cu -- bf16-I/O path of the GMA forward pass on the sm_103a tensor cores (tcgen05 + TMEM +
+// TMA), one CTA per SM, warp-specialised.
+//
+// Method (Gaussian Mixture Attention pages, gist.science summaries):
+//   "Core mechanism" item 1: gamma_ik = softmax_k(log pi_k + log N(x_i; mu_k, diag sigma2_k)).
+//     The log-density is expanded into one dense contraction per 128-token tile,
+//       L'_ik = [x_i^2 , x_i] . [-1/2 sigma2_k^-1 ; mu_k sigma2_k^-1] * log2(e)      (fp16 operands)
+//     plus the per-component constant c'_k = (log pi_k - 1/2 sum_d (mu^2/sigma2 + log sigma2)) log2(e)
+//     added in float32, followed by a base-2 softmax over k held in registers.
+//   "Core mechanism" item 2: write  [Vt | Z] = Gamma_K^T [V | 1]   (bf16 operands, fp32 TMEM accumulator)
+//                            read   O = Gamma_Q Vt / (Gamma_Q Z + eps)
+//   Rows of Gamma_K are normalised by scaling the [V | 1] row of each key by 1/s_j (s_j = row sum of
+//   the unnormalised exponentials); Gamma_Q stays unnormalised and the read divides by
+//   (gamma~ . Z + eps * s_i), which is the same quotient.
+//
+// Roles per CTA (384 threads = 3 warpgroups): warp 0 = TMA producer, warp 1 = MMA issuer (one thread)
+// and TMEM owner, warps 2-3 idle; warpgroups 1-2 (warps 4..11) = row warps: thread (q, half) owns token
+// row 32q+lane of the tile and half of its components / dimensions (TMEM lane quarter q = warp % 4).
+// The control warpgroup hands registers to the row warpgroups with setmaxnreg.
+#include <cstdio>
+#include <mutex>
+
+#include "gma_tc_common.cuh"
 
 namespace gma {
+namespace {
+
+using namespace tc;
+
+constexpr int kTile = 128;
+constexpr int kThreadsTc = 384;  // 3 warpgroups
+constexpr int kRowWarp0 = 4;     // first row warp (warpgroups 1 and 2 are row warps)
+// Register split (setmaxnreg): launch pool 384 x 168 = 64512 >= 128 x 56 + 256 x 224 = 64512, and per SM
+// sub-partition (one control warp + two row warps) 32 x (56 + 224 + 224) = 16128 <= 16384.
+constexpr uint32_t kCtrlRegs = 56, kRowRegs = 224;
+constexpr int kRowThreads = 256;
+constexpr int kStCols = 80;  // state row: [Vt (64) | Z | 15 zero]
+constexpr int kTargetCtas = 152;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s per wait
+
+// TMEM columns (512 allocated)
+constexpr uint32_t kColLog = 0;    // logits, Kp columns (<= 256)
+constexpr uint32_t kColAx = 256;   // [x^2 | x] fp16 operand, 64 columns
+constexpr uint32_t kColAcc = 320;  // write: state accumulators 80 per 128-component block; read: O (80)
+
+__host__ __device__ constexpr uint32_t align1k(uint32_t x) { return (x + 1023u) & ~1023u; }
+
+struct SmemLayout {
+  uint32_t w, g, x, v, inv, sb, c, red, total;
+};
+
+// write kernel: W | G (MN-major Gamma~, MB x 32K) | X ring | V ring | INV atom | c' | exchange
+__host__ __device__ inline SmemLayout write_layout(int Kp) {
+  SmemLayout s{};
+  const int MB = (Kp + 127) / 128;
+  s.w = 0;
+  s.g = align1k(Kp * 256);
+  s.x = s.g + MB * 32768;
+  s.v = s.x + 2 * 16384;
+  s.inv = s.v + 2 * 16384;
+  s.sb = s.inv + 16384;
+  s.c = s.sb;
+  s.red = s.c + 1024;
+  s.total = s.red + 4 * kTile * 4;
+  return s;
+}
+// read / responsibilities kernel: W | G (K-major Gamma~, ceil(Kp/64) x 16K) | X ring | SB (state operand) | c' | exchange
+__host__ __device__ inline SmemLayout read_layout(int Kp) {
+  SmemLayout s{};
+  const int KB = (Kp + 63) / 64;
+  s.w = 0;
+  s.g = align1k(Kp * 256);
+  s.x = s.g + KB * 16384;
+  s.v = s.x;
+  s.inv = s.x;
+  s.sb = s.x + 2 * 16384;
+  s.c = s.sb + KB * (kStCols * 128);
+  s.red = s.c + 1024;
+  s.total = s.red + 4 * kTile * 4;
+  return s;
+}
+
+struct Bars {
+  uint64_t w_full, sb_full;
+  uint64_t x_full[2], x_empty[2], v_full[2], v_empty[2];
+  uint64_t ax_full, ax_empty, l_full, l_empty, g_full, g_empty, o_full, o_empty;
+  uint64_t mx, sm, done;
+  uint32_t tmem_base;
+  Abort ab;
+};
+
+struct TcArgs {
+  const uint8_t* w_img;  // [H][Kp * 256] swizzled fp16 B operand of the log-density contraction
+  const float* cbias;    // [H][Kp] c'_k (log2 domain); -inf for padding components
+  float* state;          // [BH][Kp][80] (bidir) or [BH][splits][Kp][80] (causal aggregates)
+  Ctrl* ctrl;
+  void* out;             // read: O bf16 [BH][N][64]; responsibilities: gamma fp32 [BH][N][K]
+  int H, N, K, Kp, tiles, seg_tiles, splits;
+  float eps;
+  uint64_t wait_ns;
+  uint32_t fault;  // bit 0: the producer never loads the first X tile (bounded-wait test hook)
+};
+
+// ----------------------------------------------------------------------------------------------- prep
+// a1: fold (mu, sigma2, log_pi) of every head into the swizzled fp16 W image and c'; clear the error
+// word; zero `zero_n` floats of the write accumulator.  grid (Kp, H), 128 threads: thread j builds
+// element j of component k's W row.
+__global__ void __launch_bounds__(128) tc_prep_kernel(const float* __restrict__ mu, const float* __restrict__ sigma2,
+                                                      const float* __restrict__ log_pi, int H, int K, int Kp,
+                                                      uint8_t* w_img, float* cbias, Ctrl* ctrl, float* zero,
+                                                      size_t zero_n) {
+  const int k = blockIdx.x, h = blockIdx.y, j = threadIdx.x;
+  __shared__ float part[4];
+  float val = 0.f, term = 0.f;
+  if (k < K) {
+    const int dim = j & 63;
+    const float s2 = sigma2[((size_t)h * K + k) * kD + dim];
+    const float m = mu[((size_t)h * K + k) * kD + dim];
+    const float inv = 1.0f / s2;
+    val = (j < 64 ? -0.5f * inv : m * inv) * kLog2e;
+    if (j < 64) term = m * m * inv + logf(s2);
+  }
+  uint8_t* img = w_img + (size_t)h * Kp * 256;
+  *(__half*)(img + sw128_off(k, j, (uint32_t)Kp * 128)) = __float2half_rn(val);
+  // c'_k = (log pi_k - 1/2 sum_d (mu^2/sigma2 + log sigma2)) * log2(e)
+  float s = term;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if ((j & 31) == 0) part[j >> 5] = s;
+  __syncthreads();
+  if (j == 0) {
+    const float tot = part[0] + part[1];  // threads 0..63 carry the terms
+    cbias[(size_t)h * Kp + k] = k < K ? (log_pi[(size_t)h * K + k] - 0.5f * tot) * kLog2e : -INFINITY;
+  }
+  if (k == 0 && h == 0 && j == 0) {
+    ctrl->err = kErrNone;
+    ctrl->err_site = 0;
+  }
+  const size_t tid = ((size_t)blockIdx.y * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x;
+  const size_t nth = (size_t)gridDim.x * gridDim.y * blockDim.x;
+  for (size_t i = tid; i < zero_n; i += nth) zero[i] = 0.f;
+}
+
+// ----------------------------------------------------------------------------------------------- shared pieces
+struct RowCtx {
+  int warp, lane, q, hf, row;  // row warps: q = TMEM lane quarter, hf = component / dimension half
+  uint32_t lane_base;          // TMEM address bits of this warp's lane quarter
+};
+
+__device__ __forceinline__ RowCtx row_ctx() {
+  RowCtx r;
+  r.warp = threadIdx.x >> 5;
+  r.lane = threadIdx.x & 31;
+  r.q = r.warp & 3;
+  r.hf = (r.warp - kRowWarp0) >> 2;
+  r.row = r.q * 32 + r.lane;
+  r.lane_base = (uint32_t)(r.q * 32) << 16;
+  return r;
+}
+
+// Builds this thread's half of the [x^2 | x] fp16 operand row from the bf16 X tile and stores it to
+// TMEM (A operand of the log-density contraction, lane = token, two fp16 per 32-bit column).
+__device__ __forceinline__ void transform_row(const uint8_t* xs, const RowCtx& rc, uint32_t tmem) {
+  uint32_t sq[16], lin[16];
+#pragma unroll
+  for (int jj = 0; jj < 4; ++jj) {
+    const uint4 v = *reinterpret_cast<const uint4*>(xs + sw128_chunk(rc.row, 4 * rc.hf + jj));
+    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float lo = __uint_as_float(w4[i] << 16), hi = __uint_as_float(w4[i] & 0xffff0000u);
+      lin[jj * 4 + i] = pack_f16x2(lo, hi);
+      sq[jj * 4 + i] = pack_f16x2(lo * lo, hi * hi);
+    }
+  }
+  tmem_st16(tmem + rc.lane_base + kColAx + 16 * rc.hf, sq);
+  tmem_st16(tmem + rc.lane_base + kColAx + 32 + 16 * rc.hf, lin);
+}
+
+// Loads this thread's 128 logits (its component half) from TMEM into v[] and adds c'_k; components at
+// or beyond Kp read as -inf.  Returns the half-row maximum.
+__device__ __forceinline__ float load_logits(uint32_t tmem, const RowCtx& rc, const float* cs, int Kp, float* v) {
+  const int kbase = 128 * rc.hf;
+  const int nv = min(max(Kp - kbase, 0), 128);
+  uint32_t* r = reinterpret_cast<uint32_t*>(v);
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    if (32 * c < nv) tmem_ld32(tmem + rc.lane_base + kColLog + kbase + 32 * c, r + 32 * c);
+  tmem_ld_wait();
+  float mx = -INFINITY;
+#pragma unroll
+  for (int c4 = 0; c4 < 32; ++c4) {
+    const float4 cb = (4 * c4 < nv) ? *reinterpret_cast<const float4*>(cs + kbase + 4 * c4)
+                                    : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    const float b[4] = {cb.x, cb.y, cb.z, cb.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int k = 4 * c4 + i;
+      const float x = (k < nv) ? v[k] + b[i] : -INFINITY;
+      v[k] = x;
+      mx = fmaxf(mx, x);
+    }
+  }
+  return mx;
+}
+
+// e_k = 2^(v_k - m), packed to bf16 pairs in place: word i of v (as uint32) receives (e_2i, e_2i+1).
+// Slot i is read at step i/2 <= i before step i overwrites it.  Returns the float32 sum of the e_k.
+__device__ __forceinline__ float exp_pack(float* v, float m) {
+  float s0 = 0.f, s1 = 0.f;
+  uint32_t* packed = reinterpret_cast<uint32_t*>(v);
+#pragma unroll
+  for (int i = 0; i < 64; ++i) {
+    const float e0 = ex2_approx(v[2 * i] - m), e1 = ex2_approx(v[2 * i + 1] - m);
+    s0 += e0;
+    s1 += e1;
+    packed[i] = pack_bf16x2(e0, e1);
+  }
+  return s0 + s1;
+}
+
+// Stores this thread's 128 packed bf16 values (components 128*hf ...) into the swizzled Gamma~ tile
+// (row = token; 64-component blocks 16 KB apart).  Components at or beyond Kp are skipped.
+__device__ __forceinline__ void store_gamma(uint8_t* g, const RowCtx& rc, int Kp, const uint32_t* packed) {
+#pragma unroll
+  for (int cj = 0; cj < 16; ++cj) {
+    const int comp = 128 * rc.hf + 8 * cj;
+    if (comp < Kp) {
+      uint8_t* dst = g + (comp >> 6) * 16384 + sw128_chunk(rc.row, (comp & 63) >> 3);
+      *reinterpret_cast<uint4*>(dst) =
+          make_uint4(packed[4 * cj], packed[4 * cj + 1], packed[4 * cj + 2], packed[4 * cj + 3]);
+    }
+  }
+}
+
+// Exchange of one float per row between the two halves through smem, ordered by an mbarrier that
+// all 256 row threads arrive on.
+__device__ __forceinline__ bool exchange(float* red, uint64_t* bar, uint32_t parity, const RowCtx& rc, float mine,
+                                         float* partner, Bars* B, Ctrl* ctrl, uint32_t site, uint64_t ns) {
+  red[rc.hf * kTile + rc.row] = mine;
+  mbar_arrive(bar);
+  if (!wait_bounded(bar, parity, &B->ab, ctrl, site, ns)) return false;
+  *partner = red[(rc.hf ^ 1) * kTile + rc.row];
+  return true;
+}
+
+__device__ __forceinline__ void init_bars(Bars* B) {
+  mbar_init(&B->w_full, 1);
+  mbar_init(&B->sb_full, kRowThreads);
+  for (int s = 0; s < 2; ++s) {
+    mbar_init(&B->x_full[s], 1);
+    mbar_init(&B->x_empty[s], kRowThreads);
+    mbar_init(&B->v_full[s], 1);
+    mbar_init(&B->v_empty[s], 1);
+  }
+  mbar_init(&B->ax_full, kRowThreads);
+  mbar_init(&B->ax_empty, 1);
+  mbar_init(&B->l_full, 1);
+  mbar_init(&B->l_empty, kRowThreads);
+  mbar_init(&B->g_full, kRowThreads);
+  mbar_init(&B->g_empty, 1);
+  mbar_init(&B->o_full, 1);
+  mbar_init(&B->o_empty, kRowThreads);
+  mbar_init(&B->mx, kRowThreads);
+  mbar_init(&B->sm, kRowThreads);
+  mbar_init(&B->done, 1);
+  B->ab.flag = 0;
+  mbar_fence_init();
+}
+
+// Producer: W image + c' once, then per tile the X tile (and the V tile if `tmV`).
+__device__ __forceinline__ void producer(const TcArgs& a, const CUtensorMap* tmX, const CUtensorMap* tmV,
+                                         uint8_t* smem, const SmemLayout& L, Bars* B, int bh, int tile0, int T) {
+  const uint32_t wbytes = (uint32_t)a.Kp * 256, cbytes = (uint32_t)a.Kp * 4;
+  const int h = bh % a.H;
+  mbar_expect_tx(&B->w_full, wbytes + cbytes);
+  for (uint32_t o = 0; o < wbytes; o += 32768)
+    bulk_load(smem + L.w + o, a.w_img + (size_t)h * wbytes + o, min(32768u, wbytes - o), &B->w_full);
+  bulk_load(smem + L.c, a.cbias + (size_t)h * a.Kp, cbytes, &B->w_full);
+  int issued_x[2] = {-1, -1}, issued_v[2] = {-1, -1};
+  for (int t = 0; t < T; ++t) {
+    const int s = t & 1;
+    const uint32_t u = (uint32_t)(t >> 1);
+    if (!wait_bounded(&B->x_empty[s], (u & 1) ^ 1, &B->ab, a.ctrl, 10, a.wait_ns)) break;
+    if (!((a.fault & 1) && t == 0)) {
+      mbar_expect_tx(&B->x_full[s], 16384);
+      tma_load_3d(smem + L.x + s * 16384, tmX, 0, (tile0 + t) * kTile, bh, &B->x_full[s]);
+      issued_x[s] = (int)(u & 1);
+    }
+    if (tmV) {
+      if (!wait_bounded(&B->v_empty[s], (u & 1) ^ 1, &B->ab, a.ctrl, 11, a.wait_ns)) break;
+      mbar_expect_tx(&B->v_full[s], 16384);
+      tma_load_3d(smem + L.v + s * 16384, tmV, 0, (tile0 + t) * kTile, bh, &B->v_full[s]);
+      issued_v[s] = (int)(u & 1);
+    }
+  }
+  // never leave with copies in flight: wait for the last load issued on each stage
+  Abort none{0};
+  for (int s = 0; s < 2; ++s) {
+    if (issued_x[s] >= 0) wait_bounded(&B->x_full[s], (uint32_t)issued_x[s], &none, a.ctrl, 12, a.wait_ns);
+    if (issued_v[s] >= 0) wait_bounded(&B->v_full[s], (uint32_t)issued_v[s], &none, a.ctrl, 13, a.wait_ns);
+  }
+}
+
+// Issues the log-density contraction of one tile: LOG[128 x Kp] = AX[128 x 128] * W^T.
+__device__ __forceinline__ void issue_logits(uint32_t tmem, uint32_t w_addr, int Kp) {
+  const uint32_t idesc = make_idesc(128, Kp, 0, 0, 0, 0);
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    const uint64_t bd = make_sdesc(w_addr + (ks >> 2) * (uint32_t)Kp * 128 + (ks & 3) * 32, 16, 1024);
+    mma_ts(tmem + kColLog, tmem + kColAx + 8 * ks, bd, idesc, ks > 0 ? 1u : 0u);
+  }
+}
+
+// ----------------------------------------------------------------------------------------------- write / aggregate
+// grid (splits, B*H).  CTA (split, bh) covers tiles [split * seg_tiles, ...) of head-row bh and adds
+// Gamma_K^T [V | 1] over them into state[bh] (kAtomic) or stores it to state[bh][split] (causal).
+template <bool kAtomic>
+__global__ void __launch_bounds__(kThreadsTc, 1)
+    tc_write_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, TcArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ Bars B;
+  const SmemLayout L = write_layout(a.Kp);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = blockIdx.y, split = blockIdx.x;
+  const int tile0 = split * a.seg_tiles;
+  const int T = max(0, min(a.tiles, tile0 + a.seg_tiles) - tile0);
+  const int MB = (a.Kp + 127) / 128;
+
+  // zero Gamma~ (components beyond Kp stay zero: the M=128 blocks read them)
+  for (uint32_t i = threadIdx.x; i < (uint32_t)MB * 32768 / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(smem + L.g)[i] = make_uint4(0, 0, 0, 0);
+  if (threadIdx.x == 0) init_bars(&B);
+  if (warp == 1) {
+    tmem_alloc(&B.tmem_base, 512);
+    tmem_relinquish();
+  }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = B.tmem_base;
+  if (warp < kRowWarp0) {
+    setmaxnreg_dec<kCtrlRegs>();
+    if (warp == 0) {
+    if (lane == 0) producer(a, &tmK, &tmV, smem, L, &B, bh, tile0, T);
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idw = make_idesc(128, kStCols, 1, 1, 1, 1);
+      const uint32_t w_addr = smem_u32(smem + L.w), g_addr = smem_u32(smem + L.g);
+      const uint32_t v_addr = smem_u32(smem + L.v), inv_addr = smem_u32(smem + L.inv);
+      bool ok = wait_bounded(&B.w_full, 0, &B.ab, a.ctrl, 20, a.wait_ns);
+      if (ok && T > 0) ok = wait_bounded(&B.ax_full, 0, &B.ab, a.ctrl, 21, a.wait_ns);
+      if (ok && T > 0) {
+        tc_fence_after();
+        issue_logits(tmem, w_addr, a.Kp);
+        mma_commit(&B.l_full);
+        mma_commit(&B.ax_empty);
+      }
+      for (int t = 0; ok && t < T; ++t) {
+        if (t + 1 < T) {
+          ok = wait_bounded(&B.ax_full, (t + 1) & 1, &B.ab, a.ctrl, 22, a.wait_ns) &&
+               wait_bounded(&B.l_empty, t & 1, &B.ab, a.ctrl, 23, a.wait_ns);
+          if (!ok) break;
+          tc_fence_after();
+          issue_logits(tmem, w_addr, a.Kp);
+          mma_commit(&B.l_full);
+          mma_commit(&B.ax_empty);
+        }
+        ok = wait_bounded(&B.g_full, t & 1, &B.ab, a.ctrl, 24, a.wait_ns);
+        if (!ok) break;
+        tc_fence_after();
+        const int s = t & 1;
+        const uint32_t vs = v_addr + s * 16384;
+        for (int mb = 0; mb < MB; ++mb) {
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint64_t ad = make_sdesc(g_addr + mb * 32768 + ks * 2048, 16384, 1024);
+            const uint64_t bd = make_sdesc(vs + ks * 2048, inv_addr - vs, 1024);
+            mma_ss(tmem + kColAcc + kStCols * mb, ad, bd, idw, (t > 0 || ks > 0) ? 1u : 0u);
+          }
+        }
+        mma_commit(&B.g_empty);
+        mma_commit(&B.v_empty[s]);
+      }
+      mma_commit(&B.done);
+      Abort none{0};
+      wait_bounded(&B.done, 0, &none, a.ctrl, 25, a.wait_ns);
+    }
+    }
+  } else {
+    setmaxnreg_inc<kRowRegs>();
+    // ------------------------------------------------------------------ row warps
+    const RowCtx rc = row_ctx();
+    const float* cs = reinterpret_cast<const float*>(smem + L.c);
+    float* red = reinterpret_cast<float*>(smem + L.red);
+    bool ok = wait_bounded(&B.w_full, 0, &B.ab, a.ctrl, 30, a.wait_ns);
+    if (ok && T > 0) {
+      ok = wait_bounded(&B.x_full[0], 0, &B.ab, a.ctrl, 31, a.wait_ns);
+      if (ok) {
+        transform_row(smem + L.x, rc, tmem);
+        mbar_arrive(&B.x_empty[0]);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&B.ax_full);
+      }
+    }
+    float v[128];
+    for (int t = 0; ok && t < T; ++t) {
+      const int s = t & 1;
+      const int tok = (tile0 + t) * kTile + rc.row;
+      // logits of tile t -> registers; TMEM free for tile t+1
+      if (!(ok = wait_bounded(&B.l_full, t & 1, &B.ab, a.ctrl, 32, a.wait_ns))) break;
+      tc_fence_after();
+      // operand of tile t+1 first (its contraction starts as soon as the logits below are read)
+      if (t + 1 < T) {
+        const int s1 = (t + 1) & 1;
+        if (!(ok = wait_bounded(&B.x_full[s1], ((t + 1) >> 1) & 1, &B.ab, a.ctrl, 33, a.wait_ns))) break;
+        if (!(ok = wait_bounded(&B.ax_empty, t & 1, &B.ab, a.ctrl, 34, a.wait_ns))) break;
+        tc_fence_after();
+        transform_row(smem + L.x + s1 * 16384, rc, tmem);
+        mbar_arrive(&B.x_empty[s1]);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&B.ax_full);
+      }
+      float mx = load_logits(tmem, rc, cs, a.Kp, v);
+      tc_fence_before();
+      mbar_arrive(&B.l_empty);
+      float other;
+      if (!(ok = exchange(red, &B.mx, t & 1, rc, mx, &other, &B, a.ctrl, 35, a.wait_ns))) break;
+      mx = fmaxf(mx, other);
+      float sum = exp_pack(v, mx);
+      if (t > 0 && !(ok = wait_bounded(&B.g_empty, (t - 1) & 1, &B.ab, a.ctrl, 36, a.wait_ns))) break;
+      store_gamma(smem + L.g, rc, a.Kp, reinterpret_cast<const uint32_t*>(v));
+      if (!(ok = exchange(red + 2 * kTile, &B.sm, t & 1, rc, sum, &other, &B, a.ctrl, 37, a.wait_ns))) break;
+      const float inv = tok < a.N ? 1.0f / (sum + other) : 0.f;
+      // scale this key's [v | 1] row by 1/s (normalises its Gamma row inside the contraction)
+      if (!(ok = wait_bounded(&B.v_full[s], (t >> 1) & 1, &B.ab, a.ctrl, 38, a.wait_ns))) break;
+      const __nv_bfloat162 inv2 = __float2bfloat162_rn(inv);
+      uint8_t* vrow = smem + L.v + s * 16384;
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        uint4* p = reinterpret_cast<uint4*>(vrow + sw128_chunk(rc.row, 4 * rc.hf + jj));
+        uint4 x = *p;
+        __nv_bfloat162* hx = reinterpret_cast<__nv_bfloat162*>(&x);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) hx[i] = __hmul2(hx[i], inv2);
+        *p = x;
+      }
+      if (rc.hf == 0) {
+        const uint32_t one = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(inv));
+        *reinterpret_cast<uint4*>(smem + L.inv + sw128_chunk(rc.row, 0)) = make_uint4(one, 0, 0, 0);
+        *reinterpret_cast<uint4*>(smem + L.inv + sw128_chunk(rc.row, 1)) = make_uint4(0, 0, 0, 0);
+      }
+      fence_async_smem();
+      mbar_arrive(&B.g_full);
+    }
+    // epilogue: state rows of this CTA -> global
+    if (ok && T > 0 && rc.hf < MB) {
+      if (wait_bounded(&B.done, 0, &B.ab, a.ctrl, 39, a.wait_ns)) {
+        tc_fence_after();
+        const int comp = 128 * rc.hf + rc.row;
+        uint32_t r[80];
+#pragma unroll
+        for (int c = 0; c < 5; ++c) tmem_ld16(tmem + rc.lane_base + kColAcc + kStCols * rc.hf + 16 * c, r + 16 * c);
+        tmem_ld_wait();
+        if (comp < a.Kp) {
+          float* dst = kAtomic ? a.state + ((size_t)bh * a.Kp + comp) * kStCols
+                               : a.state + (((size_t)bh * a.splits + split) * a.Kp + comp) * kStCols;
+#pragma unroll
+          for (int c = 0; c < 20; ++c) {
+            const float4 f = make_float4(__uint_as_float(r[4 * c]), __uint_as_float(r[4 * c + 1]),
+                                         __uint_as_float(r[4 * c + 2]), __uint_as_float(r[4 * c + 3]));
+            if (kAtomic)
+              atomicAdd(reinterpret_cast<float4*>(dst) + c, f);
+            else
+              reinterpret_cast<float4*>(dst)[c] = f;
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ----------------------------------------------------------------------------------------------- read / responsibilities
+// kRead: grid (splits, B*H); reads state[bh] and writes O.  !kRead: writes normalised Gamma (fp32).
+template <bool kRead>
+__global__ void __launch_bounds__(kThreadsTc, 1)
+    tc_read_kernel(const __grid_constant__ CUtensorMap tmQ, TcArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ Bars B;
+  const SmemLayout L = read_layout(a.Kp);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = blockIdx.y, split = blockIdx.x;
+  const int tile0 = split * a.seg_tiles;
+  const int T = max(0, min(a.tiles, tile0 + a.seg_tiles) - tile0);
+  const int KS = a.Kp / 16;  // contraction steps of the read
+
+  if (threadIdx.x == 0) init_bars(&B);
+  if (warp == 1) {
+    tmem_alloc(&B.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = B.tmem_base;
+  if (warp < kRowWarp0) {
+    setmaxnreg_dec<kCtrlRegs>();
+    if (warp == 0) {
+    if (lane == 0) producer(a, &tmQ, nullptr, smem, L, &B, bh, tile0, T);
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idr = make_idesc(128, kStCols, 1, 1, 0, 0);
+      const uint32_t w_addr = smem_u32(smem + L.w), g_addr = smem_u32(smem + L.g), sb_addr = smem_u32(smem + L.sb);
+      bool ok = wait_bounded(&B.w_full, 0, &B.ab, a.ctrl, 40, a.wait_ns);
+      if (kRead && ok) ok = wait_bounded(&B.sb_full, 0, &B.ab, a.ctrl, 41, a.wait_ns);
+      if (ok && T > 0) ok = wait_bounded(&B.ax_full, 0, &B.ab, a.ctrl, 42, a.wait_ns);
+      if (ok && T > 0) {
+        tc_fence_after();
+        issue_logits(tmem, w_addr, a.Kp);
+        mma_commit(&B.l_full);
+        mma_commit(&B.ax_empty);
+      }
+      for (int t = 0; ok && t < T; ++t) {
+        if (t + 1 < T) {
+          ok = wait_bounded(&B.ax_full, (t + 1) & 1, &B.ab, a.ctrl, 43, a.wait_ns) &&
+               wait_bounded(&B.l_empty, t & 1, &B.ab, a.ctrl, 44, a.wait_ns);
+          if (!ok) break;
+          tc_fence_after();
+          issue_logits(tmem, w_addr, a.Kp);
+          mma_commit(&B.l_full);
+          mma_commit(&B.ax_empty);
+        }
+        if (kRead) {
+          ok = wait_bounded(&B.g_full, t & 1, &B.ab, a.ctrl, 45, a.wait_ns);
+          if (ok && t > 0) ok = wait_bounded(&B.o_empty, (t - 1) & 1, &B.ab, a.ctrl, 46, a.wait_ns);
+          if (!ok) break;
+          tc_fence_after();
+          for (int ks = 0; ks < KS; ++ks) {
+            const uint64_t ad = make_sdesc(g_addr + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
+            const uint64_t bd = make_sdesc(sb_addr + (ks >> 2) * (kStCols * 128) + (ks & 3) * 32, 16, 1024);
+            mma_ss(tmem + kColAcc, ad, bd, idr, ks > 0 ? 1u : 0u);
+          }
+          mma_commit(&B.g_empty);
+          mma_commit(&B.o_full);
+        }
+      }
+      mma_commit(&B.done);
+      Abort none{0};
+      wait_bounded(&B.done, 0, &none, a.ctrl, 47, a.wait_ns);
+    }
+    }
+  } else {
+    setmaxnreg_inc<kRowRegs>();
+    const RowCtx rc = row_ctx();
+    const float* cs = reinterpret_cast<const float*>(smem + L.c);
+    float* red = reinterpret_cast<float*>(smem + L.red);
+    const int rt = threadIdx.x - 32 * kRowWarp0;  // 0..255
+    bool ok = true;
+    if (kRead) {
+      // state [Kp][80] fp32 -> bf16 K-major operand SB[n][comp]
+      if (rt < a.Kp) {
+        const float4* src = reinterpret_cast<const float4*>(a.state + ((size_t)bh * a.Kp + rt) * kStCols);
+#pragma unroll 4
+        for (int c = 0; c < 20; ++c) {
+          const float4 f = __ldg(src + c);
+          const float e[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            *reinterpret_cast<__nv_bfloat16*>(smem + L.sb + sw128_off(4 * c + i, rt, kStCols * 128)) =
+                __float2bfloat16_rn(e[i]);
+        }
+      }
+      fence_async_smem();
+      mbar_arrive(&B.sb_full);
+    }
+    ok = wait_bounded(&B.w_full, 0, &B.ab, a.ctrl, 50, a.wait_ns);
+    if (ok && T > 0) {
+      ok = wait_bounded(&B.x_full[0], 0, &B.ab, a.ctrl, 51, a.wait_ns);
+      if (ok) {
+        transform_row(smem + L.x, rc, tmem);
+        mbar_arrive(&B.x_empty[0]);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&B.ax_full);
+      }
+    }
+    float v[128];
+    float s_prev = 1.f;
+    for (int t = 0; ok && t < T; ++t) {
+      if (!(ok = wait_bounded(&B.l_full, t & 1, &B.ab, a.ctrl, 52, a.wait_ns))) break;
+      tc_fence_after();
+      if (t + 1 < T) {
+        const int s1 = (t + 1) & 1;
+        if (!(ok = wait_bounded(&B.x_full[s1], ((t + 1) >> 1) & 1, &B.ab, a.ctrl, 53, a.wait_ns))) break;
+        if (!(ok = wait_bounded(&B.ax_empty, t & 1, &B.ab, a.ctrl, 54, a.wait_ns))) break;
+        tc_fence_after();
+        transform_row(smem + L.x + s1 * 16384, rc, tmem);
+        mbar_arrive(&B.x_empty[s1]);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&B.ax_full);
+      }
+      float mx = load_logits(tmem, rc, cs, a.Kp, v);
+      tc_fence_before();
+      mbar_arrive(&B.l_empty);
+      float other;
+      if (!(ok = exchange(red, &B.mx, t & 1, rc, mx, &other, &B, a.ctrl, 55, a.wait_ns))) break;
+      mx = fmaxf(mx, other);
+      const int tok = (tile0 + t) * kTile + rc.row;
+      if (kRead) {
+        float sum = exp_pack(v, mx);
+        if (t > 0 && !(ok = wait_bounded(&B.g_empty, (t - 1) & 1, &B.ab, a.ctrl, 56, a.wait_ns))) break;
+        store_gamma(smem + L.g, rc, a.Kp, reinterpret_cast<const uint32_t*>(v));
+        fence_async_smem();
+        mbar_arrive(&B.g_full);
+        if (!(ok = exchange(red + 2 * kTile, &B.sm, t & 1, rc, sum, &other, &B, a.ctrl, 57, a.wait_ns))) break;
+        sum += other;
+        // epilogue of the previous tile (its read contraction has had a whole tile to finish)
+        if (t > 0) {
+          if (!(ok = wait_bounded(&B.o_full, (t - 1) & 1, &B.ab, a.ctrl, 58, a.wait_ns))) break;
+          tc_fence_after();
+          uint32_t r[32], zc[16];
+          tmem_ld32(tmem + rc.lane_base + kColAcc + 32 * rc.hf, r);
+          tmem_ld16(tmem + rc.lane_base + kColAcc + 64, zc);  // zc[0] = Z column
+          tmem_ld_wait();
+          tc_fence_before();
+          mbar_arrive(&B.o_empty);
+          const int ptok = tok - kTile;
+          const float rden = 1.0f / (__uint_as_float(zc[0]) + a.eps * s_prev);
+          if (ptok < a.N) {
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) +
+                                                  ((size_t)bh * a.N + ptok) * kDv + 32 * rc.hf);
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              dst[c] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * c]) * rden, __uint_as_float(r[8 * c + 1]) * rden),
+                                  pack_bf16x2(__uint_as_float(r[8 * c + 2]) * rden, __uint_as_float(r[8 * c + 3]) * rden),
+                                  pack_bf16x2(__uint_as_float(r[8 * c + 4]) * rden, __uint_as_float(r[8 * c + 5]) * rden),
+                                  pack_bf16x2(__uint_as_float(r[8 * c + 6]) * rden, __uint_as_float(r[8 * c + 7]) * rden));
+          }
+        }
+        s_prev = sum;
+      } else {
+        // responsibilities: gamma = e / s in float32
+        float s0 = 0.f;
+#pragma unroll
+        for (int k = 0; k < 128; ++k) {
+          v[k] = ex2_approx(v[k] - mx);
+          s0 += v[k];
+        }
+        if (!(ok = exchange(red + 2 * kTile, &B.sm, t & 1, rc, s0, &other, &B, a.ctrl, 59, a.wait_ns))) break;
+        const float rs = 1.0f / (s0 + other);
+        if (tok < a.N) {
+          float* dst = reinterpret_cast<float*>(a.out) + ((size_t)bh * a.N + tok) * a.K + 128 * rc.hf;
+          const int nk = min(max(a.K - 128 * rc.hf, 0), 128);
+#pragma unroll
+          for (int k = 0; k < 128; ++k)
+            if (k < nk) dst[k] = v[k] * rs;
+        }
+      }
+    }
+    // last epilogue
+    if (kRead && ok && T > 0) {
+      if (wait_bounded(&B.o_full, (T - 1) & 1, &B.ab, a.ctrl, 60, a.wait_ns)) {
+        tc_fence_after();
+        uint32_t r[32], zc[16];
+        tmem_ld32(tmem + rc.lane_base + kColAcc + 32 * rc.hf, r);
+        tmem_ld16(tmem + rc.lane_base + kColAcc + 64, zc);
+        tmem_ld_wait();
+        const int ptok = (tile0 + T - 1) * kTile + rc.row;
+        const float rden = 1.0f / (__uint_as_float(zc[0]) + a.eps * s_prev);
+        if (ptok < a.N) {
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) +
+                                                ((size_t)bh * a.N + ptok) * kDv + 32 * rc.hf);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            dst[c] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * c]) * rden, __uint_as_float(r[8 * c + 1]) * rden),
+                                pack_bf16x2(__uint_as_float(r[8 * c + 2]) * rden, __uint_as_float(r[8 * c + 3]) * rden),
+                                pack_bf16x2(__uint_as_float(r[8 * c + 4]) * rden, __uint_as_float(r[8 * c + 5]) * rden),
+                                pack_bf16x2(__uint_as_float(r[8 * c + 6]) * rden, __uint_as_float(r[8 * c + 7]) * rden));
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ----------------------------------------------------------------------------------------------- host
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 3-D map over a [B*H][N][64] bf16 tensor, box 64 x 128 x 1, 128-byte swizzle, zero fill past N.
+bool make_map(CUtensorMap* m, const void* base, int BH, int N) {
+  EncodeTiledFn f = encode_fn();
+  if (!f) {
+    set_error_detail("cuTensorMapEncodeTiled entry point unavailable");
+    return false;
+  }
+  cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)N * kD * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)kTile, 1}, es[3] = {1, 1, 1};
+  const CUresult r = f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char msg[96];
+    snprintf(msg, sizeof msg, "cuTensorMapEncodeTiled returned CUresult %d", (int)r);
+    set_error_detail(msg);
+  }
+  return r == CUDA_SUCCESS;
+}
+
+// Dynamic shared memory of a launch: the layout plus alignment slack, never below 116 KB so that
+// exactly one CTA (which owns all 512 TMEM columns) is resident per SM.
+uint32_t smem_bytes(uint32_t layout_total) { return layout_total + 1024 > 116u * 1024 ? layout_total + 1024 : 116u * 1024; }
+
+int split_for(int BH, int tiles) {
+  int s = cdiv(kTargetCtas, BH);
+  if (s > tiles) s = tiles;
+  return s < 1 ? 1 : s;
+}
+
+uint32_t g_fault_next = 0;  // test hook, consumed by the next launch of the write kernel
+std::mutex g_fault_mu;
+
+}  // namespace
 
 TcPlan tc_plan(const gma_problem_t& p, gma_op_t op) {
   TcPlan t{};
-  t.total = simt_plan(p, op).total;
+  if (op == GMA_OP_CAUSAL) {  // the causal form still runs on the CUDA-core kernels
+    t.total = simt_plan(p, op).total;
+    return t;
+  }
+  const int BH = p.B * p.H;
+  t.Kp = (p.K + 15) / 16 * 16;
+  t.tiles = cdiv(p.N, kTile);
+  t.splits = split_for(BH, t.tiles > 0 ? t.tiles : 1);
+  t.seg_tiles = cdiv(t.tiles > 0 ? t.tiles : 1, t.splits);
+  t.splits = cdiv(t.tiles > 0 ? t.tiles : 1, t.seg_tiles);
+  t.off_w = align_up(sizeof(Ctrl));
+  t.off_c = align_up(t.off_w + (size_t)p.H * t.Kp * 256);
+  t.off_state = align_up(t.off_c + (size_t)p.H * t.Kp * 4);
+  size_t st = 0;
+  if (op == GMA_OP_BIDIR) st = (size_t)BH * t.Kp * kStCols * 4;
+  t.total = align_up(t.off_state + st);
   return t;
 }
 
 gma_status_t tc_run(const gma_problem_t& p, gma_op_t op, const void* Q, const void* K, const void* V,
                     const float* mu, const float* sigma2, const float* log_pi, void* out, void* ws,
-                    cudaStream_t stream) {
-  return simt_run(p, op, Q, K, V, mu, sigma2, log_pi, out, ws, stream);
+                    cudaStream_t st) {
+  if (op == GMA_OP_CAUSAL) return simt_run(p, op, Q, K, V, mu, sigma2, log_pi, out, ws, st);
+  const TcPlan pl = tc_plan(p, op);
+  const int BH = p.B * p.H;
+  char* base = (char*)ws;
+  TcArgs a{};
+  a.w_img = (const uint8_t*)(base + pl.off_w);
+  a.cbias = (const float*)(base + pl.off_c);
+  a.state = (float*)(base + pl.off_state);
+  a.ctrl = (Ctrl*)base;
+  a.out = out;
+  a.H = p.H;
+  a.N = p.N;
+  a.K = p.K;
+  a.Kp = pl.Kp;
+  a.tiles = pl.tiles;
+  a.seg_tiles = pl.seg_tiles;
+  a.splits = pl.splits;
+  a.eps = p.eps;
+  a.wait_ns = kWaitNs;
+  {
+    std::lock_guard<std::mutex> lock(g_fault_mu);
+    a.fault = g_fault_next;
+    g_fault_next = 0;
+  }
+  const size_t zero_n = op == GMA_OP_BIDIR ? (size_t)BH * pl.Kp * kStCols : 0;
+  GMA_LAUNCH("tc_prep", tc_prep_kernel, dim3(pl.Kp, p.H), 128, 0, st, mu, sigma2, log_pi, p.H, p.K, pl.Kp,
+             (uint8_t*)a.w_img, (float*)a.cbias, a.ctrl, a.state, zero_n);
+  if (gma_status_t e = check_launch("launch tc_prep", (const void*)tc_prep_kernel)) return e;
+  CUtensorMap mq, mk, mv;
+  if (op == GMA_OP_RESPONSIBILITIES) {
+    if (!make_map(&mq, Q, BH, p.N)) return GMA_ERR_CUDA;
+    const uint32_t smem = smem_bytes(read_layout(pl.Kp).total);
+    if (set_smem_optin((const void*)tc_read_kernel<false>, (int)smem, 0) != GMA_OK) return GMA_ERR_CUDA;
+    a.fault = 0;
+    GMA_LAUNCH("tc_resp", tc_read_kernel<false>, dim3(pl.splits, BH), kThreadsTc, smem, st, mq, a);
+    return check_launch("launch tc_resp", (const void*)tc_read_kernel<false>);
+  }
+  if (!make_map(&mq, Q, BH, p.N) || !make_map(&mk, K, BH, p.N) || !make_map(&mv, V, BH, p.N))
+    return GMA_ERR_CUDA;
+  const uint32_t smem_w = smem_bytes(write_layout(pl.Kp).total);
+  if (set_smem_optin((const void*)tc_write_kernel<true>, (int)smem_w, 0) != GMA_OK) return GMA_ERR_CUDA;
+  GMA_LAUNCH("tc_bidir_write", tc_write_kernel<true>, dim3(pl.splits, BH), kThreadsTc, smem_w, st, mk, mv, a);
+  if (gma_status_t e = check_launch("launch tc_bidir_write", (const void*)tc_write_kernel<true>)) return e;
+  a.fault = 0;
+  const uint32_t smem_r = smem_bytes(read_layout(pl.Kp).total);
+  if (set_smem_optin((const void*)tc_read_kernel<true>, (int)smem_r, 0) != GMA_OK) return GMA_ERR_CUDA;
+  GMA_LAUNCH("tc_bidir_read", tc_read_kernel<true>, dim3(pl.splits, BH), kThreadsTc, smem_r, st, mq, a);
+  return check_launch("launch tc_bidir_read", (const void*)tc_read_kernel<true>);
 }
 
-bool tc_available() { return false; }
+bool tc_available() { return encode_fn() != nullptr; }
+
+void tc_set_fault_injection(uint32_t mask) {
+  std::lock_guard<std::mutex> lock(g_fault_mu);
+  g_fault_next = mask;
+}
 
 }  // namespace gma

@@ -19,14 +19,21 @@ GMA_F32, GMA_BF16 = 0, 1
 OP_RESPONSIBILITIES, OP_BIDIR, OP_CAUSAL = 0, 1, 2
 
 EXPORTED = ("gma_workspace_bytes", "gma_responsibilities", "gma_forward_bidir", "gma_forward_causal",
-            "gma_check_device_error", "gma_status_string", "gma_version", "gma_launch_count", "gma_profile_enable",
-            "gma_profile_read", "gma_forward_bidir_static_ws", "gma_static_ws_capacity")
+            "gma_check_device_error", "gma_status_string", "gma_version", "gma_last_error", "gma_launch_count", "gma_profile_enable",
+            "gma_profile_read", "gma_forward_bidir_static_ws", "gma_static_ws_capacity",
+            "gma_debug_withhold_first_load")
 
 
 class GmaError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__("%s failed: %s (status %d)" % (where, status_string(status), status))
+        detail = ""
+        if status == GMA_ERR_CUDA:
+            try:
+                detail = " [%s]" % lib().gma_last_error().decode()
+            except Exception:  # pragma: no cover
+                pass
+        super().__init__("%s failed: %s (status %d)%s" % (where, status_string(status), status, detail))
 
 
 class Problem(ctypes.Structure):
@@ -64,12 +71,16 @@ def lib():
     L.gma_check_device_error.restype = ctypes.c_int
     L.gma_status_string.argtypes = [ctypes.c_int]
     L.gma_status_string.restype = ctypes.c_char_p
+    L.gma_last_error.argtypes = []
+    L.gma_last_error.restype = ctypes.c_char_p
     L.gma_version.argtypes = []
     L.gma_version.restype = ctypes.c_int
     L.gma_forward_bidir_static_ws.argtypes = [pp, vp, vp, vp, fp, fp, fp, vp, vp]
     L.gma_forward_bidir_static_ws.restype = ctypes.c_int
     L.gma_static_ws_capacity.argtypes = []
     L.gma_static_ws_capacity.restype = sz
+    L.gma_debug_withhold_first_load.argtypes = []
+    L.gma_debug_withhold_first_load.restype = None
     L.gma_launch_count.argtypes = []
     L.gma_launch_count.restype = ctypes.c_ulonglong
     L.gma_profile_enable.argtypes = [ctypes.c_int]

@@ -149,6 +149,10 @@ GMA_API gma_status_t gma_check_device_error(void *ws, void *stream);
 /* Static, NUL-terminated description of a status code. */
 GMA_API const char *gma_status_string(gma_status_t s);
 
+/* Static text describing the step that made the calling thread's most recent call return
+ * GMA_ERR_CUDA (with CUDA's own message), or "" if none did. */
+GMA_API const char *gma_last_error(void);
+
 /* ABI version of this library: (major << 16) | minor. */
 GMA_API int gma_version(void);
 

@@ -34,6 +34,15 @@ GMA_API gma_status_t gma_profile_enable(int on);
  */
 GMA_API int gma_profile_read(char *buf, size_t len);
 
+/*
+ * Test hook for the bounded device waits.  The next gma_forward_bidir call with dtype GMA_BF16
+ * launches its write kernel with the first key-tile load withheld: the waits on that tile run out
+ * after their limit (about one second), the kernel records the timeout in the workspace error word
+ * and every CTA exits normally, releasing its tensor memory.  gma_check_device_error() on that
+ * workspace then returns GMA_ERR_TIMEOUT.  Nothing traps or faults; the context stays usable.
+ */
+GMA_API void gma_debug_withhold_first_load(void);
+
 #ifdef __cplusplus
 }
 #endif
