@@ -33,8 +33,9 @@ constexpr int kRowWarp0 = 4;     // first row warp (warpgroups 1 and 2 are row w
 // Register split (setmaxnreg): launch pool 384 x 168 = 64512 >= 128 x 56 + 256 x 224 = 64512, and per SM
 // sub-partition (one control warp + two row warps) 32 x (56 + 224 + 224) = 16128 <= 16384.
 constexpr uint32_t kCtrlRegs = 56, kRowRegs = 224;
-constexpr int kRowThreads = 256;
+constexpr int kRowWarps = 8;  // arrival count of the barriers the row warps signal
 constexpr int kStCols = 80;  // state row: [Vt (64) | Z | 15 zero]
+constexpr int kCTable = 256;  // c' entries per head (-inf past K)
 constexpr int kTargetCtas = 152;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s per wait
@@ -92,7 +93,7 @@ struct Bars {
 
 struct TcArgs {
   const uint8_t* w_img;  // [H][Kp * 256] swizzled fp16 B operand of the log-density contraction
-  const float* cbias;    // [H][Kp] c'_k (log2 domain); -inf for padding components
+  const float* cbias;    // [H][256] c'_k (log2 domain); -inf past K
   float* state;          // [BH][Kp][80] (bidir) or [BH][splits][Kp][80] (causal aggregates)
   Ctrl* ctrl;
   void* out;             // read: O bf16 [BH][N][64]; responsibilities: gamma fp32 [BH][N][K]
@@ -103,9 +104,9 @@ struct TcArgs {
 };
 
 // ----------------------------------------------------------------------------------------------- prep
-// a1: fold (mu, sigma2, log_pi) of every head into the swizzled fp16 W image and c'; clear the error
-// word; zero `zero_n` floats of the write accumulator.  grid (Kp, H), 128 threads: thread j builds
-// element j of component k's W row.
+// a1: fold (mu, sigma2, log_pi) of every head into the swizzled fp16 W image and the 256-entry c'
+// table (-inf past K); clear the error word; zero `zero_n` floats of the write accumulator.
+// grid (256, H), 128 threads: thread j builds element j of component k's W row (k < Kp).
 __global__ void __launch_bounds__(128) tc_prep_kernel(const float* __restrict__ mu, const float* __restrict__ sigma2,
                                                       const float* __restrict__ log_pi, int H, int K, int Kp,
                                                       uint8_t* w_img, float* cbias, Ctrl* ctrl, float* zero,
@@ -122,7 +123,7 @@ __global__ void __launch_bounds__(128) tc_prep_kernel(const float* __restrict__ 
     if (j < 64) term = m * m * inv + logf(s2);
   }
   uint8_t* img = w_img + (size_t)h * Kp * 256;
-  *(__half*)(img + sw128_off(k, j, (uint32_t)Kp * 128)) = __float2half_rn(val);
+  if (k < Kp) *(__half*)(img + sw128_off(k, j, (uint32_t)Kp * 128)) = __float2half_rn(val);
   // c'_k = (log pi_k - 1/2 sum_d (mu^2/sigma2 + log sigma2)) * log2(e)
   float s = term;
 #pragma unroll
@@ -131,7 +132,7 @@ __global__ void __launch_bounds__(128) tc_prep_kernel(const float* __restrict__ 
   __syncthreads();
   if (j == 0) {
     const float tot = part[0] + part[1];  // threads 0..63 carry the terms
-    cbias[(size_t)h * Kp + k] = k < K ? (log_pi[(size_t)h * K + k] - 0.5f * tot) * kLog2e : -INFINITY;
+    cbias[(size_t)h * kCTable + k] = k < K ? (log_pi[(size_t)h * K + k] - 0.5f * tot) * kLog2e : -INFINITY;
   }
   if (k == 0 && h == 0 && j == 0) {
     ctrl->err = kErrNone;
@@ -178,54 +179,72 @@ __device__ __forceinline__ void transform_row(const uint8_t* xs, const RowCtx& r
   tmem_st16(tmem + rc.lane_base + kColAx + 32 + 16 * rc.hf, lin);
 }
 
-// Loads this thread's 128 logits (its component half) from TMEM into v[] and adds c'_k; components at
-// or beyond Kp read as -inf.  Returns the half-row maximum.
-__device__ __forceinline__ float load_logits(uint32_t tmem, const RowCtx& rc, const float* cs, int Kp, float* v) {
-  const int kbase = 128 * rc.hf;
-  const int nv = min(max(Kp - kbase, 0), 128);
+// Zeroes this thread's logit columns at or beyond Kp once per CTA: the contraction (N = Kp) never
+// writes them, and with c'_k = -inf there they then read as -inf without any per-element masking.
+template <int NC>
+__device__ __forceinline__ void zero_unused_logits(uint32_t tmem, const RowCtx& rc, int Kp) {
+  uint32_t z[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) z[i] = 0u;
+#pragma unroll
+  for (int c = 0; c < NC / 16; ++c)
+    if (NC * rc.hf + 16 * c >= Kp) tmem_st16(tmem + rc.lane_base + kColLog + NC * rc.hf + 16 * c, z);
+  tmem_st_wait();
+}
+
+// Loads this thread's NC logits (components NC*hf ...) from TMEM, adds c'_k (a 256-entry table padded
+// with -inf) in pairs, and returns the maximum.
+template <int NC>
+__device__ __forceinline__ float load_logits(uint32_t tmem, const RowCtx& rc, const float* cs, float* v) {
+  const int kbase = NC * rc.hf;
   uint32_t* r = reinterpret_cast<uint32_t*>(v);
 #pragma unroll
-  for (int c = 0; c < 4; ++c)
-    if (32 * c < nv) tmem_ld32(tmem + rc.lane_base + kColLog + kbase + 32 * c, r + 32 * c);
+  for (int c = 0; c < NC / 32; ++c) tmem_ld32(tmem + rc.lane_base + kColLog + kbase + 32 * c, r + 32 * c);
   tmem_ld_wait();
-  float mx = -INFINITY;
 #pragma unroll
-  for (int c4 = 0; c4 < 32; ++c4) {
-    const float4 cb = (4 * c4 < nv) ? *reinterpret_cast<const float4*>(cs + kbase + 4 * c4)
-                                    : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-    const float b[4] = {cb.x, cb.y, cb.z, cb.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int k = 4 * c4 + i;
-      const float x = (k < nv) ? v[k] + b[i] : -INFINITY;
-      v[k] = x;
-      mx = fmaxf(mx, x);
-    }
+  for (int c4 = 0; c4 < NC / 4; ++c4) {
+    const float4 cb = *reinterpret_cast<const float4*>(cs + kbase + 4 * c4);
+    add_f32x2(v[4 * c4], v[4 * c4 + 1], cb.x, cb.y);
+    add_f32x2(v[4 * c4 + 2], v[4 * c4 + 3], cb.z, cb.w);
   }
-  return mx;
+  float m0 = v[0], m1 = v[1], m2 = v[2], m3 = v[3];
+#pragma unroll
+  for (int i = 1; i < NC / 8; ++i) {
+    m0 = max3(m0, v[8 * i], v[8 * i + 1]);
+    m1 = max3(m1, v[8 * i + 2], v[8 * i + 3]);
+    m2 = max3(m2, v[8 * i + 4], v[8 * i + 5]);
+    m3 = max3(m3, v[8 * i + 6], v[8 * i + 7]);
+  }
+  return max3(max3(m0, m1, m2), m3, max3(v[4], v[5], fmaxf(v[6], v[7])));
 }
 
 // e_k = 2^(v_k - m), packed to bf16 pairs in place: word i of v (as uint32) receives (e_2i, e_2i+1).
 // Slot i is read at step i/2 <= i before step i overwrites it.  Returns the float32 sum of the e_k.
+template <int NC>
 __device__ __forceinline__ float exp_pack(float* v, float m) {
-  float s0 = 0.f, s1 = 0.f;
+  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
   uint32_t* packed = reinterpret_cast<uint32_t*>(v);
 #pragma unroll
-  for (int i = 0; i < 64; ++i) {
-    const float e0 = ex2_approx(v[2 * i] - m), e1 = ex2_approx(v[2 * i + 1] - m);
-    s0 += e0;
-    s1 += e1;
+  for (int i = 0; i < NC / 2; ++i) {
+    float t0 = v[2 * i], t1 = v[2 * i + 1];
+    add_f32x2(t0, t1, -m, -m);
+    const float e0 = ex2_approx(t0), e1 = ex2_approx(t1);
+    if (i & 1)
+      add_f32x2(s2, s3, e0, e1);
+    else
+      add_f32x2(s0, s1, e0, e1);
     packed[i] = pack_bf16x2(e0, e1);
   }
-  return s0 + s1;
+  return (s0 + s1) + (s2 + s3);
 }
 
-// Stores this thread's 128 packed bf16 values (components 128*hf ...) into the swizzled Gamma~ tile
+// Stores this thread's NC packed bf16 values (components NC*hf ...) into the swizzled Gamma~ tile
 // (row = token; 64-component blocks 16 KB apart).  Components at or beyond Kp are skipped.
+template <int NC>
 __device__ __forceinline__ void store_gamma(uint8_t* g, const RowCtx& rc, int Kp, const uint32_t* packed) {
 #pragma unroll
-  for (int cj = 0; cj < 16; ++cj) {
-    const int comp = 128 * rc.hf + 8 * cj;
+  for (int cj = 0; cj < NC / 8; ++cj) {
+    const int comp = NC * rc.hf + 8 * cj;
     if (comp < Kp) {
       uint8_t* dst = g + (comp >> 6) * 16384 + sw128_chunk(rc.row, (comp & 63) >> 3);
       *reinterpret_cast<uint4*>(dst) =
@@ -239,31 +258,31 @@ __device__ __forceinline__ void store_gamma(uint8_t* g, const RowCtx& rc, int Kp
 __device__ __forceinline__ bool exchange(float* red, uint64_t* bar, uint32_t parity, const RowCtx& rc, float mine,
                                          float* partner, Bars* B, Ctrl* ctrl, uint32_t site, uint64_t ns) {
   red[rc.hf * kTile + rc.row] = mine;
-  mbar_arrive(bar);
-  if (!wait_bounded(bar, parity, &B->ab, ctrl, site, ns)) return false;
+  warp_arrive(bar);
+  if (!warp_wait(bar, parity, &B->ab, ctrl, site, ns)) return false;
   *partner = red[(rc.hf ^ 1) * kTile + rc.row];
   return true;
 }
 
 __device__ __forceinline__ void init_bars(Bars* B) {
   mbar_init(&B->w_full, 1);
-  mbar_init(&B->sb_full, kRowThreads);
+  mbar_init(&B->sb_full, kRowWarps);
   for (int s = 0; s < 2; ++s) {
     mbar_init(&B->x_full[s], 1);
-    mbar_init(&B->x_empty[s], kRowThreads);
+    mbar_init(&B->x_empty[s], kRowWarps);
     mbar_init(&B->v_full[s], 1);
     mbar_init(&B->v_empty[s], 1);
   }
-  mbar_init(&B->ax_full, kRowThreads);
+  mbar_init(&B->ax_full, kRowWarps);
   mbar_init(&B->ax_empty, 1);
   mbar_init(&B->l_full, 1);
-  mbar_init(&B->l_empty, kRowThreads);
-  mbar_init(&B->g_full, kRowThreads);
+  mbar_init(&B->l_empty, kRowWarps);
+  mbar_init(&B->g_full, kRowWarps);
   mbar_init(&B->g_empty, 1);
   mbar_init(&B->o_full, 1);
-  mbar_init(&B->o_empty, kRowThreads);
-  mbar_init(&B->mx, kRowThreads);
-  mbar_init(&B->sm, kRowThreads);
+  mbar_init(&B->o_empty, kRowWarps);
+  mbar_init(&B->mx, kRowWarps);
+  mbar_init(&B->sm, kRowWarps);
   mbar_init(&B->done, 1);
   B->ab.flag = 0;
   mbar_fence_init();
@@ -272,12 +291,12 @@ __device__ __forceinline__ void init_bars(Bars* B) {
 // Producer: W image + c' once, then per tile the X tile (and the V tile if `tmV`).
 __device__ __forceinline__ void producer(const TcArgs& a, const CUtensorMap* tmX, const CUtensorMap* tmV,
                                          uint8_t* smem, const SmemLayout& L, Bars* B, int bh, int tile0, int T) {
-  const uint32_t wbytes = (uint32_t)a.Kp * 256, cbytes = (uint32_t)a.Kp * 4;
+  const uint32_t wbytes = (uint32_t)a.Kp * 256, cbytes = kCTable * 4;
   const int h = bh % a.H;
   mbar_expect_tx(&B->w_full, wbytes + cbytes);
   for (uint32_t o = 0; o < wbytes; o += 32768)
     bulk_load(smem + L.w + o, a.w_img + (size_t)h * wbytes + o, min(32768u, wbytes - o), &B->w_full);
-  bulk_load(smem + L.c, a.cbias + (size_t)h * a.Kp, cbytes, &B->w_full);
+  bulk_load(smem + L.c, a.cbias + (size_t)h * kCTable, cbytes, &B->w_full);
   int issued_x[2] = {-1, -1}, issued_v[2] = {-1, -1};
   for (int t = 0; t < T; ++t) {
     const int s = t & 1;
@@ -316,7 +335,7 @@ __device__ __forceinline__ void issue_logits(uint32_t tmem, uint32_t w_addr, int
 // ----------------------------------------------------------------------------------------------- write / aggregate
 // grid (splits, B*H).  CTA (split, bh) covers tiles [split * seg_tiles, ...) of head-row bh and adds
 // Gamma_K^T [V | 1] over them into state[bh] (kAtomic) or stores it to state[bh][split] (causal).
-template <bool kAtomic>
+template <bool kAtomic, int NC>
 __global__ void __launch_bounds__(kThreadsTc, 1)
     tc_write_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -396,49 +415,50 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     const RowCtx rc = row_ctx();
     const float* cs = reinterpret_cast<const float*>(smem + L.c);
     float* red = reinterpret_cast<float*>(smem + L.red);
-    bool ok = wait_bounded(&B.w_full, 0, &B.ab, a.ctrl, 30, a.wait_ns);
+    zero_unused_logits<NC>(tmem, rc, a.Kp);
+    bool ok = warp_wait(&B.w_full, 0, &B.ab, a.ctrl, 30, a.wait_ns);
     if (ok && T > 0) {
-      ok = wait_bounded(&B.x_full[0], 0, &B.ab, a.ctrl, 31, a.wait_ns);
+      ok = warp_wait(&B.x_full[0], 0, &B.ab, a.ctrl, 31, a.wait_ns);
       if (ok) {
         transform_row(smem + L.x, rc, tmem);
-        mbar_arrive(&B.x_empty[0]);
+        warp_arrive(&B.x_empty[0]);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&B.ax_full);
+        warp_arrive(&B.ax_full);
       }
     }
-    float v[128];
+    float v[NC];
     for (int t = 0; ok && t < T; ++t) {
       const int s = t & 1;
       const int tok = (tile0 + t) * kTile + rc.row;
       // logits of tile t -> registers; TMEM free for tile t+1
-      if (!(ok = wait_bounded(&B.l_full, t & 1, &B.ab, a.ctrl, 32, a.wait_ns))) break;
+      if (!(ok = warp_wait(&B.l_full, t & 1, &B.ab, a.ctrl, 32, a.wait_ns))) break;
       tc_fence_after();
       // operand of tile t+1 first (its contraction starts as soon as the logits below are read)
       if (t + 1 < T) {
         const int s1 = (t + 1) & 1;
-        if (!(ok = wait_bounded(&B.x_full[s1], ((t + 1) >> 1) & 1, &B.ab, a.ctrl, 33, a.wait_ns))) break;
-        if (!(ok = wait_bounded(&B.ax_empty, t & 1, &B.ab, a.ctrl, 34, a.wait_ns))) break;
+        if (!(ok = warp_wait(&B.x_full[s1], ((t + 1) >> 1) & 1, &B.ab, a.ctrl, 33, a.wait_ns))) break;
+        if (!(ok = warp_wait(&B.ax_empty, t & 1, &B.ab, a.ctrl, 34, a.wait_ns))) break;
         tc_fence_after();
         transform_row(smem + L.x + s1 * 16384, rc, tmem);
-        mbar_arrive(&B.x_empty[s1]);
+        warp_arrive(&B.x_empty[s1]);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&B.ax_full);
+        warp_arrive(&B.ax_full);
       }
-      float mx = load_logits(tmem, rc, cs, a.Kp, v);
+      float mx = load_logits<NC>(tmem, rc, cs, v);
       tc_fence_before();
-      mbar_arrive(&B.l_empty);
+      warp_arrive(&B.l_empty);
       float other;
       if (!(ok = exchange(red, &B.mx, t & 1, rc, mx, &other, &B, a.ctrl, 35, a.wait_ns))) break;
       mx = fmaxf(mx, other);
-      float sum = exp_pack(v, mx);
-      if (t > 0 && !(ok = wait_bounded(&B.g_empty, (t - 1) & 1, &B.ab, a.ctrl, 36, a.wait_ns))) break;
-      store_gamma(smem + L.g, rc, a.Kp, reinterpret_cast<const uint32_t*>(v));
+      float sum = exp_pack<NC>(v, mx);
+      if (t > 0 && !(ok = warp_wait(&B.g_empty, (t - 1) & 1, &B.ab, a.ctrl, 36, a.wait_ns))) break;
+      store_gamma<NC>(smem + L.g, rc, a.Kp, reinterpret_cast<const uint32_t*>(v));
       if (!(ok = exchange(red + 2 * kTile, &B.sm, t & 1, rc, sum, &other, &B, a.ctrl, 37, a.wait_ns))) break;
       const float inv = tok < a.N ? 1.0f / (sum + other) : 0.f;
       // scale this key's [v | 1] row by 1/s (normalises its Gamma row inside the contraction)
-      if (!(ok = wait_bounded(&B.v_full[s], (t >> 1) & 1, &B.ab, a.ctrl, 38, a.wait_ns))) break;
+      if (!(ok = warp_wait(&B.v_full[s], (t >> 1) & 1, &B.ab, a.ctrl, 38, a.wait_ns))) break;
       const __nv_bfloat162 inv2 = __float2bfloat162_rn(inv);
       uint8_t* vrow = smem + L.v + s * 16384;
 #pragma unroll
@@ -456,11 +476,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         *reinterpret_cast<uint4*>(smem + L.inv + sw128_chunk(rc.row, 1)) = make_uint4(0, 0, 0, 0);
       }
       fence_async_smem();
-      mbar_arrive(&B.g_full);
+      warp_arrive(&B.g_full);
     }
     // epilogue: state rows of this CTA -> global
     if (ok && T > 0 && rc.hf < MB) {
-      if (wait_bounded(&B.done, 0, &B.ab, a.ctrl, 39, a.wait_ns)) {
+      if (warp_wait(&B.done, 0, &B.ab, a.ctrl, 39, a.wait_ns)) {
         tc_fence_after();
         const int comp = 128 * rc.hf + rc.row;
         uint32_t r[80];
@@ -493,7 +513,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 
 // ----------------------------------------------------------------------------------------------- read / responsibilities
 // kRead: grid (splits, B*H); reads state[bh] and writes O.  !kRead: writes normalised Gamma (fp32).
-template <bool kRead>
+template <bool kRead, int NC>
 __global__ void __launch_bounds__(kThreadsTc, 1)
     tc_read_kernel(const __grid_constant__ CUtensorMap tmQ, TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -566,6 +586,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     const RowCtx rc = row_ctx();
     const float* cs = reinterpret_cast<const float*>(smem + L.c);
     float* red = reinterpret_cast<float*>(smem + L.red);
+    zero_unused_logits<NC>(tmem, rc, a.Kp);
     const int rt = threadIdx.x - 32 * kRowWarp0;  // 0..255
     bool ok = true;
     if (kRead) {
@@ -583,60 +604,60 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         }
       }
       fence_async_smem();
-      mbar_arrive(&B.sb_full);
+      warp_arrive(&B.sb_full);
     }
-    ok = wait_bounded(&B.w_full, 0, &B.ab, a.ctrl, 50, a.wait_ns);
+    ok = warp_wait(&B.w_full, 0, &B.ab, a.ctrl, 50, a.wait_ns);
     if (ok && T > 0) {
-      ok = wait_bounded(&B.x_full[0], 0, &B.ab, a.ctrl, 51, a.wait_ns);
+      ok = warp_wait(&B.x_full[0], 0, &B.ab, a.ctrl, 51, a.wait_ns);
       if (ok) {
         transform_row(smem + L.x, rc, tmem);
-        mbar_arrive(&B.x_empty[0]);
+        warp_arrive(&B.x_empty[0]);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&B.ax_full);
+        warp_arrive(&B.ax_full);
       }
     }
-    float v[128];
+    float v[NC];
     float s_prev = 1.f;
     for (int t = 0; ok && t < T; ++t) {
-      if (!(ok = wait_bounded(&B.l_full, t & 1, &B.ab, a.ctrl, 52, a.wait_ns))) break;
+      if (!(ok = warp_wait(&B.l_full, t & 1, &B.ab, a.ctrl, 52, a.wait_ns))) break;
       tc_fence_after();
       if (t + 1 < T) {
         const int s1 = (t + 1) & 1;
-        if (!(ok = wait_bounded(&B.x_full[s1], ((t + 1) >> 1) & 1, &B.ab, a.ctrl, 53, a.wait_ns))) break;
-        if (!(ok = wait_bounded(&B.ax_empty, t & 1, &B.ab, a.ctrl, 54, a.wait_ns))) break;
+        if (!(ok = warp_wait(&B.x_full[s1], ((t + 1) >> 1) & 1, &B.ab, a.ctrl, 53, a.wait_ns))) break;
+        if (!(ok = warp_wait(&B.ax_empty, t & 1, &B.ab, a.ctrl, 54, a.wait_ns))) break;
         tc_fence_after();
         transform_row(smem + L.x + s1 * 16384, rc, tmem);
-        mbar_arrive(&B.x_empty[s1]);
+        warp_arrive(&B.x_empty[s1]);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&B.ax_full);
+        warp_arrive(&B.ax_full);
       }
-      float mx = load_logits(tmem, rc, cs, a.Kp, v);
+      float mx = load_logits<NC>(tmem, rc, cs, v);
       tc_fence_before();
-      mbar_arrive(&B.l_empty);
+      warp_arrive(&B.l_empty);
       float other;
       if (!(ok = exchange(red, &B.mx, t & 1, rc, mx, &other, &B, a.ctrl, 55, a.wait_ns))) break;
       mx = fmaxf(mx, other);
       const int tok = (tile0 + t) * kTile + rc.row;
       if (kRead) {
-        float sum = exp_pack(v, mx);
-        if (t > 0 && !(ok = wait_bounded(&B.g_empty, (t - 1) & 1, &B.ab, a.ctrl, 56, a.wait_ns))) break;
-        store_gamma(smem + L.g, rc, a.Kp, reinterpret_cast<const uint32_t*>(v));
+        float sum = exp_pack<NC>(v, mx);
+        if (t > 0 && !(ok = warp_wait(&B.g_empty, (t - 1) & 1, &B.ab, a.ctrl, 56, a.wait_ns))) break;
+        store_gamma<NC>(smem + L.g, rc, a.Kp, reinterpret_cast<const uint32_t*>(v));
         fence_async_smem();
-        mbar_arrive(&B.g_full);
+        warp_arrive(&B.g_full);
         if (!(ok = exchange(red + 2 * kTile, &B.sm, t & 1, rc, sum, &other, &B, a.ctrl, 57, a.wait_ns))) break;
         sum += other;
         // epilogue of the previous tile (its read contraction has had a whole tile to finish)
         if (t > 0) {
-          if (!(ok = wait_bounded(&B.o_full, (t - 1) & 1, &B.ab, a.ctrl, 58, a.wait_ns))) break;
+          if (!(ok = warp_wait(&B.o_full, (t - 1) & 1, &B.ab, a.ctrl, 58, a.wait_ns))) break;
           tc_fence_after();
           uint32_t r[32], zc[16];
           tmem_ld32(tmem + rc.lane_base + kColAcc + 32 * rc.hf, r);
           tmem_ld16(tmem + rc.lane_base + kColAcc + 64, zc);  // zc[0] = Z column
           tmem_ld_wait();
           tc_fence_before();
-          mbar_arrive(&B.o_empty);
+          warp_arrive(&B.o_empty);
           const int ptok = tok - kTile;
           const float rden = 1.0f / (__uint_as_float(zc[0]) + a.eps * s_prev);
           if (ptok < a.N) {
@@ -655,24 +676,24 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         // responsibilities: gamma = e / s in float32
         float s0 = 0.f;
 #pragma unroll
-        for (int k = 0; k < 128; ++k) {
+        for (int k = 0; k < NC; ++k) {
           v[k] = ex2_approx(v[k] - mx);
           s0 += v[k];
         }
         if (!(ok = exchange(red + 2 * kTile, &B.sm, t & 1, rc, s0, &other, &B, a.ctrl, 59, a.wait_ns))) break;
         const float rs = 1.0f / (s0 + other);
         if (tok < a.N) {
-          float* dst = reinterpret_cast<float*>(a.out) + ((size_t)bh * a.N + tok) * a.K + 128 * rc.hf;
-          const int nk = min(max(a.K - 128 * rc.hf, 0), 128);
+          float* dst = reinterpret_cast<float*>(a.out) + ((size_t)bh * a.N + tok) * a.K + NC * rc.hf;
+          const int nk = min(max(a.K - NC * rc.hf, 0), NC);
 #pragma unroll
-          for (int k = 0; k < 128; ++k)
+          for (int k = 0; k < NC; ++k)
             if (k < nk) dst[k] = v[k] * rs;
         }
       }
     }
     // last epilogue
     if (kRead && ok && T > 0) {
-      if (wait_bounded(&B.o_full, (T - 1) & 1, &B.ab, a.ctrl, 60, a.wait_ns)) {
+      if (warp_wait(&B.o_full, (T - 1) & 1, &B.ab, a.ctrl, 60, a.wait_ns)) {
         tc_fence_after();
         uint32_t r[32], zc[16];
         tmem_ld32(tmem + rc.lane_base + kColAcc + 32 * rc.hf, r);
@@ -750,6 +771,32 @@ int split_for(int BH, int tiles) {
   return s < 1 ? 1 : s;
 }
 
+// Launches the per-tile kernels with NC components per row thread (2 * NC >= Kp).
+template <int NC>
+gma_status_t tc_launch(const gma_problem_t& p, gma_op_t op, const TcPlan& pl, TcArgs a, const void* Q, const void* K,
+                       const void* V, cudaStream_t st) {
+  const int BH = p.B * p.H;
+  CUtensorMap mq, mk, mv;
+  if (op == GMA_OP_RESPONSIBILITIES) {
+    if (!make_map(&mq, Q, BH, p.N)) return GMA_ERR_CUDA;
+    const uint32_t smem = smem_bytes(read_layout(pl.Kp).total);
+    if (set_smem_optin((const void*)tc_read_kernel<false, NC>, (int)smem, 0) != GMA_OK) return GMA_ERR_CUDA;
+    a.fault = 0;
+    GMA_LAUNCH("tc_resp", (tc_read_kernel<false, NC>), dim3(pl.splits, BH), kThreadsTc, smem, st, mq, a);
+    return check_launch("launch tc_resp", (const void*)tc_read_kernel<false, NC>);
+  }
+  if (!make_map(&mq, Q, BH, p.N) || !make_map(&mk, K, BH, p.N) || !make_map(&mv, V, BH, p.N)) return GMA_ERR_CUDA;
+  const uint32_t smem_w = smem_bytes(write_layout(pl.Kp).total);
+  if (set_smem_optin((const void*)tc_write_kernel<true, NC>, (int)smem_w, 0) != GMA_OK) return GMA_ERR_CUDA;
+  GMA_LAUNCH("tc_bidir_write", (tc_write_kernel<true, NC>), dim3(pl.splits, BH), kThreadsTc, smem_w, st, mk, mv, a);
+  if (gma_status_t e = check_launch("launch tc_bidir_write", (const void*)tc_write_kernel<true, NC>)) return e;
+  a.fault = 0;
+  const uint32_t smem_r = smem_bytes(read_layout(pl.Kp).total);
+  if (set_smem_optin((const void*)tc_read_kernel<true, NC>, (int)smem_r, 0) != GMA_OK) return GMA_ERR_CUDA;
+  GMA_LAUNCH("tc_bidir_read", (tc_read_kernel<true, NC>), dim3(pl.splits, BH), kThreadsTc, smem_r, st, mq, a);
+  return check_launch("launch tc_bidir_read", (const void*)tc_read_kernel<true, NC>);
+}
+
 uint32_t g_fault_next = 0;  // test hook, consumed by the next launch of the write kernel
 std::mutex g_fault_mu;
 
@@ -769,7 +816,7 @@ TcPlan tc_plan(const gma_problem_t& p, gma_op_t op) {
   t.splits = cdiv(t.tiles > 0 ? t.tiles : 1, t.seg_tiles);
   t.off_w = align_up(sizeof(Ctrl));
   t.off_c = align_up(t.off_w + (size_t)p.H * t.Kp * 256);
-  t.off_state = align_up(t.off_c + (size_t)p.H * t.Kp * 4);
+  t.off_state = align_up(t.off_c + (size_t)p.H * kCTable * 4);
   size_t st = 0;
   if (op == GMA_OP_BIDIR) st = (size_t)BH * t.Kp * kStCols * 4;
   t.total = align_up(t.off_state + st);
@@ -804,29 +851,13 @@ gma_status_t tc_run(const gma_problem_t& p, gma_op_t op, const void* Q, const vo
     g_fault_next = 0;
   }
   const size_t zero_n = op == GMA_OP_BIDIR ? (size_t)BH * pl.Kp * kStCols : 0;
-  GMA_LAUNCH("tc_prep", tc_prep_kernel, dim3(pl.Kp, p.H), 128, 0, st, mu, sigma2, log_pi, p.H, p.K, pl.Kp,
+  GMA_LAUNCH("tc_prep", tc_prep_kernel, dim3(kCTable, p.H), 128, 0, st, mu, sigma2, log_pi, p.H, p.K, pl.Kp,
              (uint8_t*)a.w_img, (float*)a.cbias, a.ctrl, a.state, zero_n);
   if (gma_status_t e = check_launch("launch tc_prep", (const void*)tc_prep_kernel)) return e;
-  CUtensorMap mq, mk, mv;
-  if (op == GMA_OP_RESPONSIBILITIES) {
-    if (!make_map(&mq, Q, BH, p.N)) return GMA_ERR_CUDA;
-    const uint32_t smem = smem_bytes(read_layout(pl.Kp).total);
-    if (set_smem_optin((const void*)tc_read_kernel<false>, (int)smem, 0) != GMA_OK) return GMA_ERR_CUDA;
-    a.fault = 0;
-    GMA_LAUNCH("tc_resp", tc_read_kernel<false>, dim3(pl.splits, BH), kThreadsTc, smem, st, mq, a);
-    return check_launch("launch tc_resp", (const void*)tc_read_kernel<false>);
-  }
-  if (!make_map(&mq, Q, BH, p.N) || !make_map(&mk, K, BH, p.N) || !make_map(&mv, V, BH, p.N))
-    return GMA_ERR_CUDA;
-  const uint32_t smem_w = smem_bytes(write_layout(pl.Kp).total);
-  if (set_smem_optin((const void*)tc_write_kernel<true>, (int)smem_w, 0) != GMA_OK) return GMA_ERR_CUDA;
-  GMA_LAUNCH("tc_bidir_write", tc_write_kernel<true>, dim3(pl.splits, BH), kThreadsTc, smem_w, st, mk, mv, a);
-  if (gma_status_t e = check_launch("launch tc_bidir_write", (const void*)tc_write_kernel<true>)) return e;
-  a.fault = 0;
-  const uint32_t smem_r = smem_bytes(read_layout(pl.Kp).total);
-  if (set_smem_optin((const void*)tc_read_kernel<true>, (int)smem_r, 0) != GMA_OK) return GMA_ERR_CUDA;
-  GMA_LAUNCH("tc_bidir_read", tc_read_kernel<true>, dim3(pl.splits, BH), kThreadsTc, smem_r, st, mq, a);
-  return check_launch("launch tc_bidir_read", (const void*)tc_read_kernel<true>);
+  const int nc = pl.Kp <= 64 ? 32 : (pl.Kp <= 128 ? 64 : 128);
+  if (nc == 32) return tc_launch<32>(p, op, pl, a, Q, K, V, st);
+  if (nc == 64) return tc_launch<64>(p, op, pl, a, Q, K, V, st);
+  return tc_launch<128>(p, op, pl, a, Q, K, V, st);
 }
 
 bool tc_available() { return encode_fn() != nullptr; }

@@ -50,20 +50,39 @@ struct Abort {
   volatile uint32_t flag;
 };
 
-// Bounded wait on phase `parity` of `bar`.  Returns false on timeout or abort.
+// Bounded wait on phase `parity` of `bar`.  Returns false on timeout or abort.  try_wait itself
+// suspends the thread for a while; the clock and the abort flag are checked every 16 tries.
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, Abort* ab, Ctrl* ctrl, uint32_t site,
                                              uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  for (;;) {
+  uint64_t t0 = 0;
+  for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (ab->flag) return false;
-    if (global_timer_ns() - t0 > limit_ns) {
-      ab->flag = 1;
-      if (atomicCAS(&ctrl->err, kErrNone, kErrTimeout) == kErrNone) ctrl->err_site = site;
-      return false;
+    if ((i & 15) == 0) {
+      if (ab->flag) return false;
+      const uint64_t now = global_timer_ns();
+      if (t0 == 0) t0 = now;
+      if (now - t0 > limit_ns) {
+        ab->flag = 1;
+        if (atomicCAS(&ctrl->err, kErrNone, kErrTimeout) == kErrNone) ctrl->err_site = site;
+        return false;
+      }
     }
   }
+}
+
+// wait_bounded taken by a whole warp with one outcome for every lane (row-warp control flow stays
+// uniform, which the warp-level arrivals and tcgen05 .sync.aligned operations rely on).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, Abort* ab, Ctrl* ctrl, uint32_t site,
+                                          uint64_t limit_ns) {
+  return __all_sync(0xffffffffu, wait_bounded(bar, parity, ab, ctrl, site, limit_ns));
+}
+
+// One arrival per warp on `bar` (barriers counted in warps): the warp's lanes synchronise first, which
+// orders their earlier shared-memory and tensor-memory accesses before lane 0's release-arrive.
+__device__ __forceinline__ void warp_arrive(uint64_t* bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
 // ---------------------------------------------------------------------------------------------- TMA
@@ -198,6 +217,19 @@ __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+// (a, b) += (c, d) with one packed float32x2 add.
+__device__ __forceinline__ void add_f32x2(float& a, float& b, float c, float d) {
+  asm("{\n .reg .b64 x, y;\n mov.b64 x, {%0, %1};\n mov.b64 y, {%2, %3};\n add.rn.f32x2 x, x, y;\n"
+      " mov.b64 {%0, %1}, x;\n}\n"
+      : "+f"(a), "+f"(b)
+      : "f"(c), "f"(d));
+}
+// Three-input maximum.
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
