@@ -162,7 +162,8 @@ __device__ __forceinline__ RowCtx row_ctx() {
 
 // Builds this thread's half of the [x^2 | x] fp16 operand row from the bf16 X tile and stores it to
 // TMEM (A operand of the log-density contraction, lane = token, two fp16 per 32-bit column).
-__device__ __forceinline__ void transform_row(const uint8_t* xs, const RowCtx& rc, uint32_t tmem) {
+__device__ __forceinline__ void transform_row(const uint8_t* xs, const RowCtx& rc, uint32_t tmem,
+                                              uint32_t col_ax = kColAx) {
   uint32_t sq[16], lin[16];
 #pragma unroll
   for (int jj = 0; jj < 4; ++jj) {
@@ -175,8 +176,8 @@ __device__ __forceinline__ void transform_row(const uint8_t* xs, const RowCtx& r
       sq[jj * 4 + i] = pack_f16x2(lo * lo, hi * hi);
     }
   }
-  tmem_st16(tmem + rc.lane_base + kColAx + 16 * rc.hf, sq);
-  tmem_st16(tmem + rc.lane_base + kColAx + 32 + 16 * rc.hf, lin);
+  tmem_st16(tmem + rc.lane_base + col_ax + 16 * rc.hf, sq);
+  tmem_st16(tmem + rc.lane_base + col_ax + 32 + 16 * rc.hf, lin);
 }
 
 // Zeroes this thread's logit columns at or beyond Kp once per CTA: the contraction (N = Kp) never
@@ -238,6 +239,32 @@ __device__ __forceinline__ float exp_pack(float* v, float m) {
   return (s0 + s1) + (s2 + s3);
 }
 
+// e_k = 2^(v_k - m) in place (float32); returns the sum of the e_k.
+template <int NC>
+__device__ __forceinline__ float exp_inplace(float* v, float m) {
+  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+  for (int i = 0; i < NC / 2; ++i) {
+    float t0 = v[2 * i], t1 = v[2 * i + 1];
+    add_f32x2(t0, t1, -m, -m);
+    v[2 * i] = ex2_approx(t0);
+    v[2 * i + 1] = ex2_approx(t1);
+    if (i & 1)
+      add_f32x2(s2, s3, v[2 * i], v[2 * i + 1]);
+    else
+      add_f32x2(s0, s1, v[2 * i], v[2 * i + 1]);
+  }
+  return (s0 + s1) + (s2 + s3);
+}
+
+// v_k * r packed to bf16 pairs in place (word i of v receives (v_2i r, v_2i+1 r)).
+template <int NC>
+__device__ __forceinline__ void scale_pack(float* v, float r) {
+  uint32_t* packed = reinterpret_cast<uint32_t*>(v);
+#pragma unroll
+  for (int i = 0; i < NC / 2; ++i) packed[i] = pack_bf16x2(v[2 * i] * r, v[2 * i + 1] * r);
+}
+
 // Stores this thread's NC packed bf16 values (components NC*hf ...) into the swizzled Gamma~ tile
 // (row = token; 64-component blocks 16 KB apart).  Components at or beyond Kp are skipped.
 template <int NC>
@@ -256,10 +283,10 @@ __device__ __forceinline__ void store_gamma(uint8_t* g, const RowCtx& rc, int Kp
 // Exchange of one float per row between the two halves through smem, ordered by an mbarrier that
 // all 256 row threads arrive on.
 __device__ __forceinline__ bool exchange(float* red, uint64_t* bar, uint32_t parity, const RowCtx& rc, float mine,
-                                         float* partner, Bars* B, Ctrl* ctrl, uint32_t site, uint64_t ns) {
+                                         float* partner, Abort* ab, Ctrl* ctrl, uint32_t site, uint64_t ns) {
   red[rc.hf * kTile + rc.row] = mine;
   warp_arrive(bar);
-  if (!warp_wait(bar, parity, &B->ab, ctrl, site, ns)) return false;
+  if (!warp_wait(bar, parity, ab, ctrl, site, ns)) return false;
   *partner = red[(rc.hf ^ 1) * kTile + rc.row];
   return true;
 }
@@ -323,12 +350,12 @@ __device__ __forceinline__ void producer(const TcArgs& a, const CUtensorMap* tmX
 }
 
 // Issues the log-density contraction of one tile: LOG[128 x Kp] = AX[128 x 128] * W^T.
-__device__ __forceinline__ void issue_logits(uint32_t tmem, uint32_t w_addr, int Kp) {
+__device__ __forceinline__ void issue_logits(uint32_t tmem, uint32_t w_addr, int Kp, uint32_t col_ax = kColAx) {
   const uint32_t idesc = make_idesc(128, Kp, 0, 0, 0, 0);
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
     const uint64_t bd = make_sdesc(w_addr + (ks >> 2) * (uint32_t)Kp * 128 + (ks & 3) * 32, 16, 1024);
-    mma_ts(tmem + kColLog, tmem + kColAx + 8 * ks, bd, idesc, ks > 0 ? 1u : 0u);
+    mma_ts(tmem + kColLog, tmem + col_ax + 8 * ks, bd, idesc, ks > 0 ? 1u : 0u);
   }
 }
 
@@ -450,12 +477,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       tc_fence_before();
       warp_arrive(&B.l_empty);
       float other;
-      if (!(ok = exchange(red, &B.mx, t & 1, rc, mx, &other, &B, a.ctrl, 35, a.wait_ns))) break;
+      if (!(ok = exchange(red, &B.mx, t & 1, rc, mx, &other, &B.ab, a.ctrl, 35, a.wait_ns))) break;
       mx = fmaxf(mx, other);
       float sum = exp_pack<NC>(v, mx);
       if (t > 0 && !(ok = warp_wait(&B.g_empty, (t - 1) & 1, &B.ab, a.ctrl, 36, a.wait_ns))) break;
       store_gamma<NC>(smem + L.g, rc, a.Kp, reinterpret_cast<const uint32_t*>(v));
-      if (!(ok = exchange(red + 2 * kTile, &B.sm, t & 1, rc, sum, &other, &B, a.ctrl, 37, a.wait_ns))) break;
+      if (!(ok = exchange(red + 2 * kTile, &B.sm, t & 1, rc, sum, &other, &B.ab, a.ctrl, 37, a.wait_ns))) break;
       const float inv = tok < a.N ? 1.0f / (sum + other) : 0.f;
       // scale this key's [v | 1] row by 1/s (normalises its Gamma row inside the contraction)
       if (!(ok = warp_wait(&B.v_full[s], (t >> 1) & 1, &B.ab, a.ctrl, 38, a.wait_ns))) break;
@@ -637,7 +664,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       tc_fence_before();
       warp_arrive(&B.l_empty);
       float other;
-      if (!(ok = exchange(red, &B.mx, t & 1, rc, mx, &other, &B, a.ctrl, 55, a.wait_ns))) break;
+      if (!(ok = exchange(red, &B.mx, t & 1, rc, mx, &other, &B.ab, a.ctrl, 55, a.wait_ns))) break;
       mx = fmaxf(mx, other);
       const int tok = (tile0 + t) * kTile + rc.row;
       if (kRead) {
@@ -646,7 +673,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         store_gamma<NC>(smem + L.g, rc, a.Kp, reinterpret_cast<const uint32_t*>(v));
         fence_async_smem();
         warp_arrive(&B.g_full);
-        if (!(ok = exchange(red + 2 * kTile, &B.sm, t & 1, rc, sum, &other, &B, a.ctrl, 57, a.wait_ns))) break;
+        if (!(ok = exchange(red + 2 * kTile, &B.sm, t & 1, rc, sum, &other, &B.ab, a.ctrl, 57, a.wait_ns))) break;
         sum += other;
         // epilogue of the previous tile (its read contraction has had a whole tile to finish)
         if (t > 0) {
@@ -680,7 +707,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           v[k] = ex2_approx(v[k] - mx);
           s0 += v[k];
         }
-        if (!(ok = exchange(red + 2 * kTile, &B.sm, t & 1, rc, s0, &other, &B, a.ctrl, 59, a.wait_ns))) break;
+        if (!(ok = exchange(red + 2 * kTile, &B.sm, t & 1, rc, s0, &other, &B.ab, a.ctrl, 59, a.wait_ns))) break;
         const float rs = 1.0f / (s0 + other);
         if (tok < a.N) {
           float* dst = reinterpret_cast<float*>(a.out) + ((size_t)bh * a.N + tok) * a.K + NC * rc.hf;
@@ -719,6 +746,386 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
+  }
+}
+
+// ----------------------------------------------------------------------------------------------- causal
+// Chunked causal sweep.  CTA (segment, bh) starts from the exclusive prefix state of its segment and
+// walks the segment tile by tile with the state S resident in TMEM:
+//   O_i = [gq~_i . S_prev + sum_{j in tile, j <= i} (gq~_i . gk_j) [v_j | 1]] / (... + eps s_i),
+//   S  += Gamma_K(tile)^T [V | 1]
+// (gist.science summary, "Variants and training" item 3: prefix sums, O_i depends on j <= i only).
+// The "1" column of [V | 1] is a separate N=16 contraction against a constant K-major ones tile.
+constexpr uint32_t kCColP = 128;   // intra-tile affinity P (fp32 128 cols; bf16 halves at 128 and 192)
+constexpr uint32_t kCColS = 256;   // state accumulators, 80 columns per 128-component block
+constexpr uint32_t kCColO = 416;   // output accumulator (80 columns), shared with the [x^2 | x] operand
+
+struct CausalLayout {
+  uint32_t w, gk, x, v, sbv, sbz, ones, c, red, total;
+};
+__host__ __device__ inline CausalLayout causal_layout(int Kp) {
+  CausalLayout s{};
+  const int MB = (Kp + 127) / 128, KB = (Kp + 63) / 64;
+  s.w = 0;
+  s.gk = align1k(Kp * 256);          // Gamma_K (bf16): MN-major A of the state update, K-major B of P
+  s.x = s.gk + MB * 32768;           // two X stages: key tile, query tile
+  s.v = s.x + 2 * 16384;             // V tile (MN-major B)
+  s.sbv = s.v + 16384;               // bf16 copy of S_prev[:, 0:64], MN-major B (comp groups of 1 KB)
+  s.sbz = s.sbv + (Kp / 8) * 1024;   // bf16 copy of S_prev[:, 64] as row 0 of a 16-row K-major B
+  s.ones = s.sbz + KB * 2048;        // constant ones row (K-major, 16 x 128 tokens)
+  s.c = s.ones + 4096;
+  s.red = s.c + 1024;
+  s.total = s.red + 4 * kTile * 4;
+  return s;
+}
+
+struct CBars {
+  uint64_t w_full, x_full[2], x_empty[2], v_full, v_empty;
+  uint64_t ax_full, lk_full, gk_full, lq_full, gq_full, sb_full, p_full, pb_full, o_full, s_full;
+  uint64_t mx, sm, done;
+  uint32_t tmem_base;
+  Abort ab;
+};
+
+template <int NC>
+__global__ void __launch_bounds__(kThreadsTc, 1)
+    tc_causal_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, TcArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ CBars B;
+  const CausalLayout L = causal_layout(a.Kp);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = blockIdx.y, seg = blockIdx.x;
+  const int tile0 = seg * a.seg_tiles;
+  const int T = max(0, min(a.tiles, tile0 + a.seg_tiles) - tile0);
+  const int MB = (a.Kp + 127) / 128;
+  const int KS = a.Kp / 16;
+
+  // zero Gamma_K and the state copies; ones tile: row 0 of each 64-token block is 1.0 (bf16 0x3F80)
+  for (uint32_t i = threadIdx.x; i < (uint32_t)MB * 32768 / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(smem + L.gk)[i] = make_uint4(0, 0, 0, 0);
+  for (uint32_t i = threadIdx.x; i < (L.ones - L.sbv) / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(smem + L.sbv)[i] = make_uint4(0, 0, 0, 0);
+  for (uint32_t i = threadIdx.x; i < 4096 / 16; i += blockDim.x) {
+    const uint32_t w = ((i * 16) % 2048) < 128 ? 0x3F803F80u : 0u;
+    reinterpret_cast<uint4*>(smem + L.ones)[i] = make_uint4(w, w, w, w);
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(&B.w_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&B.x_full[s], 1);
+      mbar_init(&B.x_empty[s], kRowWarps);
+    }
+    mbar_init(&B.v_full, 1);
+    mbar_init(&B.v_empty, 1);
+    mbar_init(&B.ax_full, kRowWarps);
+    mbar_init(&B.lk_full, 1);
+    mbar_init(&B.gk_full, kRowWarps);
+    mbar_init(&B.lq_full, 1);
+    mbar_init(&B.gq_full, kRowWarps);
+    mbar_init(&B.sb_full, kRowWarps);
+    mbar_init(&B.p_full, 1);
+    mbar_init(&B.pb_full, kRowWarps);
+    mbar_init(&B.o_full, 1);
+    mbar_init(&B.s_full, 1);
+    mbar_init(&B.mx, kRowWarps);
+    mbar_init(&B.sm, kRowWarps);
+    mbar_init(&B.done, 1);
+    B.ab.flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&B.tmem_base, 512);
+    tmem_relinquish();
+  }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = B.tmem_base;
+
+  if (warp < kRowWarp0) {
+    setmaxnreg_dec<kCtrlRegs>();
+    if (warp == 0 && lane == 0) {
+      // ---------------------------------------------------------------- producer
+      const uint32_t wbytes = (uint32_t)a.Kp * 256, cbytes = kCTable * 4;
+      const int h = bh % a.H;
+      mbar_expect_tx(&B.w_full, wbytes + cbytes);
+      for (uint32_t o = 0; o < wbytes; o += 32768)
+        bulk_load(smem + L.w + o, a.w_img + (size_t)h * wbytes + o, min(32768u, wbytes - o), &B.w_full);
+      bulk_load(smem + L.c, a.cbias + (size_t)h * kCTable, cbytes, &B.w_full);
+      int issued[3] = {-1, -1, -1};  // parity of the last load armed on x_full[0], x_full[1], v_full
+      for (int t = 0; t < T; ++t) {
+        const uint32_t pe = (t & 1) ^ 1;
+        const int row0 = (tile0 + t) * kTile;
+        if (!wait_bounded(&B.x_empty[0], pe, &B.ab, a.ctrl, 70, a.wait_ns)) break;
+        mbar_expect_tx(&B.x_full[0], 16384);
+        tma_load_3d(smem + L.x, &tmK, 0, row0, bh, &B.x_full[0]);
+        issued[0] = t & 1;
+        if (!wait_bounded(&B.x_empty[1], pe, &B.ab, a.ctrl, 71, a.wait_ns)) break;
+        mbar_expect_tx(&B.x_full[1], 16384);
+        tma_load_3d(smem + L.x + 16384, &tmQ, 0, row0, bh, &B.x_full[1]);
+        issued[1] = t & 1;
+        if (!wait_bounded(&B.v_empty, pe, &B.ab, a.ctrl, 72, a.wait_ns)) break;
+        mbar_expect_tx(&B.v_full, 16384);
+        tma_load_3d(smem + L.v, &tmV, 0, row0, bh, &B.v_full);
+        issued[2] = t & 1;
+      }
+      // never leave with copies in flight
+      Abort none{0};
+      if (issued[0] >= 0) wait_bounded(&B.x_full[0], (uint32_t)issued[0], &none, a.ctrl, 73, a.wait_ns);
+      if (issued[1] >= 0) wait_bounded(&B.x_full[1], (uint32_t)issued[1], &none, a.ctrl, 74, a.wait_ns);
+      if (issued[2] >= 0) wait_bounded(&B.v_full, (uint32_t)issued[2], &none, a.ctrl, 75, a.wait_ns);
+    } else if (warp == 1 && lane == 0) {
+      // ---------------------------------------------------------------- MMA issuer
+      const uint32_t w_addr = smem_u32(smem + L.w), gk = smem_u32(smem + L.gk), v_addr = smem_u32(smem + L.v);
+      const uint32_t sbv = smem_u32(smem + L.sbv), sbz = smem_u32(smem + L.sbz), ones = smem_u32(smem + L.ones);
+      const uint32_t id_c64 = make_idesc(128, 64, 1, 1, 0, 1);    // A tmem, B MN-major
+      const uint32_t id_c16 = make_idesc(128, 16, 1, 1, 0, 0);    // A tmem, B K-major
+      const uint32_t id_p = make_idesc(128, 128, 1, 1, 0, 0);     // P = Gq~ Gk^T
+      const uint32_t id_s64 = make_idesc(128, 64, 1, 1, 1, 1);    // A MN-major (Gamma_K^T), B MN-major (V)
+      const uint32_t id_s16 = make_idesc(128, 16, 1, 1, 1, 0);    // A MN-major, B K-major (ones)
+      bool ok = wait_bounded(&B.w_full, 0, &B.ab, a.ctrl, 80, a.wait_ns);
+      for (int t = 0; ok && t < T; ++t) {
+        const uint32_t ph = t & 1;
+        if (!(ok = wait_bounded(&B.ax_full, ph, &B.ab, a.ctrl, 81, a.wait_ns))) break;
+        tc_fence_after();
+        issue_logits(tmem, w_addr, a.Kp, kCColO);
+        mma_commit(&B.lk_full);
+        if (!(ok = wait_bounded(&B.gk_full, ph, &B.ab, a.ctrl, 82, a.wait_ns))) break;
+        tc_fence_after();
+        issue_logits(tmem, w_addr, a.Kp, kCColO);
+        mma_commit(&B.lq_full);
+        if (!(ok = wait_bounded(&B.gq_full, ph, &B.ab, a.ctrl, 83, a.wait_ns) &&
+                   wait_bounded(&B.sb_full, ph, &B.ab, a.ctrl, 84, a.wait_ns)))
+          break;
+        tc_fence_after();
+        for (int ks = 0; ks < KS; ++ks) {
+          const uint32_t aq = tmem + kColLog + 8 * ks;  // Gq~ (bf16 pairs) over the logit columns
+          mma_ts(tmem + kCColO, aq, make_sdesc(sbv + 2048 * ks, 16384, 1024), id_c64, ks > 0);
+          mma_ts(tmem + kCColO + 64, aq, make_sdesc(sbz + (ks >> 2) * 2048 + (ks & 3) * 32, 16, 1024), id_c16,
+                 ks > 0);
+          mma_ts(tmem + kCColP, aq, make_sdesc(gk + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024), id_p, ks > 0);
+        }
+        mma_commit(&B.p_full);
+        if (!(ok = wait_bounded(&B.pb_full, ph, &B.ab, a.ctrl, 85, a.wait_ns) &&
+                   wait_bounded(&B.v_full, ph, &B.ab, a.ctrl, 86, a.wait_ns)))
+          break;
+        tc_fence_after();
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {  // intra-tile term: O += P [V | 1]
+          const uint32_t ap = tmem + kCColP + (s < 4 ? 8 * s : 64 + 8 * (s - 4));
+          mma_ts(tmem + kCColO, ap, make_sdesc(v_addr + 2048 * s, 16384, 1024), id_c64, 1u);
+          mma_ts(tmem + kCColO + 64, ap, make_sdesc(ones + (s >> 2) * 2048 + (s & 3) * 32, 16, 1024), id_c16, 1u);
+        }
+        for (int mb = 0; mb < MB; ++mb) {  // state update: S += Gamma_K^T [V | 1]
+#pragma unroll
+          for (int s = 0; s < 8; ++s) {
+            const uint64_t ad = make_sdesc(gk + mb * 32768 + 2048 * s, 16384, 1024);
+            mma_ss(tmem + kCColS + kStCols * mb, ad, make_sdesc(v_addr + 2048 * s, 16384, 1024), id_s64, 1u);
+            mma_ss(tmem + kCColS + kStCols * mb + 64, ad,
+                   make_sdesc(ones + (s >> 2) * 2048 + (s & 3) * 32, 16, 1024), id_s16, 1u);
+          }
+        }
+        mma_commit(&B.o_full);
+        mma_commit(&B.s_full);
+        mma_commit(&B.v_empty);
+      }
+      mma_commit(&B.done);
+      Abort none{0};
+      wait_bounded(&B.done, 0, &none, a.ctrl, 87, a.wait_ns);
+    }
+  } else {
+    setmaxnreg_inc<kRowRegs>();
+    // ------------------------------------------------------------------ row warps
+    const RowCtx rc = row_ctx();
+    const float* cs = reinterpret_cast<const float*>(smem + L.c);
+    float* red = reinterpret_cast<float*>(smem + L.red);
+    zero_unused_logits<NC>(tmem, rc, a.Kp);
+    // S <- exclusive prefix state of this segment; SB <- its bf16 copy
+    if (rc.hf < MB) {
+      const int comp = 128 * rc.hf + rc.row;
+      const float* pre = a.state + (((size_t)bh * a.splits + seg) * a.Kp + comp) * kStCols;
+      uint32_t r[16];
+#pragma unroll
+      for (int c = 0; c < 5; ++c) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) r[i] = comp < a.Kp ? __float_as_uint(__ldg(pre + 16 * c + i)) : 0u;
+        tmem_st16(tmem + rc.lane_base + kCColS + kStCols * rc.hf + 16 * c, r);
+        if (comp < a.Kp) {
+          if (c < 4) {
+            uint4 lo = make_uint4(pack_bf16x2(__uint_as_float(r[0]), __uint_as_float(r[1])),
+                                  pack_bf16x2(__uint_as_float(r[2]), __uint_as_float(r[3])),
+                                  pack_bf16x2(__uint_as_float(r[4]), __uint_as_float(r[5])),
+                                  pack_bf16x2(__uint_as_float(r[6]), __uint_as_float(r[7])));
+            uint4 hi = make_uint4(pack_bf16x2(__uint_as_float(r[8]), __uint_as_float(r[9])),
+                                  pack_bf16x2(__uint_as_float(r[10]), __uint_as_float(r[11])),
+                                  pack_bf16x2(__uint_as_float(r[12]), __uint_as_float(r[13])),
+                                  pack_bf16x2(__uint_as_float(r[14]), __uint_as_float(r[15])));
+            *reinterpret_cast<uint4*>(smem + L.sbv + sw128_chunk(comp, 2 * c)) = lo;
+            *reinterpret_cast<uint4*>(smem + L.sbv + sw128_chunk(comp, 2 * c + 1)) = hi;
+          } else {
+            *reinterpret_cast<__nv_bfloat16*>(smem + L.sbz + sw128_off(0, comp, 2048)) =
+                __float2bfloat16_rn(__uint_as_float(r[0]));
+          }
+        }
+      }
+    }
+    tmem_st_wait();
+    fence_async_smem();
+    tc_fence_before();
+    warp_arrive(&B.sb_full);
+    bool ok = warp_wait(&B.w_full, 0, &B.ab, a.ctrl, 90, a.wait_ns);
+    float v[NC];
+    for (int t = 0; ok && t < T; ++t) {
+      const uint32_t ph = t & 1;
+      const int tok = (tile0 + t) * kTile + rc.row;
+      // key operand
+      if (!(ok = warp_wait(&B.x_full[0], ph, &B.ab, a.ctrl, 91, a.wait_ns))) break;
+      transform_row(smem + L.x, rc, tmem, kCColO);
+      warp_arrive(&B.x_empty[0]);
+      tmem_st_wait();
+      tc_fence_before();
+      warp_arrive(&B.ax_full);
+      // Gamma_K (normalised; zero rows past N) -> smem
+      if (!(ok = warp_wait(&B.lk_full, ph, &B.ab, a.ctrl, 92, a.wait_ns))) break;
+      tc_fence_after();
+      float mx = load_logits<NC>(tmem, rc, cs, v);
+      float other;
+      if (!(ok = exchange(red, &B.mx, 0, rc, mx, &other, &B.ab, a.ctrl, 93, a.wait_ns)))
+        break;
+      float sum = exp_inplace<NC>(v, fmaxf(mx, other));
+      if (!(ok = exchange(red + 2 * kTile, &B.sm, 0, rc, sum, &other, &B.ab, a.ctrl, 94, a.wait_ns)))
+        break;
+      scale_pack<NC>(v, tok < a.N ? 1.0f / (sum + other) : 0.f);
+      store_gamma<NC>(smem + L.gk, rc, a.Kp, reinterpret_cast<const uint32_t*>(v));
+      // query operand
+      if (!(ok = warp_wait(&B.x_full[1], ph, &B.ab, a.ctrl, 95, a.wait_ns))) break;
+      transform_row(smem + L.x + 16384, rc, tmem, kCColO);
+      warp_arrive(&B.x_empty[1]);
+      tmem_st_wait();
+      fence_async_smem();
+      tc_fence_before();
+      warp_arrive(&B.gk_full);
+      // Gamma_Q~ (unnormalised) -> TMEM over its own logit columns
+      if (!(ok = warp_wait(&B.lq_full, ph, &B.ab, a.ctrl, 96, a.wait_ns))) break;
+      tc_fence_after();
+      mx = load_logits<NC>(tmem, rc, cs, v);
+      if (!(ok = exchange(red, &B.mx, 1, rc, mx, &other, &B.ab, a.ctrl, 97, a.wait_ns)))
+        break;
+      sum = exp_pack<NC>(v, fmaxf(mx, other));
+#pragma unroll
+      for (int c = 0; c < NC / 32; ++c)
+        tmem_st16(tmem + rc.lane_base + kColLog + (NC / 2) * rc.hf + 16 * c, reinterpret_cast<uint32_t*>(v) + 16 * c);
+      if (!(ok = exchange(red + 2 * kTile, &B.sm, 1, rc, sum, &other, &B.ab, a.ctrl, 98, a.wait_ns)))
+        break;
+      const float s_q = sum + other;
+      tmem_st_wait();
+      tc_fence_before();
+      warp_arrive(&B.gq_full);
+      // intra-tile affinity: mask j > i, bf16 over the first half of this thread's own columns
+      if (!(ok = warp_wait(&B.p_full, ph, &B.ab, a.ctrl, 99, a.wait_ns))) break;
+      tc_fence_after();
+      {
+        uint32_t pr[64];
+        tmem_ld32(tmem + rc.lane_base + kCColP + 64 * rc.hf, pr);
+        tmem_ld32(tmem + rc.lane_base + kCColP + 64 * rc.hf + 32, pr + 32);
+        tmem_ld_wait();
+        const int lim = rc.row - 64 * rc.hf;  // columns c <= lim are keys j <= i
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float p0 = (2 * i <= lim) ? __uint_as_float(pr[2 * i]) : 0.f;
+          const float p1 = (2 * i + 1 <= lim) ? __uint_as_float(pr[2 * i + 1]) : 0.f;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(tmem + rc.lane_base + kCColP + 64 * rc.hf, pk);
+        tmem_st16(tmem + rc.lane_base + kCColP + 64 * rc.hf + 16, pk + 16);
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      warp_arrive(&B.pb_full);
+      // output: this thread's output dims are 16*hf + [0,16) and 32 + 16*hf + [0,16) -- the same columns it
+      // overwrites with the next key operand, so no other warp reads them afterwards
+      if (!(ok = warp_wait(&B.o_full, ph, &B.ab, a.ctrl, 100, a.wait_ns))) break;
+      tc_fence_after();
+      {
+        uint32_t o0[16], o1[16], zc[16];
+        tmem_ld16(tmem + rc.lane_base + kCColO + 16 * rc.hf, o0);
+        tmem_ld16(tmem + rc.lane_base + kCColO + 32 + 16 * rc.hf, o1);
+        tmem_ld16(tmem + rc.lane_base + kCColO + 64, zc);
+        tmem_ld_wait();
+        const float rden = 1.0f / (__uint_as_float(zc[0]) + a.eps * s_q);
+        if (tok < a.N) {
+          __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.out) + ((size_t)bh * a.N + tok) * kDv;
+          uint4* d0 = reinterpret_cast<uint4*>(orow + 16 * rc.hf);
+          uint4* d1 = reinterpret_cast<uint4*>(orow + 32 + 16 * rc.hf);
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            d0[c] = make_uint4(pack_bf16x2(__uint_as_float(o0[8 * c]) * rden, __uint_as_float(o0[8 * c + 1]) * rden),
+                               pack_bf16x2(__uint_as_float(o0[8 * c + 2]) * rden, __uint_as_float(o0[8 * c + 3]) * rden),
+                               pack_bf16x2(__uint_as_float(o0[8 * c + 4]) * rden, __uint_as_float(o0[8 * c + 5]) * rden),
+                               pack_bf16x2(__uint_as_float(o0[8 * c + 6]) * rden, __uint_as_float(o0[8 * c + 7]) * rden));
+            d1[c] = make_uint4(pack_bf16x2(__uint_as_float(o1[8 * c]) * rden, __uint_as_float(o1[8 * c + 1]) * rden),
+                               pack_bf16x2(__uint_as_float(o1[8 * c + 2]) * rden, __uint_as_float(o1[8 * c + 3]) * rden),
+                               pack_bf16x2(__uint_as_float(o1[8 * c + 4]) * rden, __uint_as_float(o1[8 * c + 5]) * rden),
+                               pack_bf16x2(__uint_as_float(o1[8 * c + 6]) * rden, __uint_as_float(o1[8 * c + 7]) * rden));
+          }
+        }
+      }
+      // bf16 copy of the updated state for the next tile's inter-tile term
+      if (!(ok = warp_wait(&B.s_full, ph, &B.ab, a.ctrl, 101, a.wait_ns))) break;
+      tc_fence_after();
+      if (rc.hf < MB) {
+        const int comp = 128 * rc.hf + rc.row;
+        uint32_t r[16];
+#pragma unroll
+        for (int c = 0; c < 5; ++c) {
+          tmem_ld16(tmem + rc.lane_base + kCColS + kStCols * rc.hf + 16 * c, r);
+          tmem_ld_wait();
+          if (comp < a.Kp) {
+            if (c < 4) {
+              uint4 lo = make_uint4(pack_bf16x2(__uint_as_float(r[0]), __uint_as_float(r[1])),
+                                    pack_bf16x2(__uint_as_float(r[2]), __uint_as_float(r[3])),
+                                    pack_bf16x2(__uint_as_float(r[4]), __uint_as_float(r[5])),
+                                    pack_bf16x2(__uint_as_float(r[6]), __uint_as_float(r[7])));
+              uint4 hi = make_uint4(pack_bf16x2(__uint_as_float(r[8]), __uint_as_float(r[9])),
+                                    pack_bf16x2(__uint_as_float(r[10]), __uint_as_float(r[11])),
+                                    pack_bf16x2(__uint_as_float(r[12]), __uint_as_float(r[13])),
+                                    pack_bf16x2(__uint_as_float(r[14]), __uint_as_float(r[15])));
+              *reinterpret_cast<uint4*>(smem + L.sbv + sw128_chunk(comp, 2 * c)) = lo;
+              *reinterpret_cast<uint4*>(smem + L.sbv + sw128_chunk(comp, 2 * c + 1)) = hi;
+            } else {
+              *reinterpret_cast<__nv_bfloat16*>(smem + L.sbz + sw128_off(0, comp, 2048)) =
+                  __float2bfloat16_rn(__uint_as_float(r[0]));
+            }
+          }
+        }
+      }
+      fence_async_smem();
+      tc_fence_before();
+      warp_arrive(&B.sb_full);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// Exclusive scan over segments: agg[bh][p][e] <- sum_{p' < p} agg[bh][p'][e].  grid (ceil(n / 256), B*H).
+__global__ void tc_scan_kernel(float* agg, int P, int n) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= n) return;
+  float* base = agg + (size_t)blockIdx.y * P * n + e;
+  float run = 0.f;
+  for (int p = 0; p < P; ++p) {
+    const float x = base[(size_t)p * n];
+    base[(size_t)p * n] = run;
+    run += x;
   }
 }
 
@@ -786,6 +1193,22 @@ gma_status_t tc_launch(const gma_problem_t& p, gma_op_t op, const TcPlan& pl, Tc
     return check_launch("launch tc_resp", (const void*)tc_read_kernel<false, NC>);
   }
   if (!make_map(&mq, Q, BH, p.N) || !make_map(&mk, K, BH, p.N) || !make_map(&mv, V, BH, p.N)) return GMA_ERR_CUDA;
+  if (op == GMA_OP_CAUSAL) {
+    // a5: segment aggregates; a6: exclusive scan over segments; a7: chunked sweep
+    const uint32_t smem_w = smem_bytes(write_layout(pl.Kp).total);
+    if (set_smem_optin((const void*)tc_write_kernel<false, NC>, (int)smem_w, 0) != GMA_OK) return GMA_ERR_CUDA;
+    GMA_LAUNCH("tc_causal_aggregate", (tc_write_kernel<false, NC>), dim3(pl.splits, BH), kThreadsTc, smem_w, st, mk,
+               mv, a);
+    if (gma_status_t e = check_launch("launch tc_causal_aggregate", (const void*)tc_write_kernel<false, NC>)) return e;
+    a.fault = 0;
+    const int n = pl.Kp * kStCols;
+    GMA_LAUNCH("tc_causal_scan", tc_scan_kernel, dim3(cdiv(n, 256), BH), 256, 0, st, a.state, pl.splits, n);
+    if (gma_status_t e = check_launch("launch tc_causal_scan", (const void*)tc_scan_kernel)) return e;
+    const uint32_t smem_c = smem_bytes(causal_layout(pl.Kp).total);
+    if (set_smem_optin((const void*)tc_causal_kernel<NC>, (int)smem_c, 0) != GMA_OK) return GMA_ERR_CUDA;
+    GMA_LAUNCH("tc_causal_chunk", tc_causal_kernel<NC>, dim3(pl.splits, BH), kThreadsTc, smem_c, st, mq, mk, mv, a);
+    return check_launch("launch tc_causal_chunk", (const void*)tc_causal_kernel<NC>);
+  }
   const uint32_t smem_w = smem_bytes(write_layout(pl.Kp).total);
   if (set_smem_optin((const void*)tc_write_kernel<true, NC>, (int)smem_w, 0) != GMA_OK) return GMA_ERR_CUDA;
   GMA_LAUNCH("tc_bidir_write", (tc_write_kernel<true, NC>), dim3(pl.splits, BH), kThreadsTc, smem_w, st, mk, mv, a);
@@ -804,10 +1227,6 @@ std::mutex g_fault_mu;
 
 TcPlan tc_plan(const gma_problem_t& p, gma_op_t op) {
   TcPlan t{};
-  if (op == GMA_OP_CAUSAL) {  // the causal form still runs on the CUDA-core kernels
-    t.total = simt_plan(p, op).total;
-    return t;
-  }
   const int BH = p.B * p.H;
   t.Kp = (p.K + 15) / 16 * 16;
   t.tiles = cdiv(p.N, kTile);
@@ -819,6 +1238,7 @@ TcPlan tc_plan(const gma_problem_t& p, gma_op_t op) {
   t.off_state = align_up(t.off_c + (size_t)p.H * kCTable * 4);
   size_t st = 0;
   if (op == GMA_OP_BIDIR) st = (size_t)BH * t.Kp * kStCols * 4;
+  if (op == GMA_OP_CAUSAL) st = (size_t)BH * t.splits * t.Kp * kStCols * 4;  // segment aggregates
   t.total = align_up(t.off_state + st);
   return t;
 }
@@ -826,7 +1246,6 @@ TcPlan tc_plan(const gma_problem_t& p, gma_op_t op) {
 gma_status_t tc_run(const gma_problem_t& p, gma_op_t op, const void* Q, const void* K, const void* V,
                     const float* mu, const float* sigma2, const float* log_pi, void* out, void* ws,
                     cudaStream_t st) {
-  if (op == GMA_OP_CAUSAL) return simt_run(p, op, Q, K, V, mu, sigma2, log_pi, out, ws, st);
   const TcPlan pl = tc_plan(p, op);
   const int BH = p.B * p.H;
   char* base = (char*)ws;
@@ -845,7 +1264,7 @@ gma_status_t tc_run(const gma_problem_t& p, gma_op_t op, const void* Q, const vo
   a.splits = pl.splits;
   a.eps = p.eps;
   a.wait_ns = kWaitNs;
-  {
+  if (op == GMA_OP_BIDIR) {
     std::lock_guard<std::mutex> lock(g_fault_mu);
     a.fault = g_fault_next;
     g_fault_next = 0;
