@@ -30,9 +30,9 @@ using namespace tc;
 constexpr int kTile = 128;
 constexpr int kThreadsTc = 384;  // 3 warpgroups
 constexpr int kRowWarp0 = 4;     // first row warp (warpgroups 1 and 2 are row warps)
-// Register split (setmaxnreg): launch pool 384 x 168 = 64512 >= 128 x 56 + 256 x 224 = 64512, and per SM
-// sub-partition (one control warp + two row warps) 32 x (56 + 224 + 224) = 16128 <= 16384.
-constexpr uint32_t kCtrlRegs = 56, kRowRegs = 224;
+// Register split (setmaxnreg): launch pool 384 x 168 = 64512 >= 128 x 88 + 256 x 208 = 64512, and per SM
+// sub-partition (one control warp + two row warps) 32 x (88 + 208 + 208) = 16128 <= 16384.
+constexpr uint32_t kCtrlRegs = 88, kRowRegs = 208;
 constexpr int kRowWarps = 8;  // arrival count of the barriers the row warps signal
 constexpr int kStCols = 80;  // state row: [Vt (64) | Z | 15 zero]
 constexpr int kCTable = 256;  // c' entries per head (-inf past K)
@@ -879,13 +879,19 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       if (issued[2] >= 0) wait_bounded(&B.v_full, (uint32_t)issued[2], &none, a.ctrl, 75, a.wait_ns);
     } else if (warp == 1 && lane == 0) {
       // ---------------------------------------------------------------- MMA issuer
-      const uint32_t w_addr = smem_u32(smem + L.w), gk = smem_u32(smem + L.gk), v_addr = smem_u32(smem + L.v);
-      const uint32_t sbv = smem_u32(smem + L.sbv), sbz = smem_u32(smem + L.sbz), ones = smem_u32(smem + L.ones);
-      const uint32_t id_c64 = make_idesc(128, 64, 1, 1, 0, 1);    // A tmem, B MN-major
-      const uint32_t id_c16 = make_idesc(128, 16, 1, 1, 0, 0);    // A tmem, B K-major
-      const uint32_t id_p = make_idesc(128, 128, 1, 1, 0, 0);     // P = Gq~ Gk^T
-      const uint32_t id_s64 = make_idesc(128, 64, 1, 1, 1, 1);    // A MN-major (Gamma_K^T), B MN-major (V)
-      const uint32_t id_s16 = make_idesc(128, 16, 1, 1, 1, 0);    // A MN-major, B K-major (ones)
+      const uint32_t w_addr = smem_u32(smem + L.w);
+      // base descriptors; every operand step below is a byte offset added to one of them
+      const uint64_t d_sbv = make_sdesc(smem_u32(smem + L.sbv), 16384, 1024);  // MN-major, 16 comps = 2 KB
+      const uint64_t d_sbz = make_sdesc(smem_u32(smem + L.sbz), 16, 1024);     // K-major, 16 rows
+      const uint64_t d_gk_k = make_sdesc(smem_u32(smem + L.gk), 16, 1024);     // Gamma_K as K-major B
+      const uint64_t d_gk_mn = make_sdesc(smem_u32(smem + L.gk), 16384, 1024); // Gamma_K^T as MN-major A
+      const uint64_t d_v = make_sdesc(smem_u32(smem + L.v), 16384, 1024);      // V, MN-major, N = 64
+      const uint64_t d_one = make_sdesc(smem_u32(smem + L.ones), 16, 1024);    // ones row, K-major, N = 16
+      constexpr uint32_t id_c64 = make_idesc(128, 64, 1, 1, 0, 1);    // A tmem, B MN-major
+      constexpr uint32_t id_c16 = make_idesc(128, 16, 1, 1, 0, 0);    // A tmem, B K-major
+      constexpr uint32_t id_p = make_idesc(128, 128, 1, 1, 0, 0);     // P = Gq~ Gk^T
+      constexpr uint32_t id_s64 = make_idesc(128, 64, 1, 1, 1, 1);    // A MN-major (Gamma_K^T), B MN-major (V)
+      constexpr uint32_t id_s16 = make_idesc(128, 16, 1, 1, 1, 0);    // A MN-major, B K-major (ones)
       bool ok = wait_bounded(&B.w_full, 0, &B.ab, a.ctrl, 80, a.wait_ns);
       for (int t = 0; ok && t < T; ++t) {
         const uint32_t ph = t & 1;
@@ -901,31 +907,32 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                    wait_bounded(&B.sb_full, ph, &B.ab, a.ctrl, 84, a.wait_ns)))
           break;
         tc_fence_after();
+#pragma unroll 1
         for (int ks = 0; ks < KS; ++ks) {
           const uint32_t aq = tmem + kColLog + 8 * ks;  // Gq~ (bf16 pairs) over the logit columns
-          mma_ts(tmem + kCColO, aq, make_sdesc(sbv + 2048 * ks, 16384, 1024), id_c64, ks > 0);
-          mma_ts(tmem + kCColO + 64, aq, make_sdesc(sbz + (ks >> 2) * 2048 + (ks & 3) * 32, 16, 1024), id_c16,
-                 ks > 0);
-          mma_ts(tmem + kCColP, aq, make_sdesc(gk + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024), id_p, ks > 0);
+          const uint32_t kofs = (ks >> 2) * 2048 + (ks & 3) * 32;
+          mma_ts(tmem + kCColO, aq, sdesc_add(d_sbv, 2048 * ks), id_c64, ks > 0);
+          mma_ts(tmem + kCColO + 64, aq, sdesc_add(d_sbz, kofs), id_c16, ks > 0);
+          mma_ts(tmem + kCColP, aq, sdesc_add(d_gk_k, (ks >> 2) * 16384 + (ks & 3) * 32), id_p, ks > 0);
         }
         mma_commit(&B.p_full);
         if (!(ok = wait_bounded(&B.pb_full, ph, &B.ab, a.ctrl, 85, a.wait_ns) &&
                    wait_bounded(&B.v_full, ph, &B.ab, a.ctrl, 86, a.wait_ns)))
           break;
         tc_fence_after();
-#pragma unroll
+#pragma unroll 1
         for (int s = 0; s < 8; ++s) {  // intra-tile term: O += P [V | 1]
           const uint32_t ap = tmem + kCColP + (s < 4 ? 8 * s : 64 + 8 * (s - 4));
-          mma_ts(tmem + kCColO, ap, make_sdesc(v_addr + 2048 * s, 16384, 1024), id_c64, 1u);
-          mma_ts(tmem + kCColO + 64, ap, make_sdesc(ones + (s >> 2) * 2048 + (s & 3) * 32, 16, 1024), id_c16, 1u);
+          mma_ts(tmem + kCColO, ap, sdesc_add(d_v, 2048 * s), id_c64, 1u);
+          mma_ts(tmem + kCColO + 64, ap, sdesc_add(d_one, (s >> 2) * 2048 + (s & 3) * 32), id_c16, 1u);
         }
+#pragma unroll 1
         for (int mb = 0; mb < MB; ++mb) {  // state update: S += Gamma_K^T [V | 1]
-#pragma unroll
+#pragma unroll 1
           for (int s = 0; s < 8; ++s) {
-            const uint64_t ad = make_sdesc(gk + mb * 32768 + 2048 * s, 16384, 1024);
-            mma_ss(tmem + kCColS + kStCols * mb, ad, make_sdesc(v_addr + 2048 * s, 16384, 1024), id_s64, 1u);
-            mma_ss(tmem + kCColS + kStCols * mb + 64, ad,
-                   make_sdesc(ones + (s >> 2) * 2048 + (s & 3) * 32, 16, 1024), id_s16, 1u);
+            const uint64_t ad = sdesc_add(d_gk_mn, mb * 32768 + 2048 * s);
+            mma_ss(tmem + kCColS + kStCols * mb, ad, sdesc_add(d_v, 2048 * s), id_s64, 1u);
+            mma_ss(tmem + kCColS + kStCols * mb + 64, ad, sdesc_add(d_one, (s >> 2) * 2048 + (s & 3) * 32), id_s16, 1u);
           }
         }
         mma_commit(&B.o_full);

@@ -199,6 +199,10 @@ __device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo, uin
   return d;
 }
 
+// Descriptor of the same operand `bytes` further on (the start-address field holds address >> 4 in
+// 14 bits; every shared-memory address here is below 256 KB, so the add never carries out of it).
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
+
 // Byte offset of 16-bit element (row r, column k) of a 128B-swizzled tile whose rows hold 64
 // elements per block and whose column blocks lie `block_stride` bytes apart.  Used both for
 // K-major operands (rows = M or N, columns = contraction) and for MN-major operands (rows =
