@@ -29,7 +29,6 @@ WORKLOAD = "sweep_bf16_B1H8N131072K256"
 METRIC = "GMA fwd tokens*heads/s at K=256 (bidir & causal)"
 UNIT = "tokens*heads/s"
 SWEEP = (4096, 16384, 65536, 131072)
-MUFU_EX2_PER_S = 9.58e12  # measured ex2.approx.f32 throughput on this machine's GB300 (profiles/peaks_probe.md)
 CPU_SAMPLE_N = 8192       # positions of the workload the oracle baseline processes
 
 
@@ -64,18 +63,22 @@ def load_peaks():
     return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, sm_max_mhz=2070.0, source="fallback")
 
 
+def kernel_source_hash():
+    """Hash of the tensor-core kernel sources (a traffic figure is valid only for the code it was taken on)."""
+    import hashlib
+    src = os.path.join(ROOT, "gaussian_mixture_sequence_gma_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in ("gma_tc.cu", "gma_tc_common.cuh", "gma_internal.h"):
+        h.update(open(os.path.join(src, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
 def traffic_for(name):
     """DRAM bytes per launch from the committed ncu summary, if taken on the current source."""
-    import hashlib
     p = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(p):
         return None
-    src = os.path.join(ROOT, "gaussian_mixture_sequence_gma_gb300", "csrc")
-    h = hashlib.sha256()
-    for f in sorted(os.listdir(src)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(open(os.path.join(src, f), "rb").read())
-    sha = h.hexdigest()[:16]
+    sha = kernel_source_hash()
     for line in open(p):
         parts = line.split()
         if len(parts) >= 3 and not line.startswith("#") and parts[0] == name and parts[2] == sha:
@@ -133,6 +136,23 @@ class ClockSampler:
                     reasons.add(n)
         return {"sm_mhz": float(np.median([r[1] for r in use])), "sm_max_mhz": float(max(r[2] for r in use)),
                 "reasons": sorted(reasons), "samples": len(use), "in_window": bool(inside)}
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Maximum of a per-rank float over all ranks (identity for one rank)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: int, ms_per_step_max: float, world: int) -> float:
+    """Whole-job throughput: every rank processes its own copy of the workload (weak scaling), and the
+    job's step time is the slowest rank's."""
+    return world * units_per_rank / (ms_per_step_max * 1e-3)
 
 
 def dist_setup():
@@ -209,6 +229,7 @@ def run_gma(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     peaks = load_peaks()
+    mufu_rate = gma.probe_ex2_rate(dev)
     w = workloads()[args.workload]
     B, H, N, K = w.B, w.H, w.N, w.K
     inp = make_workload(w)
@@ -241,11 +262,7 @@ def run_gma(args, world, rank, local):
         e1.record(stream)
         barrier()
         w1 = time.time()
-        ms = e0.elapsed_time(e1)
-        if world > 1:
-            x = torch.tensor([ms], device=dev)
-            dist.all_reduce(x, op=dist.ReduceOp.MAX)
-            ms = float(x.item())
+        ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
         return ms, (w0, w1)
 
     clocks = ClockSampler(local)
@@ -260,7 +277,7 @@ def run_gma(args, world, rank, local):
     clocks.mark(*win)
     ms_per_step = ms / args.steps
     units_per_step = 2 * B * H * N
-    value = world * units_per_step / (ms_per_step * 1e-3)
+    value = whole_job_rate(units_per_step, ms_per_step, world)
 
     # per-kernel durations (events on the launch stream), same step loop
     gma.profile_enable(True)
@@ -289,7 +306,7 @@ def run_gma(args, world, rank, local):
     e2e_ms, win = timed(e2e_step, args.steps)
     clocks.mark(*win)
     clk = clocks.stop()
-    e2e_value = world * units_per_step / (e2e_ms / args.steps * 1e-3)
+    e2e_value = whole_job_rate(units_per_step, e2e_ms / args.steps, world)
     h2d = sum(host[k].numel() * 2 for k in ("Q", "K", "V"))
     d2h = (hb.numel() + hc.numel()) * 2
 
@@ -318,7 +335,7 @@ def run_gma(args, world, rank, local):
 
     # whole-path roofline (spec definition): slowest of tensor, MUFU and HBM per token*head
     t_tensor = flop_per_tokhead(K) / (peaks["bf16"] * 1e12)
-    t_mufu = 2 * K / MUFU_EX2_PER_S
+    t_mufu = 2 * K / mufu_rate
     t_hbm = 4 * 64 * 2 / (peaks["hbm"] * 1e9)
     bound_rate = 1.0 / max(t_tensor, t_mufu, t_hbm)
     path = {"bound_tok_heads_per_s": bound_rate, "frac": value / world / bound_rate,
@@ -377,7 +394,7 @@ def run_gma(args, world, rank, local):
                 "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
                 "gpu_launches": int(launches), "roofline": roof, "cpu_baseline": cpu, "clocks": clk,
                 "roofline_path": path, "kernels": kernels, "sweep": sweep or None,
-                "mufu_ex2_per_s": MUFU_EX2_PER_S}
+                "mufu_ex2_per_s": mufu_rate}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()

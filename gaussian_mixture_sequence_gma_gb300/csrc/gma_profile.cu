@@ -58,6 +58,22 @@ void prof_after(cudaStream_t st, void* token) {
   if (i < g_recs.size()) cudaEventRecord(g_recs[i].stop, st);
 }
 
+// Throughput microbenchmark of ex2.approx.f32 (the exponential unit the softmax uses): 8 independent
+// chains per thread; x <- 2^-x keeps every value in (0.5, 1].
+__global__ void ex2_rate_kernel(float* sink, int iters) {
+  float x[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) x[j] = 0.05f * (threadIdx.x & 7) + 0.01f * j;
+  for (int it = 0; it < iters; ++it) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(x[j]) : "f"(-x[j]));
+  }
+  float s = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) s += x[j];
+  if (s == -1.0f) sink[0] = s;  // never true; keeps the chains live
+}
+
 }  // namespace gma
 
 using namespace gma;
@@ -67,6 +83,30 @@ extern "C" {
 unsigned long long gma_launch_count(void) { return g_launches.load(); }
 
 void gma_debug_withhold_first_load(void) { gma::tc_set_fault_injection(1u); }
+
+gma_status_t gma_probe_ex2_rate(void* stream, double* exps_per_second) {
+  if (!exps_per_second) return GMA_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return cuda_fail("probe: device attributes");
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) return cuda_fail("probe: events");
+  const int blocks = sms * 8, threads = 256, iters = 2048;
+  gma_status_t status = GMA_OK;
+  float ms = 0.f;
+  for (int rep = 0; rep < 2 && status == GMA_OK; ++rep) {  // first pass warms the clocks up
+    cudaEventRecord(e0, st);
+    ex2_rate_kernel<<<blocks, threads, 0, st>>>(nullptr, iters);
+    cudaEventRecord(e1, st);
+    if (cudaEventSynchronize(e1) != cudaSuccess || cudaEventElapsedTime(&ms, e0, e1) != cudaSuccess)
+      status = cuda_fail("probe: ex2 kernel");
+  }
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  if (status == GMA_OK) *exps_per_second = (double)blocks * threads * iters * 8 / (ms * 1e-3);
+  return status;
+}
 
 gma_status_t gma_profile_enable(int on) {
   std::lock_guard<std::mutex> lock(g_mu);

@@ -21,7 +21,7 @@ OP_RESPONSIBILITIES, OP_BIDIR, OP_CAUSAL = 0, 1, 2
 EXPORTED = ("gma_workspace_bytes", "gma_responsibilities", "gma_forward_bidir", "gma_forward_causal",
             "gma_check_device_error", "gma_status_string", "gma_version", "gma_last_error", "gma_launch_count", "gma_profile_enable",
             "gma_profile_read", "gma_forward_bidir_static_ws", "gma_static_ws_capacity",
-            "gma_debug_withhold_first_load")
+            "gma_debug_withhold_first_load", "gma_probe_ex2_rate")
 
 
 class GmaError(RuntimeError):
@@ -79,6 +79,8 @@ def lib():
     L.gma_forward_bidir_static_ws.restype = ctypes.c_int
     L.gma_static_ws_capacity.argtypes = []
     L.gma_static_ws_capacity.restype = sz
+    L.gma_probe_ex2_rate.argtypes = [vp, ctypes.POINTER(ctypes.c_double)]
+    L.gma_probe_ex2_rate.restype = ctypes.c_int
     L.gma_debug_withhold_first_load.argtypes = []
     L.gma_debug_withhold_first_load.restype = None
     L.gma_launch_count.argtypes = []
@@ -254,3 +256,14 @@ def profile_read() -> dict:
         name, cnt, ms = line.split()
         out[name] = (int(cnt), float(ms))
     return out
+
+
+def probe_ex2_rate(device=None) -> float:
+    """Exponentials per second of the GPU's ex2 unit (all SMs), measured now."""
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    out = ctypes.c_double(0.0)
+    with torch.cuda.device(dev):
+        s = lib().gma_probe_ex2_rate(_stream_handle(None, dev), ctypes.byref(out))
+    if s != GMA_OK:
+        raise GmaError(s, "gma_probe_ex2_rate")
+    return float(out.value)

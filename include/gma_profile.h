@@ -35,6 +35,13 @@ GMA_API gma_status_t gma_profile_enable(int on);
 GMA_API int gma_profile_read(char *buf, size_t len);
 
 /*
+ * Measures the throughput of the GPU's base-2 exponential instruction (ex2.approx.f32, the one the
+ * softmax over mixture components uses) with a short all-SM microbenchmark on `stream`, and writes
+ * exponentials per second to *exps_per_second.  Synchronous; allocates nothing on the device.
+ */
+GMA_API gma_status_t gma_probe_ex2_rate(void *stream, double *exps_per_second);
+
+/*
  * Test hook for the bounded device waits.  The next gma_forward_bidir call with dtype GMA_BF16
  * launches its write kernel with the first key-tile load withheld: the waits on that tile run out
  * after their limit (about one second), the kernel records the timeout in the workspace error word

@@ -1,0 +1,40 @@
+"""Bounded device waits: a withheld copy makes a wait run out; the kernel reports it and exits.
+
+The test hook (gma_debug_withhold_first_load) stops the producer of the next bidirectional write
+kernel from loading its first key tile.  The row warps waiting for that tile give up after the wait
+limit (about a second), record GMA_ERR_TIMEOUT in the workspace error word, and every CTA leaves
+through the common exit that releases its tensor memory.  Nothing traps or faults, so the context
+stays usable: the next call on the same workspace runs normally and passes parity.
+"""
+import time
+
+import numpy as np
+import pytest
+
+from gaussian_mixture_sequence_gma_gb300.inputs import make_inputs
+from oracle import oracle as orc
+from tests.helpers import TOL, rel_err, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def test_withheld_load_times_out_and_context_recovers():
+    import torch
+    from gaussian_mixture_sequence_gma_gb300 import gma
+    inp = make_inputs(1, 2, 512, 64, dtype="bf16", seed=21)
+    t = to_device(inp)
+    args = (t["Q"], t["K"], t["V"], t["mu"], t["sigma2"], t["log_pi"])
+    prob = gma.problem(1, 2, 512, 64, torch.bfloat16, 1e-6)
+    ws = gma.alloc_workspace(prob, gma.OP_BIDIR, "cuda")
+    gma.forward_bidir(*args, workspace=ws)
+    assert gma.check_device_error(ws) == gma.GMA_OK
+    gma.lib().gma_debug_withhold_first_load()
+    t0 = time.time()
+    gma.forward_bidir(*args, workspace=ws)
+    assert gma.check_device_error(ws) == gma.GMA_ERR_TIMEOUT
+    assert time.time() - t0 < 30
+    O = gma.forward_bidir(*args, workspace=ws).float().cpu().numpy()
+    assert gma.check_device_error(ws) == gma.GMA_OK
+    ref = orc.forward(inp["Q"], inp["K"], inp["V"], inp["mu"], inp["sigma2"], inp["log_pi"], 1e-6)
+    assert np.isfinite(O).all()
+    assert rel_err(O, ref) <= TOL["bf16"]
