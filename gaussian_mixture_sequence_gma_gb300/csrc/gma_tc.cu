@@ -86,7 +86,7 @@ struct Bars {
   uint64_t w_full, sb_full;
   uint64_t x_full[2], x_empty[2], v_full[2], v_empty[2];
   uint64_t ax_full, ax_empty, l_full, l_empty, g_full, g_empty, o_full, o_empty;
-  uint64_t mx, sm, done;
+  uint64_t mx, done;
   uint32_t tmem_base;
   Abort ab;
 };
@@ -193,50 +193,43 @@ __device__ __forceinline__ void zero_unused_logits(uint32_t tmem, const RowCtx& 
   tmem_st_wait();
 }
 
-// Loads this thread's NC logits (components NC*hf ...) from TMEM, adds c'_k (a 256-entry table padded
-// with -inf) in pairs, and returns the maximum.
+// Loads this thread's NC logits (components NC*hf ...) from TMEM in two batches (the bias and max of
+// the first overlap the second load), adds c'_k (a 256-entry table padded with -inf) in pairs, and
+// returns their maximum.
+template <int NC>
+__device__ __forceinline__ float bias_max(float* v, const float* cb, float m0, float m1) {
+#pragma unroll
+  for (int c4 = 0; c4 < NC / 4; ++c4) {
+    const float4 b = *reinterpret_cast<const float4*>(cb + 4 * c4);
+    add_f32x2(v[4 * c4], v[4 * c4 + 1], b.x, b.y);
+    add_f32x2(v[4 * c4 + 2], v[4 * c4 + 3], b.z, b.w);
+  }
+#pragma unroll
+  for (int i = 0; i < NC / 4; ++i) {
+    m0 = max3(m0, v[4 * i], v[4 * i + 1]);
+    m1 = max3(m1, v[4 * i + 2], v[4 * i + 3]);
+  }
+  return fmaxf(m0, m1);
+}
 template <int NC>
 __device__ __forceinline__ float load_logits(uint32_t tmem, const RowCtx& rc, const float* cs, float* v) {
   const int kbase = NC * rc.hf;
   uint32_t* r = reinterpret_cast<uint32_t*>(v);
+  constexpr int C = NC / 32, C1 = (C + 1) / 2;
+  const uint32_t ta = tmem + rc.lane_base + kColLog + kbase;
 #pragma unroll
-  for (int c = 0; c < NC / 32; ++c) tmem_ld32(tmem + rc.lane_base + kColLog + kbase + 32 * c, r + 32 * c);
-  tmem_ld_wait();
+  for (int c = 0; c < C1; ++c) tmem_ld32(ta + 32 * c, r + 32 * c);
 #pragma unroll
-  for (int c4 = 0; c4 < NC / 4; ++c4) {
-    const float4 cb = *reinterpret_cast<const float4*>(cs + kbase + 4 * c4);
-    add_f32x2(v[4 * c4], v[4 * c4 + 1], cb.x, cb.y);
-    add_f32x2(v[4 * c4 + 2], v[4 * c4 + 3], cb.z, cb.w);
+  for (int c = 0; c < C1; ++c) tmem_ld_wait_tied32(r + 32 * c);
+#pragma unroll
+  for (int c = C1; c < C; ++c) tmem_ld32(ta + 32 * c, r + 32 * c);
+  float m = bias_max<32 * C1>(v, cs + kbase, -INFINITY, -INFINITY);
+  if (C > C1) {
+#pragma unroll
+    for (int c = C1; c < C; ++c) tmem_ld_wait_tied32(r + 32 * c);
+    m = bias_max<32 * (C - C1) + (C == C1 ? 32 : 0)>(v + 32 * C1, cs + kbase + 32 * C1, m, -INFINITY);
   }
-  float m0 = v[0], m1 = v[1], m2 = v[2], m3 = v[3];
-#pragma unroll
-  for (int i = 1; i < NC / 8; ++i) {
-    m0 = max3(m0, v[8 * i], v[8 * i + 1]);
-    m1 = max3(m1, v[8 * i + 2], v[8 * i + 3]);
-    m2 = max3(m2, v[8 * i + 4], v[8 * i + 5]);
-    m3 = max3(m3, v[8 * i + 6], v[8 * i + 7]);
-  }
-  return max3(max3(m0, m1, m2), m3, max3(v[4], v[5], fmaxf(v[6], v[7])));
-}
-
-// e_k = 2^(v_k - m), packed to bf16 pairs in place: word i of v (as uint32) receives (e_2i, e_2i+1).
-// Slot i is read at step i/2 <= i before step i overwrites it.  Returns the float32 sum of the e_k.
-template <int NC>
-__device__ __forceinline__ float exp_pack(float* v, float m) {
-  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-  uint32_t* packed = reinterpret_cast<uint32_t*>(v);
-#pragma unroll
-  for (int i = 0; i < NC / 2; ++i) {
-    float t0 = v[2 * i], t1 = v[2 * i + 1];
-    add_f32x2(t0, t1, -m, -m);
-    const float e0 = ex2_approx(t0), e1 = ex2_approx(t1);
-    if (i & 1)
-      add_f32x2(s2, s3, e0, e1);
-    else
-      add_f32x2(s0, s1, e0, e1);
-    packed[i] = pack_bf16x2(e0, e1);
-  }
-  return (s0 + s1) + (s2 + s3);
+  return m;
 }
 
 // e_k = 2^(v_k - m) in place (float32); returns the sum of the e_k.
@@ -265,6 +258,28 @@ __device__ __forceinline__ void scale_pack(float* v, float r) {
   for (int i = 0; i < NC / 2; ++i) packed[i] = pack_bf16x2(v[2 * i] * r, v[2 * i + 1] * r);
 }
 
+// One softmax pass over this thread's half row, with a single exchange between the two halves:
+// each half exponentiates against its own maximum m_h, then (m_h, s_h) pairs are exchanged.
+// Returns the half's factor 2^(m_h - m) (m = row maximum) and the row sum s = sum_k 2^(v_k - m);
+// v keeps the float32 2^(v_k - m_h).
+struct RowScale {
+  float fac, sum;
+};
+template <int NC>
+__device__ __forceinline__ bool half_softmax(float* v, float mh, float2* red2, uint64_t* bar, uint32_t parity,
+                                             const RowCtx& rc, Abort* ab, Ctrl* ctrl, uint32_t site, uint64_t ns,
+                                             RowScale* out) {
+  const float sh = exp_inplace<NC>(v, mh == -INFINITY ? 0.f : mh);
+  red2[rc.hf * kTile + rc.row] = make_float2(mh, sh);
+  warp_arrive(bar);
+  if (!warp_wait(bar, parity, ab, ctrl, site, ns)) return false;
+  const float2 o = red2[(rc.hf ^ 1) * kTile + rc.row];
+  const float m = fmaxf(mh, o.x);
+  out->fac = ex2_approx(mh - m);
+  out->sum = sh * out->fac + o.y * ex2_approx(o.x - m);
+  return true;
+}
+
 // Stores this thread's NC packed bf16 values (components NC*hf ...) into the swizzled Gamma~ tile
 // (row = token; 64-component blocks 16 KB apart).  Components at or beyond Kp are skipped.
 template <int NC>
@@ -278,17 +293,6 @@ __device__ __forceinline__ void store_gamma(uint8_t* g, const RowCtx& rc, int Kp
           make_uint4(packed[4 * cj], packed[4 * cj + 1], packed[4 * cj + 2], packed[4 * cj + 3]);
     }
   }
-}
-
-// Exchange of one float per row between the two halves through smem, ordered by an mbarrier that
-// all 256 row threads arrive on.
-__device__ __forceinline__ bool exchange(float* red, uint64_t* bar, uint32_t parity, const RowCtx& rc, float mine,
-                                         float* partner, Abort* ab, Ctrl* ctrl, uint32_t site, uint64_t ns) {
-  red[rc.hf * kTile + rc.row] = mine;
-  warp_arrive(bar);
-  if (!warp_wait(bar, parity, ab, ctrl, site, ns)) return false;
-  *partner = red[(rc.hf ^ 1) * kTile + rc.row];
-  return true;
 }
 
 __device__ __forceinline__ void init_bars(Bars* B) {
@@ -309,7 +313,6 @@ __device__ __forceinline__ void init_bars(Bars* B) {
   mbar_init(&B->o_full, 1);
   mbar_init(&B->o_empty, kRowWarps);
   mbar_init(&B->mx, kRowWarps);
-  mbar_init(&B->sm, kRowWarps);
   mbar_init(&B->done, 1);
   B->ab.flag = 0;
   mbar_fence_init();
@@ -375,9 +378,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   const int T = max(0, min(a.tiles, tile0 + a.seg_tiles) - tile0);
   const int MB = (a.Kp + 127) / 128;
 
-  // zero Gamma~ (components beyond Kp stay zero: the M=128 blocks read them)
+  // zero Gamma~ (components beyond Kp stay zero: the M=128 blocks read them) and the ones atom
   for (uint32_t i = threadIdx.x; i < (uint32_t)MB * 32768 / 16; i += blockDim.x)
     reinterpret_cast<uint4*>(smem + L.g)[i] = make_uint4(0, 0, 0, 0);
+  for (uint32_t i = threadIdx.x; i < 16384 / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(smem + L.inv)[i] = make_uint4(0, 0, 0, 0);
+  __syncthreads();
+  // ones atom: element n = 64 of every token row of the MN-major [V | 1] operand is 1.0
+  if (threadIdx.x < kTile)
+    *reinterpret_cast<uint16_t*>(smem + L.inv + sw128_chunk(threadIdx.x, 0)) = 0x3F80u;
   if (threadIdx.x == 0) init_bars(&B);
   if (warp == 1) {
     tmem_alloc(&B.tmem_base, 512);
@@ -415,10 +424,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           mma_commit(&B.l_full);
           mma_commit(&B.ax_empty);
         }
-        ok = wait_bounded(&B.g_full, t & 1, &B.ab, a.ctrl, 24, a.wait_ns);
+        const int s = t & 1;
+        ok = wait_bounded(&B.g_full, t & 1, &B.ab, a.ctrl, 24, a.wait_ns) &&
+             wait_bounded(&B.v_full[s], (t >> 1) & 1, &B.ab, a.ctrl, 26, a.wait_ns);
         if (!ok) break;
         tc_fence_after();
-        const int s = t & 1;
         const uint32_t vs = v_addr + s * 16384;
         for (int mb = 0; mb < MB; ++mb) {
 #pragma unroll
@@ -441,7 +451,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     // ------------------------------------------------------------------ row warps
     const RowCtx rc = row_ctx();
     const float* cs = reinterpret_cast<const float*>(smem + L.c);
-    float* red = reinterpret_cast<float*>(smem + L.red);
+    float2* red2 = reinterpret_cast<float2*>(smem + L.red);
     zero_unused_logits<NC>(tmem, rc, a.Kp);
     bool ok = warp_wait(&B.w_full, 0, &B.ab, a.ctrl, 30, a.wait_ns);
     if (ok && T > 0) {
@@ -473,35 +483,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         tc_fence_before();
         warp_arrive(&B.ax_full);
       }
-      float mx = load_logits<NC>(tmem, rc, cs, v);
+      const float mh = load_logits<NC>(tmem, rc, cs, v);
       tc_fence_before();
       warp_arrive(&B.l_empty);
-      float other;
-      if (!(ok = exchange(red, &B.mx, t & 1, rc, mx, &other, &B.ab, a.ctrl, 35, a.wait_ns))) break;
-      mx = fmaxf(mx, other);
-      float sum = exp_pack<NC>(v, mx);
+      RowScale rs;
+      if (!(ok = half_softmax<NC>(v, mh, red2, &B.mx, t & 1, rc, &B.ab, a.ctrl, 35, a.wait_ns, &rs))) break;
+      // normalised Gamma_K row (zero past N), so the contraction takes [V | 1] as loaded
+      scale_pack<NC>(v, tok < a.N ? rs.fac / rs.sum : 0.f);
       if (t > 0 && !(ok = warp_wait(&B.g_empty, (t - 1) & 1, &B.ab, a.ctrl, 36, a.wait_ns))) break;
       store_gamma<NC>(smem + L.g, rc, a.Kp, reinterpret_cast<const uint32_t*>(v));
-      if (!(ok = exchange(red + 2 * kTile, &B.sm, t & 1, rc, sum, &other, &B.ab, a.ctrl, 37, a.wait_ns))) break;
-      const float inv = tok < a.N ? 1.0f / (sum + other) : 0.f;
-      // scale this key's [v | 1] row by 1/s (normalises its Gamma row inside the contraction)
-      if (!(ok = warp_wait(&B.v_full[s], (t >> 1) & 1, &B.ab, a.ctrl, 38, a.wait_ns))) break;
-      const __nv_bfloat162 inv2 = __float2bfloat162_rn(inv);
-      uint8_t* vrow = smem + L.v + s * 16384;
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        uint4* p = reinterpret_cast<uint4*>(vrow + sw128_chunk(rc.row, 4 * rc.hf + jj));
-        uint4 x = *p;
-        __nv_bfloat162* hx = reinterpret_cast<__nv_bfloat162*>(&x);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) hx[i] = __hmul2(hx[i], inv2);
-        *p = x;
-      }
-      if (rc.hf == 0) {
-        const uint32_t one = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(inv));
-        *reinterpret_cast<uint4*>(smem + L.inv + sw128_chunk(rc.row, 0)) = make_uint4(one, 0, 0, 0);
-        *reinterpret_cast<uint4*>(smem + L.inv + sw128_chunk(rc.row, 1)) = make_uint4(0, 0, 0, 0);
-      }
       fence_async_smem();
       warp_arrive(&B.g_full);
     }
@@ -612,7 +602,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     setmaxnreg_inc<kRowRegs>();
     const RowCtx rc = row_ctx();
     const float* cs = reinterpret_cast<const float*>(smem + L.c);
-    float* red = reinterpret_cast<float*>(smem + L.red);
+    float2* red2 = reinterpret_cast<float2*>(smem + L.red);
     zero_unused_logits<NC>(tmem, rc, a.Kp);
     const int rt = threadIdx.x - 32 * kRowWarp0;  // 0..255
     bool ok = true;
@@ -660,21 +650,20 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         tc_fence_before();
         warp_arrive(&B.ax_full);
       }
-      float mx = load_logits<NC>(tmem, rc, cs, v);
+      const float mh = load_logits<NC>(tmem, rc, cs, v);
       tc_fence_before();
       warp_arrive(&B.l_empty);
-      float other;
-      if (!(ok = exchange(red, &B.mx, t & 1, rc, mx, &other, &B.ab, a.ctrl, 55, a.wait_ns))) break;
-      mx = fmaxf(mx, other);
+      RowScale rs;
+      if (!(ok = half_softmax<NC>(v, mh, red2, &B.mx, t & 1, rc, &B.ab, a.ctrl, 55, a.wait_ns, &rs))) break;
       const int tok = (tile0 + t) * kTile + rc.row;
       if (kRead) {
-        float sum = exp_pack<NC>(v, mx);
+        // unnormalised gamma~ = 2^(v - m) on the row maximum; the read divides by (gamma~ . Z + eps s)
+        scale_pack<NC>(v, rs.fac);
+        const float sum = rs.sum;
         if (t > 0 && !(ok = warp_wait(&B.g_empty, (t - 1) & 1, &B.ab, a.ctrl, 56, a.wait_ns))) break;
         store_gamma<NC>(smem + L.g, rc, a.Kp, reinterpret_cast<const uint32_t*>(v));
         fence_async_smem();
         warp_arrive(&B.g_full);
-        if (!(ok = exchange(red + 2 * kTile, &B.sm, t & 1, rc, sum, &other, &B.ab, a.ctrl, 57, a.wait_ns))) break;
-        sum += other;
         // epilogue of the previous tile (its read contraction has had a whole tile to finish)
         if (t > 0) {
           if (!(ok = warp_wait(&B.o_full, (t - 1) & 1, &B.ab, a.ctrl, 58, a.wait_ns))) break;
@@ -700,21 +689,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         }
         s_prev = sum;
       } else {
-        // responsibilities: gamma = e / s in float32
-        float s0 = 0.f;
-#pragma unroll
-        for (int k = 0; k < NC; ++k) {
-          v[k] = ex2_approx(v[k] - mx);
-          s0 += v[k];
-        }
-        if (!(ok = exchange(red + 2 * kTile, &B.sm, t & 1, rc, s0, &other, &B.ab, a.ctrl, 59, a.wait_ns))) break;
-        const float rs = 1.0f / (s0 + other);
+        // responsibilities: gamma = 2^(v - m_h) 2^(m_h - m) / s in float32
+        const float r = rs.fac / rs.sum;
         if (tok < a.N) {
           float* dst = reinterpret_cast<float*>(a.out) + ((size_t)bh * a.N + tok) * a.K + NC * rc.hf;
           const int nk = min(max(a.K - NC * rc.hf, 0), NC);
 #pragma unroll
           for (int k = 0; k < NC; ++k)
-            if (k < nk) dst[k] = v[k] * rs;
+            if (k < nk) dst[k] = v[k] * r;
         }
       }
     }
@@ -782,7 +764,7 @@ __host__ __device__ inline CausalLayout causal_layout(int Kp) {
 struct CBars {
   uint64_t w_full, x_full[2], x_empty[2], v_full, v_empty;
   uint64_t ax_full, lk_full, gk_full, lq_full, gq_full, sb_full, p_full, pb_full, o_full, s_full;
-  uint64_t mx, sm, done;
+  uint64_t mx, done;
   uint32_t tmem_base;
   Abort ab;
 };
@@ -830,7 +812,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     mbar_init(&B.o_full, 1);
     mbar_init(&B.s_full, 1);
     mbar_init(&B.mx, kRowWarps);
-    mbar_init(&B.sm, kRowWarps);
     mbar_init(&B.done, 1);
     B.ab.flag = 0;
     mbar_fence_init();
@@ -948,7 +929,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     // ------------------------------------------------------------------ row warps
     const RowCtx rc = row_ctx();
     const float* cs = reinterpret_cast<const float*>(smem + L.c);
-    float* red = reinterpret_cast<float*>(smem + L.red);
+    float2* red2 = reinterpret_cast<float2*>(smem + L.red);
     zero_unused_logits<NC>(tmem, rc, a.Kp);
     // S <- exclusive prefix state of this segment; SB <- its bf16 copy
     if (rc.hf < MB) {
@@ -998,14 +979,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       // Gamma_K (normalised; zero rows past N) -> smem
       if (!(ok = warp_wait(&B.lk_full, ph, &B.ab, a.ctrl, 92, a.wait_ns))) break;
       tc_fence_after();
-      float mx = load_logits<NC>(tmem, rc, cs, v);
-      float other;
-      if (!(ok = exchange(red, &B.mx, 0, rc, mx, &other, &B.ab, a.ctrl, 93, a.wait_ns)))
-        break;
-      float sum = exp_inplace<NC>(v, fmaxf(mx, other));
-      if (!(ok = exchange(red + 2 * kTile, &B.sm, 0, rc, sum, &other, &B.ab, a.ctrl, 94, a.wait_ns)))
-        break;
-      scale_pack<NC>(v, tok < a.N ? 1.0f / (sum + other) : 0.f);
+      float mh = load_logits<NC>(tmem, rc, cs, v);
+      RowScale rs;
+      if (!(ok = half_softmax<NC>(v, mh, red2, &B.mx, 0, rc, &B.ab, a.ctrl, 93, a.wait_ns, &rs))) break;
+      scale_pack<NC>(v, tok < a.N ? rs.fac / rs.sum : 0.f);
       store_gamma<NC>(smem + L.gk, rc, a.Kp, reinterpret_cast<const uint32_t*>(v));
       // query operand
       if (!(ok = warp_wait(&B.x_full[1], ph, &B.ab, a.ctrl, 95, a.wait_ns))) break;
@@ -1018,16 +995,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       // Gamma_Q~ (unnormalised) -> TMEM over its own logit columns
       if (!(ok = warp_wait(&B.lq_full, ph, &B.ab, a.ctrl, 96, a.wait_ns))) break;
       tc_fence_after();
-      mx = load_logits<NC>(tmem, rc, cs, v);
-      if (!(ok = exchange(red, &B.mx, 1, rc, mx, &other, &B.ab, a.ctrl, 97, a.wait_ns)))
-        break;
-      sum = exp_pack<NC>(v, fmaxf(mx, other));
+      mh = load_logits<NC>(tmem, rc, cs, v);
+      if (!(ok = half_softmax<NC>(v, mh, red2, &B.mx, 1, rc, &B.ab, a.ctrl, 97, a.wait_ns, &rs))) break;
+      scale_pack<NC>(v, rs.fac);
 #pragma unroll
       for (int c = 0; c < NC / 32; ++c)
         tmem_st16(tmem + rc.lane_base + kColLog + (NC / 2) * rc.hf + 16 * c, reinterpret_cast<uint32_t*>(v) + 16 * c);
-      if (!(ok = exchange(red + 2 * kTile, &B.sm, 1, rc, sum, &other, &B.ab, a.ctrl, 98, a.wait_ns)))
-        break;
-      const float s_q = sum + other;
+      const float s_q = rs.sum;
       tmem_st_wait();
       tc_fence_before();
       warp_arrive(&B.gq_full);
