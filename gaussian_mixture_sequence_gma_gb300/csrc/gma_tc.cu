@@ -763,7 +763,7 @@ __host__ __device__ inline CausalLayout causal_layout(int Kp) {
 
 struct CBars {
   uint64_t w_full, x_full[2], x_empty[2], v_full, v_empty;
-  uint64_t ax_full, lk_full, gk_full, lq_full, gq_full, sb_full, p_full, pb_full, o_full, s_full;
+  uint64_t ax_full, lk_full, lq_go, gk_full, lq_full, gq_full, sb_full, p_full, pb_full, o_full, s_full;
   uint64_t mx, done;
   uint32_t tmem_base;
   Abort ab;
@@ -803,6 +803,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     mbar_init(&B.v_empty, 1);
     mbar_init(&B.ax_full, kRowWarps);
     mbar_init(&B.lk_full, 1);
+    mbar_init(&B.lq_go, kRowWarps);
     mbar_init(&B.gk_full, kRowWarps);
     mbar_init(&B.lq_full, 1);
     mbar_init(&B.gq_full, kRowWarps);
@@ -876,17 +877,34 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       bool ok = wait_bounded(&B.w_full, 0, &B.ab, a.ctrl, 80, a.wait_ns);
       for (int t = 0; ok && t < T; ++t) {
         const uint32_t ph = t & 1;
+        // key logits
         if (!(ok = wait_bounded(&B.ax_full, ph, &B.ab, a.ctrl, 81, a.wait_ns))) break;
         tc_fence_after();
         issue_logits(tmem, w_addr, a.Kp, kCColO);
         mma_commit(&B.lk_full);
-        if (!(ok = wait_bounded(&B.gk_full, ph, &B.ab, a.ctrl, 82, a.wait_ns))) break;
+        // query logits, as soon as the key logits are in registers and the query operand is built
+        if (!(ok = wait_bounded(&B.lq_go, ph, &B.ab, a.ctrl, 82, a.wait_ns))) break;
         tc_fence_after();
         issue_logits(tmem, w_addr, a.Kp, kCColO);
         mma_commit(&B.lq_full);
-        if (!(ok = wait_bounded(&B.gq_full, ph, &B.ab, a.ctrl, 83, a.wait_ns) &&
-                   wait_bounded(&B.sb_full, ph, &B.ab, a.ctrl, 84, a.wait_ns)))
+        // state update S += Gamma_K^T [V | 1]: needs Gamma_K, V, and the bf16 snapshot of S_prev taken
+        if (!(ok = wait_bounded(&B.gk_full, ph, &B.ab, a.ctrl, 83, a.wait_ns) &&
+                   wait_bounded(&B.v_full, ph, &B.ab, a.ctrl, 84, a.wait_ns) &&
+                   wait_bounded(&B.sb_full, ph, &B.ab, a.ctrl, 85, a.wait_ns)))
           break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int mb = 0; mb < MB; ++mb) {
+#pragma unroll 1
+          for (int s = 0; s < 8; ++s) {
+            const uint64_t ad = sdesc_add(d_gk_mn, mb * 32768 + 2048 * s);
+            mma_ss(tmem + kCColS + kStCols * mb, ad, sdesc_add(d_v, 2048 * s), id_s64, 1u);
+            mma_ss(tmem + kCColS + kStCols * mb + 64, ad, sdesc_add(d_one, (s >> 2) * 2048 + (s & 3) * 32), id_s16, 1u);
+          }
+        }
+        mma_commit(&B.s_full);
+        // inter-tile term O = Gq~ S_prev and intra-tile affinity P = Gq~ Gk^T
+        if (!(ok = wait_bounded(&B.gq_full, ph, &B.ab, a.ctrl, 86, a.wait_ns))) break;
         tc_fence_after();
 #pragma unroll 1
         for (int ks = 0; ks < KS; ++ks) {
@@ -897,27 +915,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           mma_ts(tmem + kCColP, aq, sdesc_add(d_gk_k, (ks >> 2) * 16384 + (ks & 3) * 32), id_p, ks > 0);
         }
         mma_commit(&B.p_full);
-        if (!(ok = wait_bounded(&B.pb_full, ph, &B.ab, a.ctrl, 85, a.wait_ns) &&
-                   wait_bounded(&B.v_full, ph, &B.ab, a.ctrl, 86, a.wait_ns)))
-          break;
+        // intra-tile term O += P [V | 1]
+        if (!(ok = wait_bounded(&B.pb_full, ph, &B.ab, a.ctrl, 88, a.wait_ns))) break;
         tc_fence_after();
 #pragma unroll 1
-        for (int s = 0; s < 8; ++s) {  // intra-tile term: O += P [V | 1]
+        for (int s = 0; s < 8; ++s) {
           const uint32_t ap = tmem + kCColP + (s < 4 ? 8 * s : 64 + 8 * (s - 4));
           mma_ts(tmem + kCColO, ap, sdesc_add(d_v, 2048 * s), id_c64, 1u);
           mma_ts(tmem + kCColO + 64, ap, sdesc_add(d_one, (s >> 2) * 2048 + (s & 3) * 32), id_c16, 1u);
         }
-#pragma unroll 1
-        for (int mb = 0; mb < MB; ++mb) {  // state update: S += Gamma_K^T [V | 1]
-#pragma unroll 1
-          for (int s = 0; s < 8; ++s) {
-            const uint64_t ad = sdesc_add(d_gk_mn, mb * 32768 + 2048 * s);
-            mma_ss(tmem + kCColS + kStCols * mb, ad, sdesc_add(d_v, 2048 * s), id_s64, 1u);
-            mma_ss(tmem + kCColS + kStCols * mb + 64, ad, sdesc_add(d_one, (s >> 2) * 2048 + (s & 3) * 32), id_s16, 1u);
-          }
-        }
         mma_commit(&B.o_full);
-        mma_commit(&B.s_full);
         mma_commit(&B.v_empty);
       }
       mma_commit(&B.done);
@@ -969,28 +976,29 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     for (int t = 0; ok && t < T; ++t) {
       const uint32_t ph = t & 1;
       const int tok = (tile0 + t) * kTile + rc.row;
-      // key operand
+      // key operand (the [x^2 | x] columns double as the output accumulator, free since the last epilogue)
       if (!(ok = warp_wait(&B.x_full[0], ph, &B.ab, a.ctrl, 91, a.wait_ns))) break;
       transform_row(smem + L.x, rc, tmem, kCColO);
       warp_arrive(&B.x_empty[0]);
       tmem_st_wait();
       tc_fence_before();
       warp_arrive(&B.ax_full);
-      // Gamma_K (normalised; zero rows past N) -> smem
+      // key logits -> registers; build the query operand first so its contraction starts at once
       if (!(ok = warp_wait(&B.lk_full, ph, &B.ab, a.ctrl, 92, a.wait_ns))) break;
       tc_fence_after();
+      if (!(ok = warp_wait(&B.x_full[1], ph, &B.ab, a.ctrl, 95, a.wait_ns))) break;
+      transform_row(smem + L.x + 16384, rc, tmem, kCColO);
+      warp_arrive(&B.x_empty[1]);
       float mh = load_logits<NC>(tmem, rc, cs, v);
+      tmem_st_wait();
+      tc_fence_before();
+      warp_arrive(&B.lq_go);
+      // Gamma_K (normalised; zero rows past N) -> smem
       RowScale rs;
       if (!(ok = half_softmax<NC>(v, mh, red2, &B.mx, 0, rc, &B.ab, a.ctrl, 93, a.wait_ns, &rs))) break;
       scale_pack<NC>(v, tok < a.N ? rs.fac / rs.sum : 0.f);
       store_gamma<NC>(smem + L.gk, rc, a.Kp, reinterpret_cast<const uint32_t*>(v));
-      // query operand
-      if (!(ok = warp_wait(&B.x_full[1], ph, &B.ab, a.ctrl, 95, a.wait_ns))) break;
-      transform_row(smem + L.x + 16384, rc, tmem, kCColO);
-      warp_arrive(&B.x_empty[1]);
-      tmem_st_wait();
       fence_async_smem();
-      tc_fence_before();
       warp_arrive(&B.gk_full);
       // Gamma_Q~ (unnormalised) -> TMEM over its own logit columns
       if (!(ok = warp_wait(&B.lq_full, ph, &B.ab, a.ctrl, 96, a.wait_ns))) break;
@@ -1027,35 +1035,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       }
       tc_fence_before();
       warp_arrive(&B.pb_full);
-      // output: this thread's output dims are 16*hf + [0,16) and 32 + 16*hf + [0,16) -- the same columns it
-      // overwrites with the next key operand, so no other warp reads them afterwards
-      if (!(ok = warp_wait(&B.o_full, ph, &B.ab, a.ctrl, 100, a.wait_ns))) break;
-      tc_fence_after();
-      {
-        uint32_t o0[16], o1[16], zc[16];
-        tmem_ld16(tmem + rc.lane_base + kCColO + 16 * rc.hf, o0);
-        tmem_ld16(tmem + rc.lane_base + kCColO + 32 + 16 * rc.hf, o1);
-        tmem_ld16(tmem + rc.lane_base + kCColO + 64, zc);
-        tmem_ld_wait();
-        const float rden = 1.0f / (__uint_as_float(zc[0]) + a.eps * s_q);
-        if (tok < a.N) {
-          __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.out) + ((size_t)bh * a.N + tok) * kDv;
-          uint4* d0 = reinterpret_cast<uint4*>(orow + 16 * rc.hf);
-          uint4* d1 = reinterpret_cast<uint4*>(orow + 32 + 16 * rc.hf);
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            d0[c] = make_uint4(pack_bf16x2(__uint_as_float(o0[8 * c]) * rden, __uint_as_float(o0[8 * c + 1]) * rden),
-                               pack_bf16x2(__uint_as_float(o0[8 * c + 2]) * rden, __uint_as_float(o0[8 * c + 3]) * rden),
-                               pack_bf16x2(__uint_as_float(o0[8 * c + 4]) * rden, __uint_as_float(o0[8 * c + 5]) * rden),
-                               pack_bf16x2(__uint_as_float(o0[8 * c + 6]) * rden, __uint_as_float(o0[8 * c + 7]) * rden));
-            d1[c] = make_uint4(pack_bf16x2(__uint_as_float(o1[8 * c]) * rden, __uint_as_float(o1[8 * c + 1]) * rden),
-                               pack_bf16x2(__uint_as_float(o1[8 * c + 2]) * rden, __uint_as_float(o1[8 * c + 3]) * rden),
-                               pack_bf16x2(__uint_as_float(o1[8 * c + 4]) * rden, __uint_as_float(o1[8 * c + 5]) * rden),
-                               pack_bf16x2(__uint_as_float(o1[8 * c + 6]) * rden, __uint_as_float(o1[8 * c + 7]) * rden));
-          }
-        }
-      }
-      // bf16 copy of the updated state for the next tile's inter-tile term
+      // the inter-tile term has read S_prev; snapshot the updated state for the next tile
       if (!(ok = warp_wait(&B.s_full, ph, &B.ab, a.ctrl, 101, a.wait_ns))) break;
       tc_fence_after();
       if (rc.hf < MB) {
@@ -1087,6 +1067,34 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       fence_async_smem();
       tc_fence_before();
       warp_arrive(&B.sb_full);
+      // output: this thread's output dims are 16*hf + [0,16) and 32 + 16*hf + [0,16) -- the same columns it
+      // overwrites with the next key operand, so no other warp reads them afterwards
+      if (!(ok = warp_wait(&B.o_full, ph, &B.ab, a.ctrl, 100, a.wait_ns))) break;
+      tc_fence_after();
+      {
+        uint32_t o0[16], o1[16], zc[16];
+        tmem_ld16(tmem + rc.lane_base + kCColO + 16 * rc.hf, o0);
+        tmem_ld16(tmem + rc.lane_base + kCColO + 32 + 16 * rc.hf, o1);
+        tmem_ld16(tmem + rc.lane_base + kCColO + 64, zc);
+        tmem_ld_wait();
+        const float rden = 1.0f / (__uint_as_float(zc[0]) + a.eps * s_q);
+        if (tok < a.N) {
+          __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.out) + ((size_t)bh * a.N + tok) * kDv;
+          uint4* d0 = reinterpret_cast<uint4*>(orow + 16 * rc.hf);
+          uint4* d1 = reinterpret_cast<uint4*>(orow + 32 + 16 * rc.hf);
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            d0[c] = make_uint4(pack_bf16x2(__uint_as_float(o0[8 * c]) * rden, __uint_as_float(o0[8 * c + 1]) * rden),
+                               pack_bf16x2(__uint_as_float(o0[8 * c + 2]) * rden, __uint_as_float(o0[8 * c + 3]) * rden),
+                               pack_bf16x2(__uint_as_float(o0[8 * c + 4]) * rden, __uint_as_float(o0[8 * c + 5]) * rden),
+                               pack_bf16x2(__uint_as_float(o0[8 * c + 6]) * rden, __uint_as_float(o0[8 * c + 7]) * rden));
+            d1[c] = make_uint4(pack_bf16x2(__uint_as_float(o1[8 * c]) * rden, __uint_as_float(o1[8 * c + 1]) * rden),
+                               pack_bf16x2(__uint_as_float(o1[8 * c + 2]) * rden, __uint_as_float(o1[8 * c + 3]) * rden),
+                               pack_bf16x2(__uint_as_float(o1[8 * c + 4]) * rden, __uint_as_float(o1[8 * c + 5]) * rden),
+                               pack_bf16x2(__uint_as_float(o1[8 * c + 6]) * rden, __uint_as_float(o1[8 * c + 7]) * rden));
+          }
+        }
+      }
     }
   }
   tc_fence_before();
