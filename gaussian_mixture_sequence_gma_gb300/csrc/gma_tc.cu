@@ -9,14 +9,16 @@
 //     added in float32, followed by a base-2 softmax over k held in registers.
 //   "Core mechanism" item 2: write  [Vt | Z] = Gamma_K^T [V | 1]   (bf16 operands, fp32 TMEM accumulator)
 //                            read   O = Gamma_Q Vt / (Gamma_Q Z + eps)
-//   Rows of Gamma_K are normalised by scaling the [V | 1] row of each key by 1/s_j (s_j = row sum of
-//   the unnormalised exponentials); Gamma_Q stays unnormalised and the read divides by
-//   (gamma~ . Z + eps * s_i), which is the same quotient.
+//   Gamma_K is stored unnormalised (row maximum 1) and each key's row is normalised inside the
+//   contraction by scaling its [V | 1] row by 1/s_j (s_j = row sum of the exponentials).  Gamma_Q stays
+//   unnormalised as well: the read divides by gamma~_i . (Z + eps) = gamma~_i . Z + eps s_i, which is the
+//   same quotient, with eps added once to the Z column of the state operand, so no query row needs
+//   its sum.
 //
-// Roles per CTA (384 threads = 3 warpgroups): warp 0 = TMA producer, warp 1 = MMA issuer (one thread)
-// and TMEM owner, warps 2-3 idle; warpgroups 1-2 (warps 4..11) = row warps: thread (q, half) owns token
-// row 32q+lane of the tile and half of its components / dimensions (TMEM lane quarter q = warp % 4).
-// The control warpgroup hands registers to the row warpgroups with setmaxnreg.
+// Roles per CTA (640 threads = 5 warpgroups): warp 0 = TMA producer, warp 1 = MMA issuer (one thread)
+// and TMEM owner, warps 2-3 idle; warpgroups 1-4 (warps 4..19) = row warps: thread (q, part) owns token
+// row 32q+lane of the tile and a quarter of its components / dimensions (TMEM lane quarter q = warp % 4,
+// part = warpgroup - 1).  The control warpgroup hands registers to the row warpgroups with setmaxnreg.
 #include <cstdio>
 #include <mutex>
 
@@ -28,12 +30,13 @@ namespace {
 using namespace tc;
 
 constexpr int kTile = 128;
-constexpr int kThreadsTc = 384;  // 3 warpgroups
-constexpr int kRowWarp0 = 4;     // first row warp (warpgroups 1 and 2 are row warps)
-// Register split (setmaxnreg): launch pool 384 x 168 = 64512 >= 128 x 88 + 256 x 208 = 64512, and per SM
-// sub-partition (one control warp + two row warps) 32 x (88 + 208 + 208) = 16128 <= 16384.
-constexpr uint32_t kCtrlRegs = 88, kRowRegs = 208;
-constexpr int kRowWarps = 8;  // arrival count of the barriers the row warps signal
+constexpr int kThreadsTc = 640;  // 5 warpgroups
+constexpr int kRowWarp0 = 4;     // first row warp (warpgroups 1..4 are row warps)
+constexpr int kParts = 4;        // row threads sharing one token row
+// Register split (setmaxnreg): launch pool 640 x 96 = 61440 >= 128 x 56 + 512 x 104 = 60416, and per SM
+// sub-partition (one control warp + four row warps) 32 x (56 + 4 x 104) = 15104 <= 16384.
+constexpr uint32_t kCtrlRegs = 56, kRowRegs = 104;
+constexpr int kRowWarps = 16;  // arrival count of the barriers the row warps signal
 constexpr int kStCols = 80;  // state row: [Vt (64) | Z | 15 zero]
 constexpr int kCTable = 256;  // c' entries per head (-inf past K)
 constexpr int kTargetCtas = 152;
@@ -63,7 +66,7 @@ __host__ __device__ inline SmemLayout write_layout(int Kp) {
   s.sb = s.inv + 16384;
   s.c = s.sb;
   s.red = s.c + 1024;
-  s.total = s.red + 4 * kTile * 4;
+  s.total = s.red + kParts * kTile * 8;
   return s;
 }
 // read / responsibilities kernel: W | G (K-major Gamma~, ceil(Kp/64) x 16K) | X ring | SB (state operand) | c' | exchange
@@ -78,15 +81,15 @@ __host__ __device__ inline SmemLayout read_layout(int Kp) {
   s.sb = s.x + 2 * 16384;
   s.c = s.sb + KB * (kStCols * 128);
   s.red = s.c + 1024;
-  s.total = s.red + 4 * kTile * 4;
+  s.total = s.red + kParts * kTile * 8;
   return s;
 }
 
 struct Bars {
   uint64_t w_full, sb_full;
   uint64_t x_full[2], x_empty[2], v_full[2], v_empty[2];
-  uint64_t ax_full, ax_empty, l_full, l_empty, g_full, g_empty, o_full, o_empty;
-  uint64_t mx, done;
+  uint64_t ax_full, l_full, l_empty, g_full, g_empty, o_full, o_empty;
+  uint64_t done;
   uint32_t tmem_base;
   Abort ab;
 };
@@ -144,30 +147,60 @@ __global__ void __launch_bounds__(128) tc_prep_kernel(const float* __restrict__ 
 }
 
 // ----------------------------------------------------------------------------------------------- shared pieces
+// Row-thread context.  Shared-memory positions are 32-bit shared-window addresses; every 128-row SW128
+// tile starts on a 1 KB boundary, so chunk c of a token row sits at (tile + rowsw) ^ (c << 4).
 struct RowCtx {
-  int warp, lane, q, hf, row;  // row warps: q = TMEM lane quarter, hf = component / dimension half
-  uint32_t lane_base;          // TMEM address bits of this warp's lane quarter
+  int warp, lane, q, part, row;  // row warps: q = TMEM lane quarter, part = component / dimension quarter
+  uint32_t lane_base;            // TMEM address bits of this warp's lane quarter
+  uint32_t rowsw;                // offset of chunk 0 of this token row in a 128-row SW128 tile
+  uint32_t rowq;                 // offset of chunk 2 * part (this thread's 16 of the row's 64 elements)
+  uint32_t red;                  // this row's slots in the exchange area (float2 [kParts][kTile])
+  uint32_t bar;                  // named barrier of the row's four part threads (the warps of quarter q)
 };
 
-__device__ __forceinline__ RowCtx row_ctx() {
+__device__ __forceinline__ RowCtx row_ctx(uint32_t red_area) {
   RowCtx r;
   r.warp = threadIdx.x >> 5;
   r.lane = threadIdx.x & 31;
   r.q = r.warp & 3;
-  r.hf = (r.warp - kRowWarp0) >> 2;
+  r.part = (r.warp - kRowWarp0) >> 2;
   r.row = r.q * 32 + r.lane;
   r.lane_base = (uint32_t)(r.q * 32) << 16;
+  r.rowsw = (uint32_t)(r.row >> 3) * 1024u + (uint32_t)(r.row & 7) * 128u + ((uint32_t)(r.row & 7) << 4);
+  r.rowq = r.rowsw ^ ((uint32_t)(2 * r.part) << 4);
+  r.red = red_area + (uint32_t)r.row * 8u;
+  r.bar = 1u + (uint32_t)r.q;
   return r;
 }
 
-// Builds this thread's half of the [x^2 | x] fp16 operand row from the bf16 X tile and stores it to
-// TMEM (A operand of the log-density contraction, lane = token, two fp16 per 32-bit column).
-__device__ __forceinline__ void transform_row(const uint8_t* xs, const RowCtx& rc, uint32_t tmem,
+// Row exchanges among the four part threads of a token row (the same lane of the four warps of one
+// lane quarter, so one named barrier of 128 threads).  `slot` 0 / 4 selects the .x / .y float of the
+// row's float2 slots.  Named barriers have no time limit, so every row warp executes every exchange of
+// every tile, also after a failed wait; the caller only skips the work around them.
+__device__ __forceinline__ float xchg_max(const RowCtx& rc, uint32_t slot, float mp) {
+  sts32(rc.red + (uint32_t)rc.part * (kTile * 8) + slot, mp);
+  named_bar_sync(rc.bar, 128);
+  const float a = lds32(rc.red + slot), b = lds32(rc.red + kTile * 8 + slot);
+  const float c = lds32(rc.red + 2 * kTile * 8 + slot), d = lds32(rc.red + 3 * kTile * 8 + slot);
+  return fmaxf(fmaxf(a, b), fmaxf(c, d));
+}
+__device__ __forceinline__ float xchg_sum(const RowCtx& rc, uint32_t slot, float sp) {
+  sts32(rc.red + (uint32_t)rc.part * (kTile * 8) + slot, sp);
+  named_bar_sync(rc.bar, 128);
+  const float a = lds32(rc.red + slot), b = lds32(rc.red + kTile * 8 + slot);
+  const float c = lds32(rc.red + 2 * kTile * 8 + slot), d = lds32(rc.red + 3 * kTile * 8 + slot);
+  return (a + b) + (c + d);
+}
+
+// Builds this thread's quarter (16 dims) of the [x^2 | x] fp16 operand row from the bf16 X tile at shared
+// address `xtile` and stores it to TMEM (A operand of the log-density contraction, lane = token, two
+// fp16 per 32-bit column).
+__device__ __forceinline__ void transform_row(uint32_t xtile, const RowCtx& rc, uint32_t tmem,
                                               uint32_t col_ax = kColAx) {
-  uint32_t sq[16], lin[16];
+  uint32_t sq[8], lin[8];
 #pragma unroll
-  for (int jj = 0; jj < 4; ++jj) {
-    const uint4 v = *reinterpret_cast<const uint4*>(xs + sw128_chunk(rc.row, 4 * rc.hf + jj));
+  for (int jj = 0; jj < 2; ++jj) {
+    const uint4 v = lds128((xtile + rc.rowq) ^ (uint32_t)(jj << 4));
     const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -176,8 +209,8 @@ __device__ __forceinline__ void transform_row(const uint8_t* xs, const RowCtx& r
       sq[jj * 4 + i] = pack_f16x2(lo * lo, hi * hi);
     }
   }
-  tmem_st16(tmem + rc.lane_base + col_ax + 16 * rc.hf, sq);
-  tmem_st16(tmem + rc.lane_base + col_ax + 32 + 16 * rc.hf, lin);
+  tmem_st8(tmem + rc.lane_base + col_ax + 8 * rc.part, sq);
+  tmem_st8(tmem + rc.lane_base + col_ax + 32 + 8 * rc.part, lin);
 }
 
 // Zeroes this thread's logit columns at or beyond Kp once per CTA: the contraction (N = Kp) never
@@ -189,20 +222,18 @@ __device__ __forceinline__ void zero_unused_logits(uint32_t tmem, const RowCtx& 
   for (int i = 0; i < 16; ++i) z[i] = 0u;
 #pragma unroll
   for (int c = 0; c < NC / 16; ++c)
-    if (NC * rc.hf + 16 * c >= Kp) tmem_st16(tmem + rc.lane_base + kColLog + NC * rc.hf + 16 * c, z);
+    if (NC * rc.part + 16 * c >= Kp) tmem_st16(tmem + rc.lane_base + kColLog + NC * rc.part + 16 * c, z);
   tmem_st_wait();
 }
 
-// Loads this thread's NC logits (components NC*hf ...) from TMEM in two batches (the bias and max of
-// the first overlap the second load), adds c'_k (a 256-entry table padded with -inf) in pairs, and
-// returns their maximum.
+// Adds c'_k (shared address cb, float32) to NC logits in pairs and returns their maximum.
 template <int NC>
-__device__ __forceinline__ float bias_max(float* v, const float* cb, float m0, float m1) {
+__device__ __forceinline__ float bias_max(float* v, uint32_t cb, float m0, float m1) {
 #pragma unroll
   for (int c4 = 0; c4 < NC / 4; ++c4) {
-    const float4 b = *reinterpret_cast<const float4*>(cb + 4 * c4);
-    add_f32x2(v[4 * c4], v[4 * c4 + 1], b.x, b.y);
-    add_f32x2(v[4 * c4 + 2], v[4 * c4 + 3], b.z, b.w);
+    const uint4 b = lds128(cb + 16 * c4);
+    add_f32x2(v[4 * c4], v[4 * c4 + 1], __uint_as_float(b.x), __uint_as_float(b.y));
+    add_f32x2(v[4 * c4 + 2], v[4 * c4 + 3], __uint_as_float(b.z), __uint_as_float(b.w));
   }
 #pragma unroll
   for (int i = 0; i < NC / 4; ++i) {
@@ -211,23 +242,26 @@ __device__ __forceinline__ float bias_max(float* v, const float* cb, float m0, f
   }
   return fmaxf(m0, m1);
 }
+// Loads this thread's NC logits (components NC*part ...) from TMEM in two batches (the bias and max of
+// the first overlap the second load), adds c'_k from the 256-entry table at shared address cs (-inf past
+// K), and returns the part's maximum.
 template <int NC>
-__device__ __forceinline__ float load_logits(uint32_t tmem, const RowCtx& rc, const float* cs, float* v) {
-  const int kbase = NC * rc.hf;
+__device__ __forceinline__ float load_logits(uint32_t tmem, const RowCtx& rc, uint32_t cs, float* v) {
+  const int kbase = NC * rc.part;
   uint32_t* r = reinterpret_cast<uint32_t*>(v);
-  constexpr int C = NC / 32, C1 = (C + 1) / 2;
+  constexpr int C = NC / 16, C1 = (C + 1) / 2;  // 16-column chunks; first batch
   const uint32_t ta = tmem + rc.lane_base + kColLog + kbase;
 #pragma unroll
-  for (int c = 0; c < C1; ++c) tmem_ld32(ta + 32 * c, r + 32 * c);
+  for (int c = 0; c < C1; ++c) tmem_ld16(ta + 16 * c, r + 16 * c);
 #pragma unroll
-  for (int c = 0; c < C1; ++c) tmem_ld_wait_tied32(r + 32 * c);
+  for (int c = 0; c < C1; ++c) tmem_ld_wait_tied16(r + 16 * c);
 #pragma unroll
-  for (int c = C1; c < C; ++c) tmem_ld32(ta + 32 * c, r + 32 * c);
-  float m = bias_max<32 * C1>(v, cs + kbase, -INFINITY, -INFINITY);
+  for (int c = C1; c < C; ++c) tmem_ld16(ta + 16 * c, r + 16 * c);
+  float m = bias_max<16 * C1>(v, cs + 4 * kbase, -INFINITY, -INFINITY);
   if (C > C1) {
 #pragma unroll
-    for (int c = C1; c < C; ++c) tmem_ld_wait_tied32(r + 32 * c);
-    m = bias_max<32 * (C - C1) + (C == C1 ? 32 : 0)>(v + 32 * C1, cs + kbase + 32 * C1, m, -INFINITY);
+    for (int c = C1; c < C; ++c) tmem_ld_wait_tied16(r + 16 * c);
+    m = bias_max<(C > C1 ? 16 * (C - C1) : 16)>(v + 16 * C1, cs + 4 * (kbase + 16 * C1), m, -INFINITY);
   }
   return m;
 }
@@ -250,49 +284,80 @@ __device__ __forceinline__ float exp_inplace(float* v, float m) {
   return (s0 + s1) + (s2 + s3);
 }
 
-// v_k * r packed to bf16 pairs in place (word i of v receives (v_2i r, v_2i+1 r)).
+// Shared address of this thread's first 16-byte chunk (components NC*part .. +8) in a Gamma~ tile of
+// 64-component SW128 blocks 16 KB apart; its chunk cj is at the returned address ^ (cj << 4) (the
+// thread's NC components never cross a block, and the chunk index of NC*part has no bit in common
+// with cj < NC/8).
 template <int NC>
-__device__ __forceinline__ void scale_pack(float* v, float r) {
-  uint32_t* packed = reinterpret_cast<uint32_t*>(v);
-#pragma unroll
-  for (int i = 0; i < NC / 2; ++i) packed[i] = pack_bf16x2(v[2 * i] * r, v[2 * i + 1] * r);
+__device__ __forceinline__ uint32_t gamma_row_addr(uint32_t gtile, const RowCtx& rc) {
+  const uint32_t c0 = (uint32_t)NC * rc.part;
+  return gtile + (c0 >> 6) * 16384u + (rc.rowsw ^ (((c0 & 63u) >> 3) << 4));
 }
 
-// One softmax pass over this thread's half row, with a single exchange between the two halves:
-// each half exponentiates against its own maximum m_h, then (m_h, s_h) pairs are exchanged.
-// Returns the half's factor 2^(m_h - m) (m = row maximum) and the row sum s = sum_k 2^(v_k - m);
-// v keeps the float32 2^(v_k - m_h).
-struct RowScale {
-  float fac, sum;
-};
-template <int NC>
-__device__ __forceinline__ bool half_softmax(float* v, float mh, float2* red2, uint64_t* bar, uint32_t parity,
-                                             const RowCtx& rc, Abort* ab, Ctrl* ctrl, uint32_t site, uint64_t ns,
-                                             RowScale* out) {
-  const float sh = exp_inplace<NC>(v, mh == -INFINITY ? 0.f : mh);
-  red2[rc.hf * kTile + rc.row] = make_float2(mh, sh);
-  warp_arrive(bar);
-  if (!warp_wait(bar, parity, ab, ctrl, site, ns)) return false;
-  const float2 o = red2[(rc.hf ^ 1) * kTile + rc.row];
-  const float m = fmaxf(mh, o.x);
-  out->fac = ex2_approx(mh - m);
-  out->sum = sh * out->fac + o.y * ex2_approx(o.x - m);
-  return true;
-}
-
-// Stores this thread's NC packed bf16 values (components NC*hf ...) into the swizzled Gamma~ tile
-// (row = token; 64-component blocks 16 KB apart).  Components at or beyond Kp are skipped.
-template <int NC>
-__device__ __forceinline__ void store_gamma(uint8_t* g, const RowCtx& rc, int Kp, const uint32_t* packed) {
+// One fused pass over this thread's NC logits with the row maximum m known: e = 2^(v - m) packed to
+// bf16 and stored as 16-byte chunks of 8 components at ga (gamma_row_addr), so the exponentials, the
+// float pipes and the shared-memory stores overlap across chunks.  Chunks at or beyond Kp are not
+// stored.  With kSum, returns the float32 sum of the e (else 0).
+template <int NC, bool kSum>
+__device__ __forceinline__ float exp_pack_store(const float* v, float m, uint32_t ga, const RowCtx& rc, int Kp) {
+  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+  const int nvalid = (Kp - NC * rc.part) >> 3;  // chunks of this thread below Kp
 #pragma unroll
   for (int cj = 0; cj < NC / 8; ++cj) {
-    const int comp = NC * rc.hf + 8 * cj;
-    if (comp < Kp) {
-      uint8_t* dst = g + (comp >> 6) * 16384 + sw128_chunk(rc.row, (comp & 63) >> 3);
-      *reinterpret_cast<uint4*>(dst) =
-          make_uint4(packed[4 * cj], packed[4 * cj + 1], packed[4 * cj + 2], packed[4 * cj + 3]);
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float t0 = v[8 * cj + 2 * i], t1 = v[8 * cj + 2 * i + 1];
+      add_f32x2(t0, t1, -m, -m);
+      const float e0 = ex2_approx(t0), e1 = ex2_approx(t1);
+      if (kSum) {
+        if (i & 1)
+          add_f32x2(s2, s3, e0, e1);
+        else
+          add_f32x2(s0, s1, e0, e1);
+      }
+      w[i] = pack_bf16x2(e0, e1);
     }
+    if (cj < nvalid) sts128(ga ^ (uint32_t)(cj << 4), make_uint4(w[0], w[1], w[2], w[3]));
   }
+  return kSum ? (s0 + s1) + (s2 + s3) : 0.f;
+}
+
+// Fused pass for a TMEM-resident operand: e = 2^(v - m) packed to bf16 pairs and stored over this thread's
+// NC/2 columns starting at taddr (8 words per store).  The caller waits for the stores.
+template <int NC>
+__device__ __forceinline__ void exp_pack_tmem(const float* v, float m, uint32_t taddr) {
+#pragma unroll
+  for (int c = 0; c < NC / 16; ++c) {
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float t0 = v[16 * c + 2 * i], t1 = v[16 * c + 2 * i + 1];
+      add_f32x2(t0, t1, -m, -m);
+      w[i] = pack_bf16x2(ex2_approx(t0), ex2_approx(t1));
+    }
+    tmem_st8(taddr + 8 * c, w);
+  }
+}
+
+// Scales this thread's quarter of a key's V row (two 16-byte chunks of the swizzled bf16 tile at shared
+// address vtile) by inv.
+__device__ __forceinline__ void scale_v_row(uint32_t vtile, const RowCtx& rc, float inv) {
+  const __nv_bfloat162 inv2 = __float2bfloat162_rn(inv);
+#pragma unroll
+  for (int jj = 0; jj < 2; ++jj) {
+    const uint32_t ad = (vtile + rc.rowq) ^ (uint32_t)(jj << 4);
+    uint4 x = lds128(ad);
+    __nv_bfloat162* hx = reinterpret_cast<__nv_bfloat162*>(&x);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) hx[q] = __hmul2(hx[q], inv2);
+    sts128(ad, x);
+  }
+}
+
+__device__ __forceinline__ uint16_t bf16_bits(float x) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(x);
+  return *reinterpret_cast<const uint16_t*>(&h);
 }
 
 __device__ __forceinline__ void init_bars(Bars* B) {
@@ -305,14 +370,12 @@ __device__ __forceinline__ void init_bars(Bars* B) {
     mbar_init(&B->v_empty[s], 1);
   }
   mbar_init(&B->ax_full, kRowWarps);
-  mbar_init(&B->ax_empty, 1);
   mbar_init(&B->l_full, 1);
   mbar_init(&B->l_empty, kRowWarps);
   mbar_init(&B->g_full, kRowWarps);
   mbar_init(&B->g_empty, 1);
   mbar_init(&B->o_full, 1);
   mbar_init(&B->o_empty, kRowWarps);
-  mbar_init(&B->mx, kRowWarps);
   mbar_init(&B->done, 1);
   B->ab.flag = 0;
   mbar_fence_init();
@@ -362,6 +425,24 @@ __device__ __forceinline__ void issue_logits(uint32_t tmem, uint32_t w_addr, int
   }
 }
 
+// Normalises 16 output dims of one row (acc / (z + eps s)) and stores them as bf16 (two 16-byte stores).
+__device__ __forceinline__ void store_out16(__nv_bfloat16* dst, const uint32_t* acc, float rden) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int c = 0; c < 2; ++c)
+    d[c] = make_uint4(pack_bf16x2(__uint_as_float(acc[8 * c]) * rden, __uint_as_float(acc[8 * c + 1]) * rden),
+                      pack_bf16x2(__uint_as_float(acc[8 * c + 2]) * rden, __uint_as_float(acc[8 * c + 3]) * rden),
+                      pack_bf16x2(__uint_as_float(acc[8 * c + 4]) * rden, __uint_as_float(acc[8 * c + 5]) * rden),
+                      pack_bf16x2(__uint_as_float(acc[8 * c + 6]) * rden, __uint_as_float(acc[8 * c + 7]) * rden));
+}
+__device__ __forceinline__ void store_out8(__nv_bfloat16* dst, const uint32_t* acc, float rden) {
+  *reinterpret_cast<uint4*>(dst) =
+      make_uint4(pack_bf16x2(__uint_as_float(acc[0]) * rden, __uint_as_float(acc[1]) * rden),
+                 pack_bf16x2(__uint_as_float(acc[2]) * rden, __uint_as_float(acc[3]) * rden),
+                 pack_bf16x2(__uint_as_float(acc[4]) * rden, __uint_as_float(acc[5]) * rden),
+                 pack_bf16x2(__uint_as_float(acc[6]) * rden, __uint_as_float(acc[7]) * rden));
+}
+
 // ----------------------------------------------------------------------------------------------- write / aggregate
 // grid (splits, B*H).  CTA (split, bh) covers tiles [split * seg_tiles, ...) of head-row bh and adds
 // Gamma_K^T [V | 1] over them into state[bh] (kAtomic) or stores it to state[bh][split] (causal).
@@ -369,7 +450,8 @@ template <bool kAtomic, int NC>
 __global__ void __launch_bounds__(kThreadsTc, 1)
     tc_write_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // 1 KB aligned, still shared
+  const uint32_t sbase = smem_u32(smem);
   __shared__ Bars B;
   const SmemLayout L = write_layout(a.Kp);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -378,15 +460,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   const int T = max(0, min(a.tiles, tile0 + a.seg_tiles) - tile0);
   const int MB = (a.Kp + 127) / 128;
 
-  // zero Gamma~ (components beyond Kp stay zero: the M=128 blocks read them) and the ones atom
+  // zero Gamma~ (components beyond Kp stay zero: the M=128 blocks read them) and the [1] atom
   for (uint32_t i = threadIdx.x; i < (uint32_t)MB * 32768 / 16; i += blockDim.x)
     reinterpret_cast<uint4*>(smem + L.g)[i] = make_uint4(0, 0, 0, 0);
   for (uint32_t i = threadIdx.x; i < 16384 / 16; i += blockDim.x)
     reinterpret_cast<uint4*>(smem + L.inv)[i] = make_uint4(0, 0, 0, 0);
   __syncthreads();
-  // ones atom: element n = 64 of every token row of the MN-major [V | 1] operand is 1.0
-  if (threadIdx.x < kTile)
-    *reinterpret_cast<uint16_t*>(smem + L.inv + sw128_chunk(threadIdx.x, 0)) = 0x3F80u;
+  // element n = 64 of each token row of the MN-major [V | 1] operand receives 1/s of that key every tile
   if (threadIdx.x == 0) init_bars(&B);
   if (warp == 1) {
     tmem_alloc(&B.tmem_base, 512);
@@ -411,8 +491,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       if (ok && T > 0) {
         tc_fence_after();
         issue_logits(tmem, w_addr, a.Kp);
-        mma_commit(&B.l_full);
-        mma_commit(&B.ax_empty);
+        mma_commit(&B.l_full);  // also frees the [x^2 | x] columns for the next tile
       }
       for (int t = 0; ok && t < T; ++t) {
         if (t + 1 < T) {
@@ -422,7 +501,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           tc_fence_after();
           issue_logits(tmem, w_addr, a.Kp);
           mma_commit(&B.l_full);
-          mma_commit(&B.ax_empty);
         }
         const int s = t & 1;
         ok = wait_bounded(&B.g_full, t & 1, &B.ab, a.ctrl, 24, a.wait_ns) &&
@@ -449,15 +527,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   } else {
     setmaxnreg_inc<kRowRegs>();
     // ------------------------------------------------------------------ row warps
-    const RowCtx rc = row_ctx();
-    const float* cs = reinterpret_cast<const float*>(smem + L.c);
-    float2* red2 = reinterpret_cast<float2*>(smem + L.red);
+    const RowCtx rc = row_ctx(sbase + L.red);
+    const uint32_t cs = sbase + L.c;
+    const uint32_t ga = gamma_row_addr<NC>(sbase + L.g, rc);
     zero_unused_logits<NC>(tmem, rc, a.Kp);
     bool ok = warp_wait(&B.w_full, 0, &B.ab, a.ctrl, 30, a.wait_ns);
     if (ok && T > 0) {
       ok = warp_wait(&B.x_full[0], 0, &B.ab, a.ctrl, 31, a.wait_ns);
       if (ok) {
-        transform_row(smem + L.x, rc, tmem);
+        transform_row(sbase + L.x, rc, tmem);
         warp_arrive(&B.x_empty[0]);
         tmem_st_wait();
         tc_fence_before();
@@ -465,44 +543,57 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       }
     }
     float v[NC];
-    for (int t = 0; ok && t < T; ++t) {
+    // every row warp runs all T tiles and all exchanges; after a failed wait (ok = false) it skips the
+    // work and the waits but still takes part in the exchanges, whose barriers have no time limit
+    for (int t = 0; t < T; ++t) {
       const int s = t & 1;
       const int tok = (tile0 + t) * kTile + rc.row;
-      // logits of tile t -> registers; TMEM free for tile t+1
-      if (!(ok = warp_wait(&B.l_full, t & 1, &B.ab, a.ctrl, 32, a.wait_ns))) break;
-      tc_fence_after();
-      // operand of tile t+1 first (its contraction starts as soon as the logits below are read)
-      if (t + 1 < T) {
-        const int s1 = (t + 1) & 1;
-        if (!(ok = warp_wait(&B.x_full[s1], ((t + 1) >> 1) & 1, &B.ab, a.ctrl, 33, a.wait_ns))) break;
-        if (!(ok = warp_wait(&B.ax_empty, t & 1, &B.ab, a.ctrl, 34, a.wait_ns))) break;
+      float mp = -INFINITY;
+      // logits of tile t; the [x^2 | x] columns are free again, so the operand of tile t+1 goes in first
+      if (ok) ok = warp_wait(&B.l_full, t & 1, &B.ab, a.ctrl, 32, a.wait_ns);
+      if (ok) {
         tc_fence_after();
-        transform_row(smem + L.x + s1 * 16384, rc, tmem);
-        warp_arrive(&B.x_empty[s1]);
-        tmem_st_wait();
-        tc_fence_before();
-        warp_arrive(&B.ax_full);
+        if (t + 1 < T) {
+          const int s1 = (t + 1) & 1;
+          ok = warp_wait(&B.x_full[s1], ((t + 1) >> 1) & 1, &B.ab, a.ctrl, 33, a.wait_ns);
+          if (ok) {
+            transform_row(sbase + L.x + s1 * 16384, rc, tmem);
+            warp_arrive(&B.x_empty[s1]);
+            tmem_st_wait();
+            tc_fence_before();
+            warp_arrive(&B.ax_full);
+          }
+        }
       }
-      const float mh = load_logits<NC>(tmem, rc, cs, v);
-      tc_fence_before();
-      warp_arrive(&B.l_empty);
-      RowScale rs;
-      if (!(ok = half_softmax<NC>(v, mh, red2, &B.mx, t & 1, rc, &B.ab, a.ctrl, 35, a.wait_ns, &rs))) break;
-      // normalised Gamma_K row (zero past N), so the contraction takes [V | 1] as loaded
-      scale_pack<NC>(v, tok < a.N ? rs.fac / rs.sum : 0.f);
-      if (t > 0 && !(ok = warp_wait(&B.g_empty, (t - 1) & 1, &B.ab, a.ctrl, 36, a.wait_ns))) break;
-      store_gamma<NC>(smem + L.g, rc, a.Kp, reinterpret_cast<const uint32_t*>(v));
-      fence_async_smem();
-      warp_arrive(&B.g_full);
+      if (ok) {
+        mp = load_logits<NC>(tmem, rc, cs, v);
+        tc_fence_before();
+        warp_arrive(&B.l_empty);
+      }
+      const float m = xchg_max(rc, 0, mp);
+      // Gamma~ row (unnormalised, row maximum 1) -> smem once the previous contraction has read it
+      if (ok && t > 0) ok = warp_wait(&B.g_empty, (t - 1) & 1, &B.ab, a.ctrl, 36, a.wait_ns);
+      float sp = 0.f;
+      if (ok) sp = exp_pack_store<NC, true>(v, m, ga, rc, a.Kp);
+      const float sum = xchg_sum(rc, 4, sp);
+      // normalise this key's Gamma row inside the contraction: scale its [v | 1] row by 1/s (0 past N)
+      if (ok) ok = warp_wait(&B.v_full[s], (t >> 1) & 1, &B.ab, a.ctrl, 38, a.wait_ns);
+      if (ok) {
+        const float inv = tok < a.N ? rcp_approx(sum) : 0.f;
+        scale_v_row(sbase + L.v + s * 16384, rc, inv);
+        if (rc.part == 0) sts16(sbase + L.inv + rc.rowsw, bf16_bits(inv));
+        fence_async_smem();
+        warp_arrive(&B.g_full);
+      }
     }
     // epilogue: state rows of this CTA -> global
-    if (ok && T > 0 && rc.hf < MB) {
+    if (ok && T > 0 && rc.part < MB) {
       if (warp_wait(&B.done, 0, &B.ab, a.ctrl, 39, a.wait_ns)) {
         tc_fence_after();
-        const int comp = 128 * rc.hf + rc.row;
+        const int comp = 128 * rc.part + rc.row;
         uint32_t r[80];
 #pragma unroll
-        for (int c = 0; c < 5; ++c) tmem_ld16(tmem + rc.lane_base + kColAcc + kStCols * rc.hf + 16 * c, r + 16 * c);
+        for (int c = 0; c < 5; ++c) tmem_ld16(tmem + rc.lane_base + kColAcc + kStCols * rc.part + 16 * c, r + 16 * c);
         tmem_ld_wait();
         if (comp < a.Kp) {
           float* dst = kAtomic ? a.state + ((size_t)bh * a.Kp + comp) * kStCols
@@ -534,7 +625,8 @@ template <bool kRead, int NC>
 __global__ void __launch_bounds__(kThreadsTc, 1)
     tc_read_kernel(const __grid_constant__ CUtensorMap tmQ, TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // 1 KB aligned, still shared
+  const uint32_t sbase = smem_u32(smem);
   __shared__ Bars B;
   const SmemLayout L = read_layout(a.Kp);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -566,8 +658,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       if (ok && T > 0) {
         tc_fence_after();
         issue_logits(tmem, w_addr, a.Kp);
-        mma_commit(&B.l_full);
-        mma_commit(&B.ax_empty);
+        mma_commit(&B.l_full);  // also frees the [x^2 | x] columns for the next tile
       }
       for (int t = 0; ok && t < T; ++t) {
         if (t + 1 < T) {
@@ -577,7 +668,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           tc_fence_after();
           issue_logits(tmem, w_addr, a.Kp);
           mma_commit(&B.l_full);
-          mma_commit(&B.ax_empty);
         }
         if (kRead) {
           ok = wait_bounded(&B.g_full, t & 1, &B.ab, a.ctrl, 45, a.wait_ns);
@@ -600,9 +690,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     }
   } else {
     setmaxnreg_inc<kRowRegs>();
-    const RowCtx rc = row_ctx();
-    const float* cs = reinterpret_cast<const float*>(smem + L.c);
-    float2* red2 = reinterpret_cast<float2*>(smem + L.red);
+    const RowCtx rc = row_ctx(sbase + L.red);
+    const uint32_t cs = sbase + L.c;
+    const uint32_t ga = gamma_row_addr<NC>(sbase + L.g, rc);
     zero_unused_logits<NC>(tmem, rc, a.Kp);
     const int rt = threadIdx.x - 32 * kRowWarp0;  // 0..255
     bool ok = true;
@@ -613,11 +703,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 #pragma unroll 4
         for (int c = 0; c < 20; ++c) {
           const float4 f = __ldg(src + c);
-          const float e[4] = {f.x, f.y, f.z, f.w};
+          // column kDv holds Z; eps is folded in once here so gamma~ . (Z + eps) is one contraction column
+          const float e[4] = {c == kDv / 4 ? f.x + a.eps : f.x, f.y, f.z, f.w};
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            *reinterpret_cast<__nv_bfloat16*>(smem + L.sb + sw128_off(4 * c + i, rt, kStCols * 128)) =
-                __float2bfloat16_rn(e[i]);
+          for (int i = 0; i < 4; ++i) sts16(sbase + L.sb + sw128_off(4 * c + i, rt, kStCols * 128), bf16_bits(e[i]));
         }
       }
       fence_async_smem();
@@ -627,7 +716,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     if (ok && T > 0) {
       ok = warp_wait(&B.x_full[0], 0, &B.ab, a.ctrl, 51, a.wait_ns);
       if (ok) {
-        transform_row(smem + L.x, rc, tmem);
+        transform_row(sbase + L.x, rc, tmem);
         warp_arrive(&B.x_empty[0]);
         tmem_st_wait();
         tc_fence_before();
@@ -635,65 +724,68 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       }
     }
     float v[NC];
-    float s_prev = 1.f;
-    for (int t = 0; ok && t < T; ++t) {
-      if (!(ok = warp_wait(&B.l_full, t & 1, &B.ab, a.ctrl, 52, a.wait_ns))) break;
-      tc_fence_after();
-      if (t + 1 < T) {
-        const int s1 = (t + 1) & 1;
-        if (!(ok = warp_wait(&B.x_full[s1], ((t + 1) >> 1) & 1, &B.ab, a.ctrl, 53, a.wait_ns))) break;
-        if (!(ok = warp_wait(&B.ax_empty, t & 1, &B.ab, a.ctrl, 54, a.wait_ns))) break;
+    // every row warp runs all T tiles and all exchanges (see the write kernel)
+    for (int t = 0; t < T; ++t) {
+      float mp = -INFINITY;
+      if (ok) ok = warp_wait(&B.l_full, t & 1, &B.ab, a.ctrl, 52, a.wait_ns);
+      if (ok) {
         tc_fence_after();
-        transform_row(smem + L.x + s1 * 16384, rc, tmem);
-        warp_arrive(&B.x_empty[s1]);
-        tmem_st_wait();
-        tc_fence_before();
-        warp_arrive(&B.ax_full);
-      }
-      const float mh = load_logits<NC>(tmem, rc, cs, v);
-      tc_fence_before();
-      warp_arrive(&B.l_empty);
-      RowScale rs;
-      if (!(ok = half_softmax<NC>(v, mh, red2, &B.mx, t & 1, rc, &B.ab, a.ctrl, 55, a.wait_ns, &rs))) break;
-      const int tok = (tile0 + t) * kTile + rc.row;
-      if (kRead) {
-        // unnormalised gamma~ = 2^(v - m) on the row maximum; the read divides by (gamma~ . Z + eps s)
-        scale_pack<NC>(v, rs.fac);
-        const float sum = rs.sum;
-        if (t > 0 && !(ok = warp_wait(&B.g_empty, (t - 1) & 1, &B.ab, a.ctrl, 56, a.wait_ns))) break;
-        store_gamma<NC>(smem + L.g, rc, a.Kp, reinterpret_cast<const uint32_t*>(v));
-        fence_async_smem();
-        warp_arrive(&B.g_full);
-        // epilogue of the previous tile (its read contraction has had a whole tile to finish)
-        if (t > 0) {
-          if (!(ok = warp_wait(&B.o_full, (t - 1) & 1, &B.ab, a.ctrl, 58, a.wait_ns))) break;
-          tc_fence_after();
-          uint32_t r[32], zc[16];
-          tmem_ld32(tmem + rc.lane_base + kColAcc + 32 * rc.hf, r);
-          tmem_ld16(tmem + rc.lane_base + kColAcc + 64, zc);  // zc[0] = Z column
-          tmem_ld_wait();
-          tc_fence_before();
-          warp_arrive(&B.o_empty);
-          const int ptok = tok - kTile;
-          const float rden = 1.0f / (__uint_as_float(zc[0]) + a.eps * s_prev);
-          if (ptok < a.N) {
-            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) +
-                                                  ((size_t)bh * a.N + ptok) * kDv + 32 * rc.hf);
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-              dst[c] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * c]) * rden, __uint_as_float(r[8 * c + 1]) * rden),
-                                  pack_bf16x2(__uint_as_float(r[8 * c + 2]) * rden, __uint_as_float(r[8 * c + 3]) * rden),
-                                  pack_bf16x2(__uint_as_float(r[8 * c + 4]) * rden, __uint_as_float(r[8 * c + 5]) * rden),
-                                  pack_bf16x2(__uint_as_float(r[8 * c + 6]) * rden, __uint_as_float(r[8 * c + 7]) * rden));
+        if (t + 1 < T) {
+          const int s1 = (t + 1) & 1;
+          ok = warp_wait(&B.x_full[s1], ((t + 1) >> 1) & 1, &B.ab, a.ctrl, 53, a.wait_ns);
+          if (ok) {
+            transform_row(sbase + L.x + s1 * 16384, rc, tmem);
+            warp_arrive(&B.x_empty[s1]);
+            tmem_st_wait();
+            tc_fence_before();
+            warp_arrive(&B.ax_full);
           }
         }
-        s_prev = sum;
+      }
+      if (ok) {
+        mp = load_logits<NC>(tmem, rc, cs, v);
+        tc_fence_before();
+        warp_arrive(&B.l_empty);
+      }
+      const int tok = (tile0 + t) * kTile + rc.row;
+      if (kRead) {
+        // one exchange per tile, alternating slots: a slot is rewritten only after the next exchange
+        const float m = xchg_max(rc, (uint32_t)(t & 1) * 4u, mp);
+        // unnormalised gamma~ = 2^(v - m); the read divides by gamma~ . (Z + eps) = gamma~ . Z + eps s
+        if (ok && t > 0) ok = warp_wait(&B.g_empty, (t - 1) & 1, &B.ab, a.ctrl, 56, a.wait_ns);
+        if (ok) {
+          exp_pack_store<NC, false>(v, m, ga, rc, a.Kp);
+          fence_async_smem();
+          warp_arrive(&B.g_full);
+        }
+        // epilogue of the previous tile (its read contraction has had a whole tile to finish)
+        if (ok && t > 0) {
+          ok = warp_wait(&B.o_full, (t - 1) & 1, &B.ab, a.ctrl, 58, a.wait_ns);
+          if (ok) {
+            tc_fence_after();
+            uint32_t r[16], zc[16];
+            tmem_ld16(tmem + rc.lane_base + kColAcc + 16 * rc.part, r);
+            tmem_ld16(tmem + rc.lane_base + kColAcc + 64, zc);  // zc[0] = gamma~ . (Z + eps)
+            tmem_ld_wait();
+            tc_fence_before();
+            warp_arrive(&B.o_empty);
+            const int ptok = tok - kTile;
+            const float rden = rcp_approx(__uint_as_float(zc[0]));
+            if (ptok < a.N)
+              store_out16(reinterpret_cast<__nv_bfloat16*>(a.out) + ((size_t)bh * a.N + ptok) * kDv + 16 * rc.part,
+                          r, rden);
+          }
+        }
       } else {
-        // responsibilities: gamma = 2^(v - m_h) 2^(m_h - m) / s in float32
-        const float r = rs.fac / rs.sum;
-        if (tok < a.N) {
-          float* dst = reinterpret_cast<float*>(a.out) + ((size_t)bh * a.N + tok) * a.K + NC * rc.hf;
-          const int nk = min(max(a.K - NC * rc.hf, 0), NC);
+        // responsibilities: gamma = 2^(v - m) / s in float32
+        const float m = xchg_max(rc, 0, mp);
+        float sp = 0.f;
+        if (ok) sp = exp_inplace<NC>(v, m);
+        const float sum = xchg_sum(rc, 4, sp);
+        if (ok && tok < a.N) {
+          const float r = 1.0f / sum;
+          float* dst = reinterpret_cast<float*>(a.out) + ((size_t)bh * a.N + tok) * a.K + NC * rc.part;
+          const int nk = min(max(a.K - NC * rc.part, 0), NC);
 #pragma unroll
           for (int k = 0; k < NC; ++k)
             if (k < nk) dst[k] = v[k] * r;
@@ -704,22 +796,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     if (kRead && ok && T > 0) {
       if (warp_wait(&B.o_full, (T - 1) & 1, &B.ab, a.ctrl, 60, a.wait_ns)) {
         tc_fence_after();
-        uint32_t r[32], zc[16];
-        tmem_ld32(tmem + rc.lane_base + kColAcc + 32 * rc.hf, r);
+        uint32_t r[16], zc[16];
+        tmem_ld16(tmem + rc.lane_base + kColAcc + 16 * rc.part, r);
         tmem_ld16(tmem + rc.lane_base + kColAcc + 64, zc);
         tmem_ld_wait();
         const int ptok = (tile0 + T - 1) * kTile + rc.row;
-        const float rden = 1.0f / (__uint_as_float(zc[0]) + a.eps * s_prev);
-        if (ptok < a.N) {
-          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) +
-                                                ((size_t)bh * a.N + ptok) * kDv + 32 * rc.hf);
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            dst[c] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * c]) * rden, __uint_as_float(r[8 * c + 1]) * rden),
-                                pack_bf16x2(__uint_as_float(r[8 * c + 2]) * rden, __uint_as_float(r[8 * c + 3]) * rden),
-                                pack_bf16x2(__uint_as_float(r[8 * c + 4]) * rden, __uint_as_float(r[8 * c + 5]) * rden),
-                                pack_bf16x2(__uint_as_float(r[8 * c + 6]) * rden, __uint_as_float(r[8 * c + 7]) * rden));
-        }
+        const float rden = rcp_approx(__uint_as_float(zc[0]));
+        if (ptok < a.N)
+          store_out16(reinterpret_cast<__nv_bfloat16*>(a.out) + ((size_t)bh * a.N + ptok) * kDv + 16 * rc.part, r,
+                      rden);
       }
     }
   }
@@ -737,7 +822,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 //   O_i = [gq~_i . S_prev + sum_{j in tile, j <= i} (gq~_i . gk_j) [v_j | 1]] / (... + eps s_i),
 //   S  += Gamma_K(tile)^T [V | 1]
 // (gist.science summary, "Variants and training" item 3: prefix sums, O_i depends on j <= i only).
-// The "1" column of [V | 1] is a separate N=16 contraction against a constant K-major ones tile.
+// The "1" column of [V | 1] is a separate N=16 contraction against a K-major tile whose row 0 holds
+// 1/s_j of each key j of the tile (the other rows are zero), and the V rows are scaled by the same 1/s_j.
 constexpr uint32_t kCColP = 128;   // intra-tile affinity P (fp32 128 cols; bf16 halves at 128 and 192)
 constexpr uint32_t kCColS = 256;   // state accumulators, 80 columns per 128-component block
 constexpr uint32_t kCColO = 416;   // output accumulator (80 columns), shared with the [x^2 | x] operand
@@ -754,27 +840,49 @@ __host__ __device__ inline CausalLayout causal_layout(int Kp) {
   s.v = s.x + 2 * 16384;             // V tile (MN-major B)
   s.sbv = s.v + 16384;               // bf16 copy of S_prev[:, 0:64], MN-major B (comp groups of 1 KB)
   s.sbz = s.sbv + (Kp / 8) * 1024;   // bf16 copy of S_prev[:, 64] as row 0 of a 16-row K-major B
-  s.ones = s.sbz + KB * 2048;        // constant ones row (K-major, 16 x 128 tokens)
+  s.ones = s.sbz + KB * 2048;        // 1/s row of the keys (K-major, 16 x 128 tokens)
   s.c = s.ones + 4096;
   s.red = s.c + 1024;
-  s.total = s.red + 4 * kTile * 4;
+  s.total = s.red + kParts * kTile * 8;
   return s;
 }
 
 struct CBars {
   uint64_t w_full, x_full[2], x_empty[2], v_full, v_empty;
   uint64_t ax_full, lk_full, lq_go, gk_full, lq_full, gq_full, sb_full, p_full, pb_full, o_full, s_full;
-  uint64_t mx, done;
+  uint64_t done;
   uint32_t tmem_base;
   Abort ab;
 };
+
+// Writes float32 state columns 16c .. 16c+15 of component `comp` (r) into the bf16 operands of the
+// inter-tile term: columns 0..63 into SBV (MN-major, 16-byte chunks), column 64 plus eps into row 0 of
+// SBZ (K-major).
+__device__ __forceinline__ void snapshot_state_chunk(uint32_t sbv, uint32_t sbz, int comp, int c, const uint32_t* r,
+                                                     float eps) {
+  if (c < 4) {
+    const uint4 lo = make_uint4(pack_bf16x2(__uint_as_float(r[0]), __uint_as_float(r[1])),
+                                pack_bf16x2(__uint_as_float(r[2]), __uint_as_float(r[3])),
+                                pack_bf16x2(__uint_as_float(r[4]), __uint_as_float(r[5])),
+                                pack_bf16x2(__uint_as_float(r[6]), __uint_as_float(r[7])));
+    const uint4 hi = make_uint4(pack_bf16x2(__uint_as_float(r[8]), __uint_as_float(r[9])),
+                                pack_bf16x2(__uint_as_float(r[10]), __uint_as_float(r[11])),
+                                pack_bf16x2(__uint_as_float(r[12]), __uint_as_float(r[13])),
+                                pack_bf16x2(__uint_as_float(r[14]), __uint_as_float(r[15])));
+    sts128(sbv + sw128_chunk(comp, 2 * c), lo);
+    sts128(sbv + sw128_chunk(comp, 2 * c + 1), hi);
+  } else {
+    sts16(sbz + sw128_off(0, comp, 2048), bf16_bits(__uint_as_float(r[0]) + eps));
+  }
+}
 
 template <int NC>
 __global__ void __launch_bounds__(kThreadsTc, 1)
     tc_causal_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // 1 KB aligned, still shared
+  const uint32_t sbase = smem_u32(smem);
   __shared__ CBars B;
   const CausalLayout L = causal_layout(a.Kp);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -784,15 +892,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   const int MB = (a.Kp + 127) / 128;
   const int KS = a.Kp / 16;
 
-  // zero Gamma_K and the state copies; ones tile: row 0 of each 64-token block is 1.0 (bf16 0x3F80)
+  // zero Gamma_K, the state copies and the 1/s tile (its row 0 is rewritten every tile)
   for (uint32_t i = threadIdx.x; i < (uint32_t)MB * 32768 / 16; i += blockDim.x)
     reinterpret_cast<uint4*>(smem + L.gk)[i] = make_uint4(0, 0, 0, 0);
-  for (uint32_t i = threadIdx.x; i < (L.ones - L.sbv) / 16; i += blockDim.x)
+  for (uint32_t i = threadIdx.x; i < (L.ones + 4096 - L.sbv) / 16; i += blockDim.x)
     reinterpret_cast<uint4*>(smem + L.sbv)[i] = make_uint4(0, 0, 0, 0);
-  for (uint32_t i = threadIdx.x; i < 4096 / 16; i += blockDim.x) {
-    const uint32_t w = ((i * 16) % 2048) < 128 ? 0x3F803F80u : 0u;
-    reinterpret_cast<uint4*>(smem + L.ones)[i] = make_uint4(w, w, w, w);
-  }
   if (threadIdx.x == 0) {
     mbar_init(&B.w_full, 1);
     for (int s = 0; s < 2; ++s) {
@@ -812,7 +916,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     mbar_init(&B.pb_full, kRowWarps);
     mbar_init(&B.o_full, 1);
     mbar_init(&B.s_full, 1);
-    mbar_init(&B.mx, kRowWarps);
     mbar_init(&B.done, 1);
     B.ab.flag = 0;
     mbar_fence_init();
@@ -868,12 +971,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       const uint64_t d_gk_k = make_sdesc(smem_u32(smem + L.gk), 16, 1024);     // Gamma_K as K-major B
       const uint64_t d_gk_mn = make_sdesc(smem_u32(smem + L.gk), 16384, 1024); // Gamma_K^T as MN-major A
       const uint64_t d_v = make_sdesc(smem_u32(smem + L.v), 16384, 1024);      // V, MN-major, N = 64
-      const uint64_t d_one = make_sdesc(smem_u32(smem + L.ones), 16, 1024);    // ones row, K-major, N = 16
+      const uint64_t d_one = make_sdesc(smem_u32(smem + L.ones), 16, 1024);    // 1/s row, K-major, N = 16
       constexpr uint32_t id_c64 = make_idesc(128, 64, 1, 1, 0, 1);    // A tmem, B MN-major
       constexpr uint32_t id_c16 = make_idesc(128, 16, 1, 1, 0, 0);    // A tmem, B K-major
       constexpr uint32_t id_p = make_idesc(128, 128, 1, 1, 0, 0);     // P = Gq~ Gk^T
       constexpr uint32_t id_s64 = make_idesc(128, 64, 1, 1, 1, 1);    // A MN-major (Gamma_K^T), B MN-major (V)
-      constexpr uint32_t id_s16 = make_idesc(128, 16, 1, 1, 1, 0);    // A MN-major, B K-major (ones)
+      constexpr uint32_t id_s16 = make_idesc(128, 16, 1, 1, 1, 0);    // A MN-major, B K-major (1/s row)
       bool ok = wait_bounded(&B.w_full, 0, &B.ab, a.ctrl, 80, a.wait_ns);
       for (int t = 0; ok && t < T; ++t) {
         const uint32_t ph = t & 1;
@@ -920,7 +1023,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         tc_fence_after();
 #pragma unroll 1
         for (int s = 0; s < 8; ++s) {
-          const uint32_t ap = tmem + kCColP + (s < 4 ? 8 * s : 64 + 8 * (s - 4));
+          const uint32_t ap = tmem + kCColP + 32 * (s >> 1) + 8 * (s & 1);  // bf16 P of keys 16s..16s+15
           mma_ts(tmem + kCColO, ap, sdesc_add(d_v, 2048 * s), id_c64, 1u);
           mma_ts(tmem + kCColO + 64, ap, sdesc_add(d_one, (s >> 2) * 2048 + (s & 3) * 32), id_c16, 1u);
         }
@@ -934,37 +1037,21 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   } else {
     setmaxnreg_inc<kRowRegs>();
     // ------------------------------------------------------------------ row warps
-    const RowCtx rc = row_ctx();
-    const float* cs = reinterpret_cast<const float*>(smem + L.c);
-    float2* red2 = reinterpret_cast<float2*>(smem + L.red);
+    const RowCtx rc = row_ctx(sbase + L.red);
+    const uint32_t cs = sbase + L.c;
+    const uint32_t gka = gamma_row_addr<NC>(sbase + L.gk, rc);
     zero_unused_logits<NC>(tmem, rc, a.Kp);
-    // S <- exclusive prefix state of this segment; SB <- its bf16 copy
-    if (rc.hf < MB) {
-      const int comp = 128 * rc.hf + rc.row;
+    // S <- exclusive prefix state of this segment; SB <- its bf16 copy (eps rides in the Z column)
+    if (rc.part < MB) {
+      const int comp = 128 * rc.part + rc.row;
       const float* pre = a.state + (((size_t)bh * a.splits + seg) * a.Kp + comp) * kStCols;
       uint32_t r[16];
 #pragma unroll
       for (int c = 0; c < 5; ++c) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) r[i] = comp < a.Kp ? __float_as_uint(__ldg(pre + 16 * c + i)) : 0u;
-        tmem_st16(tmem + rc.lane_base + kCColS + kStCols * rc.hf + 16 * c, r);
-        if (comp < a.Kp) {
-          if (c < 4) {
-            uint4 lo = make_uint4(pack_bf16x2(__uint_as_float(r[0]), __uint_as_float(r[1])),
-                                  pack_bf16x2(__uint_as_float(r[2]), __uint_as_float(r[3])),
-                                  pack_bf16x2(__uint_as_float(r[4]), __uint_as_float(r[5])),
-                                  pack_bf16x2(__uint_as_float(r[6]), __uint_as_float(r[7])));
-            uint4 hi = make_uint4(pack_bf16x2(__uint_as_float(r[8]), __uint_as_float(r[9])),
-                                  pack_bf16x2(__uint_as_float(r[10]), __uint_as_float(r[11])),
-                                  pack_bf16x2(__uint_as_float(r[12]), __uint_as_float(r[13])),
-                                  pack_bf16x2(__uint_as_float(r[14]), __uint_as_float(r[15])));
-            *reinterpret_cast<uint4*>(smem + L.sbv + sw128_chunk(comp, 2 * c)) = lo;
-            *reinterpret_cast<uint4*>(smem + L.sbv + sw128_chunk(comp, 2 * c + 1)) = hi;
-          } else {
-            *reinterpret_cast<__nv_bfloat16*>(smem + L.sbz + sw128_off(0, comp, 2048)) =
-                __float2bfloat16_rn(__uint_as_float(r[0]));
-          }
-        }
+        tmem_st16(tmem + rc.lane_base + kCColS + kStCols * rc.part + 16 * c, r);
+        if (comp < a.Kp) snapshot_state_chunk(sbase + L.sbv, sbase + L.sbz, comp, c, r, a.eps);
       }
     }
     tmem_st_wait();
@@ -973,126 +1060,118 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     warp_arrive(&B.sb_full);
     bool ok = warp_wait(&B.w_full, 0, &B.ab, a.ctrl, 90, a.wait_ns);
     float v[NC];
-    for (int t = 0; ok && t < T; ++t) {
+    // every row warp runs all T tiles and all exchanges (see the write kernel)
+    for (int t = 0; t < T; ++t) {
       const uint32_t ph = t & 1;
       const int tok = (tile0 + t) * kTile + rc.row;
+      float mh = -INFINITY;
       // key operand (the [x^2 | x] columns double as the output accumulator, free since the last epilogue)
-      if (!(ok = warp_wait(&B.x_full[0], ph, &B.ab, a.ctrl, 91, a.wait_ns))) break;
-      transform_row(smem + L.x, rc, tmem, kCColO);
-      warp_arrive(&B.x_empty[0]);
-      tmem_st_wait();
-      tc_fence_before();
-      warp_arrive(&B.ax_full);
+      if (ok) ok = warp_wait(&B.x_full[0], ph, &B.ab, a.ctrl, 91, a.wait_ns);
+      if (ok) {
+        transform_row(sbase + L.x, rc, tmem, kCColO);
+        warp_arrive(&B.x_empty[0]);
+        tmem_st_wait();
+        tc_fence_before();
+        warp_arrive(&B.ax_full);
+      }
       // key logits -> registers; build the query operand first so its contraction starts at once
-      if (!(ok = warp_wait(&B.lk_full, ph, &B.ab, a.ctrl, 92, a.wait_ns))) break;
-      tc_fence_after();
-      if (!(ok = warp_wait(&B.x_full[1], ph, &B.ab, a.ctrl, 95, a.wait_ns))) break;
-      transform_row(smem + L.x + 16384, rc, tmem, kCColO);
-      warp_arrive(&B.x_empty[1]);
-      float mh = load_logits<NC>(tmem, rc, cs, v);
-      tmem_st_wait();
-      tc_fence_before();
-      warp_arrive(&B.lq_go);
-      // Gamma_K (normalised; zero rows past N) -> smem
-      RowScale rs;
-      if (!(ok = half_softmax<NC>(v, mh, red2, &B.mx, 0, rc, &B.ab, a.ctrl, 93, a.wait_ns, &rs))) break;
-      scale_pack<NC>(v, tok < a.N ? rs.fac / rs.sum : 0.f);
-      store_gamma<NC>(smem + L.gk, rc, a.Kp, reinterpret_cast<const uint32_t*>(v));
-      fence_async_smem();
-      warp_arrive(&B.gk_full);
+      if (ok) ok = warp_wait(&B.lk_full, ph, &B.ab, a.ctrl, 92, a.wait_ns);
+      if (ok) {
+        tc_fence_after();
+        ok = warp_wait(&B.x_full[1], ph, &B.ab, a.ctrl, 95, a.wait_ns);
+      }
+      if (ok) {
+        transform_row(sbase + L.x + 16384, rc, tmem, kCColO);
+        warp_arrive(&B.x_empty[1]);
+        mh = load_logits<NC>(tmem, rc, cs, v);
+        tmem_st_wait();
+        tc_fence_before();
+        warp_arrive(&B.lq_go);
+      }
+      // Gamma_K~ (unnormalised) -> smem; the key's 1/s (0 past N) scales its [v | 1] row instead
+      float m = xchg_max(rc, 0, mh);
+      float sp = 0.f;
+      if (ok) sp = exp_pack_store<NC, true>(v, m, gka, rc, a.Kp);
+      const float sum = xchg_sum(rc, 4, sp);
+      if (ok) ok = warp_wait(&B.v_full, ph, &B.ab, a.ctrl, 98, a.wait_ns);
+      if (ok) {
+        const float inv = tok < a.N ? rcp_approx(sum) : 0.f;
+        scale_v_row(sbase + L.v, rc, inv);
+        if (rc.part == 0) sts16(sbase + L.ones + (uint32_t)(rc.row >> 6) * 2048u + (uint32_t)(rc.row & 63) * 2u,
+                                bf16_bits(inv));
+        fence_async_smem();
+        warp_arrive(&B.gk_full);
+      }
       // Gamma_Q~ (unnormalised) -> TMEM over its own logit columns
-      if (!(ok = warp_wait(&B.lq_full, ph, &B.ab, a.ctrl, 96, a.wait_ns))) break;
-      tc_fence_after();
-      mh = load_logits<NC>(tmem, rc, cs, v);
-      if (!(ok = half_softmax<NC>(v, mh, red2, &B.mx, 1, rc, &B.ab, a.ctrl, 97, a.wait_ns, &rs))) break;
-      scale_pack<NC>(v, rs.fac);
-#pragma unroll
-      for (int c = 0; c < NC / 32; ++c)
-        tmem_st16(tmem + rc.lane_base + kColLog + (NC / 2) * rc.hf + 16 * c, reinterpret_cast<uint32_t*>(v) + 16 * c);
-      const float s_q = rs.sum;
-      tmem_st_wait();
-      tc_fence_before();
-      warp_arrive(&B.gq_full);
-      // intra-tile affinity: mask j > i, bf16 over the first half of this thread's own columns
-      if (!(ok = warp_wait(&B.p_full, ph, &B.ab, a.ctrl, 99, a.wait_ns))) break;
-      tc_fence_after();
-      {
-        uint32_t pr[64];
-        tmem_ld32(tmem + rc.lane_base + kCColP + 64 * rc.hf, pr);
-        tmem_ld32(tmem + rc.lane_base + kCColP + 64 * rc.hf + 32, pr + 32);
+      mh = -INFINITY;
+      if (ok) ok = warp_wait(&B.lq_full, ph, &B.ab, a.ctrl, 96, a.wait_ns);
+      if (ok) {
+        tc_fence_after();
+        mh = load_logits<NC>(tmem, rc, cs, v);
+      }
+      // the .x slots are free: every key maximum was read before the key-sum exchange.  They are
+      // rewritten with the next tile's key maxima only after the o_full wait below, which completes
+      // after every row warp has arrived on pb_full, i.e. after it has read these query maxima.
+      m = xchg_max(rc, 0, mh);
+      if (ok) {
+        exp_pack_tmem<NC>(v, m, tmem + rc.lane_base + kColLog + (NC / 2) * rc.part);
+        tmem_st_wait();
+        tc_fence_before();
+        warp_arrive(&B.gq_full);
+      }
+      // intra-tile affinity: mask j > i, bf16 over the first half of this thread's own 32 columns
+      if (ok) ok = warp_wait(&B.p_full, ph, &B.ab, a.ctrl, 99, a.wait_ns);
+      if (ok) {
+        tc_fence_after();
+        uint32_t pr[32];
+        tmem_ld32(tmem + rc.lane_base + kCColP + 32 * rc.part, pr);
         tmem_ld_wait();
-        const int lim = rc.row - 64 * rc.hf;  // columns c <= lim are keys j <= i
-        uint32_t pk[32];
+        const int lim = rc.row - 32 * rc.part;  // columns c <= lim are keys j <= i
+        uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
+        for (int i = 0; i < 16; ++i) {
           const float p0 = (2 * i <= lim) ? __uint_as_float(pr[2 * i]) : 0.f;
           const float p1 = (2 * i + 1 <= lim) ? __uint_as_float(pr[2 * i + 1]) : 0.f;
           pk[i] = pack_bf16x2(p0, p1);
         }
-        tmem_st16(tmem + rc.lane_base + kCColP + 64 * rc.hf, pk);
-        tmem_st16(tmem + rc.lane_base + kCColP + 64 * rc.hf + 16, pk + 16);
+        tmem_st16(tmem + rc.lane_base + kCColP + 32 * rc.part, pk);
         tmem_st_wait();
+        tc_fence_before();
+        warp_arrive(&B.pb_full);
       }
-      tc_fence_before();
-      warp_arrive(&B.pb_full);
       // the inter-tile term has read S_prev; snapshot the updated state for the next tile
-      if (!(ok = warp_wait(&B.s_full, ph, &B.ab, a.ctrl, 101, a.wait_ns))) break;
-      tc_fence_after();
-      if (rc.hf < MB) {
-        const int comp = 128 * rc.hf + rc.row;
-        uint32_t r[16];
+      if (ok) ok = warp_wait(&B.s_full, ph, &B.ab, a.ctrl, 101, a.wait_ns);
+      if (ok) {
+        tc_fence_after();
+        if (rc.part < MB) {
+          const int comp = 128 * rc.part + rc.row;
+          uint32_t r[16];
 #pragma unroll
-        for (int c = 0; c < 5; ++c) {
-          tmem_ld16(tmem + rc.lane_base + kCColS + kStCols * rc.hf + 16 * c, r);
-          tmem_ld_wait();
-          if (comp < a.Kp) {
-            if (c < 4) {
-              uint4 lo = make_uint4(pack_bf16x2(__uint_as_float(r[0]), __uint_as_float(r[1])),
-                                    pack_bf16x2(__uint_as_float(r[2]), __uint_as_float(r[3])),
-                                    pack_bf16x2(__uint_as_float(r[4]), __uint_as_float(r[5])),
-                                    pack_bf16x2(__uint_as_float(r[6]), __uint_as_float(r[7])));
-              uint4 hi = make_uint4(pack_bf16x2(__uint_as_float(r[8]), __uint_as_float(r[9])),
-                                    pack_bf16x2(__uint_as_float(r[10]), __uint_as_float(r[11])),
-                                    pack_bf16x2(__uint_as_float(r[12]), __uint_as_float(r[13])),
-                                    pack_bf16x2(__uint_as_float(r[14]), __uint_as_float(r[15])));
-              *reinterpret_cast<uint4*>(smem + L.sbv + sw128_chunk(comp, 2 * c)) = lo;
-              *reinterpret_cast<uint4*>(smem + L.sbv + sw128_chunk(comp, 2 * c + 1)) = hi;
-            } else {
-              *reinterpret_cast<__nv_bfloat16*>(smem + L.sbz + sw128_off(0, comp, 2048)) =
-                  __float2bfloat16_rn(__uint_as_float(r[0]));
-            }
+          for (int c = 0; c < 5; ++c) {
+            tmem_ld16(tmem + rc.lane_base + kCColS + kStCols * rc.part + 16 * c, r);
+            tmem_ld_wait();
+            if (comp < a.Kp) snapshot_state_chunk(sbase + L.sbv, sbase + L.sbz, comp, c, r, a.eps);
           }
         }
+        fence_async_smem();
+        tc_fence_before();
+        warp_arrive(&B.sb_full);
       }
-      fence_async_smem();
-      tc_fence_before();
-      warp_arrive(&B.sb_full);
-      // output: this thread's output dims are 16*hf + [0,16) and 32 + 16*hf + [0,16) -- the same columns it
+      // output: this thread's output dims are 8*part + [0,8) and 32 + 8*part + [0,8) -- the same columns it
       // overwrites with the next key operand, so no other warp reads them afterwards
-      if (!(ok = warp_wait(&B.o_full, ph, &B.ab, a.ctrl, 100, a.wait_ns))) break;
-      tc_fence_after();
-      {
-        uint32_t o0[16], o1[16], zc[16];
-        tmem_ld16(tmem + rc.lane_base + kCColO + 16 * rc.hf, o0);
-        tmem_ld16(tmem + rc.lane_base + kCColO + 32 + 16 * rc.hf, o1);
-        tmem_ld16(tmem + rc.lane_base + kCColO + 64, zc);
+      if (ok) ok = warp_wait(&B.o_full, ph, &B.ab, a.ctrl, 100, a.wait_ns);
+      if (ok) {
+        tc_fence_after();
+        uint32_t o0[8], o1[8], zc[8];
+        tmem_ld8(tmem + rc.lane_base + kCColO + 8 * rc.part, o0);
+        tmem_ld8(tmem + rc.lane_base + kCColO + 32 + 8 * rc.part, o1);
+        tmem_ld8(tmem + rc.lane_base + kCColO + 64, zc);
         tmem_ld_wait();
-        const float rden = 1.0f / (__uint_as_float(zc[0]) + a.eps * s_q);
+        const float rden = rcp_approx(__uint_as_float(zc[0]));  // gq~ . (Z_i + eps)
         if (tok < a.N) {
           __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.out) + ((size_t)bh * a.N + tok) * kDv;
-          uint4* d0 = reinterpret_cast<uint4*>(orow + 16 * rc.hf);
-          uint4* d1 = reinterpret_cast<uint4*>(orow + 32 + 16 * rc.hf);
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            d0[c] = make_uint4(pack_bf16x2(__uint_as_float(o0[8 * c]) * rden, __uint_as_float(o0[8 * c + 1]) * rden),
-                               pack_bf16x2(__uint_as_float(o0[8 * c + 2]) * rden, __uint_as_float(o0[8 * c + 3]) * rden),
-                               pack_bf16x2(__uint_as_float(o0[8 * c + 4]) * rden, __uint_as_float(o0[8 * c + 5]) * rden),
-                               pack_bf16x2(__uint_as_float(o0[8 * c + 6]) * rden, __uint_as_float(o0[8 * c + 7]) * rden));
-            d1[c] = make_uint4(pack_bf16x2(__uint_as_float(o1[8 * c]) * rden, __uint_as_float(o1[8 * c + 1]) * rden),
-                               pack_bf16x2(__uint_as_float(o1[8 * c + 2]) * rden, __uint_as_float(o1[8 * c + 3]) * rden),
-                               pack_bf16x2(__uint_as_float(o1[8 * c + 4]) * rden, __uint_as_float(o1[8 * c + 5]) * rden),
-                               pack_bf16x2(__uint_as_float(o1[8 * c + 6]) * rden, __uint_as_float(o1[8 * c + 7]) * rden));
-          }
+          store_out8(orow + 8 * rc.part, o0, rden);
+          store_out8(orow + 32 + 8 * rc.part, o1, rden);
         }
       }
     }
@@ -1106,15 +1185,21 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 }
 
 // Exclusive scan over segments: agg[bh][p][e] <- sum_{p' < p} agg[bh][p'][e].  grid (ceil(n / 256), B*H).
+// Loads go out eight segments at a time so the chain over p is not one dependent load after another.
 __global__ void tc_scan_kernel(float* agg, int P, int n) {
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= n) return;
   float* base = agg + (size_t)blockIdx.y * P * n + e;
   float run = 0.f;
-  for (int p = 0; p < P; ++p) {
-    const float x = base[(size_t)p * n];
-    base[(size_t)p * n] = run;
-    run += x;
+  for (int p0 = 0; p0 < P; p0 += 8) {
+    float x[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) x[j] = (p0 + j < P) ? base[(size_t)(p0 + j) * n] : 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (p0 + j < P) base[(size_t)(p0 + j) * n] = run;
+      run += x[j];
+    }
   }
 }
 
@@ -1262,10 +1347,10 @@ gma_status_t tc_run(const gma_problem_t& p, gma_op_t op, const void* Q, const vo
   GMA_LAUNCH("tc_prep", tc_prep_kernel, dim3(kCTable, p.H), 128, 0, st, mu, sigma2, log_pi, p.H, p.K, pl.Kp,
              (uint8_t*)a.w_img, (float*)a.cbias, a.ctrl, a.state, zero_n);
   if (gma_status_t e = check_launch("launch tc_prep", (const void*)tc_prep_kernel)) return e;
-  const int nc = pl.Kp <= 64 ? 32 : (pl.Kp <= 128 ? 64 : 128);
+  const int nc = pl.Kp <= 64 ? 16 : (pl.Kp <= 128 ? 32 : 64);  // components per row thread (4 per row)
+  if (nc == 16) return tc_launch<16>(p, op, pl, a, Q, K, V, st);
   if (nc == 32) return tc_launch<32>(p, op, pl, a, Q, K, V, st);
-  if (nc == 64) return tc_launch<64>(p, op, pl, a, Q, K, V, st);
-  return tc_launch<128>(p, op, pl, a, Q, K, V, st);
+  return tc_launch<64>(p, op, pl, a, Q, K, V, st);
 }
 
 bool tc_available() { return encode_fn() != nullptr; }
