@@ -18,6 +18,12 @@
  *   [Rd] Read phase: same section, item 2: O = Gamma_Q Vt / (Gamma_Q Z + eps).
  *   [C]  Causal variant: "Variants and training" item 3: prefix sums of the
  *        latent memory and the normaliser so that O_i depends on j <= i only.
+ *   [X]  Cross-attention: gist.science summary, "Significance and claims",
+ *        closing paragraph (cross-attention applications named as future work
+ *        beyond the self-attention setting): queries of one sequence read
+ *        the latent memory written by the keys and values of another, so the
+ *        write runs over Nk keys and the read over N queries; nothing else in
+ *        [W] / [Rd] changes.
  *
  * Readings where the pages leave a step open:
  *   - The log-density keeps every term of the diagonal Gaussian, including
@@ -75,8 +81,9 @@ static void posterior(int d, int K, const double *x, const double *mu, const dou
 }
 
 typedef struct {
-  int mode; /* 0 = responsibilities, 1 = bidirectional, 2 = causal */
+  int mode; /* 0 = responsibilities, 1 = bidirectional (or cross), 2 = causal */
   int B, H, N, d, dv, K;
+  int Nk; /* keys per unit: N except for cross-attention */
   const double *Q, *Kx, *V, *mu, *sigma2, *log_pi;
   double eps;
   const int64_t *rows; /* sorted ascending, or NULL for every row */
@@ -111,16 +118,17 @@ static void run_unit(job_t *J, int unit) {
     return;
   }
 
+  const int Nk = J->Nk;
   const double *Q = J->Q + (size_t)unit * N * d;
-  const double *Kx = J->Kx + (size_t)unit * N * d;
-  const double *V = J->V + (size_t)unit * N * dv;
+  const double *Kx = J->Kx + (size_t)unit * Nk * d;
+  const double *V = J->V + (size_t)unit * Nk * dv;
   double *O = J->out + (size_t)unit * nout * dv;
   double *Vt = (double *)calloc((size_t)K * dv, sizeof(double)); /* latent memory, K x dv */
   double *Z = (double *)calloc((size_t)K, sizeof(double));       /* normaliser, K */
 
   if (J->mode == 1) {
-    /* [W] write phase over all N keys */
-    for (int j = 0; j < N; ++j) {
+    /* [W] write phase over all Nk keys */
+    for (int j = 0; j < Nk; ++j) {
       posterior(d, K, Kx + (size_t)j * d, mu, s2, ld, lp, g);
       for (int k = 0; k < K; ++k) {
         Z[k] += g[k];
@@ -216,7 +224,19 @@ int gma_oracle_forward(int causal, int B, int H, int N, int d, int dv, int K, co
                        const int64_t *rows, int64_t nrows, double *O, int nthreads) {
   job_t J;
   memset(&J, 0, sizeof J);
-  J.mode = causal ? 2 : 1; J.B = B; J.H = H; J.N = N; J.d = d; J.dv = dv; J.K = K;
+  J.mode = causal ? 2 : 1; J.B = B; J.H = H; J.N = N; J.d = d; J.dv = dv; J.K = K; J.Nk = N;
+  J.Q = Q; J.Kx = Kx; J.V = V; J.mu = mu; J.sigma2 = sigma2; J.log_pi = log_pi; J.eps = eps;
+  J.rows = rows; J.nrows = nrows; J.out = O; J.nthreads = nthreads;
+  return run_job(&J);
+}
+
+/* [X] O [B,H,nrows or N,dv] for N queries reading the memory written by Nk keys / values per unit. */
+int gma_oracle_forward_cross(int B, int H, int N, int Nk, int d, int dv, int K, const double *Q, const double *Kx,
+                             const double *V, const double *mu, const double *sigma2, const double *log_pi,
+                             double eps, const int64_t *rows, int64_t nrows, double *O, int nthreads) {
+  job_t J;
+  memset(&J, 0, sizeof J);
+  J.mode = 1; J.B = B; J.H = H; J.N = N; J.d = d; J.dv = dv; J.K = K; J.Nk = Nk;
   J.Q = Q; J.Kx = Kx; J.V = V; J.mu = mu; J.sigma2 = sigma2; J.log_pi = log_pi; J.eps = eps;
   J.rows = rows; J.nrows = nrows; J.out = O; J.nthreads = nthreads;
   return run_job(&J);

@@ -13,6 +13,9 @@ item 3; fugumt.com English abstract):
 * ``forward(causal=False)``: Vt = Gamma_K^T V, Z = Gamma_K^T 1,
   O = Gamma_Q Vt / (Gamma_Q Z + eps).
 * ``forward(causal=True)``: the same with inclusive prefix sums over keys.
+* ``forward_cross``: the bidirectional form with N queries reading the memory
+  written by Nk keys / values (gist.science summary, "Significance and claims",
+  closing paragraph: cross-attention applications named as future work).
 * ``state``: Vt and Z alone.
 
 All inputs are converted to float64 here; the C code is plain sequential
@@ -62,6 +65,9 @@ def _load(path: str | None = None):
     lib.gma_oracle_forward.argtypes = [ci, ci, ci, ci, ci, ci, ci, dp, dp, dp, dp, dp, dp, ctypes.c_double,
                                        i64p, cl, dp, ci]
     lib.gma_oracle_forward.restype = ci
+    lib.gma_oracle_forward_cross.argtypes = [ci, ci, ci, ci, ci, ci, ci, dp, dp, dp, dp, dp, dp, ctypes.c_double,
+                                             i64p, cl, dp, ci]
+    lib.gma_oracle_forward_cross.restype = ci
     lib.gma_oracle_state.argtypes = [ci, ci, ci, ci, ci, ci, dp, dp, dp, dp, dp, dp, dp]
     lib.gma_oracle_state.restype = ci
     if path is None:
@@ -121,6 +127,24 @@ def forward(Q, Kx, V, mu, sigma2, log_pi, eps, causal=False, rows=None, nthreads
     lib = lib or _load()
     lib.gma_oracle_forward(1 if causal else 0, B, H, N, d, dv, K, _ptr(Q), _ptr(Kx), _ptr(V), _ptr(mu),
                            _ptr(sigma2), _ptr(log_pi), float(eps), rp, nr, _ptr(out), nthreads or default_threads())
+    return out
+
+
+def forward_cross(Q, Kx, V, mu, sigma2, log_pi, eps, rows=None, nthreads=None, lib=None):
+    """O [B,H,N|len(rows),dv] for queries Q [B,H,N,d] reading the memory of Kx [B,H,Nk,d], V [B,H,Nk,dv]."""
+    Q, Kx, V = _f64(Q), _f64(Kx), _f64(V)
+    mu, sigma2, log_pi = _f64(mu), _f64(sigma2), _f64(log_pi)
+    B, H, N, d = Q.shape
+    Nk = Kx.shape[2]
+    dv = V.shape[-1]
+    K = mu.shape[1]
+    assert Kx.shape == (B, H, Nk, d) and V.shape[:3] == (B, H, Nk)
+    assert mu.shape == (H, K, d) and sigma2.shape == (H, K, d) and log_pi.shape == (H, K)
+    r, nr, rp = _rows(rows, N)
+    out = np.empty((B, H, nr if r is not None else N, dv), dtype=np.float64)
+    lib = lib or _load()
+    lib.gma_oracle_forward_cross(B, H, N, Nk, d, dv, K, _ptr(Q), _ptr(Kx), _ptr(V), _ptr(mu), _ptr(sigma2),
+                                 _ptr(log_pi), float(eps), rp, nr, _ptr(out), nthreads or default_threads())
     return out
 
 

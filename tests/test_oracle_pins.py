@@ -12,6 +12,11 @@ code:
 * closed forms (K = 1 means, hand-derived 1-d examples in tests/golden/);
 * invariants (permutations, prior shift, mass conservation, convex hull,
   rank <= K).
+
+Cross-attention (N queries reading the memory of Nk keys; gist.science
+summary, "Significance and claims": cross-attention named as future work) is
+pinned the same way: the materialised N x Nk affinity, the K = 1 mean, no
+keys, and key-permutation invariance.
 """
 import math
 import os
@@ -271,6 +276,55 @@ def test_causal_endpoints():
     assert np.abs(Oc[:, :, 0] - V[:, :, 0] * g / (g + eps)).max() <= 1e-12
 
 
+# ----------------------------------------------------------------------------- cross-attention
+
+def _brute_cross(Q, Kx, V, mu, sigma2, log_pi, eps):
+    GQ = _scipy_gamma(Q, mu, sigma2, log_pi)
+    GK = _scipy_gamma(Kx, mu, sigma2, log_pi)
+    A = np.einsum("bhik,bhjk->bhij", GQ, GK)  # N x Nk
+    return np.einsum("bhij,bhjc->bhic", A, V) / (A.sum(-1, keepdims=True) + eps)
+
+
+def _cross_problem(seed, N, Nk, B=2, H=2, d=5, dv=3, K=4):
+    Q, _, _, mu, sigma2, log_pi = _small_problem(seed, B=B, H=H, N=N, d=d, dv=dv, K=K, smin=0.3)
+    r = _rng(seed + 1000)
+    Kx = r.standard_normal((B, H, Nk, d))
+    V = r.standard_normal((B, H, Nk, dv))
+    return Q, Kx, V, mu, sigma2, log_pi
+
+
+@pytest.mark.parametrize("N,Nk,eps", [(17, 29, 1e-6), (31, 5, 0.37), (1, 40, 1e-6)])
+def test_cross_matches_materialised_affinity(N, Nk, eps):
+    Q, Kx, V, mu, sigma2, log_pi = _cross_problem(5, N, Nk)
+    O = orc.forward_cross(Q, Kx, V, mu, sigma2, log_pi, eps)
+    ref = _brute_cross(Q, Kx, V, mu, sigma2, log_pi, eps)
+    assert O.shape == ref.shape
+    assert np.abs(O - ref).max() <= 1e-12 * max(1.0, np.abs(ref).max())
+
+
+@pytest.mark.parametrize("eps", [1e-6, 0.5])
+def test_cross_single_component_is_key_mean(eps):
+    # K = 1: every gamma is 1, so every query reads sum_j v_j / (Nk + eps)
+    Q, Kx, V, mu, sigma2, log_pi = _cross_problem(7, 9, 23, K=1)
+    O = orc.forward_cross(Q, Kx, V, mu, sigma2, log_pi, eps)
+    want = V.sum(2, keepdims=True) / (23 + eps)
+    assert np.abs(O - np.broadcast_to(want, O.shape)).max() <= 1e-13
+
+
+def test_cross_without_keys_is_zero():
+    Q, Kx, V, mu, sigma2, log_pi = _cross_problem(8, 6, 0)
+    O = orc.forward_cross(Q, Kx, V, mu, sigma2, log_pi, 1e-6)
+    assert O.shape == (2, 2, 6, 3) and np.all(O == 0.0)
+
+
+def test_cross_key_permutation_invariance():
+    Q, Kx, V, mu, sigma2, log_pi = _cross_problem(9, 12, 19)
+    perm = _rng(3).permutation(19)
+    O1 = orc.forward_cross(Q, Kx, V, mu, sigma2, log_pi, 1e-6)
+    O2 = orc.forward_cross(Q, Kx[:, :, perm], V[:, :, perm], mu, sigma2, log_pi, 1e-6)
+    assert np.abs(O1 - O2).max() <= 1e-12
+
+
 # ----------------------------------------------------------------------------- planted mistakes
 
 MUTANTS = {
@@ -279,6 +333,9 @@ MUTANTS = {
     "drop_prior": ("double l = log_pi[k]", "double l = 0.0 * log_pi[k]"),
     "drop_eps": ("den += J->eps;", "den += 0.0;"),
     "value_index": ("g[k] * V[(size_t)j * dv + c]", "g[k] * V[(size_t)j * dv + (dv - 1 - c)]"),
+    "cross_key_stride": ("const double *Kx = J->Kx + (size_t)unit * Nk * d;",
+                         "const double *Kx = J->Kx + (size_t)unit * N * d;"),
+    "cross_write_over_queries": ("for (int j = 0; j < Nk; ++j) {", "for (int j = 0; j < N && j < Nk; ++j) {"),
     "causal_drops_first_key": ("int64_t want = J->rows ? J->rows[r] : i;",
                          "int64_t want = J->rows ? J->rows[r] : i; if (i == 0) { memset(Vt, 0, sizeof(double) * K * dv); memset(Z, 0, sizeof(double) * K); }"),
 }
@@ -294,6 +351,10 @@ def _pins_pass(lib) -> bool:
                 return False
         G = orc.responsibilities(Q, mu, sigma2, log_pi, lib=lib)
         if np.abs(G - _scipy_gamma(Q, mu, sigma2, log_pi)).max() > 1e-10:
+            return False
+        Q, Kx, V, mu, sigma2, log_pi = _cross_problem(22, 7, 13)
+        O = orc.forward_cross(Q, Kx, V, mu, sigma2, log_pi, 0.37, lib=lib)
+        if np.abs(O - _brute_cross(Q, Kx, V, mu, sigma2, log_pi, 0.37)).max() > 1e-10:
             return False
         return True
     except Exception:
