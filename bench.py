@@ -23,7 +23,7 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from gaussian_mixture_sequence_gma_gb300.inputs import bf16_bits, make_workload, workloads  # noqa: E402
+from gaussian_mixture_sequence_gma_gb300.inputs import bf16_bits, make_inputs, make_workload, workloads  # noqa: E402
 
 WORKLOAD = "sweep_bf16_B1H8N131072K256"
 METRIC = "GMA fwd tokens*heads/s at K=256 (bidir & causal)"
@@ -377,6 +377,68 @@ def run_gma(args, world, rank, local):
             if n == N:
                 path["per_form_ms"] = {f: entry[f]["ms"] for f in entry}
 
+    # widened rows: cross-attention (queries of one sequence reading the memory of another) and the
+    # causal decode step (state resident between calls), each timed with CUDA events like the sweep
+    extensions = None
+    if args.sweep and rank == 0 and world == 1:
+        extensions = {}
+        from gaussian_mixture_sequence_gma_gb300.inputs import make_cross_inputs
+        Bc, Hc, Nq, Nk, Kc = 1, 8, 16384, 131072, 256
+        ci = to_dev(make_cross_inputs(Bc, Hc, Nq, Nk, Kc, dtype="bf16", seed=13), dev)
+        pc = gma.problem(Bc, Hc, Nq, Kc, torch.bfloat16, 1e-6)
+        wsc = gma.alloc_workspace(pc, gma.OP_CROSS, dev)
+        outc = torch.empty((Bc, Hc, Nq, 64), dtype=torch.bfloat16, device=dev)
+        call = lambda: gma.forward_cross(ci["Q"], ci["K"], ci["V"], ci["mu"], ci["sigma2"], ci["log_pi"], 1e-6,
+                                         out=outc, workspace=wsc)
+        for _ in range(3):
+            call()
+        m, _ = timed(call, 20)
+        t_call = m / 20 * 1e-3
+        flop = flop_per_tokhead(Kc) / 2 * Bc * Hc * (Nq + Nk)  # each query and each key: logits + read / write
+        extensions["cross_bf16_B1H8_N16384_Nk131072_K256"] = {
+            "ms": t_call * 1e3, "tok_heads_per_s": Bc * Hc * (Nq + Nk) / t_call,
+            "tflops_algorithmic": flop / t_call / 1e12, "frac_of_bf16_peak": flop / t_call / 1e12 / peaks["bf16"]}
+        del ci, wsc, outc
+        Bd, Hd, Kd, N0 = 8, 12, 256, 2048
+        di = to_dev(make_inputs(Bd, Hd, N0 + 64, Kd, dtype="bf16", seed=3, sigma_raw_std=0.5, projection=True), dev)
+        sl = lambda x, a, b: x[:, :, a:b].contiguous()
+        state = gma.causal_state(sl(di["K"], 0, N0), sl(di["V"], 0, N0), di["mu"], di["sigma2"], di["log_pi"])
+        pd = gma.problem(Bd, Hd, 1, Kd, torch.bfloat16, 1e-6)
+        wsd = gma.alloc_workspace(pd, gma.OP_CAUSAL_DECODE, dev)
+        toks = [(sl(di["Q"], N0 + i, N0 + i + 1), sl(di["K"], N0 + i, N0 + i + 1), sl(di["V"], N0 + i, N0 + i + 1))
+                for i in range(64)]
+        outd = torch.empty((Bd, Hd, 1, 64), dtype=torch.bfloat16, device=dev)
+        it = [0]
+
+        def step():
+            q, k, v = toks[it[0] % 64]
+            it[0] += 1
+            gma.causal_decode(q, k, v, di["mu"], di["sigma2"], di["log_pi"], state, 1e-6, out=outd, workspace=wsd)
+        for _ in range(5):
+            step()
+        # 64 steps captured in one CUDA graph, so the device time per step is not hidden behind the
+        # host-side cost of a Python call per token; eager timing if capture is not possible
+        try:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for _ in range(64):
+                    step()
+            g.replay()
+            m, _ = timed(g.replay, 5)
+            t_step = m / (5 * 64) * 1e-3
+            how = "CUDA graph of 64 steps"
+        except Exception as exc:  # noqa: BLE001
+            m, _ = timed(step, 200)
+            t_step = m / 200 * 1e-3
+            how = "eager (graph capture failed: %s)" % type(exc).__name__
+        state_bytes = 2 * Bd * Hd * Kd * 65 * 4  # read + write of the resident state per step
+        t_hbm = state_bytes / (peaks["hbm"] * 1e9)
+        extensions["decode_bf16_B8H12K256_1token"] = {
+            "us_per_step": t_step * 1e6, "tok_heads_per_s": Bd * Hd / t_step, "state_bytes_per_step": state_bytes,
+            "hbm_bound_us": t_hbm * 1e6, "frac_of_hbm_bound": t_hbm / t_step,
+            "launches_per_step": 2, "timing": how}
+        del di, state, wsd, toks, outd
+
     # CPU baseline: the oracle as it stands on a bounded sample of the same workload (rank 0 only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -393,7 +455,7 @@ def run_gma(args, world, rank, local):
                 "config": config_dict(w),
                 "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
                 "gpu_launches": int(launches), "roofline": roof, "cpu_baseline": cpu, "clocks": clk,
-                "roofline_path": path, "kernels": kernels, "sweep": sweep or None,
+                "roofline_path": path, "kernels": kernels, "sweep": sweep or None, "extensions": extensions,
                 "mufu_ex2_per_s": mufu_rate}
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -62,19 +62,25 @@ gma_status_t validate_problem(const gma_problem_t* p) {
 }
 
 size_t required_bytes(const gma_problem_t& p, gma_op_t op) {
+  if (op == GMA_OP_CROSS) op = GMA_OP_BIDIR;  // the same workspace: it does not depend on N
+  if (op == GMA_OP_CAUSAL_DECODE) return simt_plan(p, GMA_OP_RESPONSIBILITIES).total;  // parameters only
   if (p.dtype == GMA_BF16) return tc_plan(p, op).total;
   return simt_plan(p, op).total;
 }
 
-gma_status_t run(const gma_problem_t* p, gma_op_t op, const void* Q, const void* K, const void* V, const float* mu,
-                 const float* sigma2, const float* log_pi, void* out, void* ws, size_t ws_bytes, void* stream) {
+// Nk: keys / values per (b, h); N (= p->N) except for cross-attention.
+gma_status_t run(const gma_problem_t* p, gma_op_t op, int Nk, const void* Q, const void* K, const void* V,
+                 const float* mu, const float* sigma2, const float* log_pi, void* out, void* ws, size_t ws_bytes,
+                 void* stream) {
   gma_status_t s = validate_problem(p);
   if (s != GMA_OK) return s;
+  if (Nk < 0) return GMA_ERR_INVALID_ARG;
+  if ((long long)p->B * p->H * (long long)Nk >= (1LL << 31)) return GMA_ERR_UNSUPPORTED;
   if (!mu || !sigma2 || !log_pi || !ws) return GMA_ERR_INVALID_ARG;
   if (p->N > 0) {  // with N == 0 nothing is read or written, so empty tensors may be null
     if (!Q || !out) return GMA_ERR_INVALID_ARG;
-    if (op != GMA_OP_RESPONSIBILITIES && (!K || !V)) return GMA_ERR_INVALID_ARG;
-    if (op != GMA_OP_RESPONSIBILITIES && (out == Q || out == K || out == V)) return GMA_ERR_INVALID_ARG;
+    if (op != GMA_OP_RESPONSIBILITIES && Nk > 0 && (!K || !V)) return GMA_ERR_INVALID_ARG;
+    if (op != GMA_OP_RESPONSIBILITIES && (out == Q || (K && out == K) || (V && out == V))) return GMA_ERR_INVALID_ARG;
   }
   const void* ptrs[] = {Q, K, V, mu, sigma2, log_pi, out};
   for (const void* q : ptrs)
@@ -84,8 +90,9 @@ gma_status_t run(const gma_problem_t* p, gma_op_t op, const void* Q, const void*
   if (p->N == 0) return GMA_OK;
   cudaStream_t st = (cudaStream_t)stream;
   cudaGetLastError();  // a stale error from earlier caller work is not ours to report
-  if (p->dtype == GMA_BF16) return tc_run(*p, op, Q, K, V, mu, sigma2, log_pi, out, ws, st);
-  return simt_run(*p, op, Q, K, V, mu, sigma2, log_pi, out, ws, st);
+  if (op == GMA_OP_CROSS) op = GMA_OP_BIDIR;  // the bidirectional kernels, with the key length Nk
+  if (p->dtype == GMA_BF16) return tc_run(*p, op, Nk, Q, K, V, mu, sigma2, log_pi, out, ws, st);
+  return simt_run(*p, op, Nk, Q, K, V, mu, sigma2, log_pi, out, ws, st);
 }
 
 }  // namespace
@@ -97,25 +104,75 @@ extern "C" {
 
 size_t gma_workspace_bytes(const gma_problem_t* p, gma_op_t op) {
   if (validate_problem(p) != GMA_OK) return 0;
-  if (op != GMA_OP_RESPONSIBILITIES && op != GMA_OP_BIDIR && op != GMA_OP_CAUSAL) return 0;
+  if (op < GMA_OP_RESPONSIBILITIES || op > GMA_OP_CAUSAL_DECODE) return 0;
   return required_bytes(*p, op);
 }
 
 gma_status_t gma_responsibilities(const gma_problem_t* p, const void* X, const float* mu, const float* sigma2,
                                   const float* log_pi, float* gamma_out, void* ws, size_t ws_bytes, void* stream) {
-  return run(p, GMA_OP_RESPONSIBILITIES, X, nullptr, nullptr, mu, sigma2, log_pi, gamma_out, ws, ws_bytes, stream);
+  return run(p, GMA_OP_RESPONSIBILITIES, p ? p->N : 0, X, nullptr, nullptr, mu, sigma2, log_pi, gamma_out, ws, ws_bytes, stream);
 }
 
 gma_status_t gma_forward_bidir(const gma_problem_t* p, const void* Q, const void* K, const void* V, const float* mu,
                                const float* sigma2, const float* log_pi, void* O, void* ws, size_t ws_bytes,
                                void* stream) {
-  return run(p, GMA_OP_BIDIR, Q, K, V, mu, sigma2, log_pi, O, ws, ws_bytes, stream);
+  return run(p, GMA_OP_BIDIR, p ? p->N : 0, Q, K, V, mu, sigma2, log_pi, O, ws, ws_bytes, stream);
 }
 
 gma_status_t gma_forward_causal(const gma_problem_t* p, const void* Q, const void* K, const void* V, const float* mu,
                                 const float* sigma2, const float* log_pi, void* O, void* ws, size_t ws_bytes,
                                 void* stream) {
-  return run(p, GMA_OP_CAUSAL, Q, K, V, mu, sigma2, log_pi, O, ws, ws_bytes, stream);
+  return run(p, GMA_OP_CAUSAL, p ? p->N : 0, Q, K, V, mu, sigma2, log_pi, O, ws, ws_bytes, stream);
+}
+
+gma_status_t gma_forward_cross(const gma_problem_t* p, int Nk, const void* Q, const void* K, const void* V,
+                               const float* mu, const float* sigma2, const float* log_pi, void* O, void* ws,
+                               size_t ws_bytes, void* stream) {
+  return run(p, GMA_OP_CROSS, Nk, Q, K, V, mu, sigma2, log_pi, O, ws, ws_bytes, stream);
+}
+
+size_t gma_state_bytes(const gma_problem_t* p) {
+  if (validate_problem(p) != GMA_OK) return 0;
+  return (size_t)p->B * p->H * p->K * (p->dv + 1) * sizeof(float);
+}
+
+gma_status_t gma_causal_state(const gma_problem_t* p, const void* K, const void* V, const float* mu,
+                              const float* sigma2, const float* log_pi, float* state, void* ws, size_t ws_bytes,
+                              void* stream) {
+  gma_status_t s = validate_problem(p);
+  if (s != GMA_OK) return s;
+  if (!mu || !sigma2 || !log_pi || !ws || !state) return GMA_ERR_INVALID_ARG;
+  if (p->N > 0 && (!K || !V)) return GMA_ERR_INVALID_ARG;
+  const void* ptrs[] = {K, V, mu, sigma2, log_pi, state};
+  for (const void* q : ptrs)
+    if (q && !aligned(q, 16)) return GMA_ERR_INVALID_ARG;
+  if (!aligned(ws, kAlign)) return GMA_ERR_INVALID_ARG;
+  if (ws_bytes < required_bytes(*p, GMA_OP_CAUSAL_STATE)) return GMA_ERR_WORKSPACE;
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaGetLastError();
+  if (p->dtype == GMA_BF16) return tc_run(*p, GMA_OP_CAUSAL_STATE, p->N, nullptr, K, V, mu, sigma2, log_pi, state, ws, st);
+  return simt_run(*p, GMA_OP_CAUSAL_STATE, p->N, nullptr, K, V, mu, sigma2, log_pi, state, ws, st);
+}
+
+gma_status_t gma_causal_decode(const gma_problem_t* p, const void* Q, const void* K, const void* V, const float* mu,
+                               const float* sigma2, const float* log_pi, float* state, void* O, void* ws,
+                               size_t ws_bytes, void* stream) {
+  gma_status_t s = validate_problem(p);
+  if (s != GMA_OK) return s;
+  if (!mu || !sigma2 || !log_pi || !ws || !state) return GMA_ERR_INVALID_ARG;
+  if (p->N > 0) {
+    if (!Q || !K || !V || !O) return GMA_ERR_INVALID_ARG;
+    if (O == Q || O == K || O == V || O == (const void*)state) return GMA_ERR_INVALID_ARG;
+  }
+  const void* ptrs[] = {Q, K, V, mu, sigma2, log_pi, state, O};
+  for (const void* q : ptrs)
+    if (q && !aligned(q, 16)) return GMA_ERR_INVALID_ARG;
+  if (!aligned(ws, kAlign)) return GMA_ERR_INVALID_ARG;
+  if (ws_bytes < required_bytes(*p, GMA_OP_CAUSAL_DECODE)) return GMA_ERR_WORKSPACE;
+  if (p->N == 0) return GMA_OK;
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaGetLastError();
+  return simt_decode(*p, Q, K, V, mu, sigma2, log_pi, state, O, ws, st);
 }
 
 gma_status_t gma_check_device_error(void* ws, void* stream) {

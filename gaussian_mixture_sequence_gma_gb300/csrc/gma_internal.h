@@ -40,7 +40,8 @@ struct SimtPlan {
   size_t off_params, off_state, total;
 };
 SimtPlan simt_plan(const gma_problem_t& p, gma_op_t op);
-gma_status_t simt_run(const gma_problem_t& p, gma_op_t op, const void* Q, const void* K, const void* V,
+// Nk: keys / values per (b, h) for the write phase (p.N except for cross-attention).
+gma_status_t simt_run(const gma_problem_t& p, gma_op_t op, int Nk, const void* Q, const void* K, const void* V,
                       const float* mu, const float* sigma2, const float* log_pi, void* out, void* ws,
                       cudaStream_t stream);
 
@@ -53,10 +54,14 @@ struct TcPlan {
   size_t off_w, off_c, off_state, total;
 };
 TcPlan tc_plan(const gma_problem_t& p, gma_op_t op);
-gma_status_t tc_run(const gma_problem_t& p, gma_op_t op, const void* Q, const void* K, const void* V,
+gma_status_t tc_run(const gma_problem_t& p, gma_op_t op, int Nk, const void* Q, const void* K, const void* V,
                     const float* mu, const float* sigma2, const float* log_pi, void* out, void* ws,
                     cudaStream_t stream);
 bool tc_available();
+// Decode T = p.N new tokens per (b, h) against `state` (float32 [B*H][K][dv + 1], in place).
+gma_status_t simt_decode(const gma_problem_t& p, const void* Q, const void* K, const void* V, const float* mu,
+                         const float* sigma2, const float* log_pi, float* state, void* out, void* ws,
+                         cudaStream_t stream);
 // Test hook: bit 0 makes the next bidirectional write launch skip its first X-tile load, so that a
 // bounded device wait runs out and reports GMA_ERR_TIMEOUT.
 void tc_set_fault_injection(uint32_t mask);

@@ -69,10 +69,14 @@ __global__ void simt_prep_kernel(const float* __restrict__ mu, const float* __re
     P.mu_t[o] = mu[i];
     P.w_t[o] = 1.0f / sigma2[i];
   }
-  for (size_t i = tid; i < (size_t)H * K; i += nth) {
-    float s = 0.f;
-    for (int j = 0; j < kD; ++j) s += logf(sigma2[i * kD + j]);
-    P.c[i] = log_pi[i] - 0.5f * s;
+  // c_k: one warp per component, two dims per lane, then a warp sum (coalesced, no serial chain)
+  const int lane = threadIdx.x & 31;
+  const size_t warp_id = tid >> 5, nwarps = nth >> 5;
+  for (size_t i = warp_id; i < (size_t)H * K; i += nwarps) {
+    float s = logf(sigma2[i * kD + lane]) + logf(sigma2[i * kD + 32 + lane]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) P.c[i] = log_pi[i] - 0.5f * s;
   }
   for (size_t i = tid; i < zero_n; i += nth) zero[i] = 0.f;
 }
@@ -319,8 +323,153 @@ __global__ void __launch_bounds__(kThreads) simt_causal_kernel(const IO* __restr
   }
 }
 
+// ----------------------------------------------------------------------------------------------- decode
+// Causal decode: the recurrent form of the prefix sums ("Variants and training" item 3).  One CTA per
+// (b, h) holds that head's state S [K][dv + 1] in shared memory and takes its T new tokens in order:
+//   S_k += gamma_K(k_t)_k [v_t | 1],   o_t = gamma_Q(q_t) . S[:, :dv] / (gamma_Q(q_t) . S[:, dv] + eps),
+// so token t sees every earlier key and itself (inclusive), exactly as the causal forward does.
+// Thread k < K owns component k (log-density, state row); the read splits the 64 value columns over
+// four groups of components.  float32 throughout; the state is read once and written back once.
+constexpr int kDecodeThreads = 256;
+
+__device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float u = __shfl_xor_sync(0xffffffffu, v, o);
+    v = is_max ? fmaxf(v, u) : v + u;
+  }
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float r = red[0];
+  for (int w = 1; w < nw; ++w) r = is_max ? fmaxf(r, red[w]) : r + red[w];
+  __syncthreads();  // red is reused by the next reduction
+  return r;
+}
+
 template <typename IO>
-gma_status_t run_typed(const gma_problem_t& p, gma_op_t op, const IO* Q, const IO* Kx, const IO* V,
+__global__ void __launch_bounds__(kDecodeThreads) simt_decode_kernel(const IO* __restrict__ Q, const IO* __restrict__ Kx,
+                                                                     const IO* __restrict__ V, const float* params, int H,
+                                                                     int Tn, int K, float* __restrict__ state, float eps,
+                                                                     IO* __restrict__ out) {
+  extern __shared__ float sm[];
+  const int bh = blockIdx.x, h = bh % H, k = threadIdx.x;
+  float* S = sm;                          // [K][kStateCols]
+  float* xq = S + (size_t)K * kStateCols;  // [kD]
+  float* xk = xq + kD;                     // [kD]
+  float* xv = xk + kD;                     // [kDv]
+  float* gq = xv + kDv;                    // [K]
+  float* part = gq + K;                    // [4][kDv]
+  float* red = part + 4 * kDv;             // [32]
+  SimtParams P = params_at(const_cast<float*>(params), H, K);
+  const float* mu_t = P.mu_t + (size_t)h * kD * K;
+  const float* w_t = P.w_t + (size_t)h * kD * K;
+  float* st = state + (size_t)bh * K * kStateCols;
+  const int n_state = K * kStateCols;
+  // float4 copies when this head's state starts on a 16-byte boundary (K a multiple of 4), so that
+  // many loads are in flight per thread; plain floats otherwise
+  const bool vec = ((reinterpret_cast<uintptr_t>(st) | reinterpret_cast<uintptr_t>(S)) & 15) == 0 && (n_state & 3) == 0;
+  if (vec) {
+#pragma unroll 4
+    for (int i = threadIdx.x; i < n_state / 4; i += blockDim.x)
+      reinterpret_cast<float4*>(S)[i] = __ldcg(reinterpret_cast<const float4*>(st) + i);
+  } else {
+#pragma unroll 8
+    for (int i = threadIdx.x; i < n_state; i += blockDim.x) S[i] = __ldcg(st + i);
+  }
+  const float ck = k < K ? __ldg(P.c + (size_t)h * K + k) : 0.f;
+  for (int t = 0; t < Tn; ++t) {
+    const size_t row = (size_t)bh * Tn + t;
+    if (threadIdx.x < kD) {
+      xq[threadIdx.x] = ld_io<IO>(Q + row * kD + threadIdx.x);
+      xk[threadIdx.x] = ld_io<IO>(Kx + row * kD + threadIdx.x);
+      xv[threadIdx.x] = ld_io<IO>(V + row * kDv + threadIdx.x);
+    }
+    __syncthreads();
+    // log-densities of the key and the query under component k (centered form)
+    float lk = -INFINITY, lq = -INFINITY;
+    if (k < K) {
+      float ak = 0.f, aq = 0.f;
+#pragma unroll 16
+      for (int j = 0; j < kD; ++j) {  // unrolled so that the parameter loads of 16 dims are in flight together
+        const float m = __ldg(mu_t + (size_t)j * K + k), w = __ldg(w_t + (size_t)j * K + k);
+        const float dk = xk[j] - m, dq = xq[j] - m;
+        ak = fmaf(dk * w, dk, ak);
+        aq = fmaf(dq * w, dq, aq);
+      }
+      lk = ck - 0.5f * ak;
+      lq = ck - 0.5f * aq;
+    }
+    const float mk = block_reduce(lk, true, red), mq = block_reduce(lq, true, red);
+    const float ek = k < K ? expf(lk - mk) : 0.f, eq = k < K ? expf(lq - mq) : 0.f;
+    const float sk = block_reduce(ek, false, red), sq = block_reduce(eq, false, red);
+    // state update (own row), then the query's responsibilities for the read
+    if (k < K) {
+      const float g = ek / sk;
+      float* Sk = S + (size_t)k * kStateCols;
+      for (int j = 0; j < kDv; ++j) Sk[j] = fmaf(g, xv[j], Sk[j]);
+      Sk[kDv] += g;
+      gq[k] = eq / sq;
+    }
+    __syncthreads();
+    // read: numerator column j over component group g4, denominator over all components
+    {
+      const int j = threadIdx.x & (kDv - 1), g4 = threadIdx.x >> 6;
+      float acc = 0.f;
+      const int k1 = min(K, g4 * 64 + 64);
+#pragma unroll 8
+      for (int kk = g4 * 64; kk < k1; ++kk) acc = fmaf(gq[kk], S[(size_t)kk * kStateCols + j], acc);
+      part[g4 * kDv + j] = acc;
+    }
+    const float den = block_reduce(k < K ? gq[k] * S[(size_t)k * kStateCols + kDv] : 0.f, false, red) + eps;
+    if (threadIdx.x < kDv) {
+      const float num = (part[threadIdx.x] + part[kDv + threadIdx.x]) + (part[2 * kDv + threadIdx.x] + part[3 * kDv + threadIdx.x]);
+      st_io<IO>(out + row * kDv + threadIdx.x, num / den);
+    }
+    __syncthreads();  // xq / xk / xv / gq / part are rewritten by the next token
+  }
+  __syncthreads();
+  if (vec) {
+#pragma unroll 4
+    for (int i = threadIdx.x; i < n_state / 4; i += blockDim.x)
+      reinterpret_cast<float4*>(st)[i] = reinterpret_cast<const float4*>(S)[i];
+  } else {
+#pragma unroll 8
+    for (int i = threadIdx.x; i < n_state; i += blockDim.x) st[i] = S[i];
+  }
+}
+
+}  // namespace
+
+// Decode T new tokens per (b, h) from `state` (float32 [B*H][K][dv + 1], updated in place).
+gma_status_t simt_decode(const gma_problem_t& p, const void* Q, const void* K, const void* V, const float* mu,
+                         const float* sigma2, const float* log_pi, float* state, void* out, void* ws,
+                         cudaStream_t st) {
+  const SimtPlan pl = simt_plan(p, GMA_OP_RESPONSIBILITIES);  // parameters only
+  char* base = (char*)ws;
+  float* params = (float*)(base + pl.off_params);
+  GMA_LAUNCH("simt_prep", simt_prep_kernel, 148, 256, 0, st, mu, sigma2, log_pi, p.H, p.K, params, (Ctrl*)base,
+             (float*)nullptr, (size_t)0);
+  if (gma_status_t e = check_launch("launch simt_prep", (const void*)simt_prep_kernel)) return e;
+  const size_t smem = ((size_t)p.K * kStateCols + 2 * kD + kDv + p.K + 4 * kDv + 32) * sizeof(float);
+  const int BH = p.B * p.H;
+  if (p.dtype == GMA_F32) {
+    if (set_smem_optin((const void*)simt_decode_kernel<float>, (int)smem, 4) != GMA_OK) return GMA_ERR_CUDA;
+    GMA_LAUNCH("simt_decode", simt_decode_kernel<float>, BH, kDecodeThreads, smem, st, (const float*)Q,
+               (const float*)K, (const float*)V, params, p.H, p.N, p.K, state, p.eps, (float*)out);
+    return check_launch("launch simt_decode", (const void*)simt_decode_kernel<float>);
+  }
+  if (set_smem_optin((const void*)simt_decode_kernel<__nv_bfloat16>, (int)smem, 4) != GMA_OK) return GMA_ERR_CUDA;
+  GMA_LAUNCH("simt_decode", simt_decode_kernel<__nv_bfloat16>, BH, kDecodeThreads, smem, st,
+             (const __nv_bfloat16*)Q, (const __nv_bfloat16*)K, (const __nv_bfloat16*)V, params, p.H, p.N, p.K, state,
+             p.eps, (__nv_bfloat16*)out);
+  return check_launch("launch simt_decode", (const void*)simt_decode_kernel<__nv_bfloat16>);
+}
+
+namespace {
+
+template <typename IO>
+gma_status_t run_typed(const gma_problem_t& p, gma_op_t op, int Nk, const IO* Q, const IO* Kx, const IO* V,
                        const float* mu, const float* sigma2, const float* log_pi, void* out, void* ws,
                        cudaStream_t st) {
   const SimtPlan pl = simt_plan(p, op);
@@ -330,10 +479,12 @@ gma_status_t run_typed(const gma_problem_t& p, gma_op_t op, const IO* Q, const I
   float* state = (float*)(base + pl.off_state);
   const int BH = p.B * p.H, K = p.K;
   const int npairs = K * kStateCols;
+  const bool write_only = op == GMA_OP_CAUSAL_STATE;  // state of all N keys, copied to `out`
+  if (write_only) op = GMA_OP_BIDIR;
   const size_t zero_n = op == GMA_OP_BIDIR ? (size_t)BH * npairs : 0;
   GMA_LAUNCH("simt_prep", simt_prep_kernel, 148, 256, 0, st, mu, sigma2, log_pi, p.H, K, params, ctrl, state, zero_n);
   if (cudaGetLastError() != cudaSuccess) return GMA_ERR_CUDA;
-  if (p.N == 0) return GMA_OK;
+  if (p.N == 0 && !write_only) return GMA_OK;
   const size_t sm_gamma = (size_t)(T * kD + T * K) * sizeof(float);
   if (op == GMA_OP_RESPONSIBILITIES) {
     if (set_smem_optin((const void*)simt_resp_kernel<IO>, (int)sm_gamma, 0) != GMA_OK) return GMA_ERR_CUDA;
@@ -343,9 +494,20 @@ gma_status_t run_typed(const gma_problem_t& p, gma_op_t op, const IO* Q, const I
   const size_t sm_write = (size_t)(T * kD + T * kDv + T * K + npairs) * sizeof(float);
   if (set_smem_optin((const void*)simt_write_kernel<IO>, (int)sm_write, 1) != GMA_OK) return GMA_ERR_CUDA;
   if (op == GMA_OP_BIDIR) {
-    GMA_LAUNCH("simt_write", simt_write_kernel<IO>, dim3(pl.splits, BH), kThreads, sm_write, st, Kx, V, params, p.H, p.N, K, pl.seg_tiles,
-                                                                           pl.splits, state, 1);
-    if (cudaGetLastError() != cudaSuccess) return GMA_ERR_CUDA;
+    // write over the Nk keys (its own split plan; the workspace layout does not depend on N)
+    if (Nk > 0) {
+      gma_problem_t pk = p;
+      pk.N = Nk;
+      const SimtPlan plk = simt_plan(pk, op);
+      GMA_LAUNCH("simt_write", simt_write_kernel<IO>, dim3(plk.splits, BH), kThreads, sm_write, st, Kx, V, params, p.H, Nk, K,
+                 plk.seg_tiles, plk.splits, state, 1);
+      if (cudaGetLastError() != cudaSuccess) return GMA_ERR_CUDA;
+    }
+    if (write_only) {  // the accumulator already has the public state layout [B*H][K][dv + 1]
+      if (cudaMemcpyAsync(out, state, (size_t)BH * npairs * sizeof(float), cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+        return cuda_fail("copy state");
+      return GMA_OK;
+    }
     const size_t sm_read = (size_t)(T * kD + T * K + T * kStateCols) * sizeof(float);
     if (set_smem_optin((const void*)simt_read_kernel<IO>, (int)sm_read, 2) != GMA_OK) return GMA_ERR_CUDA;
     GMA_LAUNCH("simt_read", simt_read_kernel<IO>, dim3(pl.tiles, BH), kThreads, sm_read, st, Q, params, p.H, p.N, K, state, p.eps,
@@ -382,19 +544,20 @@ SimtPlan simt_plan(const gma_problem_t& p, gma_op_t op) {
   const size_t params_bytes = ((size_t)2 * p.H * kD * p.K + (size_t)p.H * p.K) * sizeof(float);
   pl.off_state = align_up(pl.off_params + params_bytes);
   size_t state_bytes = 0;
-  if (op == GMA_OP_BIDIR) state_bytes = (size_t)BH * p.K * kStateCols * sizeof(float);
+  if (op == GMA_OP_BIDIR || op == GMA_OP_CROSS || op == GMA_OP_CAUSAL_STATE)
+    state_bytes = (size_t)BH * p.K * kStateCols * sizeof(float);
   if (op == GMA_OP_CAUSAL) state_bytes = (size_t)BH * pl.splits * p.K * kStateCols * sizeof(float);
   pl.total = align_up(pl.off_state + state_bytes);
   return pl;
 }
 
-gma_status_t simt_run(const gma_problem_t& p, gma_op_t op, const void* Q, const void* K, const void* V,
+gma_status_t simt_run(const gma_problem_t& p, gma_op_t op, int Nk, const void* Q, const void* K, const void* V,
                       const float* mu, const float* sigma2, const float* log_pi, void* out, void* ws,
                       cudaStream_t stream) {
   if (p.dtype == GMA_F32)
-    return run_typed<float>(p, op, (const float*)Q, (const float*)K, (const float*)V, mu, sigma2, log_pi, out, ws,
+    return run_typed<float>(p, op, Nk, (const float*)Q, (const float*)K, (const float*)V, mu, sigma2, log_pi, out, ws,
                             stream);
-  return run_typed<__nv_bfloat16>(p, op, (const __nv_bfloat16*)Q, (const __nv_bfloat16*)K, (const __nv_bfloat16*)V,
+  return run_typed<__nv_bfloat16>(p, op, Nk, (const __nv_bfloat16*)Q, (const __nv_bfloat16*)K, (const __nv_bfloat16*)V,
                                   mu, sigma2, log_pi, out, ws, stream);
 }
 

@@ -19,6 +19,7 @@
 // and TMEM owner, warps 2-3 idle; warpgroups 1-4 (warps 4..19) = row warps: thread (q, part) owns token
 // row 32q+lane of the tile and a quarter of its components / dimensions (TMEM lane quarter q = warp % 4,
 // part = warpgroup - 1).  The control warpgroup hands registers to the row warpgroups with setmaxnreg.
+#include <algorithm>
 #include <cstdio>
 #include <mutex>
 
@@ -1203,6 +1204,17 @@ __global__ void tc_scan_kernel(float* agg, int P, int n) {
   }
 }
 
+// Public causal state [B*H][K][dv + 1] from the write accumulator [B*H][Kp][80] (columns 0..64).
+__global__ void tc_state_export_kernel(const float* __restrict__ acc, int K, int Kp, size_t n, float* __restrict__ out) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const int c = (int)(i % (kDv + 1));
+    const size_t rk = i / (kDv + 1);  // bh * K + k
+    const int k = (int)(rk % K);
+    const size_t bh = rk / K;
+    out[i] = acc[(bh * Kp + k) * kStCols + c];
+  }
+}
+
 // ----------------------------------------------------------------------------------------------- host
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -1254,8 +1266,8 @@ int split_for(int BH, int tiles) {
 
 // Launches the per-tile kernels with NC components per row thread (2 * NC >= Kp).
 template <int NC>
-gma_status_t tc_launch(const gma_problem_t& p, gma_op_t op, const TcPlan& pl, TcArgs a, const void* Q, const void* K,
-                       const void* V, cudaStream_t st) {
+gma_status_t tc_launch(const gma_problem_t& p, gma_op_t op, int Nk, const TcPlan& pl, TcArgs a, const void* Q,
+                       const void* K, const void* V, cudaStream_t st) {
   const int BH = p.B * p.H;
   CUtensorMap mq, mk, mv;
   if (op == GMA_OP_RESPONSIBILITIES) {
@@ -1266,8 +1278,8 @@ gma_status_t tc_launch(const gma_problem_t& p, gma_op_t op, const TcPlan& pl, Tc
     GMA_LAUNCH("tc_resp", (tc_read_kernel<false, NC>), dim3(pl.splits, BH), kThreadsTc, smem, st, mq, a);
     return check_launch("launch tc_resp", (const void*)tc_read_kernel<false, NC>);
   }
-  if (!make_map(&mq, Q, BH, p.N) || !make_map(&mk, K, BH, p.N) || !make_map(&mv, V, BH, p.N)) return GMA_ERR_CUDA;
   if (op == GMA_OP_CAUSAL) {
+    if (!make_map(&mq, Q, BH, p.N) || !make_map(&mk, K, BH, p.N) || !make_map(&mv, V, BH, p.N)) return GMA_ERR_CUDA;
     // a5: segment aggregates; a6: exclusive scan over segments; a7: chunked sweep
     const uint32_t smem_w = smem_bytes(write_layout(pl.Kp).total);
     if (set_smem_optin((const void*)tc_write_kernel<false, NC>, (int)smem_w, 0) != GMA_OK) return GMA_ERR_CUDA;
@@ -1283,11 +1295,26 @@ gma_status_t tc_launch(const gma_problem_t& p, gma_op_t op, const TcPlan& pl, Tc
     GMA_LAUNCH("tc_causal_chunk", tc_causal_kernel<NC>, dim3(pl.splits, BH), kThreadsTc, smem_c, st, mq, mk, mv, a);
     return check_launch("launch tc_causal_chunk", (const void*)tc_causal_kernel<NC>);
   }
-  const uint32_t smem_w = smem_bytes(write_layout(pl.Kp).total);
-  if (set_smem_optin((const void*)tc_write_kernel<true, NC>, (int)smem_w, 0) != GMA_OK) return GMA_ERR_CUDA;
-  GMA_LAUNCH("tc_bidir_write", (tc_write_kernel<true, NC>), dim3(pl.splits, BH), kThreadsTc, smem_w, st, mk, mv, a);
-  if (gma_status_t e = check_launch("launch tc_bidir_write", (const void*)tc_write_kernel<true, NC>)) return e;
+  // bidirectional / cross: write over the Nk keys with their own split plan (the state layout does not
+  // depend on the sequence lengths; with Nk = 0 the zeroed state is the empty memory)
+  if (Nk > 0) {
+    gma_problem_t pk = p;
+    pk.N = Nk;
+    const TcPlan plk = tc_plan(pk, op);
+    TcArgs aw = a;
+    aw.N = Nk;
+    aw.tiles = plk.tiles;
+    aw.seg_tiles = plk.seg_tiles;
+    aw.splits = plk.splits;
+    if (!make_map(&mk, K, BH, Nk) || !make_map(&mv, V, BH, Nk)) return GMA_ERR_CUDA;
+    const uint32_t smem_w = smem_bytes(write_layout(pl.Kp).total);
+    if (set_smem_optin((const void*)tc_write_kernel<true, NC>, (int)smem_w, 0) != GMA_OK) return GMA_ERR_CUDA;
+    GMA_LAUNCH("tc_bidir_write", (tc_write_kernel<true, NC>), dim3(plk.splits, BH), kThreadsTc, smem_w, st, mk, mv, aw);
+    if (gma_status_t e = check_launch("launch tc_bidir_write", (const void*)tc_write_kernel<true, NC>)) return e;
+  }
+  if (op == GMA_OP_CAUSAL_STATE) return GMA_OK;  // the state alone
   a.fault = 0;
+  if (!make_map(&mq, Q, BH, p.N)) return GMA_ERR_CUDA;
   const uint32_t smem_r = smem_bytes(read_layout(pl.Kp).total);
   if (set_smem_optin((const void*)tc_read_kernel<true, NC>, (int)smem_r, 0) != GMA_OK) return GMA_ERR_CUDA;
   GMA_LAUNCH("tc_bidir_read", (tc_read_kernel<true, NC>), dim3(pl.splits, BH), kThreadsTc, smem_r, st, mq, a);
@@ -1311,13 +1338,13 @@ TcPlan tc_plan(const gma_problem_t& p, gma_op_t op) {
   t.off_c = align_up(t.off_w + (size_t)p.H * t.Kp * 256);
   t.off_state = align_up(t.off_c + (size_t)p.H * kCTable * 4);
   size_t st = 0;
-  if (op == GMA_OP_BIDIR) st = (size_t)BH * t.Kp * kStCols * 4;
+  if (op == GMA_OP_BIDIR || op == GMA_OP_CROSS || op == GMA_OP_CAUSAL_STATE) st = (size_t)BH * t.Kp * kStCols * 4;
   if (op == GMA_OP_CAUSAL) st = (size_t)BH * t.splits * t.Kp * kStCols * 4;  // segment aggregates
   t.total = align_up(t.off_state + st);
   return t;
 }
 
-gma_status_t tc_run(const gma_problem_t& p, gma_op_t op, const void* Q, const void* K, const void* V,
+gma_status_t tc_run(const gma_problem_t& p, gma_op_t op, int Nk, const void* Q, const void* K, const void* V,
                     const float* mu, const float* sigma2, const float* log_pi, void* out, void* ws,
                     cudaStream_t st) {
   const TcPlan pl = tc_plan(p, op);
@@ -1343,14 +1370,20 @@ gma_status_t tc_run(const gma_problem_t& p, gma_op_t op, const void* Q, const vo
     a.fault = g_fault_next;
     g_fault_next = 0;
   }
-  const size_t zero_n = op == GMA_OP_BIDIR ? (size_t)BH * pl.Kp * kStCols : 0;
+  const bool with_state = op == GMA_OP_BIDIR || op == GMA_OP_CAUSAL_STATE;  // write accumulator starts at zero
+  const size_t zero_n = with_state ? (size_t)BH * pl.Kp * kStCols : 0;
   GMA_LAUNCH("tc_prep", tc_prep_kernel, dim3(kCTable, p.H), 128, 0, st, mu, sigma2, log_pi, p.H, p.K, pl.Kp,
              (uint8_t*)a.w_img, (float*)a.cbias, a.ctrl, a.state, zero_n);
   if (gma_status_t e = check_launch("launch tc_prep", (const void*)tc_prep_kernel)) return e;
   const int nc = pl.Kp <= 64 ? 16 : (pl.Kp <= 128 ? 32 : 64);  // components per row thread (4 per row)
-  if (nc == 16) return tc_launch<16>(p, op, pl, a, Q, K, V, st);
-  if (nc == 32) return tc_launch<32>(p, op, pl, a, Q, K, V, st);
-  return tc_launch<64>(p, op, pl, a, Q, K, V, st);
+  gma_status_t e = nc == 16   ? tc_launch<16>(p, op, Nk, pl, a, Q, K, V, st)
+                   : nc == 32 ? tc_launch<32>(p, op, Nk, pl, a, Q, K, V, st)
+                              : tc_launch<64>(p, op, Nk, pl, a, Q, K, V, st);
+  if (e != GMA_OK || op != GMA_OP_CAUSAL_STATE) return e;
+  const size_t n = (size_t)BH * p.K * (kDv + 1);
+  GMA_LAUNCH("tc_state_export", tc_state_export_kernel, (unsigned)std::min<size_t>((n + 255) / 256, 4096), 256, 0, st,
+             a.state, p.K, pl.Kp, n, (float*)out);
+  return check_launch("launch tc_state_export", (const void*)tc_state_export_kernel);
 }
 
 bool tc_available() { return encode_fn() != nullptr; }

@@ -16,9 +16,9 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "li
 
 GMA_OK, GMA_ERR_INVALID_ARG, GMA_ERR_UNSUPPORTED, GMA_ERR_WORKSPACE, GMA_ERR_CUDA, GMA_ERR_TIMEOUT = range(6)
 GMA_F32, GMA_BF16 = 0, 1
-OP_RESPONSIBILITIES, OP_BIDIR, OP_CAUSAL = 0, 1, 2
+OP_RESPONSIBILITIES, OP_BIDIR, OP_CAUSAL, OP_CROSS, OP_CAUSAL_STATE, OP_CAUSAL_DECODE = 0, 1, 2, 3, 4, 5
 
-EXPORTED = ("gma_workspace_bytes", "gma_responsibilities", "gma_forward_bidir", "gma_forward_causal",
+EXPORTED = ("gma_workspace_bytes", "gma_responsibilities", "gma_forward_bidir", "gma_forward_causal", "gma_forward_cross", "gma_state_bytes", "gma_causal_state", "gma_causal_decode",
             "gma_check_device_error", "gma_status_string", "gma_version", "gma_last_error", "gma_launch_count", "gma_profile_enable",
             "gma_profile_read", "gma_forward_bidir_static_ws", "gma_static_ws_capacity",
             "gma_debug_withhold_first_load", "gma_probe_ex2_rate")
@@ -67,6 +67,14 @@ def lib():
         f = getattr(L, name)
         f.argtypes = [pp, vp, vp, vp, fp, fp, fp, vp, vp, sz, vp]
         f.restype = ctypes.c_int
+    L.gma_forward_cross.argtypes = [pp, ctypes.c_int, vp, vp, vp, fp, fp, fp, vp, vp, sz, vp]
+    L.gma_forward_cross.restype = ctypes.c_int
+    L.gma_state_bytes.argtypes = [pp]
+    L.gma_state_bytes.restype = sz
+    L.gma_causal_state.argtypes = [pp, vp, vp, fp, fp, fp, vp, vp, sz, vp]
+    L.gma_causal_state.restype = ctypes.c_int
+    L.gma_causal_decode.argtypes = [pp, vp, vp, vp, fp, fp, fp, vp, vp, vp, sz, vp]
+    L.gma_causal_decode.restype = ctypes.c_int
     L.gma_check_device_error.argtypes = [vp, vp]
     L.gma_check_device_error.restype = ctypes.c_int
     L.gma_status_string.argtypes = [ctypes.c_int]
@@ -203,6 +211,81 @@ def forward_bidir(Q, K, V, mu, sigma2, log_pi, eps=1e-6, out=None, workspace=Non
 def forward_causal(Q, K, V, mu, sigma2, log_pi, eps=1e-6, out=None, workspace=None, stream=None):
     """Causal GMA forward (inclusive prefix over key positions): O [B,H,N,64]."""
     return _forward("gma_forward_causal", OP_CAUSAL, Q, K, V, mu, sigma2, log_pi, eps, out, workspace, stream)
+
+
+def forward_cross(Q, K, V, mu, sigma2, log_pi, eps=1e-6, out=None, workspace=None, stream=None):
+    """Cross-attention GMA forward: queries Q [B,H,N,64] read the memory written by K [B,H,Nk,64] and
+    V [B,H,Nk,64]; O [B,H,N,64] in the dtype of Q."""
+    B, H, N, d = Q.shape
+    Nk = K.shape[2]
+    dv = V.shape[-1]
+    Kc = mu.shape[1]
+    _params(mu, sigma2, log_pi)
+    dev = _check_cuda(Q, K, V, mu, sigma2, log_pi)
+    if K.dtype != Q.dtype or V.dtype != Q.dtype:
+        raise TypeError("Q, K and V must share one dtype")
+    if tuple(K.shape[:2]) != (B, H) or tuple(V.shape[:3]) != (B, H, Nk):
+        raise ValueError("K [B,H,Nk,d] and V [B,H,Nk,dv] must match Q's batch and heads")
+    prob = problem(B, H, N, Kc, Q.dtype, eps, d=d, dv=dv)
+    if out is None:
+        out = torch.empty((B, H, N, dv), dtype=Q.dtype, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(prob, OP_CROSS, dev)
+    with torch.cuda.device(dev):
+        s = lib().gma_forward_cross(ctypes.byref(prob), int(Nk), _ptr(Q), _ptr(K), _ptr(V), _ptr(mu), _ptr(sigma2),
+                                    _ptr(log_pi), _ptr(out), _ptr(workspace), workspace.numel(),
+                                    _stream_handle(stream, dev))
+    if s != GMA_OK:
+        raise GmaError(s, "gma_forward_cross")
+    return out
+
+
+def causal_state(K, V, mu, sigma2, log_pi, state=None, workspace=None, stream=None):
+    """State float32 [B,H,Kc,65] (latent memory | normaliser) after the N keys / values of K, V [B,H,N,64]."""
+    B, H, N, d = K.shape
+    dv = V.shape[-1]
+    Kc = mu.shape[1]
+    _params(mu, sigma2, log_pi)
+    dev = _check_cuda(K, V, mu, sigma2, log_pi)
+    if V.dtype != K.dtype:
+        raise TypeError("K and V must share one dtype")
+    prob = problem(B, H, N, Kc, K.dtype, 0.0, d=d, dv=dv)
+    if state is None:
+        state = torch.empty((B, H, Kc, dv + 1), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(prob, OP_CAUSAL_STATE, dev)
+    with torch.cuda.device(dev):
+        s = lib().gma_causal_state(ctypes.byref(prob), _ptr(K), _ptr(V), _ptr(mu), _ptr(sigma2), _ptr(log_pi),
+                                   _ptr(state), _ptr(workspace), workspace.numel(), _stream_handle(stream, dev))
+    if s != GMA_OK:
+        raise GmaError(s, "gma_causal_state")
+    return state
+
+
+def causal_decode(Q, K, V, mu, sigma2, log_pi, state, eps=1e-6, out=None, workspace=None, stream=None):
+    """Decode the N new tokens of Q, K, V [B,H,N,64] in order against `state` (float32 [B,H,Kc,65],
+    updated in place); returns O [B,H,N,64], each row the causal output of its position."""
+    B, H, N, d = Q.shape
+    dv = V.shape[-1]
+    Kc = mu.shape[1]
+    _params(mu, sigma2, log_pi)
+    dev = _check_cuda(Q, K, V, mu, sigma2, log_pi, state)
+    if K.dtype != Q.dtype or V.dtype != Q.dtype:
+        raise TypeError("Q, K and V must share one dtype")
+    if state.dtype != torch.float32 or tuple(state.shape) != (B, H, Kc, dv + 1):
+        raise ValueError("state must be float32 [B,H,K,dv+1]")
+    prob = problem(B, H, N, Kc, Q.dtype, eps, d=d, dv=dv)
+    if out is None:
+        out = torch.empty((B, H, N, dv), dtype=Q.dtype, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(prob, OP_CAUSAL_DECODE, dev)
+    with torch.cuda.device(dev):
+        s = lib().gma_causal_decode(ctypes.byref(prob), _ptr(Q), _ptr(K), _ptr(V), _ptr(mu), _ptr(sigma2),
+                                    _ptr(log_pi), _ptr(state), _ptr(out), _ptr(workspace), workspace.numel(),
+                                    _stream_handle(stream, dev))
+    if s != GMA_OK:
+        raise GmaError(s, "gma_causal_decode")
+    return out
 
 
 def forward_bidir_static_ws(Q, K, V, mu, sigma2, log_pi, eps=1e-6, out=None, stream=None):

@@ -127,5 +127,14 @@ def make_inputs(B: int, H: int, N: int, K: int, d: int = 64, dv: int = 64, dtype
     return dict(Q=Q, K=Kx, V=V, mu=mu, sigma2=sigma2, log_pi=log_pi, dtype=dtype)
 
 
+def make_cross_inputs(B: int, H: int, N: int, Nk: int, K: int, dtype: str = "bf16", seed: int = 0,
+                      sigma_raw_std: float = 1.0) -> dict:
+    """Seeded cross-attention problem: N queries, Nk keys / values, one shared set of parameters.
+    Queries and parameters come from make_inputs(seed); keys and values from a second stream."""
+    q = make_inputs(B, H, N, K, dtype=dtype, seed=seed, sigma_raw_std=sigma_raw_std)
+    kv = make_inputs(B, H, Nk, K, dtype=dtype, seed=seed + 7919, sigma_raw_std=sigma_raw_std)
+    return dict(Q=q["Q"], K=kv["K"], V=kv["V"], mu=q["mu"], sigma2=q["sigma2"], log_pi=q["log_pi"], dtype=dtype)
+
+
 def make_workload(w: Workload, N: int | None = None) -> dict:
     return make_inputs(w.B, w.H, N or w.N, w.K, w.d, w.dv, w.dtype, w.seed, w.sigma_raw_std, w.projection)

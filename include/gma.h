@@ -67,7 +67,14 @@ typedef enum {
 
 typedef enum { GMA_F32 = 0, GMA_BF16 = 1 } gma_dtype_t;
 
-typedef enum { GMA_OP_RESPONSIBILITIES = 0, GMA_OP_BIDIR = 1, GMA_OP_CAUSAL = 2 } gma_op_t;
+typedef enum {
+  GMA_OP_RESPONSIBILITIES = 0,
+  GMA_OP_BIDIR = 1,
+  GMA_OP_CAUSAL = 2,
+  GMA_OP_CROSS = 3,
+  GMA_OP_CAUSAL_STATE = 4,
+  GMA_OP_CAUSAL_DECODE = 5
+} gma_op_t;
 
 typedef struct {
   int B, H, N; /* batch, heads, sequence length */
@@ -136,6 +143,57 @@ GMA_API size_t gma_static_ws_capacity(void);
 GMA_API gma_status_t gma_forward_causal(const gma_problem_t *p, const void *Q, const void *K, const void *V, const float *mu,
                                 const float *sigma2, const float *log_pi, void *O, void *ws, size_t ws_bytes,
                                 void *stream);
+
+/*
+ * Cross-attention GMA forward: N queries of one sequence read the latent memory written by the
+ * Nk keys / values of another,
+ *   O = Gamma_Q (Gamma_K^T V) / (Gamma_Q (Gamma_K^T 1) + eps),  Gamma_Q [N x K], Gamma_K [Nk x K].
+ * Passage: gist.science summary, "Significance and claims" (cross-attention applications named as
+ * the next step beyond the self-attention setting); the write and read phases are those of
+ * "Core mechanism" item 2 with the key sequence of its own length.
+ *   Q [B,H,N,d] (N = p->N), K [B,H,Nk,d], V [B,H,Nk,dv] in p->dtype; O [B,H,N,dv] in p->dtype.
+ * Nk >= 0; with Nk = 0 the memory is empty and O = 0 (eps > 0).  K and V may be null when
+ * Nk = 0, Q and O when N = 0.  O may not alias any input.  The workspace is the bidirectional
+ * one: gma_workspace_bytes(p, GMA_OP_CROSS) == gma_workspace_bytes(p, GMA_OP_BIDIR), and
+ * neither depends on N or Nk.
+ */
+GMA_API gma_status_t gma_forward_cross(const gma_problem_t *p, int Nk, const void *Q, const void *K, const void *V,
+                                       const float *mu, const float *sigma2, const float *log_pi, void *O, void *ws,
+                                       size_t ws_bytes, void *stream);
+
+/*
+ * Causal state (latent memory and normaliser after a prefix of keys), the object a decode step
+ * keeps between calls.  Layout: float32 [B][H][K][dv + 1]; row k of head (b, h) holds
+ * sum_j gamma_jk v_j (dv values) followed by sum_j gamma_jk, over the keys seen so far.
+ * Passage: gist.science summary, "Variants and training" item 3 (prefix sums of the latent memory
+ * and the normaliser); "Core mechanism" item 2 (Vt = Gamma_K^T V, Z = Gamma_K^T 1).
+ */
+GMA_API size_t gma_state_bytes(const gma_problem_t *p); /* B*H*K*(dv+1)*4, or 0 if p is invalid */
+
+/*
+ * State after the N keys / values of a prompt: state = sum_{j < N} gamma_Kj [v_j | 1] per (b, h).
+ *   K [B,H,N,d], V [B,H,N,dv] in p->dtype;  state float32 [B][H][K][dv+1] (written; N = 0 gives zeros).
+ * Workspace: gma_workspace_bytes(p, GMA_OP_CAUSAL_STATE).
+ */
+GMA_API gma_status_t gma_causal_state(const gma_problem_t *p, const void *K, const void *V, const float *mu,
+                                      const float *sigma2, const float *log_pi, float *state, void *ws,
+                                      size_t ws_bytes, void *stream);
+
+/*
+ * Causal decode step: the recurrent form of the prefix sums.  For each (b, h), the N = p->N new
+ * tokens are taken in order t = 0..N-1:
+ *   state += gamma_K(k_t) [v_t | 1],   O_t = gamma_Q(q_t) . state[:, :dv] / (gamma_Q(q_t) . state[:, dv] + eps),
+ * so O_t equals the causal forward output of that position over the whole sequence seen so far.
+ * Passage: gist.science summary, "Variants and training" item 3 (causal form: O_i depends on the
+ * prefix j <= i only, through running sums).
+ *   Q, K [B,H,N,d], V [B,H,N,dv] in p->dtype; O [B,H,N,dv] in p->dtype (written);
+ *   state float32 [B][H][K][dv+1] (read and updated in place; see gma_causal_state).
+ * Computed in float32 on the CUDA cores (one CTA per (b, h)); meant for small N per call.
+ * Workspace: gma_workspace_bytes(p, GMA_OP_CAUSAL_DECODE).  O may not alias any input or state.
+ */
+GMA_API gma_status_t gma_causal_decode(const gma_problem_t *p, const void *Q, const void *K, const void *V,
+                                       const float *mu, const float *sigma2, const float *log_pi, float *state,
+                                       void *O, void *ws, size_t ws_bytes, void *stream);
 
 /*
  * Synchronises `stream`, then reads the error word kept at the start of `ws`:

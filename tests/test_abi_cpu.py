@@ -119,6 +119,70 @@ def test_forward_specific_errors(L, name):
         assert call(L, name, P(), bad) == gma.GMA_ERR_INVALID_ARG
 
 
+def call_cross(L, prob, Nk, ptrs=None, ws_bytes=1 << 30):
+    p = [A + i * (1 << 16) for i in range(8)] if ptrs is None else ptrs
+    return L.gma_forward_cross(ctypes.byref(prob), Nk, p[0], p[1], p[2], p[3], p[4], p[5], p[6], p[7], ws_bytes, None)
+
+
+def test_cross_argument_errors(L):
+    for dt in (gma.GMA_F32, gma.GMA_BF16):
+        assert gma.workspace_bytes(P(dtype=dt), gma.OP_CROSS) == gma.workspace_bytes(P(dtype=dt), gma.OP_BIDIR)
+    assert call_cross(L, P(), -1) == gma.GMA_ERR_INVALID_ARG
+    assert call_cross(L, P(d=32), 16) == gma.GMA_ERR_UNSUPPORTED
+    assert call_cross(L, P(B=1 << 8, H=1 << 8), 1 << 15) == gma.GMA_ERR_UNSUPPORTED
+    ptrs = [A + i * (1 << 16) for i in range(8)]
+    for i in (1, 2):  # K / V needed when Nk > 0
+        bad = list(ptrs); bad[i] = None
+        assert call_cross(L, P(), 7, bad) == gma.GMA_ERR_INVALID_ARG
+        bad = list(ptrs); bad[i] += 8
+        assert call_cross(L, P(), 7, bad) == gma.GMA_ERR_INVALID_ARG
+    for i in (0, 1, 2):
+        bad = list(ptrs); bad[6] = bad[i]
+        assert call_cross(L, P(), 7, bad) == gma.GMA_ERR_INVALID_ARG
+    need = gma.workspace_bytes(P(), gma.OP_CROSS)
+    assert call_cross(L, P(), 7, ws_bytes=need - 1) == gma.GMA_ERR_WORKSPACE
+    # no queries: a no-op, every tensor may be null
+    nul = [None, None, None, A + 3 * (1 << 16), A + 4 * (1 << 16), A + 5 * (1 << 16), None, A + 7 * (1 << 16)]
+    assert call_cross(L, P(N=0), 5, nul, ws_bytes=need) == gma.GMA_OK
+
+
+def test_state_and_decode_argument_errors(L):
+    assert L.gma_state_bytes(ctypes.byref(P(B=2, H=3, K=17))) == 2 * 3 * 17 * 65 * 4
+    assert L.gma_state_bytes(ctypes.byref(P(d=32))) == 0
+    for op in (gma.OP_CAUSAL_STATE, gma.OP_CAUSAL_DECODE):
+        for dt in (gma.GMA_F32, gma.GMA_BF16):
+            n = gma.workspace_bytes(P(dtype=dt), op)
+            assert n > 0 and n % 256 == 0
+    assert gma.workspace_bytes(P(), 6) == 0
+    ptr = [A + i * (1 << 16) for i in range(10)]
+
+    def st(prob, p=ptr, ws_bytes=1 << 30):  # K, V, mu, sigma2, log_pi, state, ws
+        return L.gma_causal_state(ctypes.byref(prob), p[1], p[2], p[3], p[4], p[5], p[8], p[7], ws_bytes, None)
+
+    def dec(prob, p=ptr, ws_bytes=1 << 30):  # Q, K, V, mu, sigma2, log_pi, state, O, ws
+        return L.gma_causal_decode(ctypes.byref(prob), p[0], p[1], p[2], p[3], p[4], p[5], p[8], p[6], p[7],
+                                   ws_bytes, None)
+
+    for f in (st, dec):
+        assert f(P(d=32)) == gma.GMA_ERR_UNSUPPORTED
+        assert f(P(K=0)) == gma.GMA_ERR_INVALID_ARG
+        for i in (1, 2, 3, 8):
+            bad = list(ptr); bad[i] = None
+            assert f(P(), bad) == gma.GMA_ERR_INVALID_ARG
+            bad = list(ptr); bad[i] += 4
+            assert f(P(), bad) == gma.GMA_ERR_INVALID_ARG
+        bad = list(ptr); bad[7] += 16
+        assert f(P(), bad) == gma.GMA_ERR_INVALID_ARG
+    assert st(P(), ws_bytes=gma.workspace_bytes(P(), gma.OP_CAUSAL_STATE) - 1) == gma.GMA_ERR_WORKSPACE
+    assert dec(P(), ws_bytes=gma.workspace_bytes(P(), gma.OP_CAUSAL_DECODE) - 1) == gma.GMA_ERR_WORKSPACE
+    for i in (0, 1, 2, 8):  # output aliasing an input or the state
+        bad = list(ptr); bad[6] = bad[i]
+        assert dec(P(), bad) == gma.GMA_ERR_INVALID_ARG
+    # no new tokens: a no-op; Q, K, V and O may be null
+    nul = [None, None, None] + ptr[3:6] + [None] + ptr[7:]
+    assert dec(P(N=0), nul) == gma.GMA_OK
+
+
 def test_check_device_error_rejects_bad_workspace(L):
     assert L.gma_check_device_error(None, None) == gma.GMA_ERR_INVALID_ARG
     assert L.gma_check_device_error(A + 16, None) == gma.GMA_ERR_INVALID_ARG
