@@ -63,7 +63,7 @@ gma_status_t validate_problem(const gma_problem_t* p) {
 
 size_t required_bytes(const gma_problem_t& p, gma_op_t op) {
   if (op == GMA_OP_CROSS) op = GMA_OP_BIDIR;  // the same workspace: it does not depend on N
-  if (op == GMA_OP_CAUSAL_DECODE) return simt_plan(p, GMA_OP_RESPONSIBILITIES).total;  // parameters only
+  if (op == GMA_OP_CAUSAL_DECODE) return align_up(sizeof(Ctrl));  // a control block; the kernel needs no scratch
   if (p.dtype == GMA_BF16) return tc_plan(p, op).total;
   return simt_plan(p, op).total;
 }

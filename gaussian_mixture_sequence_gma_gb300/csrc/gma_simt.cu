@@ -325,11 +325,13 @@ __global__ void __launch_bounds__(kThreads) simt_causal_kernel(const IO* __restr
 
 // ----------------------------------------------------------------------------------------------- decode
 // Causal decode: the recurrent form of the prefix sums ("Variants and training" item 3).  One CTA per
-// (b, h) holds that head's state S [K][dv + 1] in shared memory and takes its T new tokens in order:
+// (b, h) holds that head's state S [K][dv + 1] and its parameters in shared memory and takes its T new
+// tokens in order:
 //   S_k += gamma_K(k_t)_k [v_t | 1],   o_t = gamma_Q(q_t) . S[:, :dv] / (gamma_Q(q_t) . S[:, dv] + eps),
 // so token t sees every earlier key and itself (inclusive), exactly as the causal forward does.
 // Thread k < K owns component k (log-density, state row); the read splits the 64 value columns over
-// four groups of components.  float32 throughout; the state is read once and written back once.
+// four groups of components.  float32 throughout; the state is read once and written back once, and
+// the parameters are folded in the prologue (one launch per call).
 constexpr int kDecodeThreads = 256;
 
 __device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) {
@@ -347,23 +349,32 @@ __device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) 
   return r;
 }
 
+// Shared-memory floats of the decode kernel for K components.
+__host__ __device__ constexpr size_t decode_smem_floats(int K) {
+  return (size_t)K * kStateCols + 2 * (size_t)kD * (K + 1) + 2 * (size_t)K + 2 * kD + kDv + 4 * kDv + 32;
+}
+
 template <typename IO>
 __global__ void __launch_bounds__(kDecodeThreads) simt_decode_kernel(const IO* __restrict__ Q, const IO* __restrict__ Kx,
-                                                                     const IO* __restrict__ V, const float* params, int H,
-                                                                     int Tn, int K, float* __restrict__ state, float eps,
+                                                                     const IO* __restrict__ V,
+                                                                     const float* __restrict__ mu,
+                                                                     const float* __restrict__ sigma2,
+                                                                     const float* __restrict__ log_pi, int H, int Tn,
+                                                                     int K, float* __restrict__ state, float eps,
                                                                      IO* __restrict__ out) {
   extern __shared__ float sm[];
   const int bh = blockIdx.x, h = bh % H, k = threadIdx.x;
-  float* S = sm;                          // [K][kStateCols]
-  float* xq = S + (size_t)K * kStateCols;  // [kD]
-  float* xk = xq + kD;                     // [kD]
-  float* xv = xk + kD;                     // [kDv]
-  float* gq = xv + kDv;                    // [K]
-  float* part = gq + K;                    // [4][kDv]
-  float* red = part + 4 * kDv;             // [32]
-  SimtParams P = params_at(const_cast<float*>(params), H, K);
-  const float* mu_t = P.mu_t + (size_t)h * kD * K;
-  const float* w_t = P.w_t + (size_t)h * kD * K;
+  const int ld = K + 1;                     // row stride of the parameter tables (conflict-free both ways)
+  float* S = sm;                            // [K][kStateCols]
+  float* mu_s = S + (size_t)K * kStateCols;  // [kD][K + 1]
+  float* w_s = mu_s + (size_t)kD * ld;       // [kD][K + 1]  1 / sigma2
+  float* c_s = w_s + (size_t)kD * ld;        // [K]
+  float* gq = c_s + K;                       // [K]
+  float* xq = gq + K;                        // [kD]
+  float* xk = xq + kD;                       // [kD]
+  float* xv = xk + kD;                       // [kDv]
+  float* part = xv + kDv;                    // [4][kDv]
+  float* red = part + 4 * kDv;               // [32]
   float* st = state + (size_t)bh * K * kStateCols;
   const int n_state = K * kStateCols;
   // float4 copies when this head's state starts on a 16-byte boundary (K a multiple of 4), so that
@@ -377,7 +388,34 @@ __global__ void __launch_bounds__(kDecodeThreads) simt_decode_kernel(const IO* _
 #pragma unroll 8
     for (int i = threadIdx.x; i < n_state; i += blockDim.x) S[i] = __ldcg(st + i);
   }
-  const float ck = k < K ? __ldg(P.c + (size_t)h * K + k) : 0.f;
+  // parameters of head h, transposed to [dim][component], and c_k = log pi_k - 1/2 sum_d log sigma2_kd:
+  // each thread takes 4 dims of one component per float4 pair; the 16 threads of a component (an
+  // aligned half-warp) add their log-variances with shuffles.  The trip count is warp-uniform.
+  const float4* mu4 = reinterpret_cast<const float4*>(mu + (size_t)h * K * kD);
+  const float4* s24 = reinterpret_cast<const float4*>(sigma2 + (size_t)h * K * kD);
+  const int n4 = K * (kD / 4), base = threadIdx.x & ~31;
+  for (int i0 = base; i0 < n4; i0 += blockDim.x) {
+    const int i4 = i0 + (threadIdx.x & 31);
+    const bool on = i4 < n4;  // whole aligned groups of 16 (n4 is a multiple of 16)
+    const int kk = i4 >> 4, j0 = (i4 & 15) << 2;
+    float lg = 0.f;
+    if (on) {
+      const float4 m = __ldg(mu4 + i4), v = __ldg(s24 + i4);
+      mu_s[(size_t)(j0 + 0) * ld + kk] = m.x;
+      mu_s[(size_t)(j0 + 1) * ld + kk] = m.y;
+      mu_s[(size_t)(j0 + 2) * ld + kk] = m.z;
+      mu_s[(size_t)(j0 + 3) * ld + kk] = m.w;
+      w_s[(size_t)(j0 + 0) * ld + kk] = 1.0f / v.x;
+      w_s[(size_t)(j0 + 1) * ld + kk] = 1.0f / v.y;
+      w_s[(size_t)(j0 + 2) * ld + kk] = 1.0f / v.z;
+      w_s[(size_t)(j0 + 3) * ld + kk] = 1.0f / v.w;
+      lg = (logf(v.x) + logf(v.y)) + (logf(v.z) + logf(v.w));
+    }
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) lg += __shfl_xor_sync(0xffffffffu, lg, o);
+    if (on && (i4 & 15) == 0) c_s[kk] = __ldg(log_pi + (size_t)h * K + kk) - 0.5f * lg;
+  }
+  __syncthreads();
   for (int t = 0; t < Tn; ++t) {
     const size_t row = (size_t)bh * Tn + t;
     if (threadIdx.x < kD) {
@@ -390,15 +428,15 @@ __global__ void __launch_bounds__(kDecodeThreads) simt_decode_kernel(const IO* _
     float lk = -INFINITY, lq = -INFINITY;
     if (k < K) {
       float ak = 0.f, aq = 0.f;
-#pragma unroll 16
-      for (int j = 0; j < kD; ++j) {  // unrolled so that the parameter loads of 16 dims are in flight together
-        const float m = __ldg(mu_t + (size_t)j * K + k), w = __ldg(w_t + (size_t)j * K + k);
+#pragma unroll 8
+      for (int j = 0; j < kD; ++j) {
+        const float m = mu_s[(size_t)j * ld + k], w = w_s[(size_t)j * ld + k];
         const float dk = xk[j] - m, dq = xq[j] - m;
         ak = fmaf(dk * w, dk, ak);
         aq = fmaf(dq * w, dq, aq);
       }
-      lk = ck - 0.5f * ak;
-      lq = ck - 0.5f * aq;
+      lk = c_s[k] - 0.5f * ak;
+      lq = c_s[k] - 0.5f * aq;
     }
     const float mk = block_reduce(lk, true, red), mq = block_reduce(lq, true, red);
     const float ek = k < K ? expf(lk - mk) : 0.f, eq = k < K ? expf(lq - mq) : 0.f;
@@ -407,6 +445,7 @@ __global__ void __launch_bounds__(kDecodeThreads) simt_decode_kernel(const IO* _
     if (k < K) {
       const float g = ek / sk;
       float* Sk = S + (size_t)k * kStateCols;
+#pragma unroll 8
       for (int j = 0; j < kDv; ++j) Sk[j] = fmaf(g, xv[j], Sk[j]);
       Sk[kDv] += g;
       gq[k] = eq / sq;
@@ -415,8 +454,8 @@ __global__ void __launch_bounds__(kDecodeThreads) simt_decode_kernel(const IO* _
     // read: numerator column j over component group g4, denominator over all components
     {
       const int j = threadIdx.x & (kDv - 1), g4 = threadIdx.x >> 6;
-      float acc = 0.f;
       const int k1 = min(K, g4 * 64 + 64);
+      float acc = 0.f;
 #pragma unroll 8
       for (int kk = g4 * 64; kk < k1; ++kk) acc = fmaf(gq[kk], S[(size_t)kk * kStateCols + j], acc);
       part[g4 * kDv + j] = acc;
@@ -441,28 +480,23 @@ __global__ void __launch_bounds__(kDecodeThreads) simt_decode_kernel(const IO* _
 
 }  // namespace
 
-// Decode T new tokens per (b, h) from `state` (float32 [B*H][K][dv + 1], updated in place).
+// Decode T new tokens per (b, h) from `state` (float32 [B*H][K][dv + 1], updated in place).  One launch;
+// the workspace is not used (its error word stays as the caller left it).
 gma_status_t simt_decode(const gma_problem_t& p, const void* Q, const void* K, const void* V, const float* mu,
-                         const float* sigma2, const float* log_pi, float* state, void* out, void* ws,
+                         const float* sigma2, const float* log_pi, float* state, void* out, void* /*ws*/,
                          cudaStream_t st) {
-  const SimtPlan pl = simt_plan(p, GMA_OP_RESPONSIBILITIES);  // parameters only
-  char* base = (char*)ws;
-  float* params = (float*)(base + pl.off_params);
-  GMA_LAUNCH("simt_prep", simt_prep_kernel, 148, 256, 0, st, mu, sigma2, log_pi, p.H, p.K, params, (Ctrl*)base,
-             (float*)nullptr, (size_t)0);
-  if (gma_status_t e = check_launch("launch simt_prep", (const void*)simt_prep_kernel)) return e;
-  const size_t smem = ((size_t)p.K * kStateCols + 2 * kD + kDv + p.K + 4 * kDv + 32) * sizeof(float);
+  const size_t smem = decode_smem_floats(p.K) * sizeof(float);
   const int BH = p.B * p.H;
   if (p.dtype == GMA_F32) {
     if (set_smem_optin((const void*)simt_decode_kernel<float>, (int)smem, 4) != GMA_OK) return GMA_ERR_CUDA;
     GMA_LAUNCH("simt_decode", simt_decode_kernel<float>, BH, kDecodeThreads, smem, st, (const float*)Q,
-               (const float*)K, (const float*)V, params, p.H, p.N, p.K, state, p.eps, (float*)out);
+               (const float*)K, (const float*)V, mu, sigma2, log_pi, p.H, p.N, p.K, state, p.eps, (float*)out);
     return check_launch("launch simt_decode", (const void*)simt_decode_kernel<float>);
   }
   if (set_smem_optin((const void*)simt_decode_kernel<__nv_bfloat16>, (int)smem, 4) != GMA_OK) return GMA_ERR_CUDA;
   GMA_LAUNCH("simt_decode", simt_decode_kernel<__nv_bfloat16>, BH, kDecodeThreads, smem, st,
-             (const __nv_bfloat16*)Q, (const __nv_bfloat16*)K, (const __nv_bfloat16*)V, params, p.H, p.N, p.K, state,
-             p.eps, (__nv_bfloat16*)out);
+             (const __nv_bfloat16*)Q, (const __nv_bfloat16*)K, (const __nv_bfloat16*)V, mu, sigma2, log_pi, p.H,
+             p.N, p.K, state, p.eps, (__nv_bfloat16*)out);
   return check_launch("launch simt_decode", (const void*)simt_decode_kernel<__nv_bfloat16>);
 }
 
