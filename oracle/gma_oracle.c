@@ -18,6 +18,12 @@
  *   [Rd] Read phase: same section, item 2: O = Gamma_Q Vt / (Gamma_Q Z + eps).
  *   [C]  Causal variant: "Variants and training" item 3: prefix sums of the
  *        latent memory and the normaliser so that O_i depends on j <= i only.
+ *   [B]  Backward pass: "Variants and training" item 3 (the Gaussian
+ *        components are parameterised differentiably and learned end to end by
+ *        backpropagation through this path): gradients of a loss L with respect
+ *        to Q, K, V, mu, sigma2 and log pi given dL/dO, bidirectional form, by
+ *        the chain rule through [Rd], [W] and [R] (written out at
+ *        gma_oracle_backward_bidir below).
  *   [X]  Cross-attention: gist.science summary, "Significance and claims",
  *        closing paragraph (cross-attention applications named as future work
  *        beyond the self-attention setting): queries of one sequence read
@@ -240,6 +246,117 @@ int gma_oracle_forward_cross(int B, int H, int N, int Nk, int d, int dv, int K, 
   J.Q = Q; J.Kx = Kx; J.V = V; J.mu = mu; J.sigma2 = sigma2; J.log_pi = log_pi; J.eps = eps;
   J.rows = rows; J.nrows = nrows; J.out = O; J.nthreads = nthreads;
   return run_job(&J);
+}
+
+/* [B] Gradients of the bidirectional forward, given G = dL/dO [B,H,N,dv].
+ * Per (b, h), with gamma rows from [R], Vt = Gamma_K^T V, Z = Gamma_K^T 1, n_i = gamma_Qi . Vt,
+ * den_i = gamma_Qi . Z + eps, O_i = n_i / den_i:
+ *   dn_i = G_i / den_i,  dden_i = -(G_i . O_i) / den_i
+ *   dgamma_Qi = Vt dn_i + Z dden_i,       dVt = sum_i gamma_Qi dn_i^T,   dZ = sum_i gamma_Qi dden_i
+ *   dgamma_Kj = dVt v_j + dZ,             dv_j = dVt^T gamma_Kj
+ *   softmax: dl = gamma * (dgamma - gamma . dgamma)
+ *   l_k(x) = log pi_k - 1/2 sum_d [(x_d - mu_kd)^2 / sigma2_kd + log sigma2_kd] - (d/2) log 2pi:
+ *     dx_d += dl_k (mu_kd - x_d) / sigma2_kd,  dmu_kd += dl_k (x_d - mu_kd) / sigma2_kd,
+ *     dsigma2_kd += dl_k (1/2) [(x_d - mu_kd)^2 / sigma2_kd^2 - 1 / sigma2_kd],  dlog_pi_k += dl_k,
+ * with the parameter gradients summed over every query and key row of every batch entry of the
+ * head.  Sequential over (b, h) units (deterministic sums); small problems only. */
+static void softmax_backward(int K, const double *g, const double *dg, double *dl) {
+  double dot = 0.0;
+  for (int k = 0; k < K; ++k) dot += g[k] * dg[k];
+  for (int k = 0; k < K; ++k) dl[k] = g[k] * (dg[k] - dot);
+}
+
+static void logdensity_backward(int d, int K, const double *x, const double *mu, const double *sigma2,
+                                const double *dl, double *dx, double *dmu, double *ds2, double *dlp) {
+  for (int j = 0; j < d; ++j) dx[j] = 0.0;
+  for (int k = 0; k < K; ++k) {
+    dlp[k] += dl[k];
+    for (int j = 0; j < d; ++j) {
+      const double s2 = sigma2[(size_t)k * d + j];
+      const double diff = x[j] - mu[(size_t)k * d + j];
+      dx[j] += dl[k] * (-diff / s2);
+      dmu[(size_t)k * d + j] += dl[k] * (diff / s2);
+      ds2[(size_t)k * d + j] += dl[k] * 0.5 * (diff * diff / (s2 * s2) - 1.0 / s2);
+    }
+  }
+}
+
+int gma_oracle_backward_bidir(int B, int H, int N, int d, int dv, int K, const double *Q, const double *Kx,
+                              const double *V, const double *mu, const double *sigma2, const double *log_pi,
+                              double eps, const double *G, double *dQ, double *dK, double *dV, double *dmu,
+                              double *dsigma2, double *dlog_pi) {
+  double *gq = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1) * K);
+  double *gk = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1) * K);
+  double *ld = (double *)malloc(sizeof(double) * K);
+  double *Vt = (double *)malloc(sizeof(double) * (size_t)K * dv), *Z = (double *)malloc(sizeof(double) * K);
+  double *dVt = (double *)malloc(sizeof(double) * (size_t)K * dv), *dZ = (double *)malloc(sizeof(double) * K);
+  double *dn = (double *)malloc(sizeof(double) * dv), *dg = (double *)malloc(sizeof(double) * K);
+  double *dl = (double *)malloc(sizeof(double) * K), *On = (double *)malloc(sizeof(double) * dv);
+  memset(dmu, 0, sizeof(double) * (size_t)H * K * d);
+  memset(dsigma2, 0, sizeof(double) * (size_t)H * K * d);
+  memset(dlog_pi, 0, sizeof(double) * (size_t)H * K);
+  for (int u = 0; u < B * H; ++u) {
+    const int h = u % H;
+    const double *mu_h = mu + (size_t)h * K * d, *s2_h = sigma2 + (size_t)h * K * d, *lp_h = log_pi + (size_t)h * K;
+    double *dmu_h = dmu + (size_t)h * K * d, *ds2_h = dsigma2 + (size_t)h * K * d, *dlp_h = dlog_pi + (size_t)h * K;
+    const double *q = Q + (size_t)u * N * d, *kx = Kx + (size_t)u * N * d, *v = V + (size_t)u * N * dv;
+    const double *g = G + (size_t)u * N * dv;
+    log_determinants(d, K, s2_h, ld);
+    memset(Vt, 0, sizeof(double) * (size_t)K * dv);
+    memset(Z, 0, sizeof(double) * K);
+    memset(dVt, 0, sizeof(double) * (size_t)K * dv);
+    memset(dZ, 0, sizeof(double) * K);
+    for (int j = 0; j < N; ++j) {
+      posterior(d, K, kx + (size_t)j * d, mu_h, s2_h, ld, lp_h, gk + (size_t)j * K);
+      for (int k = 0; k < K; ++k) {
+        Z[k] += gk[(size_t)j * K + k];
+        for (int c = 0; c < dv; ++c) Vt[(size_t)k * dv + c] += gk[(size_t)j * K + k] * v[(size_t)j * dv + c];
+      }
+    }
+    /* queries: recompute O_i, push G_i back through the read */
+    for (int i = 0; i < N; ++i) {
+      const double *gqi = gq + (size_t)i * K;
+      posterior(d, K, q + (size_t)i * d, mu_h, s2_h, ld, lp_h, gq + (size_t)i * K);
+      double den = eps;
+      for (int k = 0; k < K; ++k) den += gqi[k] * Z[k];
+      double gdoto = 0.0;
+      for (int c = 0; c < dv; ++c) {
+        double num = 0.0;
+        for (int k = 0; k < K; ++k) num += gqi[k] * Vt[(size_t)k * dv + c];
+        On[c] = num / den;
+        gdoto += g[(size_t)i * dv + c] * On[c];
+      }
+      const double dden = -gdoto / den;
+      for (int c = 0; c < dv; ++c) dn[c] = g[(size_t)i * dv + c] / den;
+      for (int k = 0; k < K; ++k) {
+        double s = Z[k] * dden;
+        for (int c = 0; c < dv; ++c) s += Vt[(size_t)k * dv + c] * dn[c];
+        dg[k] = s;
+        dZ[k] += gqi[k] * dden;
+        for (int c = 0; c < dv; ++c) dVt[(size_t)k * dv + c] += gqi[k] * dn[c];
+      }
+      softmax_backward(K, gqi, dg, dl);
+      logdensity_backward(d, K, q + (size_t)i * d, mu_h, s2_h, dl, dQ + ((size_t)u * N + i) * d, dmu_h, ds2_h, dlp_h);
+    }
+    /* keys: push dVt, dZ back through the write */
+    for (int j = 0; j < N; ++j) {
+      const double *gkj = gk + (size_t)j * K;
+      for (int k = 0; k < K; ++k) {
+        double s = dZ[k];
+        for (int c = 0; c < dv; ++c) s += dVt[(size_t)k * dv + c] * v[(size_t)j * dv + c];
+        dg[k] = s;
+      }
+      for (int c = 0; c < dv; ++c) {
+        double s = 0.0;
+        for (int k = 0; k < K; ++k) s += gkj[k] * dVt[(size_t)k * dv + c];
+        dV[((size_t)u * N + j) * dv + c] = s;
+      }
+      softmax_backward(K, gkj, dg, dl);
+      logdensity_backward(d, K, kx + (size_t)j * d, mu_h, s2_h, dl, dK + ((size_t)u * N + j) * d, dmu_h, ds2_h, dlp_h);
+    }
+  }
+  free(gq); free(gk); free(ld); free(Vt); free(Z); free(dVt); free(dZ); free(dn); free(dg); free(dl); free(On);
+  return 0;
 }
 
 /* Latent memory Vt [B,H,K,dv] and normaliser Z [B,H,K] over all N keys ([W]). */

@@ -13,6 +13,10 @@ code:
 * invariants (permutations, prior shift, mass conservation, convex hull,
   rank <= K).
 
+The backward pass (gradients given dL/dO; "Variants and training" item 3:
+the components are learned by backpropagation) is pinned by central finite
+differences of the forward oracle, element by element.
+
 Cross-attention (N queries reading the memory of Nk keys; gist.science
 summary, "Significance and claims": cross-attention named as future work) is
 pinned the same way: the materialised N x Nk affinity, the K = 1 mean, no
@@ -325,6 +329,59 @@ def test_cross_key_permutation_invariance():
     assert np.abs(O1 - O2).max() <= 1e-12
 
 
+# ----------------------------------------------------------------------------- backward
+
+def _fd_grads(Q, Kx, V, mu, sigma2, log_pi, eps, G, h=1e-6, lib=None):
+    """Central finite differences of L = sum(O * G) through the forward oracle, every element."""
+    args = [Q, Kx, V, mu, sigma2, log_pi]
+    out = []
+    for a in range(6):
+        g = np.zeros_like(args[a])
+        flat = g.reshape(-1)
+        for idx in range(flat.size):
+            vals = [x.copy() for x in args]
+            step = h * max(1.0, abs(vals[a].reshape(-1)[idx]))
+            vals[a].reshape(-1)[idx] += step
+            lp = (orc.forward(*vals, eps, causal=False, lib=lib) * G).sum()
+            vals[a].reshape(-1)[idx] -= 2 * step
+            lm = (orc.forward(*vals, eps, causal=False, lib=lib) * G).sum()
+            flat[idx] = (lp - lm) / (2 * step)
+        out.append(g)
+    return out
+
+
+@pytest.mark.parametrize("eps", [1e-6, 0.37])
+def test_backward_matches_finite_differences(eps):
+    Q, Kx, V, mu, sigma2, log_pi = _small_problem(31, B=2, H=2, N=5, d=3, dv=2, K=3, smin=0.3)
+    G = _rng(32).standard_normal((2, 2, 5, 2))
+    got = orc.backward_bidir(Q, Kx, V, mu, sigma2, log_pi, eps, G)
+    want = _fd_grads(Q, Kx, V, mu, sigma2, log_pi, eps, G)
+    for name, a, b in zip(("dQ", "dK", "dV", "dmu", "dsigma2", "dlog_pi"), got, want):
+        assert a.shape == b.shape, name
+        assert np.abs(a - b).max() <= 1e-6 * max(1.0, np.abs(b).max()), name
+
+
+def test_backward_prior_gradient_sums_to_zero():
+    # shifting every log pi_k of a head by the same constant leaves O unchanged
+    Q, Kx, V, mu, sigma2, log_pi = _small_problem(33, B=1, H=2, N=9, d=4, dv=3, K=4, smin=0.3)
+    G = _rng(34).standard_normal((1, 2, 9, 3))
+    dlp = orc.backward_bidir(Q, Kx, V, mu, sigma2, log_pi, 1e-6, G)[5]
+    assert np.abs(dlp.sum(-1)).max() <= 1e-12 * max(1.0, np.abs(dlp).max())
+
+
+def test_backward_values_gradient_is_linear_read():
+    # O is linear in V: dV_j = sum_i G_i A_ij / den_i with the materialised affinity
+    Q, Kx, V, mu, sigma2, log_pi = _small_problem(35, B=1, H=1, N=7, d=4, dv=3, K=3, smin=0.3)
+    G = _rng(36).standard_normal((1, 1, 7, 3))
+    eps = 0.2
+    GQ, GK = _scipy_gamma(Q, mu, sigma2, log_pi), _scipy_gamma(Kx, mu, sigma2, log_pi)
+    A = np.einsum("bhik,bhjk->bhij", GQ, GK)
+    den = A.sum(-1, keepdims=True) + eps
+    want = np.einsum("bhij,bhic->bhjc", A / den, G)
+    dV = orc.backward_bidir(Q, Kx, V, mu, sigma2, log_pi, eps, G)[2]
+    assert np.abs(dV - want).max() <= 1e-12 * max(1.0, np.abs(want).max())
+
+
 # ----------------------------------------------------------------------------- planted mistakes
 
 MUTANTS = {
@@ -336,6 +393,9 @@ MUTANTS = {
     "cross_key_stride": ("const double *Kx = J->Kx + (size_t)unit * Nk * d;",
                          "const double *Kx = J->Kx + (size_t)unit * N * d;"),
     "cross_write_over_queries": ("for (int j = 0; j < Nk; ++j) {", "for (int j = 0; j < N && j < Nk; ++j) {"),
+    "bwd_drops_denominator_term": ("const double dden = -gdoto / den;", "const double dden = 0.0 * gdoto;"),
+    "bwd_variance_sign": ("0.5 * (diff * diff / (s2 * s2) - 1.0 / s2)", "0.5 * (diff * diff / (s2 * s2) + 1.0 / s2)"),
+    "bwd_softmax_no_centering": ("dl[k] = g[k] * (dg[k] - dot);", "dl[k] = g[k] * dg[k];"),
     "causal_drops_first_key": ("int64_t want = J->rows ? J->rows[r] : i;",
                          "int64_t want = J->rows ? J->rows[r] : i; if (i == 0) { memset(Vt, 0, sizeof(double) * K * dv); memset(Z, 0, sizeof(double) * K); }"),
 }
@@ -352,6 +412,13 @@ def _pins_pass(lib) -> bool:
         G = orc.responsibilities(Q, mu, sigma2, log_pi, lib=lib)
         if np.abs(G - _scipy_gamma(Q, mu, sigma2, log_pi)).max() > 1e-10:
             return False
+        Q, Kx, V, mu, sigma2, log_pi = _small_problem(23, B=1, H=2, N=4, d=2, dv=2, K=3, smin=0.3)
+        G = _rng(24).standard_normal((1, 2, 4, 2))
+        got = orc.backward_bidir(Q, Kx, V, mu, sigma2, log_pi, 0.37, G, lib=lib)
+        want = _fd_grads(Q, Kx, V, mu, sigma2, log_pi, 0.37, G, lib=lib)
+        for a, b in zip(got, want):
+            if np.abs(a - b).max() > 1e-6 * max(1.0, np.abs(b).max()):
+                return False
         Q, Kx, V, mu, sigma2, log_pi = _cross_problem(22, 7, 13)
         O = orc.forward_cross(Q, Kx, V, mu, sigma2, log_pi, 0.37, lib=lib)
         if np.abs(O - _brute_cross(Q, Kx, V, mu, sigma2, log_pi, 0.37)).max() > 1e-10:
