@@ -438,6 +438,25 @@ def run_gma(args, world, rank, local):
             "hbm_bound_us": t_hbm * 1e6, "frac_of_hbm_bound": t_hbm / t_step,
             "launches_per_step": 1, "timing": how}
         del di, state, wsd, toks, outd
+        # backward pass of the bidirectional form (float32 CUDA-core kernels) on the bidir bf16 workload shape
+        wb = workloads()["bidir_bf16_B4H8N4096K128"]
+        bi = to_dev(make_workload(wb), dev)
+        gO = torch.randn((wb.B, wb.H, wb.N, 64), device=dev).to(torch.bfloat16)
+        pbk = gma.problem(wb.B, wb.H, wb.N, wb.K, torch.bfloat16, wb.eps)
+        wsb = gma.alloc_workspace(pbk, gma.OP_BACKWARD_BIDIR, dev)
+        callb = lambda: gma.backward_bidir(bi["Q"], bi["K"], bi["V"], bi["mu"], bi["sigma2"], bi["log_pi"], gO, wb.eps,
+                                           workspace=wsb)
+        callf = lambda: gma.forward_bidir(bi["Q"], bi["K"], bi["V"], bi["mu"], bi["sigma2"], bi["log_pi"], wb.eps)
+        for _ in range(2):
+            callb()
+            callf()
+        mb, _ = timed(callb, 5)
+        mf, _ = timed(callf, 5)
+        extensions["backward_bidir_bf16_B4H8N4096K128"] = {
+            "ms": mb / 5, "tok_heads_per_s": wb.B * wb.H * wb.N / (mb / 5 * 1e-3), "forward_ms": mf / 5,
+            "backward_over_forward": mb / mf, "workspace_bytes": wsb.numel(),
+            "note": "float32 CUDA-core kernels (no tensor cores yet)"}
+        del bi, gO, wsb
 
     # CPU baseline: the oracle as it stands on a bounded sample of the same workload (rank 0 only)
     cpu = None

@@ -323,6 +323,255 @@ __global__ void __launch_bounds__(kThreads) simt_causal_kernel(const IO* __restr
   }
 }
 
+// ----------------------------------------------------------------------------------------------- backward
+// Gradients of the bidirectional forward ("Variants and training" item 3: the mixture is learned end to
+// end by backpropagation), float32 on the CUDA cores.  With Vt, Z from the forward write and G = dL/dO:
+//   den_i = gamma_Qi . Z + eps, O_i = gamma_Qi . Vt / den_i, dn_i = G_i / den_i, dden_i = -(G_i . O_i) / den_i,
+//   dgamma_Qi = [Vt | Z] [dn_i | dden_i],   [dVt | dZ] = sum_i gamma_Qi [dn_i | dden_i]^T,
+//   dgamma_Kj = [dVt | dZ] [v_j | 1],       dv_j = dVt^T gamma_Kj,
+//   dl = gamma * (dgamma - gamma . dgamma)  (softmax),
+//   dx_d = sum_k dl_k (mu_kd - x_d) / sigma2_kd,  and per head, over every query and key row:
+//   D1_kd = sum dl_k (x_d - mu_kd), D2_kd = sum dl_k (x_d - mu_kd)^2, b_k = sum dl_k,
+//   dmu = D1 / sigma2,  dsigma2 = (D2 / sigma2 - b) / (2 sigma2),  dlog_pi = b.
+// The per-row dl of both sides go through the workspace to the parameter-gradient pass.
+
+// dx for the T rows of xs from dl [T][K]: sum_k dl_ik w_kd (mu_kd - x_id).
+template <typename IO>
+__device__ void dx_tile(const float* xs, const float* dl, int nvalid, const SimtParams& P, int h, int K, IO* dst) {
+  const float* mu_t = P.mu_t + (size_t)h * kD * K;
+  const float* w_t = P.w_t + (size_t)h * kD * K;
+  for (int p = threadIdx.x; p < nvalid * kD; p += blockDim.x) {
+    const int i = p / kD, j = p % kD;
+    const float x = xs[i * kD + j];
+    float s = 0.f;
+    for (int k = 0; k < K; ++k) {
+      const float m = __ldg(mu_t + (size_t)j * K + k), w = __ldg(w_t + (size_t)j * K + k);
+      s = fmaf(dl[i * K + k] * w, m - x, s);
+    }
+    st_io<IO>(dst + (size_t)i * kD + j, s);
+  }
+}
+
+// Softmax backward in place: dG <- G * (dG - G . dG), one warp per row.
+__device__ void softmax_backward_tile(const float* G, float* dG, int K) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  for (int i = warp; i < T; i += nwarps) {
+    float dot = 0.f;
+    for (int k = lane; k < K; k += 32) dot = fmaf(G[i * K + k], dG[i * K + k], dot);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+    for (int k = lane; k < K; k += 32) dG[i * K + k] = G[i * K + k] * (dG[i * K + k] - dot);
+  }
+  __syncthreads();
+}
+
+// Query side: grid (splits, B*H).  Recomputes O, pushes dO back through the read, writes dQ and dl_Q,
+// and adds [dVt | dZ] into dstate[unit][K][65].
+template <typename IO>
+__global__ void __launch_bounds__(kThreads) simt_bwd_query_kernel(const IO* __restrict__ Q, const IO* __restrict__ dO,
+                                                                  float* params, int H, int N, int K, int seg_tiles,
+                                                                  const float* __restrict__ state, float eps,
+                                                                  float* dstate, float* dlq, IO* __restrict__ dQ) {
+  extern __shared__ float sm[];
+  const int npairs = K * kStateCols;
+  float* S = sm;                // [K][65]  Vt | Z
+  float* sacc = S + npairs;     // [K][65]  dVt | dZ of this CTA
+  float* xs = sacc + npairs;    // [T][64]
+  float* gs = xs + T * kD;      // [T][64]  dO rows
+  float* dn = gs + T * kDv;     // [T][65]  numerators, then dn | dden
+  float* G = dn + T * kStateCols;  // [T][K]
+  float* dG = G + T * K;        // [T][K]
+  const int unit = blockIdx.y, h = unit % H, split = blockIdx.x;
+  const SimtParams P = params_at(params, H, K);
+  const float* S0 = state + (size_t)unit * npairs;
+  for (int p = threadIdx.x; p < npairs; p += blockDim.x) {
+    S[p] = S0[p];
+    sacc[p] = 0.f;
+  }
+  const int tiles = (N + T - 1) / T;
+  const int tb = split * seg_tiles, te = min(tiles, tb + seg_tiles);
+  for (int t = tb; t < te; ++t) {
+    const int t0 = t * T, nvalid = min(T, N - t0);
+    __syncthreads();
+    load_rows<IO>(Q + (size_t)unit * N * kD, t0, nvalid, xs);
+    load_rows<IO>(dO + (size_t)unit * N * kDv, t0, nvalid, gs);
+    __syncthreads();
+    gamma_tile(xs, nvalid, P, h, K, G);
+    for (int p = threadIdx.x; p < T * kStateCols; p += blockDim.x) {  // [num | den - eps]
+      const int i = p / kStateCols, c = p % kStateCols;
+      float s = 0.f;
+      for (int k = 0; k < K; ++k) s = fmaf(G[i * K + k], S[k * kStateCols + c], s);
+      dn[p] = s;
+    }
+    __syncthreads();
+    {  // one warp per row: O, G . O, then dn | dden (rows past N have G = 0, so all zero)
+      const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+      for (int i = warp; i < T; i += nwarps) {
+        if (i >= nvalid) {  // rows past N: no gradient (and no 0 / 0 when eps = 0)
+          dn[i * kStateCols + lane] = 0.f;
+          dn[i * kStateCols + 32 + lane] = 0.f;
+          if (lane == 0) dn[i * kStateCols + kDv] = 0.f;
+          continue;
+        }
+        const float den = dn[i * kStateCols + kDv] + eps;
+        const float o0 = dn[i * kStateCols + lane] / den, o1 = dn[i * kStateCols + 32 + lane] / den;
+        float go = gs[i * kDv + lane] * o0 + gs[i * kDv + 32 + lane] * o1;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) go += __shfl_xor_sync(0xffffffffu, go, o);
+        __syncwarp();
+        dn[i * kStateCols + lane] = gs[i * kDv + lane] / den;
+        dn[i * kStateCols + 32 + lane] = gs[i * kDv + 32 + lane] / den;
+        if (lane == 0) dn[i * kStateCols + kDv] = -go / den;
+      }
+    }
+    __syncthreads();
+    for (int p = threadIdx.x; p < T * K; p += blockDim.x) {  // dgamma_Q = [Vt | Z] [dn | dden]
+      const int i = p / K, k = p % K;
+      float s = 0.f;
+      for (int c = 0; c < kStateCols; ++c) s = fmaf(dn[i * kStateCols + c], S[k * kStateCols + c], s);
+      dG[p] = s;
+    }
+    for (int p = threadIdx.x; p < npairs; p += blockDim.x) {  // [dVt | dZ] += gamma_Q^T [dn | dden]
+      const int k = p / kStateCols, c = p % kStateCols;
+      float s = 0.f;
+      for (int i = 0; i < T; ++i) s = fmaf(G[i * K + k], dn[i * kStateCols + c], s);
+      sacc[p] += s;
+    }
+    __syncthreads();
+    softmax_backward_tile(G, dG, K);
+    float* dst = dlq + ((size_t)unit * N + t0) * K;
+    for (int p = threadIdx.x; p < nvalid * K; p += blockDim.x) dst[p] = dG[p];
+    dx_tile<IO>(xs, dG, nvalid, P, h, K, dQ + ((size_t)unit * N + t0) * kD);
+  }
+  __syncthreads();
+  float* dS = dstate + (size_t)unit * npairs;
+  for (int p = threadIdx.x; p < npairs; p += blockDim.x) atomicAdd(dS + p, sacc[p]);
+}
+
+// Key side: grid (tiles, B*H).  Pushes [dVt | dZ] back through the write: dV, dK and dl_K.
+template <typename IO>
+__global__ void __launch_bounds__(kThreads) simt_bwd_key_kernel(const IO* __restrict__ Kx, const IO* __restrict__ V,
+                                                                float* params, int H, int N, int K,
+                                                                const float* __restrict__ dstate, float* dlk,
+                                                                IO* __restrict__ dK, IO* __restrict__ dV) {
+  extern __shared__ float sm[];
+  const int npairs = K * kStateCols;
+  float* dS = sm;               // [K][65]  dVt | dZ
+  float* xs = dS + npairs;      // [T][64]
+  float* vs = xs + T * kD;      // [T][64]
+  float* G = vs + T * kDv;      // [T][K]
+  float* dG = G + T * K;        // [T][K]
+  const int unit = blockIdx.y, h = unit % H;
+  const int t0 = blockIdx.x * T, nvalid = min(T, N - t0);
+  const SimtParams P = params_at(params, H, K);
+  const float* dS0 = dstate + (size_t)unit * npairs;
+  for (int p = threadIdx.x; p < npairs; p += blockDim.x) dS[p] = dS0[p];
+  load_rows<IO>(Kx + (size_t)unit * N * kD, t0, nvalid, xs);
+  load_rows<IO>(V + (size_t)unit * N * kDv, t0, nvalid, vs);
+  __syncthreads();
+  gamma_tile(xs, nvalid, P, h, K, G);
+  for (int p = threadIdx.x; p < T * K; p += blockDim.x) {  // dgamma_K = [dVt | dZ] [v | 1]
+    const int j = p / K, k = p % K;
+    float s = dS[k * kStateCols + kDv];
+    for (int c = 0; c < kDv; ++c) s = fmaf(vs[j * kDv + c], dS[k * kStateCols + c], s);
+    dG[p] = s;
+  }
+  IO* dv_out = dV + ((size_t)unit * N + t0) * kDv;
+  for (int p = threadIdx.x; p < nvalid * kDv; p += blockDim.x) {  // dv = dVt^T gamma_K
+    const int j = p / kDv, c = p % kDv;
+    float s = 0.f;
+    for (int k = 0; k < K; ++k) s = fmaf(G[j * K + k], dS[k * kStateCols + c], s);
+    st_io<IO>(dv_out + p, s);
+  }
+  __syncthreads();
+  softmax_backward_tile(G, dG, K);
+  float* dst = dlk + ((size_t)unit * N + t0) * K;
+  for (int p = threadIdx.x; p < nvalid * K; p += blockDim.x) dst[p] = dG[p];
+  dx_tile<IO>(xs, dG, nvalid, P, h, K, dK + ((size_t)unit * N + t0) * kD);
+}
+
+// Parameter-gradient sums: grid (ceil(K / 32), H, chunks).  Thread (k within a block of 32, group of 8
+// dims) sums dl_k (x_d - mu_kd) and dl_k (x_d - mu_kd)^2 over its chunk of the head's rows (queries
+// then keys of every batch entry) and adds them into pacc[h][k][d][2] (and b_k into pb[h][k]).
+template <typename IO>
+__global__ void __launch_bounds__(kThreads) simt_bwd_param_kernel(const IO* __restrict__ Q, const IO* __restrict__ Kx,
+                                                                  const float* __restrict__ mu, const float* dlq,
+                                                                  const float* dlk, int B, int H, int N, int K,
+                                                                  int rows_per_chunk, float* pacc, float* pb) {
+  __shared__ float xs[T * kD];
+  __shared__ float ds[T * 32];
+  const int h = blockIdx.y, k0 = blockIdx.x * 32;
+  const int kl = threadIdx.x & 31, dg = threadIdx.x >> 5;  // 8 groups of 8 dims
+  const int k = k0 + kl;
+  float m[8], a1[8], a2[8], bsum = 0.f;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    m[q] = k < K ? __ldg(mu + ((size_t)h * K + k) * kD + dg * 8 + q) : 0.f;
+    a1[q] = 0.f;
+    a2[q] = 0.f;
+  }
+  const long long total = 2LL * B * N;  // rows of this head: queries then keys, batch-major
+  const long long r0 = (long long)blockIdx.z * rows_per_chunk, r1 = min(total, r0 + rows_per_chunk);
+  for (long long rb = r0; rb < r1; rb += T) {
+    const int n = (int)min((long long)T, r1 - rb);
+    __syncthreads();
+    for (int p = threadIdx.x; p < T * kD; p += blockDim.x) {
+      const int i = p / kD, j = p % kD;
+      float x = 0.f;
+      if (i < n) {
+        const long long r = rb + i, side = r / ((long long)B * N), rr = r % ((long long)B * N);
+        const long long b = rr / N, tok = rr % N, unit = b * H + h;
+        const IO* src = side == 0 ? Q : Kx;
+        x = ld_io<IO>(src + ((size_t)unit * N + tok) * kD + j);
+      }
+      xs[p] = x;
+    }
+    for (int p = threadIdx.x; p < T * 32; p += blockDim.x) {
+      const int i = p / 32, kk = k0 + (p % 32);
+      float v = 0.f;
+      if (i < n && kk < K) {
+        const long long r = rb + i, side = r / ((long long)B * N), rr = r % ((long long)B * N);
+        const long long b = rr / N, tok = rr % N, unit = b * H + h;
+        const float* src = side == 0 ? dlq : dlk;
+        v = src[((size_t)unit * N + tok) * K + kk];
+      }
+      ds[p] = v;
+    }
+    __syncthreads();
+    for (int i = 0; i < n; ++i) {
+      const float dl = ds[i * 32 + kl];
+      if (dg == 0) bsum += dl;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float diff = xs[i * kD + dg * 8 + q] - m[q];
+        const float t = dl * diff;
+        a1[q] += t;
+        a2[q] = fmaf(t, diff, a2[q]);
+      }
+    }
+  }
+  if (k < K) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      float* dst = pacc + (((size_t)h * K + k) * kD + dg * 8 + q) * 2;
+      atomicAdd(dst, a1[q]);
+      atomicAdd(dst + 1, a2[q]);
+    }
+    if (dg == 0) atomicAdd(pb + (size_t)h * K + k, bsum);
+  }
+}
+
+__global__ void simt_bwd_param_finish_kernel(const float* __restrict__ sigma2, const float* pacc, const float* pb, int H,
+                                             int K, float* dmu, float* dsigma2, float* dlog_pi) {
+  const size_t n = (size_t)H * K * kD;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const float w = 1.0f / sigma2[i], b = pb[i / kD];
+    dmu[i] = pacc[2 * i] * w;
+    dsigma2[i] = 0.5f * w * (pacc[2 * i + 1] * w - b);
+    if (i % kD == 0) dlog_pi[i / kD] = b;
+  }
+}
+
 // ----------------------------------------------------------------------------------------------- decode
 // Causal decode: the recurrent form of the prefix sums ("Variants and training" item 3).  One CTA per
 // (b, h) holds that head's state S [K][dv + 1] and its parameters in shared memory and takes its T new
@@ -479,6 +728,89 @@ __global__ void __launch_bounds__(kDecodeThreads) simt_decode_kernel(const IO* _
 }
 
 }  // namespace
+
+// Workspace of the backward pass: control block | parameters | Vt|Z | dVt|dZ | parameter sums |
+// dl of the queries | dl of the keys.  The three accumulators are contiguous (zeroed together).
+struct BwdPlan {
+  size_t off_params, off_state, off_dstate, off_pacc, off_pb, off_dlq, off_dlk, total;
+  int splits, seg_tiles, tiles;
+};
+BwdPlan bwd_plan(const gma_problem_t& p) {
+  BwdPlan b{};
+  const SimtPlan sp = simt_plan(p, GMA_OP_BIDIR);
+  const size_t BH = (size_t)p.B * p.H, npairs = (size_t)p.K * kStateCols;
+  b.splits = sp.splits;
+  b.seg_tiles = sp.seg_tiles;
+  b.tiles = sp.tiles;
+  b.off_params = sp.off_params;
+  b.off_state = sp.off_state;
+  b.off_dstate = b.off_state + BH * npairs * sizeof(float);
+  b.off_pacc = b.off_dstate + BH * npairs * sizeof(float);
+  b.off_pb = b.off_pacc + (size_t)p.H * p.K * kD * 2 * sizeof(float);
+  b.off_dlq = align_up(b.off_pb + (size_t)p.H * p.K * sizeof(float));
+  b.off_dlk = align_up(b.off_dlq + BH * p.N * p.K * sizeof(float));
+  b.total = align_up(b.off_dlk + BH * p.N * p.K * sizeof(float));
+  return b;
+}
+
+template <typename IO>
+gma_status_t backward_typed(const gma_problem_t& p, const IO* Q, const IO* Kx, const IO* V, const float* mu,
+                            const float* sigma2, const float* log_pi, const IO* dO, IO* dQ, IO* dK, IO* dV, float* dmu,
+                            float* dsigma2, float* dlog_pi, void* ws, cudaStream_t st) {
+  const BwdPlan b = bwd_plan(p);
+  char* base = (char*)ws;
+  float* params = (float*)(base + b.off_params);
+  float* state = (float*)(base + b.off_state);
+  float* dstate = (float*)(base + b.off_dstate);
+  float* pacc = (float*)(base + b.off_pacc);
+  float* pb = (float*)(base + b.off_pb);
+  float* dlq = (float*)(base + b.off_dlq);
+  float* dlk = (float*)(base + b.off_dlk);
+  const int BH = p.B * p.H, K = p.K, npairs = K * kStateCols;
+  const size_t zero_n = (b.off_dlq - b.off_state) / sizeof(float);
+  GMA_LAUNCH("simt_prep", simt_prep_kernel, 148, 256, 0, st, mu, sigma2, log_pi, p.H, K, params, (Ctrl*)base, state,
+             zero_n);
+  if (gma_status_t e = check_launch("launch simt_prep", (const void*)simt_prep_kernel)) return e;
+  if (p.N > 0) {
+    const size_t sm_write = (size_t)(T * kD + T * kDv + T * K + npairs) * sizeof(float);
+    if (set_smem_optin((const void*)simt_write_kernel<IO>, (int)sm_write, 1) != GMA_OK) return GMA_ERR_CUDA;
+    GMA_LAUNCH("simt_write", simt_write_kernel<IO>, dim3(b.splits, BH), kThreads, sm_write, st, Kx, V, params, p.H,
+               p.N, K, b.seg_tiles, b.splits, state, 1);
+    if (gma_status_t e = check_launch("launch simt_write", (const void*)simt_write_kernel<IO>)) return e;
+    const size_t sm_q = (size_t)(2 * npairs + T * kD + T * kDv + T * kStateCols + 2 * T * K) * sizeof(float);
+    if (set_smem_optin((const void*)simt_bwd_query_kernel<IO>, (int)sm_q, 5) != GMA_OK) return GMA_ERR_CUDA;
+    GMA_LAUNCH("simt_bwd_query", simt_bwd_query_kernel<IO>, dim3(b.splits, BH), kThreads, sm_q, st, Q, dO, params,
+               p.H, p.N, K, b.seg_tiles, state, p.eps, dstate, dlq, dQ);
+    if (gma_status_t e = check_launch("launch simt_bwd_query", (const void*)simt_bwd_query_kernel<IO>)) return e;
+    const size_t sm_k = (size_t)(npairs + T * kD + T * kDv + 2 * T * K) * sizeof(float);
+    if (set_smem_optin((const void*)simt_bwd_key_kernel<IO>, (int)sm_k, 6) != GMA_OK) return GMA_ERR_CUDA;
+    GMA_LAUNCH("simt_bwd_key", simt_bwd_key_kernel<IO>, dim3(b.tiles, BH), kThreads, sm_k, st, Kx, V, params, p.H,
+               p.N, K, dstate, dlk, dK, dV);
+    if (gma_status_t e = check_launch("launch simt_bwd_key", (const void*)simt_bwd_key_kernel<IO>)) return e;
+    const int rows_per_chunk = 2048;
+    const long long rows = 2LL * p.B * p.N;
+    const dim3 grid_p(cdiv(K, 32), p.H, cdiv(rows, rows_per_chunk));
+    GMA_LAUNCH("simt_bwd_param", simt_bwd_param_kernel<IO>, grid_p, kThreads, 0, st, Q, Kx, mu, dlq, dlk, p.B, p.H, p.N,
+               K, rows_per_chunk, pacc, pb);
+    if (gma_status_t e = check_launch("launch simt_bwd_param", (const void*)simt_bwd_param_kernel<IO>)) return e;
+  }
+  GMA_LAUNCH("simt_bwd_param_finish", simt_bwd_param_finish_kernel, 148, 256, 0, st, sigma2, pacc, pb, p.H, K, dmu,
+             dsigma2, dlog_pi);
+  return check_launch("launch simt_bwd_param_finish", (const void*)simt_bwd_param_finish_kernel);
+}
+
+size_t simt_backward_bytes(const gma_problem_t& p) { return bwd_plan(p).total; }
+
+gma_status_t simt_backward(const gma_problem_t& p, const void* Q, const void* K, const void* V, const float* mu,
+                           const float* sigma2, const float* log_pi, const void* dO, void* dQ, void* dK, void* dV,
+                           float* dmu, float* dsigma2, float* dlog_pi, void* ws, cudaStream_t st) {
+  if (p.dtype == GMA_F32)
+    return backward_typed<float>(p, (const float*)Q, (const float*)K, (const float*)V, mu, sigma2, log_pi,
+                                 (const float*)dO, (float*)dQ, (float*)dK, (float*)dV, dmu, dsigma2, dlog_pi, ws, st);
+  using bf = __nv_bfloat16;
+  return backward_typed<bf>(p, (const bf*)Q, (const bf*)K, (const bf*)V, mu, sigma2, log_pi, (const bf*)dO, (bf*)dQ,
+                            (bf*)dK, (bf*)dV, dmu, dsigma2, dlog_pi, ws, st);
+}
 
 // Decode T new tokens per (b, h) from `state` (float32 [B*H][K][dv + 1], updated in place).  One launch;
 // the workspace is not used (its error word stays as the caller left it).

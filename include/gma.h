@@ -73,7 +73,8 @@ typedef enum {
   GMA_OP_CAUSAL = 2,
   GMA_OP_CROSS = 3,
   GMA_OP_CAUSAL_STATE = 4,
-  GMA_OP_CAUSAL_DECODE = 5
+  GMA_OP_CAUSAL_DECODE = 5,
+  GMA_OP_BACKWARD_BIDIR = 6
 } gma_op_t;
 
 typedef struct {
@@ -196,6 +197,27 @@ GMA_API gma_status_t gma_causal_state(const gma_problem_t *p, const void *K, con
 GMA_API gma_status_t gma_causal_decode(const gma_problem_t *p, const void *Q, const void *K, const void *V,
                                        const float *mu, const float *sigma2, const float *log_pi, float *state,
                                        void *O, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Backward pass of the bidirectional forward: given dO = dL/dO, the gradients of L with respect to
+ * every input and parameter,
+ *   dQ, dK [B,H,N,d], dV [B,H,N,dv] in p->dtype (written);
+ *   dmu, dsigma2 [H,K,d], dlog_pi [H,K] float32 (written; summed over the batch and over every
+ *   query and key row, since one mixture per head routes both).
+ * Passage: gist.science summary, "Variants and training" item 3 (the Gaussian components are
+ * parameterised differentiably and trained end to end); the chain rule runs back through the read
+ * and write phases of "Core mechanism" item 2 and the GMM posterior of item 1.  The gradient with
+ * respect to sigma2 and log_pi is the one of this function's inputs: a caller that reparameterises
+ * (softplus, log-softmax) applies its own chain rule on top.
+ *   Q, K, V, mu, sigma2, log_pi, eps: as gma_forward_bidir;  dO [B,H,N,dv] in p->dtype.
+ * Computed in float32 on the CUDA cores.  The workspace, gma_workspace_bytes(p,
+ * GMA_OP_BACKWARD_BIDIR), grows with N (it holds the per-row softmax gradients, 8 B*H*N*K bytes).
+ * No output may alias an input.
+ */
+GMA_API gma_status_t gma_backward_bidir(const gma_problem_t *p, const void *Q, const void *K, const void *V,
+                                        const float *mu, const float *sigma2, const float *log_pi, const void *dO,
+                                        void *dQ, void *dK, void *dV, float *dmu, float *dsigma2, float *dlog_pi,
+                                        void *ws, size_t ws_bytes, void *stream);
 
 /*
  * Synchronises `stream`, then reads the error word kept at the start of `ws`:
