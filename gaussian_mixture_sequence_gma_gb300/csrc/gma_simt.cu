@@ -335,20 +335,33 @@ __global__ void __launch_bounds__(kThreads) simt_causal_kernel(const IO* __restr
 //   dmu = D1 / sigma2,  dsigma2 = (D2 / sigma2 - b) / (2 sigma2),  dlog_pi = b.
 // The per-row dl of both sides go through the workspace to the parameter-gradient pass.
 
-// dx for the T rows of xs from dl [T][K]: sum_k dl_ik w_kd (mu_kd - x_id).
+// dx for the T rows of xs from dl [T][K]: sum_k dl_ik w_kd (mu_kd - x_id) = (dl (w mu))_id - x_id (dl w)_id.
+// Thread (column j, row group) walks k reading mu[h][k][j] and sigma2[h][k][j] (consecutive j across a
+// warp: coalesced) and updates its T / 4 rows.
 template <typename IO>
-__device__ void dx_tile(const float* xs, const float* dl, int nvalid, const SimtParams& P, int h, int K, IO* dst) {
-  const float* mu_t = P.mu_t + (size_t)h * kD * K;
-  const float* w_t = P.w_t + (size_t)h * kD * K;
-  for (int p = threadIdx.x; p < nvalid * kD; p += blockDim.x) {
-    const int i = p / kD, j = p % kD;
-    const float x = xs[i * kD + j];
-    float s = 0.f;
-    for (int k = 0; k < K; ++k) {
-      const float m = __ldg(mu_t + (size_t)j * K + k), w = __ldg(w_t + (size_t)j * K + k);
-      s = fmaf(dl[i * K + k] * w, m - x, s);
+__device__ void dx_tile(const float* xs, const float* dl, int nvalid, const float* __restrict__ mu,
+                        const float* __restrict__ sigma2, int h, int K, IO* dst) {
+  constexpr int kRowGroups = kThreads / kD;  // 4
+  constexpr int kRows = T / kRowGroups;      // 8 rows per thread
+  const int j = threadIdx.x % kD, rg = threadIdx.x / kD;
+  const float* muh = mu + (size_t)h * K * kD + j;
+  const float* s2h = sigma2 + (size_t)h * K * kD + j;
+  float a1[kRows], a2[kRows];
+#pragma unroll
+  for (int r = 0; r < kRows; ++r) a1[r] = a2[r] = 0.f;
+  for (int k = 0; k < K; ++k) {
+    const float w = 1.0f / __ldg(s2h + (size_t)k * kD), wm = w * __ldg(muh + (size_t)k * kD);
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) {
+      const float d = dl[(rg * kRows + r) * K + k];
+      a1[r] = fmaf(d, wm, a1[r]);
+      a2[r] = fmaf(d, w, a2[r]);
     }
-    st_io<IO>(dst + (size_t)i * kD + j, s);
+  }
+#pragma unroll
+  for (int r = 0; r < kRows; ++r) {
+    const int i = rg * kRows + r;
+    if (i < nvalid) st_io<IO>(dst + (size_t)i * kD + j, a1[r] - xs[i * kD + j] * a2[r]);
   }
 }
 
@@ -369,7 +382,9 @@ __device__ void softmax_backward_tile(const float* G, float* dG, int K) {
 // and adds [dVt | dZ] into dstate[unit][K][65].
 template <typename IO>
 __global__ void __launch_bounds__(kThreads) simt_bwd_query_kernel(const IO* __restrict__ Q, const IO* __restrict__ dO,
-                                                                  float* params, int H, int N, int K, int seg_tiles,
+                                                                  float* params, const float* __restrict__ mu,
+                                                                  const float* __restrict__ sigma2, int H, int N, int K,
+                                                                  int seg_tiles,
                                                                   const float* __restrict__ state, float eps,
                                                                   float* dstate, float* dlq, IO* __restrict__ dQ) {
   extern __shared__ float sm[];
@@ -441,7 +456,7 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_query_kernel(const IO* __re
     softmax_backward_tile(G, dG, K);
     float* dst = dlq + ((size_t)unit * N + t0) * K;
     for (int p = threadIdx.x; p < nvalid * K; p += blockDim.x) dst[p] = dG[p];
-    dx_tile<IO>(xs, dG, nvalid, P, h, K, dQ + ((size_t)unit * N + t0) * kD);
+    dx_tile<IO>(xs, dG, nvalid, mu, sigma2, h, K, dQ + ((size_t)unit * N + t0) * kD);
   }
   __syncthreads();
   float* dS = dstate + (size_t)unit * npairs;
@@ -451,7 +466,8 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_query_kernel(const IO* __re
 // Key side: grid (tiles, B*H).  Pushes [dVt | dZ] back through the write: dV, dK and dl_K.
 template <typename IO>
 __global__ void __launch_bounds__(kThreads) simt_bwd_key_kernel(const IO* __restrict__ Kx, const IO* __restrict__ V,
-                                                                float* params, int H, int N, int K,
+                                                                float* params, const float* __restrict__ mu,
+                                                                const float* __restrict__ sigma2, int H, int N, int K,
                                                                 const float* __restrict__ dstate, float* dlk,
                                                                 IO* __restrict__ dK, IO* __restrict__ dV) {
   extern __shared__ float sm[];
@@ -487,7 +503,7 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_key_kernel(const IO* __rest
   softmax_backward_tile(G, dG, K);
   float* dst = dlk + ((size_t)unit * N + t0) * K;
   for (int p = threadIdx.x; p < nvalid * K; p += blockDim.x) dst[p] = dG[p];
-  dx_tile<IO>(xs, dG, nvalid, P, h, K, dK + ((size_t)unit * N + t0) * kD);
+  dx_tile<IO>(xs, dG, nvalid, mu, sigma2, h, K, dK + ((size_t)unit * N + t0) * kD);
 }
 
 // Parameter-gradient sums: grid (ceil(K / 32), H, chunks).  Thread (k within a block of 32, group of 8
@@ -780,12 +796,12 @@ gma_status_t backward_typed(const gma_problem_t& p, const IO* Q, const IO* Kx, c
     const size_t sm_q = (size_t)(2 * npairs + T * kD + T * kDv + T * kStateCols + 2 * T * K) * sizeof(float);
     if (set_smem_optin((const void*)simt_bwd_query_kernel<IO>, (int)sm_q, 5) != GMA_OK) return GMA_ERR_CUDA;
     GMA_LAUNCH("simt_bwd_query", simt_bwd_query_kernel<IO>, dim3(b.splits, BH), kThreads, sm_q, st, Q, dO, params,
-               p.H, p.N, K, b.seg_tiles, state, p.eps, dstate, dlq, dQ);
+               mu, sigma2, p.H, p.N, K, b.seg_tiles, state, p.eps, dstate, dlq, dQ);
     if (gma_status_t e = check_launch("launch simt_bwd_query", (const void*)simt_bwd_query_kernel<IO>)) return e;
     const size_t sm_k = (size_t)(npairs + T * kD + T * kDv + 2 * T * K) * sizeof(float);
     if (set_smem_optin((const void*)simt_bwd_key_kernel<IO>, (int)sm_k, 6) != GMA_OK) return GMA_ERR_CUDA;
-    GMA_LAUNCH("simt_bwd_key", simt_bwd_key_kernel<IO>, dim3(b.tiles, BH), kThreads, sm_k, st, Kx, V, params, p.H,
-               p.N, K, dstate, dlk, dK, dV);
+    GMA_LAUNCH("simt_bwd_key", simt_bwd_key_kernel<IO>, dim3(b.tiles, BH), kThreads, sm_k, st, Kx, V, params, mu,
+               sigma2, p.H, p.N, K, dstate, dlk, dK, dV);
     if (gma_status_t e = check_launch("launch simt_bwd_key", (const void*)simt_bwd_key_kernel<IO>)) return e;
     const int rows_per_chunk = 2048;
     const long long rows = 2LL * p.B * p.N;
