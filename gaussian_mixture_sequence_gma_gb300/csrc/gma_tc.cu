@@ -356,6 +356,20 @@ __device__ __forceinline__ void scale_v_row(uint32_t vtile, const RowCtx& rc, fl
   }
 }
 
+// The same for a V tile in the 32-byte swizzle: this thread's 16 dims are atom `part` (4 KB apart).
+__device__ __forceinline__ void scale_v_row32(uint32_t vtile, const RowCtx& rc, float inv) {
+  const __nv_bfloat162 inv2 = __float2bfloat162_rn(inv);
+#pragma unroll
+  for (int jj = 0; jj < 2; ++jj) {
+    const uint32_t ad = vtile + 4096u * (uint32_t)rc.part + sw32_chunk(rc.row, jj);
+    uint4 x = lds128(ad);
+    __nv_bfloat162* hx = reinterpret_cast<__nv_bfloat162*>(&x);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) hx[q] = __hmul2(hx[q], inv2);
+    sts128(ad, x);
+  }
+}
+
 __device__ __forceinline__ uint16_t bf16_bits(float x) {
   const __nv_bfloat16 h = __float2bfloat16_rn(x);
   return *reinterpret_cast<const uint16_t*>(&h);
@@ -838,11 +852,16 @@ __host__ __device__ inline CausalLayout causal_layout(int Kp) {
   s.w = 0;
   s.gk = align1k(Kp * 256);          // Gamma_K (bf16): MN-major A of the state update, K-major B of P
   s.x = s.gk + MB * 32768;           // two X stages: key tile, query tile
-  s.v = s.x + 2 * 16384;             // V tile (MN-major B)
-  s.sbv = s.v + 16384;               // bf16 copy of S_prev[:, 0:64], MN-major B (comp groups of 1 KB)
-  s.sbz = s.sbv + (Kp / 8) * 1024;   // bf16 copy of S_prev[:, 64] as row 0 of a 16-row K-major B
-  s.ones = s.sbz + KB * 2048;        // 1/s row of the keys (K-major, 16 x 128 tokens)
-  s.c = s.ones + 4096;
+  // [V | 1/s] as one MN-major B of N = 80 in the 32-byte swizzle: four 4 KB atoms of 16 value dims,
+  // then the 1/s atom (column 0 = 1/s of each key, columns 1..15 zero)
+  s.v = s.x + 2 * 16384;
+  s.ones = s.v + 16384;
+  // bf16 copy of S_prev [Kp][80] (+ eps in column 64), MN-major B of N = 80, 32-byte swizzle: five
+  // atoms of Kp rows x 32 bytes
+  s.sbv = s.ones + 4096;
+  s.sbz = s.sbv + 4 * Kp * 32;       // the fifth atom (Z + eps in column 64)
+  (void)KB;
+  s.c = s.sbz + Kp * 32;
   s.red = s.c + 1024;
   s.total = s.red + kParts * kTile * 8;
   return s;
@@ -856,11 +875,12 @@ struct CBars {
   Abort ab;
 };
 
-// Writes float32 state columns 16c .. 16c+15 of component `comp` (r) into the bf16 operands of the
-// inter-tile term: columns 0..63 into SBV (MN-major, 16-byte chunks), column 64 plus eps into row 0 of
-// SBZ (K-major).
-__device__ __forceinline__ void snapshot_state_chunk(uint32_t sbv, uint32_t sbz, int comp, int c, const uint32_t* r,
+// Writes float32 state columns 16c .. 16c+15 of component `comp` (r) into atom c of the bf16 copy of
+// S_prev (MN-major, 32-byte swizzle, atoms of Kp rows x 32 bytes at sb + c * Kp * 32); for c = 4 only
+// column 64 (Z, plus eps) is kept, as element 0 of the fifth atom.
+__device__ __forceinline__ void snapshot_state_chunk(uint32_t sb, int Kp, int comp, int c, const uint32_t* r,
                                                      float eps) {
+  const uint32_t atom = sb + (uint32_t)c * (uint32_t)Kp * 32u;
   if (c < 4) {
     const uint4 lo = make_uint4(pack_bf16x2(__uint_as_float(r[0]), __uint_as_float(r[1])),
                                 pack_bf16x2(__uint_as_float(r[2]), __uint_as_float(r[3])),
@@ -870,10 +890,10 @@ __device__ __forceinline__ void snapshot_state_chunk(uint32_t sbv, uint32_t sbz,
                                 pack_bf16x2(__uint_as_float(r[10]), __uint_as_float(r[11])),
                                 pack_bf16x2(__uint_as_float(r[12]), __uint_as_float(r[13])),
                                 pack_bf16x2(__uint_as_float(r[14]), __uint_as_float(r[15])));
-    sts128(sbv + sw128_chunk(comp, 2 * c), lo);
-    sts128(sbv + sw128_chunk(comp, 2 * c + 1), hi);
+    sts128(atom + sw32_chunk(comp, 0), lo);
+    sts128(atom + sw32_chunk(comp, 1), hi);
   } else {
-    sts16(sbz + sw128_off(0, comp, 2048), bf16_bits(__uint_as_float(r[0]) + eps));
+    sts16(atom + sw32_chunk(comp, 0), bf16_bits(__uint_as_float(r[0]) + eps));
   }
 }
 
@@ -896,8 +916,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   // zero Gamma_K, the state copies and the 1/s tile (its row 0 is rewritten every tile)
   for (uint32_t i = threadIdx.x; i < (uint32_t)MB * 32768 / 16; i += blockDim.x)
     reinterpret_cast<uint4*>(smem + L.gk)[i] = make_uint4(0, 0, 0, 0);
-  for (uint32_t i = threadIdx.x; i < (L.ones + 4096 - L.sbv) / 16; i += blockDim.x)
-    reinterpret_cast<uint4*>(smem + L.sbv)[i] = make_uint4(0, 0, 0, 0);
+  for (uint32_t i = threadIdx.x; i < (L.c - L.ones) / 16; i += blockDim.x)  // 1/s atom and the state copy
+    reinterpret_cast<uint4*>(smem + L.ones)[i] = make_uint4(0, 0, 0, 0);
   if (threadIdx.x == 0) {
     mbar_init(&B.w_full, 1);
     for (int s = 0; s < 2; ++s) {
@@ -955,7 +975,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         issued[1] = t & 1;
         if (!wait_bounded(&B.v_empty, pe, &B.ab, a.ctrl, 72, a.wait_ns)) break;
         mbar_expect_tx(&B.v_full, 16384);
-        tma_load_3d(smem + L.v, &tmV, 0, row0, bh, &B.v_full);
+        for (int a4 = 0; a4 < 4; ++a4) tma_load_3d(smem + L.v + 4096 * a4, &tmV, 16 * a4, row0, bh, &B.v_full);
         issued[2] = t & 1;
       }
       // never leave with copies in flight
@@ -967,17 +987,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       // ---------------------------------------------------------------- MMA issuer
       const uint32_t w_addr = smem_u32(smem + L.w);
       // base descriptors; every operand step below is a byte offset added to one of them
-      const uint64_t d_sbv = make_sdesc(smem_u32(smem + L.sbv), 16384, 1024);  // MN-major, 16 comps = 2 KB
-      const uint64_t d_sbz = make_sdesc(smem_u32(smem + L.sbz), 16, 1024);     // K-major, 16 rows
+      // [S_prev | Z + eps] (Kp x 80) and [V | 1/s] (128 x 80): MN-major, 32-byte swizzle, 16 rows = 512 B
+      const uint64_t d_sb = make_sdesc32(smem_u32(smem + L.sbv), (uint32_t)a.Kp * 32, 256);
+      const uint64_t d_vb = make_sdesc32(smem_u32(smem + L.v), 4096, 256);
       const uint64_t d_gk_k = make_sdesc(smem_u32(smem + L.gk), 16, 1024);     // Gamma_K as K-major B
       const uint64_t d_gk_mn = make_sdesc(smem_u32(smem + L.gk), 16384, 1024); // Gamma_K^T as MN-major A
-      const uint64_t d_v = make_sdesc(smem_u32(smem + L.v), 16384, 1024);      // V, MN-major, N = 64
-      const uint64_t d_one = make_sdesc(smem_u32(smem + L.ones), 16, 1024);    // 1/s row, K-major, N = 16
-      constexpr uint32_t id_c64 = make_idesc(128, 64, 1, 1, 0, 1);    // A tmem, B MN-major
-      constexpr uint32_t id_c16 = make_idesc(128, 16, 1, 1, 0, 0);    // A tmem, B K-major
-      constexpr uint32_t id_p = make_idesc(128, 128, 1, 1, 0, 0);     // P = Gq~ Gk^T
-      constexpr uint32_t id_s64 = make_idesc(128, 64, 1, 1, 1, 1);    // A MN-major (Gamma_K^T), B MN-major (V)
-      constexpr uint32_t id_s16 = make_idesc(128, 16, 1, 1, 1, 0);    // A MN-major, B K-major (1/s row)
+      constexpr uint32_t id_c80 = make_idesc(128, kStCols, 1, 1, 0, 1);  // A tmem, B MN-major, N = 80
+      constexpr uint32_t id_p = make_idesc(128, 128, 1, 1, 0, 0);         // P = Gq~ Gk^T
+      constexpr uint32_t id_s80 = make_idesc(128, kStCols, 1, 1, 1, 1);  // A MN-major (Gamma_K^T), B MN-major
       bool ok = wait_bounded(&B.w_full, 0, &B.ab, a.ctrl, 80, a.wait_ns);
       for (int t = 0; ok && t < T; ++t) {
         const uint32_t ph = t & 1;
@@ -1000,11 +1017,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 #pragma unroll 1
         for (int mb = 0; mb < MB; ++mb) {
 #pragma unroll 1
-          for (int s = 0; s < 8; ++s) {
-            const uint64_t ad = sdesc_add(d_gk_mn, mb * 32768 + 2048 * s);
-            mma_ss(tmem + kCColS + kStCols * mb, ad, sdesc_add(d_v, 2048 * s), id_s64, 1u);
-            mma_ss(tmem + kCColS + kStCols * mb + 64, ad, sdesc_add(d_one, (s >> 2) * 2048 + (s & 3) * 32), id_s16, 1u);
-          }
+          for (int s = 0; s < 8; ++s)
+            mma_ss(tmem + kCColS + kStCols * mb, sdesc_add(d_gk_mn, mb * 32768 + 2048 * s), sdesc_add(d_vb, 512 * s),
+                   id_s80, 1u);
         }
         mma_commit(&B.s_full);
         // inter-tile term O = Gq~ S_prev and intra-tile affinity P = Gq~ Gk^T
@@ -1013,9 +1028,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 #pragma unroll 1
         for (int ks = 0; ks < KS; ++ks) {
           const uint32_t aq = tmem + kColLog + 8 * ks;  // Gq~ (bf16 pairs) over the logit columns
-          const uint32_t kofs = (ks >> 2) * 2048 + (ks & 3) * 32;
-          mma_ts(tmem + kCColO, aq, sdesc_add(d_sbv, 2048 * ks), id_c64, ks > 0);
-          mma_ts(tmem + kCColO + 64, aq, sdesc_add(d_sbz, kofs), id_c16, ks > 0);
+          mma_ts(tmem + kCColO, aq, sdesc_add(d_sb, 512 * ks), id_c80, ks > 0);
           mma_ts(tmem + kCColP, aq, sdesc_add(d_gk_k, (ks >> 2) * 16384 + (ks & 3) * 32), id_p, ks > 0);
         }
         mma_commit(&B.p_full);
@@ -1025,8 +1038,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 #pragma unroll 1
         for (int s = 0; s < 8; ++s) {
           const uint32_t ap = tmem + kCColP + 32 * (s >> 1) + 8 * (s & 1);  // bf16 P of keys 16s..16s+15
-          mma_ts(tmem + kCColO, ap, sdesc_add(d_v, 2048 * s), id_c64, 1u);
-          mma_ts(tmem + kCColO + 64, ap, sdesc_add(d_one, (s >> 2) * 2048 + (s & 3) * 32), id_c16, 1u);
+          mma_ts(tmem + kCColO, ap, sdesc_add(d_vb, 512 * s), id_c80, 1u);
         }
         mma_commit(&B.o_full);
         mma_commit(&B.v_empty);
@@ -1052,7 +1064,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i) r[i] = comp < a.Kp ? __float_as_uint(__ldg(pre + 16 * c + i)) : 0u;
         tmem_st16(tmem + rc.lane_base + kCColS + kStCols * rc.part + 16 * c, r);
-        if (comp < a.Kp) snapshot_state_chunk(sbase + L.sbv, sbase + L.sbz, comp, c, r, a.eps);
+        if (comp < a.Kp) snapshot_state_chunk(sbase + L.sbv, a.Kp, comp, c, r, a.eps);
       }
     }
     tmem_st_wait();
@@ -1097,9 +1109,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       if (ok) ok = warp_wait(&B.v_full, ph, &B.ab, a.ctrl, 98, a.wait_ns);
       if (ok) {
         const float inv = tok < a.N ? rcp_approx(sum) : 0.f;
-        scale_v_row(sbase + L.v, rc, inv);
-        if (rc.part == 0) sts16(sbase + L.ones + (uint32_t)(rc.row >> 6) * 2048u + (uint32_t)(rc.row & 63) * 2u,
-                                bf16_bits(inv));
+        scale_v_row32(sbase + L.v, rc, inv);
+        if (rc.part == 0) sts16(sbase + L.ones + sw32_chunk(rc.row, 0), bf16_bits(inv));
         fence_async_smem();
         warp_arrive(&B.gk_full);
       }
@@ -1151,7 +1162,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           for (int c = 0; c < 5; ++c) {
             tmem_ld16(tmem + rc.lane_base + kCColS + kStCols * rc.part + 16 * c, r);
             tmem_ld_wait();
-            if (comp < a.Kp) snapshot_state_chunk(sbase + L.sbv, sbase + L.sbz, comp, c, r, a.eps);
+            if (comp < a.Kp) snapshot_state_chunk(sbase + L.sbv, a.Kp, comp, c, r, a.eps);
           }
         }
         fence_async_smem();
@@ -1234,7 +1245,9 @@ EncodeTiledFn encode_fn() {
 }
 
 // 3-D map over a [B*H][N][64] bf16 tensor, box 64 x 128 x 1, 128-byte swizzle, zero fill past N.
-bool make_map(CUtensorMap* m, const void* base, int BH, int N) {
+// 3-D map over [B*H][N][64] bf16 with 128-row boxes: 64-dim boxes in the 128-byte swizzle, or (sw32)
+// 16-dim boxes in the 32-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, int BH, int N, bool sw32 = false) {
   EncodeTiledFn f = encode_fn();
   if (!f) {
     set_error_detail("cuTensorMapEncodeTiled entry point unavailable");
@@ -1242,9 +1255,10 @@ bool make_map(CUtensorMap* m, const void* base, int BH, int N) {
   }
   cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)N, (cuuint64_t)BH};
   cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)N * kD * 2};
-  cuuint32_t box[3] = {64, (cuuint32_t)kTile, 1}, es[3] = {1, 1, 1};
+  cuuint32_t box[3] = {sw32 ? 16u : 64u, (cuuint32_t)kTile, 1}, es[3] = {1, 1, 1};
   const CUresult r = f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
-                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, sw32 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_128B,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     char msg[96];
@@ -1279,7 +1293,10 @@ gma_status_t tc_launch(const gma_problem_t& p, gma_op_t op, int Nk, const TcPlan
     return check_launch("launch tc_resp", (const void*)tc_read_kernel<false, NC>);
   }
   if (op == GMA_OP_CAUSAL) {
-    if (!make_map(&mq, Q, BH, p.N) || !make_map(&mk, K, BH, p.N) || !make_map(&mv, V, BH, p.N)) return GMA_ERR_CUDA;
+    CUtensorMap mv32;  // the chunk kernel's V tiles: four 16-dim boxes in the 32-byte swizzle
+    if (!make_map(&mq, Q, BH, p.N) || !make_map(&mk, K, BH, p.N) || !make_map(&mv, V, BH, p.N) ||
+        !make_map(&mv32, V, BH, p.N, true))
+      return GMA_ERR_CUDA;
     // a5: segment aggregates; a6: exclusive scan over segments; a7: chunked sweep
     const uint32_t smem_w = smem_bytes(write_layout(pl.Kp).total);
     if (set_smem_optin((const void*)tc_write_kernel<false, NC>, (int)smem_w, 0) != GMA_OK) return GMA_ERR_CUDA;
@@ -1292,7 +1309,7 @@ gma_status_t tc_launch(const gma_problem_t& p, gma_op_t op, int Nk, const TcPlan
     if (gma_status_t e = check_launch("launch tc_causal_scan", (const void*)tc_scan_kernel)) return e;
     const uint32_t smem_c = smem_bytes(causal_layout(pl.Kp).total);
     if (set_smem_optin((const void*)tc_causal_kernel<NC>, (int)smem_c, 0) != GMA_OK) return GMA_ERR_CUDA;
-    GMA_LAUNCH("tc_causal_chunk", tc_causal_kernel<NC>, dim3(pl.splits, BH), kThreadsTc, smem_c, st, mq, mk, mv, a);
+    GMA_LAUNCH("tc_causal_chunk", tc_causal_kernel<NC>, dim3(pl.splits, BH), kThreadsTc, smem_c, st, mq, mk, mv32, a);
     return check_launch("launch tc_causal_chunk", (const void*)tc_causal_kernel<NC>);
   }
   // bidirectional / cross: write over the Nk keys with their own split plan (the state layout does not

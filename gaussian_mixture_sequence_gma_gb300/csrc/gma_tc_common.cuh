@@ -240,6 +240,24 @@ __device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo, uin
   return d;
 }
 
+// The same for the 32-byte swizzle (swizzle mode 6): atoms of 8 rows x 32 bytes (16 bf16 along MN for
+// an MN-major operand), lbo = stride between 16-element atoms along MN, sbo = stride between 8-row groups.
+__device__ __forceinline__ uint64_t make_sdesc32(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFF) >> 4);
+  d |= (uint64_t)((lbo & 0x3FFFF) >> 4) << 16;
+  d |= (uint64_t)((sbo & 0x3FFFF) >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)6 << 61;
+  return d;
+}
+
+// Byte offset of 16-byte chunk `c` (0 or 1) of row r in a 32B-swizzled atom of 32-byte rows
+// (chunk index XOR bit 2 of the row, the TMA / MMA 32B swizzle).
+__host__ __device__ __forceinline__ uint32_t sw32_chunk(int r, int c) {
+  return (uint32_t)r * 32u + ((uint32_t)(c ^ ((r >> 2) & 1)) << 4);
+}
+
 // Descriptor of the same operand `bytes` further on (the start-address field holds address >> 4 in
 // 14 bits; every shared-memory address here is below 256 KB, so the add never carries out of it).
 __device__ __forceinline__ uint64_t sdesc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
