@@ -324,6 +324,37 @@ __device__ __forceinline__ float exp_pack_store(const float* v, float m, uint32_
   return kSum ? (s0 + s1) + (s2 + s3) : 0.f;
 }
 
+// The exponentiate-and-pack half of exp_pack_store, in place: word i of v receives the bf16 pair of
+// components 2i, 2i+1, so the shared-memory tile can still be in use by a contraction meanwhile.
+template <int NC, bool kSum>
+__device__ __forceinline__ float exp_pack_regs(float* v, float m) {
+  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+  uint32_t* w = reinterpret_cast<uint32_t*>(v);
+#pragma unroll
+  for (int i = 0; i < NC / 2; ++i) {
+    float t0 = v[2 * i], t1 = v[2 * i + 1];
+    add_f32x2(t0, t1, -m, -m);
+    const float e0 = ex2_approx(t0), e1 = ex2_approx(t1);
+    if (kSum) {
+      if (i & 1)
+        add_f32x2(s2, s3, e0, e1);
+      else
+        add_f32x2(s0, s1, e0, e1);
+    }
+    w[i] = pack_bf16x2(e0, e1);
+  }
+  return kSum ? (s0 + s1) + (s2 + s3) : 0.f;
+}
+// The store half: the NC/2 packed words of v as 16-byte chunks at ga (gamma_row_addr), below Kp.
+template <int NC>
+__device__ __forceinline__ void store_packed(const float* v, uint32_t ga, const RowCtx& rc, int Kp) {
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(v);
+  const int nvalid = (Kp - NC * rc.part) >> 3;
+#pragma unroll
+  for (int cj = 0; cj < NC / 8; ++cj)
+    if (cj < nvalid) sts128(ga ^ (uint32_t)(cj << 4), make_uint4(w[4 * cj], w[4 * cj + 1], w[4 * cj + 2], w[4 * cj + 3]));
+}
+
 // Fused pass for a TMEM-resident operand: e = 2^(v - m) packed to bf16 pairs and stored over this thread's
 // NC/2 columns starting at taddr (8 words per store).  The caller waits for the stores.
 template <int NC>
@@ -587,9 +618,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       }
       const float m = xchg_max(rc, 0, mp);
       // Gamma~ row (unnormalised, row maximum 1) -> smem once the previous contraction has read it
-      if (ok && t > 0) ok = warp_wait(&B.g_empty, (t - 1) & 1, &B.ab, a.ctrl, 36, a.wait_ns);
+      // exponentiate into registers while the previous contraction may still be reading G, then store
       float sp = 0.f;
-      if (ok) sp = exp_pack_store<NC, true>(v, m, ga, rc, a.Kp);
+      if (ok) sp = exp_pack_regs<NC, true>(v, m);
+      if (ok && t > 0) ok = warp_wait(&B.g_empty, (t - 1) & 1, &B.ab, a.ctrl, 36, a.wait_ns);
+      if (ok) store_packed<NC>(v, ga, rc, a.Kp);
       const float sum = xchg_sum(rc, 4, sp);
       // normalise this key's Gamma row inside the contraction: scale its [v | 1] row by 1/s (0 past N)
       if (ok) ok = warp_wait(&B.v_full[s], (t >> 1) & 1, &B.ab, a.ctrl, 38, a.wait_ns);
