@@ -88,7 +88,7 @@ __host__ __device__ inline SmemLayout read_layout(int Kp) {
 
 struct Bars {
   uint64_t w_full, sb_full;
-  uint64_t x_full[2], x_empty[2], v_full[2], v_empty[2];
+  uint64_t x_full[2], x_empty[2], v_empty[2];
   uint64_t ax_full, l_full, l_empty, g_full, g_empty, o_full, o_empty;
   uint64_t done;
   uint32_t tmem_base;
@@ -412,7 +412,6 @@ __device__ __forceinline__ void init_bars(Bars* B) {
   for (int s = 0; s < 2; ++s) {
     mbar_init(&B->x_full[s], 1);
     mbar_init(&B->x_empty[s], kRowWarps);
-    mbar_init(&B->v_full[s], 1);
     mbar_init(&B->v_empty[s], 1);
   }
   mbar_init(&B->ax_full, kRowWarps);
@@ -427,7 +426,10 @@ __device__ __forceinline__ void init_bars(Bars* B) {
   mbar_fence_init();
 }
 
-// Producer: W image + c' once, then per tile the X tile (and the V tile if `tmV`).
+// Producer: W image + c' once, then per tile the X tile.  With `tmV` (write kernel), iteration u also
+// brings the V tile of u - 1, on the same barrier x_full[u & 1], so a row warp that has waited for the
+// X tile it builds next also has the V tile of its current key tile; an extra iteration u = T brings
+// the last V tile alone.  The V ring slot of tile t is t & 1, released by the write contraction.
 __device__ __forceinline__ void producer(const TcArgs& a, const CUtensorMap* tmX, const CUtensorMap* tmV,
                                          uint8_t* smem, const SmemLayout& L, Bars* B, int bh, int tile0, int T) {
   const uint32_t wbytes = (uint32_t)a.Kp * 256, cbytes = kCTable * 4;
@@ -436,29 +438,29 @@ __device__ __forceinline__ void producer(const TcArgs& a, const CUtensorMap* tmX
   for (uint32_t o = 0; o < wbytes; o += 32768)
     bulk_load(smem + L.w + o, a.w_img + (size_t)h * wbytes + o, min(32768u, wbytes - o), &B->w_full);
   bulk_load(smem + L.c, a.cbias + (size_t)h * kCTable, cbytes, &B->w_full);
-  int issued_x[2] = {-1, -1}, issued_v[2] = {-1, -1};
-  for (int t = 0; t < T; ++t) {
-    const int s = t & 1;
-    const uint32_t u = (uint32_t)(t >> 1);
-    if (!wait_bounded(&B->x_empty[s], (u & 1) ^ 1, &B->ab, a.ctrl, 10, a.wait_ns)) break;
-    if (!((a.fault & 1) && t == 0)) {
-      mbar_expect_tx(&B->x_full[s], 16384);
-      tma_load_3d(smem + L.x + s * 16384, tmX, 0, (tile0 + t) * kTile, bh, &B->x_full[s]);
-      issued_x[s] = (int)(u & 1);
-    }
-    if (tmV) {
-      if (!wait_bounded(&B->v_empty[s], (u & 1) ^ 1, &B->ab, a.ctrl, 11, a.wait_ns)) break;
-      mbar_expect_tx(&B->v_full[s], 16384);
-      tma_load_3d(smem + L.v + s * 16384, tmV, 0, (tile0 + t) * kTile, bh, &B->v_full[s]);
-      issued_v[s] = (int)(u & 1);
-    }
+  int issued[2] = {-1, -1};  // parity of the last phase armed on x_full[0], x_full[1]
+  for (int u = 0; u <= T; ++u) {
+    const int s = u & 1;
+    const uint32_t ph = (uint32_t)(u >> 1) & 1;
+    const bool has_x = u < T, has_v = tmV != nullptr && u > 0;
+    if (!has_x && !has_v) break;
+    // x_full[s] is re-armed only after its previous phase has been consumed (an arrival on a phase
+    // that is still pending would over-count it), also when this iteration brings V alone
+    if (!wait_bounded(&B->x_empty[s], ph ^ 1, &B->ab, a.ctrl, 10, a.wait_ns)) break;
+    const int sv = (u - 1) & 1;
+    if (has_v && !wait_bounded(&B->v_empty[sv], ((uint32_t)((u - 1) >> 1) & 1) ^ 1, &B->ab, a.ctrl, 11, a.wait_ns)) break;
+    const bool load_x = has_x && !((a.fault & 1) && u == 0);
+    const uint32_t bytes = (load_x ? 16384u : 0u) + (has_v ? 16384u : 0u);
+    if (bytes == 0) continue;
+    mbar_expect_tx(&B->x_full[s], bytes);
+    if (load_x) tma_load_3d(smem + L.x + s * 16384, tmX, 0, (tile0 + u) * kTile, bh, &B->x_full[s]);
+    if (has_v) tma_load_3d(smem + L.v + sv * 16384, tmV, 0, (tile0 + u - 1) * kTile, bh, &B->x_full[s]);
+    issued[s] = (int)ph;
   }
-  // never leave with copies in flight: wait for the last load issued on each stage
+  // never leave with copies in flight: wait for the last phase armed on each barrier
   Abort none{0};
-  for (int s = 0; s < 2; ++s) {
-    if (issued_x[s] >= 0) wait_bounded(&B->x_full[s], (uint32_t)issued_x[s], &none, a.ctrl, 12, a.wait_ns);
-    if (issued_v[s] >= 0) wait_bounded(&B->v_full[s], (uint32_t)issued_v[s], &none, a.ctrl, 13, a.wait_ns);
-  }
+  for (int s = 0; s < 2; ++s)
+    if (issued[s] >= 0) wait_bounded(&B->x_full[s], (uint32_t)issued[s], &none, a.ctrl, 12, a.wait_ns);
 }
 
 // Issues the log-density contraction of one tile: LOG[128 x Kp] = AX[128 x 128] * W^T.
@@ -549,8 +551,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           mma_commit(&B.l_full);
         }
         const int s = t & 1;
-        ok = wait_bounded(&B.g_full, t & 1, &B.ab, a.ctrl, 24, a.wait_ns) &&
-             wait_bounded(&B.v_full[s], (t >> 1) & 1, &B.ab, a.ctrl, 26, a.wait_ns);
+        // the row warps signal g_full after scaling this tile's V rows, so V has landed as well
+        ok = wait_bounded(&B.g_full, t & 1, &B.ab, a.ctrl, 24, a.wait_ns);
         if (!ok) break;
         tc_fence_after();
         const uint32_t vs = v_addr + s * 16384;
@@ -599,16 +601,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       if (ok) ok = warp_wait(&B.l_full, t & 1, &B.ab, a.ctrl, 32, a.wait_ns);
       if (ok) {
         tc_fence_after();
-        if (t + 1 < T) {
-          const int s1 = (t + 1) & 1;
-          ok = warp_wait(&B.x_full[s1], ((t + 1) >> 1) & 1, &B.ab, a.ctrl, 33, a.wait_ns);
-          if (ok) {
-            transform_row(sbase + L.x + s1 * 16384, rc, tmem);
-            warp_arrive(&B.x_empty[s1]);
-            tmem_st_wait();
-            tc_fence_before();
-            warp_arrive(&B.ax_full);
-          }
+        // x_full of u = t + 1 brings X(t + 1) (if any) and V(t)
+        const int s1 = (t + 1) & 1;
+        ok = warp_wait(&B.x_full[s1], ((t + 1) >> 1) & 1, &B.ab, a.ctrl, 33, a.wait_ns);
+        if (ok && t + 1 < T) {
+          transform_row(sbase + L.x + s1 * 16384, rc, tmem);
+          warp_arrive(&B.x_empty[s1]);
+          tmem_st_wait();
+          tc_fence_before();
+          warp_arrive(&B.ax_full);
         }
       }
       if (ok) {
@@ -625,7 +626,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       if (ok) store_packed<NC>(v, ga, rc, a.Kp);
       const float sum = xchg_sum(rc, 4, sp);
       // normalise this key's Gamma row inside the contraction: scale its [v | 1] row by 1/s (0 past N)
-      if (ok) ok = warp_wait(&B.v_full[s], (t >> 1) & 1, &B.ab, a.ctrl, 38, a.wait_ns);
       if (ok) {
         const float inv = tok < a.N ? rcp_approx(sum) : 0.f;
         scale_v_row(sbase + L.v + s * 16384, rc, inv);
