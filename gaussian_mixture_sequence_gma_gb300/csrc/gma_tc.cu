@@ -1105,21 +1105,22 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     tc_fence_before();
     warp_arrive(&B.sb_full);
     bool ok = warp_wait(&B.w_full, 0, &B.ab, a.ctrl, 90, a.wait_ns);
+    // key operand of the first tile (later ones are built in the previous tile's epilogue; the [x^2 | x]
+    // columns double as the output accumulator)
+    if (ok && T > 0) ok = warp_wait(&B.x_full[0], 0, &B.ab, a.ctrl, 91, a.wait_ns);
+    if (ok && T > 0) {
+      transform_row(sbase + L.x, rc, tmem, kCColO);
+      warp_arrive(&B.x_empty[0]);
+      tmem_st_wait();
+      tc_fence_before();
+      warp_arrive(&B.ax_full);
+    }
     float v[NC];
     // every row warp runs all T tiles and all exchanges (see the write kernel)
     for (int t = 0; t < T; ++t) {
       const uint32_t ph = t & 1;
       const int tok = (tile0 + t) * kTile + rc.row;
       float mh = -INFINITY;
-      // key operand (the [x^2 | x] columns double as the output accumulator, free since the last epilogue)
-      if (ok) ok = warp_wait(&B.x_full[0], ph, &B.ab, a.ctrl, 91, a.wait_ns);
-      if (ok) {
-        transform_row(sbase + L.x, rc, tmem, kCColO);
-        warp_arrive(&B.x_empty[0]);
-        tmem_st_wait();
-        tc_fence_before();
-        warp_arrive(&B.ax_full);
-      }
       // key logits -> registers; build the query operand first so its contraction starts at once
       if (ok) ok = warp_wait(&B.lk_full, ph, &B.ab, a.ctrl, 92, a.wait_ns);
       if (ok) {
@@ -1203,7 +1204,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         warp_arrive(&B.sb_full);
       }
       // output: this thread's output dims are 8*part + [0,8) and 32 + 8*part + [0,8) -- the same columns it
-      // overwrites with the next key operand, so no other warp reads them afterwards
+      // overwrites with the next key operand, so no other warp reads them afterwards.  Once they are in
+      // registers the next key operand goes in (its contraction runs while this output is stored).
       if (ok) ok = warp_wait(&B.o_full, ph, &B.ab, a.ctrl, 100, a.wait_ns);
       if (ok) {
         tc_fence_after();
@@ -1212,6 +1214,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         tmem_ld8(tmem + rc.lane_base + kCColO + 32 + 8 * rc.part, o1);
         tmem_ld8(tmem + rc.lane_base + kCColO + 64, zc);
         tmem_ld_wait();
+        if (t + 1 < T) {
+          ok = warp_wait(&B.x_full[0], (t + 1) & 1, &B.ab, a.ctrl, 91, a.wait_ns);
+          if (ok) {
+            transform_row(sbase + L.x, rc, tmem, kCColO);
+            warp_arrive(&B.x_empty[0]);
+            tmem_st_wait();
+            tc_fence_before();
+            warp_arrive(&B.ax_full);
+          }
+        }
         const float rden = rcp_approx(__uint_as_float(zc[0]));  // gq~ . (Z_i + eps)
         if (tok < a.N) {
           __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.out) + ((size_t)bh * a.N + tok) * kDv;
