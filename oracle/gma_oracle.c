@@ -359,6 +359,86 @@ int gma_oracle_backward_bidir(int B, int H, int N, int d, int dv, int K, const d
   return 0;
 }
 
+/* [B] + [C] Gradients of the causal forward, given G = dL/dO.  Per (b, h), with the running state
+ * S_i = sum_{j <= i} gamma_Kj [v_j | 1] (latent memory and normaliser after key i), den_i = gamma_Qi . Z_i
+ * + eps, O_i = gamma_Qi . Vt_i / den_i, and u_i = [G_i / den_i | -(G_i . O_i) / den_i]:
+ *   dgamma_Qi = S_i u_i,
+ *   R_j = sum_{i >= j} gamma_Qi u_i^T (the suffix sum of the queries' contributions),
+ *   dgamma_Kj = R_j [v_j | 1],   dv_j = R_j[:, :dv]^T gamma_Kj,
+ * then the softmax and log-density steps of the bidirectional backward.  Forward over i, then
+ * backward over j. */
+int gma_oracle_backward_causal(int B, int H, int N, int d, int dv, int K, const double *Q, const double *Kx,
+                               const double *V, const double *mu, const double *sigma2, const double *log_pi,
+                               double eps, const double *G, double *dQ, double *dK, double *dV, double *dmu,
+                               double *dsigma2, double *dlog_pi) {
+  const int C = dv + 1;
+  double *gq = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1) * K);
+  double *gk = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1) * K);
+  double *u = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1) * C);
+  double *ld = (double *)malloc(sizeof(double) * K);
+  double *S = (double *)malloc(sizeof(double) * (size_t)K * C), *R = (double *)malloc(sizeof(double) * (size_t)K * C);
+  double *dg = (double *)malloc(sizeof(double) * K), *dl = (double *)malloc(sizeof(double) * K);
+  memset(dmu, 0, sizeof(double) * (size_t)H * K * d);
+  memset(dsigma2, 0, sizeof(double) * (size_t)H * K * d);
+  memset(dlog_pi, 0, sizeof(double) * (size_t)H * K);
+  for (int unit = 0; unit < B * H; ++unit) {
+    const int h = unit % H;
+    const double *mu_h = mu + (size_t)h * K * d, *s2_h = sigma2 + (size_t)h * K * d, *lp_h = log_pi + (size_t)h * K;
+    double *dmu_h = dmu + (size_t)h * K * d, *ds2_h = dsigma2 + (size_t)h * K * d, *dlp_h = dlog_pi + (size_t)h * K;
+    const double *q = Q + (size_t)unit * N * d, *kx = Kx + (size_t)unit * N * d, *v = V + (size_t)unit * N * dv;
+    const double *g = G + (size_t)unit * N * dv;
+    log_determinants(d, K, s2_h, ld);
+    memset(S, 0, sizeof(double) * (size_t)K * C);
+    /* forward over i: running state, output, u_i, dgamma_Q */
+    for (int i = 0; i < N; ++i) {
+      double *gqi = gq + (size_t)i * K, *gki = gk + (size_t)i * K, *ui = u + (size_t)i * C;
+      posterior(d, K, kx + (size_t)i * d, mu_h, s2_h, ld, lp_h, gki);
+      for (int k = 0; k < K; ++k) {
+        for (int c = 0; c < dv; ++c) S[(size_t)k * C + c] += gki[k] * v[(size_t)i * dv + c];
+        S[(size_t)k * C + dv] += gki[k];
+      }
+      posterior(d, K, q + (size_t)i * d, mu_h, s2_h, ld, lp_h, gqi);
+      double den = eps, go = 0.0;
+      for (int k = 0; k < K; ++k) den += gqi[k] * S[(size_t)k * C + dv];
+      for (int c = 0; c < dv; ++c) {
+        double num = 0.0;
+        for (int k = 0; k < K; ++k) num += gqi[k] * S[(size_t)k * C + c];
+        go += g[(size_t)i * dv + c] * (num / den);
+      }
+      for (int c = 0; c < dv; ++c) ui[c] = g[(size_t)i * dv + c] / den;
+      ui[dv] = -go / den;
+      for (int k = 0; k < K; ++k) {
+        double s = 0.0;
+        for (int c = 0; c < C; ++c) s += S[(size_t)k * C + c] * ui[c];
+        dg[k] = s;
+      }
+      softmax_backward(K, gqi, dg, dl);
+      logdensity_backward(d, K, q + (size_t)i * d, mu_h, s2_h, dl, dQ + ((size_t)unit * N + i) * d, dmu_h, ds2_h, dlp_h);
+    }
+    /* backward over j: suffix sums R_j, dgamma_K and dv */
+    memset(R, 0, sizeof(double) * (size_t)K * C);
+    for (int j = N - 1; j >= 0; --j) {
+      const double *gqj = gq + (size_t)j * K, *gkj = gk + (size_t)j * K, *uj = u + (size_t)j * C;
+      for (int k = 0; k < K; ++k)
+        for (int c = 0; c < C; ++c) R[(size_t)k * C + c] += gqj[k] * uj[c];
+      for (int k = 0; k < K; ++k) {
+        double s = R[(size_t)k * C + dv];
+        for (int c = 0; c < dv; ++c) s += R[(size_t)k * C + c] * v[(size_t)j * dv + c];
+        dg[k] = s;
+      }
+      for (int c = 0; c < dv; ++c) {
+        double s = 0.0;
+        for (int k = 0; k < K; ++k) s += gkj[k] * R[(size_t)k * C + c];
+        dV[((size_t)unit * N + j) * dv + c] = s;
+      }
+      softmax_backward(K, gkj, dg, dl);
+      logdensity_backward(d, K, kx + (size_t)j * d, mu_h, s2_h, dl, dK + ((size_t)unit * N + j) * d, dmu_h, ds2_h, dlp_h);
+    }
+  }
+  free(gq); free(gk); free(u); free(ld); free(S); free(R); free(dg); free(dl);
+  return 0;
+}
+
 /* Latent memory Vt [B,H,K,dv] and normaliser Z [B,H,K] over all N keys ([W]). */
 int gma_oracle_state(int B, int H, int N, int d, int dv, int K, const double *Kx, const double *V, const double *mu,
                      const double *sigma2, const double *log_pi, double *Vt, double *Z) {

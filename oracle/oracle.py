@@ -17,9 +17,10 @@ item 3; fugumt.com English abstract):
   written by Nk keys / values (gist.science summary, "Significance and claims",
   closing paragraph: cross-attention applications named as future work).
 * ``state``: Vt and Z alone.
-* ``backward_bidir``: gradients of the bidirectional forward with respect to
-  Q, K, V, mu, sigma2 and log pi given dL/dO ("Variants and training" item 3:
-  the components are learned end to end by backpropagation).
+* ``backward_bidir`` / ``backward_causal``: gradients of the bidirectional /
+  causal forward with respect to Q, K, V, mu, sigma2 and log pi given dL/dO
+  ("Variants and training" item 3: the components are learned end to end by
+  backpropagation; the causal form through its prefix sums).
 
 All inputs are converted to float64 here; the C code is plain sequential
 float64 arithmetic per (batch, head) unit.
@@ -74,6 +75,8 @@ def _load(path: str | None = None):
     lib.gma_oracle_backward_bidir.argtypes = [ci, ci, ci, ci, ci, ci, dp, dp, dp, dp, dp, dp, ctypes.c_double, dp,
                                               dp, dp, dp, dp, dp, dp]
     lib.gma_oracle_backward_bidir.restype = ci
+    lib.gma_oracle_backward_causal.argtypes = lib.gma_oracle_backward_bidir.argtypes
+    lib.gma_oracle_backward_causal.restype = ci
     lib.gma_oracle_state.argtypes = [ci, ci, ci, ci, ci, ci, dp, dp, dp, dp, dp, dp, dp]
     lib.gma_oracle_state.restype = ci
     if path is None:
@@ -168,8 +171,8 @@ def state(Kx, V, mu, sigma2, log_pi, lib=None):
     return Vt, Z
 
 
-def backward_bidir(Q, Kx, V, mu, sigma2, log_pi, eps, dO, lib=None):
-    """(dQ, dK, dV, dmu, dsigma2, dlog_pi) of the bidirectional forward given dO [B,H,N,dv]."""
+def backward_bidir(Q, Kx, V, mu, sigma2, log_pi, eps, dO, lib=None, causal=False):
+    """(dQ, dK, dV, dmu, dsigma2, dlog_pi) of the bidirectional (or causal) forward given dO [B,H,N,dv]."""
     Q, Kx, V, dO = _f64(Q), _f64(Kx), _f64(V), _f64(dO)
     mu, sigma2, log_pi = _f64(mu), _f64(sigma2), _f64(log_pi)
     B, H, N, d = Q.shape
@@ -179,7 +182,12 @@ def backward_bidir(Q, Kx, V, mu, sigma2, log_pi, eps, dO, lib=None):
     dQ, dK, dV = np.empty_like(Q), np.empty_like(Kx), np.empty_like(V)
     dmu, dsigma2, dlog_pi = np.empty_like(mu), np.empty_like(sigma2), np.empty_like(log_pi)
     lib = lib or _load()
-    lib.gma_oracle_backward_bidir(B, H, N, d, dv, K, _ptr(Q), _ptr(Kx), _ptr(V), _ptr(mu), _ptr(sigma2), _ptr(log_pi),
-                                  float(eps), _ptr(dO), _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(dmu), _ptr(dsigma2),
-                                  _ptr(dlog_pi))
+    fn = lib.gma_oracle_backward_causal if causal else lib.gma_oracle_backward_bidir
+    fn(B, H, N, d, dv, K, _ptr(Q), _ptr(Kx), _ptr(V), _ptr(mu), _ptr(sigma2), _ptr(log_pi), float(eps), _ptr(dO),
+       _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(dmu), _ptr(dsigma2), _ptr(dlog_pi))
     return dQ, dK, dV, dmu, dsigma2, dlog_pi
+
+
+def backward_causal(Q, Kx, V, mu, sigma2, log_pi, eps, dO, lib=None):
+    """(dQ, dK, dV, dmu, dsigma2, dlog_pi) of the causal forward given dO [B,H,N,dv]."""
+    return backward_bidir(Q, Kx, V, mu, sigma2, log_pi, eps, dO, lib=lib, causal=True)

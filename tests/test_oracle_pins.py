@@ -331,7 +331,7 @@ def test_cross_key_permutation_invariance():
 
 # ----------------------------------------------------------------------------- backward
 
-def _fd_grads(Q, Kx, V, mu, sigma2, log_pi, eps, G, h=1e-6, lib=None):
+def _fd_grads(Q, Kx, V, mu, sigma2, log_pi, eps, G, h=1e-6, lib=None, causal=False):
     """Central finite differences of L = sum(O * G) through the forward oracle, every element."""
     args = [Q, Kx, V, mu, sigma2, log_pi]
     out = []
@@ -342,9 +342,9 @@ def _fd_grads(Q, Kx, V, mu, sigma2, log_pi, eps, G, h=1e-6, lib=None):
             vals = [x.copy() for x in args]
             step = h * max(1.0, abs(vals[a].reshape(-1)[idx]))
             vals[a].reshape(-1)[idx] += step
-            lp = (orc.forward(*vals, eps, causal=False, lib=lib) * G).sum()
+            lp = (orc.forward(*vals, eps, causal=causal, lib=lib) * G).sum()
             vals[a].reshape(-1)[idx] -= 2 * step
-            lm = (orc.forward(*vals, eps, causal=False, lib=lib) * G).sum()
+            lm = (orc.forward(*vals, eps, causal=causal, lib=lib) * G).sum()
             flat[idx] = (lp - lm) / (2 * step)
         out.append(g)
     return out
@@ -359,6 +359,28 @@ def test_backward_matches_finite_differences(eps):
     for name, a, b in zip(("dQ", "dK", "dV", "dmu", "dsigma2", "dlog_pi"), got, want):
         assert a.shape == b.shape, name
         assert np.abs(a - b).max() <= 1e-6 * max(1.0, np.abs(b).max()), name
+
+
+@pytest.mark.parametrize("eps", [1e-6, 0.37])
+def test_causal_backward_matches_finite_differences(eps):
+    Q, Kx, V, mu, sigma2, log_pi = _small_problem(41, B=2, H=2, N=6, d=3, dv=2, K=3, smin=0.3)
+    G = _rng(42).standard_normal((2, 2, 6, 2))
+    got = orc.backward_causal(Q, Kx, V, mu, sigma2, log_pi, eps, G)
+    want = _fd_grads(Q, Kx, V, mu, sigma2, log_pi, eps, G, causal=True)
+    for name, a, b in zip(("dQ", "dK", "dV", "dmu", "dsigma2", "dlog_pi"), got, want):
+        assert a.shape == b.shape, name
+        assert np.abs(a - b).max() <= 1e-6 * max(1.0, np.abs(b).max()), name
+
+
+def test_causal_backward_last_row_only_matches_bidir():
+    # a loss on the last output alone: that row sees every key, as in the bidirectional form
+    Q, Kx, V, mu, sigma2, log_pi = _small_problem(43, B=1, H=2, N=8, d=4, dv=3, K=4, smin=0.3)
+    G = np.zeros((1, 2, 8, 3))
+    G[:, :, -1] = _rng(44).standard_normal((1, 2, 3))
+    c = orc.backward_causal(Q, Kx, V, mu, sigma2, log_pi, 1e-6, G)
+    b = orc.backward_bidir(Q, Kx, V, mu, sigma2, log_pi, 1e-6, G)
+    for x, y in zip(c, b):
+        assert np.abs(x - y).max() <= 1e-12 * max(1.0, np.abs(y).max())
 
 
 def test_backward_prior_gradient_sums_to_zero():
@@ -395,6 +417,9 @@ MUTANTS = {
     "cross_write_over_queries": ("for (int j = 0; j < Nk; ++j) {", "for (int j = 0; j < N && j < Nk; ++j) {"),
     "bwd_drops_denominator_term": ("const double dden = -gdoto / den;", "const double dden = 0.0 * gdoto;"),
     "bwd_variance_sign": ("0.5 * (diff * diff / (s2 * s2) - 1.0 / s2)", "0.5 * (diff * diff / (s2 * s2) + 1.0 / s2)"),
+    "bwd_causal_suffix_excludes_own_query": (
+        "for (int c = 0; c < C; ++c) R[(size_t)k * C + c] += gqj[k] * uj[c];\n      for (int k = 0; k < K; ++k) {\n        double s = R[(size_t)k * C + dv];",
+        "for (int c = 0; c < C; ++c) R[(size_t)k * C + c] += 0.0 * gqj[k] * uj[c];\n      for (int k = 0; k < K; ++k) {\n        double s = R[(size_t)k * C + dv];"),
     "bwd_softmax_no_centering": ("dl[k] = g[k] * (dg[k] - dot);", "dl[k] = g[k] * dg[k];"),
     "causal_drops_first_key": ("int64_t want = J->rows ? J->rows[r] : i;",
                          "int64_t want = J->rows ? J->rows[r] : i; if (i == 0) { memset(Vt, 0, sizeof(double) * K * dv); memset(Z, 0, sizeof(double) * K); }"),
@@ -414,11 +439,12 @@ def _pins_pass(lib) -> bool:
             return False
         Q, Kx, V, mu, sigma2, log_pi = _small_problem(23, B=1, H=2, N=4, d=2, dv=2, K=3, smin=0.3)
         G = _rng(24).standard_normal((1, 2, 4, 2))
-        got = orc.backward_bidir(Q, Kx, V, mu, sigma2, log_pi, 0.37, G, lib=lib)
-        want = _fd_grads(Q, Kx, V, mu, sigma2, log_pi, 0.37, G, lib=lib)
-        for a, b in zip(got, want):
-            if np.abs(a - b).max() > 1e-6 * max(1.0, np.abs(b).max()):
-                return False
+        for causal in (False, True):
+            got = orc.backward_bidir(Q, Kx, V, mu, sigma2, log_pi, 0.37, G, lib=lib, causal=causal)
+            want = _fd_grads(Q, Kx, V, mu, sigma2, log_pi, 0.37, G, lib=lib, causal=causal)
+            for a, b in zip(got, want):
+                if np.abs(a - b).max() > 1e-6 * max(1.0, np.abs(b).max()):
+                    return False
         Q, Kx, V, mu, sigma2, log_pi = _cross_problem(22, 7, 13)
         O = orc.forward_cross(Q, Kx, V, mu, sigma2, log_pi, 0.37, lib=lib)
         if np.abs(O - _brute_cross(Q, Kx, V, mu, sigma2, log_pi, 0.37)).max() > 1e-10:
