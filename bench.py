@@ -456,7 +456,22 @@ def run_gma(args, world, rank, local):
             "ms": mb / 5, "tok_heads_per_s": wb.B * wb.H * wb.N / (mb / 5 * 1e-3), "forward_ms": mf / 5,
             "backward_over_forward": mb / mf, "workspace_bytes": wsb.numel(),
             "note": "float32 CUDA-core kernels (no tensor cores yet)"}
-        del bi, gO, wsb
+        del wsb
+        pbc = gma.problem(wb.B, wb.H, wb.N, wb.K, torch.bfloat16, wb.eps)
+        wsc = gma.alloc_workspace(pbc, gma.OP_BACKWARD_CAUSAL, dev)
+        callc = lambda: gma.backward_causal(bi["Q"], bi["K"], bi["V"], bi["mu"], bi["sigma2"], bi["log_pi"], gO,
+                                            wb.eps, workspace=wsc)
+        callfc = lambda: gma.forward_causal(bi["Q"], bi["K"], bi["V"], bi["mu"], bi["sigma2"], bi["log_pi"], wb.eps)
+        for _ in range(2):
+            callc()
+            callfc()
+        mc, _ = timed(callc, 3)
+        mfc, _ = timed(callfc, 5)
+        extensions["backward_causal_bf16_B4H8N4096K128"] = {
+            "ms": mc / 3, "tok_heads_per_s": wb.B * wb.H * wb.N / (mc / 3 * 1e-3), "forward_ms": mfc / 5,
+            "backward_over_forward": (mc / 3) / (mfc / 5), "workspace_bytes": wsc.numel(),
+            "note": "float32 CUDA-core kernels (no tensor cores yet)"}
+        del bi, gO, wsc
 
     # CPU baseline: the oracle as it stands on a bounded sample of the same workload (rank 0 only)
     cpu = None

@@ -32,7 +32,10 @@ gma_status_t check_launch(const char* step, const void* func) {
 }
 
 gma_status_t set_smem_optin(const void* func, int bytes, int /*slot*/) {
-  if (bytes <= 48 * 1024) return GMA_OK;
+  // the default limit on dynamic shared memory is 48 KB minus the kernel's static shared memory
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, func) != cudaSuccess) return cuda_fail("cudaFuncGetAttributes", cudaSuccess, func);
+  if ((size_t)bytes + fa.sharedSizeBytes <= 48 * 1024) return GMA_OK;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return GMA_ERR_CUDA;
   struct Entry { const void* f; int dev; int bytes; };
@@ -64,7 +67,7 @@ gma_status_t validate_problem(const gma_problem_t* p) {
 size_t required_bytes(const gma_problem_t& p, gma_op_t op) {
   if (op == GMA_OP_CROSS) op = GMA_OP_BIDIR;  // the same workspace: it does not depend on N
   if (op == GMA_OP_CAUSAL_DECODE) return align_up(sizeof(Ctrl));  // a control block; the kernel needs no scratch
-  if (op == GMA_OP_BACKWARD_BIDIR) return simt_backward_bytes(p);
+  if (op == GMA_OP_BACKWARD_BIDIR || op == GMA_OP_BACKWARD_CAUSAL) return simt_backward_bytes(p, op == GMA_OP_BACKWARD_CAUSAL);
   if (p.dtype == GMA_BF16) return tc_plan(p, op).total;
   return simt_plan(p, op).total;
 }
@@ -96,6 +99,35 @@ gma_status_t run(const gma_problem_t* p, gma_op_t op, int Nk, const void* Q, con
   return simt_run(*p, op, Nk, Q, K, V, mu, sigma2, log_pi, out, ws, st);
 }
 
+gma_status_t run_backward(const gma_problem_t* p, bool causal, const void* Q, const void* K, const void* V, const float* mu,
+                                const float* sigma2, const float* log_pi, const void* dO, void* dQ, void* dK, void* dV,
+                                float* dmu, float* dsigma2, float* dlog_pi, void* ws, size_t ws_bytes, void* stream) {
+  gma_status_t s = validate_problem(p);
+  if (s != GMA_OK) return s;
+  if (!mu || !sigma2 || !log_pi || !ws || !dmu || !dsigma2 || !dlog_pi) return GMA_ERR_INVALID_ARG;
+  const void* ins[] = {Q, K, V, mu, sigma2, log_pi, dO};
+  const void* outs[] = {dQ, dK, dV, dmu, dsigma2, dlog_pi};
+  if (p->N > 0)
+    for (const void* q : ins)
+      if (!q) return GMA_ERR_INVALID_ARG;
+  if (p->N > 0 && (!dQ || !dK || !dV)) return GMA_ERR_INVALID_ARG;
+  for (const void* q : ins)
+    if (q && !aligned(q, 16)) return GMA_ERR_INVALID_ARG;
+  for (const void* q : outs) {
+    if (q && !aligned(q, 16)) return GMA_ERR_INVALID_ARG;
+    for (const void* r : ins)
+      if (q && q == r) return GMA_ERR_INVALID_ARG;
+  }
+  for (int i = 0; i < 6; ++i)
+    for (int j = i + 1; j < 6; ++j)
+      if (outs[i] && outs[i] == outs[j]) return GMA_ERR_INVALID_ARG;
+  if (!aligned(ws, kAlign)) return GMA_ERR_INVALID_ARG;
+  if (ws_bytes < required_bytes(*p, causal ? GMA_OP_BACKWARD_CAUSAL : GMA_OP_BACKWARD_BIDIR)) return GMA_ERR_WORKSPACE;
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaGetLastError();
+  return simt_backward(*p, causal, Q, K, V, mu, sigma2, log_pi, dO, dQ, dK, dV, dmu, dsigma2, dlog_pi, ws, st);
+}
+
 }  // namespace
 }  // namespace gma
 
@@ -105,7 +137,7 @@ extern "C" {
 
 size_t gma_workspace_bytes(const gma_problem_t* p, gma_op_t op) {
   if (validate_problem(p) != GMA_OK) return 0;
-  if (op < GMA_OP_RESPONSIBILITIES || op > GMA_OP_BACKWARD_BIDIR) return 0;
+  if (op < GMA_OP_RESPONSIBILITIES || op > GMA_OP_BACKWARD_CAUSAL) return 0;
   return required_bytes(*p, op);
 }
 
@@ -176,33 +208,19 @@ gma_status_t gma_causal_decode(const gma_problem_t* p, const void* Q, const void
   return simt_decode(*p, Q, K, V, mu, sigma2, log_pi, state, O, ws, st);
 }
 
+
 gma_status_t gma_backward_bidir(const gma_problem_t* p, const void* Q, const void* K, const void* V, const float* mu,
                                 const float* sigma2, const float* log_pi, const void* dO, void* dQ, void* dK, void* dV,
                                 float* dmu, float* dsigma2, float* dlog_pi, void* ws, size_t ws_bytes, void* stream) {
-  gma_status_t s = validate_problem(p);
-  if (s != GMA_OK) return s;
-  if (!mu || !sigma2 || !log_pi || !ws || !dmu || !dsigma2 || !dlog_pi) return GMA_ERR_INVALID_ARG;
-  const void* ins[] = {Q, K, V, mu, sigma2, log_pi, dO};
-  const void* outs[] = {dQ, dK, dV, dmu, dsigma2, dlog_pi};
-  if (p->N > 0)
-    for (const void* q : ins)
-      if (!q) return GMA_ERR_INVALID_ARG;
-  if (p->N > 0 && (!dQ || !dK || !dV)) return GMA_ERR_INVALID_ARG;
-  for (const void* q : ins)
-    if (q && !aligned(q, 16)) return GMA_ERR_INVALID_ARG;
-  for (const void* q : outs) {
-    if (q && !aligned(q, 16)) return GMA_ERR_INVALID_ARG;
-    for (const void* r : ins)
-      if (q && q == r) return GMA_ERR_INVALID_ARG;
-  }
-  for (int i = 0; i < 6; ++i)
-    for (int j = i + 1; j < 6; ++j)
-      if (outs[i] && outs[i] == outs[j]) return GMA_ERR_INVALID_ARG;
-  if (!aligned(ws, kAlign)) return GMA_ERR_INVALID_ARG;
-  if (ws_bytes < required_bytes(*p, GMA_OP_BACKWARD_BIDIR)) return GMA_ERR_WORKSPACE;
-  cudaStream_t st = (cudaStream_t)stream;
-  cudaGetLastError();
-  return simt_backward(*p, Q, K, V, mu, sigma2, log_pi, dO, dQ, dK, dV, dmu, dsigma2, dlog_pi, ws, st);
+  return gma::run_backward(p, false, Q, K, V, mu, sigma2, log_pi, dO, dQ, dK, dV, dmu, dsigma2, dlog_pi, ws, ws_bytes,
+                           stream);
+}
+
+gma_status_t gma_backward_causal(const gma_problem_t* p, const void* Q, const void* K, const void* V, const float* mu,
+                                 const float* sigma2, const float* log_pi, const void* dO, void* dQ, void* dK, void* dV,
+                                 float* dmu, float* dsigma2, float* dlog_pi, void* ws, size_t ws_bytes, void* stream) {
+  return gma::run_backward(p, true, Q, K, V, mu, sigma2, log_pi, dO, dQ, dK, dV, dmu, dsigma2, dlog_pi, ws, ws_bytes,
+                           stream);
 }
 
 gma_status_t gma_check_device_error(void* ws, void* stream) {

@@ -58,9 +58,9 @@ gma_status_t tc_run(const gma_problem_t& p, gma_op_t op, int Nk, const void* Q, 
                     const float* mu, const float* sigma2, const float* log_pi, void* out, void* ws,
                     cudaStream_t stream);
 bool tc_available();
-// Backward pass of the bidirectional forward (float32 CUDA-core kernels, both I/O dtypes).
-size_t simt_backward_bytes(const gma_problem_t& p);
-gma_status_t simt_backward(const gma_problem_t& p, const void* Q, const void* K, const void* V, const float* mu,
+// Backward pass of the bidirectional or causal forward (float32 CUDA-core kernels, both I/O dtypes).
+size_t simt_backward_bytes(const gma_problem_t& p, bool causal);
+gma_status_t simt_backward(const gma_problem_t& p, bool causal, const void* Q, const void* K, const void* V, const float* mu,
                            const float* sigma2, const float* log_pi, const void* dO, void* dQ, void* dK, void* dV,
                            float* dmu, float* dsigma2, float* dlog_pi, void* ws, cudaStream_t stream);
 // Decode T = p.N new tokens per (b, h) against `state` (float32 [B*H][K][dv + 1], in place).

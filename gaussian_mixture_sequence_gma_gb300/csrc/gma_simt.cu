@@ -506,6 +506,228 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_key_kernel(const IO* __rest
   dx_tile<IO>(xs, dG, nvalid, mu, sigma2, h, K, dK + ((size_t)unit * N + t0) * kD);
 }
 
+// ---- causal backward.  S_i = sum_{j <= i} gamma_Kj [v_j | 1] (running state), u_i = [G_i / den_i |
+// -(G_i . O_i) / den_i], R_j = sum_{i >= j} gamma_Qi u_i^T (suffix sum of the queries' contributions):
+//   dgamma_Qi = S_i u_i,   dgamma_Kj = R_j [v_j | 1],   dv_j = R_j[:, :dv]^T gamma_Kj.
+// Chunked like the forward: segment aggregates and an exclusive scan give S at each segment start; the
+// query pass walks its segment forward (intra-tile terms masked to j <= i) and leaves the segment's
+// aggregate of gamma_Q u^T; an exclusive suffix scan gives R after each segment; the key pass walks its
+// segment backward.
+
+// Masked tile products for the causal backward: A_ij = gQ_i . gK_j and W_ij = u_i . [v_j | 1] for j <= i.
+__device__ void causal_tile_products(const float* GQ, const float* GK, const float* us, const float* vs, int K,
+                                     float* A, float* W) {
+  for (int p = threadIdx.x; p < T * T; p += blockDim.x) {
+    const int i = p / T, j = p % T;
+    float a = 0.f, w = 0.f;
+    if (j <= i) {
+      for (int k = 0; k < K; ++k) a = fmaf(GQ[i * K + k], GK[j * K + k], a);
+      w = us[i * kStateCols + kDv];
+      for (int c = 0; c < kDv; ++c) w = fmaf(us[i * kStateCols + c], vs[j * kDv + c], w);
+    }
+    A[p] = a;
+    W[p] = w;
+  }
+}
+
+// Query side: grid (segments, B*H).  S starts at agg[unit][seg] (scanned); writes u, dl_Q, dQ and the
+// segment aggregate sum_i gamma_Qi u_i^T into bagg[unit][seg].
+template <typename IO>
+__global__ void __launch_bounds__(kThreads) simt_bwd_causal_query_kernel(
+    const IO* __restrict__ Q, const IO* __restrict__ Kx, const IO* __restrict__ V, const IO* __restrict__ dO,
+    float* params, const float* __restrict__ mu, const float* __restrict__ sigma2, int H, int N, int K, int seg_tiles,
+    int P, const float* agg, float eps, float* bagg, float* uglob, float* dlq, IO* __restrict__ dQ) {
+  extern __shared__ float sm[];
+  const int npairs = K * kStateCols;
+  float* S = sm;                   // [K][65]
+  float* xs = S + npairs;          // [T][64]  queries, then keys
+  float* vs = xs + T * kD;         // [T][64]
+  float* gs = vs + T * kDv;        // [T][64]  dO rows
+  float* us = gs + T * kDv;        // [T][65]  numerators, then u
+  float* GQ = us + T * kStateCols;  // [T][K]
+  float* GK = GQ + T * K;          // [T][K]
+  float* dG = GK + T * K;          // [T][K]
+  float* A = dG + T * K;           // [T][T]
+  float* W = A + T * T;            // [T][T]
+  __shared__ float xq[T * kD];     // the query rows, kept for dQ
+  const int unit = blockIdx.y, h = unit % H, seg = blockIdx.x;
+  const SimtParams Pp = params_at(params, H, K);
+  const float* S0 = agg + ((size_t)unit * P + seg) * npairs;
+  float* bout = bagg + ((size_t)unit * P + seg) * npairs;
+  for (int p = threadIdx.x; p < npairs; p += blockDim.x) {
+    S[p] = S0[p];
+    bout[p] = 0.f;
+  }
+  const int tiles = (N + T - 1) / T;
+  const int tb = seg * seg_tiles, te = min(tiles, tb + seg_tiles);
+  for (int t = tb; t < te; ++t) {
+    const int t0 = t * T, nvalid = min(T, N - t0);
+    __syncthreads();
+    load_rows<IO>(Q + (size_t)unit * N * kD, t0, nvalid, xq);
+    load_rows<IO>(dO + (size_t)unit * N * kDv, t0, nvalid, gs);
+    __syncthreads();
+    gamma_tile(xq, nvalid, Pp, h, K, GQ);
+    load_rows<IO>(Kx + (size_t)unit * N * kD, t0, nvalid, xs);
+    load_rows<IO>(V + (size_t)unit * N * kDv, t0, nvalid, vs);
+    __syncthreads();
+    gamma_tile(xs, nvalid, Pp, h, K, GK);
+    // numerators [num | den - eps] of the causal output: gQ_i . S + sum_{j <= i} A_ij [v_j | 1]
+    for (int p = threadIdx.x; p < T * T; p += blockDim.x) {
+      const int i = p / T, j = p % T;
+      float a = 0.f;
+      if (j <= i)
+        for (int k = 0; k < K; ++k) a = fmaf(GQ[i * K + k], GK[j * K + k], a);
+      A[p] = a;
+    }
+    __syncthreads();
+    for (int p = threadIdx.x; p < T * kStateCols; p += blockDim.x) {
+      const int i = p / kStateCols, c = p % kStateCols;
+      float s = 0.f;
+      for (int k = 0; k < K; ++k) s = fmaf(GQ[i * K + k], S[k * kStateCols + c], s);
+      if (c < kDv) {
+        for (int j = 0; j <= i; ++j) s = fmaf(A[i * T + j], vs[j * kDv + c], s);
+      } else {
+        for (int j = 0; j <= i; ++j) s += A[i * T + j];
+      }
+      us[p] = s;
+    }
+    __syncthreads();
+    {  // one warp per row: O, G . O, then u (rows past N: zero)
+      const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+      for (int i = warp; i < T; i += nwarps) {
+        float* ui = us + i * kStateCols;
+        if (i >= nvalid) {
+          ui[lane] = 0.f;
+          ui[32 + lane] = 0.f;
+          if (lane == 0) ui[kDv] = 0.f;
+          continue;
+        }
+        const float den = ui[kDv] + eps;
+        const float o0 = ui[lane] / den, o1 = ui[32 + lane] / den;
+        float go = gs[i * kDv + lane] * o0 + gs[i * kDv + 32 + lane] * o1;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) go += __shfl_xor_sync(0xffffffffu, go, o);
+        __syncwarp();
+        ui[lane] = gs[i * kDv + lane] / den;
+        ui[32 + lane] = gs[i * kDv + 32 + lane] / den;
+        if (lane == 0) ui[kDv] = -go / den;
+      }
+    }
+    __syncthreads();
+    float* ug = uglob + ((size_t)unit * N + t0) * kStateCols;
+    for (int p = threadIdx.x; p < nvalid * kStateCols; p += blockDim.x) ug[p] = us[p];
+    causal_tile_products(GQ, GK, us, vs, K, A, W);
+    __syncthreads();
+    for (int p = threadIdx.x; p < T * K; p += blockDim.x) {  // dgamma_Q = S u + sum_{j <= i} W_ij gK_j
+      const int i = p / K, k = p % K;
+      float s = 0.f;
+      for (int c = 0; c < kStateCols; ++c) s = fmaf(S[k * kStateCols + c], us[i * kStateCols + c], s);
+      for (int j = 0; j <= i; ++j) s = fmaf(W[i * T + j], GK[j * K + k], s);
+      dG[p] = s;
+    }
+    __syncthreads();
+    for (int p = threadIdx.x; p < npairs; p += blockDim.x) {  // segment aggregate and the running state
+      const int k = p / kStateCols, c = p % kStateCols;
+      float b = 0.f, a = 0.f;
+      for (int i = 0; i < T; ++i) b = fmaf(GQ[i * K + k], us[i * kStateCols + c], b);
+      if (c < kDv) {
+        for (int j = 0; j < T; ++j) a = fmaf(GK[j * K + k], vs[j * kDv + c], a);
+      } else {
+        for (int j = 0; j < T; ++j) a += GK[j * K + k];
+      }
+      bout[p] += b;
+      S[p] += a;
+    }
+    __syncthreads();
+    softmax_backward_tile(GQ, dG, K);
+    float* dst = dlq + ((size_t)unit * N + t0) * K;
+    for (int p = threadIdx.x; p < nvalid * K; p += blockDim.x) dst[p] = dG[p];
+    dx_tile<IO>(xq, dG, nvalid, mu, sigma2, h, K, dQ + ((size_t)unit * N + t0) * kD);
+  }
+}
+
+// Exclusive suffix scan over segments: bagg[unit][p][e] <- sum_{p' > p} bagg[unit][p'][e].
+__global__ void simt_rscan_kernel(float* bagg, int P, int npairs) {
+  const int unit = blockIdx.y;
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= npairs) return;
+  float* base = bagg + (size_t)unit * P * npairs + e;
+  float run = 0.f;
+  for (int p = P - 1; p >= 0; --p) {
+    const float t = base[(size_t)p * npairs];
+    base[(size_t)p * npairs] = run;
+    run += t;
+  }
+}
+
+// Key side: grid (segments, B*H).  R starts at bagg[unit][seg] (suffix-scanned) and the segment's tiles are
+// walked last to first; writes dl_K, dK and dV.
+template <typename IO>
+__global__ void __launch_bounds__(kThreads) simt_bwd_causal_key_kernel(
+    const IO* __restrict__ Q, const IO* __restrict__ Kx, const IO* __restrict__ V, float* params,
+    const float* __restrict__ mu, const float* __restrict__ sigma2, int H, int N, int K, int seg_tiles, int P,
+    const float* bagg, const float* uglob, float* dlk, IO* __restrict__ dK, IO* __restrict__ dV) {
+  extern __shared__ float sm[];
+  const int npairs = K * kStateCols;
+  float* R = sm;                   // [K][65]
+  float* xs = R + npairs;          // [T][64]  queries, then keys
+  float* vs = xs + T * kD;         // [T][64]
+  float* us = vs + T * kDv;        // [T][65]
+  float* GQ = us + T * kStateCols;  // [T][K]
+  float* GK = GQ + T * K;          // [T][K]
+  float* dG = GK + T * K;          // [T][K]
+  float* A = dG + T * K;           // [T][T]
+  float* W = A + T * T;            // [T][T]
+  const int unit = blockIdx.y, h = unit % H, seg = blockIdx.x;
+  const SimtParams Pp = params_at(params, H, K);
+  const float* R0 = bagg + ((size_t)unit * P + seg) * npairs;
+  for (int p = threadIdx.x; p < npairs; p += blockDim.x) R[p] = R0[p];
+  const int tiles = (N + T - 1) / T;
+  const int tb = seg * seg_tiles, te = min(tiles, tb + seg_tiles);
+  for (int t = te - 1; t >= tb; --t) {
+    const int t0 = t * T, nvalid = min(T, N - t0);
+    __syncthreads();
+    load_rows<IO>(Q + (size_t)unit * N * kD, t0, nvalid, xs);
+    for (int p = threadIdx.x; p < T * kStateCols; p += blockDim.x)
+      us[p] = p < nvalid * kStateCols ? uglob[((size_t)unit * N + t0) * kStateCols + p] : 0.f;
+    __syncthreads();
+    gamma_tile(xs, nvalid, Pp, h, K, GQ);
+    load_rows<IO>(Kx + (size_t)unit * N * kD, t0, nvalid, xs);
+    load_rows<IO>(V + (size_t)unit * N * kDv, t0, nvalid, vs);
+    __syncthreads();
+    gamma_tile(xs, nvalid, Pp, h, K, GK);
+    causal_tile_products(GQ, GK, us, vs, K, A, W);
+    __syncthreads();
+    for (int p = threadIdx.x; p < T * K; p += blockDim.x) {  // dgamma_K = R [v | 1] + sum_{i >= j} W_ij gQ_i
+      const int j = p / K, k = p % K;
+      float s = R[k * kStateCols + kDv];
+      for (int c = 0; c < kDv; ++c) s = fmaf(R[k * kStateCols + c], vs[j * kDv + c], s);
+      for (int i = j; i < T; ++i) s = fmaf(W[i * T + j], GQ[i * K + k], s);
+      dG[p] = s;
+    }
+    IO* dv_out = dV + ((size_t)unit * N + t0) * kDv;
+    for (int p = threadIdx.x; p < nvalid * kDv; p += blockDim.x) {  // dv = R^T gK + sum_{i >= j} A_ij dn_i
+      const int j = p / kDv, c = p % kDv;
+      float s = 0.f;
+      for (int k = 0; k < K; ++k) s = fmaf(GK[j * K + k], R[k * kStateCols + c], s);
+      for (int i = j; i < T; ++i) s = fmaf(A[i * T + j], us[i * kStateCols + c], s);
+      st_io<IO>(dv_out + p, s);
+    }
+    __syncthreads();
+    for (int p = threadIdx.x; p < npairs; p += blockDim.x) {  // R += gamma_Q^T u over the whole tile
+      const int k = p / kStateCols, c = p % kStateCols;
+      float b = 0.f;
+      for (int i = 0; i < T; ++i) b = fmaf(GQ[i * K + k], us[i * kStateCols + c], b);
+      R[p] += b;
+    }
+    __syncthreads();
+    softmax_backward_tile(GK, dG, K);
+    float* dst = dlk + ((size_t)unit * N + t0) * K;
+    for (int p = threadIdx.x; p < nvalid * K; p += blockDim.x) dst[p] = dG[p];
+    dx_tile<IO>(xs, dG, nvalid, mu, sigma2, h, K, dK + ((size_t)unit * N + t0) * kD);
+  }
+}
+
 // Parameter-gradient sums: grid (ceil(K / 32), H, chunks).  Thread (k within a block of 32, group of 8
 // dims) sums dl_k (x_d - mu_kd) and dl_k (x_d - mu_kd)^2 over its chunk of the head's rows (queries
 // then keys of every batch entry) and adds them into pacc[h][k][d][2] (and b_k into pb[h][k]).
@@ -745,64 +967,93 @@ __global__ void __launch_bounds__(kDecodeThreads) simt_decode_kernel(const IO* _
 
 }  // namespace
 
-// Workspace of the backward pass: control block | parameters | Vt|Z | dVt|dZ | parameter sums |
-// dl of the queries | dl of the keys.  The three accumulators are contiguous (zeroed together).
+// Workspace of the backward pass.  Bidirectional: control block | parameters | Vt|Z | dVt|dZ |
+// parameter sums | dl of the queries | dl of the keys (the three accumulators contiguous, zeroed
+// together).  Causal: control block | parameters | segment aggregates of the keys (scanned: S at each
+// segment start) | segment aggregates of the queries' gamma_Q u^T (suffix-scanned: R after each
+// segment) | parameter sums | u rows | dl of the queries | dl of the keys.
 struct BwdPlan {
-  size_t off_params, off_state, off_dstate, off_pacc, off_pb, off_dlq, off_dlk, total;
+  size_t off_params, off_state, off_dstate, off_pacc, off_pb, off_u, off_dlq, off_dlk, total;
   int splits, seg_tiles, tiles;
 };
-BwdPlan bwd_plan(const gma_problem_t& p) {
+BwdPlan bwd_plan(const gma_problem_t& p, bool causal) {
   BwdPlan b{};
-  const SimtPlan sp = simt_plan(p, GMA_OP_BIDIR);
+  const SimtPlan sp = simt_plan(p, causal ? GMA_OP_CAUSAL : GMA_OP_BIDIR);
   const size_t BH = (size_t)p.B * p.H, npairs = (size_t)p.K * kStateCols;
+  const size_t nstate = causal ? BH * sp.splits * npairs : BH * npairs;
   b.splits = sp.splits;
   b.seg_tiles = sp.seg_tiles;
   b.tiles = sp.tiles;
   b.off_params = sp.off_params;
-  b.off_state = sp.off_state;
-  b.off_dstate = b.off_state + BH * npairs * sizeof(float);
-  b.off_pacc = b.off_dstate + BH * npairs * sizeof(float);
+  b.off_state = align_up(sp.off_params + ((size_t)2 * p.H * kD * p.K + (size_t)p.H * p.K) * sizeof(float));
+  b.off_dstate = b.off_state + nstate * sizeof(float);
+  b.off_pacc = b.off_dstate + nstate * sizeof(float);
   b.off_pb = b.off_pacc + (size_t)p.H * p.K * kD * 2 * sizeof(float);
-  b.off_dlq = align_up(b.off_pb + (size_t)p.H * p.K * sizeof(float));
+  b.off_u = align_up(b.off_pb + (size_t)p.H * p.K * sizeof(float));
+  b.off_dlq = align_up(b.off_u + (causal ? BH * p.N * kStateCols * sizeof(float) : 0));
   b.off_dlk = align_up(b.off_dlq + BH * p.N * p.K * sizeof(float));
   b.total = align_up(b.off_dlk + BH * p.N * p.K * sizeof(float));
   return b;
 }
 
 template <typename IO>
-gma_status_t backward_typed(const gma_problem_t& p, const IO* Q, const IO* Kx, const IO* V, const float* mu,
-                            const float* sigma2, const float* log_pi, const IO* dO, IO* dQ, IO* dK, IO* dV, float* dmu,
-                            float* dsigma2, float* dlog_pi, void* ws, cudaStream_t st) {
-  const BwdPlan b = bwd_plan(p);
+gma_status_t backward_typed(const gma_problem_t& p, bool causal, const IO* Q, const IO* Kx, const IO* V,
+                            const float* mu, const float* sigma2, const float* log_pi, const IO* dO, IO* dQ, IO* dK,
+                            IO* dV, float* dmu, float* dsigma2, float* dlog_pi, void* ws, cudaStream_t st) {
+  const BwdPlan b = bwd_plan(p, causal);
   char* base = (char*)ws;
   float* params = (float*)(base + b.off_params);
   float* state = (float*)(base + b.off_state);
   float* dstate = (float*)(base + b.off_dstate);
   float* pacc = (float*)(base + b.off_pacc);
   float* pb = (float*)(base + b.off_pb);
+  float* urows = (float*)(base + b.off_u);
   float* dlq = (float*)(base + b.off_dlq);
   float* dlk = (float*)(base + b.off_dlk);
   const int BH = p.B * p.H, K = p.K, npairs = K * kStateCols;
-  const size_t zero_n = (b.off_dlq - b.off_state) / sizeof(float);
-  GMA_LAUNCH("simt_prep", simt_prep_kernel, 148, 256, 0, st, mu, sigma2, log_pi, p.H, K, params, (Ctrl*)base, state,
+  // bidirectional: zero Vt|Z, dVt|dZ and the parameter sums; causal: the parameter sums (the segment
+  // aggregates are stored whole)
+  float* zero = causal ? pacc : state;
+  const size_t zero_n = (b.off_u - (causal ? b.off_pacc : b.off_state)) / sizeof(float);
+  GMA_LAUNCH("simt_prep", simt_prep_kernel, 148, 256, 0, st, mu, sigma2, log_pi, p.H, K, params, (Ctrl*)base, zero,
              zero_n);
   if (gma_status_t e = check_launch("launch simt_prep", (const void*)simt_prep_kernel)) return e;
   if (p.N > 0) {
     const size_t sm_write = (size_t)(T * kD + T * kDv + T * K + npairs) * sizeof(float);
     if (set_smem_optin((const void*)simt_write_kernel<IO>, (int)sm_write, 1) != GMA_OK) return GMA_ERR_CUDA;
     GMA_LAUNCH("simt_write", simt_write_kernel<IO>, dim3(b.splits, BH), kThreads, sm_write, st, Kx, V, params, p.H,
-               p.N, K, b.seg_tiles, b.splits, state, 1);
+               p.N, K, b.seg_tiles, b.splits, state, causal ? 0 : 1);
     if (gma_status_t e = check_launch("launch simt_write", (const void*)simt_write_kernel<IO>)) return e;
-    const size_t sm_q = (size_t)(2 * npairs + T * kD + T * kDv + T * kStateCols + 2 * T * K) * sizeof(float);
-    if (set_smem_optin((const void*)simt_bwd_query_kernel<IO>, (int)sm_q, 5) != GMA_OK) return GMA_ERR_CUDA;
-    GMA_LAUNCH("simt_bwd_query", simt_bwd_query_kernel<IO>, dim3(b.splits, BH), kThreads, sm_q, st, Q, dO, params,
-               mu, sigma2, p.H, p.N, K, b.seg_tiles, state, p.eps, dstate, dlq, dQ);
-    if (gma_status_t e = check_launch("launch simt_bwd_query", (const void*)simt_bwd_query_kernel<IO>)) return e;
-    const size_t sm_k = (size_t)(npairs + T * kD + T * kDv + 2 * T * K) * sizeof(float);
-    if (set_smem_optin((const void*)simt_bwd_key_kernel<IO>, (int)sm_k, 6) != GMA_OK) return GMA_ERR_CUDA;
-    GMA_LAUNCH("simt_bwd_key", simt_bwd_key_kernel<IO>, dim3(b.tiles, BH), kThreads, sm_k, st, Kx, V, params, mu,
-               sigma2, p.H, p.N, K, dstate, dlk, dK, dV);
-    if (gma_status_t e = check_launch("launch simt_bwd_key", (const void*)simt_bwd_key_kernel<IO>)) return e;
+    if (causal) {
+      GMA_LAUNCH("simt_scan", simt_scan_kernel, dim3(cdiv(npairs, 256), BH), 256, 0, st, state, b.splits, npairs);
+      if (gma_status_t e = check_launch("launch simt_scan", (const void*)simt_scan_kernel)) return e;
+      const size_t sm_q = (size_t)(npairs + 3 * T * kD + T * kStateCols + 3 * T * K + 2 * T * T) * sizeof(float);
+      if (set_smem_optin((const void*)simt_bwd_causal_query_kernel<IO>, (int)sm_q, 7) != GMA_OK) return GMA_ERR_CUDA;
+      GMA_LAUNCH("simt_bwd_causal_query", simt_bwd_causal_query_kernel<IO>, dim3(b.splits, BH), kThreads, sm_q, st, Q,
+                 Kx, V, dO, params, mu, sigma2, p.H, p.N, K, b.seg_tiles, b.splits, state, p.eps, dstate, urows, dlq,
+                 dQ);
+      if (gma_status_t e = check_launch("launch simt_bwd_causal_query", (const void*)simt_bwd_causal_query_kernel<IO>))
+        return e;
+      GMA_LAUNCH("simt_rscan", simt_rscan_kernel, dim3(cdiv(npairs, 256), BH), 256, 0, st, dstate, b.splits, npairs);
+      if (gma_status_t e = check_launch("launch simt_rscan", (const void*)simt_rscan_kernel)) return e;
+      const size_t sm_k = (size_t)(npairs + 2 * T * kD + T * kStateCols + 3 * T * K + 2 * T * T) * sizeof(float);
+      if (set_smem_optin((const void*)simt_bwd_causal_key_kernel<IO>, (int)sm_k, 8) != GMA_OK) return GMA_ERR_CUDA;
+      GMA_LAUNCH("simt_bwd_causal_key", simt_bwd_causal_key_kernel<IO>, dim3(b.splits, BH), kThreads, sm_k, st, Q, Kx,
+                 V, params, mu, sigma2, p.H, p.N, K, b.seg_tiles, b.splits, dstate, urows, dlk, dK, dV);
+      if (gma_status_t e = check_launch("launch simt_bwd_causal_key", (const void*)simt_bwd_causal_key_kernel<IO>))
+        return e;
+    } else {
+      const size_t sm_q = (size_t)(2 * npairs + T * kD + T * kDv + T * kStateCols + 2 * T * K) * sizeof(float);
+      if (set_smem_optin((const void*)simt_bwd_query_kernel<IO>, (int)sm_q, 5) != GMA_OK) return GMA_ERR_CUDA;
+      GMA_LAUNCH("simt_bwd_query", simt_bwd_query_kernel<IO>, dim3(b.splits, BH), kThreads, sm_q, st, Q, dO, params,
+                 mu, sigma2, p.H, p.N, K, b.seg_tiles, state, p.eps, dstate, dlq, dQ);
+      if (gma_status_t e = check_launch("launch simt_bwd_query", (const void*)simt_bwd_query_kernel<IO>)) return e;
+      const size_t sm_k = (size_t)(npairs + T * kD + T * kDv + 2 * T * K) * sizeof(float);
+      if (set_smem_optin((const void*)simt_bwd_key_kernel<IO>, (int)sm_k, 6) != GMA_OK) return GMA_ERR_CUDA;
+      GMA_LAUNCH("simt_bwd_key", simt_bwd_key_kernel<IO>, dim3(b.tiles, BH), kThreads, sm_k, st, Kx, V, params, mu,
+                 sigma2, p.H, p.N, K, dstate, dlk, dK, dV);
+      if (gma_status_t e = check_launch("launch simt_bwd_key", (const void*)simt_bwd_key_kernel<IO>)) return e;
+    }
     const int rows_per_chunk = 2048;
     const long long rows = 2LL * p.B * p.N;
     const dim3 grid_p(cdiv(K, 32), p.H, cdiv(rows, rows_per_chunk));
@@ -815,17 +1066,17 @@ gma_status_t backward_typed(const gma_problem_t& p, const IO* Q, const IO* Kx, c
   return check_launch("launch simt_bwd_param_finish", (const void*)simt_bwd_param_finish_kernel);
 }
 
-size_t simt_backward_bytes(const gma_problem_t& p) { return bwd_plan(p).total; }
+size_t simt_backward_bytes(const gma_problem_t& p, bool causal) { return bwd_plan(p, causal).total; }
 
-gma_status_t simt_backward(const gma_problem_t& p, const void* Q, const void* K, const void* V, const float* mu,
-                           const float* sigma2, const float* log_pi, const void* dO, void* dQ, void* dK, void* dV,
-                           float* dmu, float* dsigma2, float* dlog_pi, void* ws, cudaStream_t st) {
+gma_status_t simt_backward(const gma_problem_t& p, bool causal, const void* Q, const void* K, const void* V,
+                           const float* mu, const float* sigma2, const float* log_pi, const void* dO, void* dQ,
+                           void* dK, void* dV, float* dmu, float* dsigma2, float* dlog_pi, void* ws, cudaStream_t st) {
   if (p.dtype == GMA_F32)
-    return backward_typed<float>(p, (const float*)Q, (const float*)K, (const float*)V, mu, sigma2, log_pi,
+    return backward_typed<float>(p, causal, (const float*)Q, (const float*)K, (const float*)V, mu, sigma2, log_pi,
                                  (const float*)dO, (float*)dQ, (float*)dK, (float*)dV, dmu, dsigma2, dlog_pi, ws, st);
   using bf = __nv_bfloat16;
-  return backward_typed<bf>(p, (const bf*)Q, (const bf*)K, (const bf*)V, mu, sigma2, log_pi, (const bf*)dO, (bf*)dQ,
-                            (bf*)dK, (bf*)dV, dmu, dsigma2, dlog_pi, ws, st);
+  return backward_typed<bf>(p, causal, (const bf*)Q, (const bf*)K, (const bf*)V, mu, sigma2, log_pi, (const bf*)dO,
+                            (bf*)dQ, (bf*)dK, (bf*)dV, dmu, dsigma2, dlog_pi, ws, st);
 }
 
 // Decode T new tokens per (b, h) from `state` (float32 [B*H][K][dv + 1], updated in place).  One launch;

@@ -811,14 +811,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           ok = warp_wait(&B.o_full, (t - 1) & 1, &B.ab, a.ctrl, 58, a.wait_ns);
           if (ok) {
             tc_fence_after();
-            uint32_t r[16], zc[16];
+            uint32_t r[16];
             tmem_ld16(tmem + rc.lane_base + kColAcc + 16 * rc.part, r);
-            tmem_ld16(tmem + rc.lane_base + kColAcc + 64, zc);  // zc[0] = gamma~ . (Z + eps)
-            tmem_ld_wait();
+            uint32_t zc = tmem_ld1(tmem + rc.lane_base + kColAcc + 64);  // gamma~ . (Z + eps)
+            tmem_ld_wait_tied1(zc);
+            tmem_ld_wait_tied16(r);
             tc_fence_before();
             warp_arrive(&B.o_empty);
             const int ptok = tok - kTile;
-            const float rden = rcp_approx(__uint_as_float(zc[0]));
+            const float rden = rcp_approx(__uint_as_float(zc));
             if (ptok < a.N)
               store_out16(reinterpret_cast<__nv_bfloat16*>(a.out) + ((size_t)bh * a.N + ptok) * kDv + 16 * rc.part,
                           r, rden);
@@ -844,12 +845,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     if (kRead && ok && T > 0) {
       if (warp_wait(&B.o_full, (T - 1) & 1, &B.ab, a.ctrl, 60, a.wait_ns)) {
         tc_fence_after();
-        uint32_t r[16], zc[16];
+        uint32_t r[16];
         tmem_ld16(tmem + rc.lane_base + kColAcc + 16 * rc.part, r);
-        tmem_ld16(tmem + rc.lane_base + kColAcc + 64, zc);
-        tmem_ld_wait();
+        uint32_t zc = tmem_ld1(tmem + rc.lane_base + kColAcc + 64);
+        tmem_ld_wait_tied1(zc);
+        tmem_ld_wait_tied16(r);
         const int ptok = (tile0 + T - 1) * kTile + rc.row;
-        const float rden = rcp_approx(__uint_as_float(zc[0]));
+        const float rden = rcp_approx(__uint_as_float(zc));
         if (ptok < a.N)
           store_out16(reinterpret_cast<__nv_bfloat16*>(a.out) + ((size_t)bh * a.N + ptok) * kDv + 16 * rc.part, r,
                       rden);

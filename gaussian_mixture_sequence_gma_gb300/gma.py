@@ -16,9 +16,10 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "li
 
 GMA_OK, GMA_ERR_INVALID_ARG, GMA_ERR_UNSUPPORTED, GMA_ERR_WORKSPACE, GMA_ERR_CUDA, GMA_ERR_TIMEOUT = range(6)
 GMA_F32, GMA_BF16 = 0, 1
-OP_RESPONSIBILITIES, OP_BIDIR, OP_CAUSAL, OP_CROSS, OP_CAUSAL_STATE, OP_CAUSAL_DECODE, OP_BACKWARD_BIDIR = range(7)
+(OP_RESPONSIBILITIES, OP_BIDIR, OP_CAUSAL, OP_CROSS, OP_CAUSAL_STATE, OP_CAUSAL_DECODE, OP_BACKWARD_BIDIR,
+ OP_BACKWARD_CAUSAL) = range(8)
 
-EXPORTED = ("gma_workspace_bytes", "gma_responsibilities", "gma_forward_bidir", "gma_forward_causal", "gma_forward_cross", "gma_state_bytes", "gma_causal_state", "gma_causal_decode", "gma_backward_bidir",
+EXPORTED = ("gma_workspace_bytes", "gma_responsibilities", "gma_forward_bidir", "gma_forward_causal", "gma_forward_cross", "gma_state_bytes", "gma_causal_state", "gma_causal_decode", "gma_backward_bidir", "gma_backward_causal",
             "gma_check_device_error", "gma_status_string", "gma_version", "gma_last_error", "gma_launch_count", "gma_profile_enable",
             "gma_profile_read", "gma_forward_bidir_static_ws", "gma_static_ws_capacity",
             "gma_debug_withhold_first_load", "gma_probe_ex2_rate")
@@ -77,6 +78,8 @@ def lib():
     L.gma_causal_decode.restype = ctypes.c_int
     L.gma_backward_bidir.argtypes = [pp, vp, vp, vp, fp, fp, fp, vp, vp, vp, vp, fp, fp, fp, vp, sz, vp]
     L.gma_backward_bidir.restype = ctypes.c_int
+    L.gma_backward_causal.argtypes = L.gma_backward_bidir.argtypes
+    L.gma_backward_causal.restype = ctypes.c_int
     L.gma_check_device_error.argtypes = [vp, vp]
     L.gma_check_device_error.restype = ctypes.c_int
     L.gma_status_string.argtypes = [ctypes.c_int]
@@ -290,7 +293,12 @@ def causal_decode(Q, K, V, mu, sigma2, log_pi, state, eps=1e-6, out=None, worksp
     return out
 
 
-def backward_bidir(Q, K, V, mu, sigma2, log_pi, dO, eps=1e-6, workspace=None, stream=None):
+def backward_causal(Q, K, V, mu, sigma2, log_pi, dO, eps=1e-6, workspace=None, stream=None):
+    """Gradients (dQ, dK, dV, dmu, dsigma2, dlog_pi) of the causal forward given dO [B,H,N,64]."""
+    return backward_bidir(Q, K, V, mu, sigma2, log_pi, dO, eps, workspace, stream, causal=True)
+
+
+def backward_bidir(Q, K, V, mu, sigma2, log_pi, dO, eps=1e-6, workspace=None, stream=None, causal=False):
     """Gradients (dQ, dK, dV, dmu, dsigma2, dlog_pi) of the bidirectional forward given dO [B,H,N,64]."""
     B, H, N, d = Q.shape
     dv = V.shape[-1]
@@ -302,14 +310,15 @@ def backward_bidir(Q, K, V, mu, sigma2, log_pi, dO, eps=1e-6, workspace=None, st
     prob = problem(B, H, N, Kc, Q.dtype, eps, d=d, dv=dv)
     dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
     dmu, dsigma2, dlog_pi = torch.empty_like(mu), torch.empty_like(sigma2), torch.empty_like(log_pi)
+    name = "gma_backward_causal" if causal else "gma_backward_bidir"
     if workspace is None:
-        workspace = alloc_workspace(prob, OP_BACKWARD_BIDIR, dev)
+        workspace = alloc_workspace(prob, OP_BACKWARD_CAUSAL if causal else OP_BACKWARD_BIDIR, dev)
     with torch.cuda.device(dev):
-        s = lib().gma_backward_bidir(ctypes.byref(prob), _ptr(Q), _ptr(K), _ptr(V), _ptr(mu), _ptr(sigma2),
+        s = getattr(lib(), name)(ctypes.byref(prob), _ptr(Q), _ptr(K), _ptr(V), _ptr(mu), _ptr(sigma2),
                                      _ptr(log_pi), _ptr(dO), _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(dmu), _ptr(dsigma2),
                                      _ptr(dlog_pi), _ptr(workspace), workspace.numel(), _stream_handle(stream, dev))
     if s != GMA_OK:
-        raise GmaError(s, "gma_backward_bidir")
+        raise GmaError(s, name)
     return dQ, dK, dV, dmu, dsigma2, dlog_pi
 
 

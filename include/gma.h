@@ -74,7 +74,8 @@ typedef enum {
   GMA_OP_CROSS = 3,
   GMA_OP_CAUSAL_STATE = 4,
   GMA_OP_CAUSAL_DECODE = 5,
-  GMA_OP_BACKWARD_BIDIR = 6
+  GMA_OP_BACKWARD_BIDIR = 6,
+  GMA_OP_BACKWARD_CAUSAL = 7
 } gma_op_t;
 
 typedef struct {
@@ -218,6 +219,20 @@ GMA_API gma_status_t gma_backward_bidir(const gma_problem_t *p, const void *Q, c
                                         const float *mu, const float *sigma2, const float *log_pi, const void *dO,
                                         void *dQ, void *dK, void *dV, float *dmu, float *dsigma2, float *dlog_pi,
                                         void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Backward pass of the causal forward: the same outputs, arguments and layouts as
+ * gma_backward_bidir, for O_i = gamma_Qi . Vt_i / (gamma_Qi . Z_i + eps) over the inclusive prefix
+ * j <= i.  Passage: gist.science summary, "Variants and training" item 3 (the causal form by prefix
+ * sums, trained end to end).  With S_i the running state, u_i = [G_i / den_i | -(G_i . O_i) / den_i] and
+ * R_j = sum_{i >= j} gamma_Qi u_i^T: dgamma_Qi = S_i u_i, dgamma_Kj = R_j [v_j | 1], dv_j = R_j^T gamma_Kj,
+ * computed per segment (forward over the queries, backward over the keys) on the CUDA cores in float32.
+ * Workspace: gma_workspace_bytes(p, GMA_OP_BACKWARD_CAUSAL), growing with N.
+ */
+GMA_API gma_status_t gma_backward_causal(const gma_problem_t *p, const void *Q, const void *K, const void *V,
+                                         const float *mu, const float *sigma2, const float *log_pi, const void *dO,
+                                         void *dQ, void *dK, void *dV, float *dmu, float *dsigma2, float *dlog_pi,
+                                         void *ws, size_t ws_bytes, void *stream);
 
 /*
  * Synchronises `stream`, then reads the error word kept at the start of `ws`:

@@ -153,7 +153,7 @@ def test_state_and_decode_argument_errors(L):
         for dt in (gma.GMA_F32, gma.GMA_BF16):
             n = gma.workspace_bytes(P(dtype=dt), op)
             assert n > 0 and n % 256 == 0
-    assert gma.workspace_bytes(P(), 7) == 0
+    assert gma.workspace_bytes(P(), 8) == 0
     ptr = [A + i * (1 << 16) for i in range(10)]
 
     def st(prob, p=ptr, ws_bytes=1 << 30):  # K, V, mu, sigma2, log_pi, state, ws
@@ -183,15 +183,16 @@ def test_state_and_decode_argument_errors(L):
     assert dec(P(N=0), nul) == gma.GMA_OK
 
 
-def test_backward_argument_errors(L):
+@pytest.mark.parametrize("name,op", [("gma_backward_bidir", 6), ("gma_backward_causal", 7)])
+def test_backward_argument_errors(L, name, op):
     for dt in (gma.GMA_F32, gma.GMA_BF16):
-        n1 = gma.workspace_bytes(P(dtype=dt, N=256), gma.OP_BACKWARD_BIDIR)
-        n2 = gma.workspace_bytes(P(dtype=dt, N=512), gma.OP_BACKWARD_BIDIR)
+        n1 = gma.workspace_bytes(P(dtype=dt, N=256), op)
+        n2 = gma.workspace_bytes(P(dtype=dt, N=512), op)
         assert n1 > 0 and n1 % 256 == 0 and n2 > n1  # holds the per-row softmax gradients
     ptr = [A + i * (1 << 16) for i in range(16)]
 
     def bwd(prob, p=ptr, ws_bytes=1 << 30):  # Q K V mu s2 lp dO | dQ dK dV dmu ds2 dlp | ws
-        return L.gma_backward_bidir(ctypes.byref(prob), *p[0:13], p[13], ws_bytes, None)
+        return getattr(L, name)(ctypes.byref(prob), *p[0:13], p[13], ws_bytes, None)
 
     assert bwd(P(d=32)) == gma.GMA_ERR_UNSUPPORTED
     assert bwd(P(K=0)) == gma.GMA_ERR_INVALID_ARG
@@ -208,7 +209,7 @@ def test_backward_argument_errors(L):
             assert bwd(P(), bad) == gma.GMA_ERR_INVALID_ARG, (o, i)
     bad = list(ptr); bad[13] += 16
     assert bwd(P(), bad) == gma.GMA_ERR_INVALID_ARG
-    assert bwd(P(), ws_bytes=gma.workspace_bytes(P(), gma.OP_BACKWARD_BIDIR) - 1) == gma.GMA_ERR_WORKSPACE
+    assert bwd(P(), ws_bytes=gma.workspace_bytes(P(), op) - 1) == gma.GMA_ERR_WORKSPACE
 
 
 def test_check_device_error_rejects_bad_workspace(L):

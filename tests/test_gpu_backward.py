@@ -1,5 +1,5 @@
-"""GPU parity of the bidirectional backward pass (gma_backward_bidir) against the float64 oracle's
-gradients, which are pinned by finite differences of the forward oracle.
+"""GPU parity of the backward passes (gma_backward_bidir, gma_backward_causal) against the float64
+oracle's gradients, which are pinned by finite differences of the forward oracle.
 
 Bar per gradient tensor: max |g_gpu - g_ref| / max |g_ref| <= 1e-3 (float32 I/O) or 2e-2 (bf16 I/O:
 inputs and dQ, dK, dV in bf16, float32 arithmetic)."""
@@ -28,14 +28,16 @@ def _dO(inp, seed):
     return round_bf16(G) if inp["dtype"] == "bf16" else G
 
 
-def check(gma, inp, eps=1e-6, seed=0):
+def check(gma, inp, eps=1e-6, seed=0, causal=False):
     import torch
     G = _dO(inp, seed)
     t = to_device(inp)
     gd = to_device(dict(Q=G, K=G, V=G, mu=inp["mu"], sigma2=inp["sigma2"], log_pi=inp["log_pi"], dtype=inp["dtype"]))["Q"]
-    got = gma.backward_bidir(t["Q"], t["K"], t["V"], t["mu"], t["sigma2"], t["log_pi"], gd, eps=eps)
+    f = gma.backward_causal if causal else gma.backward_bidir
+    got = f(t["Q"], t["K"], t["V"], t["mu"], t["sigma2"], t["log_pi"], gd, eps=eps)
     torch.cuda.synchronize()
-    ref = orc.backward_bidir(inp["Q"], inp["K"], inp["V"], inp["mu"], inp["sigma2"], inp["log_pi"], eps, G)
+    ref = orc.backward_bidir(inp["Q"], inp["K"], inp["V"], inp["mu"], inp["sigma2"], inp["log_pi"], eps, G,
+                             causal=causal)
     errs = {}
     for name, a, b in zip(NAMES, got, ref):
         a = a.float().cpu().numpy()
@@ -75,3 +77,20 @@ def test_backward_zero_length(gma):
     torch.cuda.synchronize()
     for g in got[3:]:
         assert bool((g == 0).all())
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("K", [3, 17, 64])
+def test_causal_backward_small(gma, dtype, K):
+    check(gma, make_inputs(2, 3, 150, K, dtype=dtype, seed=400 + K), seed=K, causal=True)
+
+
+@pytest.mark.parametrize("N", [1, 31, 33, 300, 1000])
+def test_causal_backward_lengths_f32(gma, N):
+    # N = 1000 spreads over several segments (suffix scan across segments).  With one key, O = v g / (g + eps)
+    # and every gradient but dV is proportional to eps: eps = 0.3 keeps it above float32 resolution.
+    check(gma, make_inputs(1, 2, N, 16, dtype="f32", seed=500 + N), eps=0.3 if N == 1 else 1e-6, seed=N, causal=True)
+
+
+def test_causal_backward_bf16_B1H2N2048K256(gma):
+    check(gma, make_inputs(1, 2, 2048, 256, dtype="bf16", seed=19), seed=19, causal=True)
