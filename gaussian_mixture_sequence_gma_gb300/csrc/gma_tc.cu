@@ -101,6 +101,7 @@ struct TcArgs {
   float* state;          // [BH][Kp][80] (bidir) or [BH][splits][Kp][80] (causal aggregates)
   Ctrl* ctrl;
   void* out;             // read: O bf16 [BH][N][64]; responsibilities: gamma fp32 [BH][N][K]
+  float* inv;            // causal: 1/s_j of every key [BH][tiles * 128] (0 past N), written by the aggregates
   int H, N, K, Kp, tiles, seg_tiles, splits;
   float eps;
   uint64_t wait_ns;
@@ -406,7 +407,7 @@ __device__ __forceinline__ uint16_t bf16_bits(float x) {
   return *reinterpret_cast<const uint16_t*>(&h);
 }
 
-__device__ __forceinline__ void init_bars(Bars* B) {
+__device__ __forceinline__ void init_bars(Bars* B, uint32_t g_empty_count) {
   mbar_init(&B->w_full, 1);
   mbar_init(&B->sb_full, kRowWarps);
   for (int s = 0; s < 2; ++s) {
@@ -418,7 +419,7 @@ __device__ __forceinline__ void init_bars(Bars* B) {
   mbar_init(&B->l_full, 1);
   mbar_init(&B->l_empty, kRowWarps);
   mbar_init(&B->g_full, kRowWarps);
-  mbar_init(&B->g_empty, 1);
+  mbar_init(&B->g_empty, g_empty_count);
   mbar_init(&B->o_full, 1);
   mbar_init(&B->o_empty, kRowWarps);
   mbar_init(&B->done, 1);
@@ -494,9 +495,13 @@ __device__ __forceinline__ void store_out8(__nv_bfloat16* dst, const uint32_t* a
 // ----------------------------------------------------------------------------------------------- write / aggregate
 // grid (splits, B*H).  CTA (split, bh) covers tiles [split * seg_tiles, ...) of head-row bh and adds
 // Gamma_K^T [V | 1] over them into state[bh] (kAtomic) or stores it to state[bh][split] (causal).
+// The causal form (!kAtomic) also keeps what the chunked sweep needs of every key: its unnormalised
+// Gamma~_K row (bf16, through tmG: [B*H][N][64 * ceil(Kp / 64)], stored tile by tile from the shared
+// operand by warp 2) and its 1/s (a.inv).
 template <bool kAtomic, int NC>
 __global__ void __launch_bounds__(kThreadsTc, 1)
-    tc_write_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, TcArgs a) {
+    tc_write_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                    const __grid_constant__ CUtensorMap tmG, TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // 1 KB aligned, still shared
   const uint32_t sbase = smem_u32(smem);
@@ -515,7 +520,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     reinterpret_cast<uint4*>(smem + L.inv)[i] = make_uint4(0, 0, 0, 0);
   __syncthreads();
   // element n = 64 of each token row of the MN-major [V | 1] operand receives 1/s of that key every tile
-  if (threadIdx.x == 0) init_bars(&B);
+  // the Gamma~ tile is free again once the contraction has read it and (causal) its store has read it
+  if (threadIdx.x == 0) init_bars(&B, kAtomic ? 1u : 2u);
   if (warp == 1) {
     tmem_alloc(&B.tmem_base, 512);
     tmem_relinquish();
@@ -528,49 +534,62 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   if (warp < kRowWarp0) {
     setmaxnreg_dec<kCtrlRegs>();
     if (warp == 0) {
-    if (lane == 0) producer(a, &tmK, &tmV, smem, L, &B, bh, tile0, T);
-  } else if (warp == 1) {
-    if (lane == 0) {
-      const uint32_t idw = make_idesc(128, kStCols, 1, 1, 1, 1);
-      const uint32_t w_addr = smem_u32(smem + L.w), g_addr = smem_u32(smem + L.g);
-      const uint32_t v_addr = smem_u32(smem + L.v), inv_addr = smem_u32(smem + L.inv);
-      bool ok = wait_bounded(&B.w_full, 0, &B.ab, a.ctrl, 20, a.wait_ns);
-      if (ok && T > 0) ok = wait_bounded(&B.ax_full, 0, &B.ab, a.ctrl, 21, a.wait_ns);
-      if (ok && T > 0) {
-        tc_fence_after();
-        issue_logits(tmem, w_addr, a.Kp);
-        mma_commit(&B.l_full);  // also frees the [x^2 | x] columns for the next tile
-      }
-      for (int t = 0; ok && t < T; ++t) {
-        if (t + 1 < T) {
-          ok = wait_bounded(&B.ax_full, (t + 1) & 1, &B.ab, a.ctrl, 22, a.wait_ns) &&
-               wait_bounded(&B.l_empty, t & 1, &B.ab, a.ctrl, 23, a.wait_ns);
-          if (!ok) break;
+      if (lane == 0) producer(a, &tmK, &tmV, smem, L, &B, bh, tile0, T);
+    } else if (warp == 1) {
+      if (lane == 0) {
+        const uint32_t idw = make_idesc(128, kStCols, 1, 1, 1, 1);
+        const uint32_t w_addr = smem_u32(smem + L.w), g_addr = smem_u32(smem + L.g);
+        const uint32_t v_addr = smem_u32(smem + L.v), inv_addr = smem_u32(smem + L.inv);
+        bool ok = wait_bounded(&B.w_full, 0, &B.ab, a.ctrl, 20, a.wait_ns);
+        if (ok && T > 0) ok = wait_bounded(&B.ax_full, 0, &B.ab, a.ctrl, 21, a.wait_ns);
+        if (ok && T > 0) {
           tc_fence_after();
           issue_logits(tmem, w_addr, a.Kp);
-          mma_commit(&B.l_full);
+          mma_commit(&B.l_full);  // also frees the [x^2 | x] columns for the next tile
         }
-        const int s = t & 1;
-        // the row warps signal g_full after scaling this tile's V rows, so V has landed as well
-        ok = wait_bounded(&B.g_full, t & 1, &B.ab, a.ctrl, 24, a.wait_ns);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t vs = v_addr + s * 16384;
-        for (int mb = 0; mb < MB; ++mb) {
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint64_t ad = make_sdesc(g_addr + mb * 32768 + ks * 2048, 16384, 1024);
-            const uint64_t bd = make_sdesc(vs + ks * 2048, inv_addr - vs, 1024);
-            mma_ss(tmem + kColAcc + kStCols * mb, ad, bd, idw, (t > 0 || ks > 0) ? 1u : 0u);
+        for (int t = 0; ok && t < T; ++t) {
+          if (t + 1 < T) {
+            ok = wait_bounded(&B.ax_full, (t + 1) & 1, &B.ab, a.ctrl, 22, a.wait_ns) &&
+                 wait_bounded(&B.l_empty, t & 1, &B.ab, a.ctrl, 23, a.wait_ns);
+            if (!ok) break;
+            tc_fence_after();
+            issue_logits(tmem, w_addr, a.Kp);
+            mma_commit(&B.l_full);
           }
+          const int s = t & 1;
+          // the row warps signal g_full after scaling this tile's V rows, so V has landed as well
+          ok = wait_bounded(&B.g_full, t & 1, &B.ab, a.ctrl, 24, a.wait_ns);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t vs = v_addr + s * 16384;
+          for (int mb = 0; mb < MB; ++mb) {
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+              const uint64_t ad = make_sdesc(g_addr + mb * 32768 + ks * 2048, 16384, 1024);
+              const uint64_t bd = make_sdesc(vs + ks * 2048, inv_addr - vs, 1024);
+              mma_ss(tmem + kColAcc + kStCols * mb, ad, bd, idw, (t > 0 || ks > 0) ? 1u : 0u);
+            }
+          }
+          mma_commit(&B.g_empty);
+          mma_commit(&B.v_empty[s]);
         }
-        mma_commit(&B.g_empty);
-        mma_commit(&B.v_empty[s]);
+        mma_commit(&B.done);
+        Abort none{0};
+        wait_bounded(&B.done, 0, &none, a.ctrl, 25, a.wait_ns);
       }
-      mma_commit(&B.done);
-      Abort none{0};
-      wait_bounded(&B.done, 0, &none, a.ctrl, 25, a.wait_ns);
-    }
+    } else if (warp == 2) {
+      if (!kAtomic && lane == 0) {
+        // Gamma~_K tile -> global once the row warps have filled it (64-component boxes, rows past N clipped)
+        const int KB = (a.Kp + 63) / 64;
+        for (int t = 0; t < T; ++t) {
+          if (!wait_bounded(&B.g_full, t & 1, &B.ab, a.ctrl, 26, a.wait_ns)) break;
+          for (int j = 0; j < KB; ++j) tma_store_3d(&tmG, sbase + L.g + 16384u * j, 64 * j, (tile0 + t) * kTile, bh);
+          bulk_commit();
+          bulk_wait_read_all();
+          mbar_arrive(&B.g_empty);
+        }
+        bulk_wait_all();
+      }
     }
   } else {
     setmaxnreg_inc<kRowRegs>();
@@ -629,7 +648,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       if (ok) {
         const float inv = tok < a.N ? rcp_approx(sum) : 0.f;
         scale_v_row(sbase + L.v + s * 16384, rc, inv);
-        if (rc.part == 0) sts16(sbase + L.inv + rc.rowsw, bf16_bits(inv));
+        if (rc.part == 0) {
+          sts16(sbase + L.inv + rc.rowsw, bf16_bits(inv));
+          if (!kAtomic) a.inv[(size_t)bh * a.tiles * kTile + tok] = inv;
+        }
         fence_async_smem();
         warp_arrive(&B.g_full);
       }
@@ -683,7 +705,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   const int T = max(0, min(a.tiles, tile0 + a.seg_tiles) - tile0);
   const int KS = a.Kp / 16;  // contraction steps of the read
 
-  if (threadIdx.x == 0) init_bars(&B);
+  if (threadIdx.x == 0) init_bars(&B, 1u);
   if (warp == 1) {
     tmem_alloc(&B.tmem_base, 512);
     tmem_relinquish();
@@ -872,39 +894,43 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 //   O_i = [gq~_i . S_prev + sum_{j in tile, j <= i} (gq~_i . gk_j) [v_j | 1]] / (... + eps s_i),
 //   S  += Gamma_K(tile)^T [V | 1]
 // (gist.science summary, "Variants and training" item 3: prefix sums, O_i depends on j <= i only).
-// The "1" column of [V | 1] is a separate N=16 contraction against a K-major tile whose row 0 holds
-// 1/s_j of each key j of the tile (the other rows are zero), and the V rows are scaled by the same 1/s_j.
+// The key side of every tile (unnormalised Gamma~_K rows and 1/s_j) was computed once by the segment
+// aggregates and is loaded here; key j's row is normalised inside the contractions by scaling its
+// [v_j | 1] row by 1/s_j.  The "1" column of [V | 1] is the fifth 32-byte-swizzle atom of the B operand,
+// whose column 0 holds 1/s_j of each key (columns 1..15 zero).
 constexpr uint32_t kCColP = 128;   // intra-tile affinity P (fp32 128 cols; bf16 halves at 128 and 192)
 constexpr uint32_t kCColS = 256;   // state accumulators, 80 columns per 128-component block
 constexpr uint32_t kCColO = 416;   // output accumulator (80 columns), shared with the [x^2 | x] operand
 
 struct CausalLayout {
-  uint32_t w, gk, x, v, sbv, sbz, ones, c, red, total;
+  uint32_t w, gk, x, v, ones, sbv, sbz, c, inv, red, total;
 };
 __host__ __device__ inline CausalLayout causal_layout(int Kp) {
   CausalLayout s{};
-  const int MB = (Kp + 127) / 128, KB = (Kp + 63) / 64;
+  const int MB = (Kp + 127) / 128;
   s.w = 0;
-  s.gk = align1k(Kp * 256);          // Gamma_K (bf16): MN-major A of the state update, K-major B of P
-  s.x = s.gk + MB * 32768;           // two X stages: key tile, query tile
+  // Gamma~_K tile as loaded: 64-component 128-byte-swizzle boxes 16 KB apart (MN-major A of the state
+  // update, K-major B of P)
+  s.gk = align1k(Kp * 256);
+  s.x = s.gk + MB * 32768;           // query X tile
   // [V | 1/s] as one MN-major B of N = 80 in the 32-byte swizzle: four 4 KB atoms of 16 value dims,
   // then the 1/s atom (column 0 = 1/s of each key, columns 1..15 zero)
-  s.v = s.x + 2 * 16384;
+  s.v = s.x + 16384;
   s.ones = s.v + 16384;
   // bf16 copy of S_prev [Kp][80] (+ eps in column 64), MN-major B of N = 80, 32-byte swizzle: five
   // atoms of Kp rows x 32 bytes
   s.sbv = s.ones + 4096;
   s.sbz = s.sbv + 4 * Kp * 32;       // the fifth atom (Z + eps in column 64)
-  (void)KB;
   s.c = s.sbz + Kp * 32;
-  s.red = s.c + 1024;
+  s.inv = s.c + 1024;                // 1/s of the tile's keys (float32)
+  s.red = s.inv + kTile * 4;
   s.total = s.red + kParts * kTile * 8;
   return s;
 }
 
 struct CBars {
-  uint64_t w_full, x_full[2], x_empty[2], v_full, v_empty;
-  uint64_t ax_full, lk_full, lq_go, gk_full, lq_full, gq_full, sb_full, p_full, pb_full, o_full, s_full;
+  uint64_t w_full, x_full, x_empty, v_full, v_empty, gk_full, gk_empty;
+  uint64_t ax_full, lq_full, vs_full, gq_full, sb_full, p_full, pb_full, o_full, s_full;
   uint64_t done;
   uint32_t tmem_base;
   Abort ab;
@@ -934,7 +960,7 @@ __device__ __forceinline__ void snapshot_state_chunk(uint32_t sb, int Kp, int co
 
 template <int NC>
 __global__ void __launch_bounds__(kThreadsTc, 1)
-    tc_causal_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+    tc_causal_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmG,
                      const __grid_constant__ CUtensorMap tmV, TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // 1 KB aligned, still shared
@@ -946,26 +972,26 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   const int tile0 = seg * a.seg_tiles;
   const int T = max(0, min(a.tiles, tile0 + a.seg_tiles) - tile0);
   const int MB = (a.Kp + 127) / 128;
+  const int KB = (a.Kp + 63) / 64;
   const int KS = a.Kp / 16;
 
-  // zero Gamma_K, the state copies and the 1/s tile (its row 0 is rewritten every tile)
+  // zero the Gamma_K blocks no load reaches (Kp <= 128), the 1/s atom (its column 0 is rewritten every
+  // tile) and the state copies
   for (uint32_t i = threadIdx.x; i < (uint32_t)MB * 32768 / 16; i += blockDim.x)
     reinterpret_cast<uint4*>(smem + L.gk)[i] = make_uint4(0, 0, 0, 0);
-  for (uint32_t i = threadIdx.x; i < (L.c - L.ones) / 16; i += blockDim.x)  // 1/s atom and the state copy
+  for (uint32_t i = threadIdx.x; i < (L.c - L.ones) / 16; i += blockDim.x)
     reinterpret_cast<uint4*>(smem + L.ones)[i] = make_uint4(0, 0, 0, 0);
   if (threadIdx.x == 0) {
     mbar_init(&B.w_full, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&B.x_full[s], 1);
-      mbar_init(&B.x_empty[s], kRowWarps);
-    }
+    mbar_init(&B.x_full, 1);
+    mbar_init(&B.x_empty, kRowWarps);
     mbar_init(&B.v_full, 1);
     mbar_init(&B.v_empty, 1);
+    mbar_init(&B.gk_full, 1);
+    mbar_init(&B.gk_empty, 1);
     mbar_init(&B.ax_full, kRowWarps);
-    mbar_init(&B.lk_full, 1);
-    mbar_init(&B.lq_go, kRowWarps);
-    mbar_init(&B.gk_full, kRowWarps);
     mbar_init(&B.lq_full, 1);
+    mbar_init(&B.vs_full, kRowWarps);
     mbar_init(&B.gq_full, kRowWarps);
     mbar_init(&B.sb_full, kRowWarps);
     mbar_init(&B.p_full, 1);
@@ -992,31 +1018,33 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       // ---------------------------------------------------------------- producer
       const uint32_t wbytes = (uint32_t)a.Kp * 256, cbytes = kCTable * 4;
       const int h = bh % a.H;
+      const float* inv_row = a.inv + (size_t)bh * a.tiles * kTile;
       mbar_expect_tx(&B.w_full, wbytes + cbytes);
       for (uint32_t o = 0; o < wbytes; o += 32768)
         bulk_load(smem + L.w + o, a.w_img + (size_t)h * wbytes + o, min(32768u, wbytes - o), &B.w_full);
       bulk_load(smem + L.c, a.cbias + (size_t)h * kCTable, cbytes, &B.w_full);
-      int issued[3] = {-1, -1, -1};  // parity of the last load armed on x_full[0], x_full[1], v_full
+      int issued[3] = {-1, -1, -1};  // parity of the last load armed on x_full, gk_full, v_full
       for (int t = 0; t < T; ++t) {
         const uint32_t pe = (t & 1) ^ 1;
         const int row0 = (tile0 + t) * kTile;
-        if (!wait_bounded(&B.x_empty[0], pe, &B.ab, a.ctrl, 70, a.wait_ns)) break;
-        mbar_expect_tx(&B.x_full[0], 16384);
-        tma_load_3d(smem + L.x, &tmK, 0, row0, bh, &B.x_full[0]);
+        if (!wait_bounded(&B.x_empty, pe, &B.ab, a.ctrl, 70, a.wait_ns)) break;
+        mbar_expect_tx(&B.x_full, 16384);
+        tma_load_3d(smem + L.x, &tmQ, 0, row0, bh, &B.x_full);
         issued[0] = t & 1;
-        if (!wait_bounded(&B.x_empty[1], pe, &B.ab, a.ctrl, 71, a.wait_ns)) break;
-        mbar_expect_tx(&B.x_full[1], 16384);
-        tma_load_3d(smem + L.x + 16384, &tmQ, 0, row0, bh, &B.x_full[1]);
+        if (!wait_bounded(&B.gk_empty, pe, &B.ab, a.ctrl, 71, a.wait_ns)) break;
+        mbar_expect_tx(&B.gk_full, (uint32_t)KB * 16384u);
+        for (int j = 0; j < KB; ++j) tma_load_3d(smem + L.gk + 16384 * j, &tmG, 64 * j, row0, bh, &B.gk_full);
         issued[1] = t & 1;
         if (!wait_bounded(&B.v_empty, pe, &B.ab, a.ctrl, 72, a.wait_ns)) break;
-        mbar_expect_tx(&B.v_full, 16384);
+        mbar_expect_tx(&B.v_full, 16384 + kTile * 4);
         for (int a4 = 0; a4 < 4; ++a4) tma_load_3d(smem + L.v + 4096 * a4, &tmV, 16 * a4, row0, bh, &B.v_full);
+        bulk_load(smem + L.inv, inv_row + row0, kTile * 4, &B.v_full);
         issued[2] = t & 1;
       }
       // never leave with copies in flight
       Abort none{0};
-      if (issued[0] >= 0) wait_bounded(&B.x_full[0], (uint32_t)issued[0], &none, a.ctrl, 73, a.wait_ns);
-      if (issued[1] >= 0) wait_bounded(&B.x_full[1], (uint32_t)issued[1], &none, a.ctrl, 74, a.wait_ns);
+      if (issued[0] >= 0) wait_bounded(&B.x_full, (uint32_t)issued[0], &none, a.ctrl, 73, a.wait_ns);
+      if (issued[1] >= 0) wait_bounded(&B.gk_full, (uint32_t)issued[1], &none, a.ctrl, 74, a.wait_ns);
       if (issued[2] >= 0) wait_bounded(&B.v_full, (uint32_t)issued[2], &none, a.ctrl, 75, a.wait_ns);
     } else if (warp == 1 && lane == 0) {
       // ---------------------------------------------------------------- MMA issuer
@@ -1033,19 +1061,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       bool ok = wait_bounded(&B.w_full, 0, &B.ab, a.ctrl, 80, a.wait_ns);
       for (int t = 0; ok && t < T; ++t) {
         const uint32_t ph = t & 1;
-        // key logits
+        // query logits
         if (!(ok = wait_bounded(&B.ax_full, ph, &B.ab, a.ctrl, 81, a.wait_ns))) break;
         tc_fence_after();
         issue_logits(tmem, w_addr, a.Kp, kCColO);
-        mma_commit(&B.lk_full);
-        // query logits, as soon as the key logits are in registers and the query operand is built
-        if (!(ok = wait_bounded(&B.lq_go, ph, &B.ab, a.ctrl, 82, a.wait_ns))) break;
-        tc_fence_after();
-        issue_logits(tmem, w_addr, a.Kp, kCColO);
         mma_commit(&B.lq_full);
-        // state update S += Gamma_K^T [V | 1]: needs Gamma_K, V, and the bf16 snapshot of S_prev taken
+        // state update S += Gamma_K^T [V | 1] while the query softmax runs: needs the loaded Gamma_K, the
+        // scaled V rows and the bf16 snapshot of S_prev taken
         if (!(ok = wait_bounded(&B.gk_full, ph, &B.ab, a.ctrl, 83, a.wait_ns) &&
-                   wait_bounded(&B.v_full, ph, &B.ab, a.ctrl, 84, a.wait_ns) &&
+                   wait_bounded(&B.vs_full, ph, &B.ab, a.ctrl, 84, a.wait_ns) &&
                    wait_bounded(&B.sb_full, ph, &B.ab, a.ctrl, 85, a.wait_ns)))
           break;
         tc_fence_after();
@@ -1067,6 +1091,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           mma_ts(tmem + kCColP, aq, sdesc_add(d_gk_k, (ks >> 2) * 16384 + (ks & 3) * 32), id_p, ks > 0);
         }
         mma_commit(&B.p_full);
+        mma_commit(&B.gk_empty);  // the state update and P were the last readers of this Gamma_K tile
         // intra-tile term O += P [V | 1]
         if (!(ok = wait_bounded(&B.pb_full, ph, &B.ab, a.ctrl, 88, a.wait_ns))) break;
         tc_fence_after();
@@ -1087,7 +1112,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     // ------------------------------------------------------------------ row warps
     const RowCtx rc = row_ctx(sbase + L.red);
     const uint32_t cs = sbase + L.c;
-    const uint32_t gka = gamma_row_addr<NC>(sbase + L.gk, rc);
     zero_unused_logits<NC>(tmem, rc, a.Kp);
     // S <- exclusive prefix state of this segment; SB <- its bf16 copy (eps rides in the Z column)
     if (rc.part < MB) {
@@ -1107,12 +1131,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     tc_fence_before();
     warp_arrive(&B.sb_full);
     bool ok = warp_wait(&B.w_full, 0, &B.ab, a.ctrl, 90, a.wait_ns);
-    // key operand of the first tile (later ones are built in the previous tile's epilogue; the [x^2 | x]
-    // columns double as the output accumulator)
-    if (ok && T > 0) ok = warp_wait(&B.x_full[0], 0, &B.ab, a.ctrl, 91, a.wait_ns);
+    // query operand of the first tile (later ones are built in the previous tile's epilogue; the
+    // [x^2 | x] columns double as the output accumulator)
+    if (ok && T > 0) ok = warp_wait(&B.x_full, 0, &B.ab, a.ctrl, 91, a.wait_ns);
     if (ok && T > 0) {
       transform_row(sbase + L.x, rc, tmem, kCColO);
-      warp_arrive(&B.x_empty[0]);
+      warp_arrive(&B.x_empty);
       tmem_st_wait();
       tc_fence_before();
       warp_arrive(&B.ax_full);
@@ -1122,45 +1146,25 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     for (int t = 0; t < T; ++t) {
       const uint32_t ph = t & 1;
       const int tok = (tile0 + t) * kTile + rc.row;
-      float mh = -INFINITY;
-      // key logits -> registers; build the query operand first so its contraction starts at once
-      if (ok) ok = warp_wait(&B.lk_full, ph, &B.ab, a.ctrl, 92, a.wait_ns);
-      if (ok) {
-        tc_fence_after();
-        ok = warp_wait(&B.x_full[1], ph, &B.ab, a.ctrl, 95, a.wait_ns);
-      }
-      if (ok) {
-        transform_row(sbase + L.x + 16384, rc, tmem, kCColO);
-        warp_arrive(&B.x_empty[1]);
-        mh = load_logits<NC>(tmem, rc, cs, v);
-        tmem_st_wait();
-        tc_fence_before();
-        warp_arrive(&B.lq_go);
-      }
-      // Gamma_K~ (unnormalised) -> smem; the key's 1/s (0 past N) scales its [v | 1] row instead
-      float m = xchg_max(rc, 0, mh);
-      float sp = 0.f;
-      if (ok) sp = exp_pack_store<NC, true>(v, m, gka, rc, a.Kp);
-      const float sum = xchg_sum(rc, 4, sp);
+      // this tile's V rows scaled by 1/s of their key (0 past N); 1/s also into the ones atom
       if (ok) ok = warp_wait(&B.v_full, ph, &B.ab, a.ctrl, 98, a.wait_ns);
       if (ok) {
-        const float inv = tok < a.N ? rcp_approx(sum) : 0.f;
+        const float inv = lds32(sbase + L.inv + 4u * (uint32_t)rc.row);
         scale_v_row32(sbase + L.v, rc, inv);
         if (rc.part == 0) sts16(sbase + L.ones + sw32_chunk(rc.row, 0), bf16_bits(inv));
         fence_async_smem();
-        warp_arrive(&B.gk_full);
+        warp_arrive(&B.vs_full);
       }
-      // Gamma_Q~ (unnormalised) -> TMEM over its own logit columns
-      mh = -INFINITY;
+      // Gamma_Q~ (unnormalised) -> TMEM over its own logit columns.  The exchange slot alternates with
+      // the tile, so a slot is rewritten only after the next tile's exchange, which every part thread
+      // reaches after reading this one.
+      float mh = -INFINITY;
       if (ok) ok = warp_wait(&B.lq_full, ph, &B.ab, a.ctrl, 96, a.wait_ns);
       if (ok) {
         tc_fence_after();
         mh = load_logits<NC>(tmem, rc, cs, v);
       }
-      // the .x slots are free: every key maximum was read before the key-sum exchange.  They are
-      // rewritten with the next tile's key maxima only after the o_full wait below, which completes
-      // after every row warp has arrived on pb_full, i.e. after it has read these query maxima.
-      m = xchg_max(rc, 0, mh);
+      const float m = xchg_max(rc, ph * 4u, mh);
       if (ok) {
         exp_pack_tmem<NC>(v, m, tmem + rc.lane_base + kColLog + (NC / 2) * rc.part);
         tmem_st_wait();
@@ -1206,27 +1210,27 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         warp_arrive(&B.sb_full);
       }
       // output: this thread's output dims are 8*part + [0,8) and 32 + 8*part + [0,8) -- the same columns it
-      // overwrites with the next key operand, so no other warp reads them afterwards.  Once they are in
-      // registers the next key operand goes in (its contraction runs while this output is stored).
+      // overwrites with the next query operand, so no other warp reads them afterwards.  Once they are in
+      // registers the next query operand goes in (its contraction runs while this output is stored).
       if (ok) ok = warp_wait(&B.o_full, ph, &B.ab, a.ctrl, 100, a.wait_ns);
       if (ok) {
         tc_fence_after();
-        uint32_t o0[8], o1[8], zc[8];
+        uint32_t o0[8], o1[8];
         tmem_ld8(tmem + rc.lane_base + kCColO + 8 * rc.part, o0);
         tmem_ld8(tmem + rc.lane_base + kCColO + 32 + 8 * rc.part, o1);
-        tmem_ld8(tmem + rc.lane_base + kCColO + 64, zc);
-        tmem_ld_wait();
+        uint32_t z = tmem_ld1(tmem + rc.lane_base + kCColO + 64);
+        tmem_ld_wait_tied8x2_1(o0, o1, z);
         if (t + 1 < T) {
-          ok = warp_wait(&B.x_full[0], (t + 1) & 1, &B.ab, a.ctrl, 91, a.wait_ns);
+          ok = warp_wait(&B.x_full, (t + 1) & 1, &B.ab, a.ctrl, 91, a.wait_ns);
           if (ok) {
             transform_row(sbase + L.x, rc, tmem, kCColO);
-            warp_arrive(&B.x_empty[0]);
+            warp_arrive(&B.x_empty);
             tmem_st_wait();
             tc_fence_before();
             warp_arrive(&B.ax_full);
           }
         }
-        const float rden = rcp_approx(__uint_as_float(zc[0]));  // gq~ . (Z_i + eps)
+        const float rden = rcp_approx(__uint_as_float(z));  // gq~ . (Z_i + eps)
         if (tok < a.N) {
           __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.out) + ((size_t)bh * a.N + tok) * kDv;
           store_out8(orow + 8 * rc.part, o0, rden);
@@ -1315,6 +1319,28 @@ bool make_map(CUtensorMap* m, const void* base, int BH, int N, bool sw32 = false
   return r == CUDA_SUCCESS;
 }
 
+// 3-D map over the causal key responsibilities Gamma~_K [B*H][N][ld] bf16 (ld = 64 * ceil(Kp / 64)): box of
+// 64 components x 128 keys in the 128-byte swizzle (the Gamma~ operand tile's blocks), zero fill past N.
+bool make_gamma_map(CUtensorMap* m, const void* base, int BH, int N, int ld) {
+  EncodeTiledFn f = encode_fn();
+  if (!f) {
+    set_error_detail("cuTensorMapEncodeTiled entry point unavailable");
+    return false;
+  }
+  cuuint64_t dims[3] = {(cuuint64_t)ld, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)ld * 2, (cuuint64_t)N * ld * 2};
+  cuuint32_t box[3] = {64u, (cuuint32_t)kTile, 1}, es[3] = {1, 1, 1};
+  const CUresult r = f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char msg[96];
+    snprintf(msg, sizeof msg, "cuTensorMapEncodeTiled (Gamma) returned CUresult %d", (int)r);
+    set_error_detail(msg);
+  }
+  return r == CUDA_SUCCESS;
+}
+
 // Dynamic shared memory of a launch: the layout plus alignment slack, never below 116 KB so that
 // exactly one CTA (which owns all 512 TMEM columns) is resident per SM.
 uint32_t smem_bytes(uint32_t layout_total) { return layout_total + 1024 > 116u * 1024 ? layout_total + 1024 : 116u * 1024; }
@@ -1328,7 +1354,7 @@ int split_for(int BH, int tiles) {
 // Launches the per-tile kernels with NC components per row thread (2 * NC >= Kp).
 template <int NC>
 gma_status_t tc_launch(const gma_problem_t& p, gma_op_t op, int Nk, const TcPlan& pl, TcArgs a, const void* Q,
-                       const void* K, const void* V, cudaStream_t st) {
+                       const void* K, const void* V, void* ws, cudaStream_t st) {
   const int BH = p.B * p.H;
   CUtensorMap mq, mk, mv;
   if (op == GMA_OP_RESPONSIBILITIES) {
@@ -1340,15 +1366,18 @@ gma_status_t tc_launch(const gma_problem_t& p, gma_op_t op, int Nk, const TcPlan
     return check_launch("launch tc_resp", (const void*)tc_read_kernel<false, NC>);
   }
   if (op == GMA_OP_CAUSAL) {
-    CUtensorMap mv32;  // the chunk kernel's V tiles: four 16-dim boxes in the 32-byte swizzle
+    CUtensorMap mv32, mg;  // the chunk kernel's V tiles (four 16-dim boxes, 32-byte swizzle); Gamma~_K
+    void* gk = (char*)ws + pl.off_gk;
+    a.inv = (float*)((char*)ws + pl.off_inv);
     if (!make_map(&mq, Q, BH, p.N) || !make_map(&mk, K, BH, p.N) || !make_map(&mv, V, BH, p.N) ||
-        !make_map(&mv32, V, BH, p.N, true))
+        !make_map(&mv32, V, BH, p.N, true) || !make_gamma_map(&mg, gk, BH, p.N, (pl.Kp + 63) / 64 * 64))
       return GMA_ERR_CUDA;
-    // a5: segment aggregates; a6: exclusive scan over segments; a7: chunked sweep
+    // a5: segment aggregates (+ Gamma~_K and 1/s of every key); a6: exclusive scan over segments;
+    // a7: chunked sweep
     const uint32_t smem_w = smem_bytes(write_layout(pl.Kp).total);
     if (set_smem_optin((const void*)tc_write_kernel<false, NC>, (int)smem_w, 0) != GMA_OK) return GMA_ERR_CUDA;
     GMA_LAUNCH("tc_causal_aggregate", (tc_write_kernel<false, NC>), dim3(pl.splits, BH), kThreadsTc, smem_w, st, mk,
-               mv, a);
+               mv, mg, a);
     if (gma_status_t e = check_launch("launch tc_causal_aggregate", (const void*)tc_write_kernel<false, NC>)) return e;
     a.fault = 0;
     const int n = pl.Kp * kStCols;
@@ -1356,7 +1385,7 @@ gma_status_t tc_launch(const gma_problem_t& p, gma_op_t op, int Nk, const TcPlan
     if (gma_status_t e = check_launch("launch tc_causal_scan", (const void*)tc_scan_kernel)) return e;
     const uint32_t smem_c = smem_bytes(causal_layout(pl.Kp).total);
     if (set_smem_optin((const void*)tc_causal_kernel<NC>, (int)smem_c, 0) != GMA_OK) return GMA_ERR_CUDA;
-    GMA_LAUNCH("tc_causal_chunk", tc_causal_kernel<NC>, dim3(pl.splits, BH), kThreadsTc, smem_c, st, mq, mk, mv32, a);
+    GMA_LAUNCH("tc_causal_chunk", tc_causal_kernel<NC>, dim3(pl.splits, BH), kThreadsTc, smem_c, st, mq, mg, mv32, a);
     return check_launch("launch tc_causal_chunk", (const void*)tc_causal_kernel<NC>);
   }
   // bidirectional / cross: write over the Nk keys with their own split plan (the state layout does not
@@ -1373,7 +1402,8 @@ gma_status_t tc_launch(const gma_problem_t& p, gma_op_t op, int Nk, const TcPlan
     if (!make_map(&mk, K, BH, Nk) || !make_map(&mv, V, BH, Nk)) return GMA_ERR_CUDA;
     const uint32_t smem_w = smem_bytes(write_layout(pl.Kp).total);
     if (set_smem_optin((const void*)tc_write_kernel<true, NC>, (int)smem_w, 0) != GMA_OK) return GMA_ERR_CUDA;
-    GMA_LAUNCH("tc_bidir_write", (tc_write_kernel<true, NC>), dim3(plk.splits, BH), kThreadsTc, smem_w, st, mk, mv, aw);
+    GMA_LAUNCH("tc_bidir_write", (tc_write_kernel<true, NC>), dim3(plk.splits, BH), kThreadsTc, smem_w, st, mk, mv, mk,
+               aw);  // (the third map is unused without the causal key store)
     if (gma_status_t e = check_launch("launch tc_bidir_write", (const void*)tc_write_kernel<true, NC>)) return e;
   }
   if (op == GMA_OP_CAUSAL_STATE) return GMA_OK;  // the state alone
@@ -1404,7 +1434,12 @@ TcPlan tc_plan(const gma_problem_t& p, gma_op_t op) {
   size_t st = 0;
   if (op == GMA_OP_BIDIR || op == GMA_OP_CROSS || op == GMA_OP_CAUSAL_STATE) st = (size_t)BH * t.Kp * kStCols * 4;
   if (op == GMA_OP_CAUSAL) st = (size_t)BH * t.splits * t.Kp * kStCols * 4;  // segment aggregates
-  t.total = align_up(t.off_state + st);
+  t.off_gk = t.off_inv = t.total = align_up(t.off_state + st);
+  if (op == GMA_OP_CAUSAL) {
+    // Gamma~_K of every key (bf16, 64-component blocks) and 1/s of every key (float32, per full tile)
+    t.off_inv = align_up(t.off_gk + (size_t)BH * p.N * ((t.Kp + 63) / 64 * 64) * 2);
+    t.total = align_up(t.off_inv + (size_t)BH * t.tiles * kTile * 4);
+  }
   return t;
 }
 
@@ -1440,9 +1475,9 @@ gma_status_t tc_run(const gma_problem_t& p, gma_op_t op, int Nk, const void* Q, 
              (uint8_t*)a.w_img, (float*)a.cbias, a.ctrl, a.state, zero_n);
   if (gma_status_t e = check_launch("launch tc_prep", (const void*)tc_prep_kernel)) return e;
   const int nc = pl.Kp <= 64 ? 16 : (pl.Kp <= 128 ? 32 : 64);  // components per row thread (4 per row)
-  gma_status_t e = nc == 16   ? tc_launch<16>(p, op, Nk, pl, a, Q, K, V, st)
-                   : nc == 32 ? tc_launch<32>(p, op, Nk, pl, a, Q, K, V, st)
-                              : tc_launch<64>(p, op, Nk, pl, a, Q, K, V, st);
+  gma_status_t e = nc == 16   ? tc_launch<16>(p, op, Nk, pl, a, Q, K, V, ws, st)
+                   : nc == 32 ? tc_launch<32>(p, op, Nk, pl, a, Q, K, V, ws, st)
+                              : tc_launch<64>(p, op, Nk, pl, a, Q, K, V, ws, st);
   if (e != GMA_OK || op != GMA_OP_CAUSAL_STATE) return e;
   const size_t n = (size_t)BH * p.K * (kDv + 1);
   GMA_LAUNCH("tc_state_export", tc_state_export_kernel, (unsigned)std::min<size_t>((n + 255) / 256, 4096), 256, 0, st,
