@@ -101,7 +101,6 @@ struct TcArgs {
   float* state;          // [BH][Kp][80] (bidir) or [BH][splits][Kp][80] (causal aggregates)
   Ctrl* ctrl;
   void* out;             // read: O bf16 [BH][N][64]; responsibilities: gamma fp32 [BH][N][K]
-  float* inv;            // causal: 1/s_j of every key [BH][tiles * 128] (0 past N), written by the aggregates
   int H, N, K, Kp, tiles, seg_tiles, splits;
   float eps;
   uint64_t wait_ns;
@@ -356,6 +355,18 @@ __device__ __forceinline__ void store_packed(const float* v, uint32_t ga, const 
     if (cj < nvalid) sts128(ga ^ (uint32_t)(cj << 4), make_uint4(w[4 * cj], w[4 * cj + 1], w[4 * cj + 2], w[4 * cj + 3]));
 }
 
+// Normalised pack in place: word i of v receives the bf16 pair of components 2i, 2i+1 times inv.
+template <int NC>
+__device__ __forceinline__ void scale_pack(float* v, float inv) {
+  uint32_t* w = reinterpret_cast<uint32_t*>(v);
+#pragma unroll
+  for (int i = 0; i < NC / 2; ++i) {
+    float e0 = v[2 * i], e1 = v[2 * i + 1];
+    mul_f32x2(e0, e1, inv, inv);
+    w[i] = pack_bf16x2(e0, e1);
+  }
+}
+
 // Fused pass for a TMEM-resident operand: e = 2^(v - m) packed to bf16 pairs and stored over this thread's
 // NC/2 columns starting at taddr (8 words per store).  The caller waits for the stores.
 template <int NC>
@@ -407,7 +418,7 @@ __device__ __forceinline__ uint16_t bf16_bits(float x) {
   return *reinterpret_cast<const uint16_t*>(&h);
 }
 
-__device__ __forceinline__ void init_bars(Bars* B, uint32_t g_empty_count) {
+__device__ __forceinline__ void init_bars(Bars* B, uint32_t g_release_count) {
   mbar_init(&B->w_full, 1);
   mbar_init(&B->sb_full, kRowWarps);
   for (int s = 0; s < 2; ++s) {
@@ -419,7 +430,7 @@ __device__ __forceinline__ void init_bars(Bars* B, uint32_t g_empty_count) {
   mbar_init(&B->l_full, 1);
   mbar_init(&B->l_empty, kRowWarps);
   mbar_init(&B->g_full, kRowWarps);
-  mbar_init(&B->g_empty, g_empty_count);
+  mbar_init(&B->g_empty, g_release_count);
   mbar_init(&B->o_full, 1);
   mbar_init(&B->o_empty, kRowWarps);
   mbar_init(&B->done, 1);
@@ -495,9 +506,10 @@ __device__ __forceinline__ void store_out8(__nv_bfloat16* dst, const uint32_t* a
 // ----------------------------------------------------------------------------------------------- write / aggregate
 // grid (splits, B*H).  CTA (split, bh) covers tiles [split * seg_tiles, ...) of head-row bh and adds
 // Gamma_K^T [V | 1] over them into state[bh] (kAtomic) or stores it to state[bh][split] (causal).
-// The causal form (!kAtomic) also keeps what the chunked sweep needs of every key: its unnormalised
-// Gamma~_K row (bf16, through tmG: [B*H][N][64 * ceil(Kp / 64)], stored tile by tile from the shared
-// operand by warp 2) and its 1/s (a.inv).
+// The bidirectional form normalises each key's Gamma~ row inside the contraction (its [v | 1] row is
+// scaled by 1/s); the causal form (!kAtomic) normalises the Gamma row itself (bf16 gamma = e / s, V as
+// loaded, a constant 1 column) and keeps it for the chunked sweep: through tmG into
+// [B*H][N][64 * ceil(Kp / 64)], stored tile by tile from the shared operand by warp 2.
 template <bool kAtomic, int NC>
 __global__ void __launch_bounds__(kThreadsTc, 1)
     tc_write_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -520,7 +532,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     reinterpret_cast<uint4*>(smem + L.inv)[i] = make_uint4(0, 0, 0, 0);
   __syncthreads();
   // element n = 64 of each token row of the MN-major [V | 1] operand receives 1/s of that key every tile
-  // the Gamma~ tile is free again once the contraction has read it and (causal) its store has read it
+  // the Gamma tile is free again once the contraction has read it and (causal) its store has read it
   if (threadIdx.x == 0) init_bars(&B, kAtomic ? 1u : 2u);
   if (warp == 1) {
     tmem_alloc(&B.tmem_base, 512);
@@ -579,7 +591,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       }
     } else if (warp == 2) {
       if (!kAtomic && lane == 0) {
-        // Gamma~_K tile -> global once the row warps have filled it (64-component boxes, rows past N clipped)
+        // Gamma_K tile -> global once the row warps have filled it (64-component boxes, rows past N clipped)
         const int KB = (a.Kp + 63) / 64;
         for (int t = 0; t < T; ++t) {
           if (!wait_bounded(&B.g_full, t & 1, &B.ab, a.ctrl, 26, a.wait_ns)) break;
@@ -598,6 +610,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     const uint32_t cs = sbase + L.c;
     const uint32_t ga = gamma_row_addr<NC>(sbase + L.g, rc);
     zero_unused_logits<NC>(tmem, rc, a.Kp);
+    // causal: element n = 64 of every row of the [V | 1] operand is 1 (rows past N have a zero gamma row)
+    if (!kAtomic && rc.part == 0) sts16(sbase + L.inv + rc.rowsw, bf16_bits(1.f));
     bool ok = warp_wait(&B.w_full, 0, &B.ab, a.ctrl, 30, a.wait_ns);
     if (ok && T > 0) {
       ok = warp_wait(&B.x_full[0], 0, &B.ab, a.ctrl, 31, a.wait_ns);
@@ -637,21 +651,32 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         warp_arrive(&B.l_empty);
       }
       const float m = xchg_max(rc, 0, mp);
-      // Gamma~ row (unnormalised, row maximum 1) -> smem once the previous contraction has read it
-      // exponentiate into registers while the previous contraction may still be reading G, then store
-      float sp = 0.f;
-      if (ok) sp = exp_pack_regs<NC, true>(v, m);
-      if (ok && t > 0) ok = warp_wait(&B.g_empty, (t - 1) & 1, &B.ab, a.ctrl, 36, a.wait_ns);
-      if (ok) store_packed<NC>(v, ga, rc, a.Kp);
-      const float sum = xchg_sum(rc, 4, sp);
-      // normalise this key's Gamma row inside the contraction: scale its [v | 1] row by 1/s (0 past N)
-      if (ok) {
-        const float inv = tok < a.N ? rcp_approx(sum) : 0.f;
-        scale_v_row(sbase + L.v + s * 16384, rc, inv);
-        if (rc.part == 0) {
-          sts16(sbase + L.inv + rc.rowsw, bf16_bits(inv));
-          if (!kAtomic) a.inv[(size_t)bh * a.tiles * kTile + tok] = inv;
+      if (kAtomic) {
+        // Gamma~ row (unnormalised, row maximum 1) -> smem once the previous contraction has read it:
+        // exponentiate into registers while the previous contraction may still be reading G, then store
+        float sp = 0.f;
+        if (ok) sp = exp_pack_regs<NC, true>(v, m);
+        if (ok && t > 0) ok = warp_wait(&B.g_empty, (t - 1) & 1, &B.ab, a.ctrl, 36, a.wait_ns);
+        if (ok) store_packed<NC>(v, ga, rc, a.Kp);
+        const float sum = xchg_sum(rc, 4, sp);
+        // normalise this key's Gamma row inside the contraction: scale its [v | 1] row by 1/s (0 past N)
+        if (ok) {
+          const float inv = tok < a.N ? rcp_approx(sum) : 0.f;
+          scale_v_row(sbase + L.v + s * 16384, rc, inv);
+          if (rc.part == 0) sts16(sbase + L.inv + rc.rowsw, bf16_bits(inv));
         }
+      } else {
+        // normalised Gamma row (0 past N) -> smem once the previous contraction and store have read it
+        float sp = 0.f;
+        if (ok) sp = exp_inplace<NC>(v, m);
+        const float sum = xchg_sum(rc, 4, sp);
+        if (ok) {
+          scale_pack<NC>(v, tok < a.N ? rcp_approx(sum) : 0.f);
+          if (t > 0) ok = warp_wait(&B.g_empty, (t - 1) & 1, &B.ab, a.ctrl, 36, a.wait_ns);
+          if (ok) store_packed<NC>(v, ga, rc, a.Kp);
+        }
+      }
+      if (ok) {
         fence_async_smem();
         warp_arrive(&B.g_full);
       }
@@ -894,16 +919,20 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 //   O_i = [gq~_i . S_prev + sum_{j in tile, j <= i} (gq~_i . gk_j) [v_j | 1]] / (... + eps s_i),
 //   S  += Gamma_K(tile)^T [V | 1]
 // (gist.science summary, "Variants and training" item 3: prefix sums, O_i depends on j <= i only).
-// The key side of every tile (unnormalised Gamma~_K rows and 1/s_j) was computed once by the segment
-// aggregates and is loaded here; key j's row is normalised inside the contractions by scaling its
-// [v_j | 1] row by 1/s_j.  The "1" column of [V | 1] is the fifth 32-byte-swizzle atom of the B operand,
-// whose column 0 holds 1/s_j of each key (columns 1..15 zero).
+// The key side of every tile was computed once by the segment aggregates and is loaded here: the
+// normalised Gamma_K rows (bf16), used with V as loaded and a constant 1 column.
+//
+// Per tile the tensor pipe runs: query logits (A = [x^2 | x] from shared memory) -> state update
+// (overlaps the query softmax) -> inter-tile term Gq~ S_prev and P = Gq~ Gk^T, interleaved -> P [V | 1]
+// after the row warps have masked P.  The next query operand is converted in shared memory while the
+// pipe works, so the next tile's logits follow P [V | 1] at once and run while this tile's output is
+// stored.
 constexpr uint32_t kCColP = 128;   // intra-tile affinity P (fp32 128 cols; bf16 halves at 128 and 192)
 constexpr uint32_t kCColS = 256;   // state accumulators, 80 columns per 128-component block
-constexpr uint32_t kCColO = 416;   // output accumulator (80 columns), shared with the [x^2 | x] operand
+constexpr uint32_t kCColO = 416;   // output accumulator (80 columns)
 
 struct CausalLayout {
-  uint32_t w, gk, x, v, ones, sbv, sbz, c, inv, red, total;
+  uint32_t w, gk, op, v, sbv, sbz, c, red, total;
 };
 __host__ __device__ inline CausalLayout causal_layout(int Kp) {
   CausalLayout s{};
@@ -912,25 +941,25 @@ __host__ __device__ inline CausalLayout causal_layout(int Kp) {
   // Gamma~_K tile as loaded: 64-component 128-byte-swizzle boxes 16 KB apart (MN-major A of the state
   // update, K-major B of P)
   s.gk = align1k(Kp * 256);
-  s.x = s.gk + MB * 32768;           // query X tile
-  // [V | 1/s] as one MN-major B of N = 80 in the 32-byte swizzle: four 4 KB atoms of 16 value dims,
-  // then the 1/s atom (column 0 = 1/s of each key, columns 1..15 zero)
-  s.v = s.x + 16384;
-  s.ones = s.v + 16384;
+  // [x^2 | x] fp16 operand of the query logits: two K-major 128-byte-swizzle blocks of 128 rows x 64;
+  // the query X tile (bf16) lands in the second block and is converted in place
+  s.op = s.gk + MB * 32768;
+  // [V | 1] as one MN-major B of N = 80 in the 32-byte swizzle: four 4 KB atoms of 16 value dims, then
+  // the constant atom (column 0 = 1, columns 1..15 zero)
+  s.v = s.op + 32768;
   // bf16 copy of S_prev [Kp][80] (+ eps in column 64), MN-major B of N = 80, 32-byte swizzle: five
   // atoms of Kp rows x 32 bytes
-  s.sbv = s.ones + 4096;
+  s.sbv = s.v + 5 * 4096;
   s.sbz = s.sbv + 4 * Kp * 32;       // the fifth atom (Z + eps in column 64)
   s.c = s.sbz + Kp * 32;
-  s.inv = s.c + 1024;                // 1/s of the tile's keys (float32)
-  s.red = s.inv + kTile * 4;
+  s.red = s.c + 1024;
   s.total = s.red + kParts * kTile * 8;
   return s;
 }
 
 struct CBars {
-  uint64_t w_full, x_full, x_empty, v_full, v_empty, gk_full, gk_empty;
-  uint64_t ax_full, lq_full, vs_full, gq_full, sb_full, p_full, pb_full, o_full, s_full;
+  uint64_t w_full, x_full, op_empty, v_full, v_empty, gk_full, gk_empty;
+  uint64_t ax_full, lq_full, gq_full, sb_full, p_full, pb_full, o_full;
   uint64_t done;
   uint32_t tmem_base;
   Abort ab;
@@ -958,6 +987,26 @@ __device__ __forceinline__ void snapshot_state_chunk(uint32_t sb, int Kp, int co
   }
 }
 
+// Converts this thread's 16 dims of its token row in place: bf16 x (as loaded into the second block of
+// the operand at `op`) -> fp16 x there and fp16 x^2 at the same place of the first block.
+__device__ __forceinline__ void convert_row(uint32_t op, const RowCtx& rc) {
+#pragma unroll
+  for (int jj = 0; jj < 2; ++jj) {
+    const uint32_t ad = (op + 16384u + rc.rowq) ^ (uint32_t)(jj << 4);
+    const uint4 v = lds128(ad);
+    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+    uint32_t sq[4], lin[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float lo = __uint_as_float(w4[i] << 16), hi = __uint_as_float(w4[i] & 0xffff0000u);
+      lin[i] = pack_f16x2(lo, hi);
+      sq[i] = pack_f16x2(lo * lo, hi * hi);
+    }
+    sts128(ad, make_uint4(lin[0], lin[1], lin[2], lin[3]));
+    sts128(ad - 16384u, make_uint4(sq[0], sq[1], sq[2], sq[3]));
+  }
+}
+
 template <int NC>
 __global__ void __launch_bounds__(kThreadsTc, 1)
     tc_causal_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmG,
@@ -975,29 +1024,26 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   const int KB = (a.Kp + 63) / 64;
   const int KS = a.Kp / 16;
 
-  // zero the Gamma_K blocks no load reaches (Kp <= 128), the 1/s atom (its column 0 is rewritten every
-  // tile) and the state copies
+  // zero the Gamma_K blocks no load reaches (Kp <= 128), the constant atom and the state copies
   for (uint32_t i = threadIdx.x; i < (uint32_t)MB * 32768 / 16; i += blockDim.x)
     reinterpret_cast<uint4*>(smem + L.gk)[i] = make_uint4(0, 0, 0, 0);
-  for (uint32_t i = threadIdx.x; i < (L.c - L.ones) / 16; i += blockDim.x)
-    reinterpret_cast<uint4*>(smem + L.ones)[i] = make_uint4(0, 0, 0, 0);
+  for (uint32_t i = threadIdx.x; i < (L.c - (L.v + 16384)) / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(smem + L.v + 16384)[i] = make_uint4(0, 0, 0, 0);
   if (threadIdx.x == 0) {
     mbar_init(&B.w_full, 1);
     mbar_init(&B.x_full, 1);
-    mbar_init(&B.x_empty, kRowWarps);
+    mbar_init(&B.op_empty, 1);
     mbar_init(&B.v_full, 1);
     mbar_init(&B.v_empty, 1);
     mbar_init(&B.gk_full, 1);
     mbar_init(&B.gk_empty, 1);
     mbar_init(&B.ax_full, kRowWarps);
     mbar_init(&B.lq_full, 1);
-    mbar_init(&B.vs_full, kRowWarps);
     mbar_init(&B.gq_full, kRowWarps);
     mbar_init(&B.sb_full, kRowWarps);
     mbar_init(&B.p_full, 1);
     mbar_init(&B.pb_full, kRowWarps);
     mbar_init(&B.o_full, 1);
-    mbar_init(&B.s_full, 1);
     mbar_init(&B.done, 1);
     B.ab.flag = 0;
     mbar_fence_init();
@@ -1018,7 +1064,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       // ---------------------------------------------------------------- producer
       const uint32_t wbytes = (uint32_t)a.Kp * 256, cbytes = kCTable * 4;
       const int h = bh % a.H;
-      const float* inv_row = a.inv + (size_t)bh * a.tiles * kTile;
       mbar_expect_tx(&B.w_full, wbytes + cbytes);
       for (uint32_t o = 0; o < wbytes; o += 32768)
         bulk_load(smem + L.w + o, a.w_img + (size_t)h * wbytes + o, min(32768u, wbytes - o), &B.w_full);
@@ -1027,18 +1072,18 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       for (int t = 0; t < T; ++t) {
         const uint32_t pe = (t & 1) ^ 1;
         const int row0 = (tile0 + t) * kTile;
-        if (!wait_bounded(&B.x_empty, pe, &B.ab, a.ctrl, 70, a.wait_ns)) break;
+        // X(t) once the previous logits contraction has read the operand
+        if (!wait_bounded(&B.op_empty, pe, &B.ab, a.ctrl, 70, a.wait_ns)) break;
         mbar_expect_tx(&B.x_full, 16384);
-        tma_load_3d(smem + L.x, &tmQ, 0, row0, bh, &B.x_full);
+        tma_load_3d(smem + L.op + 16384, &tmQ, 0, row0, bh, &B.x_full);
         issued[0] = t & 1;
         if (!wait_bounded(&B.gk_empty, pe, &B.ab, a.ctrl, 71, a.wait_ns)) break;
         mbar_expect_tx(&B.gk_full, (uint32_t)KB * 16384u);
         for (int j = 0; j < KB; ++j) tma_load_3d(smem + L.gk + 16384 * j, &tmG, 64 * j, row0, bh, &B.gk_full);
         issued[1] = t & 1;
         if (!wait_bounded(&B.v_empty, pe, &B.ab, a.ctrl, 72, a.wait_ns)) break;
-        mbar_expect_tx(&B.v_full, 16384 + kTile * 4);
+        mbar_expect_tx(&B.v_full, 16384);
         for (int a4 = 0; a4 < 4; ++a4) tma_load_3d(smem + L.v + 4096 * a4, &tmV, 16 * a4, row0, bh, &B.v_full);
-        bulk_load(smem + L.inv, inv_row + row0, kTile * 4, &B.v_full);
         issued[2] = t & 1;
       }
       // never leave with copies in flight
@@ -1048,28 +1093,33 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       if (issued[2] >= 0) wait_bounded(&B.v_full, (uint32_t)issued[2], &none, a.ctrl, 75, a.wait_ns);
     } else if (warp == 1 && lane == 0) {
       // ---------------------------------------------------------------- MMA issuer
-      const uint32_t w_addr = smem_u32(smem + L.w);
+      const uint32_t w_addr = smem_u32(smem + L.w), op_addr = smem_u32(smem + L.op);
       // base descriptors; every operand step below is a byte offset added to one of them
-      // [S_prev | Z + eps] (Kp x 80) and [V | 1/s] (128 x 80): MN-major, 32-byte swizzle, 16 rows = 512 B
+      // [S_prev | Z + eps] (Kp x 80) and [V | 1] (128 x 80): MN-major, 32-byte swizzle, 16 rows = 512 B
       const uint64_t d_sb = make_sdesc32(smem_u32(smem + L.sbv), (uint32_t)a.Kp * 32, 256);
       const uint64_t d_vb = make_sdesc32(smem_u32(smem + L.v), 4096, 256);
       const uint64_t d_gk_k = make_sdesc(smem_u32(smem + L.gk), 16, 1024);     // Gamma_K as K-major B
       const uint64_t d_gk_mn = make_sdesc(smem_u32(smem + L.gk), 16384, 1024); // Gamma_K^T as MN-major A
+      const uint32_t id_log = make_idesc(128, a.Kp, 0, 0, 0, 0);         // fp16 A and B, both K-major
       constexpr uint32_t id_c80 = make_idesc(128, kStCols, 1, 1, 0, 1);  // A tmem, B MN-major, N = 80
       constexpr uint32_t id_p = make_idesc(128, 128, 1, 1, 0, 0);         // P = Gq~ Gk^T
       constexpr uint32_t id_s80 = make_idesc(128, kStCols, 1, 1, 1, 1);  // A MN-major (Gamma_K^T), B MN-major
       bool ok = wait_bounded(&B.w_full, 0, &B.ab, a.ctrl, 80, a.wait_ns);
       for (int t = 0; ok && t < T; ++t) {
         const uint32_t ph = t & 1;
-        // query logits
+        // query logits: LOG[128 x Kp] = [x^2 | x] W^T (the previous tile's contractions have completed)
         if (!(ok = wait_bounded(&B.ax_full, ph, &B.ab, a.ctrl, 81, a.wait_ns))) break;
         tc_fence_after();
-        issue_logits(tmem, w_addr, a.Kp, kCColO);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          mma_ss(tmem + kColLog, make_sdesc(op_addr + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                 make_sdesc(w_addr + (ks >> 2) * (uint32_t)a.Kp * 128 + (ks & 3) * 32, 16, 1024), id_log, ks > 0);
         mma_commit(&B.lq_full);
-        // state update S += Gamma_K^T [V | 1] while the query softmax runs: needs the loaded Gamma_K, the
-        // scaled V rows and the bf16 snapshot of S_prev taken
+        mma_commit(&B.op_empty);
+        // state update S += Gamma_K^T [V | 1] while the query softmax runs: needs the loaded Gamma_K and V
+        // tiles and the bf16 snapshot of S_prev taken
         if (!(ok = wait_bounded(&B.gk_full, ph, &B.ab, a.ctrl, 83, a.wait_ns) &&
-                   wait_bounded(&B.vs_full, ph, &B.ab, a.ctrl, 84, a.wait_ns) &&
+                   wait_bounded(&B.v_full, ph, &B.ab, a.ctrl, 84, a.wait_ns) &&
                    wait_bounded(&B.sb_full, ph, &B.ab, a.ctrl, 85, a.wait_ns)))
           break;
         tc_fence_after();
@@ -1080,8 +1130,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             mma_ss(tmem + kCColS + kStCols * mb, sdesc_add(d_gk_mn, mb * 32768 + 2048 * s), sdesc_add(d_vb, 512 * s),
                    id_s80, 1u);
         }
-        mma_commit(&B.s_full);
-        // inter-tile term O = Gq~ S_prev and intra-tile affinity P = Gq~ Gk^T
+        // inter-tile term O = Gq~ S_prev and intra-tile affinity P = Gq~ Gk^T, interleaved
         if (!(ok = wait_bounded(&B.gq_full, ph, &B.ab, a.ctrl, 86, a.wait_ns))) break;
         tc_fence_after();
 #pragma unroll 1
@@ -1090,7 +1139,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           mma_ts(tmem + kCColO, aq, sdesc_add(d_sb, 512 * ks), id_c80, ks > 0);
           mma_ts(tmem + kCColP, aq, sdesc_add(d_gk_k, (ks >> 2) * 16384 + (ks & 3) * 32), id_p, ks > 0);
         }
-        mma_commit(&B.p_full);
+        mma_commit(&B.p_full);    // also: the inter-tile term has read S_prev
         mma_commit(&B.gk_empty);  // the state update and P were the last readers of this Gamma_K tile
         // intra-tile term O += P [V | 1]
         if (!(ok = wait_bounded(&B.pb_full, ph, &B.ab, a.ctrl, 88, a.wait_ns))) break;
@@ -1102,6 +1151,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         }
         mma_commit(&B.o_full);
         mma_commit(&B.v_empty);
+        // the next logits overwrite TMEM columns these contractions read: let them complete first
+        if (!(ok = wait_bounded(&B.o_full, ph, &B.ab, a.ctrl, 89, a.wait_ns))) break;
       }
       mma_commit(&B.done);
       Abort none{0};
@@ -1112,7 +1163,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     // ------------------------------------------------------------------ row warps
     const RowCtx rc = row_ctx(sbase + L.red);
     const uint32_t cs = sbase + L.c;
+    const uint32_t op = sbase + L.op;
     zero_unused_logits<NC>(tmem, rc, a.Kp);
+    if (rc.part == 0) sts16(sbase + L.v + 16384 + sw32_chunk(rc.row, 0), bf16_bits(1.f));  // the 1 column
     // S <- exclusive prefix state of this segment; SB <- its bf16 copy (eps rides in the Z column)
     if (rc.part < MB) {
       const int comp = 128 * rc.part + rc.row;
@@ -1131,14 +1184,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     tc_fence_before();
     warp_arrive(&B.sb_full);
     bool ok = warp_wait(&B.w_full, 0, &B.ab, a.ctrl, 90, a.wait_ns);
-    // query operand of the first tile (later ones are built in the previous tile's epilogue; the
-    // [x^2 | x] columns double as the output accumulator)
+    // query operand of the first tile (later ones are converted while the previous tile is in the
+    // tensor pipe)
     if (ok && T > 0) ok = warp_wait(&B.x_full, 0, &B.ab, a.ctrl, 91, a.wait_ns);
     if (ok && T > 0) {
-      transform_row(sbase + L.x, rc, tmem, kCColO);
-      warp_arrive(&B.x_empty);
-      tmem_st_wait();
-      tc_fence_before();
+      convert_row(op, rc);
+      fence_async_smem();
       warp_arrive(&B.ax_full);
     }
     float v[NC];
@@ -1146,15 +1197,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     for (int t = 0; t < T; ++t) {
       const uint32_t ph = t & 1;
       const int tok = (tile0 + t) * kTile + rc.row;
-      // this tile's V rows scaled by 1/s of their key (0 past N); 1/s also into the ones atom
-      if (ok) ok = warp_wait(&B.v_full, ph, &B.ab, a.ctrl, 98, a.wait_ns);
-      if (ok) {
-        const float inv = lds32(sbase + L.inv + 4u * (uint32_t)rc.row);
-        scale_v_row32(sbase + L.v, rc, inv);
-        if (rc.part == 0) sts16(sbase + L.ones + sw32_chunk(rc.row, 0), bf16_bits(inv));
-        fence_async_smem();
-        warp_arrive(&B.vs_full);
-      }
       // Gamma_Q~ (unnormalised) -> TMEM over its own logit columns.  The exchange slot alternates with
       // the tile, so a slot is rewritten only after the next tile's exchange, which every part thread
       // reaches after reading this one.
@@ -1177,7 +1219,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         tc_fence_after();
         uint32_t pr[32];
         tmem_ld32(tmem + rc.lane_base + kCColP + 32 * rc.part, pr);
-        tmem_ld_wait();
+        tmem_ld_wait_tied32(pr);
         const int lim = rc.row - 32 * rc.part;  // columns c <= lim are keys j <= i
         uint32_t pk[16];
 #pragma unroll
@@ -1191,8 +1233,17 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         tc_fence_before();
         warp_arrive(&B.pb_full);
       }
-      // the inter-tile term has read S_prev; snapshot the updated state for the next tile
-      if (ok) ok = warp_wait(&B.s_full, ph, &B.ab, a.ctrl, 101, a.wait_ns);
+      // next query operand (its X tile was loaded once this tile's logits had read the operand)
+      if (ok && t + 1 < T) {
+        ok = warp_wait(&B.x_full, (t + 1) & 1, &B.ab, a.ctrl, 91, a.wait_ns);
+        if (ok) {
+          convert_row(op, rc);
+          fence_async_smem();
+          warp_arrive(&B.ax_full);
+        }
+      }
+      // the inter-tile term has read S_prev and the state update has completed (both before p_full):
+      // snapshot the updated state for the next tile
       if (ok) {
         tc_fence_after();
         if (rc.part < MB) {
@@ -1201,7 +1252,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 #pragma unroll
           for (int c = 0; c < 5; ++c) {
             tmem_ld16(tmem + rc.lane_base + kCColS + kStCols * rc.part + 16 * c, r);
-            tmem_ld_wait();
+            tmem_ld_wait_tied16(r);
             if (comp < a.Kp) snapshot_state_chunk(sbase + L.sbv, a.Kp, comp, c, r, a.eps);
           }
         }
@@ -1209,33 +1260,18 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         tc_fence_before();
         warp_arrive(&B.sb_full);
       }
-      // output: this thread's output dims are 8*part + [0,8) and 32 + 8*part + [0,8) -- the same columns it
-      // overwrites with the next query operand, so no other warp reads them afterwards.  Once they are in
-      // registers the next query operand goes in (its contraction runs while this output is stored).
+      // output: this thread's dims 16*part + [0,16) (32 contiguous bytes), normalised by gq~ . (Z + eps)
       if (ok) ok = warp_wait(&B.o_full, ph, &B.ab, a.ctrl, 100, a.wait_ns);
       if (ok) {
         tc_fence_after();
-        uint32_t o0[8], o1[8];
-        tmem_ld8(tmem + rc.lane_base + kCColO + 8 * rc.part, o0);
-        tmem_ld8(tmem + rc.lane_base + kCColO + 32 + 8 * rc.part, o1);
+        uint32_t o16[16];
+        tmem_ld16(tmem + rc.lane_base + kCColO + 16 * rc.part, o16);
         uint32_t z = tmem_ld1(tmem + rc.lane_base + kCColO + 64);
-        tmem_ld_wait_tied8x2_1(o0, o1, z);
-        if (t + 1 < T) {
-          ok = warp_wait(&B.x_full, (t + 1) & 1, &B.ab, a.ctrl, 91, a.wait_ns);
-          if (ok) {
-            transform_row(sbase + L.x, rc, tmem, kCColO);
-            warp_arrive(&B.x_empty);
-            tmem_st_wait();
-            tc_fence_before();
-            warp_arrive(&B.ax_full);
-          }
-        }
-        const float rden = rcp_approx(__uint_as_float(z));  // gq~ . (Z_i + eps)
-        if (tok < a.N) {
-          __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.out) + ((size_t)bh * a.N + tok) * kDv;
-          store_out8(orow + 8 * rc.part, o0, rden);
-          store_out8(orow + 32 + 8 * rc.part, o1, rden);
-        }
+        tmem_ld_wait_tied16(o16);
+        tmem_ld_wait_tied1(z);
+        const float rden = rcp_approx(__uint_as_float(z));
+        if (tok < a.N)
+          store_out16(reinterpret_cast<__nv_bfloat16*>(a.out) + ((size_t)bh * a.N + tok) * kDv + 16 * rc.part, o16, rden);
       }
     }
   }
@@ -1296,16 +1332,16 @@ EncodeTiledFn encode_fn() {
 }
 
 // 3-D map over a [B*H][N][64] bf16 tensor, box 64 x 128 x 1, 128-byte swizzle, zero fill past N.
-// 3-D map over [B*H][N][64] bf16 with 128-row boxes: 64-dim boxes in the 128-byte swizzle, or (sw32)
-// 16-dim boxes in the 32-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, int BH, int N, bool sw32 = false) {
+// 3-D map over [B*H][N][ld] bf16 (ld = 64 unless given) with 128-row boxes: 64-element boxes in the
+// 128-byte swizzle, or (sw32) 16-element boxes in the 32-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, int BH, int N, bool sw32 = false, int ld = kD) {
   EncodeTiledFn f = encode_fn();
   if (!f) {
     set_error_detail("cuTensorMapEncodeTiled entry point unavailable");
     return false;
   }
-  cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)N, (cuuint64_t)BH};
-  cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)N * kD * 2};
+  cuuint64_t dims[3] = {(cuuint64_t)ld, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)ld * 2, (cuuint64_t)N * ld * 2};
   cuuint32_t box[3] = {sw32 ? 16u : 64u, (cuuint32_t)kTile, 1}, es[3] = {1, 1, 1};
   const CUresult r = f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
                        CU_TENSOR_MAP_INTERLEAVE_NONE, sw32 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_128B,
@@ -1366,9 +1402,10 @@ gma_status_t tc_launch(const gma_problem_t& p, gma_op_t op, int Nk, const TcPlan
     return check_launch("launch tc_resp", (const void*)tc_read_kernel<false, NC>);
   }
   if (op == GMA_OP_CAUSAL) {
-    CUtensorMap mv32, mg;  // the chunk kernel's V tiles (four 16-dim boxes, 32-byte swizzle); Gamma~_K
+    // Gamma_K of every key (stored by the aggregates, loaded by the sweep); the sweep's V tiles are four
+    // 16-dim boxes in the 32-byte swizzle
+    CUtensorMap mg, mv32;
     void* gk = (char*)ws + pl.off_gk;
-    a.inv = (float*)((char*)ws + pl.off_inv);
     if (!make_map(&mq, Q, BH, p.N) || !make_map(&mk, K, BH, p.N) || !make_map(&mv, V, BH, p.N) ||
         !make_map(&mv32, V, BH, p.N, true) || !make_gamma_map(&mg, gk, BH, p.N, (pl.Kp + 63) / 64 * 64))
       return GMA_ERR_CUDA;
@@ -1403,7 +1440,7 @@ gma_status_t tc_launch(const gma_problem_t& p, gma_op_t op, int Nk, const TcPlan
     const uint32_t smem_w = smem_bytes(write_layout(pl.Kp).total);
     if (set_smem_optin((const void*)tc_write_kernel<true, NC>, (int)smem_w, 0) != GMA_OK) return GMA_ERR_CUDA;
     GMA_LAUNCH("tc_bidir_write", (tc_write_kernel<true, NC>), dim3(plk.splits, BH), kThreadsTc, smem_w, st, mk, mv, mk,
-               aw);  // (the third map is unused without the causal key store)
+               aw);  // (the third map serves only the causal key store)
     if (gma_status_t e = check_launch("launch tc_bidir_write", (const void*)tc_write_kernel<true, NC>)) return e;
   }
   if (op == GMA_OP_CAUSAL_STATE) return GMA_OK;  // the state alone
@@ -1434,12 +1471,9 @@ TcPlan tc_plan(const gma_problem_t& p, gma_op_t op) {
   size_t st = 0;
   if (op == GMA_OP_BIDIR || op == GMA_OP_CROSS || op == GMA_OP_CAUSAL_STATE) st = (size_t)BH * t.Kp * kStCols * 4;
   if (op == GMA_OP_CAUSAL) st = (size_t)BH * t.splits * t.Kp * kStCols * 4;  // segment aggregates
-  t.off_gk = t.off_inv = t.total = align_up(t.off_state + st);
-  if (op == GMA_OP_CAUSAL) {
-    // Gamma~_K of every key (bf16, 64-component blocks) and 1/s of every key (float32, per full tile)
-    t.off_inv = align_up(t.off_gk + (size_t)BH * p.N * ((t.Kp + 63) / 64 * 64) * 2);
-    t.total = align_up(t.off_inv + (size_t)BH * t.tiles * kTile * 4);
-  }
+  t.off_gk = t.total = align_up(t.off_state + st);
+  if (op == GMA_OP_CAUSAL)  // normalised Gamma_K of every key (bf16, 64-component blocks)
+    t.total = align_up(t.off_gk + (size_t)BH * p.N * ((t.Kp + 63) / 64 * 64) * 2);
   return t;
 }
 

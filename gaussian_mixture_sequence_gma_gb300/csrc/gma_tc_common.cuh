@@ -321,6 +321,12 @@ __device__ __forceinline__ void add_f32x2(float& a, float& b, float c, float d) 
       : "+f"(a), "+f"(b)
       : "f"(c), "f"(d));
 }
+__device__ __forceinline__ void mul_f32x2(float& a, float& b, float c, float d) {
+  asm("{\n .reg .b64 x, y;\n mov.b64 x, {%0, %1};\n mov.b64 y, {%2, %3};\n mul.rn.f32x2 x, x, y;\n"
+      " mov.b64 {%0, %1}, x;\n}\n"
+      : "+f"(a), "+f"(b)
+      : "f"(c), "f"(d));
+}
 // Three-input maximum.
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float d;

@@ -141,8 +141,8 @@ GMA_API size_t gma_static_ws_capacity(void);
  * Passage: gist.science summary, "Variants and training" item 3 (prefix sums
  * of the latent memory and normaliser; O at position i depends on j <= i only).
  * Same arguments and layouts as gma_forward_bidir.  With bf16 I/O the workspace grows with N:
- * it holds every key's unnormalised responsibilities (bf16, B*H*N*64*ceil(K/64) elements) and
- * 1/s of every key, computed once and read back by the chunked sweep.
+ * it holds every key's responsibilities (bf16, B*H*N*64*ceil(K/64) elements), computed once by
+ * the segment aggregates and read back by the chunked sweep.
  */
 GMA_API gma_status_t gma_forward_causal(const gma_problem_t *p, const void *Q, const void *K, const void *V, const float *mu,
                                 const float *sigma2, const float *log_pi, void *O, void *ws, size_t ws_bytes,
