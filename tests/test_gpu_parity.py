@@ -82,7 +82,7 @@ def test_sweep_bf16_B1H8K256(gma, N, causal):
 # ------------------------------------------------------------------------------------ shapes and edges
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("K", [1, 3, 16, 17, 256])
+@pytest.mark.parametrize("K", [1, 3, 16, 17, 100, 200, 256])
 @pytest.mark.parametrize("causal", [False, True])
 def test_ragged_small(gma, dtype, K, causal):
     inp = make_inputs(2, 3, 300, K, dtype=dtype, seed=100 + K)
