@@ -1284,19 +1284,19 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 }
 
 // Exclusive scan over segments: agg[bh][p][e] <- sum_{p' < p} agg[bh][p'][e].  grid (ceil(n / 256), B*H).
-// Loads go out eight segments at a time so the chain over p is not one dependent load after another.
+// Each thread has all loads of up to 32 segments in flight before the first store.
 __global__ void tc_scan_kernel(float* agg, int P, int n) {
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= n) return;
   float* base = agg + (size_t)blockIdx.y * P * n + e;
   float run = 0.f;
-  for (int p0 = 0; p0 < P; p0 += 8) {
-    float x[8];
+  for (int p0 = 0; p0 < P; p0 += 32) {
+    float x[32];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) x[j] = (p0 + j < P) ? base[(size_t)(p0 + j) * n] : 0.f;
+    for (int j = 0; j < 32; ++j) x[j] = (p0 + j < P) ? __ldcg(base + (size_t)(p0 + j) * n) : 0.f;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (p0 + j < P) base[(size_t)(p0 + j) * n] = run;
+    for (int j = 0; j < 32; ++j) {
+      if (p0 + j < P) __stcg(base + (size_t)(p0 + j) * n, run);
       run += x[j];
     }
   }
