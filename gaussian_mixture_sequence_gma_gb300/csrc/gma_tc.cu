@@ -1123,31 +1123,37 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                    wait_bounded(&B.sb_full, ph, &B.ab, a.ctrl, 85, a.wait_ns)))
           break;
         tc_fence_after();
-#pragma unroll 1
-        for (int mb = 0; mb < MB; ++mb) {
-#pragma unroll 1
-          for (int s = 0; s < 8; ++s)
-            mma_ss(tmem + kCColS + kStCols * mb, sdesc_add(d_gk_mn, mb * 32768 + 2048 * s), sdesc_add(d_vb, 512 * s),
-                   id_s80, 1u);
+        // (the contraction loops are unrolled: the issuing thread's own instructions between two MMAs
+        // would otherwise leave the tensor pipe waiting)
+#pragma unroll
+        for (int mb = 0; mb < 2; ++mb) {
+          if (mb < MB) {
+#pragma unroll
+            for (int s = 0; s < 8; ++s)
+              mma_ss_off(tmem + kCColS + kStCols * mb, d_gk_mn, (mb * 32768 + 2048 * s) >> 4, d_vb, (512 * s) >> 4,
+                         id_s80, 1u);
+          }
         }
         // inter-tile term O = Gq~ S_prev and intra-tile affinity P = Gq~ Gk^T, interleaved
         if (!(ok = wait_bounded(&B.gq_full, ph, &B.ab, a.ctrl, 86, a.wait_ns))) break;
         tc_fence_after();
-#pragma unroll 1
-        for (int ks = 0; ks < KS; ++ks) {
-          const uint32_t aq = tmem + kColLog + 8 * ks;  // Gq~ (bf16 pairs) over the logit columns
-          mma_ts(tmem + kCColO, aq, sdesc_add(d_sb, 512 * ks), id_c80, ks > 0);
-          mma_ts(tmem + kCColP, aq, sdesc_add(d_gk_k, (ks >> 2) * 16384 + (ks & 3) * 32), id_p, ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < 16; ++ks) {
+          if (ks < KS) {
+            const uint32_t aq = tmem + kColLog + 8 * ks;  // Gq~ (bf16 pairs) over the logit columns
+            mma_ts_off(tmem + kCColO, aq, d_sb, (512 * ks) >> 4, id_c80, ks > 0);
+            mma_ts_off(tmem + kCColP, aq, d_gk_k, ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4, id_p, ks > 0);
+          }
         }
         mma_commit(&B.p_full);    // also: the inter-tile term has read S_prev
         mma_commit(&B.gk_empty);  // the state update and P were the last readers of this Gamma_K tile
         // intra-tile term O += P [V | 1]
         if (!(ok = wait_bounded(&B.pb_full, ph, &B.ab, a.ctrl, 88, a.wait_ns))) break;
         tc_fence_after();
-#pragma unroll 1
+#pragma unroll
         for (int s = 0; s < 8; ++s) {
           const uint32_t ap = tmem + kCColP + 32 * (s >> 1) + 8 * (s & 1);  // bf16 P of keys 16s..16s+15
-          mma_ts(tmem + kCColO, ap, sdesc_add(d_vb, 512 * s), id_c80, 1u);
+          mma_ts_off(tmem + kCColO, ap, d_vb, (512 * s) >> 4, id_c80, 1u);
         }
         mma_commit(&B.o_full);
         mma_commit(&B.v_empty);

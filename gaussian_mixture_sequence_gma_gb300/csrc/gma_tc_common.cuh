@@ -141,6 +141,25 @@ __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, 
       "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
+// The same with the descriptors given as a base plus an offset (in 16-byte units) added right before the
+// instruction, so unrolled issue loops keep only their base descriptors live.
+__device__ __forceinline__ void mma_ss_off(uint32_t d, uint64_t a, uint32_t a_off, uint64_t b, uint32_t b_off,
+                                           uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n .reg .b64 ad, bd, ao, bo;\n setp.ne.b32 p, %6, 0;\n cvt.u64.u32 ao, %2;\n"
+      " cvt.u64.u32 bo, %4;\n add.s64 ad, %1, ao;\n add.s64 bd, %3, bo;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, p;\n}\n" ::"r"(d),
+      "l"(a), "r"(a_off), "l"(b), "r"(b_off), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts_off(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t b_off, uint32_t idesc,
+                                           uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n .reg .b64 bd, bo;\n setp.ne.b32 p, %5, 0;\n cvt.u64.u32 bo, %3;\n add.s64 bd, %2, bo;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, p;\n}\n" ::"r"(d),
+      "r"(a_tmem), "l"(b), "r"(b_off), "r"(idesc), "r"(acc)
+      : "memory");
+}
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
