@@ -475,14 +475,14 @@ __device__ __forceinline__ void producer(const TcArgs& a, const CUtensorMap* tmX
     if (issued[s] >= 0) wait_bounded(&B->x_full[s], (uint32_t)issued[s], &none, a.ctrl, 12, a.wait_ns);
 }
 
-// Issues the log-density contraction of one tile: LOG[128 x Kp] = AX[128 x 128] * W^T.
-__device__ __forceinline__ void issue_logits(uint32_t tmem, uint32_t w_addr, int Kp, uint32_t col_ax = kColAx) {
+// Issues the log-density contraction of one tile: LOG[128 x Kp] = AX[128 x 128] * W^T (d_w: descriptor
+// of the K-major W image at its start).
+__device__ __forceinline__ void issue_logits(uint32_t tmem, uint64_t d_w, int Kp, uint32_t col_ax = kColAx) {
   const uint32_t idesc = make_idesc(128, Kp, 0, 0, 0, 0);
 #pragma unroll
-  for (int ks = 0; ks < 8; ++ks) {
-    const uint64_t bd = make_sdesc(w_addr + (ks >> 2) * (uint32_t)Kp * 128 + (ks & 3) * 32, 16, 1024);
-    mma_ts(tmem + kColLog, tmem + col_ax + 8 * ks, bd, idesc, ks > 0 ? 1u : 0u);
-  }
+  for (int ks = 0; ks < 8; ++ks)
+    mma_ts_off(tmem + kColLog, tmem + col_ax + 8 * ks, d_w, (ks >> 2) * (uint32_t)Kp * 8 + (ks & 3) * 2, idesc,
+               ks > 0 ? 1u : 0u);
 }
 
 // Normalises 16 output dims of one row (acc / (z + eps s)) and stores them as bf16 (two 16-byte stores).
@@ -552,11 +552,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const uint32_t idw = make_idesc(128, kStCols, 1, 1, 1, 1);
         const uint32_t w_addr = smem_u32(smem + L.w), g_addr = smem_u32(smem + L.g);
         const uint32_t v_addr = smem_u32(smem + L.v), inv_addr = smem_u32(smem + L.inv);
+        const uint64_t d_w = make_sdesc(w_addr, 16, 1024), d_g = make_sdesc(g_addr, 16384, 1024);
+        // [V | 1] of ring slot s: MN-major, the 1 atom one leading-dimension step past the V atom
+        const uint64_t d_v0 = make_sdesc(v_addr, inv_addr - v_addr, 1024);
+        const uint64_t d_v1 = make_sdesc(v_addr + 16384, inv_addr - v_addr - 16384, 1024);
         bool ok = wait_bounded(&B.w_full, 0, &B.ab, a.ctrl, 20, a.wait_ns);
         if (ok && T > 0) ok = wait_bounded(&B.ax_full, 0, &B.ab, a.ctrl, 21, a.wait_ns);
         if (ok && T > 0) {
           tc_fence_after();
-          issue_logits(tmem, w_addr, a.Kp);
+          issue_logits(tmem, d_w, a.Kp);
           mma_commit(&B.l_full);  // also frees the [x^2 | x] columns for the next tile
         }
         for (int t = 0; ok && t < T; ++t) {
@@ -565,7 +569,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                  wait_bounded(&B.l_empty, t & 1, &B.ab, a.ctrl, 23, a.wait_ns);
             if (!ok) break;
             tc_fence_after();
-            issue_logits(tmem, w_addr, a.Kp);
+            issue_logits(tmem, d_w, a.Kp);
             mma_commit(&B.l_full);
           }
           const int s = t & 1;
@@ -573,13 +577,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           ok = wait_bounded(&B.g_full, t & 1, &B.ab, a.ctrl, 24, a.wait_ns);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t vs = v_addr + s * 16384;
-          for (int mb = 0; mb < MB; ++mb) {
+          const uint64_t d_v = s ? d_v1 : d_v0;
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-              const uint64_t ad = make_sdesc(g_addr + mb * 32768 + ks * 2048, 16384, 1024);
-              const uint64_t bd = make_sdesc(vs + ks * 2048, inv_addr - vs, 1024);
-              mma_ss(tmem + kColAcc + kStCols * mb, ad, bd, idw, (t > 0 || ks > 0) ? 1u : 0u);
+          for (int mb = 0; mb < 2; ++mb) {
+            if (mb < MB) {
+#pragma unroll
+              for (int ks = 0; ks < 8; ++ks)
+                mma_ss_off(tmem + kColAcc + kStCols * mb, d_g, (mb * 32768 + ks * 2048) >> 4, d_v, (ks * 2048) >> 4, idw,
+                           (t > 0 || ks > 0) ? 1u : 0u);
             }
           }
           mma_commit(&B.g_empty);
@@ -747,12 +752,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     if (lane == 0) {
       const uint32_t idr = make_idesc(128, kStCols, 1, 1, 0, 0);
       const uint32_t w_addr = smem_u32(smem + L.w), g_addr = smem_u32(smem + L.g), sb_addr = smem_u32(smem + L.sb);
+      const uint64_t d_w = make_sdesc(w_addr, 16, 1024), d_g = make_sdesc(g_addr, 16, 1024);
+      const uint64_t d_sb = make_sdesc(sb_addr, 16, 1024);
       bool ok = wait_bounded(&B.w_full, 0, &B.ab, a.ctrl, 40, a.wait_ns);
       if (kRead && ok) ok = wait_bounded(&B.sb_full, 0, &B.ab, a.ctrl, 41, a.wait_ns);
       if (ok && T > 0) ok = wait_bounded(&B.ax_full, 0, &B.ab, a.ctrl, 42, a.wait_ns);
       if (ok && T > 0) {
         tc_fence_after();
-        issue_logits(tmem, w_addr, a.Kp);
+        issue_logits(tmem, d_w, a.Kp);
         mma_commit(&B.l_full);  // also frees the [x^2 | x] columns for the next tile
       }
       for (int t = 0; ok && t < T; ++t) {
@@ -761,7 +768,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                wait_bounded(&B.l_empty, t & 1, &B.ab, a.ctrl, 44, a.wait_ns);
           if (!ok) break;
           tc_fence_after();
-          issue_logits(tmem, w_addr, a.Kp);
+          issue_logits(tmem, d_w, a.Kp);
           mma_commit(&B.l_full);
         }
         if (kRead) {
@@ -769,10 +776,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           if (ok && t > 0) ok = wait_bounded(&B.o_empty, (t - 1) & 1, &B.ab, a.ctrl, 46, a.wait_ns);
           if (!ok) break;
           tc_fence_after();
-          for (int ks = 0; ks < KS; ++ks) {
-            const uint64_t ad = make_sdesc(g_addr + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
-            const uint64_t bd = make_sdesc(sb_addr + (ks >> 2) * (kStCols * 128) + (ks & 3) * 32, 16, 1024);
-            mma_ss(tmem + kColAcc, ad, bd, idr, ks > 0 ? 1u : 0u);
+#pragma unroll
+          for (int ks = 0; ks < 16; ++ks) {
+            if (ks < KS)
+              mma_ss_off(tmem + kColAcc, d_g, ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4, d_sb,
+                         ((ks >> 2) * (kStCols * 128) + (ks & 3) * 32) >> 4, idr, ks > 0 ? 1u : 0u);
           }
           mma_commit(&B.g_empty);
           mma_commit(&B.o_full);
@@ -1093,7 +1101,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       if (issued[2] >= 0) wait_bounded(&B.v_full, (uint32_t)issued[2], &none, a.ctrl, 75, a.wait_ns);
     } else if (warp == 1 && lane == 0) {
       // ---------------------------------------------------------------- MMA issuer
-      const uint32_t w_addr = smem_u32(smem + L.w), op_addr = smem_u32(smem + L.op);
+      const uint64_t d_w = make_sdesc(smem_u32(smem + L.w), 16, 1024), d_op = make_sdesc(smem_u32(smem + L.op), 16, 1024);
       // base descriptors; every operand step below is a byte offset added to one of them
       // [S_prev | Z + eps] (Kp x 80) and [V | 1] (128 x 80): MN-major, 32-byte swizzle, 16 rows = 512 B
       const uint64_t d_sb = make_sdesc32(smem_u32(smem + L.sbv), (uint32_t)a.Kp * 32, 256);
@@ -1112,8 +1120,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          mma_ss(tmem + kColLog, make_sdesc(op_addr + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
-                 make_sdesc(w_addr + (ks >> 2) * (uint32_t)a.Kp * 128 + (ks & 3) * 32, 16, 1024), id_log, ks > 0);
+          mma_ss_off(tmem + kColLog, d_op, ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4, d_w,
+                     (ks >> 2) * (uint32_t)a.Kp * 8 + (ks & 3) * 2, id_log, ks > 0);
         mma_commit(&B.lq_full);
         mma_commit(&B.op_empty);
         // state update S += Gamma_K^T [V | 1] while the query softmax runs: needs the loaded Gamma_K and V
