@@ -355,16 +355,13 @@ __device__ __forceinline__ void store_packed(const float* v, uint32_t ga, const 
     if (cj < nvalid) sts128(ga ^ (uint32_t)(cj << 4), make_uint4(w[4 * cj], w[4 * cj + 1], w[4 * cj + 2], w[4 * cj + 3]));
 }
 
-// Normalised pack in place: word i of v receives the bf16 pair of components 2i, 2i+1 times inv.
+// The NC/2 bf16 pairs packed in v (exp_pack_regs) times bf16(inv), in place.
 template <int NC>
-__device__ __forceinline__ void scale_pack(float* v, float inv) {
-  uint32_t* w = reinterpret_cast<uint32_t*>(v);
+__device__ __forceinline__ void scale_packed(float* v, float inv) {
+  __nv_bfloat162* w = reinterpret_cast<__nv_bfloat162*>(v);
+  const __nv_bfloat162 inv2 = __float2bfloat162_rn(inv);
 #pragma unroll
-  for (int i = 0; i < NC / 2; ++i) {
-    float e0 = v[2 * i], e1 = v[2 * i + 1];
-    mul_f32x2(e0, e1, inv, inv);
-    w[i] = pack_bf16x2(e0, e1);
-  }
+  for (int i = 0; i < NC / 2; ++i) w[i] = __hmul2(w[i], inv2);
 }
 
 // Fused pass for a TMEM-resident operand: e = 2^(v - m) packed to bf16 pairs and stored over this thread's
@@ -671,12 +668,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           if (rc.part == 0) sts16(sbase + L.inv + rc.rowsw, bf16_bits(inv));
         }
       } else {
-        // normalised Gamma row (0 past N) -> smem once the previous contraction and store have read it
+        // normalised Gamma row (0 past N) -> smem once the previous contraction and store have read it:
+        // pack the exponentials to bf16 before the sum exchange, scale the pairs by 1/s after it
         float sp = 0.f;
-        if (ok) sp = exp_inplace<NC>(v, m);
+        if (ok) sp = exp_pack_regs<NC, true>(v, m);
         const float sum = xchg_sum(rc, 4, sp);
         if (ok) {
-          scale_pack<NC>(v, tok < a.N ? rcp_approx(sum) : 0.f);
+          scale_packed<NC>(v, tok < a.N ? rcp_approx(sum) : 0.f);
           if (t > 0) ok = warp_wait(&B.g_empty, (t - 1) & 1, &B.ab, a.ctrl, 36, a.wait_ns);
           if (ok) store_packed<NC>(v, ga, rc, a.Kp);
         }
