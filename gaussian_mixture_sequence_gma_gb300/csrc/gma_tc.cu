@@ -16,7 +16,8 @@
 //   its sum.
 //
 // Roles per CTA (640 threads = 5 warpgroups): warp 0 = TMA producer, warp 1 = MMA issuer (one thread)
-// and TMEM owner, warps 2-3 idle; warpgroups 1-4 (warps 4..19) = row warps: thread (q, part) owns token
+// and TMEM owner, warps 2-3 = helpers (causal aggregates: the Gamma_K store; causal sweep: the query
+// operand) or idle; warpgroups 1-4 (warps 4..19) = row warps: thread (q, part) owns token
 // row 32q+lane of the tile and a quarter of its components / dimensions (TMEM lane quarter q = warp % 4,
 // part = warpgroup - 1).  The control warpgroup hands registers to the row warpgroups with setmaxnreg.
 #include <algorithm>
@@ -993,12 +994,13 @@ __device__ __forceinline__ void snapshot_state_chunk(uint32_t sb, int Kp, int co
   }
 }
 
-// Converts this thread's 16 dims of its token row in place: bf16 x (as loaded into the second block of
-// the operand at `op`) -> fp16 x there and fp16 x^2 at the same place of the first block.
-__device__ __forceinline__ void convert_row(uint32_t op, const RowCtx& rc) {
-#pragma unroll
-  for (int jj = 0; jj < 2; ++jj) {
-    const uint32_t ad = (op + 16384u + rc.rowq) ^ (uint32_t)(jj << 4);
+// Converts token row `row` of the query operand in place: bf16 x (as loaded into the second block of the
+// operand at `op`) -> fp16 x there and fp16 x^2 at the same place of the first block.
+__device__ __forceinline__ void convert_row(uint32_t op, int row) {
+  const uint32_t base = op + 16384u + (uint32_t)row * 128u, sw = (uint32_t)(row & 7);
+#pragma unroll 2
+  for (int c = 0; c < 8; ++c) {
+    const uint32_t ad = base + (((uint32_t)c ^ sw) << 4);
     const uint4 v = lds128(ad);
     const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
     uint32_t sq[4], lin[4];
@@ -1043,7 +1045,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     mbar_init(&B.v_empty, 1);
     mbar_init(&B.gk_full, 1);
     mbar_init(&B.gk_empty, 1);
-    mbar_init(&B.ax_full, kRowWarps);
+    mbar_init(&B.ax_full, 2);  // warps 2 and 3 build the query operand
     mbar_init(&B.lq_full, 1);
     mbar_init(&B.gq_full, kRowWarps);
     mbar_init(&B.sb_full, kRowWarps);
@@ -1169,13 +1171,24 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       mma_commit(&B.done);
       Abort none{0};
       wait_bounded(&B.done, 0, &none, a.ctrl, 87, a.wait_ns);
+    } else if (warp >= 2) {
+      // ---------------------------------------------------------------- query operand (warps 2, 3)
+      // X(t) lands once the logits of tile t-1 have read the operand; 64 token rows per warp
+      const uint32_t op = sbase + L.op;
+      const int r0 = 64 * (warp - 2) + lane;
+      for (int t = 0; t < T; ++t) {
+        if (!warp_wait(&B.x_full, t & 1, &B.ab, a.ctrl, 91, a.wait_ns)) break;
+        convert_row(op, r0);
+        convert_row(op, r0 + 32);
+        fence_async_smem();
+        warp_arrive(&B.ax_full);
+      }
     }
   } else {
     setmaxnreg_inc<kRowRegs>();
     // ------------------------------------------------------------------ row warps
     const RowCtx rc = row_ctx(sbase + L.red);
     const uint32_t cs = sbase + L.c;
-    const uint32_t op = sbase + L.op;
     zero_unused_logits<NC>(tmem, rc, a.Kp);
     if (rc.part == 0) sts16(sbase + L.v + 16384 + sw32_chunk(rc.row, 0), bf16_bits(1.f));  // the 1 column
     // S <- exclusive prefix state of this segment; SB <- its bf16 copy (eps rides in the Z column)
@@ -1196,14 +1209,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     tc_fence_before();
     warp_arrive(&B.sb_full);
     bool ok = warp_wait(&B.w_full, 0, &B.ab, a.ctrl, 90, a.wait_ns);
-    // query operand of the first tile (later ones are converted while the previous tile is in the
-    // tensor pipe)
-    if (ok && T > 0) ok = warp_wait(&B.x_full, 0, &B.ab, a.ctrl, 91, a.wait_ns);
-    if (ok && T > 0) {
-      convert_row(op, rc);
-      fence_async_smem();
-      warp_arrive(&B.ax_full);
-    }
     float v[NC];
     // every row warp runs all T tiles and all exchanges (see the write kernel)
     for (int t = 0; t < T; ++t) {
@@ -1245,27 +1250,27 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         tc_fence_before();
         warp_arrive(&B.pb_full);
       }
-      // next query operand (its X tile was loaded once this tile's logits had read the operand)
-      if (ok && t + 1 < T) {
-        ok = warp_wait(&B.x_full, (t + 1) & 1, &B.ab, a.ctrl, 91, a.wait_ns);
-        if (ok) {
-          convert_row(op, rc);
-          fence_async_smem();
-          warp_arrive(&B.ax_full);
-        }
-      }
       // the inter-tile term has read S_prev and the state update has completed (both before p_full):
-      // snapshot the updated state for the next tile
+      // snapshot the updated state for the next tile.  Parts 0 / 1 take columns 0..31 and Z of state
+      // block 0 / 1, parts 2 / 3 columns 32..63.
       if (ok) {
         tc_fence_after();
-        if (rc.part < MB) {
-          const int comp = 128 * rc.part + rc.row;
-          uint32_t r[16];
-#pragma unroll
-          for (int c = 0; c < 5; ++c) {
-            tmem_ld16(tmem + rc.lane_base + kCColS + kStCols * rc.part + 16 * c, r);
-            tmem_ld_wait_tied16(r);
-            if (comp < a.Kp) snapshot_state_chunk(sbase + L.sbv, a.Kp, comp, c, r, a.eps);
+        const int mb = rc.part & 1;
+        if (mb < MB) {
+          const int comp = 128 * mb + rc.row;
+          const uint32_t ts = tmem + rc.lane_base + kCColS + kStCols * mb;
+          const int c0 = rc.part < 2 ? 0 : 2;
+          uint32_t ra[16], rb[16];
+          tmem_ld16(ts + 16 * c0, ra);
+          tmem_ld16(ts + 16 * c0 + 16, rb);
+          uint32_t z = rc.part < 2 ? tmem_ld1(ts + 64) : 0u;
+          tmem_ld_wait_tied16(ra);
+          tmem_ld_wait_tied16(rb);
+          tmem_ld_wait_tied1(z);
+          if (comp < a.Kp) {
+            snapshot_state_chunk(sbase + L.sbv, a.Kp, comp, c0, ra, a.eps);
+            snapshot_state_chunk(sbase + L.sbv, a.Kp, comp, c0 + 1, rb, a.eps);
+            if (rc.part < 2) snapshot_state_chunk(sbase + L.sbv, a.Kp, comp, 4, &z, a.eps);
           }
         }
         fence_async_smem();
