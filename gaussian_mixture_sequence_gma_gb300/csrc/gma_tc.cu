@@ -99,7 +99,7 @@ struct Bars {
 struct TcArgs {
   const uint8_t* w_img;  // [H][Kp * 256] swizzled fp16 B operand of the log-density contraction
   const float* cbias;    // [H][256] c'_k (log2 domain); -inf past K
-  float* state;          // [BH][Kp][80] (bidir) or [BH][splits][Kp][80] (causal aggregates)
+  float* state;          // [BH][Kp][80] (bidir) or [BH][splits][80][Kp] (causal aggregates, column-major)
   Ctrl* ctrl;
   void* out;             // read: O bf16 [BH][N][64]; responsibilities: gamma fp32 [BH][N][K]
   int H, N, K, Kp, tiles, seg_tiles, splits;
@@ -695,16 +695,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         for (int c = 0; c < 5; ++c) tmem_ld16(tmem + rc.lane_base + kColAcc + kStCols * rc.part + 16 * c, r + 16 * c);
         tmem_ld_wait();
         if (comp < a.Kp) {
-          float* dst = kAtomic ? a.state + ((size_t)bh * a.Kp + comp) * kStCols
-                               : a.state + (((size_t)bh * a.splits + split) * a.Kp + comp) * kStCols;
+          if (kAtomic) {  // state[bh][comp][80]
+            float4* dst = reinterpret_cast<float4*>(a.state + ((size_t)bh * a.Kp + comp) * kStCols);
 #pragma unroll
-          for (int c = 0; c < 20; ++c) {
-            const float4 f = make_float4(__uint_as_float(r[4 * c]), __uint_as_float(r[4 * c + 1]),
-                                         __uint_as_float(r[4 * c + 2]), __uint_as_float(r[4 * c + 3]));
-            if (kAtomic)
-              atomicAdd(reinterpret_cast<float4*>(dst) + c, f);
-            else
-              reinterpret_cast<float4*>(dst)[c] = f;
+            for (int c = 0; c < 20; ++c)
+              atomicAdd(dst + c, make_float4(__uint_as_float(r[4 * c]), __uint_as_float(r[4 * c + 1]),
+                                             __uint_as_float(r[4 * c + 2]), __uint_as_float(r[4 * c + 3])));
+          } else {  // segment aggregate, column-major agg[bh][split][80][Kp]: each store covers 32 components
+            float* dst = a.state + ((size_t)bh * a.splits + split) * kStCols * a.Kp + comp;
+#pragma unroll
+            for (int c = 0; c < kStCols; ++c) dst[(size_t)c * a.Kp] = __uint_as_float(r[c]);
           }
         }
       }
@@ -1194,12 +1194,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     // S <- exclusive prefix state of this segment; SB <- its bf16 copy (eps rides in the Z column)
     if (rc.part < MB) {
       const int comp = 128 * rc.part + rc.row;
-      const float* pre = a.state + (((size_t)bh * a.splits + seg) * a.Kp + comp) * kStCols;
+      // column-major [80][Kp]: each load of a warp covers 32 consecutive components
+      const float* pre = a.state + ((size_t)bh * a.splits + seg) * kStCols * a.Kp + comp;
       uint32_t r[16];
 #pragma unroll
       for (int c = 0; c < 5; ++c) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) r[i] = comp < a.Kp ? __float_as_uint(__ldg(pre + 16 * c + i)) : 0u;
+        for (int i = 0; i < 16; ++i)
+          r[i] = comp < a.Kp ? __float_as_uint(__ldg(pre + (size_t)(16 * c + i) * a.Kp)) : 0u;
         tmem_st16(tmem + rc.lane_base + kCColS + kStCols * rc.part + 16 * c, r);
         if (comp < a.Kp) snapshot_state_chunk(sbase + L.sbv, a.Kp, comp, c, r, a.eps);
       }
