@@ -796,20 +796,19 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     const uint32_t cs = sbase + L.c;
     const uint32_t ga = gamma_row_addr<NC>(sbase + L.g, rc);
     zero_unused_logits<NC>(tmem, rc, a.Kp);
-    const int rt = threadIdx.x - 32 * kRowWarp0;  // 0..255
     bool ok = true;
     if (kRead) {
-      // state [Kp][80] fp32 -> bf16 K-major operand SB[n][comp]
-      if (rt < a.Kp) {
-        const float4* src = reinterpret_cast<const float4*>(a.state + ((size_t)bh * a.Kp + rt) * kStCols);
-#pragma unroll 4
-        for (int c = 0; c < 20; ++c) {
-          const float4 f = __ldg(src + c);
-          // column kDv holds Z; eps is folded in once here so gamma~ . (Z + eps) is one contraction column
-          const float e[4] = {c == kDv / 4 ? f.x + a.eps : f.x, f.y, f.z, f.w};
+      // state [Kp][80] fp32 -> bf16 K-major operand SB[n][comp]; the 512 row threads read it as
+      // consecutive float4 (column kDv holds Z; eps is folded in once here so gamma~ . (Z + eps) is one
+      // contraction column)
+      const float4* src = reinterpret_cast<const float4*>(a.state + (size_t)bh * a.Kp * kStCols);
+      const int nq = a.Kp * (kStCols / 4);
+      for (int i = threadIdx.x - 32 * kRowWarp0; i < nq; i += 32 * (kThreadsTc / 32 - kRowWarp0)) {
+        const float4 f = __ldg(src + i);
+        const int comp = i / (kStCols / 4), c = i - comp * (kStCols / 4);
+        const float e[4] = {c == kDv / 4 ? f.x + a.eps : f.x, f.y, f.z, f.w};
 #pragma unroll
-          for (int i = 0; i < 4; ++i) sts16(sbase + L.sb + sw128_off(4 * c + i, rt, kStCols * 128), bf16_bits(e[i]));
-        }
+        for (int j = 0; j < 4; ++j) sts16(sbase + L.sb + sw128_off(4 * c + j, comp, kStCols * 128), bf16_bits(e[j]));
       }
       fence_async_smem();
       warp_arrive(&B.sb_full);
