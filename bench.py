@@ -438,6 +438,34 @@ def run_gma(args, world, rank, local):
             "hbm_bound_us": t_hbm * 1e6, "frac_of_hbm_bound": t_hbm / t_step,
             "launches_per_step": 1, "timing": how}
         del di, state, wsd, toks, outd
+        # Transformer-block form at the language-model block shape: projection GEMM + layout + causal forward
+        from gaussian_mixture_sequence_gma_gb300.inputs import make_projected_inputs
+        Bp, Hp, Np, Kp_, dmp = 8, 12, 2048, 256, 768
+        pi_ = make_projected_inputs(Bp, Hp, Np, Kp_, dm=dmp, dtype="bf16", seed=3)
+        tp = {k: torch.from_numpy(np.ascontiguousarray(pi_[k])).to(dev) for k in ("mu", "sigma2", "log_pi", "bqkv")}
+        for k in ("X", "Wqkv"):
+            tp[k] = torch.from_numpy(bf16_bits(pi_[k]).view(np.int16)).to(dev).view(torch.bfloat16)
+        pp_ = gma.problem(Bp, Hp, Np, Kp_, torch.bfloat16, 1e-6)
+        wsp = gma.alloc_workspace(pp_, gma.OP_PROJECTED_CAUSAL, dev)
+        outp = torch.empty((Bp, Hp, Np, 64), dtype=torch.bfloat16, device=dev)
+        callp = lambda: gma.forward_projected(tp["X"], tp["Wqkv"], tp["bqkv"], tp["mu"], tp["sigma2"], tp["log_pi"],
+                                              causal=True, out=outp, workspace=wsp)
+        qkv = [torch.empty((Bp, Hp, Np, 64), dtype=torch.bfloat16, device=dev) for _ in range(3)]
+        callu = lambda: gma.forward_causal(qkv[0], qkv[1], qkv[2], tp["mu"], tp["sigma2"], tp["log_pi"], 1e-6)
+        for _ in range(3):
+            callp()
+            callu()
+        mp, _ = timed(callp, 10)
+        mu_, _ = timed(callu, 10)
+        t_p = mp / 10 * 1e-3
+        gemm_flop = 2.0 * Bp * Np * dmp * 3 * Hp * 64
+        gma_flop = flop_per_tokhead(Kp_) * Bp * Hp * Np
+        extensions["projected_causal_bf16_B8H12N2048K256_dm768"] = {
+            "ms": t_p * 1e3, "tok_heads_per_s": Bp * Hp * Np / t_p, "forward_only_ms": mu_ / 10,
+            "projection_ms": t_p * 1e3 - mu_ / 10, "tflops_algorithmic": (gemm_flop + gma_flop) / t_p / 1e12,
+            "frac_of_bf16_peak": (gemm_flop + gma_flop) / t_p / 1e12 / peaks["bf16"],
+            "note": "projection = one cuBLASLt GEMM (float32 out) + one layout kernel; Q, K, V round-trip HBM"}
+        del tp, wsp, outp, qkv
         # backward pass of the bidirectional form (float32 CUDA-core kernels) on the bidir bf16 workload shape
         wb = workloads()["bidir_bf16_B4H8N4096K128"]
         bi = to_dev(make_workload(wb), dev)

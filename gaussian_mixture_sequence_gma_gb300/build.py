@@ -68,7 +68,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
         # shared cudart: the library joins the CUDA runtime the host process (e.g. torch) already uses,
         # so the current device and stream handles are the same on both sides of the ABI
         cmd = [nvcc()] + ARCH + ["-shared", "-cudart", "shared", "-Xlinker", "-rpath=/usr/local/cuda/lib64",
-                                 "-o", tmp] + objs
+                                 "-o", tmp] + objs + ["-lcublasLt"]
         subprocess.run(cmd, check=True)
         os.replace(tmp, LIB)
     return LIB

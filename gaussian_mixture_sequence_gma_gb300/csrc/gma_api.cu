@@ -64,12 +64,34 @@ gma_status_t validate_problem(const gma_problem_t* p) {
   return GMA_OK;
 }
 
+// Projected forward: [the forward's own workspace | GEMM workspace | Y float32 [B*N][3*H*64] | Q | K | V].
+struct ProjLayout {
+  size_t base, lt, y, q, k, v, total;
+};
+ProjLayout proj_layout(const gma_problem_t& p, bool causal);
+
 size_t required_bytes(const gma_problem_t& p, gma_op_t op) {
+  if (op == GMA_OP_PROJECTED_BIDIR || op == GMA_OP_PROJECTED_CAUSAL)
+    return proj_layout(p, op == GMA_OP_PROJECTED_CAUSAL).total;
   if (op == GMA_OP_CROSS) op = GMA_OP_BIDIR;  // the same workspace: it does not depend on N
   if (op == GMA_OP_CAUSAL_DECODE) return align_up(sizeof(Ctrl));  // a control block; the kernel needs no scratch
   if (op == GMA_OP_BACKWARD_BIDIR || op == GMA_OP_BACKWARD_CAUSAL) return simt_backward_bytes(p, op == GMA_OP_BACKWARD_CAUSAL);
   if (p.dtype == GMA_BF16) return tc_plan(p, op).total;
   return simt_plan(p, op).total;
+}
+
+ProjLayout proj_layout(const gma_problem_t& p, bool causal) {
+  ProjLayout L{};
+  const size_t es = p.dtype == GMA_BF16 ? 2 : 4;
+  const size_t qkv = align_up((size_t)p.B * p.H * p.N * kD * es);
+  L.base = align_up(required_bytes(p, causal ? GMA_OP_CAUSAL : GMA_OP_BIDIR));
+  L.lt = L.base;
+  L.y = L.lt + align_up(proj_lt_workspace_bytes());
+  L.q = L.y + align_up((size_t)p.B * p.N * 3 * p.H * kD * sizeof(float));
+  L.k = L.q + qkv;
+  L.v = L.k + qkv;
+  L.total = L.v + qkv;
+  return L;
 }
 
 // Nk: keys / values per (b, h); N (= p->N) except for cross-attention.
@@ -137,8 +159,35 @@ extern "C" {
 
 size_t gma_workspace_bytes(const gma_problem_t* p, gma_op_t op) {
   if (validate_problem(p) != GMA_OK) return 0;
-  if (op < GMA_OP_RESPONSIBILITIES || op > GMA_OP_BACKWARD_CAUSAL) return 0;
+  if (op < GMA_OP_RESPONSIBILITIES || op > GMA_OP_PROJECTED_CAUSAL) return 0;
   return required_bytes(*p, op);
+}
+
+gma_status_t gma_forward_projected(const gma_problem_t* p, int causal, int dm, const void* X, const void* Wqkv,
+                                   const float* bqkv, const float* mu, const float* sigma2, const float* log_pi,
+                                   void* O, void* ws, size_t ws_bytes, void* stream) {
+  gma_status_t s = validate_problem(p);
+  if (s != GMA_OK) return s;
+  if (causal != 0 && causal != 1) return GMA_ERR_INVALID_ARG;
+  if (dm < 8 || dm % 8 != 0 || dm > (1 << 16)) return GMA_ERR_UNSUPPORTED;
+  if (!mu || !sigma2 || !log_pi || !ws || !Wqkv || !bqkv) return GMA_ERR_INVALID_ARG;
+  if (p->N > 0 && (!X || !O)) return GMA_ERR_INVALID_ARG;
+  if (O && (O == X || O == Wqkv || O == (const void*)bqkv)) return GMA_ERR_INVALID_ARG;
+  const void* ptrs[] = {X, Wqkv, bqkv, mu, sigma2, log_pi, O};
+  for (const void* q : ptrs)
+    if (q && !aligned(q, 16)) return GMA_ERR_INVALID_ARG;
+  if (!aligned(ws, kAlign)) return GMA_ERR_INVALID_ARG;
+  const gma_op_t op = causal ? GMA_OP_PROJECTED_CAUSAL : GMA_OP_PROJECTED_BIDIR;
+  if (ws_bytes < required_bytes(*p, op)) return GMA_ERR_WORKSPACE;
+  if (p->N == 0) return GMA_OK;
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaGetLastError();
+  const ProjLayout L = proj_layout(*p, causal != 0);
+  char* w = (char*)ws;
+  s = proj_run(*p, dm, X, Wqkv, bqkv, (float*)(w + L.y), w + L.q, w + L.k, w + L.v, w + L.lt, st);
+  if (s != GMA_OK) return s;
+  return run(p, causal ? GMA_OP_CAUSAL : GMA_OP_BIDIR, p->N, w + L.q, w + L.k, w + L.v, mu, sigma2, log_pi, O, ws,
+             L.base, stream);
 }
 
 gma_status_t gma_responsibilities(const gma_problem_t* p, const void* X, const float* mu, const float* sigma2,

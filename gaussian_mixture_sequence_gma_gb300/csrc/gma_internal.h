@@ -69,6 +69,11 @@ gma_status_t simt_backward(const gma_problem_t& p, bool causal, const void* Q, c
 gma_status_t simt_decode(const gma_problem_t& p, const void* Q, const void* K, const void* V, const float* mu,
                          const float* sigma2, const float* log_pi, float* state, void* out, void* ws,
                          cudaStream_t stream);
+// Q / K / V projection of a Transformer block: Y = X Wqkv (library GEMM, float32) into Y, then the bias
+// and the [B][H][N][64] layout of the I/O dtype into Q, K, V.  lt_ws: proj_lt_workspace_bytes() bytes.
+size_t proj_lt_workspace_bytes();
+gma_status_t proj_run(const gma_problem_t& p, int dm, const void* X, const void* W, const float* bias, float* Y,
+                      void* Q, void* K, void* V, void* lt_ws, cudaStream_t st);
 // Test hook: bit 0 makes the next bidirectional write launch skip its first X-tile load, so that a
 // bounded device wait runs out and reports GMA_ERR_TIMEOUT.
 void tc_set_fault_injection(uint32_t mask);

@@ -17,9 +17,10 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "li
 GMA_OK, GMA_ERR_INVALID_ARG, GMA_ERR_UNSUPPORTED, GMA_ERR_WORKSPACE, GMA_ERR_CUDA, GMA_ERR_TIMEOUT = range(6)
 GMA_F32, GMA_BF16 = 0, 1
 (OP_RESPONSIBILITIES, OP_BIDIR, OP_CAUSAL, OP_CROSS, OP_CAUSAL_STATE, OP_CAUSAL_DECODE, OP_BACKWARD_BIDIR,
- OP_BACKWARD_CAUSAL) = range(8)
+ OP_BACKWARD_CAUSAL, OP_PROJECTED_BIDIR, OP_PROJECTED_CAUSAL) = range(10)
 
 EXPORTED = ("gma_workspace_bytes", "gma_responsibilities", "gma_forward_bidir", "gma_forward_causal", "gma_forward_cross", "gma_state_bytes", "gma_causal_state", "gma_causal_decode", "gma_backward_bidir", "gma_backward_causal",
+            "gma_forward_projected",
             "gma_check_device_error", "gma_status_string", "gma_version", "gma_last_error", "gma_launch_count", "gma_profile_enable",
             "gma_profile_read", "gma_forward_bidir_static_ws", "gma_static_ws_capacity",
             "gma_debug_withhold_first_load", "gma_probe_ex2_rate")
@@ -80,6 +81,8 @@ def lib():
     L.gma_backward_bidir.restype = ctypes.c_int
     L.gma_backward_causal.argtypes = L.gma_backward_bidir.argtypes
     L.gma_backward_causal.restype = ctypes.c_int
+    L.gma_forward_projected.argtypes = [pp, ctypes.c_int, ctypes.c_int, vp, vp, fp, fp, fp, fp, vp, vp, sz, vp]
+    L.gma_forward_projected.restype = ctypes.c_int
     L.gma_check_device_error.argtypes = [vp, vp]
     L.gma_check_device_error.restype = ctypes.c_int
     L.gma_status_string.argtypes = [ctypes.c_int]
@@ -242,6 +245,34 @@ def forward_cross(Q, K, V, mu, sigma2, log_pi, eps=1e-6, out=None, workspace=Non
                                     _stream_handle(stream, dev))
     if s != GMA_OK:
         raise GmaError(s, "gma_forward_cross")
+    return out
+
+
+def forward_projected(X, Wqkv, bqkv, mu, sigma2, log_pi, causal, eps=1e-6, out=None, workspace=None, stream=None):
+    """Transformer-block form: Q, K, V = split_heads(X Wqkv + bqkv) then the GMA forward.  X [B,N,dm] and
+    Wqkv [dm, 3*H*64] in the I/O dtype (column blocks Q | K | V, head h = columns 64h..64h+63 of a
+    block), bqkv [3*H*64] float32; O [B,H,N,64] in the I/O dtype."""
+    B, N, dm = X.shape
+    Kc = mu.shape[1]
+    H = mu.shape[0]
+    _params(mu, sigma2, log_pi)
+    dev = _check_cuda(X, Wqkv, bqkv, mu, sigma2, log_pi)
+    if Wqkv.dtype != X.dtype or bqkv.dtype != torch.float32:
+        raise TypeError("Wqkv must have X's dtype and bqkv must be float32")
+    if tuple(Wqkv.shape) != (dm, 3 * H * 64) or tuple(bqkv.shape) != (3 * H * 64,):
+        raise ValueError("Wqkv must be [dm, 3*H*64] and bqkv [3*H*64] (H from mu)")
+    prob = problem(B, H, N, Kc, X.dtype, eps)
+    op = OP_PROJECTED_CAUSAL if causal else OP_PROJECTED_BIDIR
+    if out is None:
+        out = torch.empty((B, H, N, 64), dtype=X.dtype, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(prob, op, dev)
+    with torch.cuda.device(dev):
+        s = lib().gma_forward_projected(ctypes.byref(prob), 1 if causal else 0, int(dm), _ptr(X), _ptr(Wqkv),
+                                        _ptr(bqkv), _ptr(mu), _ptr(sigma2), _ptr(log_pi), _ptr(out),
+                                        _ptr(workspace), workspace.numel(), _stream_handle(stream, dev))
+    if s != GMA_OK:
+        raise GmaError(s, "gma_forward_projected")
     return out
 
 

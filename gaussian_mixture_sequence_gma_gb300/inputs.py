@@ -127,6 +127,25 @@ def make_inputs(B: int, H: int, N: int, K: int, d: int = 64, dv: int = 64, dtype
     return dict(Q=Q, K=Kx, V=V, mu=mu, sigma2=sigma2, log_pi=log_pi, dtype=dtype)
 
 
+def make_projected_inputs(B: int, H: int, N: int, K: int, dm: int | None = None, dtype: str = "bf16", seed: int = 0,
+                          sigma_raw_std: float = 0.5) -> dict:
+    """Seeded Transformer-block problem: block input X [B,N,dm] ~ N(0,1) and one [dm, 3*H*64] weight
+    (column blocks Q | K | V) with a [3*H*64] bias, both U(-1/sqrt(dm), 1/sqrt(dm)) like a default
+    linear-layer init, plus the mixture parameters.  X and Wqkv are bf16-exact for dtype 'bf16'."""
+    dm = dm or H * 64
+    rng = np.random.Generator(np.random.PCG64(seed))
+    mu, sigma2, log_pi = make_params(rng, H, K, 64, sigma_raw_std)
+    X = rng.standard_normal((B, N, dm), dtype=np.float32)
+    bound = np.float32(1.0 / np.sqrt(dm))
+    Wqkv = rng.uniform(-bound, bound, size=(dm, 3 * H * 64)).astype(np.float32)
+    bqkv = rng.uniform(-bound, bound, size=(3 * H * 64,)).astype(np.float32)
+    if dtype == "bf16":
+        X, Wqkv = round_bf16(X), round_bf16(Wqkv)
+    elif dtype != "f32":
+        raise ValueError(dtype)
+    return dict(X=X, Wqkv=Wqkv, bqkv=bqkv, mu=mu, sigma2=sigma2, log_pi=log_pi, dtype=dtype)
+
+
 def make_cross_inputs(B: int, H: int, N: int, Nk: int, K: int, dtype: str = "bf16", seed: int = 0,
                       sigma_raw_std: float = 1.0) -> dict:
     """Seeded cross-attention problem: N queries, Nk keys / values, one shared set of parameters.

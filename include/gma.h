@@ -75,7 +75,9 @@ typedef enum {
   GMA_OP_CAUSAL_STATE = 4,
   GMA_OP_CAUSAL_DECODE = 5,
   GMA_OP_BACKWARD_BIDIR = 6,
-  GMA_OP_BACKWARD_CAUSAL = 7
+  GMA_OP_BACKWARD_CAUSAL = 7,
+  GMA_OP_PROJECTED_BIDIR = 8,
+  GMA_OP_PROJECTED_CAUSAL = 9
 } gma_op_t;
 
 typedef struct {
@@ -235,6 +237,29 @@ GMA_API gma_status_t gma_backward_causal(const gma_problem_t *p, const void *Q, 
                                          const float *mu, const float *sigma2, const float *log_pi, const void *dO,
                                          void *dQ, void *dK, void *dV, float *dmu, float *dsigma2, float *dlog_pi,
                                          void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Forward pass of a Transformer block's attention with GMA in place of softmax attention, from the
+ * block input: Q, K, V are the linear projections of X (with bias), split into H heads of 64, then
+ * the bidirectional (causal = 0) or causal (causal = 1) forward above runs on them.
+ * Passage: gist.science summary, "Variants and training" (GMA as the sequence mixer of a
+ * Transformer language model; the experiments' model has d_model = 768 and 12 heads).
+ *   X     [B, N, dm] in p->dtype, dm a multiple of 8 (GMA_ERR_UNSUPPORTED otherwise)
+ *   Wqkv  [dm, 3 * H * 64] in p->dtype: columns 0 .. H*64-1 give Q (head h = columns 64h .. 64h+63),
+ *         the next H*64 give K, the last H*64 give V
+ *   bqkv  [3 * H * 64] float32 bias, same column order
+ *   O     [B, H, N, 64] in p->dtype (written)
+ * The projection is one library GEMM (cuBLASLt, float32 accumulation and output) followed by one
+ * kernel that adds the bias, rounds once to p->dtype and writes Q, K, V in the [B, H, N, 64] layout
+ * inside the workspace; Q, K, V make one round trip through HBM (the forward kernels hold no room
+ * for the 3 x dm-wide weight slices).  Workspace: gma_workspace_bytes(p, GMA_OP_PROJECTED_BIDIR or
+ * GMA_OP_PROJECTED_CAUSAL); its first part is the forward's own workspace, so
+ * gma_check_device_error(ws, ...) applies unchanged.
+ */
+GMA_API gma_status_t gma_forward_projected(const gma_problem_t *p, int causal, int dm, const void *X,
+                                           const void *Wqkv, const float *bqkv, const float *mu,
+                                           const float *sigma2, const float *log_pi, void *O, void *ws,
+                                           size_t ws_bytes, void *stream);
 
 /*
  * Synchronises `stream`, then reads the error word kept at the start of `ws`:

@@ -16,6 +16,10 @@ item 3; fugumt.com English abstract):
 * ``forward_cross``: the bidirectional form with N queries reading the memory
   written by Nk keys / values (gist.science summary, "Significance and claims",
   closing paragraph: cross-attention applications named as future work).
+* ``forward_projected``: the Transformer-block form ("Variants and training":
+  GMA as the sequence mixer of a Transformer language model): Q, K, V are the
+  biased linear projections of the block input X, split into heads of 64,
+  rounded to the I/O precision, then ``forward``.
 * ``state``: Vt and Z alone.
 * ``backward_bidir`` / ``backward_causal``: gradients of the bidirectional /
   causal forward with respect to Q, K, V, mu, sigma2 and log pi given dL/dO
@@ -191,3 +195,31 @@ def backward_bidir(Q, Kx, V, mu, sigma2, log_pi, eps, dO, lib=None, causal=False
 def backward_causal(Q, Kx, V, mu, sigma2, log_pi, eps, dO, lib=None):
     """(dQ, dK, dV, dmu, dsigma2, dlog_pi) of the causal forward given dO [B,H,N,dv]."""
     return backward_bidir(Q, Kx, V, mu, sigma2, log_pi, eps, dO, lib=lib, causal=True)
+
+
+def round_to_bf16(a) -> np.ndarray:
+    """Nearest bfloat16 value of each element (ties to even), as float64.  The projection's output is
+    rounded to the I/O precision before the forward, as a model in that precision stores it."""
+    f = np.ascontiguousarray(np.asarray(a, dtype=np.float64).astype(np.float32))
+    u = f.view(np.uint32).astype(np.uint64)
+    u = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16
+    return u.astype(np.uint32).view(np.float32).astype(np.float64).reshape(f.shape)
+
+
+def project_qkv(X, Wqkv, bqkv, H, dtype):
+    """Q, K, V [B,H,N,64] from X [B,N,dm]: Y = X Wqkv + bqkv in float64 (Wqkv [dm, 3*H*64], column
+    blocks Q | K | V, head h = columns 64h .. 64h+63 of a block), rounded to bf16 for dtype 'bf16'."""
+    X = _f64(X)
+    B, N, dm = X.shape
+    Y = X.reshape(B * N, dm) @ _f64(Wqkv) + _f64(bqkv)[None, :]
+    if dtype == "bf16":
+        Y = round_to_bf16(Y)
+    Y = Y.reshape(B, N, 3, H, 64)
+    return tuple(np.ascontiguousarray(Y[:, :, w].transpose(0, 2, 1, 3)) for w in range(3))
+
+
+def forward_projected(X, Wqkv, bqkv, mu, sigma2, log_pi, eps, causal=False, dtype="bf16", rows=None, nthreads=None,
+                      lib=None):
+    H = np.asarray(mu).shape[0]
+    Q, Kx, V = project_qkv(X, Wqkv, bqkv, H, dtype)
+    return forward(Q, Kx, V, mu, sigma2, log_pi, eps, causal=causal, rows=rows, nthreads=nthreads, lib=lib)

@@ -60,7 +60,7 @@ def test_workspace_bytes(L):
     assert gma.workspace_bytes(P(K=257), gma.OP_BIDIR) == 0
     assert gma.workspace_bytes(P(B=0), gma.OP_BIDIR) == 0
     assert gma.workspace_bytes(P(dtype=7), gma.OP_BIDIR) == 0
-    assert gma.workspace_bytes(P(), 9) == 0
+    assert gma.workspace_bytes(P(), 10) == 0
     # workspace does not grow with N for the bidirectional write state beyond the fixed split
     assert gma.workspace_bytes(P(N=1 << 20), gma.OP_BIDIR) == gma.workspace_bytes(P(N=1 << 16), gma.OP_BIDIR)
 
@@ -153,7 +153,7 @@ def test_state_and_decode_argument_errors(L):
         for dt in (gma.GMA_F32, gma.GMA_BF16):
             n = gma.workspace_bytes(P(dtype=dt), op)
             assert n > 0 and n % 256 == 0
-    assert gma.workspace_bytes(P(), 8) == 0
+    assert gma.workspace_bytes(P(), 10) == 0
     ptr = [A + i * (1 << 16) for i in range(10)]
 
     def st(prob, p=ptr, ws_bytes=1 << 30):  # K, V, mu, sigma2, log_pi, state, ws
@@ -232,3 +232,34 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(gma, "_LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         gma.lib()
+
+
+def test_projected_argument_errors(L):
+    for dt in (gma.GMA_F32, gma.GMA_BF16):
+        for op, base in ((gma.OP_PROJECTED_BIDIR, gma.OP_BIDIR), (gma.OP_PROJECTED_CAUSAL, gma.OP_CAUSAL)):
+            n = gma.workspace_bytes(P(dtype=dt), op)
+            # the forward's own workspace, the GEMM's, Y float32 [B*N][3*H*64] and Q, K, V
+            assert n % 256 == 0 and n > gma.workspace_bytes(P(dtype=dt), base) + 32 * (1 << 20) + 256 * 384 * 4
+    ptr = [A + i * (1 << 16) for i in range(10)]
+
+    def proj(prob, causal=1, dm=128, p=ptr, ws_bytes=1 << 34):  # X W b mu s2 lp O ws
+        return L.gma_forward_projected(ctypes.byref(prob), causal, dm, p[0], p[1], p[2], p[3], p[4], p[5], p[6],
+                                       p[7], ws_bytes, None)
+
+    assert proj(P(d=32)) == gma.GMA_ERR_UNSUPPORTED
+    assert proj(P(), causal=2) == gma.GMA_ERR_INVALID_ARG
+    for dm in (0, 4, 100):
+        assert proj(P(), dm=dm) == gma.GMA_ERR_UNSUPPORTED
+    for i in range(8):
+        bad = list(ptr); bad[i] = None
+        assert proj(P(), p=bad) == gma.GMA_ERR_INVALID_ARG
+    for i in range(7):
+        bad = list(ptr); bad[i] += 4
+        assert proj(P(), p=bad) == gma.GMA_ERR_INVALID_ARG
+    for i in (0, 1, 2):  # output aliasing an input
+        bad = list(ptr); bad[6] = bad[i]
+        assert proj(P(), p=bad) == gma.GMA_ERR_INVALID_ARG
+    need = gma.workspace_bytes(P(), gma.OP_PROJECTED_CAUSAL)
+    assert proj(P(), ws_bytes=need - 1) == gma.GMA_ERR_WORKSPACE
+    nul = [None, ptr[1], ptr[2], ptr[3], ptr[4], ptr[5], None, ptr[7]]
+    assert proj(P(N=0), p=nul, ws_bytes=gma.workspace_bytes(P(N=0), gma.OP_PROJECTED_CAUSAL)) == gma.GMA_OK

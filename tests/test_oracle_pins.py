@@ -468,3 +468,55 @@ def test_pins_catch_planted_mistake(name, tmp_path):
     p.write_text(mutated)
     so = orc.build(force=True, src=str(p), out=str(tmp_path / "libmutant.so"))
     assert not _pins_pass(orc._load(so)), "pins missed mutant %s" % name
+
+
+# ----------------------------------------------------------------------------- projected (Transformer block)
+
+def test_round_to_bf16_matches_torch():
+    # pinned to an independent implementation of round-to-nearest-even bfloat16 (torch's conversion)
+    torch = pytest.importorskip("torch")
+    r = np.random.Generator(np.random.PCG64(3))
+    x = np.concatenate([r.standard_normal(4096) * 10.0 ** r.integers(-6, 6, 4096),
+                        [1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, -1.0 - 2.0 ** -8, 0.0, 65504.0]])
+    ours = orc.round_to_bf16(x)
+    theirs = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(ours, theirs)
+    assert orc.round_to_bf16(np.array([1.0 + 2.0 ** -8]))[0] == 1.0  # a tie goes to the even neighbour
+
+
+def test_projection_brute_force():
+    r = np.random.Generator(np.random.PCG64(4))
+    B, N, H, dm = 2, 3, 2, 5
+    X = r.standard_normal((B, N, dm))
+    W = r.standard_normal((dm, 3 * H * 64))
+    b = r.standard_normal(3 * H * 64)
+    Q, Kx, V = orc.project_qkv(X, W, b, H, "f32")
+    for w, T in enumerate((Q, Kx, V)):
+        for bb in range(B):
+            for h in range(H):
+                for n in range(N):
+                    for dd in (0, 17, 63):
+                        c = (w * H + h) * 64 + dd
+                        want = sum(X[bb, n, m] * W[m, c] for m in range(dm)) + b[c]
+                        assert abs(T[bb, h, n, dd] - want) < 1e-12
+
+
+def test_projected_identity_weights_reduce_to_forward():
+    r = np.random.Generator(np.random.PCG64(5))
+    B, H, N, K = 1, 2, 40, 6
+    X = r.standard_normal((B, N, H * 64))
+    W = np.concatenate([np.eye(H * 64)] * 3, axis=1)
+    mu = r.standard_normal((H, K, 64))
+    sigma2 = 0.5 + r.random((H, K, 64))
+    log_pi = np.log(np.full((H, K), 1.0 / K))
+    Xh = np.ascontiguousarray(X.reshape(B, N, H, 64).transpose(0, 2, 1, 3))
+    for causal in (False, True):
+        got = orc.forward_projected(X, W, np.zeros(3 * H * 64), mu, sigma2, log_pi, 1e-6, causal=causal, dtype="f32")
+        want = orc.forward(Xh, Xh, Xh, mu, sigma2, log_pi, 1e-6, causal=causal)
+        assert np.allclose(got, want, rtol=0, atol=1e-12)
+    # a transposed weight is a different projection (the identity above would not notice it)
+    W2 = r.standard_normal((H * 64, 3 * H * 64)) / 8
+    a = orc.forward_projected(X, W2, np.zeros(3 * H * 64), mu, sigma2, log_pi, 1e-6, dtype="f32")
+    Wt = np.concatenate([W2[:, w * H * 64:(w + 1) * H * 64].T for w in range(3)], axis=1)
+    b = orc.forward_projected(X, Wt, np.zeros(3 * H * 64), mu, sigma2, log_pi, 1e-6, dtype="f32")
+    assert np.abs(a - b).max() > 1e-3
