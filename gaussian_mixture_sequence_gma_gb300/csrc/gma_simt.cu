@@ -868,9 +868,21 @@ __global__ void __launch_bounds__(kDecodeThreads) simt_decode_kernel(const IO* _
   // many loads are in flight per thread; plain floats otherwise
   const bool vec = ((reinterpret_cast<uintptr_t>(st) | reinterpret_cast<uintptr_t>(S)) & 15) == 0 && (n_state & 3) == 0;
   if (vec) {
-#pragma unroll 4
-    for (int i = threadIdx.x; i < n_state / 4; i += blockDim.x)
-      reinterpret_cast<float4*>(S)[i] = __ldcg(reinterpret_cast<const float4*>(st) + i);
+    // all of a thread's loads in flight before the first store (one round trip to memory)
+    const int n4s = n_state / 4;
+    for (int i0 = threadIdx.x; i0 < n4s; i0 += 16 * kDecodeThreads) {
+      float4 x[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int i = i0 + u * kDecodeThreads;
+        if (i < n4s) x[u] = __ldcg(reinterpret_cast<const float4*>(st) + i);
+      }
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int i = i0 + u * kDecodeThreads;
+        if (i < n4s) reinterpret_cast<float4*>(S)[i] = x[u];
+      }
+    }
   } else {
 #pragma unroll 8
     for (int i = threadIdx.x; i < n_state; i += blockDim.x) S[i] = __ldcg(st + i);
@@ -880,27 +892,42 @@ __global__ void __launch_bounds__(kDecodeThreads) simt_decode_kernel(const IO* _
   // aligned half-warp) add their log-variances with shuffles.  The trip count is warp-uniform.
   const float4* mu4 = reinterpret_cast<const float4*>(mu + (size_t)h * K * kD);
   const float4* s24 = reinterpret_cast<const float4*>(sigma2 + (size_t)h * K * kD);
-  const int n4 = K * (kD / 4), base = threadIdx.x & ~31;
-  for (int i0 = base; i0 < n4; i0 += blockDim.x) {
-    const int i4 = i0 + (threadIdx.x & 31);
-    const bool on = i4 < n4;  // whole aligned groups of 16 (n4 is a multiple of 16)
-    const int kk = i4 >> 4, j0 = (i4 & 15) << 2;
-    float lg = 0.f;
-    if (on) {
-      const float4 m = __ldg(mu4 + i4), v = __ldg(s24 + i4);
-      mu_s[(size_t)(j0 + 0) * ld + kk] = m.x;
-      mu_s[(size_t)(j0 + 1) * ld + kk] = m.y;
-      mu_s[(size_t)(j0 + 2) * ld + kk] = m.z;
-      mu_s[(size_t)(j0 + 3) * ld + kk] = m.w;
-      w_s[(size_t)(j0 + 0) * ld + kk] = 1.0f / v.x;
-      w_s[(size_t)(j0 + 1) * ld + kk] = 1.0f / v.y;
-      w_s[(size_t)(j0 + 2) * ld + kk] = 1.0f / v.z;
-      w_s[(size_t)(j0 + 3) * ld + kk] = 1.0f / v.w;
-      lg = (logf(v.x) + logf(v.y)) + (logf(v.z) + logf(v.w));
+  const int n4 = K * (kD / 4);
+  // eight float4 of each table in flight per thread; the trip count and the 16-thread component groups
+  // (aligned half-warps: n4 and the block size are multiples of 16) are warp-uniform
+  for (int i0 = threadIdx.x; i0 - (int)threadIdx.x < n4; i0 += 8 * kDecodeThreads) {
+    float4 m[8], v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i4 = i0 + u * kDecodeThreads;
+      if (i4 < n4) {
+        m[u] = __ldg(mu4 + i4);
+        v[u] = __ldg(s24 + i4);
+      }
     }
 #pragma unroll
-    for (int o = 8; o > 0; o >>= 1) lg += __shfl_xor_sync(0xffffffffu, lg, o);
-    if (on && (i4 & 15) == 0) c_s[kk] = __ldg(log_pi + (size_t)h * K + kk) - 0.5f * lg;
+    for (int u = 0; u < 8; ++u) {
+      const int i4 = i0 + u * kDecodeThreads;
+      const bool on = i4 < n4;
+      const int kk = i4 >> 4, j0 = (i4 & 15) << 2;
+      float lg = 0.f;
+      if (on) {
+        mu_s[(size_t)(j0 + 0) * ld + kk] = m[u].x;
+        mu_s[(size_t)(j0 + 1) * ld + kk] = m[u].y;
+        mu_s[(size_t)(j0 + 2) * ld + kk] = m[u].z;
+        mu_s[(size_t)(j0 + 3) * ld + kk] = m[u].w;
+        w_s[(size_t)(j0 + 0) * ld + kk] = 1.0f / v[u].x;
+        w_s[(size_t)(j0 + 1) * ld + kk] = 1.0f / v[u].y;
+        w_s[(size_t)(j0 + 2) * ld + kk] = 1.0f / v[u].z;
+        w_s[(size_t)(j0 + 3) * ld + kk] = 1.0f / v[u].w;
+        lg = (logf(v[u].x) + logf(v[u].y)) + (logf(v[u].z) + logf(v[u].w));
+      }
+      if (i0 - (int)threadIdx.x + u * kDecodeThreads < n4) {  // warp-uniform: the whole warp is on or off
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) lg += __shfl_xor_sync(0xffffffffu, lg, o);
+      }
+      if (on && (i4 & 15) == 0) c_s[kk] = __ldg(log_pi + (size_t)h * K + kk) - 0.5f * lg;
+    }
   }
   __syncthreads();
   for (int t = 0; t < Tn; ++t) {
