@@ -9,8 +9,10 @@
 //     added in float32, followed by a base-2 softmax over k held in registers.
 //   "Core mechanism" item 2: write  [Vt | Z] = Gamma_K^T [V | 1]   (bf16 operands, fp32 TMEM accumulator)
 //                            read   O = Gamma_Q Vt / (Gamma_Q Z + eps)
-//   Gamma_K is stored unnormalised (row maximum 1) and each key's row is normalised inside the
-//   contraction by scaling its [V | 1] row by 1/s_j (s_j = row sum of the exponentials).  Gamma_Q stays
+//   Bidirectional write: Gamma_K is stored unnormalised (row maximum 1) and each key's row is normalised
+//   inside the contraction by scaling its [V | 1] row by 1/s_j (s_j = row sum of the exponentials);
+//   causal aggregates: the bf16 Gamma_K rows are scaled by 1/s_j themselves and kept in HBM for the
+//   chunked sweep, which uses them with V as loaded and a constant 1 column.  Gamma_Q stays
 //   unnormalised as well: the read divides by gamma~_i . (Z + eps) = gamma~_i . Z + eps s_i, which is the
 //   same quotient, with eps added once to the Z column of the state operand, so no query row needs
 //   its sum.
@@ -397,20 +399,6 @@ __device__ __forceinline__ void scale_v_row(uint32_t vtile, const RowCtx& rc, fl
   }
 }
 
-// The same for a V tile in the 32-byte swizzle: this thread's 16 dims are atom `part` (4 KB apart).
-__device__ __forceinline__ void scale_v_row32(uint32_t vtile, const RowCtx& rc, float inv) {
-  const __nv_bfloat162 inv2 = __float2bfloat162_rn(inv);
-#pragma unroll
-  for (int jj = 0; jj < 2; ++jj) {
-    const uint32_t ad = vtile + 4096u * (uint32_t)rc.part + sw32_chunk(rc.row, jj);
-    uint4 x = lds128(ad);
-    __nv_bfloat162* hx = reinterpret_cast<__nv_bfloat162*>(&x);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) hx[q] = __hmul2(hx[q], inv2);
-    sts128(ad, x);
-  }
-}
-
 __device__ __forceinline__ uint16_t bf16_bits(float x) {
   const __nv_bfloat16 h = __float2bfloat16_rn(x);
   return *reinterpret_cast<const uint16_t*>(&h);
@@ -493,14 +481,6 @@ __device__ __forceinline__ void store_out16(__nv_bfloat16* dst, const uint32_t* 
                       pack_bf16x2(__uint_as_float(acc[8 * c + 4]) * rden, __uint_as_float(acc[8 * c + 5]) * rden),
                       pack_bf16x2(__uint_as_float(acc[8 * c + 6]) * rden, __uint_as_float(acc[8 * c + 7]) * rden));
 }
-__device__ __forceinline__ void store_out8(__nv_bfloat16* dst, const uint32_t* acc, float rden) {
-  *reinterpret_cast<uint4*>(dst) =
-      make_uint4(pack_bf16x2(__uint_as_float(acc[0]) * rden, __uint_as_float(acc[1]) * rden),
-                 pack_bf16x2(__uint_as_float(acc[2]) * rden, __uint_as_float(acc[3]) * rden),
-                 pack_bf16x2(__uint_as_float(acc[4]) * rden, __uint_as_float(acc[5]) * rden),
-                 pack_bf16x2(__uint_as_float(acc[6]) * rden, __uint_as_float(acc[7]) * rden));
-}
-
 // ----------------------------------------------------------------------------------------------- write / aggregate
 // grid (splits, B*H).  CTA (split, bh) covers tiles [split * seg_tiles, ...) of head-row bh and adds
 // Gamma_K^T [V | 1] over them into state[bh] (kAtomic) or stores it to state[bh][split] (causal).

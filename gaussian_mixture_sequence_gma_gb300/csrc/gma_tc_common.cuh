@@ -182,11 +182,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
         "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
 }
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t* r) {
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-               : "r"(taddr));
-}
 __device__ __forceinline__ uint32_t tmem_ld1(uint32_t taddr) {
   uint32_t r;
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];\n" : "=r"(r) : "r"(taddr));
@@ -195,14 +190,6 @@ __device__ __forceinline__ uint32_t tmem_ld1(uint32_t taddr) {
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_ld_wait_tied1(uint32_t& r) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r) : : "memory");
-}
-// the same for two 8-register loads and a 1-register load
-__device__ __forceinline__ void tmem_ld_wait_tied8x2_1(uint32_t* a, uint32_t* b, uint32_t& z) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;"
-               : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]), "+r"(a[7]),
-                 "+r"(b[0]), "+r"(b[1]), "+r"(b[2]), "+r"(b[3]), "+r"(b[4]), "+r"(b[5]), "+r"(b[6]), "+r"(b[7]), "+r"(z)
-               :
-               : "memory");
 }
 __device__ __forceinline__ void tmem_ld_wait_tied16(uint32_t* r) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r[0]),"+r"(r[1]),"+r"(r[2]),"+r"(r[3]),"+r"(r[4]),"+r"(r[5]),"+r"(r[6]),"+r"(r[7]),"+r"(r[8]),"+r"(r[9]),"+r"(r[10]),"+r"(r[11]),"+r"(r[12]),"+r"(r[13]),"+r"(r[14]),"+r"(r[15]) : : "memory");
@@ -303,10 +290,6 @@ __host__ __device__ __forceinline__ uint32_t sw32_chunk(int r, int c) {
   return (uint32_t)r * 32u + ((uint32_t)(c ^ ((r >> 2) & 1)) << 4);
 }
 
-// Descriptor of the same operand `bytes` further on (the start-address field holds address >> 4 in
-// 14 bits; every shared-memory address here is below 256 KB, so the add never carries out of it).
-__device__ __forceinline__ uint64_t sdesc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
-
 // Byte offset of 16-bit element (row r, column k) of a 128B-swizzled tile whose rows hold 64
 // elements per block and whose column blocks lie `block_stride` bytes apart.  Used both for
 // K-major operands (rows = M or N, columns = contraction) and for MN-major operands (rows =
@@ -315,11 +298,6 @@ __host__ __device__ __forceinline__ uint32_t sw128_off(int r, int k, uint32_t bl
   const int kb = k >> 6, kk = k & 63;
   return kb * block_stride + (r >> 3) * 1024 + (r & 7) * 128 + ((((kk >> 3) ^ (r & 7)) & 7) << 4) + (kk & 7) * 2;
 }
-// Byte offset of the 16-byte chunk `chunk` (8 elements) of row r within one 64-column block.
-__host__ __device__ __forceinline__ uint32_t sw128_chunk(int r, int chunk) {
-  return (r >> 3) * 1024 + (r & 7) * 128 + (((chunk ^ (r & 7)) & 7) << 4);
-}
-
 // ---------------------------------------------------------------------------------------------- numerics
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
@@ -336,12 +314,6 @@ __device__ __forceinline__ float rcp_approx(float x) {
 // (a, b) += (c, d) with one packed float32x2 add.
 __device__ __forceinline__ void add_f32x2(float& a, float& b, float c, float d) {
   asm("{\n .reg .b64 x, y;\n mov.b64 x, {%0, %1};\n mov.b64 y, {%2, %3};\n add.rn.f32x2 x, x, y;\n"
-      " mov.b64 {%0, %1}, x;\n}\n"
-      : "+f"(a), "+f"(b)
-      : "f"(c), "f"(d));
-}
-__device__ __forceinline__ void mul_f32x2(float& a, float& b, float c, float d) {
-  asm("{\n .reg .b64 x, y;\n mov.b64 x, {%0, %1};\n mov.b64 y, {%2, %3};\n mul.rn.f32x2 x, x, y;\n"
       " mov.b64 {%0, %1}, x;\n}\n"
       : "+f"(a), "+f"(b)
       : "f"(c), "f"(d));
