@@ -113,35 +113,46 @@ struct TcArgs {
 // ----------------------------------------------------------------------------------------------- prep
 // a1: fold (mu, sigma2, log_pi) of every head into the swizzled fp16 W image and the 256-entry c'
 // table (-inf past K); clear the error word; zero `zero_n` floats of the write accumulator.
-// grid (256, H), 128 threads: thread j builds element j of component k's W row (k < Kp).
+// grid (256 / 8, H), 128 threads: 16 threads per component, thread q of a component builds the 16-byte
+// chunk of W elements 8q .. 8q+7 of that component's row (x^2 coefficients for q < 8, x coefficients
+// after) with one store, and the q < 8 threads sum c'_k over their 8 dims.
 __global__ void __launch_bounds__(128) tc_prep_kernel(const float* __restrict__ mu, const float* __restrict__ sigma2,
                                                       const float* __restrict__ log_pi, int H, int K, int Kp,
                                                       uint8_t* w_img, float* cbias, Ctrl* ctrl, float* zero,
                                                       size_t zero_n) {
-  const int k = blockIdx.x, h = blockIdx.y, j = threadIdx.x;
-  __shared__ float part[4];
-  float val = 0.f, term = 0.f;
+  const int h = blockIdx.y, k = blockIdx.x * 8 + (threadIdx.x >> 4), q = threadIdx.x & 15;
+  const int d0 = 8 * (q & 7);
+  uint32_t w[4] = {0u, 0u, 0u, 0u};
+  float term = 0.f;
   if (k < K) {
-    const int dim = j & 63;
-    const float s2 = sigma2[((size_t)h * K + k) * kD + dim];
-    const float m = mu[((size_t)h * K + k) * kD + dim];
-    const float inv = 1.0f / s2;
-    val = (j < 64 ? -0.5f * inv : m * inv) * kLog2e;
-    if (j < 64) term = m * m * inv + logf(s2);
-  }
-  uint8_t* img = w_img + (size_t)h * Kp * 256;
-  if (k < Kp) *(__half*)(img + sw128_off(k, j, (uint32_t)Kp * 128)) = __float2half_rn(val);
-  // c'_k = (log pi_k - 1/2 sum_d (mu^2/sigma2 + log sigma2)) * log2(e)
-  float s = term;
+    const float4* m4 = reinterpret_cast<const float4*>(mu + ((size_t)h * K + k) * kD + d0);
+    const float4* s4 = reinterpret_cast<const float4*>(sigma2 + ((size_t)h * K + k) * kD + d0);
+    const float4 ma = __ldg(m4), mb = __ldg(m4 + 1), sa = __ldg(s4), sb = __ldg(s4 + 1);
+    const float m[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
+    const float s2[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
+    float val[8];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  if ((j & 31) == 0) part[j >> 5] = s;
-  __syncthreads();
-  if (j == 0) {
-    const float tot = part[0] + part[1];  // threads 0..63 carry the terms
-    cbias[(size_t)h * kCTable + k] = k < K ? (log_pi[(size_t)h * K + k] - 0.5f * tot) * kLog2e : -INFINITY;
+    for (int i = 0; i < 8; ++i) {
+      const float inv = 1.0f / s2[i];
+      val[i] = (q < 8 ? -0.5f * inv : m[i] * inv) * kLog2e;
+      if (q < 8) term += m[i] * m[i] * inv + logf(s2[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __half2 p2 = __floats2half2_rn(val[2 * i], val[2 * i + 1]);
+      w[i] = *reinterpret_cast<const uint32_t*>(&p2);
+    }
   }
-  if (k == 0 && h == 0 && j == 0) {
+  if (k < Kp)
+    *reinterpret_cast<uint4*>(w_img + (size_t)h * Kp * 256 + sw128_off(k, 8 * q, (uint32_t)Kp * 128)) =
+        make_uint4(w[0], w[1], w[2], w[3]);
+  // c'_k = (log pi_k - 1/2 sum_d (mu^2/sigma2 + log sigma2)) * log2(e); the 16 threads of a component are
+  // an aligned half-warp
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) term += __shfl_xor_sync(0xffffffffu, term, o);
+  if (q == 0 && k < kCTable)
+    cbias[(size_t)h * kCTable + k] = k < K ? (log_pi[(size_t)h * K + k] - 0.5f * term) * kLog2e : -INFINITY;
+  if (blockIdx.x == 0 && h == 0 && threadIdx.x == 0) {
     ctrl->err = kErrNone;
     ctrl->err_site = 0;
   }
@@ -1503,7 +1514,7 @@ gma_status_t tc_run(const gma_problem_t& p, gma_op_t op, int Nk, const void* Q, 
   }
   const bool with_state = op == GMA_OP_BIDIR || op == GMA_OP_CAUSAL_STATE;  // write accumulator starts at zero
   const size_t zero_n = with_state ? (size_t)BH * pl.Kp * kStCols : 0;
-  GMA_LAUNCH("tc_prep", tc_prep_kernel, dim3(kCTable, p.H), 128, 0, st, mu, sigma2, log_pi, p.H, p.K, pl.Kp,
+  GMA_LAUNCH("tc_prep", tc_prep_kernel, dim3(kCTable / 8, p.H), 128, 0, st, mu, sigma2, log_pi, p.H, p.K, pl.Kp,
              (uint8_t*)a.w_img, (float*)a.cbias, a.ctrl, a.state, zero_n);
   if (gma_status_t e = check_launch("launch tc_prep", (const void*)tc_prep_kernel)) return e;
   const int nc = pl.Kp <= 64 ? 16 : (pl.Kp <= 128 ? 32 : 64);  // components per row thread (4 per row)
