@@ -793,13 +793,23 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       // consecutive float4 (column kDv holds Z; eps is folded in once here so gamma~ . (Z + eps) is one
       // contraction column)
       const float4* src = reinterpret_cast<const float4*>(a.state + (size_t)bh * a.Kp * kStCols);
-      const int nq = a.Kp * (kStCols / 4);
-      for (int i = threadIdx.x - 32 * kRowWarp0; i < nq; i += 32 * (kThreadsTc / 32 - kRowWarp0)) {
-        const float4 f = __ldg(src + i);
-        const int comp = i / (kStCols / 4), c = i - comp * (kStCols / 4);
-        const float e[4] = {c == kDv / 4 ? f.x + a.eps : f.x, f.y, f.z, f.w};
+      const int nq = a.Kp * (kStCols / 4), nt = 32 * (kThreadsTc / 32 - kRowWarp0);
+      for (int i0 = threadIdx.x - 32 * kRowWarp0; i0 < nq; i0 += 10 * nt) {
+        float4 f[10];  // all of a thread's loads in flight before the first store (Kp <= 256: one pass)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) sts16(sbase + L.sb + sw128_off(4 * c + j, comp, kStCols * 128), bf16_bits(e[j]));
+        for (int u = 0; u < 10; ++u)
+          if (i0 + u * nt < nq) f[u] = __ldg(src + i0 + u * nt);
+#pragma unroll
+        for (int u = 0; u < 10; ++u) {
+          const int i = i0 + u * nt;
+          if (i < nq) {
+            const int comp = i / (kStCols / 4), c = i - comp * (kStCols / 4);
+            const float e[4] = {c == kDv / 4 ? f[u].x + a.eps : f[u].x, f[u].y, f[u].z, f[u].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              sts16(sbase + L.sb + sw128_off(4 * c + j, comp, kStCols * 128), bf16_bits(e[j]));
+          }
+        }
       }
       fence_async_smem();
       warp_arrive(&B.sb_full);
@@ -1186,14 +1196,21 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       const int comp = 128 * rc.part + rc.row;
       // column-major [80][Kp]: each load of a warp covers 32 consecutive components
       const float* pre = a.state + ((size_t)bh * a.splits + seg) * kStCols * a.Kp + comp;
-      uint32_t r[16];
+      // the 80 loads in two batches (columns 0..47, then 48..79): two round trips to memory, not five
 #pragma unroll
-      for (int c = 0; c < 5; ++c) {
+      for (int hb = 0; hb < 2; ++hb) {
+        const int c0 = hb ? 3 : 0, nc = hb ? 2 : 3;  // 16-column chunks of this batch
+        uint32_t r[48];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          r[i] = comp < a.Kp ? __float_as_uint(__ldg(pre + (size_t)(16 * c + i) * a.Kp)) : 0u;
-        tmem_st16(tmem + rc.lane_base + kCColS + kStCols * rc.part + 16 * c, r);
-        if (comp < a.Kp) snapshot_state_chunk(sbase + L.sbv, a.Kp, comp, c, r, a.eps);
+        for (int i = 0; i < 48; ++i)
+          if (i < 16 * nc) r[i] = comp < a.Kp ? __float_as_uint(__ldg(pre + (size_t)(16 * c0 + i) * a.Kp)) : 0u;
+#pragma unroll
+        for (int c = 0; c < 3; ++c) {
+          if (c < nc) {
+            tmem_st16(tmem + rc.lane_base + kCColS + kStCols * rc.part + 16 * (c0 + c), r + 16 * c);
+            if (comp < a.Kp) snapshot_state_chunk(sbase + L.sbv, a.Kp, comp, c0 + c, r + 16 * c, a.eps);
+          }
+        }
       }
     }
     tmem_st_wait();
