@@ -52,10 +52,11 @@ __device__ __forceinline__ SimtParams params_at(float* base, int H, int K) {
 }
 
 // Folds (mu, sigma2, log_pi) into the prepared layout, clears the error word and zeroes `zero_n`
-// floats at `zero` (the write-phase accumulator).
+// floats at `zero` (the write-phase accumulator).  wpair (backward only, else null): the pairs
+// (1 / sigma2, mu / sigma2) in the order of mu, [H][K][64][2], read by the dx step.
 __global__ void simt_prep_kernel(const float* __restrict__ mu, const float* __restrict__ sigma2,
                                  const float* __restrict__ log_pi, int H, int K, float* params, Ctrl* ctrl,
-                                 float* zero, size_t zero_n) {
+                                 float* zero, size_t zero_n, float2* wpair) {
   SimtParams P = params_at(params, H, K);
   const size_t tid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   const size_t nth = (size_t)gridDim.x * blockDim.x;
@@ -66,8 +67,10 @@ __global__ void simt_prep_kernel(const float* __restrict__ mu, const float* __re
     const int k = (int)((i / kD) % K);
     const int h = (int)(i / ((size_t)kD * K));
     const size_t o = ((size_t)h * kD + j) * K + k;
+    const float w = 1.0f / sigma2[i];
     P.mu_t[o] = mu[i];
-    P.w_t[o] = 1.0f / sigma2[i];
+    P.w_t[o] = w;
+    if (wpair) wpair[i] = make_float2(w, w * mu[i]);
   }
   // c_k: one warp per component, two dims per lane, then a warp sum (coalesced, no serial chain)
   const int lane = threadIdx.x & 31;
@@ -140,18 +143,158 @@ __device__ void gamma_tile(const float* xs, int nvalid, const SimtParams& P, int
   __syncthreads();
 }
 
-// sacc[(k, c)] += sum_i G[i][k] * [v_i | 1]_c over one tile; each pair is owned by one thread.
-__device__ __forceinline__ void accumulate_state(const float* G, const float* vs, int K, float* sacc) {
-  const int npairs = K * kStateCols;
-  for (int p = threadIdx.x; p < npairs; p += blockDim.x) {
-    const int k = p / kStateCols, c = p % kStateCols;
-    float s = 0.f;
-    if (c < kDv) {
-      for (int i = 0; i < T; ++i) s = fmaf(G[i * K + k], vs[i * kDv + c], s);
-    } else {
-      for (int i = 0; i < T; ++i) s += G[i * K + k];
+// ---- register-tiled pieces of the write and backward kernels ---------------------------------------
+// KC is K rounded up to 32, 64, 128 or 256: the width of the shared-memory gamma tiles G[T][KC] (zero past
+// K) and the row count of the state images.  A state image holds a [K][dv + 1] float32 state as S[KC][kSP]
+// (the dv columns; rows past K zero) with the normaliser column apart in Z[KC].  kSP = 68 keeps the rows
+// 16-byte aligned, and eight lanes whose 16-byte loads are one row apart hit disjoint groups of banks.
+constexpr int kSP = 68;
+
+__host__ __device__ constexpr int kc_class(int K) { return K <= 32 ? 32 : (K <= 64 ? 64 : (K <= 128 ? 128 : 256)); }
+
+template <int KC>
+__device__ __forceinline__ void load_state_image(const float* src, int K, float* S, float* Z) {
+  for (int p = threadIdx.x; p < KC * kDv; p += blockDim.x) {
+    const int k = p / kDv, c = p % kDv;
+    S[k * kSP + c] = k < K ? src[(size_t)k * kStateCols + c] : 0.f;
+  }
+  for (int k = threadIdx.x; k < KC; k += blockDim.x) Z[k] = k < K ? src[(size_t)k * kStateCols + kDv] : 0.f;
+}
+
+// Responsibilities of the T rows in xs (first `nvalid` valid) into G[T][KC]; rows past nvalid and
+// columns past K are zero.  Thread (component k, group of RPT = T KC / 256 rows) keeps RPT independent
+// sums of the centered log-density, so that each parameter is read once per tile; then one warp per
+// row takes the softmax.  Needs 256 threads.
+template <int KC>
+__device__ void gamma_tile_kc(const float* xs, int nvalid, const SimtParams& P, int h, int K, float* G) {
+  constexpr int RK = KC / 32, RPT = T * KC / kThreads;
+  const float* mu_t = P.mu_t + (size_t)h * kD * K;
+  const float* w_t = P.w_t + (size_t)h * kD * K;
+  const float* c = P.c + (size_t)h * K;
+  const int k = threadIdx.x % KC, r0 = (threadIdx.x / KC) * RPT;
+  if (k < K) {
+    float acc[RPT];
+#pragma unroll
+    for (int ii = 0; ii < RPT; ++ii) acc[ii] = 0.f;
+#pragma unroll 1
+    for (int j = 0; j < kD; j += 4) {
+      float m[4], w[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        m[t] = __ldg(mu_t + (size_t)(j + t) * K + k);
+        w[t] = __ldg(w_t + (size_t)(j + t) * K + k);
+      }
+#pragma unroll
+      for (int ii = 0; ii < RPT; ++ii) {
+        const float4 x = *reinterpret_cast<const float4*>(xs + (r0 + ii) * kD + j);
+        float d = x.x - m[0];
+        acc[ii] = fmaf(d * w[0], d, acc[ii]);
+        d = x.y - m[1];
+        acc[ii] = fmaf(d * w[1], d, acc[ii]);
+        d = x.z - m[2];
+        acc[ii] = fmaf(d * w[2], d, acc[ii]);
+        d = x.w - m[3];
+        acc[ii] = fmaf(d * w[3], d, acc[ii]);
+      }
     }
-    sacc[p] += s;
+    const float ck = __ldg(c + k);
+#pragma unroll
+    for (int ii = 0; ii < RPT; ++ii) G[(r0 + ii) * KC + k] = ck - 0.5f * acc[ii];
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  for (int i = warp; i < T; i += nwarps) {
+    float* row = G + i * KC;
+    if (i >= nvalid) {
+#pragma unroll
+      for (int r = 0; r < RK; ++r) row[lane + 32 * r] = 0.f;
+      continue;
+    }
+    float v[RK], m = -INFINITY;
+#pragma unroll
+    for (int r = 0; r < RK; ++r) {
+      v[r] = lane + 32 * r < K ? row[lane + 32 * r] : -INFINITY;
+      m = fmaxf(m, v[r]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float s = 0.f;
+#pragma unroll
+    for (int r = 0; r < RK; ++r) {
+      v[r] = lane + 32 * r < K ? expf(v[r] - m) : 0.f;
+      s += v[r];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    const float inv = 1.0f / s;
+#pragma unroll
+    for (int r = 0; r < RK; ++r) row[lane + 32 * r] = v[r] * inv;
+  }
+  __syncthreads();
+}
+
+// acc[q][e] += sum_i G[i][k0 + q] B[i][lane + 32 e] and z += sum_i G[i][k0 + lane] b_i (lanes < KC / 8):
+// warp w owns components k0 = w KC / 8 .. + KC / 8 against the 64 columns of the rows B[T][ldb];
+// b_i = bz[i], or 1 where bz is null.  G has row stride LDG.  Needs 8 warps.
+template <int KC, int LDG = KC>
+__device__ __forceinline__ void accumulate_gt(const float* G, const float* B, int ldb, const float* bz,
+                                              float (&acc)[KC / 8][2], float& z) {
+  constexpr int KW = KC / 8;
+  const int lane = threadIdx.x & 31, k0 = (threadIdx.x >> 5) * KW;
+#pragma unroll 2
+  for (int i = 0; i < T; ++i) {
+    const float b0 = B[i * ldb + lane], b1 = B[i * ldb + 32 + lane];
+    const float* g = G + i * LDG + k0;
+#pragma unroll
+    for (int q = 0; q < KW; q += 4) {
+      const float4 g4 = *reinterpret_cast<const float4*>(g + q);
+      acc[q][0] = fmaf(g4.x, b0, acc[q][0]);
+      acc[q][1] = fmaf(g4.x, b1, acc[q][1]);
+      acc[q + 1][0] = fmaf(g4.y, b0, acc[q + 1][0]);
+      acc[q + 1][1] = fmaf(g4.y, b1, acc[q + 1][1]);
+      acc[q + 2][0] = fmaf(g4.z, b0, acc[q + 2][0]);
+      acc[q + 2][1] = fmaf(g4.z, b1, acc[q + 2][1]);
+      acc[q + 3][0] = fmaf(g4.w, b0, acc[q + 3][0]);
+      acc[q + 3][1] = fmaf(g4.w, b1, acc[q + 3][1]);
+    }
+    if (lane < KW) z = fmaf(g[lane], bz ? bz[i] : 1.f, z);
+  }
+}
+
+// Copies the first nvalid rows of a tile G[T][KC] to dst[nvalid][K], and back (zero past nvalid and K).
+template <int KC>
+__device__ __forceinline__ void store_rows(const float* G, int nvalid, int K, float* dst) {
+  for (int p = threadIdx.x; p < nvalid * K; p += blockDim.x) dst[p] = G[(p / K) * KC + p % K];
+}
+// (G row stride LDG; the pad columns past KC are left alone)
+template <int KC, int LDG = KC>
+__device__ __forceinline__ void load_tile_rows(const float* src, int nvalid, int K, float* G) {
+  for (int p = threadIdx.x; p < T * KC; p += blockDim.x) {
+    const int i = p / KC, k = p % KC;
+    G[i * LDG + k] = i < nvalid && k < K ? src[(size_t)i * K + k] : 0.f;
+  }
+}
+
+// Writes (or adds, atomic != 0) the register blocks of accumulate_gt into a [K][dv + 1] state at dst.
+template <int KC>
+__device__ __forceinline__ void store_gt(float* dst, int K, const float (&acc)[KC / 8][2], float z, int atomic) {
+  constexpr int KW = KC / 8;
+  const int lane = threadIdx.x & 31, k0 = (threadIdx.x >> 5) * KW;
+#pragma unroll
+  for (int q = 0; q < KW; ++q) {
+    if (k0 + q >= K) break;
+    float* row = dst + (size_t)(k0 + q) * kStateCols;
+    if (atomic) {
+      atomicAdd(row + lane, acc[q][0]);
+      atomicAdd(row + 32 + lane, acc[q][1]);
+    } else {
+      row[lane] = acc[q][0];
+      row[32 + lane] = acc[q][1];
+    }
+  }
+  if (lane < KW && k0 + lane < K) {
+    float* zp = dst + (size_t)(k0 + lane) * kStateCols + kDv;
+    if (atomic) atomicAdd(zp, z); else *zp = z;
   }
 }
 
@@ -174,37 +317,83 @@ __global__ void __launch_bounds__(kThreads) simt_resp_kernel(const IO* __restric
   for (int i = threadIdx.x; i < nvalid * K; i += blockDim.x) out[i] = G[i];
 }
 
-// Write phase (bidirectional) or segment aggregate (causal): grid (splits, B*H).  Each CTA covers
-// tiles [split * seg_tiles, ...) of its (b,h).  atomic != 0: add into state[unit][K][65];
-// atomic == 0: store into state[unit][split][K][65].
+// Eight consecutive elements of a row as float32 (one 16-byte load for bf16, two for float32).
 template <typename IO>
-__global__ void __launch_bounds__(kThreads) simt_write_kernel(const IO* __restrict__ Kx, const IO* __restrict__ V,
+__device__ __forceinline__ void load8(const IO* __restrict__ p, float (&v)[8]);
+template <>
+__device__ __forceinline__ void load8<float>(const float* __restrict__ p, float (&v)[8]) {
+  const float4 a = __ldg(reinterpret_cast<const float4*>(p)), b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+template <>
+__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* __restrict__ p, float (&v)[8]) {
+  const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    v[2 * t] = __uint_as_float(w[t] << 16);
+    v[2 * t + 1] = __uint_as_float(w[t] & 0xffff0000u);
+  }
+}
+
+// A tile's share of one thread of 256: row r = tid / 8, elements 8 (tid % 8) .. + 7 of rows [r0, r0 + n)
+// of a [rows][64] matrix (zero past n), and its store into a [T][64] shared-memory tile.
+template <typename IO>
+__device__ __forceinline__ void fetch_tile8(const IO* __restrict__ src, int r0, int n, float (&v)[8]) {
+  const int r = threadIdx.x >> 3, c = 8 * (threadIdx.x & 7);
+#pragma unroll
+  for (int t = 0; t < 8; ++t) v[t] = 0.f;
+  if (r < n) load8<IO>(src + (size_t)(r0 + r) * kD + c, v);
+}
+__device__ __forceinline__ void put_tile8(float* dst, const float (&v)[8]) {
+  float* d = dst + (threadIdx.x >> 3) * kD + 8 * (threadIdx.x & 7);
+  *reinterpret_cast<float4*>(d) = make_float4(v[0], v[1], v[2], v[3]);
+  *reinterpret_cast<float4*>(d + 4) = make_float4(v[4], v[5], v[6], v[7]);
+}
+
+// Write phase (bidirectional) or segment aggregate (causal): grid (splits, B*H).  Each CTA covers
+// tiles [split * seg_tiles, ...) of its (b,h) and keeps its partial [Vt | Z] in registers (accumulate_gt).
+// atomic != 0: add into state[unit][K][65]; atomic == 0: store into state[unit][split][K][65].
+// gout (backward only, else null): every key's responsibilities, [B*H][N][K].
+template <typename IO, int KC>
+__global__ void __launch_bounds__(kThreads, KC <= 128 ? 2 : 1) simt_write_kernel(const IO* __restrict__ Kx, const IO* __restrict__ V,
                                                               float* params, int H, int N, int K, int seg_tiles,
-                                                              int splits, float* state, int atomic) {
+                                                              int splits, float* state, int atomic, float* gout) {
   extern __shared__ float sm[];
-  float* xs = sm;
-  float* vs = xs + T * kD;
-  float* G = vs + T * kDv;
-  float* sacc = G + T * K;  // [K][65] partial state of this CTA
+  float* xs = sm;           // [T][64]
+  float* vs = xs + T * kD;  // [T][64]
+  float* G = vs + T * kDv;  // [T][KC]
   const int unit = blockIdx.y, h = unit % H, split = blockIdx.x;
   const SimtParams P = params_at(params, H, K);
-  const int npairs = K * kStateCols;
-  for (int p = threadIdx.x; p < npairs; p += blockDim.x) sacc[p] = 0.f;
+  float acc[KC / 8][2], z = 0.f;
+#pragma unroll
+  for (int q = 0; q < KC / 8; ++q) acc[q][0] = acc[q][1] = 0.f;
   const int tiles = (N + T - 1) / T;
   const int tb = split * seg_tiles, te = min(tiles, tb + seg_tiles);
+  const IO* kb = Kx + (size_t)unit * N * kD;
+  const IO* vb = V + (size_t)unit * N * kDv;
+  float xk[8], xv[8];  // the next tile's key and value rows, loaded while the current one is worked on
+  if (tb < te) {
+    fetch_tile8<IO>(kb, tb * T, min(T, N - tb * T), xk);
+    fetch_tile8<IO>(vb, tb * T, min(T, N - tb * T), xv);
+  }
   for (int t = tb; t < te; ++t) {
     const int t0 = t * T, nvalid = min(T, N - t0);
-    load_rows<IO>(Kx + (size_t)unit * N * kD, t0, nvalid, xs);
-    load_rows<IO>(V + (size_t)unit * N * kDv, t0, nvalid, vs);
+    put_tile8(xs, xk);
+    put_tile8(vs, xv);
     __syncthreads();
-    gamma_tile(xs, nvalid, P, h, K, G);
-    accumulate_state(G, vs, K, sacc);
+    if (t + 1 < te) {
+      fetch_tile8<IO>(kb, t0 + T, min(T, N - t0 - T), xk);
+      fetch_tile8<IO>(vb, t0 + T, min(T, N - t0 - T), xv);
+    }
+    gamma_tile_kc<KC>(xs, nvalid, P, h, K, G);
+    accumulate_gt<KC>(G, vs, kDv, nullptr, acc, z);
+    if (gout) store_rows<KC>(G, nvalid, K, gout + ((size_t)unit * N + t0) * K);
     __syncthreads();
   }
-  float* dst = atomic ? state + (size_t)unit * npairs : state + ((size_t)unit * splits + split) * npairs;
-  for (int p = threadIdx.x; p < npairs; p += blockDim.x) {
-    if (atomic) atomicAdd(dst + p, sacc[p]); else dst[p] = sacc[p];
-  }
+  const size_t npairs = (size_t)K * kStateCols;
+  store_gt<KC>(atomic ? state + (size_t)unit * npairs : state + ((size_t)unit * splits + split) * npairs, K, acc, z,
+               atomic);
 }
 
 // Read phase (bidirectional): grid (tiles, B*H).
@@ -335,74 +524,184 @@ __global__ void __launch_bounds__(kThreads) simt_causal_kernel(const IO* __restr
 //   dmu = D1 / sigma2,  dsigma2 = (D2 / sigma2 - b) / (2 sigma2),  dlog_pi = b.
 // The per-row dl of both sides go through the workspace to the parameter-gradient pass.
 
-// dx for the T rows of xs from dl [T][K]: sum_k dl_ik w_kd (mu_kd - x_id) = (dl (w mu))_id - x_id (dl w)_id.
-// Thread (column j, row group) walks k reading mu[h][k][j] and sigma2[h][k][j] (consecutive j across a
-// warp: coalesced) and updates its T / 4 rows.
-template <typename IO>
-__device__ void dx_tile(const float* xs, const float* dl, int nvalid, const float* __restrict__ mu,
-                        const float* __restrict__ sigma2, int h, int K, IO* dst) {
-  constexpr int kRowGroups = kThreads / kD;  // 4
-  constexpr int kRows = T / kRowGroups;      // 8 rows per thread
-  const int j = threadIdx.x % kD, rg = threadIdx.x / kD;
-  const float* muh = mu + (size_t)h * K * kD + j;
-  const float* s2h = sigma2 + (size_t)h * K * kD + j;
-  float a1[kRows], a2[kRows];
+// a[q][e] = sum_k G[i0 + q][k] S[k][lane + 32 e]: rows i0 .. i0 + 3 of a tile (row stride LDG) times the
+// dv columns of a state image (the warp's lanes split the columns; each G row is read as a broadcast).
+template <int KC, int LDG = KC>
+__device__ __forceinline__ void rows_times_image(const float* G, const float* S, int i0, float (&a)[4][2]) {
+  const int lane = threadIdx.x & 31;
 #pragma unroll
-  for (int r = 0; r < kRows; ++r) a1[r] = a2[r] = 0.f;
-  for (int k = 0; k < K; ++k) {
-    const float w = 1.0f / __ldg(s2h + (size_t)k * kD), wm = w * __ldg(muh + (size_t)k * kD);
+  for (int q = 0; q < 4; ++q) a[q][0] = a[q][1] = 0.f;
+#pragma unroll 2
+  for (int k = 0; k < KC; k += 4) {
+    float4 g[4];
 #pragma unroll
-    for (int r = 0; r < kRows; ++r) {
-      const float d = dl[(rg * kRows + r) * K + k];
-      a1[r] = fmaf(d, wm, a1[r]);
-      a2[r] = fmaf(d, w, a2[r]);
+    for (int q = 0; q < 4; ++q) g[q] = *reinterpret_cast<const float4*>(G + (i0 + q) * LDG + k);
+    const float* sk = S + k * kSP + lane;
+    float s0[4], s1[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      s0[t] = sk[t * kSP];
+      s1[t] = sk[t * kSP + 32];
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      a[q][0] = fmaf(g[q].x, s0[0], a[q][0]);
+      a[q][1] = fmaf(g[q].x, s1[0], a[q][1]);
+      a[q][0] = fmaf(g[q].y, s0[1], a[q][0]);
+      a[q][1] = fmaf(g[q].y, s1[1], a[q][1]);
+      a[q][0] = fmaf(g[q].z, s0[2], a[q][0]);
+      a[q][1] = fmaf(g[q].z, s1[2], a[q][1]);
+      a[q][0] = fmaf(g[q].w, s0[3], a[q][0]);
+      a[q][1] = fmaf(g[q].w, s1[3], a[q][1]);
+    }
+  }
+}
+
+// b[q][r] = sum_c A[i0 + q][c] S[lane + 32 r][c] over the dv columns: rows i0 .. i0 + 3 of A[T][lda]
+// against every component row of a state image (lane + 32 r is the component).
+template <int KC>
+__device__ __forceinline__ void rows_times_image_t(const float* A, int lda, const float* S, int i0,
+                                                   float (&b)[4][KC / 32]) {
+  constexpr int RK = KC / 32;
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+#pragma unroll
+    for (int r = 0; r < RK; ++r) b[q][r] = 0.f;
+#pragma unroll 2
+  for (int c = 0; c < kDv; c += 4) {
+    float4 a4[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) a4[q] = *reinterpret_cast<const float4*>(A + (i0 + q) * lda + c);
+#pragma unroll
+    for (int r = 0; r < RK; ++r) {
+      const float4 s4 = *reinterpret_cast<const float4*>(S + (lane + 32 * r) * kSP + c);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        b[q][r] = fmaf(a4[q].x, s4.x, b[q][r]);
+        b[q][r] = fmaf(a4[q].y, s4.y, b[q][r]);
+        b[q][r] = fmaf(a4[q].z, s4.z, b[q][r]);
+        b[q][r] = fmaf(a4[q].w, s4.w, b[q][r]);
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Softmax backward of rows i0 .. i0 + 3 in registers: dg[q][r] (dgamma at component lane + 32 r) becomes
+// dl = gamma (dgamma - gamma . dgamma); G has row stride LDG.
+template <int KC, int LDG = KC>
+__device__ __forceinline__ void softmax_backward_rows(const float* G, int i0, float (&dg)[4][KC / 32]) {
+  constexpr int RK = KC / 32;
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    float g[RK], dot = 0.f;
+#pragma unroll
+    for (int r = 0; r < RK; ++r) {
+      g[r] = G[(i0 + q) * LDG + lane + 32 * r];
+      dot = fmaf(g[r], dg[q][r], dot);
+    }
+    dot = warp_sum(dot);
+#pragma unroll
+    for (int r = 0; r < RK; ++r) dg[q][r] = g[r] * (dg[q][r] - dot);
+  }
+}
+
+// dx_ij = sum_k dl_ik (mu_kj - x_ij) / sigma2_kj = (dl (mu / sigma2))_ij - x_ij (dl (1 / sigma2))_ij for the
+// tile's rows from dl[T][LDG] (zero past K).  The head's (1 / sigma2, mu / sigma2) pairs wp[K][64] pass
+// through `stage` (2048 floats of free shared memory) 16 components at a time; thread (column j, group
+// of 8 rows) then reads its pair per component and four dl values per row at a time.
+template <typename IO, int KC, int LDG = KC>
+__device__ void dx_tile_kc(const float* xs, const float* dl, int nvalid, const float2* __restrict__ wp, int K,
+                           float* stage, IO* dst) {
+  const int j = threadIdx.x % kD, rg = threadIdx.x / kD;  // 4 groups of 8 rows
+  const float2* st2 = reinterpret_cast<const float2*>(stage);
+  float a1[8], a2[8];
+#pragma unroll
+  for (int r = 0; r < 8; ++r) a1[r] = a2[r] = 0.f;
+  for (int k0 = 0; k0 < K; k0 += 16) {
+    const int nk = min(16, K - k0);
+    __syncthreads();  // the previous chunk's readers are done
+    for (int p = threadIdx.x; p < 16 * kD / 2; p += blockDim.x) {  // 512 float4 = 16 components x 64 pairs
+      const int kk = p / (kD / 2);
+      reinterpret_cast<float4*>(stage)[p] =
+          kk < nk ? __ldg(reinterpret_cast<const float4*>(wp + (size_t)k0 * kD) + p) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    __syncthreads();
+#pragma unroll 2
+    for (int kk = 0; kk < 16; kk += 4) {
+      float2 w[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) w[t] = st2[(kk + t) * kD + j];
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const float4 d = *reinterpret_cast<const float4*>(dl + (rg * 8 + r) * LDG + k0 + kk);
+        a1[r] = fmaf(d.x, w[0].y, a1[r]);
+        a2[r] = fmaf(d.x, w[0].x, a2[r]);
+        a1[r] = fmaf(d.y, w[1].y, a1[r]);
+        a2[r] = fmaf(d.y, w[1].x, a2[r]);
+        a1[r] = fmaf(d.z, w[2].y, a1[r]);
+        a2[r] = fmaf(d.z, w[2].x, a2[r]);
+        a1[r] = fmaf(d.w, w[3].y, a1[r]);
+        a2[r] = fmaf(d.w, w[3].x, a2[r]);
+      }
     }
   }
 #pragma unroll
-  for (int r = 0; r < kRows; ++r) {
-    const int i = rg * kRows + r;
+  for (int r = 0; r < 8; ++r) {
+    const int i = rg * 8 + r;
     if (i < nvalid) st_io<IO>(dst + (size_t)i * kD + j, a1[r] - xs[i * kD + j] * a2[r]);
   }
 }
 
-// Softmax backward in place: dG <- G * (dG - G . dG), one warp per row.
-__device__ void softmax_backward_tile(const float* G, float* dG, int K) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-  for (int i = warp; i < T; i += nwarps) {
-    float dot = 0.f;
-    for (int k = lane; k < K; k += 32) dot = fmaf(G[i * K + k], dG[i * K + k], dot);
+// Stores the warp's rows i0 .. i0 + 3 of dl (registers, component lane + 32 r) into the tile G[T][LDG] and,
+// for valid rows and components, into the workspace rows dst[i][K].
+template <int KC, int LDG = KC>
+__device__ __forceinline__ void store_dl_rows(const float (&dl)[4][KC / 32], int i0, int nvalid, int K, float* G,
+                                              float* dst) {
+  const int lane = threadIdx.x & 31;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-    for (int k = lane; k < K; k += 32) dG[i * K + k] = G[i * K + k] * (dG[i * K + k] - dot);
-  }
-  __syncthreads();
+  for (int q = 0; q < 4; ++q)
+#pragma unroll
+    for (int r = 0; r < KC / 32; ++r) {
+      const int k = lane + 32 * r;
+      G[(i0 + q) * LDG + k] = dl[q][r];
+      if (i0 + q < nvalid && k < K) dst[(size_t)(i0 + q) * K + k] = dl[q][r];
+    }
 }
 
-// Query side: grid (splits, B*H).  Recomputes O, pushes dO back through the read, writes dQ and dl_Q,
-// and adds [dVt | dZ] into dstate[unit][K][65].
-template <typename IO>
+// Query side: grid (splits, B*H).  Recomputes O, pushes dO back through the read, writes dQ and dl_Q, and
+// adds [dVt | dZ] into dstate[unit][K][65].  Warp w owns tile rows 4w .. 4w + 3 in the row products and
+// components w KC / 8 .. + KC / 8 of [dVt | dZ], which stay in registers across the CTA's tiles.
+template <typename IO, int KC>
 __global__ void __launch_bounds__(kThreads) simt_bwd_query_kernel(const IO* __restrict__ Q, const IO* __restrict__ dO,
-                                                                  float* params, const float* __restrict__ mu,
-                                                                  const float* __restrict__ sigma2, int H, int N, int K,
-                                                                  int seg_tiles,
+                                                                  float* params, const float2* __restrict__ wpair,
+                                                                  int H, int N, int K, int seg_tiles,
                                                                   const float* __restrict__ state, float eps,
                                                                   float* dstate, float* dlq, IO* __restrict__ dQ) {
+  constexpr int RK = KC / 32;
   extern __shared__ float sm[];
-  const int npairs = K * kStateCols;
-  float* S = sm;                // [K][65]  Vt | Z
-  float* sacc = S + npairs;     // [K][65]  dVt | dZ of this CTA
-  float* xs = sacc + npairs;    // [T][64]
-  float* gs = xs + T * kD;      // [T][64]  dO rows
-  float* dn = gs + T * kDv;     // [T][65]  numerators, then dn | dden
-  float* G = dn + T * kStateCols;  // [T][K]
-  float* dG = G + T * K;        // [T][K]
+  float* S = sm;            // [KC][kSP]  Vt image
+  float* Z = S + KC * kSP;  // [KC]
+  float* xs = Z + KC;       // [T][64]   query rows
+  float* gs = xs + T * kD;  // [T][64]   dO rows, then the dx parameter stage
+  float* dn = gs + T * kDv;  // [T][kSP]  dO / den
+  float* dd = dn + T * kSP;  // [T]       -(dO . O) / den
+  float* G = dd + T;         // [T][KC]   gamma_Q, then dl_Q
   const int unit = blockIdx.y, h = unit % H, split = blockIdx.x;
+  const int lane = threadIdx.x & 31, i0 = 4 * (threadIdx.x >> 5);
   const SimtParams P = params_at(params, H, K);
-  const float* S0 = state + (size_t)unit * npairs;
-  for (int p = threadIdx.x; p < npairs; p += blockDim.x) {
-    S[p] = S0[p];
-    sacc[p] = 0.f;
-  }
+  const size_t npairs = (size_t)K * kStateCols;
+  load_state_image<KC>(state + unit * npairs, K, S, Z);
+  float acc[KC / 8][2], zacc = 0.f;
+#pragma unroll
+  for (int q = 0; q < KC / 8; ++q) acc[q][0] = acc[q][1] = 0.f;
   const int tiles = (N + T - 1) / T;
   const int tb = split * seg_tiles, te = min(tiles, tb + seg_tiles);
   for (int t = tb; t < te; ++t) {
@@ -411,99 +710,100 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_query_kernel(const IO* __re
     load_rows<IO>(Q + (size_t)unit * N * kD, t0, nvalid, xs);
     load_rows<IO>(dO + (size_t)unit * N * kDv, t0, nvalid, gs);
     __syncthreads();
-    gamma_tile(xs, nvalid, P, h, K, G);
-    for (int p = threadIdx.x; p < T * kStateCols; p += blockDim.x) {  // [num | den - eps]
-      const int i = p / kStateCols, c = p % kStateCols;
-      float s = 0.f;
-      for (int k = 0; k < K; ++k) s = fmaf(G[i * K + k], S[k * kStateCols + c], s);
-      dn[p] = s;
-    }
-    __syncthreads();
-    {  // one warp per row: O, G . O, then dn | dden (rows past N have G = 0, so all zero)
-      const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-      for (int i = warp; i < T; i += nwarps) {
-        if (i >= nvalid) {  // rows past N: no gradient (and no 0 / 0 when eps = 0)
-          dn[i * kStateCols + lane] = 0.f;
-          dn[i * kStateCols + 32 + lane] = 0.f;
-          if (lane == 0) dn[i * kStateCols + kDv] = 0.f;
-          continue;
-        }
-        const float den = dn[i * kStateCols + kDv] + eps;
-        const float o0 = dn[i * kStateCols + lane] / den, o1 = dn[i * kStateCols + 32 + lane] / den;
-        float go = gs[i * kDv + lane] * o0 + gs[i * kDv + 32 + lane] * o1;
+    gamma_tile_kc<KC>(xs, nvalid, P, h, K, G);
+    {  // numerators and denominators of the warp's rows, then dn | dd (rows past N: zero)
+      float a[4][2], dp[4] = {0.f, 0.f, 0.f, 0.f};
+      rows_times_image<KC>(G, S, i0, a);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) go += __shfl_xor_sync(0xffffffffu, go, o);
-        __syncwarp();
-        dn[i * kStateCols + lane] = gs[i * kDv + lane] / den;
-        dn[i * kStateCols + 32 + lane] = gs[i * kDv + 32 + lane] / den;
-        if (lane == 0) dn[i * kStateCols + kDv] = -go / den;
+      for (int r = 0; r < RK; ++r) {
+        const float z = Z[lane + 32 * r];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) dp[q] = fmaf(G[(i0 + q) * KC + lane + 32 * r], z, dp[q]);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int i = i0 + q;
+        const float den = warp_sum(dp[q]) + eps;
+        float n0 = 0.f, n1 = 0.f, dv = 0.f;
+        if (i < nvalid) {
+          const float g0 = gs[i * kDv + lane], g1 = gs[i * kDv + 32 + lane];
+          const float go = warp_sum(g0 * (a[q][0] / den) + g1 * (a[q][1] / den));
+          n0 = g0 / den;
+          n1 = g1 / den;
+          dv = -go / den;
+        }
+        dn[i * kSP + lane] = n0;
+        dn[i * kSP + 32 + lane] = n1;
+        if (lane == 0) dd[i] = dv;
       }
     }
     __syncthreads();
-    for (int p = threadIdx.x; p < T * K; p += blockDim.x) {  // dgamma_Q = [Vt | Z] [dn | dden]
-      const int i = p / K, k = p % K;
-      float s = 0.f;
-      for (int c = 0; c < kStateCols; ++c) s = fmaf(dn[i * kStateCols + c], S[k * kStateCols + c], s);
-      dG[p] = s;
-    }
-    for (int p = threadIdx.x; p < npairs; p += blockDim.x) {  // [dVt | dZ] += gamma_Q^T [dn | dden]
-      const int k = p / kStateCols, c = p % kStateCols;
-      float s = 0.f;
-      for (int i = 0; i < T; ++i) s = fmaf(G[i * K + k], dn[i * kStateCols + c], s);
-      sacc[p] += s;
-    }
+    accumulate_gt<KC>(G, dn, kSP, dd, acc, zacc);  // [dVt | dZ] += gamma_Q^T [dn | dd]
+    float b[4][RK];                                // dgamma_Q = [Vt | Z] [dn | dd]
+    rows_times_image_t<KC>(dn, kSP, S, i0, b);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+      for (int r = 0; r < RK; ++r) b[q][r] = fmaf(dd[i0 + q], Z[lane + 32 * r], b[q][r]);
+    softmax_backward_rows<KC>(G, i0, b);
+    __syncthreads();  // every warp is done with gamma_Q
+    store_dl_rows<KC>(b, i0, nvalid, K, G, dlq + ((size_t)unit * N + t0) * K);
     __syncthreads();
-    softmax_backward_tile(G, dG, K);
-    float* dst = dlq + ((size_t)unit * N + t0) * K;
-    for (int p = threadIdx.x; p < nvalid * K; p += blockDim.x) dst[p] = dG[p];
-    dx_tile<IO>(xs, dG, nvalid, mu, sigma2, h, K, dQ + ((size_t)unit * N + t0) * kD);
+    dx_tile_kc<IO, KC>(xs, G, nvalid, wpair + (size_t)h * K * kD, K, gs, dQ + ((size_t)unit * N + t0) * kD);
   }
-  __syncthreads();
-  float* dS = dstate + (size_t)unit * npairs;
-  for (int p = threadIdx.x; p < npairs; p += blockDim.x) atomicAdd(dS + p, sacc[p]);
+  store_gt<KC>(dstate + unit * npairs, K, acc, zacc, 1);
 }
 
-// Key side: grid (tiles, B*H).  Pushes [dVt | dZ] back through the write: dV, dK and dl_K.
-template <typename IO>
+// Key side: grid (splits, B*H).  Pushes [dVt | dZ] back through the write: dV, dK and dl_K.  Warp w owns
+// tile rows 4w .. 4w + 3.  dlk holds gamma_K on entry (the write kernel's copy) and dl_K on exit.
+template <typename IO, int KC>
 __global__ void __launch_bounds__(kThreads) simt_bwd_key_kernel(const IO* __restrict__ Kx, const IO* __restrict__ V,
-                                                                float* params, const float* __restrict__ mu,
-                                                                const float* __restrict__ sigma2, int H, int N, int K,
-                                                                const float* __restrict__ dstate, float* dlk,
-                                                                IO* __restrict__ dK, IO* __restrict__ dV) {
+                                                                const float2* __restrict__ wpair, int H, int N, int K,
+                                                                int seg_tiles,
+                                                                const float* __restrict__ dstate,
+                                                                float* dlk, IO* __restrict__ dK, IO* __restrict__ dV) {
+  constexpr int RK = KC / 32;
   extern __shared__ float sm[];
-  const int npairs = K * kStateCols;
-  float* dS = sm;               // [K][65]  dVt | dZ
-  float* xs = dS + npairs;      // [T][64]
-  float* vs = xs + T * kD;      // [T][64]
-  float* G = vs + T * kDv;      // [T][K]
-  float* dG = G + T * K;        // [T][K]
-  const int unit = blockIdx.y, h = unit % H;
-  const int t0 = blockIdx.x * T, nvalid = min(T, N - t0);
-  const SimtParams P = params_at(params, H, K);
-  const float* dS0 = dstate + (size_t)unit * npairs;
-  for (int p = threadIdx.x; p < npairs; p += blockDim.x) dS[p] = dS0[p];
-  load_rows<IO>(Kx + (size_t)unit * N * kD, t0, nvalid, xs);
-  load_rows<IO>(V + (size_t)unit * N * kDv, t0, nvalid, vs);
-  __syncthreads();
-  gamma_tile(xs, nvalid, P, h, K, G);
-  for (int p = threadIdx.x; p < T * K; p += blockDim.x) {  // dgamma_K = [dVt | dZ] [v | 1]
-    const int j = p / K, k = p % K;
-    float s = dS[k * kStateCols + kDv];
-    for (int c = 0; c < kDv; ++c) s = fmaf(vs[j * kDv + c], dS[k * kStateCols + c], s);
-    dG[p] = s;
+  float* dS = sm;             // [KC][kSP]  dVt image
+  float* dZ = dS + KC * kSP;  // [KC]
+  float* xs = dZ + KC;        // [T][64]   key rows
+  float* vs = xs + T * kD;    // [T][64]   value rows, then the dx parameter stage
+  float* G = vs + T * kDv;    // [T][KC]   gamma_K, then dl_K
+  const int unit = blockIdx.y, h = unit % H, split = blockIdx.x;
+  const int lane = threadIdx.x & 31, i0 = 4 * (threadIdx.x >> 5);
+  load_state_image<KC>(dstate + unit * (size_t)K * kStateCols, K, dS, dZ);
+  const int tiles = (N + T - 1) / T;
+  const int tb = split * seg_tiles, te = min(tiles, tb + seg_tiles);
+  for (int t = tb; t < te; ++t) {
+    const int t0 = t * T, nvalid = min(T, N - t0);
+    __syncthreads();
+    load_rows<IO>(Kx + (size_t)unit * N * kD, t0, nvalid, xs);
+    load_rows<IO>(V + (size_t)unit * N * kDv, t0, nvalid, vs);
+    load_tile_rows<KC>(dlk + ((size_t)unit * N + t0) * K, nvalid, K, G);  // gamma_K, stored by the write
+    __syncthreads();
+    {  // dv = dVt^T gamma_K
+      float a[4][2];
+      rows_times_image<KC>(G, dS, i0, a);
+      IO* dv_out = dV + ((size_t)unit * N + t0) * kDv;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (i0 + q < nvalid) {
+          st_io<IO>(dv_out + (i0 + q) * kDv + lane, a[q][0]);
+          st_io<IO>(dv_out + (i0 + q) * kDv + 32 + lane, a[q][1]);
+        }
+    }
+    float b[4][RK];  // dgamma_K = [dVt | dZ] [v | 1]
+    rows_times_image_t<KC>(vs, kDv, dS, i0, b);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+      for (int r = 0; r < RK; ++r) b[q][r] += dZ[lane + 32 * r];
+    softmax_backward_rows<KC>(G, i0, b);
+    __syncwarp();  // the warp's reads of its own gamma_K rows are done
+    store_dl_rows<KC>(b, i0, nvalid, K, G, dlk + ((size_t)unit * N + t0) * K);
+    __syncthreads();
+    dx_tile_kc<IO, KC>(xs, G, nvalid, wpair + (size_t)h * K * kD, K, vs, dK + ((size_t)unit * N + t0) * kD);
   }
-  IO* dv_out = dV + ((size_t)unit * N + t0) * kDv;
-  for (int p = threadIdx.x; p < nvalid * kDv; p += blockDim.x) {  // dv = dVt^T gamma_K
-    const int j = p / kDv, c = p % kDv;
-    float s = 0.f;
-    for (int k = 0; k < K; ++k) s = fmaf(G[j * K + k], dS[k * kStateCols + c], s);
-    st_io<IO>(dv_out + p, s);
-  }
-  __syncthreads();
-  softmax_backward_tile(G, dG, K);
-  float* dst = dlk + ((size_t)unit * N + t0) * K;
-  for (int p = threadIdx.x; p < nvalid * K; p += blockDim.x) dst[p] = dG[p];
-  dx_tile<IO>(xs, dG, nvalid, mu, sigma2, h, K, dK + ((size_t)unit * N + t0) * kD);
 }
 
 // ---- causal backward.  S_i = sum_{j <= i} gamma_Kj [v_j | 1] (running state), u_i = [G_i / den_i |
@@ -514,136 +814,204 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_key_kernel(const IO* __rest
 // aggregate of gamma_Q u^T; an exclusive suffix scan gives R after each segment; the key pass walks its
 // segment backward.
 
-// Masked tile products for the causal backward: A_ij = gQ_i . gK_j and W_ij = u_i . [v_j | 1] for j <= i.
-__device__ void causal_tile_products(const float* GQ, const float* GK, const float* us, const float* vs, int K,
-                                     float* A, float* W) {
-  for (int p = threadIdx.x; p < T * T; p += blockDim.x) {
-    const int i = p / T, j = p % T;
-    float a = 0.f, w = 0.f;
-    if (j <= i) {
-      for (int k = 0; k < K; ++k) a = fmaf(GQ[i * K + k], GK[j * K + k], a);
-      w = us[i * kStateCols + kDv];
-      for (int c = 0; c < kDv; ++c) w = fmaf(us[i * kStateCols + c], vs[j * kDv + c], w);
-    }
-    A[p] = a;
-    W[p] = w;
+// Loads `n` valid rows (of 64) starting at row `r0` of a [rows][64] matrix into dst[T][ld] as float32;
+// rows past `n` are zero.
+template <typename IO>
+__device__ __forceinline__ void load_rows_ld(const IO* __restrict__ src, int r0, int n, float* dst, int ld) {
+  for (int i = threadIdx.x; i < T * kD; i += blockDim.x) {
+    const int r = i / kD, c = i % kD;
+    dst[r * ld + c] = r < n ? ld_io<IO>(src + (size_t)(r0 + r) * kD + c) : 0.f;
   }
 }
 
-// Query side: grid (segments, B*H).  S starts at agg[unit][seg] (scanned); writes u, dl_Q, dQ and the
-// segment aggregate sum_i gamma_Qi u_i^T into bagg[unit][seg].
-template <typename IO>
-__global__ void __launch_bounds__(kThreads) simt_bwd_causal_query_kernel(
-    const IO* __restrict__ Q, const IO* __restrict__ Kx, const IO* __restrict__ V, const IO* __restrict__ dO,
-    float* params, const float* __restrict__ mu, const float* __restrict__ sigma2, int H, int N, int K, int seg_tiles,
-    int P, const float* agg, float eps, float* bagg, float* uglob, float* dlq, IO* __restrict__ dQ) {
-  extern __shared__ float sm[];
-  const int npairs = K * kStateCols;
-  float* S = sm;                   // [K][65]
-  float* xs = S + npairs;          // [T][64]  queries, then keys
-  float* vs = xs + T * kD;         // [T][64]
-  float* gs = vs + T * kDv;        // [T][64]  dO rows
-  float* us = gs + T * kDv;        // [T][65]  numerators, then u
-  float* GQ = us + T * kStateCols;  // [T][K]
-  float* GK = GQ + T * K;          // [T][K]
-  float* dG = GK + T * K;          // [T][K]
-  float* A = dG + T * K;           // [T][T]
-  float* W = A + T * T;            // [T][T]
-  __shared__ float xq[T * kD];     // the query rows, kept for dQ
-  const int unit = blockIdx.y, h = unit % H, seg = blockIdx.x;
-  const SimtParams Pp = params_at(params, H, K);
-  const float* S0 = agg + ((size_t)unit * P + seg) * npairs;
-  float* bout = bagg + ((size_t)unit * P + seg) * npairs;
-  for (int p = threadIdx.x; p < npairs; p += blockDim.x) {
-    S[p] = S0[p];
-    bout[p] = 0.f;
+// In-tile products of the causal backward for the warp's rows i0 .. i0 + 3 (lane = j), zero for j > i:
+//   A_ij = gamma_Qi . gamma_Kj (GQ row stride KC, GK row stride KC + 4) into A[T][T],
+//   W_ij = dn_i . v_j + dd_i (dn, vs row stride kSP) into W[T][T].
+template <int KC>
+__device__ __forceinline__ void causal_tile_A(const float* GQ, const float* GK, int i0, float* A) {
+  constexpr int KG = KC + 4;
+  const int lane = threadIdx.x & 31;
+  float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
+  for (int k = 0; k < KC; k += 4) {
+    const float4 g = *reinterpret_cast<const float4*>(GK + lane * KG + k);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 f = *reinterpret_cast<const float4*>(GQ + (i0 + q) * KC + k);
+      a[q] = fmaf(f.x, g.x, fmaf(f.y, g.y, fmaf(f.z, g.z, fmaf(f.w, g.w, a[q]))));
+    }
   }
+#pragma unroll
+  for (int q = 0; q < 4; ++q) A[(i0 + q) * T + lane] = lane <= i0 + q ? a[q] : 0.f;
+}
+
+__device__ __forceinline__ void causal_tile_W(const float* dn, const float* dd, const float* vs, int i0, float* W) {
+  const int lane = threadIdx.x & 31;
+  float w[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) w[q] = dd[i0 + q];
+#pragma unroll 2
+  for (int c = 0; c < kDv; c += 4) {
+    const float4 v = *reinterpret_cast<const float4*>(vs + lane * kSP + c);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 f = *reinterpret_cast<const float4*>(dn + (i0 + q) * kSP + c);
+      w[q] = fmaf(f.x, v.x, fmaf(f.y, v.y, fmaf(f.z, v.z, fmaf(f.w, v.w, w[q]))));
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < 4; ++q) W[(i0 + q) * T + lane] = lane <= i0 + q ? w[q] : 0.f;
+}
+
+// S[k][c] += sum_i G[i][k] B[i][c], Z[k] += sum_i G[i][k] b_i (b_i = bz[i], or 1 where bz is null) over one
+// tile: a state image updated in place, warp w owning components w KC / 8 .. + KC / 8 (G row stride LDG).
+template <int KC, int LDG>
+__device__ __forceinline__ void add_gt_to_image(const float* G, const float* B, int ldb, const float* bz, float* S,
+                                                float* Z) {
+  constexpr int KW = KC / 8;
+  const int lane = threadIdx.x & 31, k0 = (threadIdx.x >> 5) * KW;
+  float z = 0.f;
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    float acc[KW];
+#pragma unroll
+    for (int q = 0; q < KW; ++q) acc[q] = 0.f;
+#pragma unroll 2
+    for (int i = 0; i < T; ++i) {
+      const float bv = B[i * ldb + 32 * e + lane];
+      const float* g = G + i * LDG + k0;
+#pragma unroll
+      for (int q = 0; q < KW; q += 4) {
+        const float4 g4 = *reinterpret_cast<const float4*>(g + q);
+        acc[q] = fmaf(g4.x, bv, acc[q]);
+        acc[q + 1] = fmaf(g4.y, bv, acc[q + 1]);
+        acc[q + 2] = fmaf(g4.z, bv, acc[q + 2]);
+        acc[q + 3] = fmaf(g4.w, bv, acc[q + 3]);
+      }
+      if (e == 0 && lane < KW) z = fmaf(g[lane], bz ? bz[i] : 1.f, z);
+    }
+#pragma unroll
+    for (int q = 0; q < KW; ++q) S[(k0 + q) * kSP + 32 * e + lane] += acc[q];
+  }
+  if (lane < KW) Z[k0 + lane] += z;
+}
+
+// Query side: grid (segments, B*H).  S starts at agg[unit][seg] (scanned) and follows the segment's tiles;
+// writes u, gamma_Q (for the key side), dl_Q, dQ and the segment aggregate sum_i gamma_Qi u_i^T into
+// bagg[unit][seg].  gamma_K comes from the aggregate pass (dlk).  Warp w owns tile rows 4w .. 4w + 3.
+template <typename IO, int KC>
+__global__ void __launch_bounds__(kThreads) simt_bwd_causal_query_kernel(
+    const IO* __restrict__ Q, const IO* __restrict__ V, const IO* __restrict__ dO, float* params,
+    const float2* __restrict__ wpair, int H, int N, int K, int seg_tiles, int P, const float* agg, float eps,
+    float* bagg, float* uglob, float* gq, const float* dlk, float* dlq, IO* __restrict__ dQ) {
+  constexpr int RK = KC / 32, KG = KC + 4;
+  extern __shared__ float sm[];
+  float* S = sm;              // [KC][kSP]  running state image
+  float* Z = S + KC * kSP;    // [KC]
+  float* xq = Z + KC;         // [T][64]    query rows
+  float* gs = xq + T * kD;    // [T][64]    dO rows, then the dx parameter stage
+  float* vs = gs + T * kDv;   // [T][kSP]   value rows
+  float* dn = vs + T * kSP;   // [T][kSP]   dO / den
+  float* dd = dn + T * kSP;   // [T]        -(dO . O) / den
+  float* GQ = dd + T;         // [T][KC]    gamma_Q, then dl_Q
+  float* GK = GQ + T * KC;    // [T][KG]    gamma_K
+  float* A = GK + T * KG;     // [T][T]
+  float* W = A + T * T;       // [T][T]
+  const int unit = blockIdx.y, h = unit % H, seg = blockIdx.x;
+  const int lane = threadIdx.x & 31, i0 = 4 * (threadIdx.x >> 5);
+  const SimtParams Pp = params_at(params, H, K);
+  const size_t npairs = (size_t)K * kStateCols;
+  load_state_image<KC>(agg + ((size_t)unit * P + seg) * npairs, K, S, Z);
+  float bacc[KC / 8][2], bz = 0.f;
+#pragma unroll
+  for (int q = 0; q < KC / 8; ++q) bacc[q][0] = bacc[q][1] = 0.f;
   const int tiles = (N + T - 1) / T;
   const int tb = seg * seg_tiles, te = min(tiles, tb + seg_tiles);
   for (int t = tb; t < te; ++t) {
     const int t0 = t * T, nvalid = min(T, N - t0);
+    const size_t row0 = (size_t)unit * N + t0;
     __syncthreads();
     load_rows<IO>(Q + (size_t)unit * N * kD, t0, nvalid, xq);
     load_rows<IO>(dO + (size_t)unit * N * kDv, t0, nvalid, gs);
+    load_rows_ld<IO>(V + (size_t)unit * N * kDv, t0, nvalid, vs, kSP);
+    load_tile_rows<KC, KG>(dlk + row0 * K, nvalid, K, GK);
     __syncthreads();
-    gamma_tile(xq, nvalid, Pp, h, K, GQ);
-    load_rows<IO>(Kx + (size_t)unit * N * kD, t0, nvalid, xs);
-    load_rows<IO>(V + (size_t)unit * N * kDv, t0, nvalid, vs);
-    __syncthreads();
-    gamma_tile(xs, nvalid, Pp, h, K, GK);
-    // numerators [num | den - eps] of the causal output: gQ_i . S + sum_{j <= i} A_ij [v_j | 1]
-    for (int p = threadIdx.x; p < T * T; p += blockDim.x) {
-      const int i = p / T, j = p % T;
-      float a = 0.f;
-      if (j <= i)
-        for (int k = 0; k < K; ++k) a = fmaf(GQ[i * K + k], GK[j * K + k], a);
-      A[p] = a;
-    }
-    __syncthreads();
-    for (int p = threadIdx.x; p < T * kStateCols; p += blockDim.x) {
-      const int i = p / kStateCols, c = p % kStateCols;
-      float s = 0.f;
-      for (int k = 0; k < K; ++k) s = fmaf(GQ[i * K + k], S[k * kStateCols + c], s);
-      if (c < kDv) {
-        for (int j = 0; j <= i; ++j) s = fmaf(A[i * T + j], vs[j * kDv + c], s);
-      } else {
-        for (int j = 0; j <= i; ++j) s += A[i * T + j];
-      }
-      us[p] = s;
-    }
-    __syncthreads();
-    {  // one warp per row: O, G . O, then u (rows past N: zero)
-      const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-      for (int i = warp; i < T; i += nwarps) {
-        float* ui = us + i * kStateCols;
-        if (i >= nvalid) {
-          ui[lane] = 0.f;
-          ui[32 + lane] = 0.f;
-          if (lane == 0) ui[kDv] = 0.f;
-          continue;
-        }
-        const float den = ui[kDv] + eps;
-        const float o0 = ui[lane] / den, o1 = ui[32 + lane] / den;
-        float go = gs[i * kDv + lane] * o0 + gs[i * kDv + 32 + lane] * o1;
+    gamma_tile_kc<KC>(xq, nvalid, Pp, h, K, GQ);
+    store_rows<KC>(GQ, nvalid, K, gq + row0 * K);
+    {  // A, then [num | den] = gamma_Q [S | Z] + sum_{j <= i} A_ij [v_j | 1], then u = [dn | dd]
+      causal_tile_A<KC>(GQ, GK, i0, A);
+      __syncwarp();
+      float a[4][2], dp[4];
+      rows_times_image<KC>(GQ, S, i0, a);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) go += __shfl_xor_sync(0xffffffffu, go, o);
-        __syncwarp();
-        ui[lane] = gs[i * kDv + lane] / den;
-        ui[32 + lane] = gs[i * kDv + 32 + lane] / den;
-        if (lane == 0) ui[kDv] = -go / den;
+      for (int q = 0; q < 4; ++q) dp[q] = A[(i0 + q) * T + lane];
+#pragma unroll
+      for (int r = 0; r < RK; ++r) {
+        const float z = Z[lane + 32 * r];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) dp[q] = fmaf(GQ[(i0 + q) * KC + lane + 32 * r], z, dp[q]);
+      }
+#pragma unroll 4
+      for (int j = 0; j < T; ++j) {
+        const float v0 = vs[j * kSP + lane], v1 = vs[j * kSP + 32 + lane];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float aij = A[(i0 + q) * T + j];
+          a[q][0] = fmaf(aij, v0, a[q][0]);
+          a[q][1] = fmaf(aij, v1, a[q][1]);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int i = i0 + q;
+        const float den = warp_sum(dp[q]) + eps;
+        float n0 = 0.f, n1 = 0.f, dv = 0.f;
+        if (i < nvalid) {
+          const float g0 = gs[i * kDv + lane], g1 = gs[i * kDv + 32 + lane];
+          const float go = warp_sum(g0 * (a[q][0] / den) + g1 * (a[q][1] / den));
+          n0 = g0 / den;
+          n1 = g1 / den;
+          dv = -go / den;
+          float* ug = uglob + (row0 + i) * kStateCols;
+          ug[lane] = n0;
+          ug[32 + lane] = n1;
+          if (lane == 0) ug[kDv] = dv;
+        }
+        dn[i * kSP + lane] = n0;
+        dn[i * kSP + 32 + lane] = n1;
+        if (lane == 0) dd[i] = dv;
       }
     }
     __syncthreads();
-    float* ug = uglob + ((size_t)unit * N + t0) * kStateCols;
-    for (int p = threadIdx.x; p < nvalid * kStateCols; p += blockDim.x) ug[p] = us[p];
-    causal_tile_products(GQ, GK, us, vs, K, A, W);
-    __syncthreads();
-    for (int p = threadIdx.x; p < T * K; p += blockDim.x) {  // dgamma_Q = S u + sum_{j <= i} W_ij gK_j
-      const int i = p / K, k = p % K;
-      float s = 0.f;
-      for (int c = 0; c < kStateCols; ++c) s = fmaf(S[k * kStateCols + c], us[i * kStateCols + c], s);
-      for (int j = 0; j <= i; ++j) s = fmaf(W[i * T + j], GK[j * K + k], s);
-      dG[p] = s;
-    }
-    __syncthreads();
-    for (int p = threadIdx.x; p < npairs; p += blockDim.x) {  // segment aggregate and the running state
-      const int k = p / kStateCols, c = p % kStateCols;
-      float b = 0.f, a = 0.f;
-      for (int i = 0; i < T; ++i) b = fmaf(GQ[i * K + k], us[i * kStateCols + c], b);
-      if (c < kDv) {
-        for (int j = 0; j < T; ++j) a = fmaf(GK[j * K + k], vs[j * kDv + c], a);
-      } else {
-        for (int j = 0; j < T; ++j) a += GK[j * K + k];
+    accumulate_gt<KC>(GQ, dn, kSP, dd, bacc, bz);  // segment aggregate of gamma_Q u^T
+    causal_tile_W(dn, dd, vs, i0, W);
+    __syncwarp();
+    float b[4][RK];  // dgamma_Q = [S | Z] u + sum_{j <= i} W_ij gamma_Kj
+    rows_times_image_t<KC>(dn, kSP, S, i0, b);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+      for (int r = 0; r < RK; ++r) b[q][r] = fmaf(dd[i0 + q], Z[lane + 32 * r], b[q][r]);
+#pragma unroll 4
+    for (int j = 0; j < T; ++j) {
+      float g[RK];
+#pragma unroll
+      for (int r = 0; r < RK; ++r) g[r] = GK[j * KG + lane + 32 * r];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float wij = W[(i0 + q) * T + j];
+#pragma unroll
+        for (int r = 0; r < RK; ++r) b[q][r] = fmaf(wij, g[r], b[q][r]);
       }
-      bout[p] += b;
-      S[p] += a;
     }
+    softmax_backward_rows<KC>(GQ, i0, b);
+    __syncthreads();  // every warp is done with S, Z and gamma_Q
+    add_gt_to_image<KC, KG>(GK, vs, kSP, nullptr, S, Z);  // S += gamma_K^T [V | 1] over the tile
+    store_dl_rows<KC>(b, i0, nvalid, K, GQ, dlq + row0 * K);
     __syncthreads();
-    softmax_backward_tile(GQ, dG, K);
-    float* dst = dlq + ((size_t)unit * N + t0) * K;
-    for (int p = threadIdx.x; p < nvalid * K; p += blockDim.x) dst[p] = dG[p];
-    dx_tile<IO>(xq, dG, nvalid, mu, sigma2, h, K, dQ + ((size_t)unit * N + t0) * kD);
+    dx_tile_kc<IO, KC>(xq, GQ, nvalid, wpair + (size_t)h * K * kD, K, gs, dQ + row0 * kD);
   }
+  store_gt<KC>(bagg + ((size_t)unit * P + seg) * npairs, K, bacc, bz, 0);
 }
 
 // Exclusive suffix scan over segments: bagg[unit][p][e] <- sum_{p' > p} bagg[unit][p'][e].
@@ -661,86 +1029,106 @@ __global__ void simt_rscan_kernel(float* bagg, int P, int npairs) {
 }
 
 // Key side: grid (segments, B*H).  R starts at bagg[unit][seg] (suffix-scanned) and the segment's tiles are
-// walked last to first; writes dl_K, dK and dV.
-template <typename IO>
+// walked last to first; gamma_Q and u come from the query side, gamma_K from the aggregate pass (dlk, which
+// holds dl_K on exit); writes dK and dV.  Warp w owns tile rows 4w .. 4w + 3 (as queries in the in-tile
+// products, as keys after them).
+template <typename IO, int KC>
 __global__ void __launch_bounds__(kThreads) simt_bwd_causal_key_kernel(
-    const IO* __restrict__ Q, const IO* __restrict__ Kx, const IO* __restrict__ V, float* params,
-    const float* __restrict__ mu, const float* __restrict__ sigma2, int H, int N, int K, int seg_tiles, int P,
-    const float* bagg, const float* uglob, float* dlk, IO* __restrict__ dK, IO* __restrict__ dV) {
+    const IO* __restrict__ Kx, const IO* __restrict__ V, const float2* __restrict__ wpair, int H, int N, int K,
+    int seg_tiles, int P, const float* bagg, const float* uglob, const float* gq, float* dlk, IO* __restrict__ dK,
+    IO* __restrict__ dV) {
+  constexpr int RK = KC / 32, KG = KC + 4;
   extern __shared__ float sm[];
-  const int npairs = K * kStateCols;
-  float* R = sm;                   // [K][65]
-  float* xs = R + npairs;          // [T][64]  queries, then keys
-  float* vs = xs + T * kD;         // [T][64]
-  float* us = vs + T * kDv;        // [T][65]
-  float* GQ = us + T * kStateCols;  // [T][K]
-  float* GK = GQ + T * K;          // [T][K]
-  float* dG = GK + T * K;          // [T][K]
-  float* A = dG + T * K;           // [T][T]
-  float* W = A + T * T;            // [T][T]
+  float* R = sm;              // [KC][kSP]  running suffix image
+  float* Rz = R + KC * kSP;   // [KC]
+  float* xs = Rz + KC;        // [T][64]    key rows
+  float* vs = xs + T * kD;    // [T][kSP]   value rows, then the dx parameter stage
+  float* dn = vs + T * kSP;   // [T][kSP]   u rows (dv part)
+  float* dd = dn + T * kSP;   // [T]        u rows (normaliser part)
+  float* GQ = dd + T;         // [T][KC]    gamma_Q
+  float* GK = GQ + T * KC;    // [T][KG]    gamma_K, then dl_K
+  float* A = GK + T * KG;     // [T][T]
+  float* W = A + T * T;       // [T][T]
   const int unit = blockIdx.y, h = unit % H, seg = blockIdx.x;
-  const SimtParams Pp = params_at(params, H, K);
-  const float* R0 = bagg + ((size_t)unit * P + seg) * npairs;
-  for (int p = threadIdx.x; p < npairs; p += blockDim.x) R[p] = R0[p];
+  const int lane = threadIdx.x & 31, i0 = 4 * (threadIdx.x >> 5);
+  const size_t npairs = (size_t)K * kStateCols;
+  load_state_image<KC>(bagg + ((size_t)unit * P + seg) * npairs, K, R, Rz);
   const int tiles = (N + T - 1) / T;
   const int tb = seg * seg_tiles, te = min(tiles, tb + seg_tiles);
   for (int t = te - 1; t >= tb; --t) {
     const int t0 = t * T, nvalid = min(T, N - t0);
+    const size_t row0 = (size_t)unit * N + t0;
     __syncthreads();
-    load_rows<IO>(Q + (size_t)unit * N * kD, t0, nvalid, xs);
-    for (int p = threadIdx.x; p < T * kStateCols; p += blockDim.x)
-      us[p] = p < nvalid * kStateCols ? uglob[((size_t)unit * N + t0) * kStateCols + p] : 0.f;
-    __syncthreads();
-    gamma_tile(xs, nvalid, Pp, h, K, GQ);
     load_rows<IO>(Kx + (size_t)unit * N * kD, t0, nvalid, xs);
-    load_rows<IO>(V + (size_t)unit * N * kDv, t0, nvalid, vs);
-    __syncthreads();
-    gamma_tile(xs, nvalid, Pp, h, K, GK);
-    causal_tile_products(GQ, GK, us, vs, K, A, W);
-    __syncthreads();
-    for (int p = threadIdx.x; p < T * K; p += blockDim.x) {  // dgamma_K = R [v | 1] + sum_{i >= j} W_ij gQ_i
-      const int j = p / K, k = p % K;
-      float s = R[k * kStateCols + kDv];
-      for (int c = 0; c < kDv; ++c) s = fmaf(R[k * kStateCols + c], vs[j * kDv + c], s);
-      for (int i = j; i < T; ++i) s = fmaf(W[i * T + j], GQ[i * K + k], s);
-      dG[p] = s;
-    }
-    IO* dv_out = dV + ((size_t)unit * N + t0) * kDv;
-    for (int p = threadIdx.x; p < nvalid * kDv; p += blockDim.x) {  // dv = R^T gK + sum_{i >= j} A_ij dn_i
-      const int j = p / kDv, c = p % kDv;
-      float s = 0.f;
-      for (int k = 0; k < K; ++k) s = fmaf(GK[j * K + k], R[k * kStateCols + c], s);
-      for (int i = j; i < T; ++i) s = fmaf(A[i * T + j], us[i * kStateCols + c], s);
-      st_io<IO>(dv_out + p, s);
+    load_rows_ld<IO>(V + (size_t)unit * N * kDv, t0, nvalid, vs, kSP);
+    load_tile_rows<KC>(gq + row0 * K, nvalid, K, GQ);
+    load_tile_rows<KC, KG>(dlk + row0 * K, nvalid, K, GK);
+    for (int p = threadIdx.x; p < T * kStateCols; p += blockDim.x) {
+      const int i = p / kStateCols, c = p % kStateCols;
+      const float u = i < nvalid ? uglob[row0 * kStateCols + p] : 0.f;
+      if (c < kDv) dn[i * kSP + c] = u; else dd[i] = u;
     }
     __syncthreads();
-    for (int p = threadIdx.x; p < npairs; p += blockDim.x) {  // R += gamma_Q^T u over the whole tile
-      const int k = p / kStateCols, c = p % kStateCols;
-      float b = 0.f;
-      for (int i = 0; i < T; ++i) b = fmaf(GQ[i * K + k], us[i * kStateCols + c], b);
-      R[p] += b;
-    }
+    causal_tile_A<KC>(GQ, GK, i0, A);
+    causal_tile_W(dn, dd, vs, i0, W);
     __syncthreads();
-    softmax_backward_tile(GK, dG, K);
-    float* dst = dlk + ((size_t)unit * N + t0) * K;
-    for (int p = threadIdx.x; p < nvalid * K; p += blockDim.x) dst[p] = dG[p];
-    dx_tile<IO>(xs, dG, nvalid, mu, sigma2, h, K, dK + ((size_t)unit * N + t0) * kD);
+    float b[4][RK];  // dgamma_Kj = R [v_j | 1] + sum_{i >= j} W_ij gamma_Qi
+    rows_times_image_t<KC>(vs, kSP, R, i0, b);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+      for (int r = 0; r < RK; ++r) b[q][r] += Rz[lane + 32 * r];
+    float a[4][2];  // dv_j = R^T gamma_Kj + sum_{i >= j} A_ij dn_i
+    rows_times_image<KC, KG>(GK, R, i0, a);
+#pragma unroll 4
+    for (int i = 0; i < T; ++i) {
+      float g[RK];
+#pragma unroll
+      for (int r = 0; r < RK; ++r) g[r] = GQ[i * KC + lane + 32 * r];
+      const float d0 = dn[i * kSP + lane], d1 = dn[i * kSP + 32 + lane];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float wij = W[i * T + i0 + q], aij = A[i * T + i0 + q];
+#pragma unroll
+        for (int r = 0; r < RK; ++r) b[q][r] = fmaf(wij, g[r], b[q][r]);
+        a[q][0] = fmaf(aij, d0, a[q][0]);
+        a[q][1] = fmaf(aij, d1, a[q][1]);
+      }
+    }
+    IO* dv_out = dV + row0 * kDv;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (i0 + q < nvalid) {
+        st_io<IO>(dv_out + (i0 + q) * kDv + lane, a[q][0]);
+        st_io<IO>(dv_out + (i0 + q) * kDv + 32 + lane, a[q][1]);
+      }
+    softmax_backward_rows<KC, KG>(GK, i0, b);
+    __syncthreads();  // every warp is done with R, Rz, gamma_Q and the value rows
+    add_gt_to_image<KC, KC>(GQ, dn, kSP, dd, R, Rz);  // R += gamma_Q^T u over the tile
+    store_dl_rows<KC, KG>(b, i0, nvalid, K, GK, dlk + row0 * K);
+    __syncthreads();
+    dx_tile_kc<IO, KC, KG>(xs, GK, nvalid, wpair + (size_t)h * K * kD, K, vs, dK + row0 * kD);
   }
 }
 
-// Parameter-gradient sums: grid (ceil(K / 32), H, chunks).  Thread (k within a block of 32, group of 8
-// dims) sums dl_k (x_d - mu_kd) and dl_k (x_d - mu_kd)^2 over its chunk of the head's rows (queries
-// then keys of every batch entry) and adds them into pacc[h][k][d][2] (and b_k into pb[h][k]).
+// Parameter-gradient sums: grid (ceil(K / 32), H, ctas).  The rows of head h (queries then keys of every
+// batch entry, 2 B N in all) are split into ranges of rows_per_cta; a CTA walks its range in tiles of at
+// most T rows that stay within one (side, batch entry) and loads the next tile into registers while it
+// works on the current one.  Thread (k within a block of 32, group of 8 dims) sums dl_k (x_d - mu_kd)
+// and dl_k (x_d - mu_kd)^2 and adds them into pacc[h][k][d][2] (and b_k into pb[h][k]).
 template <typename IO>
 __global__ void __launch_bounds__(kThreads) simt_bwd_param_kernel(const IO* __restrict__ Q, const IO* __restrict__ Kx,
                                                                   const float* __restrict__ mu, const float* dlq,
                                                                   const float* dlk, int B, int H, int N, int K,
-                                                                  int rows_per_chunk, float* pacc, float* pb) {
-  __shared__ float xs[T * kD];
+                                                                  long long rows_per_cta, float* pacc, float* pb) {
+  __shared__ __align__(16) float xs[T * kD];
   __shared__ float ds[T * 32];
   const int h = blockIdx.y, k0 = blockIdx.x * 32;
   const int kl = threadIdx.x & 31, dg = threadIdx.x >> 5;  // 8 groups of 8 dims
   const int k = k0 + kl;
+  const int fi = threadIdx.x >> 3, fc = threadIdx.x & 7;  // fetch: row fi, dims 8 fc .. 8 fc + 7, dl 4 fc .. 4 fc + 3
+  const long long total = 2LL * B * N;
+  const long long r0 = (long long)blockIdx.z * rows_per_cta, r1 = min(total, r0 + rows_per_cta);
   float m[8], a1[8], a2[8], bsum = 0.f;
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
@@ -748,40 +1136,46 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_param_kernel(const IO* __re
     a1[q] = 0.f;
     a2[q] = 0.f;
   }
-  const long long total = 2LL * B * N;  // rows of this head: queries then keys, batch-major
-  const long long r0 = (long long)blockIdx.z * rows_per_chunk, r1 = min(total, r0 + rows_per_chunk);
-  for (long long rb = r0; rb < r1; rb += T) {
-    const int n = (int)min((long long)T, r1 - rb);
-    __syncthreads();
-    for (int p = threadIdx.x; p < T * kD; p += blockDim.x) {
-      const int i = p / kD, j = p % kD;
-      float x = 0.f;
-      if (i < n) {
-        const long long r = rb + i, side = r / ((long long)B * N), rr = r % ((long long)B * N);
-        const long long b = rr / N, tok = rr % N, unit = b * H + h;
-        const IO* src = side == 0 ? Q : Kx;
-        x = ld_io<IO>(src + ((size_t)unit * N + tok) * kD + j);
-      }
-      xs[p] = x;
+  // the tile starting at virtual row rb: its row count, and this thread's share of x and dl
+  auto fetch = [&](long long rb, int& n, float (&xv)[8], float (&dv)[4]) {
+    const long long sb = rb / N;  // side * B + b
+    const int n0 = (int)(rb - sb * N), side = (int)(sb / B), b = (int)(sb % B);
+    n = (int)min((long long)min(T, N - n0), r1 - rb);
+    const size_t row = ((size_t)b * H + h) * N + n0 + fi;
+    const bool ok = fi < n;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) xv[t] = 0.f;
+    if (ok) load8<IO>((side == 0 ? Q : Kx) + row * kD + 8 * fc, xv);
+    const float* dsrc = (side == 0 ? dlq : dlk) + row * K;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int kk = k0 + 4 * fc + t;
+      dv[t] = ok && kk < K ? dsrc[kk] : 0.f;
     }
-    for (int p = threadIdx.x; p < T * 32; p += blockDim.x) {
-      const int i = p / 32, kk = k0 + (p % 32);
-      float v = 0.f;
-      if (i < n && kk < K) {
-        const long long r = rb + i, side = r / ((long long)B * N), rr = r % ((long long)B * N);
-        const long long b = rr / N, tok = rr % N, unit = b * H + h;
-        const float* src = side == 0 ? dlq : dlk;
-        v = src[((size_t)unit * N + tok) * K + kk];
-      }
-      ds[p] = v;
-    }
+  };
+  int n = 0;
+  float xv[8], dv[4];
+  if (r0 < r1) fetch(r0, n, xv, dv);
+  for (long long rb = r0; rb < r1;) {
+    const int ncur = n;
+    __syncthreads();  // the previous tile's readers are done
+    *reinterpret_cast<float4*>(xs + fi * kD + 8 * fc) = make_float4(xv[0], xv[1], xv[2], xv[3]);
+    *reinterpret_cast<float4*>(xs + fi * kD + 8 * fc + 4) = make_float4(xv[4], xv[5], xv[6], xv[7]);
+#pragma unroll
+    for (int t = 0; t < 4; ++t) ds[fi * 32 + 4 * fc + t] = dv[t];
     __syncthreads();
-    for (int i = 0; i < n; ++i) {
+    rb += ncur;
+    if (rb < r1) fetch(rb, n, xv, dv);  // in flight while this tile is summed
+#pragma unroll 4
+    for (int i = 0; i < ncur; ++i) {
       const float dl = ds[i * 32 + kl];
-      if (dg == 0) bsum += dl;
+      bsum += dl;
+      const float4 x0 = *reinterpret_cast<const float4*>(xs + i * kD + dg * 8);
+      const float4 x1 = *reinterpret_cast<const float4*>(xs + i * kD + dg * 8 + 4);
+      const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
-        const float diff = xs[i * kD + dg * 8 + q] - m[q];
+        const float diff = x[q] - m[q];
         const float t = dl * diff;
         a1[q] += t;
         a2[q] = fmaf(t, diff, a2[q]);
@@ -995,22 +1389,31 @@ __global__ void __launch_bounds__(kDecodeThreads) simt_decode_kernel(const IO* _
 }  // namespace
 
 // Workspace of the backward pass.  Bidirectional: control block | parameters | Vt|Z | dVt|dZ |
-// parameter sums | dl of the queries | dl of the keys (the three accumulators contiguous, zeroed
-// together).  Causal: control block | parameters | segment aggregates of the keys (scanned: S at each
-// segment start) | segment aggregates of the queries' gamma_Q u^T (suffix-scanned: R after each
-// segment) | parameter sums | u rows | dl of the queries | dl of the keys.
+// parameter sums | dl of the queries | dl of the keys (gamma_K until the key side) | (1 / sigma2,
+// mu / sigma2) pairs (the three accumulators contiguous, zeroed together).  Causal: control block |
+// parameters | segment aggregates of the keys (scanned: S at each segment start) | segment aggregates of
+// the queries' gamma_Q u^T (suffix-scanned: R after each segment) | parameter sums | u rows | dl of the
+// queries | dl of the keys (gamma_K until the key side) | pairs | gamma_Q.
 struct BwdPlan {
-  size_t off_params, off_state, off_dstate, off_pacc, off_pb, off_u, off_dlq, off_dlk, total;
+  size_t off_params, off_state, off_dstate, off_pacc, off_pb, off_u, off_dlq, off_dlk, off_wpair, off_gq, total;
   int splits, seg_tiles, tiles;
 };
 BwdPlan bwd_plan(const gma_problem_t& p, bool causal) {
   BwdPlan b{};
   const SimtPlan sp = simt_plan(p, causal ? GMA_OP_CAUSAL : GMA_OP_BIDIR);
   const size_t BH = (size_t)p.B * p.H, npairs = (size_t)p.K * kStateCols;
-  const size_t nstate = causal ? BH * sp.splits * npairs : BH * npairs;
+  b.tiles = sp.tiles;
   b.splits = sp.splits;
   b.seg_tiles = sp.seg_tiles;
-  b.tiles = sp.tiles;
+  if (causal) {  // one wave of the causal query / key kernels: two CTAs per SM, one when K > 128
+    const int units = kc_class(p.K) <= 128 ? kTargetUnits : kTargetUnits / 2;
+    const int nt = b.tiles > 0 ? b.tiles : 1;
+    int want = units / (int)(BH > 0 ? BH : 1);
+    want = want < 1 ? 1 : (want > nt ? nt : want);
+    b.seg_tiles = cdiv(nt, want);
+    b.splits = cdiv(nt, b.seg_tiles);
+  }
+  const size_t nstate = causal ? BH * b.splits * npairs : BH * npairs;
   b.off_params = sp.off_params;
   b.off_state = align_up(sp.off_params + ((size_t)2 * p.H * kD * p.K + (size_t)p.H * p.K) * sizeof(float));
   b.off_dstate = b.off_state + nstate * sizeof(float);
@@ -1019,8 +1422,109 @@ BwdPlan bwd_plan(const gma_problem_t& p, bool causal) {
   b.off_u = align_up(b.off_pb + (size_t)p.H * p.K * sizeof(float));
   b.off_dlq = align_up(b.off_u + (causal ? BH * p.N * kStateCols * sizeof(float) : 0));
   b.off_dlk = align_up(b.off_dlq + BH * p.N * p.K * sizeof(float));
-  b.total = align_up(b.off_dlk + BH * p.N * p.K * sizeof(float));
+  b.off_wpair = align_up(b.off_dlk + BH * p.N * p.K * sizeof(float));
+  b.off_gq = align_up(b.off_wpair + (size_t)p.H * p.K * kD * sizeof(float2));
+  b.total = align_up(b.off_gq + (causal ? BH * p.N * p.K * sizeof(float) : 0));
   return b;
+}
+
+// Splits of a per-(b, h) tile loop that fill the GPU in one wave: the resident CTAs of `func` on every SM,
+// shared among the B*H units.
+gma_status_t fill_splits(const void* func, size_t smem, int BH, int tiles, int* splits, int* seg_tiles) {
+  int dev = 0, nsm = 0, occ = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, func, kThreads, smem) != cudaSuccess)
+    return cuda_fail("occupancy query", cudaSuccess, func);
+  const int nt = tiles > 0 ? tiles : 1;
+  int want = nsm * (occ > 0 ? occ : 1) / (BH > 0 ? BH : 1);
+  want = want < 1 ? 1 : (want > nt ? nt : want);
+  *seg_tiles = cdiv(nt, want);
+  *splits = cdiv(nt, *seg_tiles);
+  return GMA_OK;
+}
+
+// Write phase / segment aggregates (simt_write_kernel) for the KC class of K.
+template <typename IO, int KC>
+gma_status_t launch_write_kc(int splits, int BH, cudaStream_t st, const IO* Kx, const IO* V, float* params, int H,
+                             int N, int K, int seg_tiles, float* state, int atomic, float* gout = nullptr) {
+  const size_t sm = (size_t)(T * kD + T * kDv + T * KC) * sizeof(float);
+  const auto kfn = simt_write_kernel<IO, KC>;
+  if (set_smem_optin((const void*)kfn, (int)sm, 1) != GMA_OK) return GMA_ERR_CUDA;
+  GMA_LAUNCH("simt_write", kfn, dim3(splits, BH), kThreads, sm, st, Kx, V, params, H, N, K, seg_tiles, splits,
+             state, atomic, gout);
+  return check_launch("launch simt_write", (const void*)kfn);
+}
+
+template <typename IO>
+gma_status_t launch_write(int splits, int BH, cudaStream_t st, const IO* Kx, const IO* V, float* params, int H, int N,
+                          int K, int seg_tiles, float* state, int atomic) {
+  switch (kc_class(K)) {
+    case 32: return launch_write_kc<IO, 32>(splits, BH, st, Kx, V, params, H, N, K, seg_tiles, state, atomic);
+    case 64: return launch_write_kc<IO, 64>(splits, BH, st, Kx, V, params, H, N, K, seg_tiles, state, atomic);
+    case 128: return launch_write_kc<IO, 128>(splits, BH, st, Kx, V, params, H, N, K, seg_tiles, state, atomic);
+    default: return launch_write_kc<IO, 256>(splits, BH, st, Kx, V, params, H, N, K, seg_tiles, state, atomic);
+  }
+}
+
+// Bidirectional backward after the parameter fold: write (Vt | Z), the query side, the key side; each
+// loop sized to fill the GPU.
+template <typename IO, int KC>
+gma_status_t backward_bidir_kc(const gma_problem_t& p, const IO* Q, const IO* Kx, const IO* V, const IO* dO, IO* dQ,
+                               IO* dK, IO* dV, float* params, const float2* wpair, float* state, float* dstate,
+                               float* dlq, float* dlk, cudaStream_t st) {
+  const int BH = p.B * p.H, K = p.K, tiles = cdiv(p.N, T);
+  int splits = 1, seg = 1;
+  const size_t sm_w = (size_t)(T * kD + T * kDv + T * KC) * sizeof(float);
+  const auto wfn = simt_write_kernel<IO, KC>;
+  if (gma_status_t e = fill_splits((const void*)wfn, sm_w, BH, tiles, &splits, &seg)) return e;
+  if (gma_status_t e = launch_write_kc<IO, KC>(splits, BH, st, Kx, V, params, p.H, p.N, K, seg, state, 1, dlk))
+    return e;
+  const size_t sm_q = (size_t)(KC * kSP + KC + T * kD + T * kDv + T * kSP + T + T * KC) * sizeof(float);
+  const auto qfn = simt_bwd_query_kernel<IO, KC>;
+  if (set_smem_optin((const void*)qfn, (int)sm_q, 5) != GMA_OK) return GMA_ERR_CUDA;
+  if (gma_status_t e = fill_splits((const void*)qfn, sm_q, BH, tiles, &splits, &seg)) return e;
+  GMA_LAUNCH("simt_bwd_query", qfn, dim3(splits, BH), kThreads, sm_q, st, Q, dO, params, wpair, p.H, p.N, K, seg,
+             state, p.eps, dstate, dlq, dQ);
+  if (gma_status_t e = check_launch("launch simt_bwd_query", (const void*)qfn)) return e;
+  const size_t sm_k = (size_t)(KC * kSP + KC + T * kD + T * kDv + T * KC) * sizeof(float);
+  const auto kkfn = simt_bwd_key_kernel<IO, KC>;
+  if (set_smem_optin((const void*)kkfn, (int)sm_k, 6) != GMA_OK) return GMA_ERR_CUDA;
+  if (gma_status_t e = fill_splits((const void*)kkfn, sm_k, BH, tiles, &splits, &seg)) return e;
+  GMA_LAUNCH("simt_bwd_key", kkfn, dim3(splits, BH), kThreads, sm_k, st, Kx, V, wpair, p.H, p.N, K, seg,
+             dstate, dlk, dK, dV);
+  return check_launch("launch simt_bwd_key", (const void*)kkfn);
+}
+
+// Causal backward after the parameter fold: segment aggregates (+ every key's gamma_K into dlk), scan,
+// query side (u, gamma_Q, dl_Q, dQ, the queries' segment aggregates), suffix scan, key side (dl_K, dK, dV).
+template <typename IO, int KC>
+gma_status_t backward_causal_kc(const gma_problem_t& p, const BwdPlan& b, const IO* Q, const IO* Kx, const IO* V,
+                                const IO* dO, IO* dQ, IO* dK, IO* dV, float* params, const float2* wpair, float* state,
+                                float* dstate, float* urows, float* gq, float* dlq, float* dlk, cudaStream_t st) {
+  constexpr int KG = KC + 4;
+  const int BH = p.B * p.H, K = p.K, npairs = K * kStateCols;
+  if (gma_status_t e = launch_write_kc<IO, KC>(b.splits, BH, st, Kx, V, params, p.H, p.N, K, b.seg_tiles, state, 0,
+                                               dlk))
+    return e;
+  GMA_LAUNCH("simt_scan", simt_scan_kernel, dim3(cdiv(npairs, 256), BH), 256, 0, st, state, b.splits, npairs);
+  if (gma_status_t e = check_launch("launch simt_scan", (const void*)simt_scan_kernel)) return e;
+  const size_t sm_q =
+      (size_t)(KC * kSP + KC + T * kD + T * kDv + 2 * T * kSP + T + T * KC + T * KG + 2 * T * T) * sizeof(float);
+  const auto qfn = simt_bwd_causal_query_kernel<IO, KC>;
+  if (set_smem_optin((const void*)qfn, (int)sm_q, 7) != GMA_OK) return GMA_ERR_CUDA;
+  GMA_LAUNCH("simt_bwd_causal_query", qfn, dim3(b.splits, BH), kThreads, sm_q, st, Q, V, dO, params, wpair, p.H, p.N,
+             K, b.seg_tiles, b.splits, state, p.eps, dstate, urows, gq, dlk, dlq, dQ);
+  if (gma_status_t e = check_launch("launch simt_bwd_causal_query", (const void*)qfn)) return e;
+  GMA_LAUNCH("simt_rscan", simt_rscan_kernel, dim3(cdiv(npairs, 256), BH), 256, 0, st, dstate, b.splits, npairs);
+  if (gma_status_t e = check_launch("launch simt_rscan", (const void*)simt_rscan_kernel)) return e;
+  const size_t sm_k =
+      (size_t)(KC * kSP + KC + T * kD + 2 * T * kSP + T + T * KC + T * KG + 2 * T * T) * sizeof(float);
+  const auto kfn = simt_bwd_causal_key_kernel<IO, KC>;
+  if (set_smem_optin((const void*)kfn, (int)sm_k, 8) != GMA_OK) return GMA_ERR_CUDA;
+  GMA_LAUNCH("simt_bwd_causal_key", kfn, dim3(b.splits, BH), kThreads, sm_k, st, Kx, V, wpair, p.H, p.N, K,
+             b.seg_tiles, b.splits, dstate, urows, gq, dlk, dK, dV);
+  return check_launch("launch simt_bwd_causal_key", (const void*)kfn);
 }
 
 template <typename IO>
@@ -1037,55 +1541,70 @@ gma_status_t backward_typed(const gma_problem_t& p, bool causal, const IO* Q, co
   float* urows = (float*)(base + b.off_u);
   float* dlq = (float*)(base + b.off_dlq);
   float* dlk = (float*)(base + b.off_dlk);
-  const int BH = p.B * p.H, K = p.K, npairs = K * kStateCols;
+  float2* wpair = (float2*)(base + b.off_wpair);
+  float* gq = (float*)(base + b.off_gq);
+  const int K = p.K;
   // bidirectional: zero Vt|Z, dVt|dZ and the parameter sums; causal: the parameter sums (the segment
   // aggregates are stored whole)
   float* zero = causal ? pacc : state;
   const size_t zero_n = (b.off_u - (causal ? b.off_pacc : b.off_state)) / sizeof(float);
   GMA_LAUNCH("simt_prep", simt_prep_kernel, 148, 256, 0, st, mu, sigma2, log_pi, p.H, K, params, (Ctrl*)base, zero,
-             zero_n);
+             zero_n, wpair);
   if (gma_status_t e = check_launch("launch simt_prep", (const void*)simt_prep_kernel)) return e;
   if (p.N > 0) {
-    const size_t sm_write = (size_t)(T * kD + T * kDv + T * K + npairs) * sizeof(float);
-    if (set_smem_optin((const void*)simt_write_kernel<IO>, (int)sm_write, 1) != GMA_OK) return GMA_ERR_CUDA;
-    GMA_LAUNCH("simt_write", simt_write_kernel<IO>, dim3(b.splits, BH), kThreads, sm_write, st, Kx, V, params, p.H,
-               p.N, K, b.seg_tiles, b.splits, state, causal ? 0 : 1);
-    if (gma_status_t e = check_launch("launch simt_write", (const void*)simt_write_kernel<IO>)) return e;
     if (causal) {
-      GMA_LAUNCH("simt_scan", simt_scan_kernel, dim3(cdiv(npairs, 256), BH), 256, 0, st, state, b.splits, npairs);
-      if (gma_status_t e = check_launch("launch simt_scan", (const void*)simt_scan_kernel)) return e;
-      const size_t sm_q = (size_t)(npairs + 3 * T * kD + T * kStateCols + 3 * T * K + 2 * T * T) * sizeof(float);
-      if (set_smem_optin((const void*)simt_bwd_causal_query_kernel<IO>, (int)sm_q, 7) != GMA_OK) return GMA_ERR_CUDA;
-      GMA_LAUNCH("simt_bwd_causal_query", simt_bwd_causal_query_kernel<IO>, dim3(b.splits, BH), kThreads, sm_q, st, Q,
-                 Kx, V, dO, params, mu, sigma2, p.H, p.N, K, b.seg_tiles, b.splits, state, p.eps, dstate, urows, dlq,
-                 dQ);
-      if (gma_status_t e = check_launch("launch simt_bwd_causal_query", (const void*)simt_bwd_causal_query_kernel<IO>))
-        return e;
-      GMA_LAUNCH("simt_rscan", simt_rscan_kernel, dim3(cdiv(npairs, 256), BH), 256, 0, st, dstate, b.splits, npairs);
-      if (gma_status_t e = check_launch("launch simt_rscan", (const void*)simt_rscan_kernel)) return e;
-      const size_t sm_k = (size_t)(npairs + 2 * T * kD + T * kStateCols + 3 * T * K + 2 * T * T) * sizeof(float);
-      if (set_smem_optin((const void*)simt_bwd_causal_key_kernel<IO>, (int)sm_k, 8) != GMA_OK) return GMA_ERR_CUDA;
-      GMA_LAUNCH("simt_bwd_causal_key", simt_bwd_causal_key_kernel<IO>, dim3(b.splits, BH), kThreads, sm_k, st, Q, Kx,
-                 V, params, mu, sigma2, p.H, p.N, K, b.seg_tiles, b.splits, dstate, urows, dlk, dK, dV);
-      if (gma_status_t e = check_launch("launch simt_bwd_causal_key", (const void*)simt_bwd_causal_key_kernel<IO>))
-        return e;
+      gma_status_t e;
+      switch (kc_class(K)) {
+        case 32:
+          e = backward_causal_kc<IO, 32>(p, b, Q, Kx, V, dO, dQ, dK, dV, params, wpair, state, dstate, urows, gq, dlq,
+                                         dlk, st);
+          break;
+        case 64:
+          e = backward_causal_kc<IO, 64>(p, b, Q, Kx, V, dO, dQ, dK, dV, params, wpair, state, dstate, urows, gq, dlq,
+                                         dlk, st);
+          break;
+        case 128:
+          e = backward_causal_kc<IO, 128>(p, b, Q, Kx, V, dO, dQ, dK, dV, params, wpair, state, dstate, urows, gq, dlq,
+                                          dlk, st);
+          break;
+        default:
+          e = backward_causal_kc<IO, 256>(p, b, Q, Kx, V, dO, dQ, dK, dV, params, wpair, state, dstate, urows, gq, dlq,
+                                          dlk, st);
+      }
+      if (e != GMA_OK) return e;
     } else {
-      const size_t sm_q = (size_t)(2 * npairs + T * kD + T * kDv + T * kStateCols + 2 * T * K) * sizeof(float);
-      if (set_smem_optin((const void*)simt_bwd_query_kernel<IO>, (int)sm_q, 5) != GMA_OK) return GMA_ERR_CUDA;
-      GMA_LAUNCH("simt_bwd_query", simt_bwd_query_kernel<IO>, dim3(b.splits, BH), kThreads, sm_q, st, Q, dO, params,
-                 mu, sigma2, p.H, p.N, K, b.seg_tiles, state, p.eps, dstate, dlq, dQ);
-      if (gma_status_t e = check_launch("launch simt_bwd_query", (const void*)simt_bwd_query_kernel<IO>)) return e;
-      const size_t sm_k = (size_t)(npairs + T * kD + T * kDv + 2 * T * K) * sizeof(float);
-      if (set_smem_optin((const void*)simt_bwd_key_kernel<IO>, (int)sm_k, 6) != GMA_OK) return GMA_ERR_CUDA;
-      GMA_LAUNCH("simt_bwd_key", simt_bwd_key_kernel<IO>, dim3(b.tiles, BH), kThreads, sm_k, st, Kx, V, params, mu,
-                 sigma2, p.H, p.N, K, dstate, dlk, dK, dV);
-      if (gma_status_t e = check_launch("launch simt_bwd_key", (const void*)simt_bwd_key_kernel<IO>)) return e;
+      gma_status_t e;
+      switch (kc_class(K)) {
+        case 32:
+          e = backward_bidir_kc<IO, 32>(p, Q, Kx, V, dO, dQ, dK, dV, params, wpair, state, dstate, dlq, dlk, st);
+          break;
+        case 64:
+          e = backward_bidir_kc<IO, 64>(p, Q, Kx, V, dO, dQ, dK, dV, params, wpair, state, dstate, dlq, dlk, st);
+          break;
+        case 128:
+          e = backward_bidir_kc<IO, 128>(p, Q, Kx, V, dO, dQ, dK, dV, params, wpair, state, dstate, dlq, dlk, st);
+          break;
+        default:
+          e = backward_bidir_kc<IO, 256>(p, Q, Kx, V, dO, dQ, dK, dV, params, wpair, state, dstate, dlq, dlk, st);
+      }
+      if (e != GMA_OK) return e;
     }
-    const int rows_per_chunk = 2048;
+    // parameter sums: one wave of CTAs over the 2 B N rows of every head
+    int dev = 0, nsm = 0, occ = 0;
+    const auto pfn = simt_bwd_param_kernel<IO>;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, pfn, kThreads, 0) != cudaSuccess)
+      return cuda_fail("occupancy query", cudaSuccess, (const void*)pfn);
     const long long rows = 2LL * p.B * p.N;
-    const dim3 grid_p(cdiv(K, 32), p.H, cdiv(rows, rows_per_chunk));
-    GMA_LAUNCH("simt_bwd_param", simt_bwd_param_kernel<IO>, grid_p, kThreads, 0, st, Q, Kx, mu, dlq, dlk, p.B, p.H, p.N,
-               K, rows_per_chunk, pacc, pb);
+    const int per_head = cdiv(K, 32) * p.H;
+    long long ctas = (long long)nsm * (occ > 0 ? occ : 1) / per_head;
+    ctas = ctas < 1 ? 1 : (ctas > 65535 ? 65535 : ctas);
+    long long rows_per_cta = (rows + ctas - 1) / ctas;
+    rows_per_cta = (rows_per_cta + T - 1) / T * T;
+    const dim3 grid_p(cdiv(K, 32), p.H, (unsigned)((rows + rows_per_cta - 1) / rows_per_cta));
+    GMA_LAUNCH("simt_bwd_param", pfn, grid_p, kThreads, 0, st, Q, Kx, mu, dlq, dlk, p.B, p.H, p.N, K, rows_per_cta,
+               pacc, pb);
     if (gma_status_t e = check_launch("launch simt_bwd_param", (const void*)simt_bwd_param_kernel<IO>)) return e;
   }
   GMA_LAUNCH("simt_bwd_param_finish", simt_bwd_param_finish_kernel, 148, 256, 0, st, sigma2, pacc, pb, p.H, K, dmu,
@@ -1142,7 +1661,8 @@ gma_status_t run_typed(const gma_problem_t& p, gma_op_t op, int Nk, const IO* Q,
   const bool write_only = op == GMA_OP_CAUSAL_STATE;  // state of all N keys, copied to `out`
   if (write_only) op = GMA_OP_BIDIR;
   const size_t zero_n = op == GMA_OP_BIDIR ? (size_t)BH * npairs : 0;
-  GMA_LAUNCH("simt_prep", simt_prep_kernel, 148, 256, 0, st, mu, sigma2, log_pi, p.H, K, params, ctrl, state, zero_n);
+  GMA_LAUNCH("simt_prep", simt_prep_kernel, 148, 256, 0, st, mu, sigma2, log_pi, p.H, K, params, ctrl, state, zero_n,
+             nullptr);
   if (cudaGetLastError() != cudaSuccess) return GMA_ERR_CUDA;
   if (p.N == 0 && !write_only) return GMA_OK;
   const size_t sm_gamma = (size_t)(T * kD + T * K) * sizeof(float);
@@ -1151,17 +1671,14 @@ gma_status_t run_typed(const gma_problem_t& p, gma_op_t op, int Nk, const IO* Q,
     GMA_LAUNCH("simt_resp", simt_resp_kernel<IO>, dim3(pl.tiles, BH), kThreads, sm_gamma, st, Q, params, p.H, p.N, K, (float*)out);
     return cudaGetLastError() == cudaSuccess ? GMA_OK : GMA_ERR_CUDA;
   }
-  const size_t sm_write = (size_t)(T * kD + T * kDv + T * K + npairs) * sizeof(float);
-  if (set_smem_optin((const void*)simt_write_kernel<IO>, (int)sm_write, 1) != GMA_OK) return GMA_ERR_CUDA;
   if (op == GMA_OP_BIDIR) {
     // write over the Nk keys (its own split plan; the workspace layout does not depend on N)
     if (Nk > 0) {
       gma_problem_t pk = p;
       pk.N = Nk;
       const SimtPlan plk = simt_plan(pk, op);
-      GMA_LAUNCH("simt_write", simt_write_kernel<IO>, dim3(plk.splits, BH), kThreads, sm_write, st, Kx, V, params, p.H, Nk, K,
-                 plk.seg_tiles, plk.splits, state, 1);
-      if (cudaGetLastError() != cudaSuccess) return GMA_ERR_CUDA;
+      if (gma_status_t e = launch_write<IO>(plk.splits, BH, st, Kx, V, params, p.H, Nk, K, plk.seg_tiles, state, 1))
+        return e;
     }
     if (write_only) {  // the accumulator already has the public state layout [B*H][K][dv + 1]
       if (cudaMemcpyAsync(out, state, (size_t)BH * npairs * sizeof(float), cudaMemcpyDeviceToDevice, st) != cudaSuccess)
@@ -1175,9 +1692,8 @@ gma_status_t run_typed(const gma_problem_t& p, gma_op_t op, int Nk, const IO* Q,
     return cudaGetLastError() == cudaSuccess ? GMA_OK : GMA_ERR_CUDA;
   }
   // causal
-  GMA_LAUNCH("simt_write", simt_write_kernel<IO>, dim3(pl.splits, BH), kThreads, sm_write, st, Kx, V, params, p.H, p.N, K, pl.seg_tiles,
-                                                                         pl.splits, state, 0);
-  if (cudaGetLastError() != cudaSuccess) return GMA_ERR_CUDA;
+  if (gma_status_t e = launch_write<IO>(pl.splits, BH, st, Kx, V, params, p.H, p.N, K, pl.seg_tiles, state, 0))
+    return e;
   GMA_LAUNCH("simt_scan", simt_scan_kernel, dim3(cdiv(npairs, 256), BH), 256, 0, st, state, pl.splits, npairs);
   if (cudaGetLastError() != cudaSuccess) return GMA_ERR_CUDA;
   const size_t sm_causal = (size_t)(npairs + T * kD + T * kDv + 2 * T * K + T * T + T * kStateCols) * sizeof(float);

@@ -50,7 +50,7 @@ def check(gma, inp, eps=1e-6, seed=0, causal=False):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("K", [3, 17, 64])
+@pytest.mark.parametrize("K", [3, 17, 64, 100, 128])
 def test_backward_small(gma, dtype, K):
     check(gma, make_inputs(2, 3, 150, K, dtype=dtype, seed=200 + K), seed=K)
 
@@ -80,7 +80,7 @@ def test_backward_zero_length(gma):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("K", [3, 17, 64])
+@pytest.mark.parametrize("K", [3, 17, 64, 100, 128])
 def test_causal_backward_small(gma, dtype, K):
     check(gma, make_inputs(2, 3, 150, K, dtype=dtype, seed=400 + K), seed=K, causal=True)
 
