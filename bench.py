@@ -470,7 +470,7 @@ def run_gma(args, world, rank, local):
         extensions["decode_bf16_B8H12K256_1token"] = {
             "us_per_step": t_step * 1e6, "tok_heads_per_s": Bd * Hd / t_step, "state_bytes_per_step": state_bytes,
             "hbm_bound_us": t_hbm * 1e6, "frac_of_hbm_bound": t_hbm / t_step,
-            "launches_per_step": 1, "timing": how}
+            "launches_per_step": 2, "timing": how}
         del di, state, wsd, toks, outd
         # Transformer-block form at the language-model block shape: projection GEMM + layout + causal forward
         from gaussian_mixture_sequence_gma_gb300.inputs import make_projected_inputs

@@ -74,7 +74,7 @@ size_t required_bytes(const gma_problem_t& p, gma_op_t op) {
   if (op == GMA_OP_PROJECTED_BIDIR || op == GMA_OP_PROJECTED_CAUSAL)
     return proj_layout(p, op == GMA_OP_PROJECTED_CAUSAL).total;
   if (op == GMA_OP_CROSS) op = GMA_OP_BIDIR;  // the same workspace: it does not depend on N
-  if (op == GMA_OP_CAUSAL_DECODE) return align_up(sizeof(Ctrl));  // a control block; the kernel needs no scratch
+  if (op == GMA_OP_CAUSAL_DECODE) return simt_decode_bytes(p);
   if (op == GMA_OP_BACKWARD_BIDIR || op == GMA_OP_BACKWARD_CAUSAL) return simt_backward_bytes(p, op == GMA_OP_BACKWARD_CAUSAL);
   if (p.dtype == GMA_BF16) return tc_plan(p, op).total;
   return simt_plan(p, op).total;

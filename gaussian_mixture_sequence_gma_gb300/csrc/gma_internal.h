@@ -65,7 +65,9 @@ size_t simt_backward_bytes(const gma_problem_t& p, bool causal);
 gma_status_t simt_backward(const gma_problem_t& p, bool causal, const void* Q, const void* K, const void* V, const float* mu,
                            const float* sigma2, const float* log_pi, const void* dO, void* dQ, void* dK, void* dV,
                            float* dmu, float* dsigma2, float* dlog_pi, void* ws, cudaStream_t stream);
-// Decode T = p.N new tokens per (b, h) against `state` (float32 [B*H][K][dv + 1], in place).
+// Decode T = p.N new tokens per (b, h) against `state` (float32 [B*H][K][dv + 1], in place).  Workspace:
+// simt_decode_bytes(p) (a control block and every head's folded parameters).
+size_t simt_decode_bytes(const gma_problem_t& p);
 gma_status_t simt_decode(const gma_problem_t& p, const void* Q, const void* K, const void* V, const float* mu,
                          const float* sigma2, const float* log_pi, float* state, void* out, void* ws,
                          cudaStream_t stream);

@@ -14,6 +14,7 @@
 #include <cuda_bf16.h>
 
 #include "gma_internal.h"
+#include "gma_tc_common.cuh"
 
 namespace gma {
 namespace {
@@ -1230,100 +1231,141 @@ __device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) 
   return r;
 }
 
-// Shared-memory floats of the decode kernel for K components.
+// Two block-wide reductions at once (a0 over one value, a1 over another); both max or both sum.
+__device__ __forceinline__ float2 block_reduce2(float a0, float a1, bool is_max, float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float u0 = __shfl_xor_sync(0xffffffffu, a0, o), u1 = __shfl_xor_sync(0xffffffffu, a1, o);
+    a0 = is_max ? fmaxf(a0, u0) : a0 + u0;
+    a1 = is_max ? fmaxf(a1, u1) : a1 + u1;
+  }
+  if (lane == 0) {
+    red[2 * warp] = a0;
+    red[2 * warp + 1] = a1;
+  }
+  __syncthreads();
+  float2 r = make_float2(red[0], red[1]);
+  for (int w = 1; w < nw; ++w) {
+    r.x = is_max ? fmaxf(r.x, red[2 * w]) : r.x + red[2 * w];
+    r.y = is_max ? fmaxf(r.y, red[2 * w + 1]) : r.y + red[2 * w + 1];
+  }
+  __syncthreads();  // red is reused by the next reduction
+  return r;
+}
+
+// Folded parameters of one head for the decode kernel, in the order of its shared memory:
+// mu_t [kD][K + 1], w_t = 1 / sigma2 [kD][K + 1] (row stride K + 1: conflict-free along either index),
+// c [K] = log pi_k - 1/2 sum_d log sigma2_kd; rounded up to a multiple of 4 floats.
+__host__ __device__ constexpr size_t decode_head_floats(int K) {
+  return (2 * (size_t)kD * (K + 1) + (size_t)K + 3) / 4 * 4;
+}
+
+// Shared-memory floats of the decode kernel for K components: the state, one head's folded parameters,
+// and the per-token rows and scratch.
 __host__ __device__ constexpr size_t decode_smem_floats(int K) {
-  return (size_t)K * kStateCols + 2 * (size_t)kD * (K + 1) + 2 * (size_t)K + 2 * kD + kDv + 4 * kDv + 32;
+  return (size_t)K * kStateCols + decode_head_floats(K) + (size_t)K + 2 * kD + kDv + 4 * kDv + 64;
+}
+
+// The fold for every head, once per decode call: into `folded`, decode_head_floats(K) floats per head.
+// Grid (ceil(K / 32), H): a block reads 32 components' rows of mu and sigma2 (coalesced), transposes them
+// through shared memory and writes 32-component runs of every dim row.
+__global__ void __launch_bounds__(256) simt_decode_fold_kernel(const float* __restrict__ mu,
+                                                               const float* __restrict__ sigma2,
+                                                               const float* __restrict__ log_pi, int H, int K,
+                                                               float* __restrict__ folded) {
+  __shared__ float tm[kD][33], tw[kD][33];
+  const int h = blockIdx.y, k0 = blockIdx.x * 32, t = threadIdx.x;
+  const int r = t >> 3, c0 = 8 * (t & 7);  // component k0 + r, dims c0 .. c0 + 7
+  const size_t ld = (size_t)K + 1;
+  float* f = folded + (size_t)h * decode_head_floats(K);
+  float lg = 0.f;
+  if (k0 + r < K) {
+    const size_t o = ((size_t)h * K + k0 + r) * kD + c0;
+    const float4 m0 = __ldg(reinterpret_cast<const float4*>(mu + o));
+    const float4 m1 = __ldg(reinterpret_cast<const float4*>(mu + o) + 1);
+    const float4 s0 = __ldg(reinterpret_cast<const float4*>(sigma2 + o));
+    const float4 s1 = __ldg(reinterpret_cast<const float4*>(sigma2 + o) + 1);
+    const float mv[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+    const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      tm[c0 + q][r] = mv[q];
+      tw[c0 + q][r] = 1.0f / sv[q];
+      lg += logf(sv[q]);
+    }
+  }
+#pragma unroll
+  for (int o = 4; o > 0; o >>= 1) lg += __shfl_xor_sync(0xffffffffu, lg, o);  // the 8 threads of a component
+  if ((t & 7) == 0 && k0 + r < K) f[2 * (size_t)kD * ld + k0 + r] = __ldg(log_pi + (size_t)h * K + k0 + r) - 0.5f * lg;
+  __syncthreads();
+  const int kk = t & 31;
+  if (k0 + kk < K) {
+#pragma unroll
+    for (int j = t >> 5; j < kD; j += 8) {
+      f[(size_t)j * ld + k0 + kk] = tm[j][kk];
+      f[(size_t)kD * ld + (size_t)j * ld + k0 + kk] = tw[j][kk];
+    }
+  }
 }
 
 template <typename IO>
 __global__ void __launch_bounds__(kDecodeThreads) simt_decode_kernel(const IO* __restrict__ Q, const IO* __restrict__ Kx,
                                                                      const IO* __restrict__ V,
-                                                                     const float* __restrict__ mu,
-                                                                     const float* __restrict__ sigma2,
-                                                                     const float* __restrict__ log_pi, int H, int Tn,
+                                                                     const float* __restrict__ folded, int H, int Tn,
                                                                      int K, float* __restrict__ state, float eps,
-                                                                     IO* __restrict__ out) {
-  extern __shared__ float sm[];
+                                                                     IO* __restrict__ out, Ctrl* ctrl) {
+  extern __shared__ __align__(16) float sm[];
+  __shared__ uint64_t bar;
+  __shared__ tc::Abort ab;
   const int bh = blockIdx.x, h = bh % H, k = threadIdx.x;
-  const int ld = K + 1;                     // row stride of the parameter tables (conflict-free both ways)
-  float* S = sm;                            // [K][kStateCols]
-  float* mu_s = S + (size_t)K * kStateCols;  // [kD][K + 1]
-  float* w_s = mu_s + (size_t)kD * ld;       // [kD][K + 1]  1 / sigma2
-  float* c_s = w_s + (size_t)kD * ld;        // [K]
-  float* gq = c_s + K;                       // [K]
+  const int ld = K + 1;                      // row stride of the parameter tables (conflict-free both ways)
+  const size_t hs = decode_head_floats(K);
+  float* S = sm;                             // [K][kStateCols]
+  float* mu_s = S + (size_t)K * kStateCols;  // [kD][K + 1]  } one head's folded parameters,
+  float* w_s = mu_s + (size_t)kD * ld;       // [kD][K + 1]  } copied as they lie in `folded`
+  float* c_s = w_s + (size_t)kD * ld;        // [K]          }
+  float* gq = mu_s + hs;                     // [K]
   float* xq = gq + K;                        // [kD]
   float* xk = xq + kD;                       // [kD]
   float* xv = xk + kD;                       // [kDv]
   float* part = xv + kDv;                    // [4][kDv]
-  float* red = part + 4 * kDv;               // [32]
+  float* red = part + 4 * kDv;               // [64]
   float* st = state + (size_t)bh * K * kStateCols;
+  const float* fh = folded + (size_t)h * hs;
   const int n_state = K * kStateCols;
-  // float4 copies when this head's state starts on a 16-byte boundary (K a multiple of 4), so that
-  // many loads are in flight per thread; plain floats otherwise
-  const bool vec = ((reinterpret_cast<uintptr_t>(st) | reinterpret_cast<uintptr_t>(S)) & 15) == 0 && (n_state & 3) == 0;
+  // state and parameters: bulk copies (TMA engine, 16 KB pieces on one mbarrier) when both start on a
+  // 16-byte boundary (K a multiple of 4; the sizes then are multiples of 16 bytes too), else plain loads
+  const uint32_t state_bytes = (uint32_t)n_state * 4u, param_bytes = (uint32_t)hs * 4u;
+  const bool vec = ((reinterpret_cast<uintptr_t>(st) | reinterpret_cast<uintptr_t>(fh)) & 15) == 0 && (K & 3) == 0;
   if (vec) {
-    // all of a thread's loads in flight before the first store (one round trip to memory)
-    const int n4s = n_state / 4;
-    for (int i0 = threadIdx.x; i0 < n4s; i0 += 16 * kDecodeThreads) {
-      float4 x[16];
-#pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const int i = i0 + u * kDecodeThreads;
-        if (i < n4s) x[u] = __ldcg(reinterpret_cast<const float4*>(st) + i);
-      }
-#pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const int i = i0 + u * kDecodeThreads;
-        if (i < n4s) reinterpret_cast<float4*>(S)[i] = x[u];
+    if (threadIdx.x == 0) {
+      ab.flag = 0;
+      tc::mbar_init(&bar, 1);
+      tc::mbar_fence_init();
+      tc::mbar_expect_tx(&bar, state_bytes + param_bytes);
+      constexpr uint32_t kPiece = 16384;
+      for (uint32_t o = 0; o < state_bytes; o += kPiece)
+        tc::bulk_load(reinterpret_cast<char*>(S) + o, reinterpret_cast<const char*>(st) + o,
+                      state_bytes - o < kPiece ? state_bytes - o : kPiece, &bar);
+      for (uint32_t o = 0; o < param_bytes; o += kPiece)
+        tc::bulk_load(reinterpret_cast<char*>(mu_s) + o, reinterpret_cast<const char*>(fh) + o,
+                      param_bytes - o < kPiece ? param_bytes - o : kPiece, &bar);
+      if (!tc::wait_bounded(&bar, 0, &ab, ctrl, 0x20u, 1000000000ull)) {
+        ab.flag = 1;
+        tc::Abort again{0};  // give the copies in flight another bounded while to land before leaving
+        tc::wait_bounded(&bar, 0, &again, ctrl, 0x20u, 1000000000ull);
       }
     }
+    __syncthreads();
+    if (ab.flag) return;  // the copy did not land in time: the error word says so; the state is untouched
   } else {
 #pragma unroll 8
     for (int i = threadIdx.x; i < n_state; i += blockDim.x) S[i] = __ldcg(st + i);
+#pragma unroll 8
+    for (int i = threadIdx.x; i < (int)hs; i += blockDim.x) mu_s[i] = __ldg(fh + i);
+    __syncthreads();
   }
-  // parameters of head h, transposed to [dim][component], and c_k = log pi_k - 1/2 sum_d log sigma2_kd:
-  // each thread takes 4 dims of one component per float4 pair; the 16 threads of a component (an
-  // aligned half-warp) add their log-variances with shuffles.  The trip count is warp-uniform.
-  const float4* mu4 = reinterpret_cast<const float4*>(mu + (size_t)h * K * kD);
-  const float4* s24 = reinterpret_cast<const float4*>(sigma2 + (size_t)h * K * kD);
-  const int n4 = K * (kD / 4);
-  // eight float4 of each table in flight per thread; the trip count and the 16-thread component groups
-  // (aligned half-warps: n4 and the block size are multiples of 16) are warp-uniform
-  for (int i0 = threadIdx.x; i0 - (int)threadIdx.x < n4; i0 += 8 * kDecodeThreads) {
-    float4 m[8], v[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int i4 = i0 + u * kDecodeThreads;
-      if (i4 < n4) {
-        m[u] = __ldg(mu4 + i4);
-        v[u] = __ldg(s24 + i4);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int i4 = i0 + u * kDecodeThreads;
-      const bool on = i4 < n4;
-      const int kk = i4 >> 4, j0 = (i4 & 15) << 2;
-      float lg = 0.f;
-      if (on) {
-        mu_s[(size_t)(j0 + 0) * ld + kk] = m[u].x;
-        mu_s[(size_t)(j0 + 1) * ld + kk] = m[u].y;
-        mu_s[(size_t)(j0 + 2) * ld + kk] = m[u].z;
-        mu_s[(size_t)(j0 + 3) * ld + kk] = m[u].w;
-        w_s[(size_t)(j0 + 0) * ld + kk] = 1.0f / v[u].x;
-        w_s[(size_t)(j0 + 1) * ld + kk] = 1.0f / v[u].y;
-        w_s[(size_t)(j0 + 2) * ld + kk] = 1.0f / v[u].z;
-        w_s[(size_t)(j0 + 3) * ld + kk] = 1.0f / v[u].w;
-        lg = (logf(v[u].x) + logf(v[u].y)) + (logf(v[u].z) + logf(v[u].w));
-      }
-      if (i0 - (int)threadIdx.x + u * kDecodeThreads < n4) {  // warp-uniform: the whole warp is on or off
-#pragma unroll
-        for (int o = 8; o > 0; o >>= 1) lg += __shfl_xor_sync(0xffffffffu, lg, o);
-      }
-      if (on && (i4 & 15) == 0) c_s[kk] = __ldg(log_pi + (size_t)h * K + kk) - 0.5f * lg;
-    }
-  }
-  __syncthreads();
   for (int t = 0; t < Tn; ++t) {
     const size_t row = (size_t)bh * Tn + t;
     if (threadIdx.x < kD) {
@@ -1346,9 +1388,10 @@ __global__ void __launch_bounds__(kDecodeThreads) simt_decode_kernel(const IO* _
       lk = c_s[k] - 0.5f * ak;
       lq = c_s[k] - 0.5f * aq;
     }
-    const float mk = block_reduce(lk, true, red), mq = block_reduce(lq, true, red);
-    const float ek = k < K ? expf(lk - mk) : 0.f, eq = k < K ? expf(lq - mq) : 0.f;
-    const float sk = block_reduce(ek, false, red), sq = block_reduce(eq, false, red);
+    const float2 mx = block_reduce2(lk, lq, true, red);
+    const float ek = k < K ? expf(lk - mx.x) : 0.f, eq = k < K ? expf(lq - mx.y) : 0.f;
+    const float2 sm2 = block_reduce2(ek, eq, false, red);
+    const float sk = sm2.x, sq = sm2.y;
     // state update (own row), then the query's responsibilities for the read
     if (k < K) {
       const float g = ek / sk;
@@ -1375,12 +1418,19 @@ __global__ void __launch_bounds__(kDecodeThreads) simt_decode_kernel(const IO* _
     }
     __syncthreads();  // xq / xk / xv / gq / part are rewritten by the next token
   }
-  __syncthreads();
   if (vec) {
-#pragma unroll 4
-    for (int i = threadIdx.x; i < n_state / 4; i += blockDim.x)
-      reinterpret_cast<float4*>(st)[i] = reinterpret_cast<const float4*>(S)[i];
+    tc::fence_async_smem();  // this thread's shared-memory writes become visible to the bulk copy
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      constexpr uint32_t kPiece = 16384;
+      for (uint32_t o = 0; o < state_bytes; o += kPiece)
+        tc::bulk_store(reinterpret_cast<char*>(st) + o, reinterpret_cast<const char*>(S) + o,
+                       state_bytes - o < kPiece ? state_bytes - o : kPiece);
+      tc::bulk_commit();
+      tc::bulk_wait_all();
+    }
   } else {
+    __syncthreads();
 #pragma unroll 8
     for (int i = threadIdx.x; i < n_state; i += blockDim.x) st[i] = S[i];
   }
@@ -1625,23 +1675,32 @@ gma_status_t simt_backward(const gma_problem_t& p, bool causal, const void* Q, c
                             (bf*)dQ, (bf*)dK, (bf*)dV, dmu, dsigma2, dlog_pi, ws, st);
 }
 
-// Decode T new tokens per (b, h) from `state` (float32 [B*H][K][dv + 1], updated in place).  One launch;
-// the workspace is not used (its error word stays as the caller left it).
+// Decode T new tokens per (b, h) from `state` (float32 [B*H][K][dv + 1], updated in place).  Two launches:
+// the parameter fold of every head into the workspace (after its control block, whose error word stays as
+// the caller left it), then one CTA per (b, h).
+size_t simt_decode_bytes(const gma_problem_t& p) {
+  return align_up(sizeof(Ctrl)) + align_up((size_t)p.H * decode_head_floats(p.K) * sizeof(float));
+}
+
 gma_status_t simt_decode(const gma_problem_t& p, const void* Q, const void* K, const void* V, const float* mu,
-                         const float* sigma2, const float* log_pi, float* state, void* out, void* /*ws*/,
+                         const float* sigma2, const float* log_pi, float* state, void* out, void* ws,
                          cudaStream_t st) {
   const size_t smem = decode_smem_floats(p.K) * sizeof(float);
   const int BH = p.B * p.H;
+  float* folded = (float*)((char*)ws + align_up(sizeof(Ctrl)));
+  GMA_LAUNCH("simt_decode_fold", simt_decode_fold_kernel, dim3(cdiv(p.K, 32), p.H), 256, 0, st, mu, sigma2, log_pi,
+             p.H, p.K, folded);
+  if (gma_status_t e = check_launch("launch simt_decode_fold", (const void*)simt_decode_fold_kernel)) return e;
   if (p.dtype == GMA_F32) {
     if (set_smem_optin((const void*)simt_decode_kernel<float>, (int)smem, 4) != GMA_OK) return GMA_ERR_CUDA;
     GMA_LAUNCH("simt_decode", simt_decode_kernel<float>, BH, kDecodeThreads, smem, st, (const float*)Q,
-               (const float*)K, (const float*)V, mu, sigma2, log_pi, p.H, p.N, p.K, state, p.eps, (float*)out);
+               (const float*)K, (const float*)V, folded, p.H, p.N, p.K, state, p.eps, (float*)out, (Ctrl*)ws);
     return check_launch("launch simt_decode", (const void*)simt_decode_kernel<float>);
   }
   if (set_smem_optin((const void*)simt_decode_kernel<__nv_bfloat16>, (int)smem, 4) != GMA_OK) return GMA_ERR_CUDA;
   GMA_LAUNCH("simt_decode", simt_decode_kernel<__nv_bfloat16>, BH, kDecodeThreads, smem, st,
-             (const __nv_bfloat16*)Q, (const __nv_bfloat16*)K, (const __nv_bfloat16*)V, mu, sigma2, log_pi, p.H,
-             p.N, p.K, state, p.eps, (__nv_bfloat16*)out);
+             (const __nv_bfloat16*)Q, (const __nv_bfloat16*)K, (const __nv_bfloat16*)V, folded, p.H, p.N, p.K, state,
+             p.eps, (__nv_bfloat16*)out, (Ctrl*)ws);
   return check_launch("launch simt_decode", (const void*)simt_decode_kernel<__nv_bfloat16>);
 }
 

@@ -194,9 +194,12 @@ GMA_API gma_status_t gma_causal_state(const gma_problem_t *p, const void *K, con
  * prefix j <= i only, through running sums).
  *   Q, K [B,H,N,d], V [B,H,N,dv] in p->dtype; O [B,H,N,dv] in p->dtype (written);
  *   state float32 [B][H][K][dv+1] (read and updated in place; see gma_causal_state).
- * Computed in float32 on the CUDA cores, one launch of one CTA per (b, h) that keeps the head's state
- * and parameters in shared memory; meant for small N per call.  Workspace:
- * gma_workspace_bytes(p, GMA_OP_CAUSAL_DECODE) (a small control block this build leaves untouched).
+ * Computed in float32 on the CUDA cores in two launches: the parameter fold of every head (1 / sigma2,
+ * the component constants) into the workspace, then one CTA per (b, h) that keeps the head's state and
+ * folded parameters in shared memory; meant for small N per call.  Workspace:
+ * gma_workspace_bytes(p, GMA_OP_CAUSAL_DECODE): a control block (not cleared here; its error word
+ * records a copy into shared memory that did not land within 1 s, which leaves the state untouched,
+ * see gma_check_device_error) and the folded parameters, 4 H (128 (K + 1) + K) bytes rounded up.
  * O may not alias any input or the state.
  */
 GMA_API gma_status_t gma_causal_decode(const gma_problem_t *p, const void *Q, const void *K, const void *V,
