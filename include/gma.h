@@ -234,7 +234,8 @@ GMA_API gma_status_t gma_backward_bidir(const gma_problem_t *p, const void *Q, c
  * sums, trained end to end).  With S_i the running state, u_i = [G_i / den_i | -(G_i . O_i) / den_i] and
  * R_j = sum_{i >= j} gamma_Qi u_i^T: dgamma_Qi = S_i u_i, dgamma_Kj = R_j [v_j | 1], dv_j = R_j^T gamma_Kj,
  * computed per segment (forward over the queries, backward over the keys) on the CUDA cores in float32.
- * Workspace: gma_workspace_bytes(p, GMA_OP_BACKWARD_CAUSAL), growing with N.
+ * Workspace: gma_workspace_bytes(p, GMA_OP_BACKWARD_CAUSAL), growing with N (per-row softmax
+ * gradients, the queries' responsibilities and the u rows: 4 B*H*N*(3K + dv + 1) bytes and more).
  */
 GMA_API gma_status_t gma_backward_causal(const gma_problem_t *p, const void *Q, const void *K, const void *V,
                                          const float *mu, const float *sigma2, const float *log_pi, const void *dO,
