@@ -265,6 +265,25 @@ def run_gma(args, world, rank, local):
         ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
         return ms, (w0, w1)
 
+    # per-call distribution: each call bracketed by its own events, with L2 flushed (a 2 x L2 buffer
+    # written) outside the bracket before every call; returns [p10, median, p90] in ms
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_buf = torch.empty(max(2 * l2, 1 << 20) // 4, dtype=torch.float32, device=dev)
+
+    def timed_each(fn, n):
+        barrier()
+        ts = []
+        for _ in range(n):
+            flush_buf.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        return [float(x) for x in np.percentile(ts, [10, 50, 90])]
+
     clocks = ClockSampler(local)
     for _ in range(args.warmup):
         step(t["Q"], t["K"], t["V"])
@@ -278,6 +297,8 @@ def run_gma(args, world, rank, local):
     ms_per_step = ms / args.steps
     units_per_step = 2 * B * H * N
     value = whole_job_rate(units_per_step, ms_per_step, world)
+
+    step_dist = timed_each(lambda: step(t["Q"], t["K"], t["V"]), args.steps)
 
     # per-kernel durations (events on the launch stream), same step loop
     gma.profile_enable(True)
@@ -403,7 +424,10 @@ def run_gma(args, world, rank, local):
                 torch.cuda.synchronize(dev)
                 peak_call = torch.cuda.max_memory_allocated(dev) - base
                 inputs_b = 3 * wi.B * wi.H * n * 64 * 2
+                dist_ms = timed_each(lambda: fn(ti["Q"], ti["K"], ti["V"], ti["mu"], ti["sigma2"], ti["log_pi"],
+                                                wi.eps, out=out, workspace=ws), min(reps, 20))
                 entry[form] = {"ms": m / reps, "tok_heads_per_s": wi.B * wi.H * n / (m / reps * 1e-3),
+                               "ms_p10_median_p90_l2_flushed": dist_ms,
                                "workspace_bytes": ws.numel(), "call_peak_bytes_beyond_inputs": peak_call,
                                "inputs_bytes": inputs_b}
                 del ws, out, ws2, out2
@@ -551,6 +575,7 @@ def run_gma(args, world, rank, local):
                 "config": config_dict(w),
                 "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
                 "gpu_launches": int(launches), "roofline": roof, "cpu_baseline": cpu, "clocks": clk,
+                "step_ms_p10_median_p90_l2_flushed": step_dist,
                 "roofline_path": path, "kernels": kernels, "sweep": sweep or None, "extensions": extensions,
                 "mufu_ex2_per_s": mufu_rate}
         print(json.dumps(line), flush=True)
