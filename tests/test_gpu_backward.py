@@ -94,3 +94,32 @@ def test_causal_backward_lengths_f32(gma, N):
 
 def test_causal_backward_bf16_B1H2N2048K256(gma):
     check(gma, make_inputs(1, 2, 2048, 256, dtype="bf16", seed=19), seed=19, causal=True)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_full_size_one_head(gma, causal):
+    """The bench's backward workload (B=4 H=8 N=4096 K=128, bf16), launched whole as the bench times it;
+    the oracle checks head 3 over every batch entry, so that head's dmu, dsigma2 and dlog_pi are
+    complete sums and dQ, dK, dV are checked for all 4 x 4096 of its rows."""
+    import torch
+    from gaussian_mixture_sequence_gma_gb300.inputs import make_workload, workloads
+    w = workloads()["bidir_bf16_B4H8N4096K128"]
+    inp = make_workload(w)
+    G = _dO(inp, 77)
+    t = to_device(inp)
+    gd = to_device(dict(Q=G, K=G, V=G, mu=inp["mu"], sigma2=inp["sigma2"], log_pi=inp["log_pi"], dtype="bf16"))["Q"]
+    f = gma.backward_causal if causal else gma.backward_bidir
+    got = f(t["Q"], t["K"], t["V"], t["mu"], t["sigma2"], t["log_pi"], gd, eps=w.eps)
+    torch.cuda.synchronize()
+    h = 3
+    ref = orc.backward_bidir(inp["Q"][:, h:h + 1], inp["K"][:, h:h + 1], inp["V"][:, h:h + 1], inp["mu"][h:h + 1],
+                             inp["sigma2"][h:h + 1], inp["log_pi"][h:h + 1], w.eps, G[:, h:h + 1], causal=causal)
+    errs = {}
+    for name, a, b in zip(NAMES, got, ref):
+        a = a.float().cpu().numpy()
+        a = a[:, h:h + 1] if name in ("dQ", "dK", "dV") else a[h:h + 1]
+        assert a.shape == b.shape, name
+        assert np.isfinite(a).all(), name
+        errs[name] = rel_err(a, b)
+    bad = {k: v for k, v in errs.items() if v > TOL["bf16"]}
+    assert not bad, "max rel err above the bar: %s" % bad

@@ -110,3 +110,23 @@ def test_decode_lm_shape_bf16_B8H12K256(gma):
     R = orc.forward(inp["Q"], inp["K"], inp["V"], inp["mu"], inp["sigma2"], inp["log_pi"], 1e-6, causal=True,
                     rows=np.arange(2048, 2052))
     assert rel_err(O, R) <= TOL["bf16"]
+
+
+def test_decode_bench_shape(gma):
+    """The bench's decode shape (B=8, H=12, K=256, bf16, one token per call, 96 CTAs) after a 300-token
+    prompt, three steps: every head's outputs and final state against the oracle."""
+    N0, T = 300, 3
+    inp = make_inputs(8, 12, N0 + T, 256, dtype="bf16", seed=90, sigma_raw_std=0.5)
+    t = to_device(inp)
+    state = gma.causal_state(t["K"][:, :, :N0].contiguous(), t["V"][:, :, :N0].contiguous(), t["mu"], t["sigma2"],
+                             t["log_pi"])
+    outs = []
+    for s in range(T):
+        d = _slice(t, N0 + s, N0 + s + 1)
+        outs.append(gma.causal_decode(d["Q"], d["K"], d["V"], t["mu"], t["sigma2"], t["log_pi"], state))
+    O = np.concatenate([o.float().cpu().numpy() for o in outs], axis=2)
+    R = orc.forward(inp["Q"], inp["K"], inp["V"], inp["mu"], inp["sigma2"], inp["log_pi"], 1e-6, causal=True,
+                    rows=np.arange(N0, N0 + T))
+    assert np.isfinite(O).all()
+    assert rel_err(O, R) <= TOL["bf16"]
+    assert rel_err(state.cpu().numpy(), _ref_state(inp, N0 + T)) <= TOL["bf16"]
