@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "gma.h"
 
 namespace gma {
@@ -90,6 +92,32 @@ void prof_after(cudaStream_t st, void* token);
     void* gma_prof_token_ = ::gma::prof_before((stream), (name));   \
     kernel<<<(grid), (block), (smem), (stream)>>>(__VA_ARGS__);     \
     ::gma::prof_after((stream), gma_prof_token_);                   \
+  } while (0)
+
+// Programmatic dependent launch: the kernel may start while the previous kernel on the stream is
+// finishing; it must execute griddepcontrol.wait (dep_wait) in every thread before it reads what that
+// kernel wrote, and it may read what kernels before that one wrote only after the wait as well.
+template <typename... KArgs, typename... Args>
+inline void launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                             Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+#define GMA_LAUNCH_DEPENDENT(name, kernel, grid, block, smem, stream, ...)                  \
+  do {                                                                                    \
+    void* gma_prof_token_ = ::gma::prof_before((stream), (name));                         \
+    ::gma::launch_dependent(kernel, dim3(grid), dim3(block), (smem), (stream), __VA_ARGS__); \
+    ::gma::prof_after((stream), gma_prof_token_);                                         \
   } while (0)
 
 // Records a description of the failing step (and the pending CUDA error, if any) for

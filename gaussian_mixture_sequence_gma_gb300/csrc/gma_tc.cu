@@ -120,6 +120,7 @@ __global__ void __launch_bounds__(128) tc_prep_kernel(const float* __restrict__ 
                                                       const float* __restrict__ log_pi, int H, int K, int Kp,
                                                       uint8_t* w_img, float* cbias, Ctrl* ctrl, float* zero,
                                                       size_t zero_n) {
+  dep_launch_next();  // the main kernel sets itself up meanwhile and waits for this grid before reading
   const int h = blockIdx.y, k = blockIdx.x * 8 + (threadIdx.x >> 4), q = threadIdx.x & 15;
   const int d0 = 8 * (q & 7);
   uint32_t w[4] = {0u, 0u, 0u, 0u};
@@ -531,6 +532,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  dep_wait();  // the parameter fold (and zeroed accumulator) of this call are complete
   const uint32_t tmem = B.tmem_base;
   if (warp < kRowWarp0) {
     setmaxnreg_dec<kCtrlRegs>();
@@ -733,6 +735,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  dep_wait();  // the write (and before it the parameter fold) of this call are complete
   const uint32_t tmem = B.tmem_base;
   if (warp < kRowWarp0) {
     setmaxnreg_dec<kCtrlRegs>();
@@ -1064,6 +1067,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  dep_wait();  // the scan (and before it the aggregates and the parameter fold) of this call are complete
   const uint32_t tmem = B.tmem_base;
 
   if (warp < kRowWarp0) {
@@ -1312,6 +1316,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 // Exclusive scan over segments: agg[bh][p][e] <- sum_{p' < p} agg[bh][p'][e].  grid (ceil(n / 256), B*H).
 // Each thread has all loads of up to 32 segments in flight before the first store.
 __global__ void tc_scan_kernel(float* agg, int P, int n) {
+  dep_wait();         // the aggregates are complete
+  dep_launch_next();  // the sweep sets itself up meanwhile and waits for this grid before reading
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= n) return;
   float* base = agg + (size_t)blockIdx.y * P * n + e;
@@ -1424,7 +1430,7 @@ gma_status_t tc_launch(const gma_problem_t& p, gma_op_t op, int Nk, const TcPlan
     const uint32_t smem = smem_bytes(read_layout(pl.Kp).total);
     if (set_smem_optin((const void*)tc_read_kernel<false, NC>, (int)smem, 0) != GMA_OK) return GMA_ERR_CUDA;
     a.fault = 0;
-    GMA_LAUNCH("tc_resp", (tc_read_kernel<false, NC>), dim3(pl.splits, BH), kThreadsTc, smem, st, mq, a);
+    GMA_LAUNCH_DEPENDENT("tc_resp", (tc_read_kernel<false, NC>), dim3(pl.splits, BH), kThreadsTc, smem, st, mq, a);
     return check_launch("launch tc_resp", (const void*)tc_read_kernel<false, NC>);
   }
   if (op == GMA_OP_CAUSAL) {
@@ -1439,16 +1445,17 @@ gma_status_t tc_launch(const gma_problem_t& p, gma_op_t op, int Nk, const TcPlan
     // a7: chunked sweep
     const uint32_t smem_w = smem_bytes(write_layout(pl.Kp).total);
     if (set_smem_optin((const void*)tc_write_kernel<false, NC>, (int)smem_w, 0) != GMA_OK) return GMA_ERR_CUDA;
-    GMA_LAUNCH("tc_causal_aggregate", (tc_write_kernel<false, NC>), dim3(pl.splits, BH), kThreadsTc, smem_w, st, mk,
-               mv, mg, a);
+    GMA_LAUNCH_DEPENDENT("tc_causal_aggregate", (tc_write_kernel<false, NC>), dim3(pl.splits, BH), kThreadsTc, smem_w,
+                         st, mk, mv, mg, a);
     if (gma_status_t e = check_launch("launch tc_causal_aggregate", (const void*)tc_write_kernel<false, NC>)) return e;
     a.fault = 0;
     const int n = pl.Kp * kStCols;
-    GMA_LAUNCH("tc_causal_scan", tc_scan_kernel, dim3(cdiv(n, 256), BH), 256, 0, st, a.state, pl.splits, n);
+    GMA_LAUNCH_DEPENDENT("tc_causal_scan", tc_scan_kernel, dim3(cdiv(n, 256), BH), 256, 0, st, a.state, pl.splits, n);
     if (gma_status_t e = check_launch("launch tc_causal_scan", (const void*)tc_scan_kernel)) return e;
     const uint32_t smem_c = smem_bytes(causal_layout(pl.Kp).total);
     if (set_smem_optin((const void*)tc_causal_kernel<NC>, (int)smem_c, 0) != GMA_OK) return GMA_ERR_CUDA;
-    GMA_LAUNCH("tc_causal_chunk", tc_causal_kernel<NC>, dim3(pl.splits, BH), kThreadsTc, smem_c, st, mq, mg, mv32, a);
+    GMA_LAUNCH_DEPENDENT("tc_causal_chunk", tc_causal_kernel<NC>, dim3(pl.splits, BH), kThreadsTc, smem_c, st, mq, mg,
+                         mv32, a);
     return check_launch("launch tc_causal_chunk", (const void*)tc_causal_kernel<NC>);
   }
   // bidirectional / cross: write over the Nk keys with their own split plan (the state layout does not
@@ -1465,8 +1472,8 @@ gma_status_t tc_launch(const gma_problem_t& p, gma_op_t op, int Nk, const TcPlan
     if (!make_map(&mk, K, BH, Nk) || !make_map(&mv, V, BH, Nk)) return GMA_ERR_CUDA;
     const uint32_t smem_w = smem_bytes(write_layout(pl.Kp).total);
     if (set_smem_optin((const void*)tc_write_kernel<true, NC>, (int)smem_w, 0) != GMA_OK) return GMA_ERR_CUDA;
-    GMA_LAUNCH("tc_bidir_write", (tc_write_kernel<true, NC>), dim3(plk.splits, BH), kThreadsTc, smem_w, st, mk, mv, mk,
-               aw);  // (the third map serves only the causal key store)
+    GMA_LAUNCH_DEPENDENT("tc_bidir_write", (tc_write_kernel<true, NC>), dim3(plk.splits, BH), kThreadsTc, smem_w, st,
+                         mk, mv, mk, aw);  // (the third map serves only the causal key store)
     if (gma_status_t e = check_launch("launch tc_bidir_write", (const void*)tc_write_kernel<true, NC>)) return e;
   }
   if (op == GMA_OP_CAUSAL_STATE) return GMA_OK;  // the state alone
@@ -1474,7 +1481,8 @@ gma_status_t tc_launch(const gma_problem_t& p, gma_op_t op, int Nk, const TcPlan
   if (!make_map(&mq, Q, BH, p.N)) return GMA_ERR_CUDA;
   const uint32_t smem_r = smem_bytes(read_layout(pl.Kp).total);
   if (set_smem_optin((const void*)tc_read_kernel<true, NC>, (int)smem_r, 0) != GMA_OK) return GMA_ERR_CUDA;
-  GMA_LAUNCH("tc_bidir_read", (tc_read_kernel<true, NC>), dim3(pl.splits, BH), kThreadsTc, smem_r, st, mq, a);
+  GMA_LAUNCH_DEPENDENT("tc_bidir_read", (tc_read_kernel<true, NC>), dim3(pl.splits, BH), kThreadsTc, smem_r, st, mq,
+                       a);
   return check_launch("launch tc_bidir_read", (const void*)tc_read_kernel<true, NC>);
 }
 

@@ -22,6 +22,14 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// ---------------------------------------------------------------------------------------------- launch order
+// Waits until the previous kernel on the stream has completed and its writes are visible (a no-op for a
+// kernel launched without programmatic dependent launch).
+__device__ __forceinline__ void dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel on the stream (launched as dependent) start once every CTA of this one has
+// executed this or exited.
+__device__ __forceinline__ void dep_launch_next() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 // ---------------------------------------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
