@@ -1275,6 +1275,7 @@ __global__ void __launch_bounds__(256) simt_decode_fold_kernel(const float* __re
                                                                const float* __restrict__ log_pi, int H, int K,
                                                                float* __restrict__ folded) {
   __shared__ float tm[kD][33], tw[kD][33];
+  tc::dep_launch_next();  // the decode kernel starts its state copy meanwhile
   const int h = blockIdx.y, k0 = blockIdx.x * 32, t = threadIdx.x;
   const int r = t >> 3, c0 = 8 * (t & 7);  // component k0 + r, dims c0 .. c0 + 7
   const size_t ld = (size_t)K + 1;
@@ -1345,9 +1346,10 @@ __global__ void __launch_bounds__(kDecodeThreads) simt_decode_kernel(const IO* _
       tc::mbar_fence_init();
       tc::mbar_expect_tx(&bar, state_bytes + param_bytes);
       constexpr uint32_t kPiece = 16384;
-      for (uint32_t o = 0; o < state_bytes; o += kPiece)
+      for (uint32_t o = 0; o < state_bytes; o += kPiece)  // the state does not depend on the fold
         tc::bulk_load(reinterpret_cast<char*>(S) + o, reinterpret_cast<const char*>(st) + o,
                       state_bytes - o < kPiece ? state_bytes - o : kPiece, &bar);
+      tc::dep_wait();  // the fold of this call is complete
       for (uint32_t o = 0; o < param_bytes; o += kPiece)
         tc::bulk_load(reinterpret_cast<char*>(mu_s) + o, reinterpret_cast<const char*>(fh) + o,
                       param_bytes - o < kPiece ? param_bytes - o : kPiece, &bar);
@@ -1357,9 +1359,11 @@ __global__ void __launch_bounds__(kDecodeThreads) simt_decode_kernel(const IO* _
         tc::wait_bounded(&bar, 0, &again, ctrl, 0x20u, 1000000000ull);
       }
     }
+    tc::dep_wait();
     __syncthreads();
     if (ab.flag) return;  // the copy did not land in time: the error word says so; the state is untouched
   } else {
+    tc::dep_wait();
 #pragma unroll 8
     for (int i = threadIdx.x; i < n_state; i += blockDim.x) S[i] = __ldcg(st + i);
 #pragma unroll 8
@@ -1693,12 +1697,12 @@ gma_status_t simt_decode(const gma_problem_t& p, const void* Q, const void* K, c
   if (gma_status_t e = check_launch("launch simt_decode_fold", (const void*)simt_decode_fold_kernel)) return e;
   if (p.dtype == GMA_F32) {
     if (set_smem_optin((const void*)simt_decode_kernel<float>, (int)smem, 4) != GMA_OK) return GMA_ERR_CUDA;
-    GMA_LAUNCH("simt_decode", simt_decode_kernel<float>, BH, kDecodeThreads, smem, st, (const float*)Q,
+    GMA_LAUNCH_DEPENDENT("simt_decode", simt_decode_kernel<float>, BH, kDecodeThreads, smem, st, (const float*)Q,
                (const float*)K, (const float*)V, folded, p.H, p.N, p.K, state, p.eps, (float*)out, (Ctrl*)ws);
     return check_launch("launch simt_decode", (const void*)simt_decode_kernel<float>);
   }
   if (set_smem_optin((const void*)simt_decode_kernel<__nv_bfloat16>, (int)smem, 4) != GMA_OK) return GMA_ERR_CUDA;
-  GMA_LAUNCH("simt_decode", simt_decode_kernel<__nv_bfloat16>, BH, kDecodeThreads, smem, st,
+  GMA_LAUNCH_DEPENDENT("simt_decode", simt_decode_kernel<__nv_bfloat16>, BH, kDecodeThreads, smem, st,
              (const __nv_bfloat16*)Q, (const __nv_bfloat16*)K, (const __nv_bfloat16*)V, folded, p.H, p.N, p.K, state,
              p.eps, (__nv_bfloat16*)out, (Ctrl*)ws);
   return check_launch("launch simt_decode", (const void*)simt_decode_kernel<__nv_bfloat16>);
