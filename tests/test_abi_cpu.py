@@ -263,3 +263,14 @@ def test_projected_argument_errors(L):
     assert proj(P(), ws_bytes=need - 1) == gma.GMA_ERR_WORKSPACE
     nul = [None, ptr[1], ptr[2], ptr[3], ptr[4], ptr[5], None, ptr[7]]
     assert proj(P(N=0), p=nul, ws_bytes=gma.workspace_bytes(P(N=0), gma.OP_PROJECTED_CAUSAL)) == gma.GMA_OK
+
+
+def test_decode_workspace_size():
+    """The decode workspace is the documented control block (256 B) plus every head's folded parameters,
+    4 H (128 (K + 1) + K) bytes with each head's block rounded up to 16 bytes, the total to 256."""
+    for B, H, K in ((1, 1, 1), (2, 3, 17), (8, 12, 256), (4, 8, 128)):
+        head = (2 * 64 * (K + 1) + K + 3) // 4 * 4 * 4
+        want = 256 + (H * head + 255) // 256 * 256
+        for dt in (gma.GMA_F32, gma.GMA_BF16):
+            for N in (1, 64):
+                assert gma.workspace_bytes(P(B=B, H=H, K=K, N=N, dtype=dt), gma.OP_CAUSAL_DECODE) == want
