@@ -165,8 +165,9 @@ __device__ __forceinline__ void load_state_image(const float* src, int K, float*
 // Responsibilities of the T rows in xs (first `nvalid` valid) into G[T][KC]; rows past nvalid and
 // columns past K are zero.  Thread (component k, group of RPT = T KC / 256 rows) keeps RPT independent
 // sums of the centered log-density, so that each parameter is read once per tile; then one warp per
-// row takes the softmax.  Needs 256 threads.
-template <int KC>
+// row takes the softmax.  Needs 256 threads.  UJ: unroll of the loop over dims (2 where the registers
+// allow it).
+template <int KC, int UJ = 1>
 __device__ void gamma_tile_kc(const float* xs, int nvalid, const SimtParams& P, int h, int K, float* G) {
   constexpr int RK = KC / 32, RPT = T * KC / kThreads;
   const float* mu_t = P.mu_t + (size_t)h * kD * K;
@@ -177,7 +178,7 @@ __device__ void gamma_tile_kc(const float* xs, int nvalid, const SimtParams& P, 
     float acc[RPT];
 #pragma unroll
     for (int ii = 0; ii < RPT; ++ii) acc[ii] = 0.f;
-#pragma unroll 1
+#pragma unroll UJ
     for (int j = 0; j < kD; j += 4) {
       float m[4], w[4];
 #pragma unroll
@@ -270,6 +271,14 @@ __device__ __forceinline__ void store_rows(const float* G, int nvalid, int K, fl
 // (G row stride LDG; the pad columns past KC are left alone)
 template <int KC, int LDG = KC>
 __device__ __forceinline__ void load_tile_rows(const float* src, int nvalid, int K, float* G) {
+  if ((K & 3) == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {  // 16-byte words
+    for (int p = threadIdx.x; p < T * KC / 4; p += blockDim.x) {
+      const int i = p / (KC / 4), k = 4 * (p % (KC / 4));
+      *reinterpret_cast<float4*>(G + i * LDG + k) =
+          i < nvalid && k < K ? *reinterpret_cast<const float4*>(src + (size_t)i * K + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    return;
+  }
   for (int p = threadIdx.x; p < T * KC; p += blockDim.x) {
     const int i = p / KC, k = p % KC;
     G[i * LDG + k] = i < nvalid && k < K ? src[(size_t)i * K + k] : 0.f;
@@ -711,7 +720,7 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_query_kernel(const IO* __re
     load_rows<IO>(Q + (size_t)unit * N * kD, t0, nvalid, xs);
     load_rows<IO>(dO + (size_t)unit * N * kDv, t0, nvalid, gs);
     __syncthreads();
-    gamma_tile_kc<KC>(xs, nvalid, P, h, K, G);
+    gamma_tile_kc<KC, 2>(xs, nvalid, P, h, K, G);
     {  // numerators and denominators of the warp's rows, then dn | dd (rows past N: zero)
       float a[4][2], dp[4] = {0.f, 0.f, 0.f, 0.f};
       rows_times_image<KC>(G, S, i0, a);
@@ -937,7 +946,7 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_causal_query_kernel(
     load_rows_ld<IO>(V + (size_t)unit * N * kDv, t0, nvalid, vs, kSP);
     load_tile_rows<KC, KG>(dlk + row0 * K, nvalid, K, GK);
     __syncthreads();
-    gamma_tile_kc<KC>(xq, nvalid, Pp, h, K, GQ);
+    gamma_tile_kc<KC, 2>(xq, nvalid, Pp, h, K, GQ);
     store_rows<KC>(GQ, nvalid, K, gq + row0 * K);
     {  // A, then [num | den] = gamma_Q [S | Z] + sum_{j <= i} A_ij [v_j | 1], then u = [dn | dd]
       causal_tile_A<KC>(GQ, GK, i0, A);
