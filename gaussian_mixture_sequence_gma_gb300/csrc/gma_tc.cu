@@ -22,11 +22,6 @@
 // operand) or idle; warpgroups 1-4 (warps 4..19) = row warps: thread (q, part) owns token
 // row 32q+lane of the tile and a quarter of its components / dimensions (TMEM lane quarter q = warp % 4,
 // part = warpgroup - 1).  The control warpgroup hands registers to the row warpgroups with setmaxnreg.
-//
-// Launch order of one call: the parameter fold, then write -> read (bidirectional) or aggregates -> scan
-// -> sweep (causal).  Every kernel after the fold is a programmatic dependent launch: it zeroes its
-// shared tiles, initialises its barriers and allocates TMEM while its predecessor finishes, and executes
-// griddepcontrol.wait in every thread before it reads anything an earlier kernel of the call wrote.
 #include <algorithm>
 #include <cstdio>
 #include <mutex>
