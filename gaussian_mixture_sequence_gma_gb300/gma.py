@@ -22,7 +22,7 @@ GMA_F32, GMA_BF16 = 0, 1
 EXPORTED = ("gma_workspace_bytes", "gma_responsibilities", "gma_forward_bidir", "gma_forward_causal", "gma_forward_cross", "gma_state_bytes", "gma_causal_state", "gma_causal_decode", "gma_backward_bidir", "gma_backward_causal",
             "gma_forward_projected",
             "gma_check_device_error", "gma_status_string", "gma_version", "gma_last_error", "gma_launch_count", "gma_profile_enable",
-            "gma_profile_read", "gma_forward_bidir_static_ws", "gma_static_ws_capacity",
+            "gma_profile_read", "gma_forward_bidir_static_ws", "gma_static_ws_capacity", "gma_static_ws_check_error",
             "gma_debug_withhold_first_load", "gma_probe_ex2_rate")
 
 
@@ -95,6 +95,8 @@ def lib():
     L.gma_forward_bidir_static_ws.restype = ctypes.c_int
     L.gma_static_ws_capacity.argtypes = []
     L.gma_static_ws_capacity.restype = sz
+    L.gma_static_ws_check_error.argtypes = [vp]
+    L.gma_static_ws_check_error.restype = ctypes.c_int
     L.gma_probe_ex2_rate.argtypes = [vp, ctypes.POINTER(ctypes.c_double)]
     L.gma_probe_ex2_rate.restype = ctypes.c_int
     L.gma_debug_withhold_first_load.argtypes = []
@@ -359,7 +361,14 @@ def forward_bidir_static_ws(Q, K, V, mu, sigma2, log_pi, eps=1e-6, out=None, str
     B, H, N, d = Q.shape
     dv = V.shape[-1]
     _params(mu, sigma2, log_pi)
-    dev = _check_cuda(Q, K, V, mu, sigma2, log_pi)
+    # the library reads K and V with Q's element size; a mismatch would read past their buffers
+    if K.dtype != Q.dtype or V.dtype != Q.dtype:
+        raise TypeError("Q, K and V must share one dtype")
+    if tuple(K.shape) != (B, H, N, d) or tuple(V.shape[:3]) != (B, H, N):
+        raise ValueError("K must be [B,H,N,d] and V [B,H,N,dv] with Q's B, H, N")
+    if out is not None and (out.dtype != Q.dtype or tuple(out.shape) != (B, H, N, dv)):
+        raise TypeError("out must have Q's dtype and shape [B,H,N,dv]")
+    dev = _check_cuda(Q, K, V, mu, sigma2, log_pi) if out is None else _check_cuda(Q, K, V, mu, sigma2, log_pi, out)
     prob = problem(B, H, N, mu.shape[1], Q.dtype, eps, d=d, dv=dv)
     if out is None:
         out = torch.empty((B, H, N, dv), dtype=Q.dtype, device=dev)
@@ -373,6 +382,14 @@ def forward_bidir_static_ws(Q, K, V, mu, sigma2, log_pi, eps=1e-6, out=None, str
 
 def static_ws_capacity() -> int:
     return int(lib().gma_static_ws_capacity())
+
+
+def static_ws_check_error(stream=None, device=None) -> int:
+    """Synchronises the stream and returns the status held in the library-held array's error word
+    (the array used by forward_bidir_static_ws on the current device)."""
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        return int(lib().gma_static_ws_check_error(_stream_handle(stream, dev)))
 
 
 def check_device_error(workspace, stream=None) -> int:

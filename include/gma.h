@@ -123,11 +123,13 @@ GMA_API gma_status_t gma_forward_bidir(const gma_problem_t *p, const void *Q, co
  *   - Problems whose gma_workspace_bytes(p, GMA_OP_BIDIR) exceeds gma_static_ws_capacity()
  *     return GMA_ERR_WORKSPACE before launching anything.
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress
- *     with that device current) and caches it; make that first call before any stream capture.
+ *     with that device current) and caches it together with the identity of the current CUDA
+ *     context; a call in another context (for example after cudaDeviceReset) looks it up again.
+ *     Make the first call on a device before any stream capture.
  *   - Every call shares the one array; each call clears what must start at zero.  Calls whose
  *     GPU work overlaps (several streams or host threads) race on it and must be serialised.
- *   - gma_check_device_error() cannot be pointed at this array; timeouts surface as a status
- *     only through the regular entry points.
+ *   - A bounded device wait that runs out sets the error word at the start of the array (the
+ *     call itself has already returned GMA_OK); gma_static_ws_check_error() reads it.
  * Arguments and layouts as gma_forward_bidir, without ws / ws_bytes.
  */
 GMA_API gma_status_t gma_forward_bidir_static_ws(const gma_problem_t *p, const void *Q, const void *K, const void *V,
@@ -136,6 +138,15 @@ GMA_API gma_status_t gma_forward_bidir_static_ws(const gma_problem_t *p, const v
 
 /* Size in bytes of the library-held scratch array used by gma_forward_bidir_static_ws(). */
 GMA_API size_t gma_static_ws_capacity(void);
+
+/*
+ * gma_check_device_error() for the library-held array of gma_forward_bidir_static_ws(): synchronises
+ * `stream`, then reads the array's error word into host memory (allocating nothing).  GMA_OK if no
+ * device wait of the most recent call on the current device timed out, GMA_ERR_TIMEOUT if one did,
+ * GMA_ERR_CUDA if the synchronisation or the copy failed.  Like the entry point it serves, it has no
+ * counterpart in the method.
+ */
+GMA_API gma_status_t gma_static_ws_check_error(void *stream);
 
 /*
  * Causal GMA forward: row i uses the inclusive prefix sums over keys j <= i,

@@ -274,3 +274,27 @@ def test_decode_workspace_size():
         for dt in (gma.GMA_F32, gma.GMA_BF16):
             for N in (1, 64):
                 assert gma.workspace_bytes(P(B=B, H=H, K=K, N=N, dtype=dt), gma.OP_CAUSAL_DECODE) == want
+
+
+def test_static_ws_binding_rejects_mixed_dtypes_before_any_call(L, monkeypatch):
+    """forward_bidir_static_ws checks that K and V share Q's dtype (the library reads them with Q's
+    element size) and that a caller-supplied out matches Q, before anything reaches the library."""
+    import torch
+
+    def never(*a, **k):
+        raise AssertionError("the library must not be called")
+
+    monkeypatch.setattr(gma, "_check_cuda", never)
+    q = torch.zeros(1, 2, 8, 64, dtype=torch.float32)
+    kb = torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16)
+    mu, s2, lp = torch.zeros(2, 4, 64), torch.ones(2, 4, 64), torch.zeros(2, 4)
+    with pytest.raises(TypeError):
+        gma.forward_bidir_static_ws(q, kb, q, mu, s2, lp)
+    with pytest.raises(TypeError):
+        gma.forward_bidir_static_ws(q, q, kb, mu, s2, lp)
+    with pytest.raises(TypeError):
+        gma.forward_bidir_static_ws(q, q, q, mu, s2, lp, out=torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16))
+    with pytest.raises(TypeError):
+        gma.forward_bidir_static_ws(q, q, q, mu, s2, lp, out=torch.zeros(1, 2, 7, 64))
+    with pytest.raises(ValueError):
+        gma.forward_bidir_static_ws(q, torch.zeros(1, 2, 9, 64), q, mu, s2, lp)

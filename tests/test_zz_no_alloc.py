@@ -70,3 +70,22 @@ def test_static_ws_binding_wrapper(gma):
     a = gma.forward_bidir_static_ws(*args).float().cpu().numpy()
     b = gma.forward_bidir(*args).float().cpu().numpy()
     assert rel_err(a, b) <= TOL["bf16"]
+
+
+def test_static_ws_timeout_is_readable_without_allocation(gma):
+    """A bounded wait that runs out inside the allocation-free call (the first key tile withheld by the
+    test hook) leaves GMA_ERR_TIMEOUT in the library-held array's error word; the accessor reads it,
+    and the next call clears it and computes normally."""
+    import torch
+    inp = make_inputs(1, 2, 512, 64, dtype="bf16", seed=41)
+    t = to_device(inp)
+    args = (t["Q"], t["K"], t["V"], t["mu"], t["sigma2"], t["log_pi"])
+    ref = gma.forward_bidir(*args).float().cpu().numpy()
+    gma.forward_bidir_static_ws(*args)
+    assert gma.static_ws_check_error() == gma.GMA_OK
+    gma.lib().gma_debug_withhold_first_load()
+    gma.forward_bidir_static_ws(*args)
+    assert gma.static_ws_check_error() == gma.GMA_ERR_TIMEOUT
+    got = gma.forward_bidir_static_ws(*args).float().cpu().numpy()
+    assert gma.static_ws_check_error() == gma.GMA_OK
+    assert rel_err(got, ref) <= TOL["bf16"]
