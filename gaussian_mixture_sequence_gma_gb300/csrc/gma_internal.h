@@ -54,7 +54,6 @@ struct TcPlan {
   int splits;      // CTAs per (b,h) in the write phase / segments in the causal path
   int seg_tiles;   // tiles per split or segment
   size_t off_w, off_c, off_state;
-  size_t off_gk;  // causal: normalised Gamma_K of every key (empty otherwise)
   size_t total;
 };
 TcPlan tc_plan(const gma_problem_t& p, gma_op_t op);

@@ -27,6 +27,13 @@
 #include <mutex>
 
 #include "gma_tc_common.cuh"
+#include "gma_trace.cuh"
+
+#ifdef GMA_WAIT_NOBO
+#define WAITC wait_bounded
+#else
+#define WAITC wait_bounded_bo
+#endif
 
 namespace gma {
 namespace {
@@ -40,6 +47,9 @@ constexpr int kParts = 4;        // row threads sharing one token row
 // Register split (setmaxnreg): launch pool 640 x 96 = 61440 >= 128 x 56 + 512 x 104 = 60416, and per SM
 // sub-partition (one control warp + four row warps) 32 x (56 + 4 x 104) = 15104 <= 16384.
 constexpr uint32_t kCtrlRegs = 56, kRowRegs = 104;
+// The causal sweep's row code needs 112: 128 x 32 + 512 x 112 = 61440, per SM sub-partition
+// 32 x (32 + 4 x 112) = 15360 (its issuers use rolled loops to fit in 32).
+constexpr uint32_t kCtrlRegsC = 32, kRowRegsC = 112;
 constexpr int kRowWarps = 16;  // arrival count of the barriers the row warps signal
 constexpr int kStCols = 80;  // state row: [Vt (64) | Z | 15 zero]
 constexpr int kCTable = 256;  // c' entries per head (-inf past K)
@@ -370,13 +380,29 @@ __device__ __forceinline__ void store_packed(const float* v, uint32_t ga, const 
     if (cj < nvalid) sts128(ga ^ (uint32_t)(cj << 4), make_uint4(w[4 * cj], w[4 * cj + 1], w[4 * cj + 2], w[4 * cj + 3]));
 }
 
-// The NC/2 bf16 pairs packed in v (exp_pack_regs) times bf16(inv), in place.
+// (a, b) *= (c, d) with one packed float32x2 multiply.
+__device__ __forceinline__ void mul_f32x2(float& a, float& b, float c, float d) {
+  asm("{\n .reg .b64 x, y;\n mov.b64 x, {%0, %1};\n mov.b64 y, {%2, %3};\n mul.rn.f32x2 x, x, y;\n"
+      " mov.b64 {%0, %1}, x;\n}\n"
+      : "+f"(a), "+f"(b)
+      : "f"(c), "f"(d));
+}
+// The NC float32 values of v times inv, rounded to bf16 pairs and stored as 16-byte chunks at ga
+// (gamma_row_addr), below Kp.
 template <int NC>
-__device__ __forceinline__ void scale_packed(float* v, float inv) {
-  __nv_bfloat162* w = reinterpret_cast<__nv_bfloat162*>(v);
-  const __nv_bfloat162 inv2 = __float2bfloat162_rn(inv);
+__device__ __forceinline__ void scale_pack_store(const float* v, float inv, uint32_t ga, const RowCtx& rc, int Kp) {
+  const int nvalid = (Kp - NC * rc.part) >> 3;
 #pragma unroll
-  for (int i = 0; i < NC / 2; ++i) w[i] = __hmul2(w[i], inv2);
+  for (int cj = 0; cj < NC / 8; ++cj) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float t0 = v[8 * cj + 2 * i], t1 = v[8 * cj + 2 * i + 1];
+      mul_f32x2(t0, t1, inv, inv);
+      w[i] = pack_bf16x2(t0, t1);
+    }
+    if (cj < nvalid) sts128(ga ^ (uint32_t)(cj << 4), make_uint4(w[0], w[1], w[2], w[3]));
+  }
 }
 
 // Fused pass for a TMEM-resident operand: e = 2^(v - m) packed to bf16 pairs and stored over this thread's
@@ -498,12 +524,10 @@ __device__ __forceinline__ void store_out16(__nv_bfloat16* dst, const uint32_t* 
 // Gamma_K^T [V | 1] over them into state[bh] (kAtomic) or stores it to state[bh][split] (causal).
 // The bidirectional form normalises each key's Gamma~ row inside the contraction (its [v | 1] row is
 // scaled by 1/s); the causal form (!kAtomic) normalises the Gamma row itself (bf16 gamma = e / s, V as
-// loaded, a constant 1 column) and keeps it for the chunked sweep: through tmG into
-// [B*H][N][64 * ceil(Kp / 64)], stored tile by tile from the shared operand by warp 2.
+// loaded, a constant 1 column).
 template <bool kAtomic, int NC>
 __global__ void __launch_bounds__(kThreadsTc, 1)
-    tc_write_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                    const __grid_constant__ CUtensorMap tmG, TcArgs a) {
+    tc_write_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // 1 KB aligned, still shared
   const uint32_t sbase = smem_u32(smem);
@@ -522,8 +546,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     reinterpret_cast<uint4*>(smem + L.inv)[i] = make_uint4(0, 0, 0, 0);
   __syncthreads();
   // element n = 64 of each token row of the MN-major [V | 1] operand receives 1/s of that key every tile
-  // the Gamma tile is free again once the contraction has read it and (causal) its store has read it
-  if (threadIdx.x == 0) init_bars(&B, kAtomic ? 1u : 2u);
+  // the Gamma tile is free again once the contraction has read it
+  if (threadIdx.x == 0) init_bars(&B, 1u);
   if (warp == 1) {
     tmem_alloc(&B.tmem_base, 512);
     tmem_relinquish();
@@ -559,6 +583,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             ok = wait_bounded(&B.ax_full, (t + 1) & 1, &B.ab, a.ctrl, 22, a.wait_ns) &&
                  wait_bounded(&B.l_empty, t & 1, &B.ab, a.ctrl, 23, a.wait_ns);
             if (!ok) break;
+            GMA_TRACE_AT(22, t);
             tc_fence_after();
             issue_logits(tmem, d_w, a.Kp);
             mma_commit(&B.l_full);
@@ -567,6 +592,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           // the row warps signal g_full after scaling this tile's V rows, so V has landed as well
           ok = wait_bounded(&B.g_full, t & 1, &B.ab, a.ctrl, 24, a.wait_ns);
           if (!ok) break;
+          GMA_TRACE_AT(20, t);
           tc_fence_after();
           const uint64_t d_v = s ? d_v1 : d_v0;
 #pragma unroll
@@ -580,23 +606,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           }
           mma_commit(&B.g_empty);
           mma_commit(&B.v_empty[s]);
+          GMA_TRACE_AT(21, t);
         }
         mma_commit(&B.done);
         Abort none{0};
         wait_bounded(&B.done, 0, &none, a.ctrl, 25, a.wait_ns);
-      }
-    } else if (warp == 2) {
-      if (!kAtomic && lane == 0) {
-        // Gamma_K tile -> global once the row warps have filled it (64-component boxes, rows past N clipped)
-        const int KB = (a.Kp + 63) / 64;
-        for (int t = 0; t < T; ++t) {
-          if (!wait_bounded(&B.g_full, t & 1, &B.ab, a.ctrl, 26, a.wait_ns)) break;
-          for (int j = 0; j < KB; ++j) tma_store_3d(&tmG, sbase + L.g + 16384u * j, 64 * j, (tile0 + t) * kTile, bh);
-          bulk_commit();
-          bulk_wait_read_all();
-          mbar_arrive(&B.g_empty);
-        }
-        bulk_wait_all();
       }
     }
   } else {
@@ -626,8 +640,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       const int s = t & 1;
       const int tok = (tile0 + t) * kTile + rc.row;
       float mp = -INFINITY;
+      if (warp == kRowWarp0) GMA_TRACE_AT(0, t);
       // logits of tile t; the [x^2 | x] columns are free again, so the operand of tile t+1 goes in first
       if (ok) ok = warp_wait(&B.l_full, t & 1, &B.ab, a.ctrl, 32, a.wait_ns);
+      if (warp == kRowWarp0) GMA_TRACE_AT(1, t);
       if (ok) {
         tc_fence_after();
         // x_full of u = t + 1 brings X(t + 1) (if any) and V(t)
@@ -641,20 +657,27 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           warp_arrive(&B.ax_full);
         }
       }
+      if (warp == kRowWarp0) GMA_TRACE_AT(2, t);
       if (ok) {
         mp = load_logits<NC>(tmem, rc, cs, v);
         tc_fence_before();
         warp_arrive(&B.l_empty);
       }
+      if (warp == kRowWarp0) GMA_TRACE_AT(3, t);
       const float m = xchg_max(rc, 0, mp);
+      if (warp == kRowWarp0) GMA_TRACE_AT(4, t);
       if (kAtomic) {
         // Gamma~ row (unnormalised, row maximum 1) -> smem once the previous contraction has read it:
         // exponentiate into registers while the previous contraction may still be reading G, then store
         float sp = 0.f;
         if (ok) sp = exp_pack_regs<NC, true>(v, m);
+        if (warp == kRowWarp0) GMA_TRACE_AT(5, t);
         if (ok && t > 0) ok = warp_wait(&B.g_empty, (t - 1) & 1, &B.ab, a.ctrl, 36, a.wait_ns);
+        if (warp == kRowWarp0) GMA_TRACE_AT(6, t);
         if (ok) store_packed<NC>(v, ga, rc, a.Kp);
+        if (warp == kRowWarp0) GMA_TRACE_AT(7, t);
         const float sum = xchg_sum(rc, 4, sp);
+        if (warp == kRowWarp0) GMA_TRACE_AT(8, t);
         // normalise this key's Gamma row inside the contraction: scale its [v | 1] row by 1/s (0 past N)
         if (ok) {
           const float inv = tok < a.N ? rcp_approx(sum) : 0.f;
@@ -665,18 +688,20 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         // normalised Gamma row (0 past N) -> smem once the previous contraction and store have read it:
         // pack the exponentials to bf16 before the sum exchange, scale the pairs by 1/s after it
         float sp = 0.f;
-        if (ok) sp = exp_pack_regs<NC, true>(v, m);
+        if (ok) sp = exp_inplace<NC>(v, m);
         const float sum = xchg_sum(rc, 4, sp);
         if (ok) {
-          scale_packed<NC>(v, tok < a.N ? rcp_approx(sum) : 0.f);
+          const float inv = tok < a.N ? rcp_approx(sum) : 0.f;
           if (t > 0) ok = warp_wait(&B.g_empty, (t - 1) & 1, &B.ab, a.ctrl, 36, a.wait_ns);
-          if (ok) store_packed<NC>(v, ga, rc, a.Kp);
+          if (ok) scale_pack_store<NC>(v, inv, ga, rc, a.Kp);
         }
       }
+      if (warp == kRowWarp0) GMA_TRACE_AT(9, t);
       if (ok) {
         fence_async_smem();
         warp_arrive(&B.g_full);
       }
+      if (warp == kRowWarp0) GMA_TRACE_AT(10, t);
     }
     // epilogue: state rows of this CTA -> global
     if (ok && T > 0 && rc.part < MB) {
@@ -929,38 +954,39 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 //   O_i = [gq~_i . S_prev + sum_{j in tile, j <= i} (gq~_i . gk_j) [v_j | 1]] / (... + eps s_i),
 //   S  += Gamma_K(tile)^T [V | 1]
 // (gist.science summary, "Variants and training" item 3: prefix sums, O_i depends on j <= i only).
-// The key side of every tile was computed once by the segment aggregates and is loaded here: the
-// normalised Gamma_K rows (bf16), used with V as loaded and a constant 1 column.
+// Both sides of every tile are computed here from Q and K; no responsibilities are read from or
+// written to global memory.
 //
-// Per tile the tensor pipe runs: query logits (A = [x^2 | x] from shared memory) -> state update
-// (overlaps the query softmax) -> inter-tile term Gq~ S_prev and P = Gq~ Gk^T, interleaved -> P [V | 1]
-// after the row warps have masked P.  The next query operand is converted in shared memory while the
-// pipe works, so the next tile's logits follow P [V | 1] at once and run while this tile's output is
-// stored.
-constexpr uint32_t kCColP = 128;   // intra-tile affinity P (fp32 128 cols; bf16 halves at 128 and 192)
+// TMEM: L (columns 0..255) holds, in turn, the key logits, the query logits, then Gamma~_Q (bf16 pairs,
+// columns 0..127) beside P = Gamma~_Q Gamma_K^T (columns 128..255); S (256..415); OX (416..495) holds
+// the [x^2 | x] operand of the key logits, then that of the query logits, then the output accumulator.
+// Three MMA issuers run side by side (each issuing thread waits about 100 cycles per instruction, so
+// the N = 80 / 128 contractions reach the tensor pipe's rate only when several threads issue):
+// warp 1 the logits and the state update, warp 2 the inter-tile term and P [V | 1], warp 3 P.
+constexpr uint32_t kCColP = 128;   // P (fp32 128 columns; bf16 pairs in its first 64 after masking)
 constexpr uint32_t kCColS = 256;   // state accumulators, 80 columns per 128-component block
-constexpr uint32_t kCColO = 416;   // output accumulator (80 columns)
+constexpr uint32_t kCColO = 416;   // logit operands, then the output accumulator (80 columns)
 
 struct CausalLayout {
-  uint32_t w, gk, op, v, sbv, sbz, c, red, total;
+  uint32_t w, gk, xk, xq, v, sbv, sbz, c, red, total;
 };
 __host__ __device__ inline CausalLayout causal_layout(int Kp) {
   CausalLayout s{};
   const int MB = (Kp + 127) / 128;
   s.w = 0;
-  // Gamma~_K tile as loaded: 64-component 128-byte-swizzle boxes 16 KB apart (MN-major A of the state
-  // update, K-major B of P)
+  // normalised Gamma_K tile: 64-component 128-byte-swizzle blocks 16 KB apart (MN-major A of the state
+  // update, K-major B of P), written by the row warps
   s.gk = align1k(Kp * 256);
-  // [x^2 | x] fp16 operand of the query logits: two K-major 128-byte-swizzle blocks of 128 rows x 64;
-  // the query X tile (bf16) lands in the second block and is converted in place
-  s.op = s.gk + MB * 32768;
+  // the key and query X tiles (bf16, 128-byte swizzle), read by the row warps into the logit operand
+  s.xk = s.gk + MB * 32768;
+  s.xq = s.xk + 16384;
   // [V | 1] as one MN-major B of N = 80 in the 32-byte swizzle: four 4 KB atoms of 16 value dims, then
   // the constant atom (column 0 = 1, columns 1..15 zero)
-  s.v = s.op + 32768;
+  s.v = s.xq + 16384;
   // bf16 copy of S_prev [Kp][80] (+ eps in column 64), MN-major B of N = 80, 32-byte swizzle: five
   // atoms of Kp rows x 32 bytes
   s.sbv = s.v + 5 * 4096;
-  s.sbz = s.sbv + 4 * Kp * 32;       // the fifth atom (Z + eps in column 64)
+  s.sbz = s.sbv + 4 * Kp * 32;  // the fifth atom (Z + eps in column 64)
   s.c = s.sbz + Kp * 32;
   s.red = s.c + 1024;
   s.total = s.red + kParts * kTile * 8;
@@ -968,9 +994,10 @@ __host__ __device__ inline CausalLayout causal_layout(int Kp) {
 }
 
 struct CBars {
-  uint64_t w_full, x_full, op_empty, v_full, v_empty, gk_full, gk_empty;
-  uint64_t ax_full, lq_full, gq_full, sb_full, p_full, pb_full, o_full;
-  uint64_t done;
+  uint64_t w_full, xk_full, xk_empty, xq_full, xq_empty, v_full, v_empty;
+  uint64_t ax_full, lk_full, lq_full, gk_full, gk_empty, gq_full, sb_full, s_done, p_full, pb_full, o_full;
+  uint64_t o_staged, o_stored;
+  uint64_t done[3];
   uint32_t tmem_base;
   Abort ab;
 };
@@ -997,31 +1024,33 @@ __device__ __forceinline__ void snapshot_state_chunk(uint32_t sb, int Kp, int co
   }
 }
 
-// Converts token row `row` of the query operand in place: bf16 x (as loaded into the second block of the
-// operand at `op`) -> fp16 x there and fp16 x^2 at the same place of the first block.
-__device__ __forceinline__ void convert_row(uint32_t op, int row) {
-  const uint32_t base = op + 16384u + (uint32_t)row * 128u, sw = (uint32_t)(row & 7);
-#pragma unroll 2
-  for (int c = 0; c < 8; ++c) {
-    const uint32_t ad = base + (((uint32_t)c ^ sw) << 4);
-    const uint4 v = lds128(ad);
-    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-    uint32_t sq[4], lin[4];
+// 8 output dims normalised (acc / den) and packed to bf16 (one 16-byte chunk).
+__device__ __forceinline__ uint4 pack_out8(const uint32_t* acc, float rden) {
+  return make_uint4(pack_bf16x2(__uint_as_float(acc[0]) * rden, __uint_as_float(acc[1]) * rden),
+                    pack_bf16x2(__uint_as_float(acc[2]) * rden, __uint_as_float(acc[3]) * rden),
+                    pack_bf16x2(__uint_as_float(acc[4]) * rden, __uint_as_float(acc[5]) * rden),
+                    pack_bf16x2(__uint_as_float(acc[6]) * rden, __uint_as_float(acc[7]) * rden));
+}
+
+// Scales this thread's 16 value dims (atom `part` of the 32-byte-swizzled [V | 1] operand at vb: four 4 KB
+// atoms of 16 dims, then the constant atom) of the key row rc.row by inv.
+__device__ __forceinline__ void scale_v_row32(uint32_t vb, const RowCtx& rc, float inv) {
+  const __nv_bfloat162 inv2 = __float2bfloat162_rn(inv);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float lo = __uint_as_float(w4[i] << 16), hi = __uint_as_float(w4[i] & 0xffff0000u);
-      lin[i] = pack_f16x2(lo, hi);
-      sq[i] = pack_f16x2(lo * lo, hi * hi);
-    }
-    sts128(ad, make_uint4(lin[0], lin[1], lin[2], lin[3]));
-    sts128(ad - 16384u, make_uint4(sq[0], sq[1], sq[2], sq[3]));
+  for (int c = 0; c < 2; ++c) {
+    const uint32_t ad = vb + 4096u * (uint32_t)rc.part + sw32_chunk(rc.row, c);
+    uint4 x = lds128(ad);
+    __nv_bfloat162* hx = reinterpret_cast<__nv_bfloat162*>(&x);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) hx[q] = __hmul2(hx[q], inv2);
+    sts128(ad, x);
   }
 }
 
 template <int NC>
 __global__ void __launch_bounds__(kThreadsTc, 1)
-    tc_causal_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmG,
-                     const __grid_constant__ CUtensorMap tmV, TcArgs a) {
+    tc_causal_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // 1 KB aligned, still shared
   const uint32_t sbase = smem_u32(smem);
@@ -1032,30 +1061,36 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   const int tile0 = seg * a.seg_tiles;
   const int T = max(0, min(a.tiles, tile0 + a.seg_tiles) - tile0);
   const int MB = (a.Kp + 127) / 128;
-  const int KB = (a.Kp + 63) / 64;
   const int KS = a.Kp / 16;
 
-  // zero the Gamma_K blocks no load reaches (Kp <= 128), the constant atom and the state copies
+  // zero the Gamma_K blocks (components past Kp stay zero: the M = 128 blocks read them), the constant
+  // atom and the state copies
   for (uint32_t i = threadIdx.x; i < (uint32_t)MB * 32768 / 16; i += blockDim.x)
     reinterpret_cast<uint4*>(smem + L.gk)[i] = make_uint4(0, 0, 0, 0);
   for (uint32_t i = threadIdx.x; i < (L.c - (L.v + 16384)) / 16; i += blockDim.x)
     reinterpret_cast<uint4*>(smem + L.v + 16384)[i] = make_uint4(0, 0, 0, 0);
   if (threadIdx.x == 0) {
     mbar_init(&B.w_full, 1);
-    mbar_init(&B.x_full, 1);
-    mbar_init(&B.op_empty, 1);
+    mbar_init(&B.xk_full, 1);
+    mbar_init(&B.xk_empty, kRowWarps);
+    mbar_init(&B.xq_full, 1);
+    mbar_init(&B.xq_empty, kRowWarps);
     mbar_init(&B.v_full, 1);
-    mbar_init(&B.v_empty, 1);
-    mbar_init(&B.gk_full, 1);
-    mbar_init(&B.gk_empty, 1);
-    mbar_init(&B.ax_full, 2);  // warps 2 and 3 build the query operand
+    mbar_init(&B.v_empty, 2);    // the state update and P [V | 1] read V
+    mbar_init(&B.ax_full, kRowWarps);
+    mbar_init(&B.lk_full, 1);
     mbar_init(&B.lq_full, 1);
+    mbar_init(&B.gk_full, kRowWarps);
+    mbar_init(&B.gk_empty, 2);   // the state update and P read Gamma_K
     mbar_init(&B.gq_full, kRowWarps);
     mbar_init(&B.sb_full, kRowWarps);
-    mbar_init(&B.p_full, 1);
+    mbar_init(&B.s_done, 1);
+    mbar_init(&B.p_full, 2);     // the inter-tile term and P
     mbar_init(&B.pb_full, kRowWarps);
     mbar_init(&B.o_full, 1);
-    mbar_init(&B.done, 1);
+    mbar_init(&B.o_staged, kRowWarps);
+    mbar_init(&B.o_stored, 1);
+    for (int i = 0; i < 3; ++i) mbar_init(&B.done[i], 1);
     B.ab.flag = 0;
     mbar_fence_init();
   }
@@ -1071,7 +1106,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   const uint32_t tmem = B.tmem_base;
 
   if (warp < kRowWarp0) {
-    setmaxnreg_dec<kCtrlRegs>();
+    setmaxnreg_dec<kCtrlRegsC>();
     if (warp == 0 && lane == 0) {
       // ---------------------------------------------------------------- producer
       const uint32_t wbytes = (uint32_t)a.Kp * 256, cbytes = kCTable * 4;
@@ -1080,63 +1115,68 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       for (uint32_t o = 0; o < wbytes; o += 32768)
         bulk_load(smem + L.w + o, a.w_img + (size_t)h * wbytes + o, min(32768u, wbytes - o), &B.w_full);
       bulk_load(smem + L.c, a.cbias + (size_t)h * kCTable, cbytes, &B.w_full);
-      int issued[3] = {-1, -1, -1};  // parity of the last load armed on x_full, gk_full, v_full
+      int issued[3] = {-1, -1, -1};  // parity of the last load armed on xk_full, xq_full, v_full
       for (int t = 0; t < T; ++t) {
         const uint32_t pe = (t & 1) ^ 1;
         const int row0 = (tile0 + t) * kTile;
-        // X(t) once the previous logits contraction has read the operand
-        if (!wait_bounded(&B.op_empty, pe, &B.ab, a.ctrl, 70, a.wait_ns)) break;
-        mbar_expect_tx(&B.x_full, 16384);
-        tma_load_3d(smem + L.op + 16384, &tmQ, 0, row0, bh, &B.x_full);
+        // each X slot once the row warps have built the previous tile's operand from it
+        if (!WAITC(&B.xk_empty, pe, &B.ab, a.ctrl, 70, a.wait_ns)) break;
+        mbar_expect_tx(&B.xk_full, 16384);
+        tma_load_3d(smem + L.xk, &tmK, 0, row0, bh, &B.xk_full);
         issued[0] = t & 1;
-        if (!wait_bounded(&B.gk_empty, pe, &B.ab, a.ctrl, 71, a.wait_ns)) break;
-        mbar_expect_tx(&B.gk_full, (uint32_t)KB * 16384u);
-        for (int j = 0; j < KB; ++j) tma_load_3d(smem + L.gk + 16384 * j, &tmG, 64 * j, row0, bh, &B.gk_full);
+        if (!WAITC(&B.xq_empty, pe, &B.ab, a.ctrl, 71, a.wait_ns)) break;
+        mbar_expect_tx(&B.xq_full, 16384);
+        tma_load_3d(smem + L.xq, &tmQ, 0, row0, bh, &B.xq_full);
         issued[1] = t & 1;
-        if (!wait_bounded(&B.v_empty, pe, &B.ab, a.ctrl, 72, a.wait_ns)) break;
+        if (!WAITC(&B.v_empty, pe, &B.ab, a.ctrl, 72, a.wait_ns)) break;
         mbar_expect_tx(&B.v_full, 16384);
         for (int a4 = 0; a4 < 4; ++a4) tma_load_3d(smem + L.v + 4096 * a4, &tmV, 16 * a4, row0, bh, &B.v_full);
         issued[2] = t & 1;
       }
       // never leave with copies in flight
       Abort none{0};
-      if (issued[0] >= 0) wait_bounded(&B.x_full, (uint32_t)issued[0], &none, a.ctrl, 73, a.wait_ns);
-      if (issued[1] >= 0) wait_bounded(&B.gk_full, (uint32_t)issued[1], &none, a.ctrl, 74, a.wait_ns);
-      if (issued[2] >= 0) wait_bounded(&B.v_full, (uint32_t)issued[2], &none, a.ctrl, 75, a.wait_ns);
+      if (issued[0] >= 0) WAITC(&B.xk_full, (uint32_t)issued[0], &none, a.ctrl, 73, a.wait_ns);
+      if (issued[1] >= 0) WAITC(&B.xq_full, (uint32_t)issued[1], &none, a.ctrl, 74, a.wait_ns);
+      if (issued[2] >= 0) WAITC(&B.v_full, (uint32_t)issued[2], &none, a.ctrl, 75, a.wait_ns);
     } else if (warp == 1 && lane == 0) {
-      // ---------------------------------------------------------------- MMA issuer
-      const uint64_t d_w = make_sdesc(smem_u32(smem + L.w), 16, 1024), d_op = make_sdesc(smem_u32(smem + L.op), 16, 1024);
-      // base descriptors; every operand step below is a byte offset added to one of them
-      // [S_prev | Z + eps] (Kp x 80) and [V | 1] (128 x 80): MN-major, 32-byte swizzle, 16 rows = 512 B
-      const uint64_t d_sb = make_sdesc32(smem_u32(smem + L.sbv), (uint32_t)a.Kp * 32, 256);
-      const uint64_t d_vb = make_sdesc32(smem_u32(smem + L.v), 4096, 256);
-      const uint64_t d_gk_k = make_sdesc(smem_u32(smem + L.gk), 16, 1024);     // Gamma_K as K-major B
-      const uint64_t d_gk_mn = make_sdesc(smem_u32(smem + L.gk), 16384, 1024); // Gamma_K^T as MN-major A
-      const uint32_t id_log = make_idesc(128, a.Kp, 0, 0, 0, 0);         // fp16 A and B, both K-major
-      constexpr uint32_t id_c80 = make_idesc(128, kStCols, 1, 1, 0, 1);  // A tmem, B MN-major, N = 80
-      constexpr uint32_t id_p = make_idesc(128, 128, 1, 1, 0, 0);         // P = Gq~ Gk^T
-      constexpr uint32_t id_s80 = make_idesc(128, kStCols, 1, 1, 1, 1);  // A MN-major (Gamma_K^T), B MN-major
-      bool ok = wait_bounded(&B.w_full, 0, &B.ab, a.ctrl, 80, a.wait_ns);
+      // ---------------------------------------------------------------- issuer 1: logits, state update
+      const uint64_t d_w = make_sdesc(smem_u32(smem + L.w), 16, 1024);
+      const uint64_t d_vb = make_sdesc32(smem_u32(smem + L.v), 4096, 256);          // [V | 1], N = 80
+      const uint64_t d_gk_mn = make_sdesc(smem_u32(smem + L.gk), 16384, 1024);     // Gamma_K^T as MN-major A
+      constexpr uint32_t id_s80 = make_idesc(128, kStCols, 1, 1, 1, 1);
+      bool ok = WAITC(&B.w_full, 0, &B.ab, a.ctrl, 80, a.wait_ns);
       for (int t = 0; ok && t < T; ++t) {
         const uint32_t ph = t & 1;
-        // query logits: LOG[128 x Kp] = [x^2 | x] W^T (the previous tile's contractions have completed)
-        if (!(ok = wait_bounded(&B.ax_full, ph, &B.ab, a.ctrl, 81, a.wait_ns))) break;
+        // key logits: the key operand is in OX and L is free (the row warps have taken the previous
+        // tile's output, which follows P [V | 1])
+        if (!(ok = WAITC(&B.ax_full, 0, &B.ab, a.ctrl, 81, a.wait_ns))) break;
+        GMA_TRACE_AT(20, t);
         tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          mma_ss_off(tmem + kColLog, d_op, ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4, d_w,
-                     (ks >> 2) * (uint32_t)a.Kp * 8 + (ks & 3) * 2, id_log, ks > 0);
+        issue_logits(tmem, d_w, a.Kp, kCColO);
+        mma_commit(&B.lk_full);
+        GMA_TRACE_AT(21, t);
+#ifdef GMA_TRACE
+        { Abort none{0}; wait_bounded(&B.lk_full, ph, &none, a.ctrl, 0, a.wait_ns); }
+        GMA_TRACE_AT(26, t);
+#endif
+        // query logits: the row warps have loaded the key logits and put the query operand in OX
+        if (!(ok = WAITC(&B.ax_full, 1, &B.ab, a.ctrl, 82, a.wait_ns))) break;
+        GMA_TRACE_AT(22, t);
+        tc_fence_after();
+        issue_logits(tmem, d_w, a.Kp, kCColO);
         mma_commit(&B.lq_full);
-        mma_commit(&B.op_empty);
-        // state update S += Gamma_K^T [V | 1] while the query softmax runs: needs the loaded Gamma_K and V
-        // tiles and the bf16 snapshot of S_prev taken
-        if (!(ok = wait_bounded(&B.gk_full, ph, &B.ab, a.ctrl, 83, a.wait_ns) &&
-                   wait_bounded(&B.v_full, ph, &B.ab, a.ctrl, 84, a.wait_ns) &&
-                   wait_bounded(&B.sb_full, ph, &B.ab, a.ctrl, 85, a.wait_ns)))
+        GMA_TRACE_AT(23, t);
+#ifdef GMA_TRACE
+        { Abort none{0}; wait_bounded(&B.lq_full, ph, &none, a.ctrl, 0, a.wait_ns); }
+        GMA_TRACE_AT(27, t);
+#endif
+        // S += Gamma_K^T [V | 1] once Gamma_K and V are in and the snapshot of the previous S is taken
+        if (!(ok = WAITC(&B.gk_full, ph, &B.ab, a.ctrl, 83, a.wait_ns) &&
+                   WAITC(&B.v_full, ph, &B.ab, a.ctrl, 84, a.wait_ns) &&
+                   WAITC(&B.sb_full, ph, &B.ab, a.ctrl, 85, a.wait_ns)))
           break;
+        GMA_TRACE_AT(24, t);
         tc_fence_after();
-        // (the contraction loops are unrolled: the issuing thread's own instructions between two MMAs
-        // would otherwise leave the tensor pipe waiting)
 #pragma unroll
         for (int mb = 0; mb < 2; ++mb) {
           if (mb < MB) {
@@ -1146,55 +1186,87 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                          id_s80, 1u);
           }
         }
-        // inter-tile term O = Gq~ S_prev and intra-tile affinity P = Gq~ Gk^T, interleaved
-        if (!(ok = wait_bounded(&B.gq_full, ph, &B.ab, a.ctrl, 86, a.wait_ns))) break;
+        mma_commit(&B.s_done);
+        mma_commit(&B.gk_empty);
+        mma_commit(&B.v_empty);
+        GMA_TRACE_AT(25, t);
+      }
+      mma_commit(&B.done[0]);
+      Abort none{0};
+      WAITC(&B.done[0], 0, &none, a.ctrl, 86, a.wait_ns);
+    } else if (warp == 2 && lane == 0) {
+      // ---------------------------------------------------------------- issuer 2: O = Gq~ S_prev, O += P [V | 1]
+      const uint64_t d_sb = make_sdesc32(smem_u32(smem + L.sbv), (uint32_t)a.Kp * 32, 256);
+      const uint64_t d_vb = make_sdesc32(smem_u32(smem + L.v), 4096, 256);
+      constexpr uint32_t id_c80 = make_idesc(128, kStCols, 1, 1, 0, 1);  // A tmem, B MN-major, N = 80
+      bool ok = true;
+      for (int t = 0; ok && t < T; ++t) {
+        const uint32_t ph = t & 1;
+        if (!(ok = WAITC(&B.gq_full, ph, &B.ab, a.ctrl, 87, a.wait_ns) &&
+                   WAITC(&B.sb_full, ph, &B.ab, a.ctrl, 88, a.wait_ns)))
+          break;
+        GMA_TRACE_AT(30, t);
         tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < 16; ++ks) {
-          if (ks < KS) {
-            const uint32_t aq = tmem + kColLog + 8 * ks;  // Gq~ (bf16 pairs) over the logit columns
-            mma_ts_off(tmem + kCColO, aq, d_sb, (512 * ks) >> 4, id_c80, ks > 0);
-            mma_ts_off(tmem + kCColP, aq, d_gk_k, ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4, id_p, ks > 0);
-          }
-        }
-        mma_commit(&B.p_full);    // also: the inter-tile term has read S_prev
-        mma_commit(&B.gk_empty);  // the state update and P were the last readers of this Gamma_K tile
-        // intra-tile term O += P [V | 1]
-        if (!(ok = wait_bounded(&B.pb_full, ph, &B.ab, a.ctrl, 88, a.wait_ns))) break;
+        // (the issuing thread waits ~100 cycles per instruction here, so a rolled loop costs nothing and
+        // keeps this role's register footprint small)
+#pragma unroll 1
+        for (int ks = 0; ks < KS; ++ks)
+          mma_ts_off(tmem + kCColO, tmem + kColLog + 8 * ks, d_sb, (uint32_t)(512 * ks) >> 4, id_c80, ks > 0);
+        mma_commit(&B.p_full);
+        GMA_TRACE_AT(31, t);
+        if (!(ok = WAITC(&B.pb_full, ph, &B.ab, a.ctrl, 89, a.wait_ns))) break;
+        GMA_TRACE_AT(32, t);
         tc_fence_after();
-#pragma unroll
+#pragma unroll 1
         for (int s = 0; s < 8; ++s) {
           const uint32_t ap = tmem + kCColP + 32 * (s >> 1) + 8 * (s & 1);  // bf16 P of keys 16s..16s+15
-          mma_ts_off(tmem + kCColO, ap, d_vb, (512 * s) >> 4, id_c80, 1u);
+          mma_ts_off(tmem + kCColO, ap, d_vb, (uint32_t)(512 * s) >> 4, id_c80, 1u);
         }
         mma_commit(&B.o_full);
         mma_commit(&B.v_empty);
-        // the next logits overwrite TMEM columns these contractions read: let them complete first
-        if (!(ok = wait_bounded(&B.o_full, ph, &B.ab, a.ctrl, 89, a.wait_ns))) break;
+        GMA_TRACE_AT(33, t);
       }
-      mma_commit(&B.done);
+      mma_commit(&B.done[1]);
       Abort none{0};
-      wait_bounded(&B.done, 0, &none, a.ctrl, 87, a.wait_ns);
-    } else if (warp >= 2) {
-      // ---------------------------------------------------------------- query operand (warps 2, 3)
-      // X(t) lands once the logits of tile t-1 have read the operand; 64 token rows per warp
-      const uint32_t op = sbase + L.op;
-      const int r0 = 64 * (warp - 2) + lane;
-      for (int t = 0; t < T; ++t) {
-        if (!warp_wait(&B.x_full, t & 1, &B.ab, a.ctrl, 91, a.wait_ns)) break;
-        convert_row(op, r0);
-        convert_row(op, r0 + 32);
-        fence_async_smem();
-        warp_arrive(&B.ax_full);
+      WAITC(&B.done[1], 0, &none, a.ctrl, 90, a.wait_ns);
+    } else if (warp == 3 && lane == 0) {
+      // ---------------------------------------------------------------- issuer 3: P = Gq~ Gk^T
+      const uint64_t d_gk_k = make_sdesc(smem_u32(smem + L.gk), 16, 1024);  // Gamma_K as K-major B
+      constexpr uint32_t id_p = make_idesc(128, 128, 1, 1, 0, 0);
+      bool ok = true;
+      for (int t = 0; ok && t < T; ++t) {
+        const uint32_t ph = t & 1;
+        if (!(ok = WAITC(&B.gq_full, ph, &B.ab, a.ctrl, 91, a.wait_ns) &&
+                   WAITC(&B.gk_full, ph, &B.ab, a.ctrl, 92, a.wait_ns)))
+          break;
+        GMA_TRACE_AT(40, t);
+        tc_fence_after();
+#pragma unroll 1
+        for (int ks = 0; ks < KS; ++ks)
+          mma_ts_off(tmem + kCColP, tmem + kColLog + 8 * ks, d_gk_k, (uint32_t)((ks >> 2) * 16384 + (ks & 3) * 32) >> 4,
+                     id_p, ks > 0);
+        mma_commit(&B.p_full);
+        mma_commit(&B.gk_empty);
+        GMA_TRACE_AT(41, t);
+        // the row warps stage the normalised bf16 output tile in the (then unused) first Gamma_K block;
+        // one tensor store writes it (rows past N clipped), then the block is handed back
+        if (!(ok = WAITC(&B.o_staged, ph, &B.ab, a.ctrl, 94, a.wait_ns))) break;
+        tma_store_3d(&tmO, smem_u32(smem + L.gk), 0, (tile0 + t) * kTile, bh);
+        bulk_commit();
+        bulk_wait_read_all();
+        mbar_arrive(&B.o_stored);
       }
+      bulk_wait_all();
+      mma_commit(&B.done[2]);
+      Abort none{0};
+      WAITC(&B.done[2], 0, &none, a.ctrl, 93, a.wait_ns);
     }
   } else {
-    setmaxnreg_inc<kRowRegs>();
+    setmaxnreg_inc<kRowRegsC>();
     // ------------------------------------------------------------------ row warps
     const RowCtx rc = row_ctx(sbase + L.red);
     const uint32_t cs = sbase + L.c;
-    zero_unused_logits<NC>(tmem, rc, a.Kp);
-    if (rc.part == 0) sts16(sbase + L.v + 16384 + sw32_chunk(rc.row, 0), bf16_bits(1.f));  // the 1 column
+    const uint32_t ga = gamma_row_addr<NC>(sbase + L.gk, rc);
     // S <- exclusive prefix state of this segment; SB <- its bf16 copy (eps rides in the Z column)
     if (rc.part < MB) {
       const int comp = 128 * rc.part + rc.row;
@@ -1221,51 +1293,114 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     fence_async_smem();
     tc_fence_before();
     warp_arrive(&B.sb_full);
-    bool ok = warp_wait(&B.w_full, 0, &B.ab, a.ctrl, 90, a.wait_ns);
+    bool ok = warp_wait(&B.w_full, 0, &B.ab, a.ctrl, 100, a.wait_ns);
+    // logit columns past Kp: never written by the logits contractions; zero (with c' = -inf they read as
+    // -inf) or, at Kp <= 128, stale P values (finite, so the same)
+    zero_unused_logits<NC>(tmem, rc, a.Kp);
     float v[NC];
-    // every row warp runs all T tiles and all exchanges (see the write kernel)
+    // every row warp runs all T tiles and all exchanges (see the write kernel); exchange e of the CTA uses
+    // slot (e & 1), three per tile
     for (int t = 0; t < T; ++t) {
       const uint32_t ph = t & 1;
       const int tok = (tile0 + t) * kTile + rc.row;
-      // Gamma_Q~ (unnormalised) -> TMEM over its own logit columns.  The exchange slot alternates with
-      // the tile, so a slot is rewritten only after the next tile's exchange, which every part thread
-      // reaches after reading this one.
-      float mh = -INFINITY;
-      if (ok) ok = warp_wait(&B.lq_full, ph, &B.ab, a.ctrl, 96, a.wait_ns);
+      const uint32_t s0 = (uint32_t)((3 * t) & 1) * 4u, s1 = s0 ^ 4u;
+      if (warp == kRowWarp0) GMA_TRACE_AT(0, t);
+      // key operand -> OX (this thread overwrites only the output columns it read itself last tile)
+      if (ok) ok = warp_wait(&B.xk_full, ph, &B.ab, a.ctrl, 101, a.wait_ns);
+      if (warp == kRowWarp0) GMA_TRACE_AT(1, t);
+      if (ok) {
+        transform_row(sbase + L.xk, rc, tmem, kCColO);
+        warp_arrive(&B.xk_empty);
+        tmem_st_wait();
+        tc_fence_before();
+        warp_arrive(&B.ax_full);
+      }
+      // key logits -> registers; then the query operand -> OX
+      float mk = -INFINITY;
+      if (warp == kRowWarp0) GMA_TRACE_AT(2, t);
+      if (ok) ok = warp_wait(&B.lk_full, ph, &B.ab, a.ctrl, 102, a.wait_ns);
+      if (warp == kRowWarp0) GMA_TRACE_AT(3, t);
+      if (ok) {
+        // the key logits have completed, so OX is free: the query operand goes in first (while no
+        // logits are held in registers), then the key logits are loaded and both L and OX handed over
+        tc_fence_after();
+        ok = warp_wait(&B.xq_full, ph, &B.ab, a.ctrl, 103, a.wait_ns);
+        if (ok) {
+          transform_row(sbase + L.xq, rc, tmem, kCColO);
+          warp_arrive(&B.xq_empty);
+          mk = load_logits<NC>(tmem, rc, cs, v);
+          tmem_st_wait();
+          tc_fence_before();
+          warp_arrive(&B.ax_full);
+        }
+      }
+      if (warp == kRowWarp0) GMA_TRACE_AT(4, t);
+      // key softmax: the unnormalised Gamma~_K row (row maximum 1) -> smem once the previous tile's readers
+      // are done; the key's [v | 1] row is scaled by 1/s (0 past N), which normalises it inside both the
+      // state update and P [V | 1] (P then carries s_j, the scaled row divides it out)
+      const float m_k = xchg_max(rc, s0, mk);
+      if (warp == kRowWarp0) GMA_TRACE_AT(5, t);
+      float sp = 0.f;
+      if (ok && t > 0)
+        ok = warp_wait(&B.gk_empty, (t - 1) & 1, &B.ab, a.ctrl, 104, a.wait_ns) &&
+             warp_wait(&B.o_stored, (t - 1) & 1, &B.ab, a.ctrl, 110, a.wait_ns);
+      if (ok) sp = exp_pack_store<NC, true>(v, m_k, ga, rc, a.Kp);
+      if (warp == kRowWarp0) GMA_TRACE_AT(6, t);
+      const float sum = xchg_sum(rc, s1, sp);
+      if (warp == kRowWarp0) GMA_TRACE_AT(7, t);
+      if (ok) ok = warp_wait(&B.v_full, ph, &B.ab, a.ctrl, 109, a.wait_ns);
+      if (ok) {
+        const float inv = tok < a.N ? rcp_approx(sum) : 0.f;
+        scale_v_row32(sbase + L.v, rc, inv);
+        if (rc.part == 0) sts16(sbase + L.v + 16384 + sw32_chunk(rc.row, 0), bf16_bits(inv));
+        fence_async_smem();
+        warp_arrive(&B.gk_full);
+      }
+      if (warp == kRowWarp0) GMA_TRACE_AT(8, t);
+      // query softmax: Gamma~_Q (unnormalised) -> TMEM over its own logit columns
+      float mq = -INFINITY;
+      if (ok) ok = warp_wait(&B.lq_full, ph, &B.ab, a.ctrl, 105, a.wait_ns);
+      if (warp == kRowWarp0) GMA_TRACE_AT(9, t);
       if (ok) {
         tc_fence_after();
-        mh = load_logits<NC>(tmem, rc, cs, v);
+        mq = load_logits<NC>(tmem, rc, cs, v);
       }
-      const float m = xchg_max(rc, ph * 4u, mh);
+      if (warp == kRowWarp0) GMA_TRACE_AT(10, t);
+      const float m_q = xchg_max(rc, s0, mq);
+      if (warp == kRowWarp0) GMA_TRACE_AT(11, t);
       if (ok) {
-        exp_pack_tmem<NC>(v, m, tmem + rc.lane_base + kColLog + (NC / 2) * rc.part);
+        exp_pack_tmem<NC>(v, m_q, tmem + rc.lane_base + kColLog + (NC / 2) * rc.part);
         tmem_st_wait();
         tc_fence_before();
         warp_arrive(&B.gq_full);
       }
+      if (warp == kRowWarp0) GMA_TRACE_AT(12, t);
       // intra-tile affinity: mask j > i, bf16 over the first half of this thread's own 32 columns
-      if (ok) ok = warp_wait(&B.p_full, ph, &B.ab, a.ctrl, 99, a.wait_ns);
+      if (ok) ok = warp_wait(&B.p_full, ph, &B.ab, a.ctrl, 106, a.wait_ns);
+      if (warp == kRowWarp0) GMA_TRACE_AT(13, t);
       if (ok) {
         tc_fence_after();
         uint32_t pr[32];
         tmem_ld32(tmem + rc.lane_base + kCColP + 32 * rc.part, pr);
         tmem_ld_wait_tied32(pr);
         const int lim = rc.row - 32 * rc.part;  // columns c <= lim are keys j <= i
-        uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const float p0 = (2 * i <= lim) ? __uint_as_float(pr[2 * i]) : 0.f;
           const float p1 = (2 * i + 1 <= lim) ? __uint_as_float(pr[2 * i + 1]) : 0.f;
-          pk[i] = pack_bf16x2(p0, p1);
+          pr[i] = pack_bf16x2(p0, p1);
         }
-        tmem_st16(tmem + rc.lane_base + kCColP + 32 * rc.part, pk);
+        tmem_st16(tmem + rc.lane_base + kCColP + 32 * rc.part, pr);
         tmem_st_wait();
         tc_fence_before();
         warp_arrive(&B.pb_full);
       }
-      // the inter-tile term has read S_prev and the state update has completed (both before p_full):
+      // the inter-tile term has read S_prev (before p_full); once the state update has completed,
       // snapshot the updated state for the next tile.  Parts 0 / 1 take columns 0..31 and Z of state
       // block 0 / 1, parts 2 / 3 columns 32..63.
+      if (warp == kRowWarp0) GMA_TRACE_AT(14, t);
+      if (ok) ok = warp_wait(&B.s_done, ph, &B.ab, a.ctrl, 107, a.wait_ns);
+      if (warp == kRowWarp0) GMA_TRACE_AT(15, t);
       if (ok) {
         tc_fence_after();
         const int mb = rc.part & 1;
@@ -1273,36 +1408,48 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           const int comp = 128 * mb + rc.row;
           const uint32_t ts = tmem + rc.lane_base + kCColS + kStCols * mb;
           const int c0 = rc.part < 2 ? 0 : 2;
-          uint32_t ra[16], rb[16];
-          tmem_ld16(ts + 16 * c0, ra);
-          tmem_ld16(ts + 16 * c0 + 16, rb);
-          uint32_t z = rc.part < 2 ? tmem_ld1(ts + 64) : 0u;
-          tmem_ld_wait_tied16(ra);
-          tmem_ld_wait_tied16(rb);
-          tmem_ld_wait_tied1(z);
-          if (comp < a.Kp) {
-            snapshot_state_chunk(sbase + L.sbv, a.Kp, comp, c0, ra, a.eps);
-            snapshot_state_chunk(sbase + L.sbv, a.Kp, comp, c0 + 1, rb, a.eps);
-            if (rc.part < 2) snapshot_state_chunk(sbase + L.sbv, a.Kp, comp, 4, &z, a.eps);
+          uint32_t ra[16];
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            tmem_ld16(ts + 16 * (c0 + c), ra);
+            tmem_ld_wait_tied16(ra);
+            if (comp < a.Kp) snapshot_state_chunk(sbase + L.sbv, a.Kp, comp, c0 + c, ra, a.eps);
+          }
+          if (rc.part < 2) {
+            uint32_t z = tmem_ld1(ts + 64);
+            tmem_ld_wait_tied1(z);
+            if (comp < a.Kp) snapshot_state_chunk(sbase + L.sbv, a.Kp, comp, 4, &z, a.eps);
           }
         }
         fence_async_smem();
         tc_fence_before();
         warp_arrive(&B.sb_full);
       }
-      // output: this thread's dims 16*part + [0,16) (32 contiguous bytes), normalised by gq~ . (Z + eps)
-      if (ok) ok = warp_wait(&B.o_full, ph, &B.ab, a.ctrl, 100, a.wait_ns);
+      // output: dims 8 part + [0, 8) and 32 + 8 part + [0, 8) -- the columns this thread's part of the
+      // next key operand overwrites -- normalised by gq~ . (Z + eps)
+      if (warp == kRowWarp0) GMA_TRACE_AT(16, t);
+      if (ok) ok = warp_wait(&B.o_full, ph, &B.ab, a.ctrl, 108, a.wait_ns);
+      if (warp == kRowWarp0) GMA_TRACE_AT(17, t);
       if (ok) {
         tc_fence_after();
-        uint32_t o16[16];
-        tmem_ld16(tmem + rc.lane_base + kCColO + 16 * rc.part, o16);
+        uint32_t oa[8], ob[8];
+        tmem_ld8(tmem + rc.lane_base + kCColO + 8 * rc.part, oa);
+        tmem_ld8(tmem + rc.lane_base + kCColO + 32 + 8 * rc.part, ob);
         uint32_t z = tmem_ld1(tmem + rc.lane_base + kCColO + 64);
-        tmem_ld_wait_tied16(o16);
+        tmem_ld_wait_tied8(oa);
+        tmem_ld_wait_tied8(ob);
         tmem_ld_wait_tied1(z);
         const float rden = rcp_approx(__uint_as_float(z));
-        if (tok < a.N)
-          store_out16(reinterpret_cast<__nv_bfloat16*>(a.out) + ((size_t)bh * a.N + tok) * kDv + 16 * rc.part, o16, rden);
+        // Gamma_K's readers (P, state update) have completed (p_full, s_done): its first block takes the
+        // output tile in the 128-byte swizzle of the output tensor map (dims 8 part.. and 32 + 8 part..
+        // are 16-byte chunks part and 4 + part of the token row)
+        const uint32_t orow = sbase + L.gk + rc.rowsw;
+        sts128(orow ^ ((uint32_t)rc.part << 4), pack_out8(oa, rden));
+        sts128(orow ^ ((uint32_t)(4 + rc.part) << 4), pack_out8(ob, rden));
+        fence_async_smem();
+        warp_arrive(&B.o_staged);
       }
+      if (warp == kRowWarp0) GMA_TRACE_AT(18, t);
     }
   }
   tc_fence_before();
@@ -1387,28 +1534,6 @@ bool make_map(CUtensorMap* m, const void* base, int BH, int N, bool sw32 = false
   return r == CUDA_SUCCESS;
 }
 
-// 3-D map over the causal key responsibilities Gamma~_K [B*H][N][ld] bf16 (ld = 64 * ceil(Kp / 64)): box of
-// 64 components x 128 keys in the 128-byte swizzle (the Gamma~ operand tile's blocks), zero fill past N.
-bool make_gamma_map(CUtensorMap* m, const void* base, int BH, int N, int ld) {
-  EncodeTiledFn f = encode_fn();
-  if (!f) {
-    set_error_detail("cuTensorMapEncodeTiled entry point unavailable");
-    return false;
-  }
-  cuuint64_t dims[3] = {(cuuint64_t)ld, (cuuint64_t)N, (cuuint64_t)BH};
-  cuuint64_t strides[2] = {(cuuint64_t)ld * 2, (cuuint64_t)N * ld * 2};
-  cuuint32_t box[3] = {64u, (cuuint32_t)kTile, 1}, es[3] = {1, 1, 1};
-  const CUresult r = f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
-                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) {
-    char msg[96];
-    snprintf(msg, sizeof msg, "cuTensorMapEncodeTiled (Gamma) returned CUresult %d", (int)r);
-    set_error_detail(msg);
-  }
-  return r == CUDA_SUCCESS;
-}
-
 // Dynamic shared memory of a launch: the layout plus alignment slack, never below 116 KB so that
 // exactly one CTA (which owns all 512 TMEM columns) is resident per SM.
 uint32_t smem_bytes(uint32_t layout_total) { return layout_total + 1024 > 116u * 1024 ? layout_total + 1024 : 116u * 1024; }
@@ -1434,19 +1559,17 @@ gma_status_t tc_launch(const gma_problem_t& p, gma_op_t op, int Nk, const TcPlan
     return check_launch("launch tc_resp", (const void*)tc_read_kernel<false, NC>);
   }
   if (op == GMA_OP_CAUSAL) {
-    // Gamma_K of every key (stored by the aggregates, loaded by the sweep); the sweep's V tiles are four
-    // 16-dim boxes in the 32-byte swizzle
-    CUtensorMap mg, mv32;
-    void* gk = (char*)ws + pl.off_gk;
+    // the sweep's V tiles are four 16-dim boxes in the 32-byte swizzle
+    CUtensorMap mv32, mo;
     if (!make_map(&mq, Q, BH, p.N) || !make_map(&mk, K, BH, p.N) || !make_map(&mv, V, BH, p.N) ||
-        !make_map(&mv32, V, BH, p.N, true) || !make_gamma_map(&mg, gk, BH, p.N, (pl.Kp + 63) / 64 * 64))
+        !make_map(&mv32, V, BH, p.N, true) || !make_map(&mo, a.out, BH, p.N))
       return GMA_ERR_CUDA;
-    // a5: segment aggregates (+ Gamma~_K and 1/s of every key); a6: exclusive scan over segments;
-    // a7: chunked sweep
+    // a5: segment aggregates; a6: exclusive scan over segments; a7: chunked sweep (both sides of every
+    // tile recomputed there)
     const uint32_t smem_w = smem_bytes(write_layout(pl.Kp).total);
     if (set_smem_optin((const void*)tc_write_kernel<false, NC>, (int)smem_w, 0) != GMA_OK) return GMA_ERR_CUDA;
     GMA_LAUNCH_DEPENDENT("tc_causal_aggregate", (tc_write_kernel<false, NC>), dim3(pl.splits, BH), kThreadsTc, smem_w,
-                         st, mk, mv, mg, a);
+                         st, mk, mv, a);
     if (gma_status_t e = check_launch("launch tc_causal_aggregate", (const void*)tc_write_kernel<false, NC>)) return e;
     a.fault = 0;
     const int n = pl.Kp * kStCols;
@@ -1454,8 +1577,8 @@ gma_status_t tc_launch(const gma_problem_t& p, gma_op_t op, int Nk, const TcPlan
     if (gma_status_t e = check_launch("launch tc_causal_scan", (const void*)tc_scan_kernel)) return e;
     const uint32_t smem_c = smem_bytes(causal_layout(pl.Kp).total);
     if (set_smem_optin((const void*)tc_causal_kernel<NC>, (int)smem_c, 0) != GMA_OK) return GMA_ERR_CUDA;
-    GMA_LAUNCH_DEPENDENT("tc_causal_chunk", tc_causal_kernel<NC>, dim3(pl.splits, BH), kThreadsTc, smem_c, st, mq, mg,
-                         mv32, a);
+    GMA_LAUNCH_DEPENDENT("tc_causal_chunk", tc_causal_kernel<NC>, dim3(pl.splits, BH), kThreadsTc, smem_c, st, mq, mk,
+                         mv32, mo, a);
     return check_launch("launch tc_causal_chunk", (const void*)tc_causal_kernel<NC>);
   }
   // bidirectional / cross: write over the Nk keys with their own split plan (the state layout does not
@@ -1473,7 +1596,7 @@ gma_status_t tc_launch(const gma_problem_t& p, gma_op_t op, int Nk, const TcPlan
     const uint32_t smem_w = smem_bytes(write_layout(pl.Kp).total);
     if (set_smem_optin((const void*)tc_write_kernel<true, NC>, (int)smem_w, 0) != GMA_OK) return GMA_ERR_CUDA;
     GMA_LAUNCH_DEPENDENT("tc_bidir_write", (tc_write_kernel<true, NC>), dim3(plk.splits, BH), kThreadsTc, smem_w, st,
-                         mk, mv, mk, aw);  // (the third map serves only the causal key store)
+                         mk, mv, aw);
     if (gma_status_t e = check_launch("launch tc_bidir_write", (const void*)tc_write_kernel<true, NC>)) return e;
   }
   if (op == GMA_OP_CAUSAL_STATE) return GMA_OK;  // the state alone
@@ -1505,9 +1628,7 @@ TcPlan tc_plan(const gma_problem_t& p, gma_op_t op) {
   size_t st = 0;
   if (op == GMA_OP_BIDIR || op == GMA_OP_CROSS || op == GMA_OP_CAUSAL_STATE) st = (size_t)BH * t.Kp * kStCols * 4;
   if (op == GMA_OP_CAUSAL) st = (size_t)BH * t.splits * t.Kp * kStCols * 4;  // segment aggregates
-  t.off_gk = t.total = align_up(t.off_state + st);
-  if (op == GMA_OP_CAUSAL)  // normalised Gamma_K of every key (bf16, 64-component blocks)
-    t.total = align_up(t.off_gk + (size_t)BH * p.N * ((t.Kp + 63) / 64 * 64) * 2);
+  t.total = align_up(t.off_state + st);
   return t;
 }
 
@@ -1561,3 +1682,14 @@ void tc_set_fault_injection(uint32_t mask) {
 }
 
 }  // namespace gma
+
+#ifdef GMA_TRACE
+extern "C" GMA_API int gma_debug_trace_read(unsigned long long* host, size_t n) {
+  if (n > (size_t)gma::kTraceIds * gma::kTraceTiles) n = (size_t)gma::kTraceIds * gma::kTraceTiles;
+  return cudaMemcpyFromSymbol(host, gma::g_trace, n * sizeof(unsigned long long)) == cudaSuccess ? 0 : -1;
+}
+extern "C" GMA_API int gma_debug_trace_clear(void) {
+  static unsigned long long zero[gma::kTraceIds * gma::kTraceTiles];
+  return cudaMemcpyToSymbol(gma::g_trace, zero, sizeof zero) == cudaSuccess ? 0 : -1;
+}
+#endif

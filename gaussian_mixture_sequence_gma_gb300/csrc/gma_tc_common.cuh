@@ -11,6 +11,13 @@
 
 #include "gma_internal.h"
 
+#ifndef GMA_WAIT_SPIN
+#define GMA_WAIT_SPIN 4
+#endif
+#ifndef GMA_WAIT_SLEEP_NS
+#define GMA_WAIT_SLEEP_NS 64
+#endif
+
 namespace gma {
 namespace tc {
 
@@ -44,6 +51,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
@@ -66,6 +82,33 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, Abo
   uint64_t t0 = 0;
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 15) == 0) {
+      if (ab->flag) return false;
+      const uint64_t now = global_timer_ns();
+      if (t0 == 0) t0 = now;
+      if (now - t0 > limit_ns) {
+        ab->flag = 1;
+        if (atomicCAS(&ctrl->err, kErrNone, kErrTimeout) == kErrNone) ctrl->err_site = site;
+        return false;
+      }
+    }
+  }
+}
+
+// wait_bounded for a single control thread (producer, MMA issuer): after a few unsuccessful tries it
+// sleeps between tries, so that waiting threads take few issue slots and shared-memory cycles from the
+// row warps.
+__device__ __forceinline__ bool wait_bounded_bo(uint64_t* bar, uint32_t parity, Abort* ab, Ctrl* ctrl, uint32_t site,
+                                                uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  uint64_t t0 = 0;
+  for (uint32_t i = 1;; ++i) {
+#ifdef GMA_WAIT_POLL
+    if (mbar_test_wait(bar, parity)) return true;
+#else
+    if (mbar_try_wait(bar, parity)) return true;
+    if (i >= GMA_WAIT_SPIN) __nanosleep(GMA_WAIT_SLEEP_NS);
+#endif
     if ((i & 15) == 0) {
       if (ab->flag) return false;
       const uint64_t now = global_timer_ns();
@@ -195,6 +238,14 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
         "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t* r) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait_tied8(uint32_t* r) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r[0]),"+r"(r[1]),"+r"(r[2]),"+r"(r[3]),"+r"(r[4]),"+r"(r[5]),"+r"(r[6]),"+r"(r[7]) : : "memory");
 }
 __device__ __forceinline__ uint32_t tmem_ld1(uint32_t taddr) {
   uint32_t r;

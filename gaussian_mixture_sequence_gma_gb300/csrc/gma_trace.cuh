@@ -1,0 +1,22 @@
+// gma_trace.cuh -- optional cycle trace of one CTA (development builds only).
+//
+// Compiled to nothing unless the library is built with -DGMA_TRACE.  A trace build records, for the CTA
+// at grid position (0, 0), clock64() at numbered points of each role's tile loop into a device array
+// of kTraceIds x kTraceTiles slots (point id, tile index), read back with gma_debug_trace_read().
+#pragma once
+
+#ifdef GMA_TRACE
+namespace gma {
+constexpr int kTraceIds = 64, kTraceTiles = 64;
+static __device__ unsigned long long g_trace[kTraceIds * kTraceTiles];  // one per translation unit
+}  // namespace gma
+#define GMA_TRACE_AT(id, t)                                                                        \
+  do {                                                                                             \
+    if (blockIdx.x == 0 && blockIdx.y == 0 && (threadIdx.x & 31) == 0 && (t) < ::gma::kTraceTiles) \
+      ::gma::g_trace[(id) * ::gma::kTraceTiles + (t)] = clock64();                                 \
+  } while (0)
+#else
+#define GMA_TRACE_AT(id, t) \
+  do {                      \
+  } while (0)
+#endif

@@ -153,9 +153,10 @@ GMA_API gma_status_t gma_static_ws_check_error(void *stream);
  *   O_i = gamma_Qi . (sum_{j<=i} gamma_Kj v_j^T) / (gamma_Qi . sum_{j<=i} gamma_Kj + eps).
  * Passage: gist.science summary, "Variants and training" item 3 (prefix sums
  * of the latent memory and normaliser; O at position i depends on j <= i only).
- * Same arguments and layouts as gma_forward_bidir.  With bf16 I/O the workspace grows with N:
- * it holds every key's responsibilities (bf16, B*H*N*64*ceil(K/64) elements), computed once by
- * the segment aggregates and read back by the chunked sweep.
+ * Same arguments and layouts as gma_forward_bidir.  The workspace does not grow with N: it holds
+ * the per-segment prefix states (at most 152 segments over all B*H rows at bf16 I/O); no per-position
+ * responsibilities are stored.  With bf16 I/O the key responsibilities are computed twice -- once for
+ * the segment sums, once inside the chunked sweep -- and never leave the chip.
  */
 GMA_API gma_status_t gma_forward_causal(const gma_problem_t *p, const void *Q, const void *K, const void *V, const float *mu,
                                 const float *sigma2, const float *log_pi, void *O, void *ws, size_t ws_bytes,
