@@ -214,8 +214,25 @@ def to_dev(inp, dev):
     import torch
     t = {k: torch.from_numpy(inp[k]).to(dev) for k in ("mu", "sigma2", "log_pi")}
     for k in ("Q", "K", "V"):
-        t[k] = torch.from_numpy(bf16_bits(inp[k]).view(np.int16)).to(dev).view(torch.bfloat16)
+        if inp.get("dtype", "bf16") == "f32":
+            t[k] = torch.from_numpy(np.ascontiguousarray(inp[k])).to(dev)
+        else:
+            t[k] = torch.from_numpy(bf16_bits(inp[k]).view(np.int16)).to(dev).view(torch.bfloat16)
     return t
+
+
+def rel_err(O, ref):
+    """max |O - O_ref| / max |O_ref| over the compared outputs (the parity measure of the tests)."""
+    O = np.asarray(O, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    return float(np.abs(O - ref).max() / np.abs(ref).max())
+
+
+def parity_rows(N, n=64, seed=0):
+    """Rows compared against the oracle on a long sequence: both ends, tile boundaries, random rows."""
+    r = np.random.Generator(np.random.PCG64(seed))
+    fixed = [0, 1, N - 2, N - 1] + [b for b in (127, 128, 129, 4095, 4096, 65535, 65536) if b < N]
+    return np.unique(np.concatenate([np.array(fixed, dtype=np.int64), r.integers(0, N, size=n, dtype=np.int64)]))
 
 
 def run_gma(args, world, rank, local):
@@ -468,25 +485,25 @@ def run_gma(args, world, rank, local):
         outd = torch.empty((Bd, Hd, 1, 64), dtype=torch.bfloat16, device=dev)
         it = [0]
 
-        def step():
+        def decode_step():
             q, k, v = toks[it[0] % 64]
             it[0] += 1
             gma.causal_decode(q, k, v, di["mu"], di["sigma2"], di["log_pi"], state, 1e-6, out=outd, workspace=wsd)
         for _ in range(5):
-            step()
+            decode_step()
         # 64 steps captured in one CUDA graph, so the device time per step is not hidden behind the
         # host-side cost of a Python call per token; eager timing if capture is not possible
         try:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
                 for _ in range(64):
-                    step()
+                    decode_step()
             g.replay()
             m, _ = timed(g.replay, 5)
             t_step = m / (5 * 64) * 1e-3
             how = "CUDA graph of 64 steps"
         except Exception as exc:  # noqa: BLE001
-            m, _ = timed(step, 200)
+            m, _ = timed(decode_step, 200)
             t_step = m / 200 * 1e-3
             how = "eager (graph capture failed: %s)" % type(exc).__name__
         state_bytes = 2 * Bd * Hd * Kd * 65 * 4  # read + write of the resident state per step
@@ -559,14 +576,61 @@ def run_gma(args, world, rank, local):
             "note": "float32 CUDA-core kernels (no tensor cores yet)"}
         del bi, gO, wsc
 
-    # CPU baseline: the oracle as it stands on a bounded sample of the same workload (rank 0 only)
+    # CPU baseline: the oracle as it stands on a bounded sample of the same workload (rank 0 only).
+    # The same leg measures parity: the timed step's outputs, and every listed workload's, against the
+    # float64 oracle (max |O - O_ref| / max |O_ref|; sampled rows on the long sequences).
     cpu = None
+    parity = None
+    configs = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from oracle import oracle as orc
         n_pos = min(CPU_SAMPLE_N, N)
         dt, units, cores = oracle_sample(inp, n_pos)
         cpu = {"value": units / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": "first %d positions of each of the %d (b,h) units, bidirectional + causal (%.1f s)"
                          % (n_pos, B * H, dt)}
+        step(t["Q"], t["K"], t["V"])
+        torch.cuda.synchronize(dev)
+        rows = parity_rows(N, seed=N)
+        parity = {"workload": w.name, "rows_per_head": int(len(rows)), "tolerance": 2e-2,
+                  "measure": "max |O - O_ref| / max |O_ref| against the float64 oracle"}
+        for form, O_dev, causal in (("bidir", Ob, False), ("causal", Oc, True)):
+            ref = orc.forward(inp["Q"], inp["K"], inp["V"], inp["mu"], inp["sigma2"], inp["log_pi"], w.eps,
+                              causal=causal, rows=rows)
+            parity[form] = rel_err(O_dev.float().cpu().numpy()[:, :, rows], ref)
+        # the listed workloads (configs 1-4): device time per call, fraction of the path roofline, parity
+        configs = {}
+        for name in ("bidir_f32_B1H1N1024K16", "bidir_bf16_B4H8N4096K128", "causal_bf16_B4H8N4096K128",
+                     "causal_lm_bf16_B8H12N2048K256"):
+            wc = workloads()[name]
+            ic = make_workload(wc)
+            tc_ = to_dev(ic, dev)
+            fn = gma.forward_causal if wc.causal else gma.forward_bidir
+            dt_ = torch.float32 if wc.dtype == "f32" else torch.bfloat16
+            pc_ = gma.problem(wc.B, wc.H, wc.N, wc.K, dt_, wc.eps)
+            wsx = gma.alloc_workspace(pc_, gma.OP_CAUSAL if wc.causal else gma.OP_BIDIR, dev)
+            outx = torch.empty((wc.B, wc.H, wc.N, 64), dtype=dt_, device=dev)
+            callx = lambda: fn(tc_["Q"], tc_["K"], tc_["V"], tc_["mu"], tc_["sigma2"], tc_["log_pi"], wc.eps, out=outx,
+                               workspace=wsx)
+            for _ in range(5):
+                callx()
+            reps = 50
+            mx, _ = timed(callx, reps)
+            t_call = mx / reps * 1e-3
+            esz = 4 if wc.dtype == "f32" else 2
+            t_bound = max(flop_per_tokhead(wc.K) / (peaks["bf16"] * 1e12), 2 * wc.K / mufu_rate,
+                          4 * 64 * esz / (peaks["hbm"] * 1e9)) * wc.B * wc.H * wc.N
+            rws = None if wc.B * wc.H * wc.N <= 131072 else parity_rows(wc.N, seed=7)
+            ref = orc.forward(ic["Q"], ic["K"], ic["V"], ic["mu"], ic["sigma2"], ic["log_pi"], wc.eps,
+                              causal=bool(wc.causal), rows=rws)
+            got = outx.float().cpu().numpy()
+            if rws is not None:
+                got = got[:, :, rws]
+            configs[name] = {"ms": t_call * 1e3, "tok_heads_per_s": wc.B * wc.H * wc.N / t_call,
+                             "frac_of_path_roofline": t_bound / t_call, "parity_max_rel_err": rel_err(got, ref),
+                             "parity_rows": "all" if rws is None else "%d per head" % len(rws),
+                             "tolerance": 1e-3 if wc.dtype == "f32" else 2e-2}
+            del wsx, outx, tc_
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -577,7 +641,7 @@ def run_gma(args, world, rank, local):
                 "gpu_launches": int(launches), "roofline": roof, "cpu_baseline": cpu, "clocks": clk,
                 "step_ms_p10_median_p90_l2_flushed": step_dist,
                 "roofline_path": path, "kernels": kernels, "sweep": sweep or None, "extensions": extensions,
-                "mufu_ex2_per_s": mufu_rate}
+                "parity": parity, "configs": configs, "mufu_ex2_per_s": mufu_rate}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()

@@ -278,7 +278,7 @@ gma_status_t gma_check_device_error(void* ws, void* stream) {
   Ctrl c;
   if (cudaMemcpyAsync(&c, ws, sizeof(Ctrl), cudaMemcpyDeviceToHost, st) != cudaSuccess) return GMA_ERR_CUDA;
   if (cudaStreamSynchronize(st) != cudaSuccess) return GMA_ERR_CUDA;
-  return c.err == kErrNone ? GMA_OK : GMA_ERR_TIMEOUT;
+  return c.err == kErrNone ? GMA_OK : (c.err == kErrRange ? GMA_ERR_RANGE : GMA_ERR_TIMEOUT);
 }
 
 const char* gma_status_string(gma_status_t s) {
@@ -289,6 +289,7 @@ const char* gma_status_string(gma_status_t s) {
     case GMA_ERR_WORKSPACE: return "workspace too small";
     case GMA_ERR_CUDA: return "CUDA runtime error";
     case GMA_ERR_TIMEOUT: return "a bounded device wait timed out";
+    case GMA_ERR_RANGE: return "a parameter is outside the range of the fp16 log-density operands";
   }
   return "unknown status";
 }

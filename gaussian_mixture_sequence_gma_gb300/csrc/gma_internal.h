@@ -27,7 +27,7 @@ struct Ctrl {
 static_assert(sizeof(Ctrl) == 256, "control block is one aligned section");
 
 // Device error codes written into Ctrl::err.
-enum : uint32_t { kErrNone = 0, kErrTimeout = 1 };
+enum : uint32_t { kErrNone = 0, kErrTimeout = 1, kErrRange = 2 };
 
 inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
 inline int cdiv(long long a, long long b) { return (int)((a + b - 1) / b); }
@@ -49,11 +49,11 @@ gma_status_t simt_run(const gma_problem_t& p, gma_op_t op, int Nk, const void* Q
 
 // ---- tensor-core (bf16 I/O) path ----------------------------------------------------------------
 struct TcPlan {
-  int Kp;          // K rounded up to a multiple of 16 (MMA N granularity)
+  int Kp;          // K rounded up to 64, 128 or 256: the width of the log-density contraction (4 x the components per row thread)
   int tiles;       // ceil(N / 128)
   int splits;      // CTAs per (b,h) in the write phase / segments in the causal path
   int seg_tiles;   // tiles per split or segment
-  size_t off_w, off_c, off_state;
+  size_t off_w, off_c, off_flags, off_state;  // off_flags: per-head range flags of the parameter fold
   size_t total;
 };
 TcPlan tc_plan(const gma_problem_t& p, gma_op_t op);

@@ -61,6 +61,12 @@ constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s per wait
 constexpr uint32_t kColLog = 0;    // logits, Kp columns (<= 256)
 constexpr uint32_t kColAx = 256;   // [x^2 | x] fp16 operand, 64 columns
 constexpr uint32_t kColAcc = 320;  // write: state accumulators 80 per 128-component block; read: O (80)
+constexpr uint32_t kColOnes = 480; // [256 | 1] fp16 A columns of the constant step of the log-density contraction
+
+// Bytes per head of the prepared B operand of the log-density contraction: the K-major W image
+// (Kp rows x 256 B, two 64-element 128-byte-swizzle blocks) followed by the constant step (Kp rows x 32 B,
+// 32-byte swizzle: c'/256 rounded to fp16 and the fp16 remainder, against A columns [256, 1]).
+__host__ __device__ constexpr uint32_t w_head_bytes(int Kp) { return (uint32_t)Kp * 288u; }
 
 __host__ __device__ constexpr uint32_t align1k(uint32_t x) { return (x + 1023u) & ~1023u; }
 
@@ -73,44 +79,44 @@ __host__ __device__ inline SmemLayout write_layout(int Kp) {
   SmemLayout s{};
   const int MB = (Kp + 127) / 128;
   s.w = 0;
-  s.g = align1k(Kp * 256);
+  s.g = align1k(w_head_bytes(Kp));
   s.x = s.g + MB * 32768;
   s.v = s.x + 2 * 16384;
   s.inv = s.v + 2 * 16384;
   s.sb = s.inv + 16384;
   s.c = s.sb;
-  s.red = s.c + 1024;
+  s.red = s.c;
   s.total = s.red + kParts * kTile * 8;
   return s;
 }
-// read / responsibilities kernel: W | G (K-major Gamma~, ceil(Kp/64) x 16K) | X ring | SB (state operand) | c' | exchange
+// responsibilities kernel: W | X ring | exchange
 __host__ __device__ inline SmemLayout read_layout(int Kp) {
   SmemLayout s{};
-  const int KB = (Kp + 63) / 64;
   s.w = 0;
-  s.g = align1k(Kp * 256);
-  s.x = s.g + KB * 16384;
+  s.g = align1k(w_head_bytes(Kp));
+  s.x = s.g;
   s.v = s.x;
   s.inv = s.x;
   s.sb = s.x + 2 * 16384;
-  s.c = s.sb + KB * (kStCols * 128);
-  s.red = s.c + 1024;
+  s.c = s.sb;
+  s.red = s.c;
   s.total = s.red + kParts * kTile * 8;
   return s;
 }
 
 struct Bars {
-  uint64_t w_full, sb_full;
+  uint64_t w_full;
   uint64_t x_full[2], x_empty[2], v_empty[2];
-  uint64_t ax_full, l_full, l_empty, g_full, g_empty, o_full, o_empty;
-  uint64_t done;
+  uint64_t ax_full, l_full, l_empty, g_full, g_empty;
+  uint64_t done, done_l;
   uint32_t tmem_base;
   Abort ab;
 };
 
 struct TcArgs {
-  const uint8_t* w_img;  // [H][Kp * 256] swizzled fp16 B operand of the log-density contraction
+  const uint8_t* w_img;  // [H][w_head_bytes(Kp)] swizzled fp16 B operand of the log-density contraction
   const float* cbias;    // [H][256] c'_k (log2 domain); -inf past K
+  const uint32_t* range_flags;  // [H][32] non-zero where a block of the parameter fold saw an fp16 overflow
   float* state;          // [BH][Kp][80] (bidir) or [BH][splits][80][Kp] (causal aggregates, column-major)
   Ctrl* ctrl;
   void* out;             // read: O bf16 [BH][N][64]; responsibilities: gamma fp32 [BH][N][K]
@@ -129,44 +135,78 @@ struct TcArgs {
 __global__ void __launch_bounds__(128) tc_prep_kernel(const float* __restrict__ mu, const float* __restrict__ sigma2,
                                                       const float* __restrict__ log_pi, int H, int K, int Kp,
                                                       uint8_t* w_img, float* cbias, Ctrl* ctrl, float* zero,
-                                                      size_t zero_n) {
+                                                      size_t zero_n, uint32_t* range_flags) {
   dep_launch_next();  // the main kernel sets itself up meanwhile and waits for this grid before reading
   const int h = blockIdx.y, k = blockIdx.x * 8 + (threadIdx.x >> 4), q = threadIdx.x & 15;
   const int d0 = 8 * (q & 7);
   uint32_t w[4] = {0u, 0u, 0u, 0u};
   float term = 0.f;
+  int bad = 0;
   if (k < K) {
     const float4* m4 = reinterpret_cast<const float4*>(mu + ((size_t)h * K + k) * kD + d0);
     const float4* s4 = reinterpret_cast<const float4*>(sigma2 + ((size_t)h * K + k) * kD + d0);
     const float4 ma = __ldg(m4), mb = __ldg(m4 + 1), sa = __ldg(s4), sb = __ldg(s4 + 1);
     const float m[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
     const float s2[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
+    // Consistent rounding: a = fp16(-1/2 sigma2^-1 log2 e) first, then b = fp16(-2 a mu), and the constant
+    // carries b^2 / (4 a) = a mu'^2 with mu' = b / (-2 a), so a x^2 + b x + a mu'^2 = a (x - mu')^2 exactly:
+    // the expanded form is the centred one for a mean within 2^-12 |mu| of mu (and a variance within 2^-12
+    // relative), instead of three large terms each rounded on its own that cancel near the best component.
+    // Threads q < 8 hold a (x^2 coefficients of dims d0..d0+7) and sum log sigma2; threads q >= 8 hold b and
+    // sum a mu'^2.
     float val[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const float inv = 1.0f / s2[i];
-      val[i] = (q < 8 ? -0.5f * inv : m[i] * inv) * kLog2e;
-      if (q < 8) term += m[i] * m[i] * inv + logf(s2[i]);
+      const float af = __half2float(__float2half_rn(-0.5f / s2[i] * kLog2e));
+      if (q < 8) {
+        val[i] = af;
+        term += logf(s2[i]);
+      } else {
+        const float bf = __half2float(__float2half_rn(-2.0f * af * m[i]));
+        val[i] = bf;
+        term += (bf * bf) / (4.0f * af);  // a mu'^2 (<= 0)
+      }
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const __half2 p2 = __floats2half2_rn(val[2 * i], val[2 * i + 1]);
+      const __half2 p2 = __floats2half2_rn(val[2 * i], val[2 * i + 1]);  // exact: val is already fp16
       w[i] = *reinterpret_cast<const uint32_t*>(&p2);
+      // fp16 overflow (sigma2 too small, |mu| / sigma2 too large) or a non-finite parameter
+      if (!isfinite(val[2 * i]) || !isfinite(val[2 * i + 1])) bad = 1;
     }
   }
   if (k < Kp)
-    *reinterpret_cast<uint4*>(w_img + (size_t)h * Kp * 256 + sw128_off(k, 8 * q, (uint32_t)Kp * 128)) =
+    *reinterpret_cast<uint4*>(w_img + (size_t)h * w_head_bytes(Kp) + sw128_off(k, 8 * q, (uint32_t)Kp * 128)) =
         make_uint4(w[0], w[1], w[2], w[3]);
-  // c'_k = (log pi_k - 1/2 sum_d (mu^2/sigma2 + log sigma2)) * log2(e); the 16 threads of a component are
-  // an aligned half-warp
+  // c'_k = log pi_k log2(e) + sum_d a mu'^2 - 1/2 log2(e) sum_d log sigma2 (the two partial sums above, kept
+  // apart by the half of the component's 16 threads that formed them; the 16 are an aligned half-warp)
+  float lsum = q < 8 ? term : 0.f, qsum = q < 8 ? 0.f : term;
 #pragma unroll
-  for (int o = 8; o > 0; o >>= 1) term += __shfl_xor_sync(0xffffffffu, term, o);
-  if (q == 0 && k < kCTable)
-    cbias[(size_t)h * kCTable + k] = k < K ? (log_pi[(size_t)h * K + k] - 0.5f * term) * kLog2e : -INFINITY;
+  for (int o = 8; o > 0; o >>= 1) {
+    lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+    qsum += __shfl_xor_sync(0xffffffffu, qsum, o);
+  }
+  const float cprime = k < K ? log_pi[(size_t)h * K + k] * kLog2e + qsum - 0.5f * kLog2e * lsum : -INFINITY;
+  if (q == 0 && k < kCTable) cbias[(size_t)h * kCTable + k] = cprime;
+  if (q == 0 && k < Kp) {
+    // constant step of the contraction: [256 | 1] . [fp16(c'/256) | fp16(c' - 256 fp16(c'/256))] = c' to
+    // about 2^-22 |c'| (-inf past K, so the padding components never win the row maximum)
+    const __half hi = __float2half_rn(k < K ? cprime * (1.0f / 256.0f) : -INFINITY);
+    const __half lo = __float2half_rn(k < K ? cprime - 256.0f * __half2float(hi) : 0.0f);
+    if (k < K && (!isfinite(__half2float(hi)) || !isfinite(__half2float(lo)))) bad = 1;
+    const __half2 hl = __halves2half2(hi, lo);
+    uint8_t* cimg = w_img + (size_t)h * w_head_bytes(Kp) + (size_t)Kp * 256;
+    *reinterpret_cast<uint4*>(cimg + sw32_chunk(k, 0)) = make_uint4(*reinterpret_cast<const uint32_t*>(&hl), 0u, 0u, 0u);
+    *reinterpret_cast<uint4*>(cimg + sw32_chunk(k, 1)) = make_uint4(0u, 0u, 0u, 0u);
+  }
   if (blockIdx.x == 0 && h == 0 && threadIdx.x == 0) {
     ctrl->err = kErrNone;
     ctrl->err_site = 0;
   }
+  // one flag per block, rewritten every call (so nothing needs clearing); the next kernel turns it
+  // into the error word after this grid has completed
+  const int any_bad = __syncthreads_or(bad);
+  if (threadIdx.x == 0) range_flags[blockIdx.y * gridDim.x + blockIdx.x] = any_bad ? 1u : 0u;
   const size_t tid = ((size_t)blockIdx.y * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x;
   const size_t nth = (size_t)gridDim.x * gridDim.y * blockDim.x;
   for (size_t i = tid; i < zero_n; i += nth) zero[i] = 0.f;
@@ -442,38 +482,42 @@ __device__ __forceinline__ uint16_t bf16_bits(float x) {
   return *reinterpret_cast<const uint16_t*>(&h);
 }
 
-__device__ __forceinline__ void init_bars(Bars* B, uint32_t g_release_count) {
+// g_release_count: arrivals that free the Gamma tile / a V slot (the write issuers); x_release_count:
+// arrivals that free an X slot; done_count: issuers that commit to `done`.
+__device__ __forceinline__ void init_bars(Bars* B, uint32_t g_release_count, uint32_t x_release_count,
+                                          uint32_t done_count) {
   mbar_init(&B->w_full, 1);
-  mbar_init(&B->sb_full, kRowWarps);
   for (int s = 0; s < 2; ++s) {
     mbar_init(&B->x_full[s], 1);
-    mbar_init(&B->x_empty[s], kRowWarps);
-    mbar_init(&B->v_empty[s], 1);
+    mbar_init(&B->x_empty[s], x_release_count);
+    mbar_init(&B->v_empty[s], g_release_count);
   }
   mbar_init(&B->ax_full, kRowWarps);
   mbar_init(&B->l_full, 1);
   mbar_init(&B->l_empty, kRowWarps);
   mbar_init(&B->g_full, kRowWarps);
   mbar_init(&B->g_empty, g_release_count);
-  mbar_init(&B->o_full, 1);
-  mbar_init(&B->o_empty, kRowWarps);
-  mbar_init(&B->done, 1);
+  mbar_init(&B->done, done_count);
+  mbar_init(&B->done_l, 1);
   B->ab.flag = 0;
   mbar_fence_init();
 }
 
-// Producer: W image + c' once, then per tile the X tile.  With `tmV` (write kernel), iteration u also
+// Producer: W image (with its constant step) once, then per tile the X tile.  With `tmV` (write kernel), iteration u also
 // brings the V tile of u - 1, on the same barrier x_full[u & 1], so a row warp that has waited for the
 // X tile it builds next also has the V tile of its current key tile; an extra iteration u = T brings
 // the last V tile alone.  The V ring slot of tile t is t & 1, released by the write contraction.
 __device__ __forceinline__ void producer(const TcArgs& a, const CUtensorMap* tmX, const CUtensorMap* tmV,
                                          uint8_t* smem, const SmemLayout& L, Bars* B, int bh, int tile0, int T) {
-  const uint32_t wbytes = (uint32_t)a.Kp * 256, cbytes = kCTable * 4;
+  const uint32_t wbytes = w_head_bytes(a.Kp);
   const int h = bh % a.H;
-  mbar_expect_tx(&B->w_full, wbytes + cbytes);
+  // the parameter fold of this head (complete: this grid waited for it) flagged an fp16 overflow
+  uint32_t bad = 0;
+  for (int i = 0; i < kCTable / 8; ++i) bad |= a.range_flags[h * (kCTable / 8) + i];
+  if (bad) atomicCAS(&a.ctrl->err, kErrNone, kErrRange);
+  mbar_expect_tx(&B->w_full, wbytes);
   for (uint32_t o = 0; o < wbytes; o += 32768)
     bulk_load(smem + L.w + o, a.w_img + (size_t)h * wbytes + o, min(32768u, wbytes - o), &B->w_full);
-  bulk_load(smem + L.c, a.cbias + (size_t)h * kCTable, cbytes, &B->w_full);
   int issued[2] = {-1, -1};  // parity of the last phase armed on x_full[0], x_full[1]
   for (int u = 0; u <= T; ++u) {
     const int s = u & 1;
@@ -508,16 +552,57 @@ __device__ __forceinline__ void issue_logits(uint32_t tmem, uint64_t d_w, int Kp
     mma_ts_off(tmem + kColLog, tmem + col_ax + 8 * ks, d_w, (ks >> 2) * (uint32_t)Kp * 8 + (ks & 3) * 2, idesc,
                ks > 0 ? 1u : 0u);
 }
+// The same plus the constant step (A = the [256 | 1] columns at kColOnes, B = the 32-byte-swizzled c' image
+// d_c), so the logits come out with c'_k added.
+__device__ __forceinline__ void issue_logits_c(uint32_t tmem, uint64_t d_w, uint64_t d_c, int Kp) {
+  issue_logits(tmem, d_w, Kp);
+  mma_ts(tmem + kColLog, tmem + kColOnes, d_c, make_idesc(128, Kp, 0, 0, 0, 0), 1u);
+}
 
-// Normalises 16 output dims of one row (acc / (z + eps s)) and stores them as bf16 (two 16-byte stores).
-__device__ __forceinline__ void store_out16(__nv_bfloat16* dst, const uint32_t* acc, float rden) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
+// Writes the [256 | 1] fp16 pair (and zeros) into the 8 constant-step A columns of this thread's TMEM lane
+// (one thread per lane).
+__device__ __forceinline__ void write_ones_cols(uint32_t tmem, const RowCtx& rc) {
+  uint32_t w[8] = {pack_f16x2(256.0f, 1.0f), 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+  tmem_st8(tmem + rc.lane_base + kColOnes, w);
+}
+
+// Loads this thread's NC logits (components NC*part ..., c' already included) from TMEM in two batches
+// (the maximum of the first overlaps the second load) and returns the part's maximum.
+template <int NC>
+__device__ __forceinline__ float load_logits_c(uint32_t tmem, const RowCtx& rc, float* v) {
+  uint32_t* r = reinterpret_cast<uint32_t*>(v);
+  constexpr int C = NC / 16, C1 = (C + 1) / 2;
+  const uint32_t ta = tmem + rc.lane_base + kColLog + NC * rc.part;
 #pragma unroll
-  for (int c = 0; c < 2; ++c)
-    d[c] = make_uint4(pack_bf16x2(__uint_as_float(acc[8 * c]) * rden, __uint_as_float(acc[8 * c + 1]) * rden),
-                      pack_bf16x2(__uint_as_float(acc[8 * c + 2]) * rden, __uint_as_float(acc[8 * c + 3]) * rden),
-                      pack_bf16x2(__uint_as_float(acc[8 * c + 4]) * rden, __uint_as_float(acc[8 * c + 5]) * rden),
-                      pack_bf16x2(__uint_as_float(acc[8 * c + 6]) * rden, __uint_as_float(acc[8 * c + 7]) * rden));
+  for (int c = 0; c < C1; ++c) tmem_ld16(ta + 16 * c, r + 16 * c);
+#pragma unroll
+  for (int c = 0; c < C1; ++c) tmem_ld_wait_tied16(r + 16 * c);
+#pragma unroll
+  for (int c = C1; c < C; ++c) tmem_ld16(ta + 16 * c, r + 16 * c);
+  float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < 4 * C1; ++i) {
+    m0 = max3(m0, v[4 * i], v[4 * i + 1]);
+    m1 = max3(m1, v[4 * i + 2], v[4 * i + 3]);
+  }
+  if (C > C1) {
+#pragma unroll
+    for (int c = C1; c < C; ++c) tmem_ld_wait_tied16(r + 16 * c);
+#pragma unroll
+    for (int i = 4 * C1; i < 4 * C; ++i) {
+      m0 = max3(m0, v[4 * i], v[4 * i + 1]);
+      m1 = max3(m1, v[4 * i + 2], v[4 * i + 3]);
+    }
+  }
+  return fmaxf(m0, m1);
+}
+
+// 8 output dims normalised (acc / den) and packed to bf16 (one 16-byte chunk).
+__device__ __forceinline__ uint4 pack_out8(const uint32_t* acc, float rden) {
+  return make_uint4(pack_bf16x2(__uint_as_float(acc[0]) * rden, __uint_as_float(acc[1]) * rden),
+                    pack_bf16x2(__uint_as_float(acc[2]) * rden, __uint_as_float(acc[3]) * rden),
+                    pack_bf16x2(__uint_as_float(acc[4]) * rden, __uint_as_float(acc[5]) * rden),
+                    pack_bf16x2(__uint_as_float(acc[6]) * rden, __uint_as_float(acc[7]) * rden));
 }
 // ----------------------------------------------------------------------------------------------- write / aggregate
 // grid (splits, B*H).  CTA (split, bh) covers tiles [split * seg_tiles, ...) of head-row bh and adds
@@ -545,9 +630,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   for (uint32_t i = threadIdx.x; i < 16384 / 16; i += blockDim.x)
     reinterpret_cast<uint4*>(smem + L.inv)[i] = make_uint4(0, 0, 0, 0);
   __syncthreads();
-  // element n = 64 of each token row of the MN-major [V | 1] operand receives 1/s of that key every tile
-  // the Gamma tile is free again once the contraction has read it
-  if (threadIdx.x == 0) init_bars(&B, 1u);
+  // element n = 64 of each token row of the MN-major [V | 1] operand receives 1/s of that key every tile;
+  // the Gamma tile and the V slot are free again once every write issuer (one per 128-component block)
+  // has read them
+  if (threadIdx.x == 0) init_bars(&B, (uint32_t)MB, (uint32_t)kRowWarps, (uint32_t)MB);
   if (warp == 1) {
     tmem_alloc(&B.tmem_base, 512);
     tmem_relinquish();
@@ -564,62 +650,62 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       if (lane == 0) producer(a, &tmK, &tmV, smem, L, &B, bh, tile0, T);
     } else if (warp == 1) {
       if (lane == 0) {
+        // issuer 1: the log-density contraction of every tile (into L once the row warps have taken the
+        // previous logits and built this tile's operand)
+        const uint32_t w_addr = smem_u32(smem + L.w);
+        const uint64_t d_w = make_sdesc(w_addr, 16, 1024), d_c = make_sdesc32(w_addr + (uint32_t)a.Kp * 256, 16, 256);
+        bool ok = wait_bounded(&B.w_full, 0, &B.ab, a.ctrl, 20, a.wait_ns);
+        for (int t = 0; ok && t < T; ++t) {
+          ok = wait_bounded(&B.ax_full, t & 1, &B.ab, a.ctrl, 22, a.wait_ns) &&
+               (t == 0 || wait_bounded(&B.l_empty, (t - 1) & 1, &B.ab, a.ctrl, 23, a.wait_ns));
+          if (!ok) break;
+          GMA_TRACE_AT(52, t);
+          tc_fence_after();
+          issue_logits_c(tmem, d_w, d_c, a.Kp);
+          mma_commit(&B.l_full);  // also frees the [x^2 | x] columns for the next tile
+        }
+        mma_commit(&B.done_l);
+        Abort none{0};
+        wait_bounded(&B.done_l, 0, &none, a.ctrl, 25, a.wait_ns);
+      }
+    } else if (warp - 2 < MB) {
+      if (lane == 0) {
+        // issuers 2 / 3: component block mb = warp - 2 of the write contraction, Gamma~_K^T [V/s | 1/s]
+        const int mb = warp - 2;
         const uint32_t idw = make_idesc(128, kStCols, 1, 1, 1, 1);
-        const uint32_t w_addr = smem_u32(smem + L.w), g_addr = smem_u32(smem + L.g);
+        const uint32_t g_addr = smem_u32(smem + L.g) + (uint32_t)mb * 32768u;
         const uint32_t v_addr = smem_u32(smem + L.v), inv_addr = smem_u32(smem + L.inv);
-        const uint64_t d_w = make_sdesc(w_addr, 16, 1024), d_g = make_sdesc(g_addr, 16384, 1024);
+        const uint64_t d_g = make_sdesc(g_addr, 16384, 1024);
         // [V | 1] of ring slot s: MN-major, the 1 atom one leading-dimension step past the V atom
         const uint64_t d_v0 = make_sdesc(v_addr, inv_addr - v_addr, 1024);
         const uint64_t d_v1 = make_sdesc(v_addr + 16384, inv_addr - v_addr - 16384, 1024);
-        bool ok = wait_bounded(&B.w_full, 0, &B.ab, a.ctrl, 20, a.wait_ns);
-        if (ok && T > 0) ok = wait_bounded(&B.ax_full, 0, &B.ab, a.ctrl, 21, a.wait_ns);
-        if (ok && T > 0) {
-          tc_fence_after();
-          issue_logits(tmem, d_w, a.Kp);
-          mma_commit(&B.l_full);  // also frees the [x^2 | x] columns for the next tile
-        }
+        bool ok = true;
         for (int t = 0; ok && t < T; ++t) {
-          if (t + 1 < T) {
-            ok = wait_bounded(&B.ax_full, (t + 1) & 1, &B.ab, a.ctrl, 22, a.wait_ns) &&
-                 wait_bounded(&B.l_empty, t & 1, &B.ab, a.ctrl, 23, a.wait_ns);
-            if (!ok) break;
-            GMA_TRACE_AT(22, t);
-            tc_fence_after();
-            issue_logits(tmem, d_w, a.Kp);
-            mma_commit(&B.l_full);
-          }
           const int s = t & 1;
           // the row warps signal g_full after scaling this tile's V rows, so V has landed as well
           ok = wait_bounded(&B.g_full, t & 1, &B.ab, a.ctrl, 24, a.wait_ns);
           if (!ok) break;
-          GMA_TRACE_AT(20, t);
+          GMA_TRACE_AT(20 + mb, t);
           tc_fence_after();
           const uint64_t d_v = s ? d_v1 : d_v0;
 #pragma unroll
-          for (int mb = 0; mb < 2; ++mb) {
-            if (mb < MB) {
-#pragma unroll
-              for (int ks = 0; ks < 8; ++ks)
-                mma_ss_off(tmem + kColAcc + kStCols * mb, d_g, (mb * 32768 + ks * 2048) >> 4, d_v, (ks * 2048) >> 4, idw,
-                           (t > 0 || ks > 0) ? 1u : 0u);
-            }
-          }
+          for (int ks = 0; ks < 8; ++ks)
+            mma_ss_off(tmem + kColAcc + kStCols * mb, d_g, (ks * 2048) >> 4, d_v, (ks * 2048) >> 4, idw,
+                       (t > 0 || ks > 0) ? 1u : 0u);
           mma_commit(&B.g_empty);
           mma_commit(&B.v_empty[s]);
-          GMA_TRACE_AT(21, t);
         }
         mma_commit(&B.done);
         Abort none{0};
-        wait_bounded(&B.done, 0, &none, a.ctrl, 25, a.wait_ns);
+        wait_bounded(&B.done, 0, &none, a.ctrl, 26, a.wait_ns);
       }
     }
   } else {
     setmaxnreg_inc<kRowRegs>();
     // ------------------------------------------------------------------ row warps
     const RowCtx rc = row_ctx(sbase + L.red);
-    const uint32_t cs = sbase + L.c;
     const uint32_t ga = gamma_row_addr<NC>(sbase + L.g, rc);
-    zero_unused_logits<NC>(tmem, rc, a.Kp);
+    if (rc.part == 0) write_ones_cols(tmem, rc);
     // causal: element n = 64 of every row of the [V | 1] operand is 1 (rows past N have a zero gamma row)
     if (!kAtomic && rc.part == 0) sts16(sbase + L.inv + rc.rowsw, bf16_bits(1.f));
     bool ok = warp_wait(&B.w_full, 0, &B.ab, a.ctrl, 30, a.wait_ns);
@@ -640,10 +726,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       const int s = t & 1;
       const int tok = (tile0 + t) * kTile + rc.row;
       float mp = -INFINITY;
-      if (warp == kRowWarp0) GMA_TRACE_AT(0, t);
+      if (warp == kRowWarp0) GMA_TRACE_AT(30, t);
       // logits of tile t; the [x^2 | x] columns are free again, so the operand of tile t+1 goes in first
       if (ok) ok = warp_wait(&B.l_full, t & 1, &B.ab, a.ctrl, 32, a.wait_ns);
-      if (warp == kRowWarp0) GMA_TRACE_AT(1, t);
+      if (warp == kRowWarp0) GMA_TRACE_AT(31, t);
       if (ok) {
         tc_fence_after();
         // x_full of u = t + 1 brings X(t + 1) (if any) and V(t)
@@ -657,27 +743,27 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           warp_arrive(&B.ax_full);
         }
       }
-      if (warp == kRowWarp0) GMA_TRACE_AT(2, t);
+      if (warp == kRowWarp0) GMA_TRACE_AT(32, t);
       if (ok) {
-        mp = load_logits<NC>(tmem, rc, cs, v);
+        mp = load_logits_c<NC>(tmem, rc, v);
         tc_fence_before();
         warp_arrive(&B.l_empty);
       }
-      if (warp == kRowWarp0) GMA_TRACE_AT(3, t);
+      if (warp == kRowWarp0) GMA_TRACE_AT(33, t);
       const float m = xchg_max(rc, 0, mp);
-      if (warp == kRowWarp0) GMA_TRACE_AT(4, t);
+      if (warp == kRowWarp0) GMA_TRACE_AT(34, t);
       if (kAtomic) {
         // Gamma~ row (unnormalised, row maximum 1) -> smem once the previous contraction has read it:
         // exponentiate into registers while the previous contraction may still be reading G, then store
         float sp = 0.f;
         if (ok) sp = exp_pack_regs<NC, true>(v, m);
-        if (warp == kRowWarp0) GMA_TRACE_AT(5, t);
+        if (warp == kRowWarp0) GMA_TRACE_AT(35, t);
         if (ok && t > 0) ok = warp_wait(&B.g_empty, (t - 1) & 1, &B.ab, a.ctrl, 36, a.wait_ns);
-        if (warp == kRowWarp0) GMA_TRACE_AT(6, t);
+        if (warp == kRowWarp0) GMA_TRACE_AT(36, t);
         if (ok) store_packed<NC>(v, ga, rc, a.Kp);
-        if (warp == kRowWarp0) GMA_TRACE_AT(7, t);
+        if (warp == kRowWarp0) GMA_TRACE_AT(37, t);
         const float sum = xchg_sum(rc, 4, sp);
-        if (warp == kRowWarp0) GMA_TRACE_AT(8, t);
+        if (warp == kRowWarp0) GMA_TRACE_AT(38, t);
         // normalise this key's Gamma row inside the contraction: scale its [v | 1] row by 1/s (0 past N)
         if (ok) {
           const float inv = tok < a.N ? rcp_approx(sum) : 0.f;
@@ -696,12 +782,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           if (ok) scale_pack_store<NC>(v, inv, ga, rc, a.Kp);
         }
       }
-      if (warp == kRowWarp0) GMA_TRACE_AT(9, t);
+      if (warp == kRowWarp0) GMA_TRACE_AT(39, t);
       if (ok) {
         fence_async_smem();
         warp_arrive(&B.g_full);
       }
-      if (warp == kRowWarp0) GMA_TRACE_AT(10, t);
+      if (warp == kRowWarp0) GMA_TRACE_AT(40, t);
     }
     // epilogue: state rows of this CTA -> global
     if (ok && T > 0 && rc.part < MB) {
@@ -736,11 +822,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   }
 }
 
-// ----------------------------------------------------------------------------------------------- read / responsibilities
-// kRead: grid (splits, B*H); reads state[bh] and writes O.  !kRead: writes normalised Gamma (fp32).
-template <bool kRead, int NC>
-__global__ void __launch_bounds__(kThreadsTc, 1)
-    tc_read_kernel(const __grid_constant__ CUtensorMap tmQ, TcArgs a) {
+// ----------------------------------------------------------------------------------------------- responsibilities
+// a8: grid (splits, B*H); writes the normalised Gamma (float32 [BH][N][K]) of every token: the logits
+// (issuer 1, c' included by the constant step) and a float32 softmax over k in the row warps.
+template <int NC>
+__global__ void __launch_bounds__(kThreadsTc, 1) tc_resp_kernel(const __grid_constant__ CUtensorMap tmQ, TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // 1 KB aligned, still shared
   const uint32_t sbase = smem_u32(smem);
@@ -750,9 +836,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   const int bh = blockIdx.y, split = blockIdx.x;
   const int tile0 = split * a.seg_tiles;
   const int T = max(0, min(a.tiles, tile0 + a.seg_tiles) - tile0);
-  const int KS = a.Kp / 16;  // contraction steps of the read
 
-  if (threadIdx.x == 0) init_bars(&B, 1u);
+  if (threadIdx.x == 0) init_bars(&B, 1u, (uint32_t)kRowWarps, 1u);
   if (warp == 1) {
     tmem_alloc(&B.tmem_base, 512);
     tmem_relinquish();
@@ -760,89 +845,35 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  dep_wait();  // the write (and before it the parameter fold) of this call are complete
+  dep_wait();  // the parameter fold of this call is complete
   const uint32_t tmem = B.tmem_base;
   if (warp < kRowWarp0) {
     setmaxnreg_dec<kCtrlRegs>();
     if (warp == 0) {
-    if (lane == 0) producer(a, &tmQ, nullptr, smem, L, &B, bh, tile0, T);
-  } else if (warp == 1) {
-    if (lane == 0) {
-      const uint32_t idr = make_idesc(128, kStCols, 1, 1, 0, 0);
-      const uint32_t w_addr = smem_u32(smem + L.w), g_addr = smem_u32(smem + L.g), sb_addr = smem_u32(smem + L.sb);
-      const uint64_t d_w = make_sdesc(w_addr, 16, 1024), d_g = make_sdesc(g_addr, 16, 1024);
-      const uint64_t d_sb = make_sdesc(sb_addr, 16, 1024);
-      bool ok = wait_bounded(&B.w_full, 0, &B.ab, a.ctrl, 40, a.wait_ns);
-      if (kRead && ok) ok = wait_bounded(&B.sb_full, 0, &B.ab, a.ctrl, 41, a.wait_ns);
-      if (ok && T > 0) ok = wait_bounded(&B.ax_full, 0, &B.ab, a.ctrl, 42, a.wait_ns);
-      if (ok && T > 0) {
-        tc_fence_after();
-        issue_logits(tmem, d_w, a.Kp);
-        mma_commit(&B.l_full);  // also frees the [x^2 | x] columns for the next tile
-      }
-      for (int t = 0; ok && t < T; ++t) {
-        if (t + 1 < T) {
-          ok = wait_bounded(&B.ax_full, (t + 1) & 1, &B.ab, a.ctrl, 43, a.wait_ns) &&
-               wait_bounded(&B.l_empty, t & 1, &B.ab, a.ctrl, 44, a.wait_ns);
+      if (lane == 0) producer(a, &tmQ, nullptr, smem, L, &B, bh, tile0, T);
+    } else if (warp == 1) {
+      if (lane == 0) {
+        const uint32_t w_addr = smem_u32(smem + L.w);
+        const uint64_t d_w = make_sdesc(w_addr, 16, 1024), d_c = make_sdesc32(w_addr + (uint32_t)a.Kp * 256, 16, 256);
+        bool ok = wait_bounded(&B.w_full, 0, &B.ab, a.ctrl, 40, a.wait_ns);
+        for (int t = 0; ok && t < T; ++t) {
+          ok = wait_bounded(&B.ax_full, t & 1, &B.ab, a.ctrl, 43, a.wait_ns) &&
+               (t == 0 || wait_bounded(&B.l_empty, (t - 1) & 1, &B.ab, a.ctrl, 44, a.wait_ns));
           if (!ok) break;
           tc_fence_after();
-          issue_logits(tmem, d_w, a.Kp);
-          mma_commit(&B.l_full);
+          issue_logits_c(tmem, d_w, d_c, a.Kp);
+          mma_commit(&B.l_full);  // also frees the [x^2 | x] columns for the next tile
         }
-        if (kRead) {
-          ok = wait_bounded(&B.g_full, t & 1, &B.ab, a.ctrl, 45, a.wait_ns);
-          if (ok && t > 0) ok = wait_bounded(&B.o_empty, (t - 1) & 1, &B.ab, a.ctrl, 46, a.wait_ns);
-          if (!ok) break;
-          tc_fence_after();
-#pragma unroll
-          for (int ks = 0; ks < 16; ++ks) {
-            if (ks < KS)
-              mma_ss_off(tmem + kColAcc, d_g, ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4, d_sb,
-                         ((ks >> 2) * (kStCols * 128) + (ks & 3) * 32) >> 4, idr, ks > 0 ? 1u : 0u);
-          }
-          mma_commit(&B.g_empty);
-          mma_commit(&B.o_full);
-        }
+        mma_commit(&B.done_l);
+        Abort none{0};
+        wait_bounded(&B.done_l, 0, &none, a.ctrl, 47, a.wait_ns);
       }
-      mma_commit(&B.done);
-      Abort none{0};
-      wait_bounded(&B.done, 0, &none, a.ctrl, 47, a.wait_ns);
-    }
     }
   } else {
     setmaxnreg_inc<kRowRegs>();
     const RowCtx rc = row_ctx(sbase + L.red);
-    const uint32_t cs = sbase + L.c;
-    const uint32_t ga = gamma_row_addr<NC>(sbase + L.g, rc);
-    zero_unused_logits<NC>(tmem, rc, a.Kp);
-    bool ok = true;
-    if (kRead) {
-      // state [Kp][80] fp32 -> bf16 K-major operand SB[n][comp]; the 512 row threads read it as
-      // consecutive float4 (column kDv holds Z; eps is folded in once here so gamma~ . (Z + eps) is one
-      // contraction column)
-      const float4* src = reinterpret_cast<const float4*>(a.state + (size_t)bh * a.Kp * kStCols);
-      const int nq = a.Kp * (kStCols / 4), nt = 32 * (kThreadsTc / 32 - kRowWarp0);
-      for (int i0 = threadIdx.x - 32 * kRowWarp0; i0 < nq; i0 += 10 * nt) {
-        float4 f[10];  // all of a thread's loads in flight before the first store (Kp <= 256: one pass)
-#pragma unroll
-        for (int u = 0; u < 10; ++u)
-          if (i0 + u * nt < nq) f[u] = __ldg(src + i0 + u * nt);
-#pragma unroll
-        for (int u = 0; u < 10; ++u) {
-          const int i = i0 + u * nt;
-          if (i < nq) {
-            const int comp = i / (kStCols / 4), c = i - comp * (kStCols / 4);
-            const float e[4] = {c == kDv / 4 ? f[u].x + a.eps : f[u].x, f[u].y, f[u].z, f[u].w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              sts16(sbase + L.sb + sw128_off(4 * c + j, comp, kStCols * 128), bf16_bits(e[j]));
-          }
-        }
-      }
-      fence_async_smem();
-      warp_arrive(&B.sb_full);
-    }
-    ok = warp_wait(&B.w_full, 0, &B.ab, a.ctrl, 50, a.wait_ns);
+    if (rc.part == 0) write_ones_cols(tmem, rc);
+    bool ok = warp_wait(&B.w_full, 0, &B.ab, a.ctrl, 50, a.wait_ns);
     if (ok && T > 0) {
       ok = warp_wait(&B.x_full[0], 0, &B.ab, a.ctrl, 51, a.wait_ns);
       if (ok) {
@@ -873,71 +904,354 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         }
       }
       if (ok) {
-        mp = load_logits<NC>(tmem, rc, cs, v);
+        mp = load_logits_c<NC>(tmem, rc, v);
         tc_fence_before();
         warp_arrive(&B.l_empty);
       }
       const int tok = (tile0 + t) * kTile + rc.row;
-      if (kRead) {
-        // one exchange per tile, alternating slots: a slot is rewritten only after the next exchange
-        const float m = xchg_max(rc, (uint32_t)(t & 1) * 4u, mp);
-        // unnormalised gamma~ = 2^(v - m); the read divides by gamma~ . (Z + eps) = gamma~ . Z + eps s
-        if (ok && t > 0) ok = warp_wait(&B.g_empty, (t - 1) & 1, &B.ab, a.ctrl, 56, a.wait_ns);
-        if (ok) {
-          exp_pack_store<NC, false>(v, m, ga, rc, a.Kp);
-          fence_async_smem();
-          warp_arrive(&B.g_full);
-        }
-        // epilogue of the previous tile (its read contraction has had a whole tile to finish)
-        if (ok && t > 0) {
-          ok = warp_wait(&B.o_full, (t - 1) & 1, &B.ab, a.ctrl, 58, a.wait_ns);
-          if (ok) {
-            tc_fence_after();
-            uint32_t r[16];
-            tmem_ld16(tmem + rc.lane_base + kColAcc + 16 * rc.part, r);
-            uint32_t zc = tmem_ld1(tmem + rc.lane_base + kColAcc + 64);  // gamma~ . (Z + eps)
-            tmem_ld_wait_tied1(zc);
-            tmem_ld_wait_tied16(r);
-            tc_fence_before();
-            warp_arrive(&B.o_empty);
-            const int ptok = tok - kTile;
-            const float rden = rcp_approx(__uint_as_float(zc));
-            if (ptok < a.N)
-              store_out16(reinterpret_cast<__nv_bfloat16*>(a.out) + ((size_t)bh * a.N + ptok) * kDv + 16 * rc.part,
-                          r, rden);
-          }
-        }
-      } else {
-        // responsibilities: gamma = 2^(v - m) / s in float32
-        const float m = xchg_max(rc, 0, mp);
-        float sp = 0.f;
-        if (ok) sp = exp_inplace<NC>(v, m);
-        const float sum = xchg_sum(rc, 4, sp);
-        if (ok && tok < a.N) {
-          const float r = 1.0f / sum;
-          float* dst = reinterpret_cast<float*>(a.out) + ((size_t)bh * a.N + tok) * a.K + NC * rc.part;
-          const int nk = min(max(a.K - NC * rc.part, 0), NC);
+      // gamma = 2^(v - m) / s in float32
+      const float m = xchg_max(rc, 0, mp);
+      float sp = 0.f;
+      if (ok) sp = exp_inplace<NC>(v, m);
+      const float sum = xchg_sum(rc, 4, sp);
+      if (ok && tok < a.N) {
+        const float r = 1.0f / sum;
+        float* dst = reinterpret_cast<float*>(a.out) + ((size_t)bh * a.N + tok) * a.K + NC * rc.part;
+        const int nk = min(max(a.K - NC * rc.part, 0), NC);
 #pragma unroll
-          for (int k = 0; k < NC; ++k)
-            if (k < nk) dst[k] = v[k] * r;
+        for (int k = 0; k < NC; ++k)
+          if (k < nk) dst[k] = v[k] * r;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ----------------------------------------------------------------------------------------------- read (two groups)
+// Bidirectional read with two tiles in flight.  The 16 row warps form two groups of 8; group g takes the
+// tiles t with t & 1 == g and owns TMEM columns 256 g .. 256 g + 255, which hold in turn the tile's
+// logits, then Gamma~_Q (bf16 pairs, compacted in place) beside the output accumulator.  Within a group
+// two threads share a token row (half h owns components h NC2 .. h NC2 + NC2 - 1) and stream their
+// logits from TMEM twice (maximum, then exponentials), so few registers are live and the other group's
+// tile proceeds meanwhile.  The [x^2 | x] operand of the logits is built in shared memory (TMEM has no
+// room for it), so the log-density contraction reads both operands from shared memory.  Issuer g
+// (warp 1 + g) issues group g's logits and read contractions and its output tile stores.
+struct R2Layout {
+  uint32_t w, a0, ones, sb, stg0, red, total;
+};
+__host__ __device__ inline R2Layout read2_layout(int Kp) {
+  R2Layout s{};
+  const int KB = (Kp + 63) / 64;
+  s.w = 0;
+  s.a0 = align1k(w_head_bytes(Kp));   // two [x^2 | x] operands (x^2 block, then x block, 16 KB each)
+  s.ones = s.a0 + 2 * 32768;          // the constant step's A: 128 rows x [256 | 1 | 0 ...] fp16, 32-byte swizzle
+  s.sb = s.ones + 4096;               // state operand [80][Kp] bf16, K-major
+  s.stg0 = align1k(s.sb + KB * (kStCols * 128));  // two 16 KB output staging tiles
+  s.red = s.stg0 + 2 * 16384;         // maximum exchange: [group][slot][row][half] float
+  s.total = s.red + 2 * 2 * kTile * 2 * 4;
+  return s;
+}
+
+struct R2Bars {
+  uint64_t w_full;
+  uint64_t x_full[2], a_empty[2], a_full[2], l_full[2], g_full[2], o_full[2], r_empty[2], o_staged[2], st_done[2];
+  uint64_t done[2];
+  uint32_t tmem_base;
+  Abort ab;
+};
+
+template <int NC2>
+__global__ void __launch_bounds__(kThreadsTc, 1)
+    tc_read2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmO, TcArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // 1 KB aligned, still shared
+  const uint32_t sbase = smem_u32(smem);
+  __shared__ R2Bars B;
+  const R2Layout L = read2_layout(a.Kp);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = blockIdx.y, split = blockIdx.x;
+  const int tile0 = split * a.seg_tiles;
+  const int T = max(0, min(a.tiles, tile0 + a.seg_tiles) - tile0);
+  const int KS = a.Kp / 16;
+  constexpr int kGroupWarps = 8;
+  // output accumulator columns within a group's region: past the compacted Gamma~_Q of half 0
+  // (NC2 / 2 columns) and clear of half 1's (the last NC2 / 2 columns of 2 NC2)
+  constexpr uint32_t kColOut = NC2 == 128 ? 64u : 128u;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&B.w_full, 1);
+    for (int g = 0; g < 2; ++g) {
+      mbar_init(&B.x_full[g], 1);
+      mbar_init(&B.a_empty[g], 1);
+      mbar_init(&B.a_full[g], kGroupWarps);
+      mbar_init(&B.l_full[g], 1);
+      mbar_init(&B.g_full[g], kGroupWarps);
+      mbar_init(&B.o_full[g], 1);
+      mbar_init(&B.r_empty[g], kGroupWarps);
+      mbar_init(&B.o_staged[g], kGroupWarps);
+      mbar_init(&B.st_done[g], 1);
+      mbar_init(&B.done[g], 1);
+    }
+    B.ab.flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&B.tmem_base, 512);
+    tmem_relinquish();
+  }
+  dep_wait();  // the write (and before it the parameter fold) of this call are complete
+  if (warp >= kRowWarp0) {
+    const int i = threadIdx.x - 32 * kRowWarp0;  // 0 .. 511
+    // the constant step's A rows: [256 | 1 | 0 ...] (fp16), 32-byte swizzle
+    if (i < kTile) {
+      *reinterpret_cast<uint4*>(smem + L.ones + sw32_chunk(i, 0)) = make_uint4(pack_f16x2(256.0f, 1.0f), 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(smem + L.ones + sw32_chunk(i, 1)) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    // state [Kp][80] fp32 -> bf16 K-major operand SB[n][comp] (eps folded into column 64 once)
+    const float4* src = reinterpret_cast<const float4*>(a.state + (size_t)bh * a.Kp * kStCols);
+    const int nq = a.Kp * (kStCols / 4), nt = 32 * (kThreadsTc / 32 - kRowWarp0);
+    for (int i0 = i; i0 < nq; i0 += 10 * nt) {
+      float4 f[10];
+#pragma unroll
+      for (int u = 0; u < 10; ++u)
+        if (i0 + u * nt < nq) f[u] = __ldg(src + i0 + u * nt);
+#pragma unroll
+      for (int u = 0; u < 10; ++u) {
+        const int ii = i0 + u * nt;
+        if (ii < nq) {
+          const int comp = ii / (kStCols / 4), c = ii - comp * (kStCols / 4);
+          const float e[4] = {c == kDv / 4 ? f[u].x + a.eps : f[u].x, f[u].y, f[u].z, f[u].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) sts16(sbase + L.sb + sw128_off(4 * c + j, comp, kStCols * 128), bf16_bits(e[j]));
         }
       }
     }
-    // last epilogue
-    if (kRead && ok && T > 0) {
-      if (warp_wait(&B.o_full, (T - 1) & 1, &B.ab, a.ctrl, 60, a.wait_ns)) {
-        tc_fence_after();
-        uint32_t r[16];
-        tmem_ld16(tmem + rc.lane_base + kColAcc + 16 * rc.part, r);
-        uint32_t zc = tmem_ld1(tmem + rc.lane_base + kColAcc + 64);
-        tmem_ld_wait_tied1(zc);
-        tmem_ld_wait_tied16(r);
-        const int ptok = (tile0 + T - 1) * kTile + rc.row;
-        const float rden = rcp_approx(__uint_as_float(zc));
-        if (ptok < a.N)
-          store_out16(reinterpret_cast<__nv_bfloat16*>(a.out) + ((size_t)bh * a.N + ptok) * kDv + 16 * rc.part, r,
-                      rden);
+  }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = B.tmem_base;
+
+  if (warp < kRowWarp0) {
+    setmaxnreg_dec<kCtrlRegs>();
+    if (warp == 0 && lane == 0) {
+      // ---------------------------------------------------------------- producer: W image, X tiles
+      const uint32_t wbytes = w_head_bytes(a.Kp);
+      const int h = bh % a.H;
+      mbar_expect_tx(&B.w_full, wbytes);
+      for (uint32_t o = 0; o < wbytes; o += 32768)
+        bulk_load(smem + L.w + o, a.w_img + (size_t)h * wbytes + o, min(32768u, wbytes - o), &B.w_full);
+      int issued[2] = {-1, -1};
+      for (int t = 0; t < T; ++t) {
+        const int g = t & 1;
+        const uint32_t k = (uint32_t)(t >> 1);
+        // the x block of group g's operand once the logits of its previous tile have read it
+        if (t >= 2 && !wait_bounded(&B.a_empty[g], (k - 1) & 1, &B.ab, a.ctrl, 110, a.wait_ns)) break;
+        mbar_expect_tx(&B.x_full[g], 16384);
+        tma_load_3d(smem + L.a0 + 32768 * g + 16384, &tmQ, 0, (tile0 + t) * kTile, bh, &B.x_full[g]);
+        issued[g] = (int)(k & 1);
       }
+      Abort none{0};
+      for (int g = 0; g < 2; ++g)
+        if (issued[g] >= 0) wait_bounded(&B.x_full[g], (uint32_t)issued[g], &none, a.ctrl, 111, a.wait_ns);
+    } else if ((warp == 1 || warp == 2) && lane == 0) {
+      // ---------------------------------------------------------------- issuer of group g
+      const int g = warp - 1;
+      const uint32_t rg = tmem + 256u * (uint32_t)g;
+      const uint32_t w_addr = smem_u32(smem + L.w), a_addr = smem_u32(smem + L.a0) + 32768u * (uint32_t)g;
+      const uint64_t d_w = make_sdesc(w_addr, 16, 1024), d_c = make_sdesc32(w_addr + (uint32_t)a.Kp * 256, 16, 256);
+      const uint64_t d_a = make_sdesc(a_addr, 16, 1024), d_ones = make_sdesc32(smem_u32(smem + L.ones), 16, 256);
+      const uint64_t d_sb = make_sdesc(smem_u32(smem + L.sb), 16, 1024);
+      const uint32_t id_log = make_idesc(128, a.Kp, 0, 0, 0, 0);
+      constexpr uint32_t idr = make_idesc(128, kStCols, 1, 1, 0, 0);
+      bool ok = wait_bounded(&B.w_full, 0, &B.ab, a.ctrl, 112, a.wait_ns);
+      for (int t = g; ok && t < T; t += 2) {
+        const uint32_t k = (uint32_t)(t >> 1), ph = k & 1;
+        // logits: the group's operand is built and its region free (the previous output has been read)
+        if (!(ok = wait_bounded(&B.a_full[g], ph, &B.ab, a.ctrl, 113, a.wait_ns) &&
+                   (t < 2 || wait_bounded(&B.r_empty[g], ph ^ 1, &B.ab, a.ctrl, 114, a.wait_ns))))
+          break;
+        GMA_TRACE_AT(20, t);
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          mma_ss_off(rg, d_a, ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4, d_w, (ks >> 2) * (uint32_t)a.Kp * 8 + (ks & 3) * 2,
+                     id_log, ks > 0 ? 1u : 0u);
+        mma_ss(rg, d_ones, d_c, id_log, 1u);
+        mma_commit(&B.l_full[g]);
+        mma_commit(&B.a_empty[g]);
+        GMA_TRACE_AT(21, t);
+        // the previous tile's output (staged by the rows after its read) while this tile's logits run
+        if (t >= 2) {
+          if (!(ok = wait_bounded(&B.o_staged[g], ph ^ 1, &B.ab, a.ctrl, 116, a.wait_ns))) break;
+          GMA_TRACE_AT(24, t);
+          tma_store_3d(&tmO, smem_u32(smem + L.stg0) + 16384u * (uint32_t)g, 0, (tile0 + t - 2) * kTile, bh);
+          bulk_commit();
+          bulk_wait_read_all();
+          mbar_arrive(&B.st_done[g]);
+          GMA_TRACE_AT(25, t);
+        }
+        // read: Gamma~_Q (TMEM, compacted) [Vt | Z + eps] into the region's output columns
+        if (!(ok = wait_bounded(&B.g_full[g], ph, &B.ab, a.ctrl, 115, a.wait_ns))) break;
+        GMA_TRACE_AT(22, t);
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < 16; ++ks) {
+          if (ks < KS) {
+            const uint32_t acol = ks < NC2 / 16 ? 8u * ks : (uint32_t)(3 * NC2 / 2) + 8u * (ks - NC2 / 16);
+            mma_ts_off(rg + kColOut, rg + acol, d_sb, ((ks >> 2) * (kStCols * 128) + (ks & 3) * 32) >> 4, idr,
+                       ks > 0 ? 1u : 0u);
+          }
+        }
+        mma_commit(&B.o_full[g]);
+        GMA_TRACE_AT(23, t);
+      }
+      // the group's last output tile
+      const int tl = g + 2 * ((T - 1 - g) / 2);  // last tile of this group (if any)
+      if (ok && g < T) {
+        if (wait_bounded(&B.o_staged[g], (uint32_t)(tl >> 1) & 1u, &B.ab, a.ctrl, 118, a.wait_ns)) {
+          tma_store_3d(&tmO, smem_u32(smem + L.stg0) + 16384u * (uint32_t)g, 0, (tile0 + tl) * kTile, bh);
+          bulk_commit();
+        }
+      }
+      bulk_wait_all();
+      mma_commit(&B.done[g]);
+      Abort none{0};
+      wait_bounded(&B.done[g], 0, &none, a.ctrl, 117, a.wait_ns);
+    }
+  } else {
+    setmaxnreg_inc<kRowRegs>();
+    // ------------------------------------------------------------------ row warps
+    const int wi = warp - kRowWarp0;
+    const int g = wi / kGroupWarps, half = (wi % kGroupWarps) / 4, q = warp & 3;
+    const int row = 32 * q + lane;
+    const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+    const uint32_t rg = tmem + lane_base + 256u * (uint32_t)g;
+    const uint32_t rowsw = (uint32_t)(row >> 3) * 1024u + (uint32_t)(row & 7) * 128u + ((uint32_t)(row & 7) << 4);
+    const uint32_t bar = 1u + 4u * (uint32_t)g + (uint32_t)q;  // the two warps sharing this quarter's rows
+    const uint32_t red = sbase + L.red + (uint32_t)g * (2 * kTile * 2 * 4);
+    const uint32_t a_x = sbase + L.a0 + 32768u * (uint32_t)g + 16384u;  // x block of the group's operand
+    const uint32_t stg = sbase + L.stg0 + 16384u * (uint32_t)g;
+    const uint32_t lcol = (uint32_t)(NC2 * half);                         // this half's logit columns
+    // packed Gamma~ pairs of chunk c (32 components): half 0 compacts upwards from column 0, half 1
+    // downwards into the top of its own columns, so neither overwrites logits still to be read
+    const uint32_t gcol0 = half == 0 ? 0u : (uint32_t)(3 * NC2 / 2);
+    // [x^2 | x] fp16 operand of this row (dims 32 half .. + 31) of tile u, built in place from its bf16 tile
+    auto build_operand = [&](int u) {
+      if (!warp_wait(&B.x_full[g], (uint32_t)(u >> 1) & 1u, &B.ab, a.ctrl, 121, a.wait_ns)) return false;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t ad = (a_x + rowsw) ^ ((uint32_t)(4 * half + j) << 4);
+        const uint4 v = lds128(ad);
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+        uint32_t sq[4], lin[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float lo = __uint_as_float(w4[e] << 16), hi = __uint_as_float(w4[e] & 0xffff0000u);
+          lin[e] = pack_f16x2(lo, hi);
+          sq[e] = pack_f16x2(lo * lo, hi * hi);
+        }
+        sts128(ad, make_uint4(lin[0], lin[1], lin[2], lin[3]));
+        sts128(ad - 16384u, make_uint4(sq[0], sq[1], sq[2], sq[3]));
+      }
+      fence_async_smem();
+      warp_arrive(&B.a_full[g]);
+      return true;
+    };
+    bool ok = warp_wait(&B.w_full, 0, &B.ab, a.ctrl, 120, a.wait_ns);
+    if (ok && g < T) ok = build_operand(g);
+    for (int t = g; t < T; t += 2) {
+      const uint32_t k = (uint32_t)(t >> 1), ph = k & 1;
+      if (wi == 0) GMA_TRACE_AT(0, t);
+      // pass 1: this half's maximum, exchanged with the partner thread of the row
+      float mh = -INFINITY;
+      if (wi == 0) GMA_TRACE_AT(2, t);
+      if (ok) ok = warp_wait(&B.l_full[g], ph, &B.ab, a.ctrl, 122, a.wait_ns);
+      if (wi == 0) GMA_TRACE_AT(3, t);
+      if (ok) {
+        tc_fence_after();
+        // chunk c + 1's load is in flight while chunk c is reduced
+        float m0 = -INFINITY, m1 = -INFINITY;
+        uint32_t ra[32], rb[32];
+        tmem_ld32(rg + lcol, ra);
+#pragma unroll
+        for (int c = 0; c < NC2 / 32; ++c) {
+          uint32_t* cur = (c & 1) ? rb : ra;
+          uint32_t* nxt = (c & 1) ? ra : rb;
+          tmem_ld_wait_tied32(cur);
+          if (c + 1 < NC2 / 32) tmem_ld32(rg + lcol + 32 * (c + 1), nxt);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            m0 = max3(m0, __uint_as_float(cur[4 * e]), __uint_as_float(cur[4 * e + 1]));
+            m1 = max3(m1, __uint_as_float(cur[4 * e + 2]), __uint_as_float(cur[4 * e + 3]));
+          }
+        }
+        mh = fmaxf(m0, m1);
+      }
+      if (wi == 0) GMA_TRACE_AT(4, t);
+      const uint32_t slot = red + (ph * kTile + (uint32_t)row) * 8u;
+      sts32(slot + 4u * (uint32_t)half, mh);
+      named_bar_sync(bar, 64);
+      const float m = fmaxf(mh, lds32(slot + 4u * (uint32_t)(half ^ 1)));
+      if (wi == 0) GMA_TRACE_AT(5, t);
+      // pass 2: unnormalised gamma~ = 2^(v - m) packed to bf16 in place (half 1 walks its chunks
+      // downwards); the read divides by gamma~ . (Z + eps) = gamma~ . Z + eps s
+      if (ok) {
+        // chunk order: half 0 upwards, half 1 downwards; the next chunk's load is in flight while this one is
+        // exponentiated (its source never overlaps this chunk's packed destination)
+        uint32_t ra[32], rb[32];
+        tmem_ld32(rg + lcol + 32 * (half == 0 ? 0 : NC2 / 32 - 1), ra);
+#pragma unroll
+        for (int cc = 0; cc < NC2 / 32; ++cc) {
+          const int c = half == 0 ? cc : NC2 / 32 - 1 - cc;
+          uint32_t* cur = (cc & 1) ? rb : ra;
+          uint32_t* nxt = (cc & 1) ? ra : rb;
+          tmem_ld_wait_tied32(cur);
+          if (cc + 1 < NC2 / 32) tmem_ld32(rg + lcol + 32 * (half == 0 ? c + 1 : c - 1), nxt);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            float t0 = __uint_as_float(cur[2 * e]), t1 = __uint_as_float(cur[2 * e + 1]);
+            add_f32x2(t0, t1, -m, -m);
+            cur[e] = pack_bf16x2(ex2_approx(t0), ex2_approx(t1));
+          }
+          tmem_st16(rg + gcol0 + 16 * c, cur);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        warp_arrive(&B.g_full[g]);
+      }
+      // the next tile's operand while this tile's read contraction runs (its X tile landed long ago: the
+      // producer loads it once this tile's logits have read the operand buffer)
+      if (ok && t + 2 < T) ok = build_operand(t + 2);
+      if (wi == 0) GMA_TRACE_AT(6, t);
+      // epilogue: dims 32 half .. + 31 divided by column 64, staged as bf16 for the tensor store
+      if (ok) ok = warp_wait(&B.o_full[g], ph, &B.ab, a.ctrl, 123, a.wait_ns);
+      if (wi == 0) GMA_TRACE_AT(7, t);
+      if (ok) {
+        tc_fence_after();
+        uint32_t r[32];
+        tmem_ld32(rg + kColOut + 32 * half, r);
+        uint32_t zc = tmem_ld1(rg + kColOut + 64);
+        tmem_ld_wait_tied32(r);
+        tmem_ld_wait_tied1(zc);
+        tc_fence_before();
+        warp_arrive(&B.r_empty[g]);
+        const float rden = rcp_approx(__uint_as_float(zc));
+        if (t >= 2) ok = warp_wait(&B.st_done[g], ph ^ 1, &B.ab, a.ctrl, 124, a.wait_ns);
+        if (ok) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) sts128((stg + rowsw) ^ ((uint32_t)(4 * half + j) << 4), pack_out8(r + 8 * j, rden));
+          fence_async_smem();
+          warp_arrive(&B.o_staged[g]);
+        }
+      }
+      if (wi == 0) GMA_TRACE_AT(8, t);
     }
   }
   tc_fence_before();
@@ -1024,13 +1338,6 @@ __device__ __forceinline__ void snapshot_state_chunk(uint32_t sb, int Kp, int co
   }
 }
 
-// 8 output dims normalised (acc / den) and packed to bf16 (one 16-byte chunk).
-__device__ __forceinline__ uint4 pack_out8(const uint32_t* acc, float rden) {
-  return make_uint4(pack_bf16x2(__uint_as_float(acc[0]) * rden, __uint_as_float(acc[1]) * rden),
-                    pack_bf16x2(__uint_as_float(acc[2]) * rden, __uint_as_float(acc[3]) * rden),
-                    pack_bf16x2(__uint_as_float(acc[4]) * rden, __uint_as_float(acc[5]) * rden),
-                    pack_bf16x2(__uint_as_float(acc[6]) * rden, __uint_as_float(acc[7]) * rden));
-}
 
 // Scales this thread's 16 value dims (atom `part` of the 32-byte-swizzled [V | 1] operand at vb: four 4 KB
 // atoms of 16 dims, then the constant atom) of the key row rc.row by inv.
@@ -1109,11 +1416,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     setmaxnreg_dec<kCtrlRegsC>();
     if (warp == 0 && lane == 0) {
       // ---------------------------------------------------------------- producer
+      // the W image without its constant step (c' is added from the float32 table, which needs no
+      // shared memory for the constant step's B operand)
       const uint32_t wbytes = (uint32_t)a.Kp * 256, cbytes = kCTable * 4;
       const int h = bh % a.H;
       mbar_expect_tx(&B.w_full, wbytes + cbytes);
       for (uint32_t o = 0; o < wbytes; o += 32768)
-        bulk_load(smem + L.w + o, a.w_img + (size_t)h * wbytes + o, min(32768u, wbytes - o), &B.w_full);
+        bulk_load(smem + L.w + o, a.w_img + (size_t)h * w_head_bytes(a.Kp) + o, min(32768u, wbytes - o), &B.w_full);
       bulk_load(smem + L.c, a.cbias + (size_t)h * kCTable, cbytes, &B.w_full);
       int issued[3] = {-1, -1, -1};  // parity of the last load armed on xk_full, xq_full, v_full
       for (int t = 0; t < T; ++t) {
@@ -1553,10 +1862,10 @@ gma_status_t tc_launch(const gma_problem_t& p, gma_op_t op, int Nk, const TcPlan
   if (op == GMA_OP_RESPONSIBILITIES) {
     if (!make_map(&mq, Q, BH, p.N)) return GMA_ERR_CUDA;
     const uint32_t smem = smem_bytes(read_layout(pl.Kp).total);
-    if (set_smem_optin((const void*)tc_read_kernel<false, NC>, (int)smem, 0) != GMA_OK) return GMA_ERR_CUDA;
+    if (set_smem_optin((const void*)tc_resp_kernel<NC>, (int)smem, 0) != GMA_OK) return GMA_ERR_CUDA;
     a.fault = 0;
-    GMA_LAUNCH_DEPENDENT("tc_resp", (tc_read_kernel<false, NC>), dim3(pl.splits, BH), kThreadsTc, smem, st, mq, a);
-    return check_launch("launch tc_resp", (const void*)tc_read_kernel<false, NC>);
+    GMA_LAUNCH_DEPENDENT("tc_resp", tc_resp_kernel<NC>, dim3(pl.splits, BH), kThreadsTc, smem, st, mq, a);
+    return check_launch("launch tc_resp", (const void*)tc_resp_kernel<NC>);
   }
   if (op == GMA_OP_CAUSAL) {
     // the sweep's V tiles are four 16-dim boxes in the 32-byte swizzle
@@ -1601,12 +1910,12 @@ gma_status_t tc_launch(const gma_problem_t& p, gma_op_t op, int Nk, const TcPlan
   }
   if (op == GMA_OP_CAUSAL_STATE) return GMA_OK;  // the state alone
   a.fault = 0;
-  if (!make_map(&mq, Q, BH, p.N)) return GMA_ERR_CUDA;
-  const uint32_t smem_r = smem_bytes(read_layout(pl.Kp).total);
-  if (set_smem_optin((const void*)tc_read_kernel<true, NC>, (int)smem_r, 0) != GMA_OK) return GMA_ERR_CUDA;
-  GMA_LAUNCH_DEPENDENT("tc_bidir_read", (tc_read_kernel<true, NC>), dim3(pl.splits, BH), kThreadsTc, smem_r, st, mq,
-                       a);
-  return check_launch("launch tc_bidir_read", (const void*)tc_read_kernel<true, NC>);
+  CUtensorMap mo;
+  if (!make_map(&mq, Q, BH, p.N) || !make_map(&mo, a.out, BH, p.N)) return GMA_ERR_CUDA;
+  const uint32_t smem_r = smem_bytes(read2_layout(pl.Kp).total);
+  if (set_smem_optin((const void*)tc_read2_kernel<2 * NC>, (int)smem_r, 0) != GMA_OK) return GMA_ERR_CUDA;
+  GMA_LAUNCH_DEPENDENT("tc_bidir_read", tc_read2_kernel<2 * NC>, dim3(pl.splits, BH), kThreadsTc, smem_r, st, mq, mo, a);
+  return check_launch("launch tc_bidir_read", (const void*)tc_read2_kernel<2 * NC>);
 }
 
 uint32_t g_fault_next = 0;  // test hook, consumed by the next launch of the write kernel
@@ -1617,14 +1926,15 @@ std::mutex g_fault_mu;
 TcPlan tc_plan(const gma_problem_t& p, gma_op_t op) {
   TcPlan t{};
   const int BH = p.B * p.H;
-  t.Kp = (p.K + 15) / 16 * 16;
+  t.Kp = p.K <= 64 ? 64 : (p.K <= 128 ? 128 : 256);  // = 4 NC: every row thread's logit columns are written
   t.tiles = cdiv(p.N, kTile);
   t.splits = split_for(BH, t.tiles > 0 ? t.tiles : 1);
   t.seg_tiles = cdiv(t.tiles > 0 ? t.tiles : 1, t.splits);
   t.splits = cdiv(t.tiles > 0 ? t.tiles : 1, t.seg_tiles);
   t.off_w = align_up(sizeof(Ctrl));
-  t.off_c = align_up(t.off_w + (size_t)p.H * t.Kp * 256);
-  t.off_state = align_up(t.off_c + (size_t)p.H * kCTable * 4);
+  t.off_c = align_up(t.off_w + (size_t)p.H * w_head_bytes(t.Kp));
+  t.off_flags = align_up(t.off_c + (size_t)p.H * kCTable * 4);
+  t.off_state = align_up(t.off_flags + (size_t)p.H * (kCTable / 8) * 4);
   size_t st = 0;
   if (op == GMA_OP_BIDIR || op == GMA_OP_CROSS || op == GMA_OP_CAUSAL_STATE) st = (size_t)BH * t.Kp * kStCols * 4;
   if (op == GMA_OP_CAUSAL) st = (size_t)BH * t.splits * t.Kp * kStCols * 4;  // segment aggregates
@@ -1641,6 +1951,7 @@ gma_status_t tc_run(const gma_problem_t& p, gma_op_t op, int Nk, const void* Q, 
   TcArgs a{};
   a.w_img = (const uint8_t*)(base + pl.off_w);
   a.cbias = (const float*)(base + pl.off_c);
+  a.range_flags = (const uint32_t*)(base + pl.off_flags);
   a.state = (float*)(base + pl.off_state);
   a.ctrl = (Ctrl*)base;
   a.out = out;
@@ -1661,7 +1972,7 @@ gma_status_t tc_run(const gma_problem_t& p, gma_op_t op, int Nk, const void* Q, 
   const bool with_state = op == GMA_OP_BIDIR || op == GMA_OP_CAUSAL_STATE;  // write accumulator starts at zero
   const size_t zero_n = with_state ? (size_t)BH * pl.Kp * kStCols : 0;
   GMA_LAUNCH("tc_prep", tc_prep_kernel, dim3(kCTable / 8, p.H), 128, 0, st, mu, sigma2, log_pi, p.H, p.K, pl.Kp,
-             (uint8_t*)a.w_img, (float*)a.cbias, a.ctrl, a.state, zero_n);
+             (uint8_t*)a.w_img, (float*)a.cbias, a.ctrl, a.state, zero_n, (uint32_t*)a.range_flags);
   if (gma_status_t e = check_launch("launch tc_prep", (const void*)tc_prep_kernel)) return e;
   const int nc = pl.Kp <= 64 ? 16 : (pl.Kp <= 128 ? 32 : 64);  // components per row thread (4 per row)
   gma_status_t e = nc == 16   ? tc_launch<16>(p, op, Nk, pl, a, Q, K, V, ws, st)

@@ -14,7 +14,7 @@ import torch
 
 _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libgma.so")
 
-GMA_OK, GMA_ERR_INVALID_ARG, GMA_ERR_UNSUPPORTED, GMA_ERR_WORKSPACE, GMA_ERR_CUDA, GMA_ERR_TIMEOUT = range(6)
+GMA_OK, GMA_ERR_INVALID_ARG, GMA_ERR_UNSUPPORTED, GMA_ERR_WORKSPACE, GMA_ERR_CUDA, GMA_ERR_TIMEOUT, GMA_ERR_RANGE = range(7)
 GMA_F32, GMA_BF16 = 0, 1
 (OP_RESPONSIBILITIES, OP_BIDIR, OP_CAUSAL, OP_CROSS, OP_CAUSAL_STATE, OP_CAUSAL_DECODE, OP_BACKWARD_BIDIR,
  OP_BACKWARD_CAUSAL, OP_PROJECTED_BIDIR, OP_PROJECTED_CAUSAL) = range(10)

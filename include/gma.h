@@ -38,7 +38,20 @@
  *     GMA_BF16 runs the log-density contraction with fp16 operands and the
  *     write/read contractions with bf16 operands on the tcgen05 tensor cores,
  *     all accumulated in float32; the output is rounded to bf16 (RNE).
- *     For GMA_BF16, |q|, |k| must stay below 255 (fp16 range of q^2).
+ *     For GMA_BF16, |q|, |k| must stay below 255 (fp16 range of q^2), and the folded
+ *     parameters must fit fp16: sigma2 > 1.1e-5 (-1/2 sigma2^-1 log2(e) > -65504),
+ *     |mu| / sigma2 < 45000 and |c'_k| < 1.6e7 for the component constant
+ *     c'_k = (log pi_k - 1/2 sum_d (mu^2 / sigma2 + log sigma2)) log2(e).  A call whose
+ *     parameters break these bounds (or hold NaN / inf) still runs, and sets the
+ *     workspace error word: gma_check_device_error() then returns GMA_ERR_RANGE.
+ *     Accuracy of GMA_BF16 (the bounds above only keep the operands finite): the
+ *     expanded form a x^2 + b x + c' keeps about 2^-12 of each term's size, so the
+ *     absolute log-density error grows with sigma2^-1 (x^2 + |mu x| + mu^2) summed
+ *     over the dimensions.  With unit-scale q, k, mu and sigma2 = softplus(N(0, s))
+ *     + 1e-2 (s <= 1), or a minority of components at the 1e-2 floor, outputs stay
+ *     within 2e-2 of exact (max |error| / max |O|); when most components or
+ *     dimensions sit at the floor, or |q|, |k| grow past ~3 with variances near it,
+ *     the error reaches 0.03 - 0.16.  Use GMA_F32 (centred form, float32) there.
  */
 #ifndef GMA_H_
 #define GMA_H_
@@ -62,7 +75,8 @@ typedef enum {
   GMA_ERR_UNSUPPORTED = 2, /* d, dv, K or dtype outside what this build runs */
   GMA_ERR_WORKSPACE = 3,   /* ws_bytes smaller than gma_workspace_bytes() */
   GMA_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
-  GMA_ERR_TIMEOUT = 5      /* a bounded device wait gave up (see ws error word) */
+  GMA_ERR_TIMEOUT = 5,     /* a bounded device wait gave up (see ws error word) */
+  GMA_ERR_RANGE = 6        /* bf16 I/O: a folded parameter does not fit the fp16 operands (see ws error word) */
 } gma_status_t;
 
 typedef enum { GMA_F32 = 0, GMA_BF16 = 1 } gma_dtype_t;
@@ -281,7 +295,9 @@ GMA_API gma_status_t gma_forward_projected(const gma_problem_t *p, int causal, i
  * Synchronises `stream`, then reads the error word kept at the start of `ws`:
  * GMA_OK if no device wait timed out since the word was last cleared (every
  * forward/responsibilities call clears it when it starts), GMA_ERR_TIMEOUT if
- * one did, GMA_ERR_CUDA if the synchronisation itself failed.  `ws` must be a
+ * one did, GMA_ERR_RANGE if (bf16 I/O) a folded parameter did not fit the fp16
+ * operands (see the precision note above), GMA_ERR_CUDA if the synchronisation
+ * itself failed.  `ws` must be a
  * workspace previously passed to one of the calls above.
  */
 GMA_API gma_status_t gma_check_device_error(void *ws, void *stream);

@@ -40,7 +40,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_status_strings_and_version(L):
-    for s in range(6):
+    for s in range(7):
         assert len(gma.status_string(s)) > 0
     assert L.gma_version() >= 1
 
