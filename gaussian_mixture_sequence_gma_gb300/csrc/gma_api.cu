@@ -50,6 +50,22 @@ gma_status_t set_smem_optin(const void* func, int bytes, int /*slot*/) {
   return GMA_OK;
 }
 
+gma_status_t set_carveout_max(const void* func) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GMA_ERR_CUDA;
+  struct Entry { const void* f; int dev; };
+  static std::mutex mu;
+  static std::vector<Entry> done;
+  std::lock_guard<std::mutex> lock(mu);
+  for (auto& e : done)
+    if (e.f == func && e.dev == dev) return GMA_OK;
+  if (cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared) !=
+      cudaSuccess)
+    return cuda_fail("cudaFuncSetAttribute(shared memory carveout)");
+  done.push_back({func, dev});
+  return GMA_OK;
+}
+
 namespace {
 
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }

@@ -129,5 +129,8 @@ void set_error_detail(const char* msg);
 
 // Sets the dynamic shared-memory opt-in of a kernel once per device.
 gma_status_t set_smem_optin(const void* func, int bytes, int slot);
+// Asks for the largest shared-memory carveout for a small kernel that runs between the large-shared-memory
+// kernels, so that the SMs need not change their L1 / shared split around it (once per device).
+gma_status_t set_carveout_max(const void* func);
 
 }  // namespace gma

@@ -52,6 +52,7 @@ constexpr uint32_t kCtrlRegs = 56, kRowRegs = 104;
 constexpr uint32_t kCtrlRegsC = 32, kRowRegsC = 112;
 constexpr int kRowWarps = 16;  // arrival count of the barriers the row warps signal
 constexpr int kStCols = 80;  // state row: [Vt (64) | Z | 15 zero]
+constexpr int kStRow = 68;   // row of the accumulated state in global memory: [Vt (64) | Z | 3 zero]
 constexpr int kCTable = 256;  // c' entries per head (-inf past K)
 constexpr int kTargetCtas = 152;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -117,7 +118,7 @@ struct TcArgs {
   const uint8_t* w_img;  // [H][w_head_bytes(Kp)] swizzled fp16 B operand of the log-density contraction
   const float* cbias;    // [H][256] c'_k (log2 domain); -inf past K
   const uint32_t* range_flags;  // [H][32] non-zero where a block of the parameter fold saw an fp16 overflow
-  float* state;          // [BH][Kp][80] (bidir) or [BH][splits][80][Kp] (causal aggregates, column-major)
+  float* state;          // [BH][Kp][68] (bidir: [Vt | Z | 0 0 0]) or [BH][splits][80][Kp] (causal aggregates, column-major)
   Ctrl* ctrl;
   void* out;             // read: O bf16 [BH][N][64]; responsibilities: gamma fp32 [BH][N][K]
   int H, N, K, Kp, tiles, seg_tiles, splits;
@@ -132,11 +133,16 @@ struct TcArgs {
 // grid (256 / 8, H), 128 threads: 16 threads per component, thread q of a component builds the 16-byte
 // chunk of W elements 8q .. 8q+7 of that component's row (x^2 coefficients for q < 8, x coefficients
 // after) with one store, and the q < 8 threads sum c'_k over their 8 dims.
-__global__ void __launch_bounds__(128) tc_prep_kernel(const float* __restrict__ mu, const float* __restrict__ sigma2,
+__global__ void __launch_bounds__(128, 16) tc_prep_kernel(const float* __restrict__ mu, const float* __restrict__ sigma2,
                                                       const float* __restrict__ log_pi, int H, int K, int Kp,
                                                       uint8_t* w_img, float* cbias, Ctrl* ctrl, float* zero,
                                                       size_t zero_n, uint32_t* range_flags) {
+  // Launched as a dependent of whatever precedes it on the stream: nothing is read or written before that
+  // grid has completed (it may produce the parameters, or still read the previous call's W image).  The
+  // 32-register bound lets a CTA of this grid sit beside a running tensor-core CTA meanwhile.
   dep_launch_next();  // the main kernel sets itself up meanwhile and waits for this grid before reading
+  dep_wait();
+  if (threadIdx.x == 0) GMA_SPAN_AT(8);
   const int h = blockIdx.y, k = blockIdx.x * 8 + (threadIdx.x >> 4), q = threadIdx.x & 15;
   const int d0 = 8 * (q & 7);
   uint32_t w[4] = {0u, 0u, 0u, 0u};
@@ -210,6 +216,7 @@ __global__ void __launch_bounds__(128) tc_prep_kernel(const float* __restrict__ 
   const size_t tid = ((size_t)blockIdx.y * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x;
   const size_t nth = (size_t)gridDim.x * gridDim.y * blockDim.x;
   for (size_t i = tid; i < zero_n; i += nth) zero[i] = 0.f;
+  if (threadIdx.x == 0) GMA_SPAN_AT(9);
 }
 
 // ----------------------------------------------------------------------------------------------- shared pieces
@@ -623,6 +630,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   const int tile0 = split * a.seg_tiles;
   const int T = max(0, min(a.tiles, tile0 + a.seg_tiles) - tile0);
   const int MB = (a.Kp + 127) / 128;
+  if (threadIdx.x == 0) GMA_SPAN_AT(0);
 
   // zero Gamma~ (components beyond Kp stay zero: the M=128 blocks read them) and the [1] atom
   for (uint32_t i = threadIdx.x; i < (uint32_t)MB * 32768 / 16; i += blockDim.x)
@@ -643,6 +651,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   __syncthreads();
   tc_fence_after();
   dep_wait();  // the parameter fold (and zeroed accumulator) of this call are complete
+  // the next kernel (read, scan or state export) may be scheduled as SMs free up; it waits for this grid's
+  // completion before it reads anything this grid writes
+  dep_launch_next();
+  if (threadIdx.x == 0) GMA_SPAN_AT(1);
   const uint32_t tmem = B.tmem_base;
   if (warp < kRowWarp0) {
     setmaxnreg_dec<kCtrlRegs>();
@@ -790,7 +802,38 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       if (warp == kRowWarp0) GMA_TRACE_AT(40, t);
     }
     // epilogue: state rows of this CTA -> global
-    if (ok && T > 0 && rc.part < MB) {
+    if (kAtomic) {
+      // bidirectional: the CTA's rows [Vt | Z] (68 floats per component) are staged in shared memory (over the
+      // Gamma~ and X areas, idle once the last contraction is done) and added to state[bh] by bulk reductions
+      if (T > 0 && rc.part < MB) {
+        const uint32_t stage = sbase + L.g;
+        if (ok && warp_wait(&B.done, 0, &B.ab, a.ctrl, 39, a.wait_ns)) {
+          tc_fence_after();
+          const int comp = 128 * rc.part + rc.row;
+          uint32_t r[80];
+#pragma unroll
+          for (int c = 0; c < 5; ++c) tmem_ld16(tmem + rc.lane_base + kColAcc + kStCols * rc.part + 16 * c, r + 16 * c);
+          tmem_ld_wait();
+          if (comp < a.Kp) {
+#pragma unroll
+            for (int c = 0; c < kStRow / 4; ++c)
+              sts128(stage + (uint32_t)(comp * kStRow + 4 * c) * 4u,
+                     c == kDv / 4 ? make_uint4(r[kDv], 0u, 0u, 0u)
+                                  : make_uint4(r[4 * c], r[4 * c + 1], r[4 * c + 2], r[4 * c + 3]));
+          }
+        }
+        fence_async_smem();
+        named_bar_sync(15, (uint32_t)MB * 128u);
+        if (threadIdx.x == 32 * kRowWarp0 && ok) {
+          const uint32_t bytes = (uint32_t)a.Kp * kStRow * 4u, chunk = bytes / 4u;  // 16-byte multiples
+          float* dst = a.state + (size_t)bh * a.Kp * kStRow;
+          for (uint32_t o = 0; o < bytes; o += chunk)
+            bulk_reduce_add_f32(reinterpret_cast<uint8_t*>(dst) + o, stage + o, chunk);
+          bulk_commit();
+          bulk_wait_read_all();
+        }
+      }
+    } else if (ok && T > 0 && rc.part < MB) {
       if (warp_wait(&B.done, 0, &B.ab, a.ctrl, 39, a.wait_ns)) {
         tc_fence_after();
         const int comp = 128 * rc.part + rc.row;
@@ -798,24 +841,18 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 #pragma unroll
         for (int c = 0; c < 5; ++c) tmem_ld16(tmem + rc.lane_base + kColAcc + kStCols * rc.part + 16 * c, r + 16 * c);
         tmem_ld_wait();
-        if (comp < a.Kp) {
-          if (kAtomic) {  // state[bh][comp][80]
-            float4* dst = reinterpret_cast<float4*>(a.state + ((size_t)bh * a.Kp + comp) * kStCols);
+        if (comp < a.Kp) {  // segment aggregate, column-major agg[bh][split][80][Kp]: each store covers 32 components
+          float* dst = a.state + ((size_t)bh * a.splits + split) * kStCols * a.Kp + comp;
 #pragma unroll
-            for (int c = 0; c < 20; ++c)
-              atomicAdd(dst + c, make_float4(__uint_as_float(r[4 * c]), __uint_as_float(r[4 * c + 1]),
-                                             __uint_as_float(r[4 * c + 2]), __uint_as_float(r[4 * c + 3])));
-          } else {  // segment aggregate, column-major agg[bh][split][80][Kp]: each store covers 32 components
-            float* dst = a.state + ((size_t)bh * a.splits + split) * kStCols * a.Kp + comp;
-#pragma unroll
-            for (int c = 0; c < kStCols; ++c) dst[(size_t)c * a.Kp] = __uint_as_float(r[c]);
-          }
+          for (int c = 0; c < kStCols; ++c) dst[(size_t)c * a.Kp] = __uint_as_float(r[c]);
         }
       }
     }
+    if (threadIdx.x == 32 * kRowWarp0) GMA_SPAN_AT(2);
   }
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) GMA_SPAN_AT(3);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -982,6 +1019,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   // output accumulator columns within a group's region: past the compacted Gamma~_Q of half 0
   // (NC2 / 2 columns) and clear of half 1's (the last NC2 / 2 columns of 2 NC2)
   constexpr uint32_t kColOut = NC2 == 128 ? 64u : 128u;
+  if (threadIdx.x == 0) GMA_SPAN_AT(4);
 
   if (threadIdx.x == 0) {
     mbar_init(&B.w_full, 1);
@@ -1005,6 +1043,17 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     tmem_relinquish();
   }
   dep_wait();  // the write (and before it the parameter fold) of this call are complete
+  if (threadIdx.x == 0) {
+    // the W image and the first X tile of each group land while the state operand is built
+    const uint32_t wbytes = w_head_bytes(a.Kp);
+    mbar_expect_tx(&B.w_full, wbytes);
+    for (uint32_t o = 0; o < wbytes; o += 32768)
+      bulk_load(smem + L.w + o, a.w_img + (size_t)(bh % a.H) * wbytes + o, min(32768u, wbytes - o), &B.w_full);
+    for (int t = 0; t < 2 && t < T; ++t) {
+      mbar_expect_tx(&B.x_full[t], 16384);
+      tma_load_3d(smem + L.a0 + 32768 * t + 16384, &tmQ, 0, (tile0 + t) * kTile, bh, &B.x_full[t]);
+    }
+  }
   if (warp >= kRowWarp0) {
     const int i = threadIdx.x - 32 * kRowWarp0;  // 0 .. 511
     // the constant step's A rows: [256 | 1 | 0 ...] (fp16), 32-byte swizzle
@@ -1012,22 +1061,29 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       *reinterpret_cast<uint4*>(smem + L.ones + sw32_chunk(i, 0)) = make_uint4(pack_f16x2(256.0f, 1.0f), 0u, 0u, 0u);
       *reinterpret_cast<uint4*>(smem + L.ones + sw32_chunk(i, 1)) = make_uint4(0u, 0u, 0u, 0u);
     }
-    // state [Kp][80] fp32 -> bf16 K-major operand SB[n][comp] (eps folded into column 64 once)
-    const float4* src = reinterpret_cast<const float4*>(a.state + (size_t)bh * a.Kp * kStCols);
-    const int nq = a.Kp * (kStCols / 4), nt = 32 * (kThreadsTc / 32 - kRowWarp0);
-    for (int i0 = i; i0 < nq; i0 += 10 * nt) {
-      float4 f[10];
+    // state [Kp][80] fp32 -> bf16 K-major operand SB[n][comp] (eps folded into column 64 once): one item is
+    // 8 consecutive components of column n, packed into one 16-byte chunk; consecutive threads take
+    // consecutive n, so each of the 8 loads of an item is coalesced across the warp
+    const float* src = a.state + (size_t)bh * a.Kp * kStRow;
+    const int items = kStCols * (a.Kp / 8), nt = 32 * (kThreadsTc / 32 - kRowWarp0);
+    for (int i0 = i; i0 < items; i0 += 2 * nt) {
+      float f[2][8];
 #pragma unroll
-      for (int u = 0; u < 10; ++u)
-        if (i0 + u * nt < nq) f[u] = __ldg(src + i0 + u * nt);
+      for (int u = 0; u < 2; ++u) {
+        const int it = i0 + u * nt, n = it % kStCols, c8 = it / kStCols;
+        if (it < items) {
 #pragma unroll
-      for (int u = 0; u < 10; ++u) {
-        const int ii = i0 + u * nt;
-        if (ii < nq) {
-          const int comp = ii / (kStCols / 4), c = ii - comp * (kStCols / 4);
-          const float e[4] = {c == kDv / 4 ? f[u].x + a.eps : f[u].x, f[u].y, f[u].z, f[u].w};
+          for (int j = 0; j < 8; ++j) f[u][j] = n <= kDv ? __ldg(src + (size_t)(8 * c8 + j) * kStRow + n) : 0.f;
+        }
+      }
 #pragma unroll
-          for (int j = 0; j < 4; ++j) sts16(sbase + L.sb + sw128_off(4 * c + j, comp, kStCols * 128), bf16_bits(e[j]));
+      for (int u = 0; u < 2; ++u) {
+        const int it = i0 + u * nt, n = it % kStCols, c8 = it / kStCols;
+        if (it < items) {
+          const float e = n == kDv ? a.eps : 0.f;
+          const uint4 v = make_uint4(pack_bf16x2(f[u][0] + e, f[u][1] + e), pack_bf16x2(f[u][2] + e, f[u][3] + e),
+                                     pack_bf16x2(f[u][4] + e, f[u][5] + e), pack_bf16x2(f[u][6] + e, f[u][7] + e));
+          sts128(sbase + L.sb + sw128_off(n, 8 * c8, kStCols * 128), v);
         }
       }
     }
@@ -1036,23 +1092,20 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (threadIdx.x == 0) GMA_SPAN_AT(5);
   const uint32_t tmem = B.tmem_base;
 
   if (warp < kRowWarp0) {
     setmaxnreg_dec<kCtrlRegs>();
     if (warp == 0 && lane == 0) {
-      // ---------------------------------------------------------------- producer: W image, X tiles
-      const uint32_t wbytes = w_head_bytes(a.Kp);
-      const int h = bh % a.H;
-      mbar_expect_tx(&B.w_full, wbytes);
-      for (uint32_t o = 0; o < wbytes; o += 32768)
-        bulk_load(smem + L.w + o, a.w_img + (size_t)h * wbytes + o, min(32768u, wbytes - o), &B.w_full);
-      int issued[2] = {-1, -1};
-      for (int t = 0; t < T; ++t) {
+      // ---------------------------------------------------------------- producer: X tiles 2 .. T-1 (the W
+      // image and tiles 0 and 1 were issued in the prologue)
+      int issued[2] = {T > 0 ? 0 : -1, T > 1 ? 0 : -1};
+      for (int t = 2; t < T; ++t) {
         const int g = t & 1;
         const uint32_t k = (uint32_t)(t >> 1);
         // the x block of group g's operand once the logits of its previous tile have read it
-        if (t >= 2 && !wait_bounded(&B.a_empty[g], (k - 1) & 1, &B.ab, a.ctrl, 110, a.wait_ns)) break;
+        if (!wait_bounded(&B.a_empty[g], (k - 1) & 1, &B.ab, a.ctrl, 110, a.wait_ns)) break;
         mbar_expect_tx(&B.x_full[g], 16384);
         tma_load_3d(smem + L.a0 + 32768 * g + 16384, &tmQ, 0, (tile0 + t) * kTile, bh, &B.x_full[g]);
         issued[g] = (int)(k & 1);
@@ -1253,9 +1306,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       }
       if (wi == 0) GMA_TRACE_AT(8, t);
     }
+    if (wi == 0 && lane == 0) GMA_SPAN_AT(6);
   }
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) GMA_SPAN_AT(7);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -1771,33 +1826,35 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 
 // Exclusive scan over segments: agg[bh][p][e] <- sum_{p' < p} agg[bh][p'][e].  grid (ceil(n / 256), B*H).
 // Each thread has all loads of up to 32 segments in flight before the first store.
-__global__ void tc_scan_kernel(float* agg, int P, int n) {
+// 128 threads of at most 32 registers, so that its CTAs fit beside a running aggregate CTA and start the
+// moment that grid completes.
+__global__ void __launch_bounds__(128, 16) tc_scan_kernel(float* agg, int P, int n) {
   dep_wait();         // the aggregates are complete
   dep_launch_next();  // the sweep sets itself up meanwhile and waits for this grid before reading
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= n) return;
   float* base = agg + (size_t)blockIdx.y * P * n + e;
   float run = 0.f;
-  for (int p0 = 0; p0 < P; p0 += 32) {
-    float x[32];
+  for (int p0 = 0; p0 < P; p0 += 8) {
+    float x[8];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) x[j] = (p0 + j < P) ? __ldcg(base + (size_t)(p0 + j) * n) : 0.f;
+    for (int j = 0; j < 8; ++j) x[j] = (p0 + j < P) ? __ldcg(base + (size_t)(p0 + j) * n) : 0.f;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
+    for (int j = 0; j < 8; ++j) {
       if (p0 + j < P) __stcg(base + (size_t)(p0 + j) * n, run);
       run += x[j];
     }
   }
 }
 
-// Public causal state [B*H][K][dv + 1] from the write accumulator [B*H][Kp][80] (columns 0..64).
+// Public causal state [B*H][K][dv + 1] from the write accumulator [B*H][Kp][68] (columns 0..64).
 __global__ void tc_state_export_kernel(const float* __restrict__ acc, int K, int Kp, size_t n, float* __restrict__ out) {
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
     const int c = (int)(i % (kDv + 1));
     const size_t rk = i / (kDv + 1);  // bh * K + k
     const int k = (int)(rk % K);
     const size_t bh = rk / K;
-    out[i] = acc[(bh * Kp + k) * kStCols + c];
+    out[i] = acc[(bh * Kp + k) * kStRow + c];
   }
 }
 
@@ -1882,7 +1939,8 @@ gma_status_t tc_launch(const gma_problem_t& p, gma_op_t op, int Nk, const TcPlan
     if (gma_status_t e = check_launch("launch tc_causal_aggregate", (const void*)tc_write_kernel<false, NC>)) return e;
     a.fault = 0;
     const int n = pl.Kp * kStCols;
-    GMA_LAUNCH_DEPENDENT("tc_causal_scan", tc_scan_kernel, dim3(cdiv(n, 256), BH), 256, 0, st, a.state, pl.splits, n);
+    if (set_carveout_max((const void*)tc_scan_kernel) != GMA_OK) return GMA_ERR_CUDA;
+    GMA_LAUNCH_DEPENDENT("tc_causal_scan", tc_scan_kernel, dim3(cdiv(n, 128), BH), 128, 0, st, a.state, pl.splits, n);
     if (gma_status_t e = check_launch("launch tc_causal_scan", (const void*)tc_scan_kernel)) return e;
     const uint32_t smem_c = smem_bytes(causal_layout(pl.Kp).total);
     if (set_smem_optin((const void*)tc_causal_kernel<NC>, (int)smem_c, 0) != GMA_OK) return GMA_ERR_CUDA;
@@ -1936,7 +1994,7 @@ TcPlan tc_plan(const gma_problem_t& p, gma_op_t op) {
   t.off_flags = align_up(t.off_c + (size_t)p.H * kCTable * 4);
   t.off_state = align_up(t.off_flags + (size_t)p.H * (kCTable / 8) * 4);
   size_t st = 0;
-  if (op == GMA_OP_BIDIR || op == GMA_OP_CROSS || op == GMA_OP_CAUSAL_STATE) st = (size_t)BH * t.Kp * kStCols * 4;
+  if (op == GMA_OP_BIDIR || op == GMA_OP_CROSS || op == GMA_OP_CAUSAL_STATE) st = (size_t)BH * t.Kp * kStRow * 4;
   if (op == GMA_OP_CAUSAL) st = (size_t)BH * t.splits * t.Kp * kStCols * 4;  // segment aggregates
   t.total = align_up(t.off_state + st);
   return t;
@@ -1970,8 +2028,9 @@ gma_status_t tc_run(const gma_problem_t& p, gma_op_t op, int Nk, const void* Q, 
     g_fault_next = 0;
   }
   const bool with_state = op == GMA_OP_BIDIR || op == GMA_OP_CAUSAL_STATE;  // write accumulator starts at zero
-  const size_t zero_n = with_state ? (size_t)BH * pl.Kp * kStCols : 0;
-  GMA_LAUNCH("tc_prep", tc_prep_kernel, dim3(kCTable / 8, p.H), 128, 0, st, mu, sigma2, log_pi, p.H, p.K, pl.Kp,
+  const size_t zero_n = with_state ? (size_t)BH * pl.Kp * kStRow : 0;
+  if (set_carveout_max((const void*)tc_prep_kernel) != GMA_OK) return GMA_ERR_CUDA;
+  GMA_LAUNCH_DEPENDENT("tc_prep", tc_prep_kernel, dim3(kCTable / 8, p.H), 128, 0, st, mu, sigma2, log_pi, p.H, p.K, pl.Kp,
              (uint8_t*)a.w_img, (float*)a.cbias, a.ctrl, a.state, zero_n, (uint32_t*)a.range_flags);
   if (gma_status_t e = check_launch("launch tc_prep", (const void*)tc_prep_kernel)) return e;
   const int nc = pl.Kp <= 64 ? 16 : (pl.Kp <= 128 ? 32 : 64);  // components per row thread (4 per row)
@@ -1999,8 +2058,13 @@ extern "C" GMA_API int gma_debug_trace_read(unsigned long long* host, size_t n) 
   if (n > (size_t)gma::kTraceIds * gma::kTraceTiles) n = (size_t)gma::kTraceIds * gma::kTraceTiles;
   return cudaMemcpyFromSymbol(host, gma::g_trace, n * sizeof(unsigned long long)) == cudaSuccess ? 0 : -1;
 }
+extern "C" GMA_API int gma_debug_span_read(unsigned long long* host, size_t n) {
+  if (n > (size_t)gma::kSpanSlots * gma::kSpanCtas) n = (size_t)gma::kSpanSlots * gma::kSpanCtas;
+  return cudaMemcpyFromSymbol(host, gma::g_span, n * sizeof(unsigned long long)) == cudaSuccess ? 0 : -1;
+}
 extern "C" GMA_API int gma_debug_trace_clear(void) {
-  static unsigned long long zero[gma::kTraceIds * gma::kTraceTiles];
-  return cudaMemcpyToSymbol(gma::g_trace, zero, sizeof zero) == cudaSuccess ? 0 : -1;
+  static unsigned long long zero[gma::kSpanSlots * gma::kSpanCtas];
+  if (cudaMemcpyToSymbol(gma::g_span, zero, sizeof zero) != cudaSuccess) return -1;
+  return cudaMemcpyToSymbol(gma::g_trace, zero, (size_t)gma::kTraceIds * gma::kTraceTiles * 8) == cudaSuccess ? 0 : -1;
 }
 #endif

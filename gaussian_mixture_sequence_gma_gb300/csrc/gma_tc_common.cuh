@@ -158,6 +158,13 @@ __device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t 
                "r"(bytes)
                : "memory");
 }
+// Bulk float32 add shared -> global (each element of the global range += the shared one, performed at
+// L2; 16-byte aligned addresses, size a multiple of 16), bulk-group completion.
+__device__ __forceinline__ void bulk_reduce_add_f32(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"((uint64_t)dst),
+               "r"(src), "r"(bytes)
+               : "memory");
+}
 // Tiled store shared -> global (rows past the tensor's extent are not written), bulk-group completion.
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2) {
   asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"((uint64_t)map),

@@ -15,7 +15,25 @@ static __device__ unsigned long long g_trace[kTraceIds * kTraceTiles];  // one p
     if (blockIdx.x == 0 && blockIdx.y == 0 && (threadIdx.x & 31) == 0 && (t) < ::gma::kTraceTiles) \
       ::gma::g_trace[(id) * ::gma::kTraceTiles + (t)] = clock64();                                 \
   } while (0)
+// Span points: %globaltimer (ns) of every CTA (linear index below kSpanCtas) at point `slot`, taken by
+// the calling thread.
+namespace gma {
+constexpr int kSpanSlots = 10, kSpanCtas = 2048;
+static __device__ unsigned long long g_span[kSpanSlots * kSpanCtas];
+}  // namespace gma
+#define GMA_SPAN_AT(slot)                                                                  \
+  do {                                                                                     \
+    const unsigned cta_ = blockIdx.y * gridDim.x + blockIdx.x;                             \
+    if (cta_ < (unsigned)::gma::kSpanCtas) {                                               \
+      unsigned long long g_;                                                               \
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(g_));                               \
+      ::gma::g_span[(slot) * ::gma::kSpanCtas + cta_] = g_;                                \
+    }                                                                                      \
+  } while (0)
 #else
+#define GMA_SPAN_AT(slot) \
+  do {                    \
+  } while (0)
 #define GMA_TRACE_AT(id, t) \
   do {                      \
   } while (0)
