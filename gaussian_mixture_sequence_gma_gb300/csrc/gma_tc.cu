@@ -613,10 +613,9 @@ __device__ __forceinline__ uint4 pack_out8(const uint32_t* acc, float rden) {
 }
 // ----------------------------------------------------------------------------------------------- write / aggregate
 // grid (splits, B*H).  CTA (split, bh) covers tiles [split * seg_tiles, ...) of head-row bh and adds
-// Gamma_K^T [V | 1] over them into state[bh] (kAtomic) or stores it to state[bh][split] (causal).
-// The bidirectional form normalises each key's Gamma~ row inside the contraction (its [v | 1] row is
-// scaled by 1/s); the causal form (!kAtomic) normalises the Gamma row itself (bf16 gamma = e / s, V as
-// loaded, a constant 1 column).
+// Gamma_K^T [V | 1] over them into state[bh] (kAtomic: bulk reduce-add) or stores it to state[bh][split]
+// (causal segment aggregates).  Both normalise each key's Gamma row before it is packed (bf16 gamma =
+// e / s, 0 past N) and use [V | 1] as loaded, with a constant 1 column.
 template <bool kAtomic, int NC>
 __global__ void __launch_bounds__(kThreadsTc, 1)
     tc_write_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, TcArgs a) {
@@ -718,8 +717,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     const RowCtx rc = row_ctx(sbase + L.red);
     const uint32_t ga = gamma_row_addr<NC>(sbase + L.g, rc);
     if (rc.part == 0) write_ones_cols(tmem, rc);
-    // causal: element n = 64 of every row of the [V | 1] operand is 1 (rows past N have a zero gamma row)
-    if (!kAtomic && rc.part == 0) sts16(sbase + L.inv + rc.rowsw, bf16_bits(1.f));
+    // element n = 64 of every row of the [V | 1] operand is 1 (rows past N have a zero Gamma row)
+    if (rc.part == 0) sts16(sbase + L.inv + rc.rowsw, bf16_bits(1.f));
     bool ok = warp_wait(&B.w_full, 0, &B.ab, a.ctrl, 30, a.wait_ns);
     if (ok && T > 0) {
       ok = warp_wait(&B.x_full[0], 0, &B.ab, a.ctrl, 31, a.wait_ns);
@@ -735,13 +734,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     // every row warp runs all T tiles and all exchanges; after a failed wait (ok = false) it skips the
     // work and the waits but still takes part in the exchanges, whose barriers have no time limit
     for (int t = 0; t < T; ++t) {
-      const int s = t & 1;
       const int tok = (tile0 + t) * kTile + rc.row;
       float mp = -INFINITY;
       if (warp == kRowWarp0) GMA_TRACE_AT(30, t);
-      // logits of tile t; the [x^2 | x] columns are free again, so the operand of tile t+1 goes in first
+      // logits of tile t; the [x^2 | x] columns are free again, so the operand of tile t+1 goes in first:
+      // its TMEM stores drain while the logits are loaded, and one wait covers both before the operand
+      // and the logit columns are handed back to the issuer
       if (ok) ok = warp_wait(&B.l_full, t & 1, &B.ab, a.ctrl, 32, a.wait_ns);
       if (warp == kRowWarp0) GMA_TRACE_AT(31, t);
+      bool next_op = false;
       if (ok) {
         tc_fence_after();
         // x_full of u = t + 1 brings X(t + 1) (if any) and V(t)
@@ -750,49 +751,33 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         if (ok && t + 1 < T) {
           transform_row(sbase + L.x + s1 * 16384, rc, tmem);
           warp_arrive(&B.x_empty[s1]);
-          tmem_st_wait();
-          tc_fence_before();
-          warp_arrive(&B.ax_full);
+          next_op = true;
         }
       }
       if (warp == kRowWarp0) GMA_TRACE_AT(32, t);
       if (ok) {
         mp = load_logits_c<NC>(tmem, rc, v);
+        if (next_op) tmem_st_wait();
         tc_fence_before();
+        if (next_op) warp_arrive(&B.ax_full);
         warp_arrive(&B.l_empty);
       }
       if (warp == kRowWarp0) GMA_TRACE_AT(33, t);
       const float m = xchg_max(rc, 0, mp);
       if (warp == kRowWarp0) GMA_TRACE_AT(34, t);
-      if (kAtomic) {
-        // Gamma~ row (unnormalised, row maximum 1) -> smem once the previous contraction has read it:
-        // exponentiate into registers while the previous contraction may still be reading G, then store
-        float sp = 0.f;
-        if (ok) sp = exp_pack_regs<NC, true>(v, m);
-        if (warp == kRowWarp0) GMA_TRACE_AT(35, t);
-        if (ok && t > 0) ok = warp_wait(&B.g_empty, (t - 1) & 1, &B.ab, a.ctrl, 36, a.wait_ns);
-        if (warp == kRowWarp0) GMA_TRACE_AT(36, t);
-        if (ok) store_packed<NC>(v, ga, rc, a.Kp);
+      // normalised Gamma row (0 past N) -> smem once the previous contraction has read the tile: the
+      // exponentials stay in float32 registers through the sum exchange, then are scaled by 1/s, packed
+      // to bf16 and stored ([V | 1] is used as loaded)
+      float sp = 0.f;
+      if (ok) sp = exp_inplace<NC>(v, m);
+      if (warp == kRowWarp0) GMA_TRACE_AT(35, t);
+      const float sum = xchg_sum(rc, 4, sp);
+      if (warp == kRowWarp0) GMA_TRACE_AT(36, t);
+      if (ok) {
+        const float inv = tok < a.N ? rcp_approx(sum) : 0.f;
+        if (t > 0) ok = warp_wait(&B.g_empty, (t - 1) & 1, &B.ab, a.ctrl, 36, a.wait_ns);
         if (warp == kRowWarp0) GMA_TRACE_AT(37, t);
-        const float sum = xchg_sum(rc, 4, sp);
-        if (warp == kRowWarp0) GMA_TRACE_AT(38, t);
-        // normalise this key's Gamma row inside the contraction: scale its [v | 1] row by 1/s (0 past N)
-        if (ok) {
-          const float inv = tok < a.N ? rcp_approx(sum) : 0.f;
-          scale_v_row(sbase + L.v + s * 16384, rc, inv);
-          if (rc.part == 0) sts16(sbase + L.inv + rc.rowsw, bf16_bits(inv));
-        }
-      } else {
-        // normalised Gamma row (0 past N) -> smem once the previous contraction and store have read it:
-        // pack the exponentials to bf16 before the sum exchange, scale the pairs by 1/s after it
-        float sp = 0.f;
-        if (ok) sp = exp_inplace<NC>(v, m);
-        const float sum = xchg_sum(rc, 4, sp);
-        if (ok) {
-          const float inv = tok < a.N ? rcp_approx(sum) : 0.f;
-          if (t > 0) ok = warp_wait(&B.g_empty, (t - 1) & 1, &B.ab, a.ctrl, 36, a.wait_ns);
-          if (ok) scale_pack_store<NC>(v, inv, ga, rc, a.Kp);
-        }
+        if (ok) scale_pack_store<NC>(v, inv, ga, rc, a.Kp);
       }
       if (warp == kRowWarp0) GMA_TRACE_AT(39, t);
       if (ok) {
