@@ -109,6 +109,7 @@ struct Bars {
   uint64_t w_full;
   uint64_t x_full[2], x_empty[2], v_empty[2];
   uint64_t ax_full, l_full, l_empty, g_full, g_empty;
+  uint64_t g_fullq[4];  // write: Gamma rows of lane quarter q (tokens 32q .. 32q+31) stored
   uint64_t done, done_l;
   uint32_t tmem_base;
   Abort ab;
@@ -469,21 +470,6 @@ __device__ __forceinline__ void exp_pack_tmem(const float* v, float m, uint32_t 
   }
 }
 
-// Scales this thread's quarter of a key's V row (two 16-byte chunks of the swizzled bf16 tile at shared
-// address vtile) by inv.
-__device__ __forceinline__ void scale_v_row(uint32_t vtile, const RowCtx& rc, float inv) {
-  const __nv_bfloat162 inv2 = __float2bfloat162_rn(inv);
-#pragma unroll
-  for (int jj = 0; jj < 2; ++jj) {
-    const uint32_t ad = (vtile + rc.rowq) ^ (uint32_t)(jj << 4);
-    uint4 x = lds128(ad);
-    __nv_bfloat162* hx = reinterpret_cast<__nv_bfloat162*>(&x);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) hx[q] = __hmul2(hx[q], inv2);
-    sts128(ad, x);
-  }
-}
-
 __device__ __forceinline__ uint16_t bf16_bits(float x) {
   const __nv_bfloat16 h = __float2bfloat16_rn(x);
   return *reinterpret_cast<const uint16_t*>(&h);
@@ -503,6 +489,7 @@ __device__ __forceinline__ void init_bars(Bars* B, uint32_t g_release_count, uin
   mbar_init(&B->l_full, 1);
   mbar_init(&B->l_empty, kRowWarps);
   mbar_init(&B->g_full, kRowWarps);
+  for (int q = 0; q < 4; ++q) mbar_init(&B->g_fullq[q], kRowWarps / 4);
   mbar_init(&B->g_empty, g_release_count);
   mbar_init(&B->done, done_count);
   mbar_init(&B->done_l, 1);
@@ -674,6 +661,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           tc_fence_after();
           issue_logits_c(tmem, d_w, d_c, a.Kp);
           mma_commit(&B.l_full);  // also frees the [x^2 | x] columns for the next tile
+          GMA_TRACE_AT(53, t);
         }
         mma_commit(&B.done_l);
         Abort none{0};
@@ -693,18 +681,25 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         bool ok = true;
         for (int t = 0; ok && t < T; ++t) {
           const int s = t & 1;
-          // the row warps signal g_full after scaling this tile's V rows, so V has landed as well
-          ok = wait_bounded(&B.g_full, t & 1, &B.ab, a.ctrl, 24, a.wait_ns);
-          if (!ok) break;
-          GMA_TRACE_AT(20 + mb, t);
-          tc_fence_after();
+          // the K-steps of lane quarter q (tokens 32q .. 32q+31) go in once that quarter's row warps have
+          // stored their Gamma rows (they waited for this tile's V before, so V has landed as well)
           const uint64_t d_v = s ? d_v1 : d_v0;
+          for (int q = 0; ok && q < 4; ++q) {
+            ok = wait_bounded(&B.g_fullq[q], t & 1, &B.ab, a.ctrl, 24, a.wait_ns);
+            if (!ok) break;
+            if (q == 0) GMA_TRACE_AT(20 + mb, t);
+            tc_fence_after();
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            mma_ss_off(tmem + kColAcc + kStCols * mb, d_g, (ks * 2048) >> 4, d_v, (ks * 2048) >> 4, idw,
-                       (t > 0 || ks > 0) ? 1u : 0u);
+            for (int k2 = 0; k2 < 2; ++k2) {
+              const int ks = 2 * q + k2;
+              mma_ss_off(tmem + kColAcc + kStCols * mb, d_g, (ks * 2048) >> 4, d_v, (ks * 2048) >> 4, idw,
+                         (t > 0 || ks > 0) ? 1u : 0u);
+            }
+          }
+          if (!ok) break;
           mma_commit(&B.g_empty);
           mma_commit(&B.v_empty[s]);
+          GMA_TRACE_AT(22 + mb, t);
         }
         mma_commit(&B.done);
         Abort none{0};
@@ -782,9 +777,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       if (warp == kRowWarp0) GMA_TRACE_AT(39, t);
       if (ok) {
         fence_async_smem();
-        warp_arrive(&B.g_full);
+        warp_arrive(&B.g_fullq[rc.q]);
       }
       if (warp == kRowWarp0) GMA_TRACE_AT(40, t);
+      if (warp > kRowWarp0 && warp < kRowWarp0 + 4) GMA_TRACE_AT(40 + warp - kRowWarp0, t);
     }
     // epilogue: state rows of this CTA -> global
     if (kAtomic) {
