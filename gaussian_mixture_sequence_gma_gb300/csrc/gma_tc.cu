@@ -368,66 +368,6 @@ __device__ __forceinline__ uint32_t gamma_row_addr(uint32_t gtile, const RowCtx&
   return gtile + (c0 >> 6) * 16384u + (rc.rowsw ^ (((c0 & 63u) >> 3) << 4));
 }
 
-// One fused pass over this thread's NC logits with the row maximum m known: e = 2^(v - m) packed to
-// bf16 and stored as 16-byte chunks of 8 components at ga (gamma_row_addr), so the exponentials, the
-// float pipes and the shared-memory stores overlap across chunks.  Chunks at or beyond Kp are not
-// stored.  With kSum, returns the float32 sum of the e (else 0).
-template <int NC, bool kSum>
-__device__ __forceinline__ float exp_pack_store(const float* v, float m, uint32_t ga, const RowCtx& rc, int Kp) {
-  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-  const int nvalid = (Kp - NC * rc.part) >> 3;  // chunks of this thread below Kp
-#pragma unroll
-  for (int cj = 0; cj < NC / 8; ++cj) {
-    uint32_t w[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float t0 = v[8 * cj + 2 * i], t1 = v[8 * cj + 2 * i + 1];
-      add_f32x2(t0, t1, -m, -m);
-      const float e0 = ex2_approx(t0), e1 = ex2_approx(t1);
-      if (kSum) {
-        if (i & 1)
-          add_f32x2(s2, s3, e0, e1);
-        else
-          add_f32x2(s0, s1, e0, e1);
-      }
-      w[i] = pack_bf16x2(e0, e1);
-    }
-    if (cj < nvalid) sts128(ga ^ (uint32_t)(cj << 4), make_uint4(w[0], w[1], w[2], w[3]));
-  }
-  return kSum ? (s0 + s1) + (s2 + s3) : 0.f;
-}
-
-// The exponentiate-and-pack half of exp_pack_store, in place: word i of v receives the bf16 pair of
-// components 2i, 2i+1, so the shared-memory tile can still be in use by a contraction meanwhile.
-template <int NC, bool kSum>
-__device__ __forceinline__ float exp_pack_regs(float* v, float m) {
-  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-  uint32_t* w = reinterpret_cast<uint32_t*>(v);
-#pragma unroll
-  for (int i = 0; i < NC / 2; ++i) {
-    float t0 = v[2 * i], t1 = v[2 * i + 1];
-    add_f32x2(t0, t1, -m, -m);
-    const float e0 = ex2_approx(t0), e1 = ex2_approx(t1);
-    if (kSum) {
-      if (i & 1)
-        add_f32x2(s2, s3, e0, e1);
-      else
-        add_f32x2(s0, s1, e0, e1);
-    }
-    w[i] = pack_bf16x2(e0, e1);
-  }
-  return kSum ? (s0 + s1) + (s2 + s3) : 0.f;
-}
-// The store half: the NC/2 packed words of v as 16-byte chunks at ga (gamma_row_addr), below Kp.
-template <int NC>
-__device__ __forceinline__ void store_packed(const float* v, uint32_t ga, const RowCtx& rc, int Kp) {
-  const uint32_t* w = reinterpret_cast<const uint32_t*>(v);
-  const int nvalid = (Kp - NC * rc.part) >> 3;
-#pragma unroll
-  for (int cj = 0; cj < NC / 8; ++cj)
-    if (cj < nvalid) sts128(ga ^ (uint32_t)(cj << 4), make_uint4(w[4 * cj], w[4 * cj + 1], w[4 * cj + 2], w[4 * cj + 3]));
-}
-
 // (a, b) *= (c, d) with one packed float32x2 multiply.
 __device__ __forceinline__ void mul_f32x2(float& a, float& b, float c, float d) {
   asm("{\n .reg .b64 x, y;\n mov.b64 x, {%0, %1};\n mov.b64 y, {%2, %3};\n mul.rn.f32x2 x, x, y;\n"
@@ -1375,20 +1315,6 @@ __device__ __forceinline__ void snapshot_state_chunk(uint32_t sb, int Kp, int co
 }
 
 
-// Scales this thread's 16 value dims (atom `part` of the 32-byte-swizzled [V | 1] operand at vb: four 4 KB
-// atoms of 16 dims, then the constant atom) of the key row rc.row by inv.
-__device__ __forceinline__ void scale_v_row32(uint32_t vb, const RowCtx& rc, float inv) {
-  const __nv_bfloat162 inv2 = __float2bfloat162_rn(inv);
-#pragma unroll
-  for (int c = 0; c < 2; ++c) {
-    const uint32_t ad = vb + 4096u * (uint32_t)rc.part + sw32_chunk(rc.row, c);
-    uint4 x = lds128(ad);
-    __nv_bfloat162* hx = reinterpret_cast<__nv_bfloat162*>(&x);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) hx[q] = __hmul2(hx[q], inv2);
-    sts128(ad, x);
-  }
-}
 
 template <int NC>
 __global__ void __launch_bounds__(kThreadsTc, 1)
@@ -1559,7 +1485,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           mma_ts_off(tmem + kCColO, tmem + kColLog + 8 * ks, d_sb, (uint32_t)(512 * ks) >> 4, id_c80, ks > 0);
         mma_commit(&B.p_full);
         GMA_TRACE_AT(31, t);
-        if (!(ok = WAITC(&B.pb_full, ph, &B.ab, a.ctrl, 89, a.wait_ns))) break;
+        if (!(ok = WAITC(&B.pb_full, ph, &B.ab, a.ctrl, 89, a.wait_ns) &&
+                   WAITC(&B.v_full, ph, &B.ab, a.ctrl, 95, a.wait_ns)))
+          break;
         GMA_TRACE_AT(32, t);
         tc_fence_after();
 #pragma unroll 1
@@ -1634,6 +1562,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         }
       }
     }
+    // the constant atom of [V | 1]: column 0 is 1 for every key row (rows past N have a zero Gamma_K row)
+    if (rc.part == 0) sts16(sbase + L.v + 16384 + sw32_chunk(rc.row, 0), bf16_bits(1.f));
     tmem_st_wait();
     fence_async_smem();
     tc_fence_before();
@@ -1660,6 +1590,37 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         tc_fence_before();
         warp_arrive(&B.ax_full);
       }
+      // while the key logits run: snapshot the state after tile t-1's update for this tile's inter-tile
+      // term (the previous inter-tile term has read S_prev before p_full of t-1; this tile's state update
+      // waits for the snapshot).  Parts 0 / 1 take columns 0..31 and Z of state block 0 / 1, parts 2 / 3
+      // columns 32..63.
+      if (warp == kRowWarp0) GMA_TRACE_AT(14, t);
+      if (ok && t > 0) ok = warp_wait(&B.s_done, (t - 1) & 1, &B.ab, a.ctrl, 107, a.wait_ns);
+      if (warp == kRowWarp0) GMA_TRACE_AT(15, t);
+      if (ok && t > 0) {
+        tc_fence_after();
+        const int mb = rc.part & 1;
+        if (mb < MB) {
+          const int comp = 128 * mb + rc.row;
+          const uint32_t ts = tmem + rc.lane_base + kCColS + kStCols * mb;
+          const int c0 = rc.part < 2 ? 0 : 2;
+          uint32_t ra[16];
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            tmem_ld16(ts + 16 * (c0 + c), ra);
+            tmem_ld_wait_tied16(ra);
+            if (comp < a.Kp) snapshot_state_chunk(sbase + L.sbv, a.Kp, comp, c0 + c, ra, a.eps);
+          }
+          if (rc.part < 2) {
+            uint32_t z = tmem_ld1(ts + 64);
+            tmem_ld_wait_tied1(z);
+            if (comp < a.Kp) snapshot_state_chunk(sbase + L.sbv, a.Kp, comp, 4, &z, a.eps);
+          }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        warp_arrive(&B.sb_full);
+      }
       // key logits -> registers; then the query operand -> OX
       float mk = -INFINITY;
       if (warp == kRowWarp0) GMA_TRACE_AT(2, t);
@@ -1680,24 +1641,22 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         }
       }
       if (warp == kRowWarp0) GMA_TRACE_AT(4, t);
-      // key softmax: the unnormalised Gamma~_K row (row maximum 1) -> smem once the previous tile's readers
-      // are done; the key's [v | 1] row is scaled by 1/s (0 past N), which normalises it inside both the
-      // state update and P [V | 1] (P then carries s_j, the scaled row divides it out)
+      // key softmax: the normalised Gamma_K row (0 past N) -> smem once the previous tile's readers are done
+      // (state update, P, and the output tile staged in its first block); [V | 1] is used as loaded
       const float m_k = xchg_max(rc, s0, mk);
       if (warp == kRowWarp0) GMA_TRACE_AT(5, t);
       float sp = 0.f;
-      if (ok && t > 0)
-        ok = warp_wait(&B.gk_empty, (t - 1) & 1, &B.ab, a.ctrl, 104, a.wait_ns) &&
-             warp_wait(&B.o_stored, (t - 1) & 1, &B.ab, a.ctrl, 110, a.wait_ns);
-      if (ok) sp = exp_pack_store<NC, true>(v, m_k, ga, rc, a.Kp);
+      if (ok) sp = exp_inplace<NC>(v, m_k);
       if (warp == kRowWarp0) GMA_TRACE_AT(6, t);
       const float sum = xchg_sum(rc, s1, sp);
       if (warp == kRowWarp0) GMA_TRACE_AT(7, t);
-      if (ok) ok = warp_wait(&B.v_full, ph, &B.ab, a.ctrl, 109, a.wait_ns);
+      if (ok && t > 0)
+        ok = warp_wait(&B.gk_empty, (t - 1) & 1, &B.ab, a.ctrl, 104, a.wait_ns) &&
+             warp_wait(&B.o_stored, (t - 1) & 1, &B.ab, a.ctrl, 110, a.wait_ns);
+      if (warp == kRowWarp0) GMA_TRACE_AT(19, t);
       if (ok) {
         const float inv = tok < a.N ? rcp_approx(sum) : 0.f;
-        scale_v_row32(sbase + L.v, rc, inv);
-        if (rc.part == 0) sts16(sbase + L.v + 16384 + sw32_chunk(rc.row, 0), bf16_bits(inv));
+        scale_pack_store<NC>(v, inv, ga, rc, a.Kp);
         fence_async_smem();
         warp_arrive(&B.gk_full);
       }
@@ -1739,36 +1698,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         tmem_st_wait();
         tc_fence_before();
         warp_arrive(&B.pb_full);
-      }
-      // the inter-tile term has read S_prev (before p_full); once the state update has completed,
-      // snapshot the updated state for the next tile.  Parts 0 / 1 take columns 0..31 and Z of state
-      // block 0 / 1, parts 2 / 3 columns 32..63.
-      if (warp == kRowWarp0) GMA_TRACE_AT(14, t);
-      if (ok) ok = warp_wait(&B.s_done, ph, &B.ab, a.ctrl, 107, a.wait_ns);
-      if (warp == kRowWarp0) GMA_TRACE_AT(15, t);
-      if (ok) {
-        tc_fence_after();
-        const int mb = rc.part & 1;
-        if (mb < MB) {
-          const int comp = 128 * mb + rc.row;
-          const uint32_t ts = tmem + rc.lane_base + kCColS + kStCols * mb;
-          const int c0 = rc.part < 2 ? 0 : 2;
-          uint32_t ra[16];
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            tmem_ld16(ts + 16 * (c0 + c), ra);
-            tmem_ld_wait_tied16(ra);
-            if (comp < a.Kp) snapshot_state_chunk(sbase + L.sbv, a.Kp, comp, c0 + c, ra, a.eps);
-          }
-          if (rc.part < 2) {
-            uint32_t z = tmem_ld1(ts + 64);
-            tmem_ld_wait_tied1(z);
-            if (comp < a.Kp) snapshot_state_chunk(sbase + L.sbv, a.Kp, comp, 4, &z, a.eps);
-          }
-        }
-        fence_async_smem();
-        tc_fence_before();
-        warp_arrive(&B.sb_full);
       }
       // output: dims 8 part + [0, 8) and 32 + 8 part + [0, 8) -- the columns this thread's part of the
       // next key operand overwrites -- normalised by gq~ . (Z + eps)
