@@ -3,6 +3,8 @@
 #include <cuda_runtime.h>
 
 #include <cstdio>
+#include <atomic>
+#include <cstdlib>
 #include <mutex>
 #include <vector>
 
@@ -48,6 +50,33 @@ gma_status_t set_smem_optin(const void* func, int bytes, int /*slot*/) {
     return cuda_fail("cudaFuncSetAttribute(max dynamic shared memory)");
   done.push_back({func, dev, bytes});
   return GMA_OK;
+}
+
+namespace {
+constexpr uint64_t kDefaultWaitNs = 1000000000ull;  // 1 s
+constexpr uint64_t kMinWaitNs = 1000000ull;         // 1 ms
+constexpr uint64_t kMaxWaitNs = 600000000000ull;    // 10 min
+std::atomic<uint64_t> g_wait_ns{0};                 // 0: not set through the API
+
+uint64_t env_wait_ns() {
+  static const uint64_t v = [] {
+    const char* e = std::getenv("GMA_WAIT_LIMIT_MS");
+    if (!e || !*e) return (uint64_t)0;
+    char* end = nullptr;
+    const double ms = std::strtod(e, &end);
+    if (end == e || !(ms > 0)) return (uint64_t)0;
+    const double ns = ms * 1e6;
+    return ns < (double)kMinWaitNs ? kMinWaitNs : (ns > (double)kMaxWaitNs ? kMaxWaitNs : (uint64_t)ns);
+  }();
+  return v;
+}
+}  // namespace
+
+uint64_t wait_limit_ns() {
+  const uint64_t v = g_wait_ns.load(std::memory_order_relaxed);
+  if (v) return v;
+  const uint64_t e = env_wait_ns();
+  return e ? e : kDefaultWaitNs;
 }
 
 gma_status_t set_carveout_max(const void* func) {
@@ -114,6 +143,10 @@ ProjLayout proj_layout(const gma_problem_t& p, bool causal) {
 gma_status_t run(const gma_problem_t* p, gma_op_t op, int Nk, const void* Q, const void* K, const void* V,
                  const float* mu, const float* sigma2, const float* log_pi, void* out, void* ws, size_t ws_bytes,
                  void* stream) {
+  static const char* const kNames[] = {"gma_responsibilities", "gma_forward_bidir", "gma_forward_causal",
+                                       "gma_forward_cross", "gma_causal_state"};
+  const int oi = (int)op;
+  NvtxScope range(oi >= 0 && oi < 5 ? kNames[oi] : "gma_call");
   gma_status_t s = validate_problem(p);
   if (s != GMA_OK) return s;
   if (Nk < 0) return GMA_ERR_INVALID_ARG;
@@ -172,6 +205,14 @@ gma_status_t run_backward(const gma_problem_t* p, bool causal, const void* Q, co
 using namespace gma;
 
 extern "C" {
+
+gma_status_t gma_set_wait_limit_ns(uint64_t ns) {
+  if (ns != 0 && (ns < gma::kMinWaitNs || ns > gma::kMaxWaitNs)) return GMA_ERR_INVALID_ARG;
+  gma::g_wait_ns.store(ns, std::memory_order_relaxed);
+  return GMA_OK;
+}
+
+uint64_t gma_get_wait_limit_ns(void) { return gma::wait_limit_ns(); }
 
 size_t gma_workspace_bytes(const gma_problem_t* p, gma_op_t op) {
   if (validate_problem(p) != GMA_OK) return 0;

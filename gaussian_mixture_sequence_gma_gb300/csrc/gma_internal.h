@@ -81,8 +81,20 @@ gma_status_t proj_run(const gma_problem_t& p, int dm, const void* X, const void*
 // bounded device wait runs out and reports GMA_ERR_TIMEOUT.
 void tc_set_fault_injection(uint32_t mask);
 
-// Launch bookkeeping: counts every kernel launch and, while profiling is on, brackets it with a
-// CUDA event pair on the launch stream.
+// NVTX range for the lifetime of the object (one per C-ABI call).
+struct NvtxScope {
+  explicit NvtxScope(const char* name);
+  ~NvtxScope();
+  NvtxScope(const NvtxScope&) = delete;
+  NvtxScope& operator=(const NvtxScope&) = delete;
+};
+
+// Limit of every bounded device wait of the tensor-core kernels, in ns: gma_set_wait_limit_ns(), else the
+// environment variable GMA_WAIT_LIMIT_MS (read once), else 1 s.
+uint64_t wait_limit_ns();
+
+// Launch bookkeeping: counts every kernel launch, brackets it with an NVTX range named for its phase
+// and, while profiling is on, with a CUDA event pair on the launch stream.
 void* prof_before(cudaStream_t st, const char* name);
 void prof_after(cudaStream_t st, void* token);
 

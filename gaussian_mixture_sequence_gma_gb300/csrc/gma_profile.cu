@@ -1,5 +1,6 @@
-// gma_profile.cu -- launch counter and optional per-kernel CUDA-event timing.
+// gma_profile.cu -- launch counter, NVTX ranges and optional per-kernel CUDA-event timing.
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <atomic>
 #include <cstdio>
@@ -40,8 +41,14 @@ cudaEvent_t take_event() {
 
 }  // namespace
 
+NvtxScope::NvtxScope(const char* name) { nvtxRangePushA(name); }
+NvtxScope::~NvtxScope() { nvtxRangePop(); }
+
+// Every launch is bracketed by an NVTX range named for its phase (nested inside the range of the C-ABI
+// call that made it), so a timeline tool shows which call and phase enqueued each kernel.
 void* prof_before(cudaStream_t st, const char* name) {
   g_launches.fetch_add(1, std::memory_order_relaxed);
+  nvtxRangePushA(name);
   if (!g_recording.load(std::memory_order_relaxed)) return nullptr;
   std::lock_guard<std::mutex> lock(g_mu);
   Rec r{name, take_event(), take_event()};
@@ -52,6 +59,7 @@ void* prof_before(cudaStream_t st, const char* name) {
 }
 
 void prof_after(cudaStream_t st, void* token) {
+  nvtxRangePop();
   if (!token) return;
   std::lock_guard<std::mutex> lock(g_mu);
   size_t i = (size_t)(uintptr_t)token - 1;

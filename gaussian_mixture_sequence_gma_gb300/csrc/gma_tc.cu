@@ -56,7 +56,6 @@ constexpr int kStRow = 68;   // row of the accumulated state in global memory: [
 constexpr int kCTable = 256;  // c' entries per head (-inf past K)
 constexpr int kTargetCtas = 152;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s per wait
 
 // TMEM columns (512 allocated)
 constexpr uint32_t kColLog = 0;    // logits, Kp columns (<= 256)
@@ -1931,7 +1930,7 @@ gma_status_t tc_run(const gma_problem_t& p, gma_op_t op, int Nk, const void* Q, 
   a.seg_tiles = pl.seg_tiles;
   a.splits = pl.splits;
   a.eps = p.eps;
-  a.wait_ns = kWaitNs;
+  a.wait_ns = wait_limit_ns();
   if (op == GMA_OP_BIDIR) {
     std::lock_guard<std::mutex> lock(g_fault_mu);
     a.fault = g_fault_next;

@@ -23,7 +23,7 @@ EXPORTED = ("gma_workspace_bytes", "gma_responsibilities", "gma_forward_bidir", 
             "gma_forward_projected",
             "gma_check_device_error", "gma_status_string", "gma_version", "gma_last_error", "gma_launch_count", "gma_profile_enable",
             "gma_profile_read", "gma_forward_bidir_static_ws", "gma_static_ws_capacity", "gma_static_ws_check_error",
-            "gma_debug_withhold_first_load", "gma_probe_ex2_rate")
+            "gma_debug_withhold_first_load", "gma_probe_ex2_rate", "gma_set_wait_limit_ns", "gma_get_wait_limit_ns")
 
 
 class GmaError(RuntimeError):
@@ -101,6 +101,10 @@ def lib():
     L.gma_probe_ex2_rate.restype = ctypes.c_int
     L.gma_debug_withhold_first_load.argtypes = []
     L.gma_debug_withhold_first_load.restype = None
+    L.gma_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    L.gma_set_wait_limit_ns.restype = ctypes.c_int
+    L.gma_get_wait_limit_ns.argtypes = []
+    L.gma_get_wait_limit_ns.restype = ctypes.c_uint64
     L.gma_launch_count.argtypes = []
     L.gma_launch_count.restype = ctypes.c_ulonglong
     L.gma_profile_enable.argtypes = [ctypes.c_int]
@@ -397,6 +401,17 @@ def check_device_error(workspace, stream=None) -> int:
     dev = workspace.device
     with torch.cuda.device(dev):
         return int(lib().gma_check_device_error(_ptr(workspace), _stream_handle(stream, dev)))
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    """Process-wide limit of the bf16 kernels' bounded device waits (0: the default, GMA_WAIT_LIMIT_MS or 1 s)."""
+    st = int(lib().gma_set_wait_limit_ns(int(ns)))
+    if st != GMA_OK:
+        raise GmaError(st, "gma_set_wait_limit_ns")
+
+
+def wait_limit_ns() -> int:
+    return int(lib().gma_get_wait_limit_ns())
 
 
 def launch_count() -> int:

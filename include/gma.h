@@ -302,6 +302,21 @@ GMA_API gma_status_t gma_forward_projected(const gma_problem_t *p, int causal, i
  */
 GMA_API gma_status_t gma_check_device_error(void *ws, void *stream);
 
+/*
+ * Time limit of every bounded device wait of the bf16 (tensor-core) kernels,
+ * process-wide: a wait that runs this long sets the workspace error word
+ * (GMA_ERR_TIMEOUT through gma_check_device_error()) and the kernel returns.
+ * The library has no counterpart in the pages; it is the failure-detection knob
+ * of this implementation.  gma_set_wait_limit_ns(0) restores the default: the
+ * environment variable GMA_WAIT_LIMIT_MS (milliseconds, read once, clamped to
+ * [1 ms, 10 min]) if set, else 1 s.  Other values must lie in [1e6, 6e11] ns,
+ * else GMA_ERR_INVALID_ARG and the limit is unchanged.  Takes effect for calls
+ * made afterwards; kernels already enqueued keep the limit they were given.
+ * gma_get_wait_limit_ns() returns the limit the next call will use.
+ */
+GMA_API gma_status_t gma_set_wait_limit_ns(uint64_t ns);
+GMA_API uint64_t gma_get_wait_limit_ns(void);
+
 /* Static, NUL-terminated description of a status code. */
 GMA_API const char *gma_status_string(gma_status_t s);
 

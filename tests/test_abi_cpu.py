@@ -4,6 +4,7 @@ import ctypes
 import os
 import re
 import subprocess
+import sys
 
 import pytest
 
@@ -298,3 +299,37 @@ def test_static_ws_binding_rejects_mixed_dtypes_before_any_call(L, monkeypatch):
         gma.forward_bidir_static_ws(q, q, q, mu, s2, lp, out=torch.zeros(1, 2, 7, 64))
     with pytest.raises(ValueError):
         gma.forward_bidir_static_ws(q, torch.zeros(1, 2, 9, 64), q, mu, s2, lp)
+
+
+def test_wait_limit_setter(L):
+    """The bounded-wait limit: default 1 s, settable within [1 ms, 10 min], 0 restores the default,
+    out-of-range values are refused and leave the limit unchanged."""
+    assert L.gma_set_wait_limit_ns(0) == gma.GMA_OK
+    default = L.gma_get_wait_limit_ns()
+    env = os.environ.get("GMA_WAIT_LIMIT_MS")
+    assert default == (int(float(env) * 1e6) if env else 1_000_000_000)
+    try:
+        assert L.gma_set_wait_limit_ns(20_000_000) == gma.GMA_OK
+        assert L.gma_get_wait_limit_ns() == 20_000_000
+        assert L.gma_set_wait_limit_ns(999_999) == gma.GMA_ERR_INVALID_ARG
+        assert L.gma_set_wait_limit_ns(600_000_000_001) == gma.GMA_ERR_INVALID_ARG
+        assert L.gma_get_wait_limit_ns() == 20_000_000
+        gma.set_wait_limit_ns(5_000_000)
+        assert gma.wait_limit_ns() == 5_000_000
+        with pytest.raises(gma.GmaError):
+            gma.set_wait_limit_ns(1)
+    finally:
+        assert L.gma_set_wait_limit_ns(0) == gma.GMA_OK
+    assert L.gma_get_wait_limit_ns() == default
+
+
+def test_wait_limit_environment_variable():
+    """GMA_WAIT_LIMIT_MS sets the default of a fresh process (clamped to [1 ms, 10 min])."""
+    code = ("from gaussian_mixture_sequence_gma_gb300 import gma; print(gma.wait_limit_ns())")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    for ms, want in (("250", 250_000_000), ("0.0001", 1_000_000), ("1e9", 600_000_000_000), ("junk", 1_000_000_000)):
+        env = dict(os.environ, GMA_WAIT_LIMIT_MS=ms)
+        out = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True, text=True,
+                             timeout=120)
+        assert out.returncode == 0, out.stderr
+        assert int(out.stdout.strip().splitlines()[-1]) == want, ms

@@ -38,3 +38,32 @@ def test_withheld_load_times_out_and_context_recovers():
     ref = orc.forward(inp["Q"], inp["K"], inp["V"], inp["mu"], inp["sigma2"], inp["log_pi"], 1e-6)
     assert np.isfinite(O).all()
     assert rel_err(O, ref) <= TOL["bf16"]
+
+
+def test_short_wait_limit_reports_sooner():
+    """With the limit set to 20 ms the withheld load is reported as GMA_ERR_TIMEOUT well within the 1 s
+    default (a chain of a few bounded waits, each 20 ms), and restoring the default leaves the next call
+    normal."""
+    import torch
+    from gaussian_mixture_sequence_gma_gb300 import gma
+    inp = make_inputs(1, 2, 512, 64, dtype="bf16", seed=22)
+    t = to_device(inp)
+    args = (t["Q"], t["K"], t["V"], t["mu"], t["sigma2"], t["log_pi"])
+    prob = gma.problem(1, 2, 512, 64, torch.bfloat16, 1e-6)
+    ws = gma.alloc_workspace(prob, gma.OP_BIDIR, "cuda")
+    gma.forward_bidir(*args, workspace=ws)
+    assert gma.check_device_error(ws) == gma.GMA_OK
+    gma.set_wait_limit_ns(20_000_000)
+    try:
+        gma.lib().gma_debug_withhold_first_load()
+        torch.cuda.synchronize()
+        t0 = time.time()
+        gma.forward_bidir(*args, workspace=ws)
+        assert gma.check_device_error(ws) == gma.GMA_ERR_TIMEOUT
+        assert time.time() - t0 < 0.9
+    finally:
+        gma.set_wait_limit_ns(0)
+    O = gma.forward_bidir(*args, workspace=ws).float().cpu().numpy()
+    assert gma.check_device_error(ws) == gma.GMA_OK
+    ref = orc.forward(inp["Q"], inp["K"], inp["V"], inp["mu"], inp["sigma2"], inp["log_pi"], 1e-6)
+    assert rel_err(O, ref) <= TOL["bf16"]
