@@ -548,7 +548,7 @@ def run_gma(args, world, rank, local):
             "ms": t_p * 1e3, "tok_heads_per_s": Bp * Hp * Np / t_p, "forward_only_ms": mu_ / 10,
             "projection_ms": t_p * 1e3 - mu_ / 10, "tflops_algorithmic": (gemm_flop + gma_flop) / t_p / 1e12,
             "frac_of_bf16_peak": (gemm_flop + gma_flop) / t_p / 1e12 / peaks["bf16"],
-            "note": "projection = one cuBLASLt GEMM (float32 out) + one layout kernel; Q, K, V round-trip HBM"}
+            "note": "projection = one tcgen05 GEMM with bias and layout in its epilogue (bf16 Q, K, V round-trip HBM)"}
         del tp, wsp, outp, qkv
         # backward pass of the bidirectional form (float32 CUDA-core kernels) on the bidir bf16 workload shape
         wb = workloads()["bidir_bf16_B4H8N4096K128"]

@@ -131,8 +131,9 @@ ProjLayout proj_layout(const gma_problem_t& p, bool causal) {
   const size_t qkv = align_up((size_t)p.B * p.H * p.N * kD * es);
   L.base = align_up(required_bytes(p, causal ? GMA_OP_CAUSAL : GMA_OP_BIDIR));
   L.lt = L.base;
-  L.y = L.lt + align_up(proj_lt_workspace_bytes());
-  L.q = L.y + align_up((size_t)p.B * p.N * 3 * p.H * kD * sizeof(float));
+  const bool lib_gemm = p.dtype != GMA_BF16;  // float32 I/O: library GEMM workspace and a float32 Y
+  L.y = L.lt + (lib_gemm ? align_up(proj_lt_workspace_bytes()) : 0);
+  L.q = L.y + (lib_gemm ? align_up((size_t)p.B * p.N * 3 * p.H * kD * sizeof(float)) : 0);
   L.k = L.q + qkv;
   L.v = L.k + qkv;
   L.total = L.v + qkv;
@@ -142,7 +143,7 @@ ProjLayout proj_layout(const gma_problem_t& p, bool causal) {
 // Nk: keys / values per (b, h); N (= p->N) except for cross-attention.
 gma_status_t run(const gma_problem_t* p, gma_op_t op, int Nk, const void* Q, const void* K, const void* V,
                  const float* mu, const float* sigma2, const float* log_pi, void* out, void* ws, size_t ws_bytes,
-                 void* stream) {
+                 void* stream, bool clear_err = true) {
   static const char* const kNames[] = {"gma_responsibilities", "gma_forward_bidir", "gma_forward_causal",
                                        "gma_forward_cross", "gma_causal_state"};
   const int oi = (int)op;
@@ -166,7 +167,7 @@ gma_status_t run(const gma_problem_t* p, gma_op_t op, int Nk, const void* Q, con
   cudaStream_t st = (cudaStream_t)stream;
   cudaGetLastError();  // a stale error from earlier caller work is not ours to report
   if (op == GMA_OP_CROSS) op = GMA_OP_BIDIR;  // the bidirectional kernels, with the key length Nk
-  if (p->dtype == GMA_BF16) return tc_run(*p, op, Nk, Q, K, V, mu, sigma2, log_pi, out, ws, st);
+  if (p->dtype == GMA_BF16) return tc_run(*p, op, Nk, Q, K, V, mu, sigma2, log_pi, out, ws, st, clear_err);
   return simt_run(*p, op, Nk, Q, K, V, mu, sigma2, log_pi, out, ws, st);
 }
 
@@ -241,10 +242,11 @@ gma_status_t gma_forward_projected(const gma_problem_t* p, int causal, int dm, c
   cudaGetLastError();
   const ProjLayout L = proj_layout(*p, causal != 0);
   char* w = (char*)ws;
-  s = proj_run(*p, dm, X, Wqkv, bqkv, (float*)(w + L.y), w + L.q, w + L.k, w + L.v, w + L.lt, st);
+  s = proj_run(*p, dm, X, Wqkv, bqkv, (float*)(w + L.y), w + L.q, w + L.k, w + L.v, w + L.lt, (Ctrl*)ws, st);
   if (s != GMA_OK) return s;
+  // bf16: the projection kernel cleared the error word and reports its bounded waits there
   return run(p, causal ? GMA_OP_CAUSAL : GMA_OP_BIDIR, p->N, w + L.q, w + L.k, w + L.v, mu, sigma2, log_pi, O, ws,
-             L.base, stream);
+             L.base, stream, p->dtype != GMA_BF16);
 }
 
 gma_status_t gma_responsibilities(const gma_problem_t* p, const void* X, const float* mu, const float* sigma2,

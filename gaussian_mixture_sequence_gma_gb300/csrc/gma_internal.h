@@ -1,6 +1,7 @@
 // gma_internal.h -- host-side plumbing shared by the translation units of libgma.so.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -57,10 +58,16 @@ struct TcPlan {
   size_t total;
 };
 TcPlan tc_plan(const gma_problem_t& p, gma_op_t op);
+// clear_err: the parameter fold clears the workspace error word first (false when an earlier kernel of
+// the same call, the tcgen05 projection, has already cleared it and may have reported into it).
 gma_status_t tc_run(const gma_problem_t& p, gma_op_t op, int Nk, const void* Q, const void* K, const void* V,
                     const float* mu, const float* sigma2, const float* log_pi, void* out, void* ws,
-                    cudaStream_t stream);
+                    cudaStream_t stream, bool clear_err = true);
 bool tc_available();
+// Tensor map over a row-major bf16 matrix [rows][cols]: boxes of box_cols x box_rows, 128-byte swizzle,
+// zero fill outside (a 3-D map with a unit outer dimension, read with 3-D tensor loads).
+bool make_map_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols,
+                   uint32_t box_rows);
 // Backward pass of the bidirectional or causal forward (float32 CUDA-core kernels, both I/O dtypes).
 size_t simt_backward_bytes(const gma_problem_t& p, bool causal);
 gma_status_t simt_backward(const gma_problem_t& p, bool causal, const void* Q, const void* K, const void* V, const float* mu,
@@ -72,11 +79,13 @@ size_t simt_decode_bytes(const gma_problem_t& p);
 gma_status_t simt_decode(const gma_problem_t& p, const void* Q, const void* K, const void* V, const float* mu,
                          const float* sigma2, const float* log_pi, float* state, void* out, void* ws,
                          cudaStream_t stream);
-// Q / K / V projection of a Transformer block: Y = X Wqkv (library GEMM, float32) into Y, then the bias
-// and the [B][H][N][64] layout of the I/O dtype into Q, K, V.  lt_ws: proj_lt_workspace_bytes() bytes.
+// Q / K / V projection of a Transformer block into Q, K, V ([B][H][N][64], I/O dtype, bias added).  bf16:
+// one tcgen05 GEMM with the layout in its epilogue; it clears ctrl's error word and reports its own
+// bounded waits there (Y and lt_ws unused).  float32: library GEMM into Y (float32), then a layout
+// kernel; lt_ws: proj_lt_workspace_bytes() bytes.
 size_t proj_lt_workspace_bytes();
 gma_status_t proj_run(const gma_problem_t& p, int dm, const void* X, const void* W, const float* bias, float* Y,
-                      void* Q, void* K, void* V, void* lt_ws, cudaStream_t st);
+                      void* Q, void* K, void* V, void* lt_ws, Ctrl* ctrl, cudaStream_t st);
 // Test hook: bit 0 makes the next bidirectional write launch skip its first X-tile load, so that a
 // bounded device wait runs out and reports GMA_ERR_TIMEOUT.
 void tc_set_fault_injection(uint32_t mask);

@@ -3,16 +3,18 @@
 // attention of a Transformer block whose queries, keys and values are linear projections of the
 // block input; the causal language model of the experiments uses it at d_model = 768, 12 heads).
 //
-// One plain library GEMM, Y [B*N][3*H*64] = X [B*N][dm] Wqkv [dm][3*H*64], float32 accumulation and
-// float32 output (cuBLASLt), then one layout kernel that adds the bias in float32, rounds once to the
-// I/O dtype and writes Q, K, V as [B][H][N][64] for the GMA kernels.  Column block 0 of Y holds Q,
-// block 1 K, block 2 V; within a block, columns 64h .. 64h+63 are head h.
+// bf16 I/O: one hand-written tcgen05 GEMM, Y [B*N][3*H*64] = X [B*N][dm] Wqkv [dm][3*H*64] with float32
+// accumulation in TMEM, whose epilogue adds the bias in float32, rounds once to bf16 and writes Q, K, V
+// as [B][H][N][64] for the GMA kernels (no float32 Y).  float32 I/O: one plain library GEMM (cuBLASLt,
+// float32 output) and one layout kernel doing the same.  Column block 0 of Y holds Q, block 1 K, block 2
+// V; within a block, columns 64h .. 64h+63 are head h.
 #include <cublasLt.h>
 
 #include <cstdio>
 #include <mutex>
 
 #include "gma_internal.h"
+#include "gma_tc_common.cuh"
 
 namespace gma {
 namespace {
@@ -74,12 +76,156 @@ __global__ void __launch_bounds__(256) proj_layout_kernel(const float* __restric
   }
 }
 
+// ---- bf16: one hand-written tcgen05 GEMM with the bias, the rounding and the layout in its epilogue ----
+// Y [M = B*N][Ncol] = X [M][dm] Wqkv [dm][Ncol] in 128 x 256 tiles, one tile per CTA, two CTAs per SM (each
+// holds 97 KB of shared memory and 256 TMEM columns, so one CTA's epilogue overlaps the other's
+// contractions).  A = X tile (K-major, 128-byte swizzle); B = Wqkv tile read as an MN-major operand: four
+// 64-column boxes of 64 rows, 8 KB apart.  The K loop runs over 64-wide blocks of dm in a two-stage TMA
+// ring (zero fill past dm, M and Ncol).  Warp 0 loads, one thread of warp 1 issues the contractions (and
+// warp 1 owns the TMEM columns), warps 2-5 take a lane quarter of the accumulator each: 16 columns at a
+// time, + bias in float32, rounded once to bf16, stored straight into Q, K or V [B][H][N][64].
+constexpr int kPBM = 128, kPBN = 256, kPBK = 64, kPStages = 2, kPThreads = 192;
+constexpr uint32_t kPStageA = kPBM * kPBK * 2, kPStageB = kPBN * kPBK * 2, kPStage = kPStageA + kPStageB;
+constexpr uint32_t kPSmem = kPStages * kPStage + 1024;  // + 1 KB alignment slack
+
+struct ProjBars {
+  uint64_t full[kPStages], empty[kPStages], acc;
+  uint32_t tmem;
+  tc::Abort ab;
+};
+
+__global__ void __launch_bounds__(kPThreads, 2)
+    proj_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                   const float* __restrict__ bias, int M, int Ncol, int dm, int H, int N, __nv_bfloat16* __restrict__ Q,
+                   __nv_bfloat16* __restrict__ K, __nv_bfloat16* __restrict__ V, Ctrl* ctrl, uint64_t wait_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
+  __shared__ ProjBars B;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.x * kPBM, n0 = blockIdx.y * kPBN;
+  const int KB = (dm + kPBK - 1) / kPBK;
+  // this call's error word starts clear (the forward that follows leaves it as this kernel left it)
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+    ctrl->err = kErrNone;
+    ctrl->err_site = 0;
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPStages; ++s) {
+      tc::mbar_init(&B.full[s], 1);
+      tc::mbar_init(&B.empty[s], 1);
+    }
+    tc::mbar_init(&B.acc, 1);
+    B.ab.flag = 0;
+    tc::mbar_fence_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(&B.tmem, 256);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = B.tmem;
+  const uint32_t sa = tc::smem_u32(smem);
+  if (warp == 0) {
+    if (lane == 0) {
+      int last[kPStages];
+      for (int s = 0; s < kPStages; ++s) last[s] = -1;
+      for (int kb = 0; kb < KB; ++kb) {
+        const int s = kb % kPStages;
+        const uint32_t ph = (uint32_t)(kb / kPStages) & 1u;
+        // the slot is free once the contractions of its previous block have read it
+        if (kb >= kPStages && !tc::wait_bounded(&B.empty[s], ph ^ 1u, &B.ab, ctrl, 130, wait_ns)) break;
+        tc::mbar_expect_tx(&B.full[s], kPStage);
+        uint8_t* st = smem + (size_t)s * kPStage;
+        tc::tma_load_3d(st, &tmX, kPBK * kb, m0, 0, &B.full[s]);
+#pragma unroll
+        for (int i = 0; i < kPBN / 64; ++i)
+          tc::tma_load_3d(st + kPStageA + 8192 * i, &tmW, n0 + 64 * i, kPBK * kb, 0, &B.full[s]);
+        last[s] = (int)ph;
+      }
+      // never leave with copies in flight
+      tc::Abort none{0};
+      for (int s = 0; s < kPStages; ++s)
+        if (last[s] >= 0) tc::wait_bounded(&B.full[s], (uint32_t)last[s], &none, ctrl, 131, wait_ns);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc::make_idesc(kPBM, kPBN, 1, 1, 0, 1);  // bf16 x bf16, A K-major, B MN-major
+      bool ok = true;
+      for (int kb = 0; kb < KB; ++kb) {
+        const int s = kb % kPStages;
+        if (!(ok = tc::wait_bounded(&B.full[s], (uint32_t)(kb / kPStages) & 1u, &B.ab, ctrl, 132, wait_ns))) break;
+        tc::tc_fence_after();
+        const uint32_t a = sa + (uint32_t)s * kPStage;
+        const uint64_t da = tc::make_sdesc(a, 16, 1024), db = tc::make_sdesc(a + kPStageA, 8192, 1024);
+#pragma unroll
+        for (int ks = 0; ks < kPBK / 16; ++ks)
+          tc::mma_ss_off(tmem, da, (uint32_t)(32 * ks) >> 4, db, (uint32_t)(2048 * ks) >> 4, idesc,
+                         (kb > 0 || ks > 0) ? 1u : 0u);
+        tc::mma_commit(&B.empty[s]);
+      }
+      tc::mma_commit(&B.acc);
+      tc::Abort none{0};
+      tc::wait_bounded(&B.acc, 0, &none, ctrl, 133, wait_ns);  // the contractions are done before TMEM is freed
+    }
+  } else {
+    // epilogue: warp w reads TMEM lane quarter w % 4, token row m0 + 32 (w % 4) + lane
+    const int q = warp & 3, m = m0 + 32 * q + lane;
+    const bool ok = tc::warp_wait(&B.acc, 0, &B.ab, ctrl, 134, wait_ns);
+    if (ok) {
+      tc::tc_fence_after();
+      const int b = m / N, n = m - (m / N) * N;
+      const int hc = H * kD;  // columns of each of Q, K, V
+#pragma unroll 2
+      for (int c = 0; c < kPBN / 16; ++c) {
+        uint32_t r[16];
+        tc::tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + 16 * c, r);
+        tc::tmem_ld_wait_tied16(r);
+        const int col = n0 + 16 * c;
+        if (col < Ncol && m < M) {
+          const float4* bs = reinterpret_cast<const float4*>(bias + col);
+          uint32_t u[8];
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const float4 bb = __ldg(bs + k4);
+            u[2 * k4] = tc::pack_bf16x2(__uint_as_float(r[4 * k4]) + bb.x, __uint_as_float(r[4 * k4 + 1]) + bb.y);
+            u[2 * k4 + 1] = tc::pack_bf16x2(__uint_as_float(r[4 * k4 + 2]) + bb.z, __uint_as_float(r[4 * k4 + 3]) + bb.w);
+          }
+          const int w = col / hc, hh = (col - w * hc) / kD, d = col - w * hc - hh * kD;
+          __nv_bfloat16* dst = (w == 0 ? Q : (w == 1 ? K : V)) + (((size_t)b * H + hh) * N + n) * kD + d;
+          reinterpret_cast<uint4*>(dst)[0] = make_uint4(u[0], u[1], u[2], u[3]);
+          reinterpret_cast<uint4*>(dst)[1] = make_uint4(u[4], u[5], u[6], u[7]);
+        }
+      }
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, 256);
+  }
+}
+
 }  // namespace
 
 size_t proj_lt_workspace_bytes() { return (size_t)32 << 20; }
 
 gma_status_t proj_run(const gma_problem_t& p, int dm, const void* X, const void* W, const float* bias, float* Y,
-                      void* Q, void* K, void* V, void* lt_ws, cudaStream_t st) {
+                      void* Q, void* K, void* V, void* lt_ws, Ctrl* ctrl, cudaStream_t st) {
+  if (p.dtype == GMA_BF16) {
+    const int M = p.B * p.N, Ncol = 3 * p.H * kD;
+    CUtensorMap mx, mw;
+    if (!make_map_rows(&mx, X, (uint64_t)M, (uint64_t)dm, kPBK, kPBM) ||
+        !make_map_rows(&mw, W, (uint64_t)dm, (uint64_t)Ncol, 64, kPBK))
+      return GMA_ERR_CUDA;
+    if (set_smem_optin((const void*)proj_tc_kernel, (int)kPSmem, 5) != GMA_OK) return GMA_ERR_CUDA;
+    GMA_LAUNCH("proj_tc", proj_tc_kernel, dim3(cdiv(M, kPBM), cdiv(Ncol, kPBN)), kPThreads, kPSmem, st, mx, mw, bias, M,
+               Ncol, dm, p.H, p.N, (__nv_bfloat16*)Q, (__nv_bfloat16*)K, (__nv_bfloat16*)V, ctrl, wait_limit_ns());
+    return check_launch("launch proj_tc", (const void*)proj_tc_kernel);
+  }
+  (void)ctrl;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return cuda_fail("cudaGetDevice");
   const int M = p.B * p.N, Ncol = 3 * p.H * kD;

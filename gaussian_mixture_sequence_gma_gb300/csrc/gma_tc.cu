@@ -129,14 +129,15 @@ struct TcArgs {
 
 // ----------------------------------------------------------------------------------------------- prep
 // a1: fold (mu, sigma2, log_pi) of every head into the swizzled fp16 W image and the 256-entry c'
-// table (-inf past K); clear the error word; zero `zero_n` floats of the write accumulator.
+// table (-inf past K); clear the error word (unless clear_err is 0: an earlier kernel of the same call
+// cleared it and may have reported into it); zero `zero_n` floats of the write accumulator.
 // grid (256 / 8, H), 128 threads: 16 threads per component, thread q of a component builds the 16-byte
 // chunk of W elements 8q .. 8q+7 of that component's row (x^2 coefficients for q < 8, x coefficients
 // after) with one store, and the q < 8 threads sum c'_k over their 8 dims.
 __global__ void __launch_bounds__(128, 16) tc_prep_kernel(const float* __restrict__ mu, const float* __restrict__ sigma2,
                                                       const float* __restrict__ log_pi, int H, int K, int Kp,
                                                       uint8_t* w_img, float* cbias, Ctrl* ctrl, float* zero,
-                                                      size_t zero_n, uint32_t* range_flags) {
+                                                      size_t zero_n, uint32_t* range_flags, int clear_err) {
   // Launched as a dependent of whatever precedes it on the stream: nothing is read or written before that
   // grid has completed (it may produce the parameters, or still read the previous call's W image).  The
   // 32-register bound lets a CTA of this grid sit beside a running tensor-core CTA meanwhile.
@@ -205,7 +206,7 @@ __global__ void __launch_bounds__(128, 16) tc_prep_kernel(const float* __restric
     *reinterpret_cast<uint4*>(cimg + sw32_chunk(k, 0)) = make_uint4(*reinterpret_cast<const uint32_t*>(&hl), 0u, 0u, 0u);
     *reinterpret_cast<uint4*>(cimg + sw32_chunk(k, 1)) = make_uint4(0u, 0u, 0u, 0u);
   }
-  if (blockIdx.x == 0 && h == 0 && threadIdx.x == 0) {
+  if (clear_err && blockIdx.x == 0 && h == 0 && threadIdx.x == 0) {
     ctrl->err = kErrNone;
     ctrl->err_site = 0;
   }
@@ -1186,6 +1187,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           uint32_t* cur = (cc & 1) ? rb : ra;
           uint32_t* nxt = (cc & 1) ? ra : rb;
           tmem_ld_wait_tied32(cur);
+          if (wi == 0) GMA_TRACE_AT(10 + cc, t);
           if (cc + 1 < NC2 / 32) tmem_ld32(rg + lcol + 32 * (half == 0 ? c + 1 : c - 1), nxt);
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
@@ -1194,8 +1196,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             cur[e] = pack_bf16x2(ex2_approx(t0), ex2_approx(t1));
           }
           tmem_st16(rg + gcol0 + 16 * c, cur);
+          if (wi == 0) GMA_TRACE_AT(14 + cc, t);
         }
         tmem_st_wait();
+        if (wi == 0) GMA_TRACE_AT(18, t);
         tc_fence_before();
         warp_arrive(&B.g_full[g]);
       }
@@ -1809,6 +1813,33 @@ bool make_map(CUtensorMap* m, const void* base, int BH, int N, bool sw32 = false
   return r == CUDA_SUCCESS;
 }
 
+}  // namespace
+
+// Map over a row-major bf16 matrix [rows][cols] (row pitch cols * 2 bytes) as a 3-D tensor with a unit
+// outer dimension, boxes of box_cols x box_rows in the 128-byte swizzle, zero fill outside the matrix.
+bool make_map_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols,
+                   uint32_t box_rows) {
+  EncodeTiledFn f = encode_fn();
+  if (!f) {
+    set_error_detail("cuTensorMapEncodeTiled entry point unavailable");
+    return false;
+  }
+  cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, 1};
+  cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)cols * rows * 2};
+  cuuint32_t box[3] = {box_cols, box_rows, 1}, es[3] = {1, 1, 1};
+  const CUresult r = f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char msg[96];
+    snprintf(msg, sizeof msg, "cuTensorMapEncodeTiled returned CUresult %d", (int)r);
+    set_error_detail(msg);
+  }
+  return r == CUDA_SUCCESS;
+}
+
+namespace {
+
 // Dynamic shared memory of a launch: the layout plus alignment slack, never below 116 KB so that
 // exactly one CTA (which owns all 512 TMEM columns) is resident per SM.
 uint32_t smem_bytes(uint32_t layout_total) { return layout_total + 1024 > 116u * 1024 ? layout_total + 1024 : 116u * 1024; }
@@ -1911,7 +1942,7 @@ TcPlan tc_plan(const gma_problem_t& p, gma_op_t op) {
 
 gma_status_t tc_run(const gma_problem_t& p, gma_op_t op, int Nk, const void* Q, const void* K, const void* V,
                     const float* mu, const float* sigma2, const float* log_pi, void* out, void* ws,
-                    cudaStream_t st) {
+                    cudaStream_t st, bool clear_err) {
   const TcPlan pl = tc_plan(p, op);
   const int BH = p.B * p.H;
   char* base = (char*)ws;
@@ -1940,7 +1971,7 @@ gma_status_t tc_run(const gma_problem_t& p, gma_op_t op, int Nk, const void* Q, 
   const size_t zero_n = with_state ? (size_t)BH * pl.Kp * kStRow : 0;
   if (set_carveout_max((const void*)tc_prep_kernel) != GMA_OK) return GMA_ERR_CUDA;
   GMA_LAUNCH_DEPENDENT("tc_prep", tc_prep_kernel, dim3(kCTable / 8, p.H), 128, 0, st, mu, sigma2, log_pi, p.H, p.K, pl.Kp,
-             (uint8_t*)a.w_img, (float*)a.cbias, a.ctrl, a.state, zero_n, (uint32_t*)a.range_flags);
+             (uint8_t*)a.w_img, (float*)a.cbias, a.ctrl, a.state, zero_n, (uint32_t*)a.range_flags, clear_err ? 1 : 0);
   if (gma_status_t e = check_launch("launch tc_prep", (const void*)tc_prep_kernel)) return e;
   const int nc = pl.Kp <= 64 ? 16 : (pl.Kp <= 128 ? 32 : 64);  // components per row thread (4 per row)
   gma_status_t e = nc == 16   ? tc_launch<16>(p, op, Nk, pl, a, Q, K, V, ws, st)

@@ -279,12 +279,14 @@ GMA_API gma_status_t gma_backward_causal(const gma_problem_t *p, const void *Q, 
  *         the next H*64 give K, the last H*64 give V
  *   bqkv  [3 * H * 64] float32 bias, same column order
  *   O     [B, H, N, 64] in p->dtype (written)
- * The projection is one library GEMM (cuBLASLt, float32 accumulation and output) followed by one
- * kernel that adds the bias, rounds once to p->dtype and writes Q, K, V in the [B, H, N, 64] layout
- * inside the workspace; Q, K, V make one round trip through HBM (the forward kernels hold no room
- * for the 3 x dm-wide weight slices).  Workspace: gma_workspace_bytes(p, GMA_OP_PROJECTED_BIDIR or
- * GMA_OP_PROJECTED_CAUSAL); its first part is the forward's own workspace, so
- * gma_check_device_error(ws, ...) applies unchanged.
+ * bf16: the projection is one tcgen05 GEMM (float32 accumulation in tensor memory) whose epilogue
+ * adds the bias in float32, rounds once to bf16 and writes Q, K, V in the [B, H, N, 64] layout
+ * inside the workspace.  float32: one library GEMM (cuBLASLt, float32 accumulation and output)
+ * followed by one kernel doing the same.  Q, K, V make one round trip through HBM (the forward
+ * kernels hold no room for the 3 x dm-wide weight slices).  Workspace: gma_workspace_bytes(p,
+ * GMA_OP_PROJECTED_BIDIR or GMA_OP_PROJECTED_CAUSAL); its first part is the forward's own workspace,
+ * so gma_check_device_error(ws, ...) applies unchanged (it also reports the projection's bounded
+ * waits).
  */
 GMA_API gma_status_t gma_forward_projected(const gma_problem_t *p, int causal, int dm, const void *X,
                                            const void *Wqkv, const float *bqkv, const float *mu,

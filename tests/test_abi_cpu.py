@@ -239,8 +239,15 @@ def test_projected_argument_errors(L):
     for dt in (gma.GMA_F32, gma.GMA_BF16):
         for op, base in ((gma.OP_PROJECTED_BIDIR, gma.OP_BIDIR), (gma.OP_PROJECTED_CAUSAL, gma.OP_CAUSAL)):
             n = gma.workspace_bytes(P(dtype=dt), op)
-            # the forward's own workspace, the GEMM's, Y float32 [B*N][3*H*64] and Q, K, V
-            assert n % 256 == 0 and n > gma.workspace_bytes(P(dtype=dt), base) + 32 * (1 << 20) + 256 * 384 * 4
+            pr = P(dtype=dt)
+            qkv = 3 * (-(-pr.B * pr.H * pr.N * 64 * (2 if dt == gma.GMA_BF16 else 4) // 256) * 256)
+            fwd = -(-gma.workspace_bytes(pr, base) // 256) * 256
+            if dt == gma.GMA_BF16:
+                # the forward's own workspace and Q, K, V (the tcgen05 projection keeps no float32 Y)
+                assert n == fwd + qkv
+            else:
+                # the forward's own workspace, the library GEMM's, Y float32 [B*N][3*H*64] and Q, K, V
+                assert n % 256 == 0 and n > fwd + 32 * (1 << 20) + 256 * 384 * 4 + qkv - 256
     ptr = [A + i * (1 << 16) for i in range(10)]
 
     def proj(prob, causal=1, dm=128, p=ptr, ws_bytes=1 << 34):  # X W b mu s2 lp O ws
