@@ -77,24 +77,28 @@ __global__ void __launch_bounds__(256) proj_layout_kernel(const float* __restric
 }
 
 // ---- bf16: one hand-written tcgen05 GEMM with the bias, the rounding and the layout in its epilogue ----
-// Y [M = B*N][Ncol] = X [M][dm] Wqkv [dm][Ncol] in 128 x 256 tiles, one tile per CTA, two CTAs per SM (each
-// holds 97 KB of shared memory and 256 TMEM columns, so one CTA's epilogue overlaps the other's
-// contractions).  A = X tile (K-major, 128-byte swizzle); B = Wqkv tile read as an MN-major operand: four
-// 64-column boxes of 64 rows, 8 KB apart.  The K loop runs over 64-wide blocks of dm in a two-stage TMA
-// ring (zero fill past dm, M and Ncol).  Warp 0 loads, one thread of warp 1 issues the contractions (and
-// warp 1 owns the TMEM columns), warps 2-5 take a lane quarter of the accumulator each: 16 columns at a
-// time, + bias in float32, rounded once to bf16, stored straight into Q, K or V [B][H][N][64].
-constexpr int kPBM = 128, kPBN = 256, kPBK = 64, kPStages = 2, kPThreads = 192;
+// Y [M = B*N][Ncol] = X [M][dm] Wqkv [dm][Ncol] in 256 x 256 tiles, one tile per CTA, one CTA per SM.  The
+// tile is two 128-row halves with their own accumulators (all 512 TMEM columns) that share every Wqkv
+// stage, so each stage of Wqkv is read from L2 once per 256 rows of X: the operands of this GEMM are
+// re-read by every tile, and L2-to-SM traffic, not the tensor pipe, bounds it at smaller tiles.
+// A = X rows (K-major, 128-byte swizzle, two 128-row boxes); B = Wqkv read as an MN-major operand: four
+// 64-column boxes of 64 rows, 8 KB apart.  The K loop runs over 64-wide blocks of dm in a three-stage
+// TMA ring (zero fill past dm, M and Ncol).  Warp 0 loads; one thread of warp 1 (rows 0-127) and one of
+// warp 2 (rows 128-255) issue the contractions of their half (a thread issuing tcgen05.mma waits about
+// as long as the instruction runs, so one issuer would bound the tile); warp 1 owns the TMEM columns.
+// Warps 4-11 each take one lane quarter of one half: 16 columns at a time, + bias in float32, rounded
+// once to bf16, stored straight into Q, K or V [B][H][N][64].
+constexpr int kPBM = 256, kPBN = 256, kPBK = 64, kPStages = 3, kPThreads = 384;
 constexpr uint32_t kPStageA = kPBM * kPBK * 2, kPStageB = kPBN * kPBK * 2, kPStage = kPStageA + kPStageB;
 constexpr uint32_t kPSmem = kPStages * kPStage + 1024;  // + 1 KB alignment slack
 
 struct ProjBars {
-  uint64_t full[kPStages], empty[kPStages], acc;
+  uint64_t full[kPStages], empty[kPStages], acc[2];
   uint32_t tmem;
   tc::Abort ab;
 };
 
-__global__ void __launch_bounds__(kPThreads, 2)
+__global__ void __launch_bounds__(kPThreads, 1)
     proj_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                    const float* __restrict__ bias, int M, int Ncol, int dm, int H, int N, __nv_bfloat16* __restrict__ Q,
                    __nv_bfloat16* __restrict__ K, __nv_bfloat16* __restrict__ V, Ctrl* ctrl, uint64_t wait_ns) {
@@ -112,14 +116,15 @@ __global__ void __launch_bounds__(kPThreads, 2)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kPStages; ++s) {
       tc::mbar_init(&B.full[s], 1);
-      tc::mbar_init(&B.empty[s], 1);
+      tc::mbar_init(&B.empty[s], 2);  // both issuers read every stage
     }
-    tc::mbar_init(&B.acc, 1);
+    tc::mbar_init(&B.acc[0], 1);
+    tc::mbar_init(&B.acc[1], 1);
     B.ab.flag = 0;
     tc::mbar_fence_init();
   }
   if (warp == 1) {
-    tc::tmem_alloc(&B.tmem, 256);
+    tc::tmem_alloc(&B.tmem, 512);
     tc::tmem_relinquish();
   }
   tc::tc_fence_before();
@@ -134,11 +139,12 @@ __global__ void __launch_bounds__(kPThreads, 2)
       for (int kb = 0; kb < KB; ++kb) {
         const int s = kb % kPStages;
         const uint32_t ph = (uint32_t)(kb / kPStages) & 1u;
-        // the slot is free once the contractions of its previous block have read it
+        // the slot is free once both halves' contractions of its previous block have read it
         if (kb >= kPStages && !tc::wait_bounded(&B.empty[s], ph ^ 1u, &B.ab, ctrl, 130, wait_ns)) break;
         tc::mbar_expect_tx(&B.full[s], kPStage);
         uint8_t* st = smem + (size_t)s * kPStage;
         tc::tma_load_3d(st, &tmX, kPBK * kb, m0, 0, &B.full[s]);
+        tc::tma_load_3d(st + kPStageA / 2, &tmX, kPBK * kb, m0 + kPBM / 2, 0, &B.full[s]);
 #pragma unroll
         for (int i = 0; i < kPBN / 64; ++i)
           tc::tma_load_3d(st + kPStageA + 8192 * i, &tmW, n0 + 64 * i, kPBK * kb, 0, &B.full[s]);
@@ -149,30 +155,32 @@ __global__ void __launch_bounds__(kPThreads, 2)
       for (int s = 0; s < kPStages; ++s)
         if (last[s] >= 0) tc::wait_bounded(&B.full[s], (uint32_t)last[s], &none, ctrl, 131, wait_ns);
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == 2) {
     if (lane == 0) {
-      constexpr uint32_t idesc = tc::make_idesc(kPBM, kPBN, 1, 1, 0, 1);  // bf16 x bf16, A K-major, B MN-major
+      const int hf = warp - 1;  // row half: rows 128 hf .. 128 hf + 127, accumulator columns 256 hf ..
+      constexpr uint32_t idesc = tc::make_idesc(128, kPBN, 1, 1, 0, 1);  // bf16 x bf16, A K-major, B MN-major
       bool ok = true;
       for (int kb = 0; kb < KB; ++kb) {
         const int s = kb % kPStages;
         if (!(ok = tc::wait_bounded(&B.full[s], (uint32_t)(kb / kPStages) & 1u, &B.ab, ctrl, 132, wait_ns))) break;
         tc::tc_fence_after();
         const uint32_t a = sa + (uint32_t)s * kPStage;
-        const uint64_t da = tc::make_sdesc(a, 16, 1024), db = tc::make_sdesc(a + kPStageA, 8192, 1024);
+        const uint64_t da = tc::make_sdesc(a + (uint32_t)hf * (kPStageA / 2), 16, 1024);
+        const uint64_t db = tc::make_sdesc(a + kPStageA, 8192, 1024);
 #pragma unroll
         for (int ks = 0; ks < kPBK / 16; ++ks)
-          tc::mma_ss_off(tmem, da, (uint32_t)(32 * ks) >> 4, db, (uint32_t)(2048 * ks) >> 4, idesc,
-                         (kb > 0 || ks > 0) ? 1u : 0u);
+          tc::mma_ss_off(tmem + 256u * (uint32_t)hf, da, (uint32_t)(32 * ks) >> 4, db, (uint32_t)(2048 * ks) >> 4,
+                         idesc, (kb > 0 || ks > 0) ? 1u : 0u);
         tc::mma_commit(&B.empty[s]);
       }
-      tc::mma_commit(&B.acc);
+      tc::mma_commit(&B.acc[hf]);
       tc::Abort none{0};
-      tc::wait_bounded(&B.acc, 0, &none, ctrl, 133, wait_ns);  // the contractions are done before TMEM is freed
+      tc::wait_bounded(&B.acc[hf], 0, &none, ctrl, 133, wait_ns);  // contractions done before TMEM is freed
     }
-  } else {
-    // epilogue: warp w reads TMEM lane quarter w % 4, token row m0 + 32 (w % 4) + lane
-    const int q = warp & 3, m = m0 + 32 * q + lane;
-    const bool ok = tc::warp_wait(&B.acc, 0, &B.ab, ctrl, 134, wait_ns);
+  } else if (warp >= 4) {
+    // epilogue: warp w reads TMEM lane quarter w % 4 of half (w - 4) / 4: token row m0 + 128 half + 32 q + lane
+    const int q = warp & 3, hf = (warp - 4) >> 2, m = m0 + 128 * hf + 32 * q + lane;
+    const bool ok = tc::warp_wait(&B.acc[hf], 0, &B.ab, ctrl, 134, wait_ns);
     if (ok) {
       tc::tc_fence_after();
       const int b = m / N, n = m - (m / N) * N;
@@ -180,7 +188,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
 #pragma unroll 2
       for (int c = 0; c < kPBN / 16; ++c) {
         uint32_t r[16];
-        tc::tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + 16 * c, r);
+        tc::tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + 256u * (uint32_t)hf + 16 * c, r);
         tc::tmem_ld_wait_tied16(r);
         const int col = n0 + 16 * c;
         if (col < Ncol && m < M) {
@@ -204,7 +212,7 @@ __global__ void __launch_bounds__(kPThreads, 2)
   __syncthreads();
   if (warp == 1) {
     tc::tc_fence_after();
-    tc::tmem_dealloc(tmem, 256);
+    tc::tmem_dealloc(tmem, 512);
   }
 }
 
@@ -217,7 +225,7 @@ gma_status_t proj_run(const gma_problem_t& p, int dm, const void* X, const void*
   if (p.dtype == GMA_BF16) {
     const int M = p.B * p.N, Ncol = 3 * p.H * kD;
     CUtensorMap mx, mw;
-    if (!make_map_rows(&mx, X, (uint64_t)M, (uint64_t)dm, kPBK, kPBM) ||
+    if (!make_map_rows(&mx, X, (uint64_t)M, (uint64_t)dm, kPBK, kPBM / 2) ||
         !make_map_rows(&mw, W, (uint64_t)dm, (uint64_t)Ncol, 64, kPBK))
       return GMA_ERR_CUDA;
     if (set_smem_optin((const void*)proj_tc_kernel, (int)kPSmem, 5) != GMA_OK) return GMA_ERR_CUDA;
