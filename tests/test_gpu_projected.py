@@ -77,3 +77,12 @@ def test_projected_equals_forward_on_its_projection(gma):
     O2 = gma.forward_causal(qkv[0], qkv[1], qkv[2], t["mu"], t["sigma2"], t["log_pi"])
     # torch's GEMM may round a few projected values differently from cuBLASLt's: compare with the bar
     assert rel_err(O1.float().cpu().numpy(), O2.float().cpu().numpy()) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("B,H,N,dm", [(1, 1, 5, 8), (3, 1, 129, 1000), (1, 3, 257, 40)])
+def test_projected_edge_shapes_bf16(gma, B, H, N, dm):
+    """Edges of the bf16 projection GEMM's tiling: dm below one K block (8) and far above it with a tail
+    (1000), one head (192 output columns, a partial column tile), row counts that are not multiples of
+    the 256-row tile and tiles that cross a batch boundary."""
+    inp = make_projected_inputs(B, H, N, 16, dm=dm, dtype="bf16", seed=90 + dm)
+    check(gma, inp, True)
