@@ -4,24 +4,25 @@
 // Method (Gaussian Mixture Attention pages, gist.science summaries):
 //   "Core mechanism" item 1: gamma_ik = softmax_k(log pi_k + log N(x_i; mu_k, diag sigma2_k)).
 //     The log-density is expanded into one dense contraction per 128-token tile,
-//       L'_ik = [x_i^2 , x_i] . [-1/2 sigma2_k^-1 ; mu_k sigma2_k^-1] * log2(e)      (fp16 operands)
-//     plus the per-component constant c'_k = (log pi_k - 1/2 sum_d (mu^2/sigma2 + log sigma2)) log2(e)
-//     added in float32, followed by a base-2 softmax over k held in registers.
+//       L'_ik = [x_i^2 , x_i , 1] . [a_k ; b_k ; c'_k]                                   (fp16 operands)
+//     with a = -1/2 sigma2^-1 log2(e) and b = -2 a mu rounded consistently (the expanded form is then
+//     exactly a (x - mu')^2 for a mean within 2^-12 |mu| of mu) and the component constant
+//     c'_k = (log pi_k - 1/2 sum_d log sigma2) log2(e) + sum_d a mu'^2 as one extra K-step (fp16 hi / lo
+//     parts of c'/256 against a constant [256 | 1] block; the causal sweep adds it from a float32 table
+//     instead), followed by a base-2 softmax over k held in registers.
 //   "Core mechanism" item 2: write  [Vt | Z] = Gamma_K^T [V | 1]   (bf16 operands, fp32 TMEM accumulator)
 //                            read   O = Gamma_Q Vt / (Gamma_Q Z + eps)
-//   Bidirectional write: Gamma_K is stored unnormalised (row maximum 1) and each key's row is normalised
-//   inside the contraction by scaling its [V | 1] row by 1/s_j (s_j = row sum of the exponentials);
-//   causal aggregates: the bf16 Gamma_K rows are scaled by 1/s_j themselves and kept in HBM for the
-//   chunked sweep, which uses them with V as loaded and a constant 1 column.  Gamma_Q stays
-//   unnormalised as well: the read divides by gamma~_i . (Z + eps) = gamma~_i . Z + eps s_i, which is the
-//   same quotient, with eps added once to the Z column of the state operand, so no query row needs
-//   its sum.
+//   Keys are normalised before packing (bf16 gamma = e / s_j, 0 past N) and used with [V | 1] as loaded
+//   and a constant 1 column, in the bidirectional write, the causal aggregates and the chunked sweep.
+//   Gamma_Q stays unnormalised: the read divides by gamma~_i . (Z + eps) = gamma~_i . Z + eps s_i, which
+//   is the same quotient, with eps added once to the Z column of the state operand, so no query row
+//   needs its sum.  No responsibility goes to global memory except through the responsibilities entry.
 //
-// Roles per CTA (640 threads = 5 warpgroups): warp 0 = TMA producer, warp 1 = MMA issuer (one thread)
-// and TMEM owner, warps 2-3 = helpers (causal aggregates: the Gamma_K store; causal sweep: the query
-// operand) or idle; warpgroups 1-4 (warps 4..19) = row warps: thread (q, part) owns token
+// Roles per CTA (640 threads): warps 0-3 are control warps (TMA producer; one MMA-issuing thread per
+// independent contraction, since a thread issuing tcgen05.mma waits about as long as the instruction
+// runs; warp 1 also owns the TMEM columns), warps 4..19 are row warps: thread (q, part) owns token
 // row 32q+lane of the tile and a quarter of its components / dimensions (TMEM lane quarter q = warp % 4,
-// part = warpgroup - 1).  The control warpgroup hands registers to the row warpgroups with setmaxnreg.
+// part = warpgroup - 1).  The control warps hand registers to the row warps with setmaxnreg.
 #include <algorithm>
 #include <cstdio>
 #include <mutex>
@@ -29,11 +30,6 @@
 #include "gma_tc_common.cuh"
 #include "gma_trace.cuh"
 
-#ifdef GMA_WAIT_NOBO
-#define WAITC wait_bounded
-#else
-#define WAITC wait_bounded_bo
-#endif
 
 namespace gma {
 namespace {
@@ -609,7 +605,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       }
     } else if (warp - 2 < MB) {
       if (lane == 0) {
-        // issuers 2 / 3: component block mb = warp - 2 of the write contraction, Gamma~_K^T [V/s | 1/s]
+        // issuers 2 / 3: component block mb = warp - 2 of the write contraction, Gamma_K^T [V | 1]
         const int mb = warp - 2;
         const uint32_t idw = make_idesc(128, kStCols, 1, 1, 1, 1);
         const uint32_t g_addr = smem_u32(smem + L.g) + (uint32_t)mb * 32768u;
@@ -1394,36 +1390,36 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const uint32_t pe = (t & 1) ^ 1;
         const int row0 = (tile0 + t) * kTile;
         // each X slot once the row warps have built the previous tile's operand from it
-        if (!WAITC(&B.xk_empty, pe, &B.ab, a.ctrl, 70, a.wait_ns)) break;
+        if (!wait_bounded_bo(&B.xk_empty, pe, &B.ab, a.ctrl, 70, a.wait_ns)) break;
         mbar_expect_tx(&B.xk_full, 16384);
         tma_load_3d(smem + L.xk, &tmK, 0, row0, bh, &B.xk_full);
         issued[0] = t & 1;
-        if (!WAITC(&B.xq_empty, pe, &B.ab, a.ctrl, 71, a.wait_ns)) break;
+        if (!wait_bounded_bo(&B.xq_empty, pe, &B.ab, a.ctrl, 71, a.wait_ns)) break;
         mbar_expect_tx(&B.xq_full, 16384);
         tma_load_3d(smem + L.xq, &tmQ, 0, row0, bh, &B.xq_full);
         issued[1] = t & 1;
-        if (!WAITC(&B.v_empty, pe, &B.ab, a.ctrl, 72, a.wait_ns)) break;
+        if (!wait_bounded_bo(&B.v_empty, pe, &B.ab, a.ctrl, 72, a.wait_ns)) break;
         mbar_expect_tx(&B.v_full, 16384);
         for (int a4 = 0; a4 < 4; ++a4) tma_load_3d(smem + L.v + 4096 * a4, &tmV, 16 * a4, row0, bh, &B.v_full);
         issued[2] = t & 1;
       }
       // never leave with copies in flight
       Abort none{0};
-      if (issued[0] >= 0) WAITC(&B.xk_full, (uint32_t)issued[0], &none, a.ctrl, 73, a.wait_ns);
-      if (issued[1] >= 0) WAITC(&B.xq_full, (uint32_t)issued[1], &none, a.ctrl, 74, a.wait_ns);
-      if (issued[2] >= 0) WAITC(&B.v_full, (uint32_t)issued[2], &none, a.ctrl, 75, a.wait_ns);
+      if (issued[0] >= 0) wait_bounded_bo(&B.xk_full, (uint32_t)issued[0], &none, a.ctrl, 73, a.wait_ns);
+      if (issued[1] >= 0) wait_bounded_bo(&B.xq_full, (uint32_t)issued[1], &none, a.ctrl, 74, a.wait_ns);
+      if (issued[2] >= 0) wait_bounded_bo(&B.v_full, (uint32_t)issued[2], &none, a.ctrl, 75, a.wait_ns);
     } else if (warp == 1 && lane == 0) {
       // ---------------------------------------------------------------- issuer 1: logits, state update
       const uint64_t d_w = make_sdesc(smem_u32(smem + L.w), 16, 1024);
       const uint64_t d_vb = make_sdesc32(smem_u32(smem + L.v), 4096, 256);          // [V | 1], N = 80
       const uint64_t d_gk_mn = make_sdesc(smem_u32(smem + L.gk), 16384, 1024);     // Gamma_K^T as MN-major A
       constexpr uint32_t id_s80 = make_idesc(128, kStCols, 1, 1, 1, 1);
-      bool ok = WAITC(&B.w_full, 0, &B.ab, a.ctrl, 80, a.wait_ns);
+      bool ok = wait_bounded_bo(&B.w_full, 0, &B.ab, a.ctrl, 80, a.wait_ns);
       for (int t = 0; ok && t < T; ++t) {
         const uint32_t ph = t & 1;
         // key logits: the key operand is in OX and L is free (the row warps have taken the previous
         // tile's output, which follows P [V | 1])
-        if (!(ok = WAITC(&B.ax_full, 0, &B.ab, a.ctrl, 81, a.wait_ns))) break;
+        if (!(ok = wait_bounded_bo(&B.ax_full, 0, &B.ab, a.ctrl, 81, a.wait_ns))) break;
         GMA_TRACE_AT(20, t);
         tc_fence_after();
         issue_logits(tmem, d_w, a.Kp, kCColO);
@@ -1434,7 +1430,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         GMA_TRACE_AT(26, t);
 #endif
         // query logits: the row warps have loaded the key logits and put the query operand in OX
-        if (!(ok = WAITC(&B.ax_full, 1, &B.ab, a.ctrl, 82, a.wait_ns))) break;
+        if (!(ok = wait_bounded_bo(&B.ax_full, 1, &B.ab, a.ctrl, 82, a.wait_ns))) break;
         GMA_TRACE_AT(22, t);
         tc_fence_after();
         issue_logits(tmem, d_w, a.Kp, kCColO);
@@ -1445,9 +1441,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         GMA_TRACE_AT(27, t);
 #endif
         // S += Gamma_K^T [V | 1] once Gamma_K and V are in and the snapshot of the previous S is taken
-        if (!(ok = WAITC(&B.gk_full, ph, &B.ab, a.ctrl, 83, a.wait_ns) &&
-                   WAITC(&B.v_full, ph, &B.ab, a.ctrl, 84, a.wait_ns) &&
-                   WAITC(&B.sb_full, ph, &B.ab, a.ctrl, 85, a.wait_ns)))
+        if (!(ok = wait_bounded_bo(&B.gk_full, ph, &B.ab, a.ctrl, 83, a.wait_ns) &&
+                   wait_bounded_bo(&B.v_full, ph, &B.ab, a.ctrl, 84, a.wait_ns) &&
+                   wait_bounded_bo(&B.sb_full, ph, &B.ab, a.ctrl, 85, a.wait_ns)))
           break;
         GMA_TRACE_AT(24, t);
         tc_fence_after();
@@ -1467,7 +1463,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       }
       mma_commit(&B.done[0]);
       Abort none{0};
-      WAITC(&B.done[0], 0, &none, a.ctrl, 86, a.wait_ns);
+      wait_bounded_bo(&B.done[0], 0, &none, a.ctrl, 86, a.wait_ns);
     } else if (warp == 2 && lane == 0) {
       // ---------------------------------------------------------------- issuer 2: O = Gq~ S_prev, O += P [V | 1]
       const uint64_t d_sb = make_sdesc32(smem_u32(smem + L.sbv), (uint32_t)a.Kp * 32, 256);
@@ -1476,8 +1472,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       bool ok = true;
       for (int t = 0; ok && t < T; ++t) {
         const uint32_t ph = t & 1;
-        if (!(ok = WAITC(&B.gq_full, ph, &B.ab, a.ctrl, 87, a.wait_ns) &&
-                   WAITC(&B.sb_full, ph, &B.ab, a.ctrl, 88, a.wait_ns)))
+        if (!(ok = wait_bounded_bo(&B.gq_full, ph, &B.ab, a.ctrl, 87, a.wait_ns) &&
+                   wait_bounded_bo(&B.sb_full, ph, &B.ab, a.ctrl, 88, a.wait_ns)))
           break;
         GMA_TRACE_AT(30, t);
         tc_fence_after();
@@ -1488,8 +1484,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           mma_ts_off(tmem + kCColO, tmem + kColLog + 8 * ks, d_sb, (uint32_t)(512 * ks) >> 4, id_c80, ks > 0);
         mma_commit(&B.p_full);
         GMA_TRACE_AT(31, t);
-        if (!(ok = WAITC(&B.pb_full, ph, &B.ab, a.ctrl, 89, a.wait_ns) &&
-                   WAITC(&B.v_full, ph, &B.ab, a.ctrl, 95, a.wait_ns)))
+        if (!(ok = wait_bounded_bo(&B.pb_full, ph, &B.ab, a.ctrl, 89, a.wait_ns) &&
+                   wait_bounded_bo(&B.v_full, ph, &B.ab, a.ctrl, 95, a.wait_ns)))
           break;
         GMA_TRACE_AT(32, t);
         tc_fence_after();
@@ -1504,7 +1500,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       }
       mma_commit(&B.done[1]);
       Abort none{0};
-      WAITC(&B.done[1], 0, &none, a.ctrl, 90, a.wait_ns);
+      wait_bounded_bo(&B.done[1], 0, &none, a.ctrl, 90, a.wait_ns);
     } else if (warp == 3 && lane == 0) {
       // ---------------------------------------------------------------- issuer 3: P = Gq~ Gk^T
       const uint64_t d_gk_k = make_sdesc(smem_u32(smem + L.gk), 16, 1024);  // Gamma_K as K-major B
@@ -1512,8 +1508,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       bool ok = true;
       for (int t = 0; ok && t < T; ++t) {
         const uint32_t ph = t & 1;
-        if (!(ok = WAITC(&B.gq_full, ph, &B.ab, a.ctrl, 91, a.wait_ns) &&
-                   WAITC(&B.gk_full, ph, &B.ab, a.ctrl, 92, a.wait_ns)))
+        if (!(ok = wait_bounded_bo(&B.gq_full, ph, &B.ab, a.ctrl, 91, a.wait_ns) &&
+                   wait_bounded_bo(&B.gk_full, ph, &B.ab, a.ctrl, 92, a.wait_ns)))
           break;
         GMA_TRACE_AT(40, t);
         tc_fence_after();
@@ -1526,7 +1522,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         GMA_TRACE_AT(41, t);
         // the row warps stage the normalised bf16 output tile in the (then unused) first Gamma_K block;
         // one tensor store writes it (rows past N clipped), then the block is handed back
-        if (!(ok = WAITC(&B.o_staged, ph, &B.ab, a.ctrl, 94, a.wait_ns))) break;
+        if (!(ok = wait_bounded_bo(&B.o_staged, ph, &B.ab, a.ctrl, 94, a.wait_ns))) break;
         tma_store_3d(&tmO, smem_u32(smem + L.gk), 0, (tile0 + t) * kTile, bh);
         bulk_commit();
         bulk_wait_read_all();
@@ -1535,7 +1531,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       bulk_wait_all();
       mma_commit(&B.done[2]);
       Abort none{0};
-      WAITC(&B.done[2], 0, &none, a.ctrl, 93, a.wait_ns);
+      wait_bounded_bo(&B.done[2], 0, &none, a.ctrl, 93, a.wait_ns);
     }
   } else {
     setmaxnreg_inc<kRowRegsC>();

@@ -51,15 +51,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
@@ -103,12 +94,8 @@ __device__ __forceinline__ bool wait_bounded_bo(uint64_t* bar, uint32_t parity, 
   if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = 0;
   for (uint32_t i = 1;; ++i) {
-#ifdef GMA_WAIT_POLL
-    if (mbar_test_wait(bar, parity)) return true;
-#else
     if (mbar_try_wait(bar, parity)) return true;
     if (i >= GMA_WAIT_SPIN) __nanosleep(GMA_WAIT_SLEEP_NS);
-#endif
     if ((i & 15) == 0) {
       if (ab->flag) return false;
       const uint64_t now = global_timer_ns();
