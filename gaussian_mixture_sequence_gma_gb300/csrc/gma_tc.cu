@@ -1840,10 +1840,28 @@ namespace {
 // exactly one CTA (which owns all 512 TMEM columns) is resident per SM.
 uint32_t smem_bytes(uint32_t layout_total) { return layout_total + 1024 > 116u * 1024 ? layout_total + 1024 : 116u * 1024; }
 
+// Segments per head row.  Each CTA walks one segment of seg = ceil(tiles / s) tiles and owns an SM, so
+// a launch of BH * s CTAs runs in ceil(BH * s / 152) waves of seg tiles.  Over the largest s that fits
+// in w = 1 .. 8 waves, the count minimises waves * (seg + 1), the 1 standing for a CTA's fixed cost
+// (set-up and epilogue); ties go to fewer segments.  At most 8 * 152 segments (or B*H, if larger) are
+// used, so the causal aggregates stay independent of N.
 int split_for(int BH, int tiles) {
-  int s = cdiv(kTargetCtas, BH);
-  if (s > tiles) s = tiles;
-  return s < 1 ? 1 : s;
+  if (BH < 1 || tiles < 1) return 1;
+  int best = 1;
+  long long best_cost = -1;
+  for (int w = 1; w <= 8; ++w) {
+    const long long fit = (long long)w * kTargetCtas / BH;
+    const int s = (int)std::max(1LL, std::min<long long>(fit, tiles));
+    const int seg = cdiv(tiles, s);
+    const int splits = cdiv(tiles, seg);
+    const long long ctas = (long long)BH * splits;
+    const long long cost = ((ctas + kTargetCtas - 1) / kTargetCtas) * (seg + 1);
+    if (best_cost < 0 || cost < best_cost || (cost == best_cost && splits < best)) {
+      best_cost = cost;
+      best = splits;
+    }
+  }
+  return best;
 }
 
 // Launches the per-tile kernels with NC components per row thread (2 * NC >= Kp).
