@@ -168,7 +168,8 @@ GMA_API gma_status_t gma_static_ws_check_error(void *stream);
  * Passage: gist.science summary, "Variants and training" item 3 (prefix sums
  * of the latent memory and normaliser; O at position i depends on j <= i only).
  * Same arguments and layouts as gma_forward_bidir.  The workspace does not grow with N: it holds
- * the per-segment prefix states (at most 152 segments over all B*H rows at bf16 I/O); no per-position
+ * the per-segment prefix states (at bf16 I/O at most 8 x 152 segments over all B*H rows, or B*H
+ * segments if B*H is larger); no per-position
  * responsibilities are stored.  With bf16 I/O the key responsibilities are computed twice -- once for
  * the segment sums, once inside the chunked sweep -- and never leave the chip.
  */
