@@ -159,10 +159,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
     if (lane == 0) {
       const int hf = warp - 1;  // row half: rows 128 hf .. 128 hf + 127, accumulator columns 256 hf ..
       constexpr uint32_t idesc = tc::make_idesc(128, kPBN, 1, 1, 0, 1);  // bf16 x bf16, A K-major, B MN-major
-      bool ok = true;
       for (int kb = 0; kb < KB; ++kb) {
         const int s = kb % kPStages;
-        if (!(ok = tc::wait_bounded(&B.full[s], (uint32_t)(kb / kPStages) & 1u, &B.ab, ctrl, 132, wait_ns))) break;
+        if (!tc::wait_bounded(&B.full[s], (uint32_t)(kb / kPStages) & 1u, &B.ab, ctrl, 132, wait_ns)) break;
         tc::tc_fence_after();
         const uint32_t a = sa + (uint32_t)s * kPStage;
         const uint64_t da = tc::make_sdesc(a + (uint32_t)hf * (kPStageA / 2), 16, 1024);

@@ -283,6 +283,27 @@ __device__ __forceinline__ void transform_row(uint32_t xtile, const RowCtx& rc, 
   tmem_st8(tmem + rc.lane_base + col_ax + 32 + 8 * rc.part, lin);
 }
 
+// The same quarter of the operand row into shared memory at `adst` (1 KB aligned): the x^2 block, then
+// the x block 16 KB on, each 128 rows of 64 fp16 in the 128-byte swizzle of the X tile, so a chunk keeps
+// its position (K-major A of the log-density contraction).
+__device__ __forceinline__ void transform_row_smem(uint32_t xtile, const RowCtx& rc, uint32_t adst) {
+#pragma unroll
+  for (int jj = 0; jj < 2; ++jj) {
+    const uint32_t off = rc.rowq ^ (uint32_t)(jj << 4);
+    const uint4 v = lds128(xtile + off);
+    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+    uint32_t sq[4], lin[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float lo = __uint_as_float(w4[i] << 16), hi = __uint_as_float(w4[i] & 0xffff0000u);
+      lin[i] = pack_f16x2(lo, hi);
+      sq[i] = pack_f16x2(lo * lo, hi * hi);
+    }
+    sts128(adst + off, make_uint4(sq[0], sq[1], sq[2], sq[3]));
+    sts128(adst + 16384u + off, make_uint4(lin[0], lin[1], lin[2], lin[3]));
+  }
+}
+
 // Zeroes this thread's logit columns at or beyond Kp once per CTA: the contraction (N = Kp) never
 // writes them, and with c'_k = -inf there they then read as -inf without any per-element masking.
 template <int NC>
@@ -481,6 +502,15 @@ __device__ __forceinline__ void issue_logits(uint32_t tmem, uint64_t d_w, int Kp
   for (int ks = 0; ks < 8; ++ks)
     mma_ts_off(tmem + kColLog, tmem + col_ax + 8 * ks, d_w, (ks >> 2) * (uint32_t)Kp * 8 + (ks & 3) * 2, idesc,
                ks > 0 ? 1u : 0u);
+}
+// The same with the [x^2 | x] operand in shared memory (d_a: K-major, 128-byte swizzle, the x block 16 KB
+// after the x^2 block).
+__device__ __forceinline__ void issue_logits_ss(uint32_t tmem, uint64_t d_a, uint64_t d_w, int Kp) {
+  const uint32_t idesc = make_idesc(128, Kp, 0, 0, 0, 0);
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks)
+    mma_ss_off(tmem + kColLog, d_a, (uint32_t)((ks >> 2) * 16384 + (ks & 3) * 32) >> 4, d_w,
+               (ks >> 2) * (uint32_t)Kp * 8 + (ks & 3) * 2, idesc, ks > 0 ? 1u : 0u);
 }
 // The same plus the constant step (A = the [256 | 1] columns at kColOnes, B = the 32-byte-swizzled c' image
 // d_c), so the logits come out with c'_k added.
@@ -1248,16 +1278,19 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 //
 // TMEM: L (columns 0..255) holds, in turn, the key logits, the query logits, then Gamma~_Q (bf16 pairs,
 // columns 0..127) beside P = Gamma~_Q Gamma_K^T (columns 128..255); S (256..415); OX (416..495) holds
-// the [x^2 | x] operand of the key logits, then that of the query logits, then the output accumulator.
+// the [x^2 | x] operand of the query logits, then the output accumulator.  The key logits read their
+// operand from shared memory: the row warps build tile t+1's, and snapshot the state for its inter-tile
+// term, while P [V | 1] of tile t runs, and its key logits start as soon as that contraction is done,
+// so they overlap tile t's output instead of opening tile t+1.
 // Three MMA issuers run side by side (each issuing thread waits about 100 cycles per instruction, so
 // the N = 80 / 128 contractions reach the tensor pipe's rate only when several threads issue):
 // warp 1 the logits and the state update, warp 2 the inter-tile term and P [V | 1], warp 3 P.
 constexpr uint32_t kCColP = 128;   // P (fp32 128 columns; bf16 pairs in its first 64 after masking)
 constexpr uint32_t kCColS = 256;   // state accumulators, 80 columns per 128-component block
-constexpr uint32_t kCColO = 416;   // logit operands, then the output accumulator (80 columns)
+constexpr uint32_t kCColO = 416;   // query logit operand, then the output accumulator (80 columns)
 
 struct CausalLayout {
-  uint32_t w, gk, xk, xq, v, sbv, sbz, c, red, total;
+  uint32_t w, gk, xk, xq, v, sbv, sbz, c, red, ak, total;
 };
 __host__ __device__ inline CausalLayout causal_layout(int Kp) {
   CausalLayout s{};
@@ -1279,12 +1312,22 @@ __host__ __device__ inline CausalLayout causal_layout(int Kp) {
   s.c = s.sbz + Kp * 32;
   s.red = s.c + 1024;
   s.total = s.red + kParts * kTile * 8;
+  // the [x^2 | x] fp16 operand of the key logits (K-major, 128-byte swizzle: the x^2 block, then the x
+  // block 16 KB on), built while the previous tile's P [V | 1] runs.  At Kp = 256 it takes Gamma_K
+  // blocks 2 and 3, free from the moment P and the state update have read them until the key softmax
+  // stores the next Gamma_K (after the key logits have read the operand); below, a region of its own.
+  if (MB >= 2) {
+    s.ak = s.gk + 32768;
+  } else {
+    s.ak = align1k(s.total);
+    s.total = s.ak + 32768;
+  }
   return s;
 }
 
 struct CBars {
   uint64_t w_full, xk_full, xk_empty, xq_full, xq_empty, v_full, v_empty;
-  uint64_t ax_full, lk_full, lq_full, gk_full, gk_empty, gq_full, sb_full, s_done, p_full, pb_full, o_full;
+  uint64_t ak_full, ax_full, lk_full, lq_full, gk_full, gk_empty, gq_full, sb_full, s_done, p_full, pb_full, o_full;
   uint64_t o_staged, o_stored;
   uint64_t done[3];
   uint32_t tmem_base;
@@ -1345,6 +1388,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     mbar_init(&B.xq_empty, kRowWarps);
     mbar_init(&B.v_full, 1);
     mbar_init(&B.v_empty, 2);    // the state update and P [V | 1] read V
+    mbar_init(&B.ak_full, kRowWarps);
     mbar_init(&B.ax_full, kRowWarps);
     mbar_init(&B.lk_full, 1);
     mbar_init(&B.lq_full, 1);
@@ -1413,16 +1457,19 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       const uint64_t d_w = make_sdesc(smem_u32(smem + L.w), 16, 1024);
       const uint64_t d_vb = make_sdesc32(smem_u32(smem + L.v), 4096, 256);          // [V | 1], N = 80
       const uint64_t d_gk_mn = make_sdesc(smem_u32(smem + L.gk), 16384, 1024);     // Gamma_K^T as MN-major A
+      const uint64_t d_ak = make_sdesc(smem_u32(smem + L.ak), 16, 1024);           // key [x^2 | x], K-major A
       constexpr uint32_t id_s80 = make_idesc(128, kStCols, 1, 1, 1, 1);
       bool ok = wait_bounded_bo(&B.w_full, 0, &B.ab, a.ctrl, 80, a.wait_ns);
       for (int t = 0; ok && t < T; ++t) {
         const uint32_t ph = t & 1;
-        // key logits: the key operand is in OX and L is free (the row warps have taken the previous
-        // tile's output, which follows P [V | 1])
-        if (!(ok = wait_bounded_bo(&B.ax_full, 0, &B.ab, a.ctrl, 81, a.wait_ns))) break;
+        // key logits: the key operand is in shared memory (the row warps build tile t's while P [V | 1]
+        // of tile t-1 runs) and L is free once that contraction has read the bf16 P
+        if (!(ok = wait_bounded_bo(&B.ak_full, ph, &B.ab, a.ctrl, 81, a.wait_ns) &&
+                   (t == 0 || wait_bounded_bo(&B.o_full, ph ^ 1u, &B.ab, a.ctrl, 96, a.wait_ns))))
+          break;
         GMA_TRACE_AT(20, t);
         tc_fence_after();
-        issue_logits(tmem, d_w, a.Kp, kCColO);
+        issue_logits_ss(tmem, d_ak, d_w, a.Kp);
         mma_commit(&B.lk_full);
         GMA_TRACE_AT(21, t);
 #ifdef GMA_TRACE
@@ -1430,7 +1477,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         GMA_TRACE_AT(26, t);
 #endif
         // query logits: the row warps have loaded the key logits and put the query operand in OX
-        if (!(ok = wait_bounded_bo(&B.ax_full, 1, &B.ab, a.ctrl, 82, a.wait_ns))) break;
+        if (!(ok = wait_bounded_bo(&B.ax_full, ph, &B.ab, a.ctrl, 82, a.wait_ns))) break;
         GMA_TRACE_AT(22, t);
         tc_fence_after();
         issue_logits(tmem, d_w, a.Kp, kCColO);
@@ -1571,6 +1618,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     // logit columns past Kp: never written by the logits contractions; zero (with c' = -inf they read as
     // -inf) or, at Kp <= 128, stale P values (finite, so the same)
     zero_unused_logits<NC>(tmem, rc, a.Kp);
+    // the key operand of tile u -> shared memory (K-major A of the key logits)
+    auto build_key = [&](int u) {
+      if (!warp_wait(&B.xk_full, (uint32_t)u & 1u, &B.ab, a.ctrl, 101, a.wait_ns)) return false;
+      transform_row_smem(sbase + L.xk, rc, sbase + L.ak);
+      fence_async_smem();
+      warp_arrive(&B.xk_empty);
+      warp_arrive(&B.ak_full);
+      return true;
+    };
+    if (ok && T > 0) ok = build_key(0);
     float v[NC];
     // every row warp runs all T tiles and all exchanges (see the write kernel); exchange e of the CTA uses
     // slot (e & 1), three per tile
@@ -1579,55 +1636,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       const int tok = (tile0 + t) * kTile + rc.row;
       const uint32_t s0 = (uint32_t)((3 * t) & 1) * 4u, s1 = s0 ^ 4u;
       if (warp == kRowWarp0) GMA_TRACE_AT(0, t);
-      // key operand -> OX (this thread overwrites only the output columns it read itself last tile)
-      if (ok) ok = warp_wait(&B.xk_full, ph, &B.ab, a.ctrl, 101, a.wait_ns);
-      if (warp == kRowWarp0) GMA_TRACE_AT(1, t);
-      if (ok) {
-        transform_row(sbase + L.xk, rc, tmem, kCColO);
-        warp_arrive(&B.xk_empty);
-        tmem_st_wait();
-        tc_fence_before();
-        warp_arrive(&B.ax_full);
-      }
-      // while the key logits run: snapshot the state after tile t-1's update for this tile's inter-tile
-      // term (the previous inter-tile term has read S_prev before p_full of t-1; this tile's state update
-      // waits for the snapshot).  Parts 0 / 1 take columns 0..31 and Z of state block 0 / 1, parts 2 / 3
-      // columns 32..63.
-      if (warp == kRowWarp0) GMA_TRACE_AT(14, t);
-      if (ok && t > 0) ok = warp_wait(&B.s_done, (t - 1) & 1, &B.ab, a.ctrl, 107, a.wait_ns);
-      if (warp == kRowWarp0) GMA_TRACE_AT(15, t);
-      if (ok && t > 0) {
-        tc_fence_after();
-        const int mb = rc.part & 1;
-        if (mb < MB) {
-          const int comp = 128 * mb + rc.row;
-          const uint32_t ts = tmem + rc.lane_base + kCColS + kStCols * mb;
-          const int c0 = rc.part < 2 ? 0 : 2;
-          uint32_t ra[16];
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            tmem_ld16(ts + 16 * (c0 + c), ra);
-            tmem_ld_wait_tied16(ra);
-            if (comp < a.Kp) snapshot_state_chunk(sbase + L.sbv, a.Kp, comp, c0 + c, ra, a.eps);
-          }
-          if (rc.part < 2) {
-            uint32_t z = tmem_ld1(ts + 64);
-            tmem_ld_wait_tied1(z);
-            if (comp < a.Kp) snapshot_state_chunk(sbase + L.sbv, a.Kp, comp, 4, &z, a.eps);
-          }
-        }
-        fence_async_smem();
-        tc_fence_before();
-        warp_arrive(&B.sb_full);
-      }
       // key logits -> registers; then the query operand -> OX
       float mk = -INFINITY;
       if (warp == kRowWarp0) GMA_TRACE_AT(2, t);
       if (ok) ok = warp_wait(&B.lk_full, ph, &B.ab, a.ctrl, 102, a.wait_ns);
       if (warp == kRowWarp0) GMA_TRACE_AT(3, t);
       if (ok) {
-        // the key logits have completed, so OX is free: the query operand goes in first (while no
-        // logits are held in registers), then the key logits are loaded and both L and OX handed over
+        // OX is free (this thread read its output columns at the end of the previous tile): the query
+        // operand goes in first (while no logits are held in registers), then the key logits are
+        // loaded and both L and OX handed over
         tc_fence_after();
         ok = warp_wait(&B.xq_full, ph, &B.ab, a.ctrl, 103, a.wait_ns);
         if (ok) {
@@ -1698,8 +1715,44 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         tc_fence_before();
         warp_arrive(&B.pb_full);
       }
+      // while P [V | 1] runs: the state after this tile's update -> the bf16 copy read by the next tile's
+      // inter-tile term (this tile's has completed with P), then the next tile's key operand -> shared
+      // memory (P and the state update have read this tile's Gamma_K).  Every tile waits for its state
+      // update, since the output below is staged in Gamma_K's first block.  Parts 0 / 1 take columns
+      // 0..31 and Z of state block 0 / 1, parts 2 / 3 columns 32..63.
+      if (warp == kRowWarp0) GMA_TRACE_AT(14, t);
+      if (ok) ok = warp_wait(&B.s_done, ph, &B.ab, a.ctrl, 107, a.wait_ns);
+      if (warp == kRowWarp0) GMA_TRACE_AT(15, t);
+      if (t + 1 < T) {
+        if (ok) {
+          tc_fence_after();
+          const int mb = rc.part & 1;
+          if (mb < MB) {
+            const int comp = 128 * mb + rc.row;
+            const uint32_t ts = tmem + rc.lane_base + kCColS + kStCols * mb;
+            const int c0 = rc.part < 2 ? 0 : 2;
+            uint32_t ra[16];
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              tmem_ld16(ts + 16 * (c0 + c), ra);
+              tmem_ld_wait_tied16(ra);
+              if (comp < a.Kp) snapshot_state_chunk(sbase + L.sbv, a.Kp, comp, c0 + c, ra, a.eps);
+            }
+            if (rc.part < 2) {
+              uint32_t z = tmem_ld1(ts + 64);
+              tmem_ld_wait_tied1(z);
+              if (comp < a.Kp) snapshot_state_chunk(sbase + L.sbv, a.Kp, comp, 4, &z, a.eps);
+            }
+          }
+          fence_async_smem();
+          tc_fence_before();
+          warp_arrive(&B.sb_full);
+        }
+        if (ok) ok = build_key(t + 1);
+      }
+      if (warp == kRowWarp0) GMA_TRACE_AT(1, t);
       // output: dims 8 part + [0, 8) and 32 + 8 part + [0, 8) -- the columns this thread's part of the
-      // next key operand overwrites -- normalised by gq~ . (Z + eps)
+      // next query operand overwrites -- normalised by gq~ . (Z + eps)
       if (warp == kRowWarp0) GMA_TRACE_AT(16, t);
       if (ok) ok = warp_wait(&B.o_full, ph, &B.ab, a.ctrl, 108, a.wait_ns);
       if (warp == kRowWarp0) GMA_TRACE_AT(17, t);
