@@ -64,11 +64,14 @@ def test_decode_continues_the_prompt(gma, dtype, K):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_decode_from_empty_state_is_causal_forward(gma, dtype):
+@pytest.mark.parametrize("K", [1, 5, 64, 200])
+def test_decode_from_empty_state_is_causal_forward(gma, dtype, K):
+    # K <= 16 runs 64 threads (one per output column) with idle component slots; K = 200 leaves part
+    # of the last warps idle
     import torch
-    inp = make_inputs(1, 4, 37, 64, dtype=dtype, seed=50)
+    inp = make_inputs(1, 4, 37, K, dtype=dtype, seed=50 + K)
     t = to_device(inp)
-    state = torch.zeros((1, 4, 64, 65), dtype=torch.float32, device="cuda")
+    state = torch.zeros((1, 4, K, 65), dtype=torch.float32, device="cuda")
     O = gma.causal_decode(t["Q"], t["K"], t["V"], t["mu"], t["sigma2"], t["log_pi"], state).float().cpu().numpy()
     R = orc.forward(inp["Q"], inp["K"], inp["V"], inp["mu"], inp["sigma2"], inp["log_pi"], 1e-6, causal=True)
     assert rel_err(O, R) <= TOL[dtype]
