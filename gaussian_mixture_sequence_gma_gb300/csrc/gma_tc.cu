@@ -1073,9 +1073,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       bool ok = wait_bounded(&B.w_full, 0, &B.ab, a.ctrl, 112, a.wait_ns);
       for (int t = g; ok && t < T; t += 2) {
         const uint32_t k = (uint32_t)(t >> 1), ph = k & 1;
-        // logits: the group's operand is built and its region free (the previous output has been read)
+        // logits: the group's operand is built and its region free (the previous output has been read),
+        // and the previous tile's logits (the other group's) have completed.  Left to themselves, the two
+        // chains settle into a rhythm in which their logits and softmax passes coincide (tile loops of
+        // 108 - 114 us per CTA at B=1 H=8 N=131072 K=256); kept one logits contraction apart, each
+        // group's softmax runs beside the other's contractions.  (The other group's next logits wait
+        // for this group's, so the awaited phase is the last one that can have completed.)
         if (!(ok = wait_bounded(&B.a_full[g], ph, &B.ab, a.ctrl, 113, a.wait_ns) &&
-                   (t < 2 || wait_bounded(&B.r_empty[g], ph ^ 1, &B.ab, a.ctrl, 114, a.wait_ns))))
+                   (t < 2 || wait_bounded(&B.r_empty[g], ph ^ 1, &B.ab, a.ctrl, 114, a.wait_ns)) &&
+                   (t == 0 || wait_bounded(&B.l_full[g ^ 1], (uint32_t)((t - 1) >> 1) & 1u, &B.ab, a.ctrl, 119,
+                                           a.wait_ns))))
           break;
         GMA_TRACE_AT(20, t);
         tc_fence_after();
