@@ -66,6 +66,34 @@ def test_workspace_bytes(L):
     assert gma.workspace_bytes(P(N=1 << 20), gma.OP_BIDIR) == gma.workspace_bytes(P(N=1 << 16), gma.OP_BIDIR)
 
 
+def _segments(BH, tiles, sms=152):
+    """The causal path's segment count per head row: over the largest count fitting in w = 1..8 waves of
+    one CTA per SM, the one with the fewest waves * (tiles per segment + 1); ties to fewer segments."""
+    best, best_cost = 1, None
+    for w in range(1, 9):
+        s = max(1, min(w * sms // BH, tiles))
+        seg = -(-tiles // s)
+        splits = -(-tiles // seg)
+        cost = -(-BH * splits // sms) * (seg + 1)
+        if best_cost is None or cost < best_cost or (cost == best_cost and splits < best):
+            best, best_cost = splits, cost
+    return best
+
+
+@pytest.mark.parametrize("B,H,N,K,want", [(8, 12, 2048, 256, 3), (4, 8, 4096, 128, 4), (1, 8, 131072, 256, 19),
+                                          (12, 1, 8192, 64, 11), (1000, 1, 2048, 256, 1)])
+def test_causal_segments_follow_the_wave_rule(B, H, N, K, want):
+    """bf16 causal workspace = a part independent of N + B*H segments x Kp x 80 float32 aggregates, so
+    the difference against a one-tile problem (one segment) gives the segment count the library chose."""
+    kp = 64 if K <= 64 else (128 if K <= 128 else 256)
+    assert _segments(B * H, N // 128) == want
+    big = gma.workspace_bytes(P(B=B, H=H, N=N, K=K), gma.OP_CAUSAL)
+    one = gma.workspace_bytes(P(B=B, H=H, N=128, K=K), gma.OP_CAUSAL)
+    per_segment = B * H * kp * 80 * 4
+    # both totals are rounded up to 256 bytes; the aggregates are a multiple of 256 bytes here
+    assert big - one == (want - 1) * per_segment
+
+
 # Fake, 256-aligned "device" addresses: every call below must fail (or no-op) before any CUDA call.
 A = 1 << 20
 
