@@ -184,25 +184,34 @@ __global__ void __launch_bounds__(kPThreads, 1)
       tc::tc_fence_after();
       const int b = m / N, n = m - (m / N) * N;
       const int hc = H * kD;  // columns of each of Q, K, V
-#pragma unroll 2
-      for (int c = 0; c < kPBN / 16; ++c) {
-        uint32_t r[16];
-        tc::tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + 256u * (uint32_t)hf + 16 * c, r);
-        tc::tmem_ld_wait_tied16(r);
-        const int col = n0 + 16 * c;
-        if (col < Ncol && m < M) {
-          const float4* bs = reinterpret_cast<const float4*>(bias + col);
-          uint32_t u[8];
+      // four 16-column loads in flight per wait (one round trip per 64 columns, not per 16)
+#pragma unroll 1
+      for (int c4 = 0; c4 < kPBN / 64; ++c4) {
+        uint32_t r[64];
 #pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4) {
-            const float4 bb = __ldg(bs + k4);
-            u[2 * k4] = tc::pack_bf16x2(__uint_as_float(r[4 * k4]) + bb.x, __uint_as_float(r[4 * k4 + 1]) + bb.y);
-            u[2 * k4 + 1] = tc::pack_bf16x2(__uint_as_float(r[4 * k4 + 2]) + bb.z, __uint_as_float(r[4 * k4 + 3]) + bb.w);
+        for (int j = 0; j < 4; ++j)
+          tc::tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + 256u * (uint32_t)hf + 64 * c4 + 16 * j, r + 16 * j);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) tc::tmem_ld_wait_tied16(r + 16 * j);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int col = n0 + 64 * c4 + 16 * j;
+          if (col < Ncol && m < M) {
+            const float4* bs = reinterpret_cast<const float4*>(bias + col);
+            const uint32_t* rj = r + 16 * j;
+            uint32_t u[8];
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) {
+              const float4 bb = __ldg(bs + k4);
+              u[2 * k4] = tc::pack_bf16x2(__uint_as_float(rj[4 * k4]) + bb.x, __uint_as_float(rj[4 * k4 + 1]) + bb.y);
+              u[2 * k4 + 1] =
+                  tc::pack_bf16x2(__uint_as_float(rj[4 * k4 + 2]) + bb.z, __uint_as_float(rj[4 * k4 + 3]) + bb.w);
+            }
+            const int w = col / hc, hh = (col - w * hc) / kD, d = col - w * hc - hh * kD;
+            __nv_bfloat16* dst = (w == 0 ? Q : (w == 1 ? K : V)) + (((size_t)b * H + hh) * N + n) * kD + d;
+            reinterpret_cast<uint4*>(dst)[0] = make_uint4(u[0], u[1], u[2], u[3]);
+            reinterpret_cast<uint4*>(dst)[1] = make_uint4(u[4], u[5], u[6], u[7]);
           }
-          const int w = col / hc, hh = (col - w * hc) / kD, d = col - w * hc - hh * kD;
-          __nv_bfloat16* dst = (w == 0 ? Q : (w == 1 ? K : V)) + (((size_t)b * H + hh) * N + n) * kD + d;
-          reinterpret_cast<uint4*>(dst)[0] = make_uint4(u[0], u[1], u[2], u[3]);
-          reinterpret_cast<uint4*>(dst)[1] = make_uint4(u[4], u[5], u[6], u[7]);
         }
       }
     }
