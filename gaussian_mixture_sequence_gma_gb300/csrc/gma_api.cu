@@ -316,6 +316,39 @@ gma_status_t gma_causal_decode(const gma_problem_t* p, const void* Q, const void
   return simt_decode(*p, Q, K, V, mu, sigma2, log_pi, state, O, ws, st);
 }
 
+gma_status_t gma_decode_prepare(const gma_problem_t* p, const float* mu, const float* sigma2, const float* log_pi,
+                                void* ws, size_t ws_bytes, void* stream) {
+  gma_status_t s = validate_problem(p);
+  if (s != GMA_OK) return s;
+  if (!mu || !sigma2 || !log_pi || !ws) return GMA_ERR_INVALID_ARG;
+  const void* ptrs[] = {mu, sigma2, log_pi};
+  for (const void* q : ptrs)
+    if (!aligned(q, 16)) return GMA_ERR_INVALID_ARG;
+  if (!aligned(ws, kAlign)) return GMA_ERR_INVALID_ARG;
+  if (ws_bytes < required_bytes(*p, GMA_OP_CAUSAL_DECODE)) return GMA_ERR_WORKSPACE;
+  cudaGetLastError();
+  return simt_decode_fold(*p, mu, sigma2, log_pi, ws, (cudaStream_t)stream);
+}
+
+gma_status_t gma_causal_decode_prepared(const gma_problem_t* p, const void* Q, const void* K, const void* V,
+                                        float* state, void* O, void* ws, size_t ws_bytes, void* stream) {
+  gma_status_t s = validate_problem(p);
+  if (s != GMA_OK) return s;
+  if (!ws || !state) return GMA_ERR_INVALID_ARG;
+  if (p->N > 0) {
+    if (!Q || !K || !V || !O) return GMA_ERR_INVALID_ARG;
+    if (O == Q || O == K || O == V || O == (const void*)state) return GMA_ERR_INVALID_ARG;
+  }
+  const void* ptrs[] = {Q, K, V, state, O};
+  for (const void* q : ptrs)
+    if (q && !aligned(q, 16)) return GMA_ERR_INVALID_ARG;
+  if (!aligned(ws, kAlign)) return GMA_ERR_INVALID_ARG;
+  if (ws_bytes < required_bytes(*p, GMA_OP_CAUSAL_DECODE)) return GMA_ERR_WORKSPACE;
+  if (p->N == 0) return GMA_OK;
+  cudaGetLastError();
+  return simt_decode_run(*p, Q, K, V, state, O, ws, false, (cudaStream_t)stream);
+}
+
 
 gma_status_t gma_backward_bidir(const gma_problem_t* p, const void* Q, const void* K, const void* V, const float* mu,
                                 const float* sigma2, const float* log_pi, const void* dO, void* dQ, void* dK, void* dV,

@@ -79,6 +79,12 @@ size_t simt_decode_bytes(const gma_problem_t& p);
 gma_status_t simt_decode(const gma_problem_t& p, const void* Q, const void* K, const void* V, const float* mu,
                          const float* sigma2, const float* log_pi, float* state, void* out, void* ws,
                          cudaStream_t stream);
+// The two halves of simt_decode: the parameter fold into the workspace, and the decode reading it
+// (dependent = 1: launched as a dependent of the fold just before it).
+gma_status_t simt_decode_fold(const gma_problem_t& p, const float* mu, const float* sigma2, const float* log_pi,
+                              void* ws, cudaStream_t st);
+gma_status_t simt_decode_run(const gma_problem_t& p, const void* Q, const void* K, const void* V, float* state,
+                             void* out, void* ws, bool dependent, cudaStream_t st);
 // Q / K / V projection of a Transformer block into Q, K, V ([B][H][N][64], I/O dtype, bias added).  bf16:
 // one tcgen05 GEMM with the layout in its epilogue; it clears ctrl's error word and reports its own
 // bounded waits there (Y and lt_ws unused).  float32: library GEMM into Y (float32), then a layout

@@ -1695,26 +1695,49 @@ size_t simt_decode_bytes(const gma_problem_t& p) {
   return align_up(sizeof(Ctrl)) + align_up((size_t)p.H * decode_head_floats(p.K) * sizeof(float));
 }
 
-gma_status_t simt_decode(const gma_problem_t& p, const void* Q, const void* K, const void* V, const float* mu,
-                         const float* sigma2, const float* log_pi, float* state, void* out, void* ws,
-                         cudaStream_t st) {
-  const size_t smem = decode_smem_floats(p.K) * sizeof(float);
-  const int BH = p.B * p.H;
+gma_status_t simt_decode_fold(const gma_problem_t& p, const float* mu, const float* sigma2, const float* log_pi,
+                              void* ws, cudaStream_t st) {
   float* folded = (float*)((char*)ws + align_up(sizeof(Ctrl)));
   GMA_LAUNCH("simt_decode_fold", simt_decode_fold_kernel, dim3(cdiv(p.K, 32), p.H), 256, 0, st, mu, sigma2, log_pi,
              p.H, p.K, folded);
-  if (gma_status_t e = check_launch("launch simt_decode_fold", (const void*)simt_decode_fold_kernel)) return e;
+  return check_launch("launch simt_decode_fold", (const void*)simt_decode_fold_kernel);
+}
+
+// The decode kernel copies the state before its grid dependency wait: launched as a dependent only of
+// the fold (which itself waited for everything earlier, so the previous decode's state writes are
+// complete), otherwise as a plain launch.
+gma_status_t simt_decode_run(const gma_problem_t& p, const void* Q, const void* K, const void* V, float* state,
+                             void* out, void* ws, bool dependent, cudaStream_t st) {
+  const size_t smem = decode_smem_floats(p.K) * sizeof(float);
+  const int BH = p.B * p.H;
+  const float* folded = (const float*)((const char*)ws + align_up(sizeof(Ctrl)));
   if (p.dtype == GMA_F32) {
     if (set_smem_optin((const void*)simt_decode_kernel<float>, (int)smem, 4) != GMA_OK) return GMA_ERR_CUDA;
-    GMA_LAUNCH_DEPENDENT("simt_decode", simt_decode_kernel<float>, BH, kDecodeThreads, smem, st, (const float*)Q,
-               (const float*)K, (const float*)V, folded, p.H, p.N, p.K, state, p.eps, (float*)out, (Ctrl*)ws);
+    if (dependent)
+      GMA_LAUNCH_DEPENDENT("simt_decode", simt_decode_kernel<float>, BH, kDecodeThreads, smem, st, (const float*)Q,
+                           (const float*)K, (const float*)V, folded, p.H, p.N, p.K, state, p.eps, (float*)out,
+                           (Ctrl*)ws);
+    else
+      GMA_LAUNCH("simt_decode", simt_decode_kernel<float>, BH, kDecodeThreads, smem, st, (const float*)Q,
+                 (const float*)K, (const float*)V, folded, p.H, p.N, p.K, state, p.eps, (float*)out, (Ctrl*)ws);
     return check_launch("launch simt_decode", (const void*)simt_decode_kernel<float>);
   }
-  if (set_smem_optin((const void*)simt_decode_kernel<__nv_bfloat16>, (int)smem, 4) != GMA_OK) return GMA_ERR_CUDA;
-  GMA_LAUNCH_DEPENDENT("simt_decode", simt_decode_kernel<__nv_bfloat16>, BH, kDecodeThreads, smem, st,
-             (const __nv_bfloat16*)Q, (const __nv_bfloat16*)K, (const __nv_bfloat16*)V, folded, p.H, p.N, p.K, state,
-             p.eps, (__nv_bfloat16*)out, (Ctrl*)ws);
-  return check_launch("launch simt_decode", (const void*)simt_decode_kernel<__nv_bfloat16>);
+  using bf = __nv_bfloat16;
+  if (set_smem_optin((const void*)simt_decode_kernel<bf>, (int)smem, 4) != GMA_OK) return GMA_ERR_CUDA;
+  if (dependent)
+    GMA_LAUNCH_DEPENDENT("simt_decode", simt_decode_kernel<bf>, BH, kDecodeThreads, smem, st, (const bf*)Q,
+                         (const bf*)K, (const bf*)V, folded, p.H, p.N, p.K, state, p.eps, (bf*)out, (Ctrl*)ws);
+  else
+    GMA_LAUNCH("simt_decode", simt_decode_kernel<bf>, BH, kDecodeThreads, smem, st, (const bf*)Q, (const bf*)K,
+               (const bf*)V, folded, p.H, p.N, p.K, state, p.eps, (bf*)out, (Ctrl*)ws);
+  return check_launch("launch simt_decode", (const void*)simt_decode_kernel<bf>);
+}
+
+gma_status_t simt_decode(const gma_problem_t& p, const void* Q, const void* K, const void* V, const float* mu,
+                         const float* sigma2, const float* log_pi, float* state, void* out, void* ws,
+                         cudaStream_t st) {
+  if (gma_status_t e = simt_decode_fold(p, mu, sigma2, log_pi, ws, st)) return e;
+  return simt_decode_run(p, Q, K, V, state, out, ws, true, st);
 }
 
 namespace {

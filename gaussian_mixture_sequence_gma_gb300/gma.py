@@ -19,7 +19,7 @@ GMA_F32, GMA_BF16 = 0, 1
 (OP_RESPONSIBILITIES, OP_BIDIR, OP_CAUSAL, OP_CROSS, OP_CAUSAL_STATE, OP_CAUSAL_DECODE, OP_BACKWARD_BIDIR,
  OP_BACKWARD_CAUSAL, OP_PROJECTED_BIDIR, OP_PROJECTED_CAUSAL) = range(10)
 
-EXPORTED = ("gma_workspace_bytes", "gma_responsibilities", "gma_forward_bidir", "gma_forward_causal", "gma_forward_cross", "gma_state_bytes", "gma_causal_state", "gma_causal_decode", "gma_backward_bidir", "gma_backward_causal",
+EXPORTED = ("gma_workspace_bytes", "gma_responsibilities", "gma_forward_bidir", "gma_forward_causal", "gma_forward_cross", "gma_state_bytes", "gma_causal_state", "gma_causal_decode", "gma_decode_prepare", "gma_causal_decode_prepared", "gma_backward_bidir", "gma_backward_causal",
             "gma_forward_projected",
             "gma_check_device_error", "gma_status_string", "gma_version", "gma_last_error", "gma_launch_count", "gma_profile_enable",
             "gma_profile_read", "gma_forward_bidir_static_ws", "gma_static_ws_capacity", "gma_static_ws_check_error",
@@ -77,6 +77,10 @@ def lib():
     L.gma_causal_state.restype = ctypes.c_int
     L.gma_causal_decode.argtypes = [pp, vp, vp, vp, fp, fp, fp, vp, vp, vp, sz, vp]
     L.gma_causal_decode.restype = ctypes.c_int
+    L.gma_decode_prepare.argtypes = [pp, fp, fp, fp, vp, sz, vp]
+    L.gma_decode_prepare.restype = ctypes.c_int
+    L.gma_causal_decode_prepared.argtypes = [pp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.gma_causal_decode_prepared.restype = ctypes.c_int
     L.gma_backward_bidir.argtypes = [pp, vp, vp, vp, fp, fp, fp, vp, vp, vp, vp, fp, fp, fp, vp, sz, vp]
     L.gma_backward_bidir.restype = ctypes.c_int
     L.gma_backward_causal.argtypes = L.gma_backward_bidir.argtypes
@@ -327,6 +331,44 @@ def causal_decode(Q, K, V, mu, sigma2, log_pi, state, eps=1e-6, out=None, worksp
                                     _stream_handle(stream, dev))
     if s != GMA_OK:
         raise GmaError(s, "gma_causal_decode")
+    return out
+
+
+def decode_prepare(mu, sigma2, log_pi, dtype=torch.bfloat16, workspace=None, stream=None):
+    """Fold the parameters once for causal_decode_prepared; returns the decode workspace holding them
+    (valid for any B and dtype with these H and K, as long as the parameters do not change)."""
+    H, Kc, d = mu.shape
+    _params(mu, sigma2, log_pi)
+    dev = _check_cuda(mu, sigma2, log_pi)
+    prob = problem(1, H, 1, Kc, dtype, 1e-6, d=d, dv=d)
+    if workspace is None:
+        workspace = alloc_workspace(prob, OP_CAUSAL_DECODE, dev)
+    with torch.cuda.device(dev):
+        s = lib().gma_decode_prepare(ctypes.byref(prob), _ptr(mu), _ptr(sigma2), _ptr(log_pi), _ptr(workspace),
+                                     workspace.numel(), _stream_handle(stream, dev))
+    if s != GMA_OK:
+        raise GmaError(s, "gma_decode_prepare")
+    return workspace
+
+
+def causal_decode_prepared(Q, K, V, state, workspace, eps=1e-6, out=None, stream=None):
+    """causal_decode with the parameters folded by decode_prepare into `workspace` (one launch)."""
+    B, H, N, d = Q.shape
+    dv = V.shape[-1]
+    Kc = state.shape[2]
+    dev = _check_cuda(Q, K, V, state, workspace)
+    if K.dtype != Q.dtype or V.dtype != Q.dtype:
+        raise TypeError("Q, K and V must share one dtype")
+    if state.dtype != torch.float32 or tuple(state.shape) != (B, H, Kc, dv + 1):
+        raise ValueError("state must be float32 [B,H,K,dv+1]")
+    prob = problem(B, H, N, Kc, Q.dtype, eps, d=d, dv=dv)
+    if out is None:
+        out = torch.empty((B, H, N, dv), dtype=Q.dtype, device=dev)
+    with torch.cuda.device(dev):
+        s = lib().gma_causal_decode_prepared(ctypes.byref(prob), _ptr(Q), _ptr(K), _ptr(V), _ptr(state), _ptr(out),
+                                             _ptr(workspace), workspace.numel(), _stream_handle(stream, dev))
+    if s != GMA_OK:
+        raise GmaError(s, "gma_causal_decode_prepared")
     return out
 
 

@@ -234,6 +234,22 @@ GMA_API gma_status_t gma_causal_decode(const gma_problem_t *p, const void *Q, co
                                        void *O, void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * The decode step split for fixed parameters: gma_decode_prepare runs only the parameter fold of
+ * gma_causal_decode into the workspace (gma_workspace_bytes(p, GMA_OP_CAUSAL_DECODE), the same layout;
+ * p->N is not used), and gma_causal_decode_prepared runs only the decode with the folded parameters
+ * found there, once per call, as long as the parameters have not changed.  The outputs and the state
+ * are bit-identical to gma_causal_decode with the same parameters.  A prepared call is one launch,
+ * ordered after everything earlier on the stream; a prepare must be ordered after any decode still
+ * reading the workspace (same stream, or an event).  Errors as gma_causal_decode; a workspace that was
+ * never prepared for these parameters is not detected (the outputs are then those of whatever folded
+ * parameters it holds).
+ */
+GMA_API gma_status_t gma_decode_prepare(const gma_problem_t *p, const float *mu, const float *sigma2,
+                                        const float *log_pi, void *ws, size_t ws_bytes, void *stream);
+GMA_API gma_status_t gma_causal_decode_prepared(const gma_problem_t *p, const void *Q, const void *K, const void *V,
+                                                float *state, void *O, void *ws, size_t ws_bytes, void *stream);
+
+/*
  * Backward pass of the bidirectional forward: given dO = dL/dO, the gradients of L with respect to
  * every input and parameter,
  *   dQ, dK [B,H,N,d], dV [B,H,N,dv] in p->dtype (written);

@@ -301,6 +301,37 @@ def test_projected_argument_errors(L):
     assert proj(P(N=0), p=nul, ws_bytes=gma.workspace_bytes(P(N=0), gma.OP_PROJECTED_CAUSAL)) == gma.GMA_OK
 
 
+def test_prepared_decode_argument_errors(L):
+    """gma_decode_prepare / gma_causal_decode_prepared check their arguments before any CUDA call."""
+    ptr = [A + i * (1 << 16) for i in range(10)]
+    need = gma.workspace_bytes(P(), gma.OP_CAUSAL_DECODE)
+
+    def prep(prob, p=ptr, ws_bytes=1 << 30):  # mu, sigma2, log_pi, ws
+        return L.gma_decode_prepare(ctypes.byref(prob), p[3], p[4], p[5], p[7], ws_bytes, None)
+
+    def run(prob, p=ptr, ws_bytes=1 << 30):  # Q, K, V, state, O, ws
+        return L.gma_causal_decode_prepared(ctypes.byref(prob), p[0], p[1], p[2], p[8], p[6], p[7], ws_bytes, None)
+
+    for f, idx in ((prep, (3, 4, 5, 7)), (run, (0, 1, 2, 6, 7, 8))):
+        assert f(P(d=32)) == gma.GMA_ERR_UNSUPPORTED
+        assert f(P(K=0)) == gma.GMA_ERR_INVALID_ARG
+        assert f(P(K=300)) == gma.GMA_ERR_UNSUPPORTED
+        for i in idx:
+            bad = list(ptr)
+            bad[i] = None
+            assert f(P(), bad) == gma.GMA_ERR_INVALID_ARG, (f.__name__, i)
+            bad[i] = ptr[i] + 4
+            assert f(P(), bad) == gma.GMA_ERR_INVALID_ARG, (f.__name__, i)
+        assert f(P(), ws_bytes=need - 1) == gma.GMA_ERR_WORKSPACE
+    # outputs may not alias an input or the state
+    for j in (0, 1, 2, 8):
+        alias = list(ptr)
+        alias[6] = ptr[j]
+        assert run(P(), alias) == gma.GMA_ERR_INVALID_ARG
+    # no new token: nothing to do, also without Q, K, V and O
+    assert run(P(N=0), [None, None, None, None, None, None, None, ptr[7], ptr[8], None], ws_bytes=need) == gma.GMA_OK
+
+
 def test_decode_workspace_size():
     """The decode workspace is the documented control block (256 B) plus every head's folded parameters,
     4 H (128 (K + 1) + K) bytes with each head's block rounded up to 16 bytes, the total to 256."""

@@ -133,3 +133,31 @@ def test_decode_bench_shape(gma):
     assert np.isfinite(O).all()
     assert rel_err(O, R) <= TOL["bf16"]
     assert rel_err(state.cpu().numpy(), _ref_state(inp, N0 + T)) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("K", [17, 256])
+def test_prepared_decode_is_bit_identical(gma, dtype, K):
+    """gma_decode_prepare + gma_causal_decode_prepared give the outputs and state of gma_causal_decode
+    bit for bit (the same fold, the same decode kernel), step after step with the parameters folded
+    once, and a multi-token prepared call equals the single-token ones."""
+    import torch
+    N0, T = 300, 6
+    inp = make_inputs(2, 3, N0 + T, K, dtype=dtype, seed=80 + K)
+    t = to_device(inp)
+    p = _slice(t, 0, N0)
+    s_ref = gma.causal_state(p["K"], p["V"], t["mu"], t["sigma2"], t["log_pi"])
+    s_pre, s_multi = s_ref.clone(), s_ref.clone()
+    ws = gma.decode_prepare(t["mu"], t["sigma2"], t["log_pi"], dtype=t["Q"].dtype)
+    for i in range(N0, N0 + T):
+        d = _slice(t, i, i + 1)
+        o_ref = gma.causal_decode(d["Q"], d["K"], d["V"], t["mu"], t["sigma2"], t["log_pi"], s_ref)
+        o_pre = gma.causal_decode_prepared(d["Q"], d["K"], d["V"], s_pre, ws)
+        assert torch.equal(o_ref, o_pre)
+        assert torch.equal(s_ref, s_pre)
+    d = _slice(t, N0, N0 + T)
+    o_multi = gma.causal_decode_prepared(d["Q"], d["K"], d["V"], s_multi, ws)
+    assert torch.equal(s_multi, s_ref)
+    R = orc.forward(inp["Q"], inp["K"], inp["V"], inp["mu"], inp["sigma2"], inp["log_pi"], 1e-6, causal=True,
+                    rows=np.arange(N0, N0 + T))
+    assert rel_err(o_multi.float().cpu().numpy(), R) <= TOL[dtype]
