@@ -79,6 +79,23 @@ uint64_t wait_limit_ns() {
   return e ? e : kDefaultWaitNs;
 }
 
+namespace {
+std::atomic<int> g_det{-1};  // -1: not set through the API
+
+bool env_det() {
+  static const bool v = [] {
+    const char* e = std::getenv("GMA_DETERMINISTIC");
+    return e && *e && !(e[0] == '0' && e[1] == 0);
+  }();
+  return v;
+}
+}  // namespace
+
+bool deterministic() {
+  const int v = g_det.load(std::memory_order_relaxed);
+  return v < 0 ? env_det() : v != 0;
+}
+
 gma_status_t set_carveout_max(const void* func) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return GMA_ERR_CUDA;
@@ -113,23 +130,25 @@ gma_status_t validate_problem(const gma_problem_t* p) {
 struct ProjLayout {
   size_t base, lt, y, q, k, v, total;
 };
-ProjLayout proj_layout(const gma_problem_t& p, bool causal);
+ProjLayout proj_layout(const gma_problem_t& p, bool causal, bool det);
 
-size_t required_bytes(const gma_problem_t& p, gma_op_t op) {
+// det: the deterministic reduction mode (taken once per call, so that the size checked is the one used).
+size_t required_bytes(const gma_problem_t& p, gma_op_t op, bool det) {
   if (op == GMA_OP_PROJECTED_BIDIR || op == GMA_OP_PROJECTED_CAUSAL)
-    return proj_layout(p, op == GMA_OP_PROJECTED_CAUSAL).total;
+    return proj_layout(p, op == GMA_OP_PROJECTED_CAUSAL, det).total;
   if (op == GMA_OP_CROSS) op = GMA_OP_BIDIR;  // the same workspace: it does not depend on N
   if (op == GMA_OP_CAUSAL_DECODE) return simt_decode_bytes(p);
-  if (op == GMA_OP_BACKWARD_BIDIR || op == GMA_OP_BACKWARD_CAUSAL) return simt_backward_bytes(p, op == GMA_OP_BACKWARD_CAUSAL);
-  if (p.dtype == GMA_BF16) return tc_plan(p, op).total;
-  return simt_plan(p, op).total;
+  if (op == GMA_OP_BACKWARD_BIDIR || op == GMA_OP_BACKWARD_CAUSAL)
+    return simt_backward_bytes(p, op == GMA_OP_BACKWARD_CAUSAL, det);
+  if (p.dtype == GMA_BF16) return tc_plan(p, op, det).total;
+  return simt_plan(p, op, det).total;
 }
 
-ProjLayout proj_layout(const gma_problem_t& p, bool causal) {
+ProjLayout proj_layout(const gma_problem_t& p, bool causal, bool det) {
   ProjLayout L{};
   const size_t es = p.dtype == GMA_BF16 ? 2 : 4;
   const size_t qkv = align_up((size_t)p.B * p.H * p.N * kD * es);
-  L.base = align_up(required_bytes(p, causal ? GMA_OP_CAUSAL : GMA_OP_BIDIR));
+  L.base = align_up(required_bytes(p, causal ? GMA_OP_CAUSAL : GMA_OP_BIDIR, det));
   L.lt = L.base;
   const bool lib_gemm = p.dtype != GMA_BF16;  // float32 I/O: library GEMM workspace and a float32 Y
   L.y = L.lt + (lib_gemm ? align_up(proj_lt_workspace_bytes()) : 0);
@@ -143,7 +162,7 @@ ProjLayout proj_layout(const gma_problem_t& p, bool causal) {
 // Nk: keys / values per (b, h); N (= p->N) except for cross-attention.
 gma_status_t run(const gma_problem_t* p, gma_op_t op, int Nk, const void* Q, const void* K, const void* V,
                  const float* mu, const float* sigma2, const float* log_pi, void* out, void* ws, size_t ws_bytes,
-                 void* stream, bool clear_err = true) {
+                 void* stream, bool clear_err = true, int det_mode = -1) {
   static const char* const kNames[] = {"gma_responsibilities", "gma_forward_bidir", "gma_forward_causal",
                                        "gma_forward_cross", "gma_causal_state"};
   const int oi = (int)op;
@@ -162,13 +181,14 @@ gma_status_t run(const gma_problem_t* p, gma_op_t op, int Nk, const void* Q, con
   for (const void* q : ptrs)
     if (q && !aligned(q, 16)) return GMA_ERR_INVALID_ARG;
   if (!aligned(ws, kAlign)) return GMA_ERR_INVALID_ARG;
-  if (ws_bytes < required_bytes(*p, op)) return GMA_ERR_WORKSPACE;
+  const bool det = det_mode < 0 ? deterministic() : det_mode != 0;
+  if (ws_bytes < required_bytes(*p, op, det)) return GMA_ERR_WORKSPACE;
   if (p->N == 0) return GMA_OK;
   cudaStream_t st = (cudaStream_t)stream;
   cudaGetLastError();  // a stale error from earlier caller work is not ours to report
   if (op == GMA_OP_CROSS) op = GMA_OP_BIDIR;  // the bidirectional kernels, with the key length Nk
-  if (p->dtype == GMA_BF16) return tc_run(*p, op, Nk, Q, K, V, mu, sigma2, log_pi, out, ws, st, clear_err);
-  return simt_run(*p, op, Nk, Q, K, V, mu, sigma2, log_pi, out, ws, st);
+  if (p->dtype == GMA_BF16) return tc_run(*p, op, Nk, Q, K, V, mu, sigma2, log_pi, out, ws, st, clear_err, det);
+  return simt_run(*p, op, Nk, Q, K, V, mu, sigma2, log_pi, out, ws, st, det);
 }
 
 gma_status_t run_backward(const gma_problem_t* p, bool causal, const void* Q, const void* K, const void* V, const float* mu,
@@ -194,10 +214,12 @@ gma_status_t run_backward(const gma_problem_t* p, bool causal, const void* Q, co
     for (int j = i + 1; j < 6; ++j)
       if (outs[i] && outs[i] == outs[j]) return GMA_ERR_INVALID_ARG;
   if (!aligned(ws, kAlign)) return GMA_ERR_INVALID_ARG;
-  if (ws_bytes < required_bytes(*p, causal ? GMA_OP_BACKWARD_CAUSAL : GMA_OP_BACKWARD_BIDIR)) return GMA_ERR_WORKSPACE;
+  const bool det = deterministic();
+  if (ws_bytes < required_bytes(*p, causal ? GMA_OP_BACKWARD_CAUSAL : GMA_OP_BACKWARD_BIDIR, det))
+    return GMA_ERR_WORKSPACE;
   cudaStream_t st = (cudaStream_t)stream;
   cudaGetLastError();
-  return simt_backward(*p, causal, Q, K, V, mu, sigma2, log_pi, dO, dQ, dK, dV, dmu, dsigma2, dlog_pi, ws, st);
+  return simt_backward(*p, causal, Q, K, V, mu, sigma2, log_pi, dO, dQ, dK, dV, dmu, dsigma2, dlog_pi, ws, st, det);
 }
 
 }  // namespace
@@ -215,10 +237,18 @@ gma_status_t gma_set_wait_limit_ns(uint64_t ns) {
 
 uint64_t gma_get_wait_limit_ns(void) { return gma::wait_limit_ns(); }
 
+gma_status_t gma_set_deterministic(int mode) {
+  if (mode < -1 || mode > 1) return GMA_ERR_INVALID_ARG;
+  gma::g_det.store(mode, std::memory_order_relaxed);
+  return GMA_OK;
+}
+
+int gma_get_deterministic(void) { return gma::deterministic() ? 1 : 0; }
+
 size_t gma_workspace_bytes(const gma_problem_t* p, gma_op_t op) {
   if (validate_problem(p) != GMA_OK) return 0;
   if (op < GMA_OP_RESPONSIBILITIES || op > GMA_OP_PROJECTED_CAUSAL) return 0;
-  return required_bytes(*p, op);
+  return required_bytes(*p, op, deterministic());
 }
 
 gma_status_t gma_forward_projected(const gma_problem_t* p, int causal, int dm, const void* X, const void* Wqkv,
@@ -236,17 +266,18 @@ gma_status_t gma_forward_projected(const gma_problem_t* p, int causal, int dm, c
     if (q && !aligned(q, 16)) return GMA_ERR_INVALID_ARG;
   if (!aligned(ws, kAlign)) return GMA_ERR_INVALID_ARG;
   const gma_op_t op = causal ? GMA_OP_PROJECTED_CAUSAL : GMA_OP_PROJECTED_BIDIR;
-  if (ws_bytes < required_bytes(*p, op)) return GMA_ERR_WORKSPACE;
+  const bool det = deterministic();
+  if (ws_bytes < required_bytes(*p, op, det)) return GMA_ERR_WORKSPACE;
   if (p->N == 0) return GMA_OK;
   cudaStream_t st = (cudaStream_t)stream;
   cudaGetLastError();
-  const ProjLayout L = proj_layout(*p, causal != 0);
+  const ProjLayout L = proj_layout(*p, causal != 0, det);
   char* w = (char*)ws;
-  s = proj_run(*p, dm, X, Wqkv, bqkv, (float*)(w + L.y), w + L.q, w + L.k, w + L.v, w + L.lt, (Ctrl*)ws, st);
+  s = proj_run(*p, dm, X, Wqkv, bqkv, (float*)(w + L.y), w + L.q, w + L.k, w + L.v, w + L.lt, (Ctrl*)ws, st, det);
   if (s != GMA_OK) return s;
   // bf16: the projection kernel cleared the error word and reports its bounded waits there
   return run(p, causal ? GMA_OP_CAUSAL : GMA_OP_BIDIR, p->N, w + L.q, w + L.k, w + L.v, mu, sigma2, log_pi, O, ws,
-             L.base, stream, p->dtype != GMA_BF16);
+             L.base, stream, p->dtype != GMA_BF16, det ? 1 : 0);
 }
 
 gma_status_t gma_responsibilities(const gma_problem_t* p, const void* X, const float* mu, const float* sigma2,
@@ -288,11 +319,13 @@ gma_status_t gma_causal_state(const gma_problem_t* p, const void* K, const void*
   for (const void* q : ptrs)
     if (q && !aligned(q, 16)) return GMA_ERR_INVALID_ARG;
   if (!aligned(ws, kAlign)) return GMA_ERR_INVALID_ARG;
-  if (ws_bytes < required_bytes(*p, GMA_OP_CAUSAL_STATE)) return GMA_ERR_WORKSPACE;
+  const bool det = deterministic();
+  if (ws_bytes < required_bytes(*p, GMA_OP_CAUSAL_STATE, det)) return GMA_ERR_WORKSPACE;
   cudaStream_t st = (cudaStream_t)stream;
   cudaGetLastError();
-  if (p->dtype == GMA_BF16) return tc_run(*p, GMA_OP_CAUSAL_STATE, p->N, nullptr, K, V, mu, sigma2, log_pi, state, ws, st);
-  return simt_run(*p, GMA_OP_CAUSAL_STATE, p->N, nullptr, K, V, mu, sigma2, log_pi, state, ws, st);
+  if (p->dtype == GMA_BF16)
+    return tc_run(*p, GMA_OP_CAUSAL_STATE, p->N, nullptr, K, V, mu, sigma2, log_pi, state, ws, st, true, det);
+  return simt_run(*p, GMA_OP_CAUSAL_STATE, p->N, nullptr, K, V, mu, sigma2, log_pi, state, ws, st, det);
 }
 
 gma_status_t gma_causal_decode(const gma_problem_t* p, const void* Q, const void* K, const void* V, const float* mu,
@@ -309,7 +342,7 @@ gma_status_t gma_causal_decode(const gma_problem_t* p, const void* Q, const void
   for (const void* q : ptrs)
     if (q && !aligned(q, 16)) return GMA_ERR_INVALID_ARG;
   if (!aligned(ws, kAlign)) return GMA_ERR_INVALID_ARG;
-  if (ws_bytes < required_bytes(*p, GMA_OP_CAUSAL_DECODE)) return GMA_ERR_WORKSPACE;
+  if (ws_bytes < required_bytes(*p, GMA_OP_CAUSAL_DECODE, false)) return GMA_ERR_WORKSPACE;
   if (p->N == 0) return GMA_OK;
   cudaStream_t st = (cudaStream_t)stream;
   cudaGetLastError();
@@ -325,7 +358,7 @@ gma_status_t gma_decode_prepare(const gma_problem_t* p, const float* mu, const f
   for (const void* q : ptrs)
     if (!aligned(q, 16)) return GMA_ERR_INVALID_ARG;
   if (!aligned(ws, kAlign)) return GMA_ERR_INVALID_ARG;
-  if (ws_bytes < required_bytes(*p, GMA_OP_CAUSAL_DECODE)) return GMA_ERR_WORKSPACE;
+  if (ws_bytes < required_bytes(*p, GMA_OP_CAUSAL_DECODE, false)) return GMA_ERR_WORKSPACE;
   cudaGetLastError();
   return simt_decode_fold(*p, mu, sigma2, log_pi, ws, (cudaStream_t)stream);
 }
@@ -343,7 +376,7 @@ gma_status_t gma_causal_decode_prepared(const gma_problem_t* p, const void* Q, c
   for (const void* q : ptrs)
     if (q && !aligned(q, 16)) return GMA_ERR_INVALID_ARG;
   if (!aligned(ws, kAlign)) return GMA_ERR_INVALID_ARG;
-  if (ws_bytes < required_bytes(*p, GMA_OP_CAUSAL_DECODE)) return GMA_ERR_WORKSPACE;
+  if (ws_bytes < required_bytes(*p, GMA_OP_CAUSAL_DECODE, false)) return GMA_ERR_WORKSPACE;
   if (p->N == 0) return GMA_OK;
   cudaGetLastError();
   return simt_decode_run(*p, Q, K, V, state, O, ws, false, (cudaStream_t)stream);

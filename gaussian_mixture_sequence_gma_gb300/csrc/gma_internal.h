@@ -40,13 +40,16 @@ struct SimtPlan {
   int tiles;       // ceil(N / tile)
   int splits;      // CTAs per (b,h) for the write phase (bidir) or segments (causal)
   int seg_tiles;   // tiles per segment / split
-  size_t off_params, off_state, total;
+  bool det;        // deterministic reduction mode: the write's partial states are stored, then summed
+  size_t off_params, off_state, off_agg, total;  // off_agg: the partial states (det only)
 };
-SimtPlan simt_plan(const gma_problem_t& p, gma_op_t op);
+// det: plan for the deterministic reduction mode (the bidirectional, cross and state workspaces then
+// hold the write's partial states of at most kTargetUnits + B*H CTAs, whatever the key length).
+SimtPlan simt_plan(const gma_problem_t& p, gma_op_t op, bool det = false);
 // Nk: keys / values per (b, h) for the write phase (p.N except for cross-attention).
 gma_status_t simt_run(const gma_problem_t& p, gma_op_t op, int Nk, const void* Q, const void* K, const void* V,
                       const float* mu, const float* sigma2, const float* log_pi, void* out, void* ws,
-                      cudaStream_t stream);
+                      cudaStream_t stream, bool det = false);
 
 // ---- tensor-core (bf16 I/O) path ----------------------------------------------------------------
 struct TcPlan {
@@ -54,25 +57,29 @@ struct TcPlan {
   int tiles;       // ceil(N / 128)
   int splits;      // CTAs per (b,h) in the write phase / segments in the causal path
   int seg_tiles;   // tiles per split or segment
+  bool det;        // deterministic reduction mode: the write's per-CTA states are stored, then summed
   size_t off_w, off_c, off_flags, off_state;  // off_flags: per-head range flags of the parameter fold
+  size_t off_agg;  // det only: the write's per-CTA states (at most max(152, B*H) CTAs, any key length)
   size_t total;
 };
-TcPlan tc_plan(const gma_problem_t& p, gma_op_t op);
+TcPlan tc_plan(const gma_problem_t& p, gma_op_t op, bool det = false);
 // clear_err: the parameter fold clears the workspace error word first (false when an earlier kernel of
 // the same call, the tcgen05 projection, has already cleared it and may have reported into it).
 gma_status_t tc_run(const gma_problem_t& p, gma_op_t op, int Nk, const void* Q, const void* K, const void* V,
                     const float* mu, const float* sigma2, const float* log_pi, void* out, void* ws,
-                    cudaStream_t stream, bool clear_err = true);
+                    cudaStream_t stream, bool clear_err = true, bool det = false);
 bool tc_available();
 // Tensor map over a row-major bf16 matrix [rows][cols]: boxes of box_cols x box_rows, 128-byte swizzle,
 // zero fill outside (a 3-D map with a unit outer dimension, read with 3-D tensor loads).
 bool make_map_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols,
                    uint32_t box_rows);
 // Backward pass of the bidirectional or causal forward (float32 CUDA-core kernels, both I/O dtypes).
-size_t simt_backward_bytes(const gma_problem_t& p, bool causal);
+// det: every sum across CTAs (the state, its gradient and the parameter sums) is taken from stored
+// partials in a fixed order.
+size_t simt_backward_bytes(const gma_problem_t& p, bool causal, bool det = false);
 gma_status_t simt_backward(const gma_problem_t& p, bool causal, const void* Q, const void* K, const void* V, const float* mu,
                            const float* sigma2, const float* log_pi, const void* dO, void* dQ, void* dK, void* dV,
-                           float* dmu, float* dsigma2, float* dlog_pi, void* ws, cudaStream_t stream);
+                           float* dmu, float* dsigma2, float* dlog_pi, void* ws, cudaStream_t stream, bool det = false);
 // Decode T = p.N new tokens per (b, h) against `state` (float32 [B*H][K][dv + 1], in place).  Workspace:
 // simt_decode_bytes(p) (a control block and every head's folded parameters).
 size_t simt_decode_bytes(const gma_problem_t& p);
@@ -88,12 +95,14 @@ gma_status_t simt_decode_run(const gma_problem_t& p, const void* Q, const void* 
 // Q / K / V projection of a Transformer block into Q, K, V ([B][H][N][64], I/O dtype, bias added).  bf16:
 // one tcgen05 GEMM with the layout in its epilogue; it clears ctrl's error word and reports its own
 // bounded waits there (Y and lt_ws unused).  float32: library GEMM into Y (float32), then a layout
-// kernel; lt_ws: proj_lt_workspace_bytes() bytes.
+// kernel; lt_ws: proj_lt_workspace_bytes() bytes.  det: the library GEMM is restricted to algorithms
+// without a split-K reduction (the tcgen05 GEMM has none).
 size_t proj_lt_workspace_bytes();
 gma_status_t proj_run(const gma_problem_t& p, int dm, const void* X, const void* W, const float* bias, float* Y,
-                      void* Q, void* K, void* V, void* lt_ws, Ctrl* ctrl, cudaStream_t st);
+                      void* Q, void* K, void* V, void* lt_ws, Ctrl* ctrl, cudaStream_t st, bool det = false);
 // Test hook: bit 0 makes the next bidirectional write launch skip its first X-tile load, so that a
-// bounded device wait runs out and reports GMA_ERR_TIMEOUT.
+// bounded device wait runs out and reports GMA_ERR_TIMEOUT.  The environment variable GMA_FAULT_INJECT
+// (anything but "" or "0") sets it for the first bidirectional call of the process.
 void tc_set_fault_injection(uint32_t mask);
 
 // NVTX range for the lifetime of the object (one per C-ABI call).
@@ -107,6 +116,13 @@ struct NvtxScope {
 // Limit of every bounded device wait of the tensor-core kernels, in ns: gma_set_wait_limit_ns(), else the
 // environment variable GMA_WAIT_LIMIT_MS (read once), else 1 s.
 uint64_t wait_limit_ns();
+
+// Deterministic reduction mode: gma_set_deterministic(), else the environment variable GMA_DETERMINISTIC
+// (read once; a value other than empty or "0" turns it on), else off.  When on, no sum across CTAs uses
+// atomics: each CTA stores its partial, and one thread per element adds the partials up in a fixed
+// order, so that repeated calls on the same inputs give bitwise-equal outputs.  The workspaces of the
+// affected calls grow by the partials.
+bool deterministic();
 
 // Launch bookkeeping: counts every kernel launch, brackets it with an NVTX range named for its phase
 // and, while profiling is on, with a CUDA event pair on the launch stream.

@@ -22,7 +22,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 
 struct LtPlan {
-  int M = 0, Ncol = 0, dm = 0, dtype = -1;
+  int M = 0, Ncol = 0, dm = 0, dtype = -1, det = -1;
   cublasLtMatmulAlgo_t algo{};
   bool valid = false;
 };
@@ -229,7 +229,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
 size_t proj_lt_workspace_bytes() { return (size_t)32 << 20; }
 
 gma_status_t proj_run(const gma_problem_t& p, int dm, const void* X, const void* W, const float* bias, float* Y,
-                      void* Q, void* K, void* V, void* lt_ws, Ctrl* ctrl, cudaStream_t st) {
+                      void* Q, void* K, void* V, void* lt_ws, Ctrl* ctrl, cudaStream_t st, bool det) {
   if (p.dtype == GMA_BF16) {
     const int M = p.B * p.N, Ncol = 3 * p.H * kD;
     CUtensorMap mx, mw;
@@ -262,13 +262,18 @@ gma_status_t proj_run(const gma_problem_t& p, int dm, const void* X, const void*
     ret = lt_fail("cublasLt descriptor setup", s);
   }
   LtPlan& plan = g_plan[dev];
-  if (ret == GMA_OK && !(plan.valid && plan.M == M && plan.Ncol == Ncol && plan.dm == dm && plan.dtype == (int)p.dtype)) {
+  if (ret == GMA_OK && !(plan.valid && plan.M == M && plan.Ncol == Ncol && plan.dm == dm && plan.dtype == (int)p.dtype &&
+                        plan.det == (int)det)) {
     size_t wsb = proj_lt_workspace_bytes();
+    // deterministic reduction mode: no split-K reduction scheme, so each output is one in-order sum
+    uint32_t schemes = (uint32_t)CUBLASLT_REDUCTION_SCHEME_NONE;
     cublasLtMatmulHeuristicResult_t res{};
     int found = 0;
     if ((s = cublasLtMatmulPreferenceCreate(&pref)) != CUBLAS_STATUS_SUCCESS ||
         (s = cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES, &wsb, sizeof wsb)) !=
             CUBLAS_STATUS_SUCCESS ||
+        (det && (s = cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_REDUCTION_SCHEME_MASK, &schemes,
+                                                          sizeof schemes)) != CUBLAS_STATUS_SUCCESS) ||
         (s = cublasLtMatmulAlgoGetHeuristic(g_lt[dev], op, la, lb, lc, lc, pref, 1, &res, &found)) !=
             CUBLAS_STATUS_SUCCESS) {
       ret = lt_fail("cublasLtMatmulAlgoGetHeuristic", s);
@@ -280,6 +285,7 @@ gma_status_t proj_run(const gma_problem_t& p, int dm, const void* X, const void*
       plan.Ncol = Ncol;
       plan.dm = dm;
       plan.dtype = (int)p.dtype;
+      plan.det = (int)det;
       plan.algo = res.algo;
       plan.valid = true;
     }

@@ -436,6 +436,18 @@ __global__ void __launch_bounds__(kThreads) simt_read_kernel(const IO* __restric
   }
 }
 
+// Deterministic reduction mode: state[unit][e] = sum over p = 0 .. P-1 of part[unit][p][e], added in the
+// order of p.  grid (ceil(npairs / 256), B*H).
+__global__ void simt_state_sum_kernel(const float* __restrict__ part, int P, int npairs, float* __restrict__ state) {
+  const int unit = blockIdx.y;
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= npairs) return;
+  const float* src = part + (size_t)unit * P * npairs + e;
+  float s = 0.f;
+  for (int p = 0; p < P; ++p) s += src[(size_t)p * npairs];
+  state[(size_t)unit * npairs + e] = s;
+}
+
 // Exclusive scan over segments: agg[unit][p][e] <- sum_{p' < p} agg[unit][p'][e].  grid (ceil(K*65/256), B*H).
 __global__ void simt_scan_kernel(float* agg, int P, int npairs) {
   const int unit = blockIdx.y;
@@ -687,14 +699,16 @@ __device__ __forceinline__ void store_dl_rows(const float (&dl)[4][KC / 32], int
 }
 
 // Query side: grid (splits, B*H).  Recomputes O, pushes dO back through the read, writes dQ and dl_Q, and
-// adds [dVt | dZ] into dstate[unit][K][65].  Warp w owns tile rows 4w .. 4w + 3 in the row products and
+// adds [dVt | dZ] into dstate[unit][K][65] (dsplits = 0) or stores this CTA's share into
+// dstate[unit][split][K][65] (dsplits = the grid's splits; the deterministic reduction mode).  Warp w owns tile rows 4w .. 4w + 3 in the row products and
 // components w KC / 8 .. + KC / 8 of [dVt | dZ], which stay in registers across the CTA's tiles.
 template <typename IO, int KC>
 __global__ void __launch_bounds__(kThreads) simt_bwd_query_kernel(const IO* __restrict__ Q, const IO* __restrict__ dO,
                                                                   float* params, const float2* __restrict__ wpair,
                                                                   int H, int N, int K, int seg_tiles,
                                                                   const float* __restrict__ state, float eps,
-                                                                  float* dstate, float* dlq, IO* __restrict__ dQ) {
+                                                                  float* dstate, int dsplits, float* dlq,
+                                                                  IO* __restrict__ dQ) {
   constexpr int RK = KC / 32;
   extern __shared__ float sm[];
   float* S = sm;            // [KC][kSP]  Vt image
@@ -761,7 +775,10 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_query_kernel(const IO* __re
     __syncthreads();
     dx_tile_kc<IO, KC>(xs, G, nvalid, wpair + (size_t)h * K * kD, K, gs, dQ + ((size_t)unit * N + t0) * kD);
   }
-  store_gt<KC>(dstate + unit * npairs, K, acc, zacc, 1);
+  if (dsplits > 0)
+    store_gt<KC>(dstate + ((size_t)unit * dsplits + blockIdx.x) * npairs, K, acc, zacc, 0);
+  else
+    store_gt<KC>(dstate + unit * npairs, K, acc, zacc, 1);
 }
 
 // Key side: grid (splits, B*H).  Pushes [dVt | dZ] back through the write: dV, dK and dl_K.  Warp w owns
@@ -1125,12 +1142,15 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_causal_key_kernel(
 // batch entry, 2 B N in all) are split into ranges of rows_per_cta; a CTA walks its range in tiles of at
 // most T rows that stay within one (side, batch entry) and loads the next tile into registers while it
 // works on the current one.  Thread (k within a block of 32, group of 8 dims) sums dl_k (x_d - mu_kd)
-// and dl_k (x_d - mu_kd)^2 and adds them into pacc[h][k][d][2] (and b_k into pb[h][k]).
+// and dl_k (x_d - mu_kd)^2 and adds them into pacc[h][k][d][2] (and b_k into pb[h][k]); with zstride > 0
+// (the deterministic reduction mode) it stores them instead into the slice of its row range, at
+// pacc + blockIdx.z * zstride (and pb + blockIdx.z * zstride).
 template <typename IO>
 __global__ void __launch_bounds__(kThreads) simt_bwd_param_kernel(const IO* __restrict__ Q, const IO* __restrict__ Kx,
                                                                   const float* __restrict__ mu, const float* dlq,
                                                                   const float* dlk, int B, int H, int N, int K,
-                                                                  long long rows_per_cta, float* pacc, float* pb) {
+                                                                  long long rows_per_cta, float* pacc, float* pb,
+                                                                  size_t zstride) {
   __shared__ __align__(16) float xs[T * kD];
   __shared__ float ds[T * 32];
   const int h = blockIdx.y, k0 = blockIdx.x * 32;
@@ -1192,7 +1212,13 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_param_kernel(const IO* __re
       }
     }
   }
-  if (k < K) {
+  if (k < K && zstride > 0) {
+    const size_t zo = (size_t)blockIdx.z * zstride;
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      *reinterpret_cast<float2*>(pacc + zo + (((size_t)h * K + k) * kD + dg * 8 + q) * 2) = make_float2(a1[q], a2[q]);
+    if (dg == 0) pb[zo + (size_t)h * K + k] = bsum;
+  } else if (k < K) {
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       float* dst = pacc + (((size_t)h * K + k) * kD + dg * 8 + q) * 2;
@@ -1203,13 +1229,23 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_param_kernel(const IO* __re
   }
 }
 
+// The parameter gradients from the sums; Z slices of sums zstride floats apart are added in slice order
+// first (Z = 1: the sums themselves).
 __global__ void simt_bwd_param_finish_kernel(const float* __restrict__ sigma2, const float* pacc, const float* pb, int H,
-                                             int K, float* dmu, float* dsigma2, float* dlog_pi) {
+                                             int K, int Z, size_t zstride, float* dmu, float* dsigma2,
+                                             float* dlog_pi) {
   const size_t n = (size_t)H * K * kD;
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
-    const float w = 1.0f / sigma2[i], b = pb[i / kD];
-    dmu[i] = pacc[2 * i] * w;
-    dsigma2[i] = 0.5f * w * (pacc[2 * i + 1] * w - b);
+    float s1 = pacc[2 * i], s2 = pacc[2 * i + 1], b = pb[i / kD];
+    for (int z = 1; z < Z; ++z) {
+      const size_t zo = (size_t)z * zstride;
+      s1 += pacc[zo + 2 * i];
+      s2 += pacc[zo + 2 * i + 1];
+      b += pb[zo + i / kD];
+    }
+    const float w = 1.0f / sigma2[i];
+    dmu[i] = s1 * w;
+    dsigma2[i] = 0.5f * w * (s2 * w - b);
     if (i % kD == 0) dlog_pi[i / kD] = b;
   }
 }
@@ -1457,11 +1493,17 @@ __global__ void __launch_bounds__(kDecodeThreads) simt_decode_kernel(const IO* _
 // parameters | segment aggregates of the keys (scanned: S at each segment start) | segment aggregates of
 // the queries' gamma_Q u^T (suffix-scanned: R after each segment) | parameter sums | u rows | dl of the
 // queries | dl of the keys (gamma_K until the key side) | pairs | gamma_Q.
+// Deterministic reduction mode, after these: the per-CTA partials of Vt|Z and of dVt|dZ (bidirectional
+// only; one area, used by the two in turn) and pz slices of the parameter sums (pacc then pb, one slice
+// per range of rows).
+constexpr int kParamSlices = 16;
 struct BwdPlan {
-  size_t off_params, off_state, off_dstate, off_pacc, off_pb, off_u, off_dlq, off_dlk, off_wpair, off_gq, total;
-  int splits, seg_tiles, tiles;
+  size_t off_params, off_state, off_dstate, off_pacc, off_pb, off_u, off_dlq, off_dlk, off_wpair, off_gq;
+  size_t off_part, off_ppart, pstride, total;  // pstride: floats per slice of the parameter sums
+  int splits, seg_tiles, tiles, pz;
+  bool det;
 };
-BwdPlan bwd_plan(const gma_problem_t& p, bool causal) {
+BwdPlan bwd_plan(const gma_problem_t& p, bool causal, bool det) {
   BwdPlan b{};
   const SimtPlan sp = simt_plan(p, causal ? GMA_OP_CAUSAL : GMA_OP_BIDIR);
   const size_t BH = (size_t)p.B * p.H, npairs = (size_t)p.K * kStateCols;
@@ -1488,6 +1530,16 @@ BwdPlan bwd_plan(const gma_problem_t& p, bool causal) {
   b.off_wpair = align_up(b.off_dlk + BH * p.N * p.K * sizeof(float));
   b.off_gq = align_up(b.off_wpair + (size_t)p.H * p.K * kD * sizeof(float2));
   b.total = align_up(b.off_gq + (causal ? BH * p.N * p.K * sizeof(float) : 0));
+  b.det = det;
+  b.pz = 1;
+  b.pstride = ((size_t)p.H * p.K * (2 * kD + 1) + 3) / 4 * 4;  // 16-byte slices (float2 stores)
+  b.off_part = b.off_ppart = b.total;
+  if (det) {
+    b.off_ppart = align_up(b.off_part + (causal ? 0 : BH * b.splits * npairs * sizeof(float)));
+    const long long rows = 2LL * p.B * p.N;
+    b.pz = (int)std::max(1LL, std::min<long long>(kParamSlices, (rows + T - 1) / T));
+    b.total = align_up(b.off_ppart + (size_t)b.pz * b.pstride * sizeof(float));
+  }
   return b;
 }
 
@@ -1532,24 +1584,45 @@ gma_status_t launch_write(int splits, int BH, cudaStream_t st, const IO* Kx, con
 
 // Bidirectional backward after the parameter fold: write (Vt | Z), the query side, the key side; each
 // loop sized to fill the GPU.
+// part (the deterministic reduction mode, else null): the write and the query side store per-CTA partials
+// there, with the plan's splits, and each is summed in a fixed order.
 template <typename IO, int KC>
-gma_status_t backward_bidir_kc(const gma_problem_t& p, const IO* Q, const IO* Kx, const IO* V, const IO* dO, IO* dQ,
-                               IO* dK, IO* dV, float* params, const float2* wpair, float* state, float* dstate,
-                               float* dlq, float* dlk, cudaStream_t st) {
-  const int BH = p.B * p.H, K = p.K, tiles = cdiv(p.N, T);
+gma_status_t backward_bidir_kc(const gma_problem_t& p, const BwdPlan& b, const IO* Q, const IO* Kx, const IO* V,
+                               const IO* dO, IO* dQ, IO* dK, IO* dV, float* params, const float2* wpair, float* state,
+                               float* dstate, float* dlq, float* dlk, float* part, cudaStream_t st) {
+  const int BH = p.B * p.H, K = p.K, tiles = cdiv(p.N, T), npairs = K * kStateCols;
   int splits = 1, seg = 1;
   const size_t sm_w = (size_t)(T * kD + T * kDv + T * KC) * sizeof(float);
   const auto wfn = simt_write_kernel<IO, KC>;
-  if (gma_status_t e = fill_splits((const void*)wfn, sm_w, BH, tiles, &splits, &seg)) return e;
-  if (gma_status_t e = launch_write_kc<IO, KC>(splits, BH, st, Kx, V, params, p.H, p.N, K, seg, state, 1, dlk))
-    return e;
+  if (part) {
+    if (gma_status_t e = launch_write_kc<IO, KC>(b.splits, BH, st, Kx, V, params, p.H, p.N, K, b.seg_tiles, part, 0,
+                                                 dlk))
+      return e;
+    GMA_LAUNCH("simt_state_sum", simt_state_sum_kernel, dim3(cdiv(npairs, 256), BH), 256, 0, st, part, b.splits,
+               npairs, state);
+    if (gma_status_t e = check_launch("launch simt_state_sum", (const void*)simt_state_sum_kernel)) return e;
+  } else {
+    if (gma_status_t e = fill_splits((const void*)wfn, sm_w, BH, tiles, &splits, &seg)) return e;
+    if (gma_status_t e = launch_write_kc<IO, KC>(splits, BH, st, Kx, V, params, p.H, p.N, K, seg, state, 1, dlk))
+      return e;
+  }
   const size_t sm_q = (size_t)(KC * kSP + KC + T * kD + T * kDv + T * kSP + T + T * KC) * sizeof(float);
   const auto qfn = simt_bwd_query_kernel<IO, KC>;
   if (set_smem_optin((const void*)qfn, (int)sm_q, 5) != GMA_OK) return GMA_ERR_CUDA;
-  if (gma_status_t e = fill_splits((const void*)qfn, sm_q, BH, tiles, &splits, &seg)) return e;
+  if (part) {
+    splits = b.splits;
+    seg = b.seg_tiles;
+  } else if (gma_status_t e = fill_splits((const void*)qfn, sm_q, BH, tiles, &splits, &seg)) {
+    return e;
+  }
   GMA_LAUNCH("simt_bwd_query", qfn, dim3(splits, BH), kThreads, sm_q, st, Q, dO, params, wpair, p.H, p.N, K, seg,
-             state, p.eps, dstate, dlq, dQ);
+             state, p.eps, part ? part : dstate, part ? splits : 0, dlq, dQ);
   if (gma_status_t e = check_launch("launch simt_bwd_query", (const void*)qfn)) return e;
+  if (part) {
+    GMA_LAUNCH("simt_state_sum", simt_state_sum_kernel, dim3(cdiv(npairs, 256), BH), 256, 0, st, part, splits, npairs,
+               dstate);
+    if (gma_status_t e = check_launch("launch simt_state_sum", (const void*)simt_state_sum_kernel)) return e;
+  }
   const size_t sm_k = (size_t)(KC * kSP + KC + T * kD + T * kDv + T * KC) * sizeof(float);
   const auto kkfn = simt_bwd_key_kernel<IO, KC>;
   if (set_smem_optin((const void*)kkfn, (int)sm_k, 6) != GMA_OK) return GMA_ERR_CUDA;
@@ -1593,8 +1666,8 @@ gma_status_t backward_causal_kc(const gma_problem_t& p, const BwdPlan& b, const 
 template <typename IO>
 gma_status_t backward_typed(const gma_problem_t& p, bool causal, const IO* Q, const IO* Kx, const IO* V,
                             const float* mu, const float* sigma2, const float* log_pi, const IO* dO, IO* dQ, IO* dK,
-                            IO* dV, float* dmu, float* dsigma2, float* dlog_pi, void* ws, cudaStream_t st) {
-  const BwdPlan b = bwd_plan(p, causal);
+                            IO* dV, float* dmu, float* dsigma2, float* dlog_pi, void* ws, cudaStream_t st, bool det) {
+  const BwdPlan b = bwd_plan(p, causal, det);
   char* base = (char*)ws;
   float* params = (float*)(base + b.off_params);
   float* state = (float*)(base + b.off_state);
@@ -1606,6 +1679,8 @@ gma_status_t backward_typed(const gma_problem_t& p, bool causal, const IO* Q, co
   float* dlk = (float*)(base + b.off_dlk);
   float2* wpair = (float2*)(base + b.off_wpair);
   float* gq = (float*)(base + b.off_gq);
+  float* part = det && !causal ? (float*)(base + b.off_part) : nullptr;
+  float* ppart = (float*)(base + b.off_ppart);
   const int K = p.K;
   // bidirectional: zero Vt|Z, dVt|dZ and the parameter sums; causal: the parameter sums (the segment
   // aggregates are stored whole)
@@ -1614,6 +1689,7 @@ gma_status_t backward_typed(const gma_problem_t& p, bool causal, const IO* Q, co
   GMA_LAUNCH("simt_prep", simt_prep_kernel, 148, 256, 0, st, mu, sigma2, log_pi, p.H, K, params, (Ctrl*)base, zero,
              zero_n, wpair);
   if (gma_status_t e = check_launch("launch simt_prep", (const void*)simt_prep_kernel)) return e;
+  int pz_used = 1;  // slices of the parameter sums the finish adds up (1: the zeroed or atomic sums)
   if (p.N > 0) {
     if (causal) {
       gma_status_t e;
@@ -1639,53 +1715,69 @@ gma_status_t backward_typed(const gma_problem_t& p, bool causal, const IO* Q, co
       gma_status_t e;
       switch (kc_class(K)) {
         case 32:
-          e = backward_bidir_kc<IO, 32>(p, Q, Kx, V, dO, dQ, dK, dV, params, wpair, state, dstate, dlq, dlk, st);
+          e = backward_bidir_kc<IO, 32>(p, b, Q, Kx, V, dO, dQ, dK, dV, params, wpair, state, dstate, dlq, dlk, part,
+                                        st);
           break;
         case 64:
-          e = backward_bidir_kc<IO, 64>(p, Q, Kx, V, dO, dQ, dK, dV, params, wpair, state, dstate, dlq, dlk, st);
+          e = backward_bidir_kc<IO, 64>(p, b, Q, Kx, V, dO, dQ, dK, dV, params, wpair, state, dstate, dlq, dlk, part,
+                                        st);
           break;
         case 128:
-          e = backward_bidir_kc<IO, 128>(p, Q, Kx, V, dO, dQ, dK, dV, params, wpair, state, dstate, dlq, dlk, st);
+          e = backward_bidir_kc<IO, 128>(p, b, Q, Kx, V, dO, dQ, dK, dV, params, wpair, state, dstate, dlq, dlk, part,
+                                        st);
           break;
         default:
-          e = backward_bidir_kc<IO, 256>(p, Q, Kx, V, dO, dQ, dK, dV, params, wpair, state, dstate, dlq, dlk, st);
+          e = backward_bidir_kc<IO, 256>(p, b, Q, Kx, V, dO, dQ, dK, dV, params, wpair, state, dstate, dlq, dlk, part,
+                                        st);
       }
       if (e != GMA_OK) return e;
     }
-    // parameter sums: one wave of CTAs over the 2 B N rows of every head
-    int dev = 0, nsm = 0, occ = 0;
+    // parameter sums: one wave of CTAs over the 2 B N rows of every head (deterministic: the plan's pz
+    // ranges of rows, each stored into its own slice)
     const auto pfn = simt_bwd_param_kernel<IO>;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, pfn, kThreads, 0) != cudaSuccess)
-      return cuda_fail("occupancy query", cudaSuccess, (const void*)pfn);
     const long long rows = 2LL * p.B * p.N;
-    const int per_head = cdiv(K, 32) * p.H;
-    long long ctas = (long long)nsm * (occ > 0 ? occ : 1) / per_head;
-    ctas = ctas < 1 ? 1 : (ctas > 65535 ? 65535 : ctas);
+    long long ctas = b.pz;
+    if (!det) {
+      int dev = 0, nsm = 0, occ = 0;
+      if (cudaGetDevice(&dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, pfn, kThreads, 0) != cudaSuccess)
+        return cuda_fail("occupancy query", cudaSuccess, (const void*)pfn);
+      const int per_head = cdiv(K, 32) * p.H;
+      ctas = (long long)nsm * (occ > 0 ? occ : 1) / per_head;
+      ctas = ctas < 1 ? 1 : (ctas > 65535 ? 65535 : ctas);
+    }
     long long rows_per_cta = (rows + ctas - 1) / ctas;
     rows_per_cta = (rows_per_cta + T - 1) / T * T;
-    const dim3 grid_p(cdiv(K, 32), p.H, (unsigned)((rows + rows_per_cta - 1) / rows_per_cta));
+    const int zc = (int)((rows + rows_per_cta - 1) / rows_per_cta);  // <= pz when det
+    const dim3 grid_p(cdiv(K, 32), p.H, (unsigned)zc);
+    if (det) {
+      pacc = ppart;
+      pb = ppart + (size_t)p.H * K * kD * 2;
+    }
     GMA_LAUNCH("simt_bwd_param", pfn, grid_p, kThreads, 0, st, Q, Kx, mu, dlq, dlk, p.B, p.H, p.N, K, rows_per_cta,
-               pacc, pb);
+               pacc, pb, det ? b.pstride : (size_t)0);
     if (gma_status_t e = check_launch("launch simt_bwd_param", (const void*)simt_bwd_param_kernel<IO>)) return e;
+    if (det) pz_used = zc;
   }
-  GMA_LAUNCH("simt_bwd_param_finish", simt_bwd_param_finish_kernel, 148, 256, 0, st, sigma2, pacc, pb, p.H, K, dmu,
-             dsigma2, dlog_pi);
+  GMA_LAUNCH("simt_bwd_param_finish", simt_bwd_param_finish_kernel, 148, 256, 0, st, sigma2, pacc, pb, p.H, K, pz_used,
+             b.pstride, dmu, dsigma2, dlog_pi);
   return check_launch("launch simt_bwd_param_finish", (const void*)simt_bwd_param_finish_kernel);
 }
 
-size_t simt_backward_bytes(const gma_problem_t& p, bool causal) { return bwd_plan(p, causal).total; }
+size_t simt_backward_bytes(const gma_problem_t& p, bool causal, bool det) { return bwd_plan(p, causal, det).total; }
 
 gma_status_t simt_backward(const gma_problem_t& p, bool causal, const void* Q, const void* K, const void* V,
                            const float* mu, const float* sigma2, const float* log_pi, const void* dO, void* dQ,
-                           void* dK, void* dV, float* dmu, float* dsigma2, float* dlog_pi, void* ws, cudaStream_t st) {
+                           void* dK, void* dV, float* dmu, float* dsigma2, float* dlog_pi, void* ws, cudaStream_t st,
+                           bool det) {
   if (p.dtype == GMA_F32)
     return backward_typed<float>(p, causal, (const float*)Q, (const float*)K, (const float*)V, mu, sigma2, log_pi,
-                                 (const float*)dO, (float*)dQ, (float*)dK, (float*)dV, dmu, dsigma2, dlog_pi, ws, st);
+                                 (const float*)dO, (float*)dQ, (float*)dK, (float*)dV, dmu, dsigma2, dlog_pi, ws, st,
+                                 det);
   using bf = __nv_bfloat16;
   return backward_typed<bf>(p, causal, (const bf*)Q, (const bf*)K, (const bf*)V, mu, sigma2, log_pi, (const bf*)dO,
-                            (bf*)dQ, (bf*)dK, (bf*)dV, dmu, dsigma2, dlog_pi, ws, st);
+                            (bf*)dQ, (bf*)dK, (bf*)dV, dmu, dsigma2, dlog_pi, ws, st, det);
 }
 
 // Decode T new tokens per (b, h) from `state` (float32 [B*H][K][dv + 1], updated in place).  Two launches:
@@ -1745,8 +1837,8 @@ namespace {
 template <typename IO>
 gma_status_t run_typed(const gma_problem_t& p, gma_op_t op, int Nk, const IO* Q, const IO* Kx, const IO* V,
                        const float* mu, const float* sigma2, const float* log_pi, void* out, void* ws,
-                       cudaStream_t st) {
-  const SimtPlan pl = simt_plan(p, op);
+                       cudaStream_t st, bool det) {
+  const SimtPlan pl = simt_plan(p, op, det);
   char* base = (char*)ws;
   Ctrl* ctrl = (Ctrl*)base;
   float* params = (float*)(base + pl.off_params);
@@ -1772,8 +1864,17 @@ gma_status_t run_typed(const gma_problem_t& p, gma_op_t op, int Nk, const IO* Q,
       gma_problem_t pk = p;
       pk.N = Nk;
       const SimtPlan plk = simt_plan(pk, op);
-      if (gma_status_t e = launch_write<IO>(plk.splits, BH, st, Kx, V, params, p.H, Nk, K, plk.seg_tiles, state, 1))
+      if (pl.det) {  // each write CTA stores its own state; one fixed-order sum per element
+        float* part = (float*)(base + pl.off_agg);
+        if (gma_status_t e = launch_write<IO>(plk.splits, BH, st, Kx, V, params, p.H, Nk, K, plk.seg_tiles, part, 0))
+          return e;
+        GMA_LAUNCH("simt_state_sum", simt_state_sum_kernel, dim3(cdiv(npairs, 256), BH), 256, 0, st, part, plk.splits,
+                   npairs, state);
+        if (gma_status_t e = check_launch("launch simt_state_sum", (const void*)simt_state_sum_kernel)) return e;
+      } else if (gma_status_t e = launch_write<IO>(plk.splits, BH, st, Kx, V, params, p.H, Nk, K, plk.seg_tiles,
+                                                   state, 1)) {
         return e;
+      }
     }
     if (write_only) {  // the accumulator already has the public state layout [B*H][K][dv + 1]
       if (cudaMemcpyAsync(out, state, (size_t)BH * npairs * sizeof(float), cudaMemcpyDeviceToDevice, st) != cudaSuccess)
@@ -1801,8 +1902,9 @@ gma_status_t run_typed(const gma_problem_t& p, gma_op_t op, int Nk, const IO* Q,
 
 }  // namespace
 
-SimtPlan simt_plan(const gma_problem_t& p, gma_op_t op) {
+SimtPlan simt_plan(const gma_problem_t& p, gma_op_t op, bool det) {
   SimtPlan pl{};
+  pl.det = det;
   const int BH = p.B * p.H;
   pl.tiles = cdiv(p.N, T);
   int want = cdiv(kTargetUnits, BH);
@@ -1818,18 +1920,23 @@ SimtPlan simt_plan(const gma_problem_t& p, gma_op_t op) {
   if (op == GMA_OP_BIDIR || op == GMA_OP_CROSS || op == GMA_OP_CAUSAL_STATE)
     state_bytes = (size_t)BH * p.K * kStateCols * sizeof(float);
   if (op == GMA_OP_CAUSAL) state_bytes = (size_t)BH * pl.splits * p.K * kStateCols * sizeof(float);
-  pl.total = align_up(pl.off_state + state_bytes);
+  pl.off_agg = align_up(pl.off_state + state_bytes);
+  size_t agg_bytes = 0;
+  // the write's own plan over the key length: B*H * splits <= B*H * ceil(kTargetUnits / (B*H))
+  if (det && (op == GMA_OP_BIDIR || op == GMA_OP_CROSS || op == GMA_OP_CAUSAL_STATE))
+    agg_bytes = ((size_t)kTargetUnits + BH) * p.K * kStateCols * sizeof(float);
+  pl.total = align_up(pl.off_agg + agg_bytes);
   return pl;
 }
 
 gma_status_t simt_run(const gma_problem_t& p, gma_op_t op, int Nk, const void* Q, const void* K, const void* V,
                       const float* mu, const float* sigma2, const float* log_pi, void* out, void* ws,
-                      cudaStream_t stream) {
+                      cudaStream_t stream, bool det) {
   if (p.dtype == GMA_F32)
     return run_typed<float>(p, op, Nk, (const float*)Q, (const float*)K, (const float*)V, mu, sigma2, log_pi, out, ws,
-                            stream);
+                            stream, det);
   return run_typed<__nv_bfloat16>(p, op, Nk, (const __nv_bfloat16*)Q, (const __nv_bfloat16*)K, (const __nv_bfloat16*)V,
-                                  mu, sigma2, log_pi, out, ws, stream);
+                                  mu, sigma2, log_pi, out, ws, stream, det);
 }
 
 }  // namespace gma

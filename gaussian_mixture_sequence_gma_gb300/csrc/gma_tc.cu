@@ -25,6 +25,7 @@
 // part = warpgroup - 1).  The control warps hand registers to the row warps with setmaxnreg.
 #include <algorithm>
 #include <cstdio>
+#include <cstdlib>
 #include <mutex>
 
 #include "gma_tc_common.cuh"
@@ -1816,6 +1817,22 @@ __global__ void __launch_bounds__(128, 16) tc_scan_kernel(float* agg, int P, int
   }
 }
 
+// Deterministic reduction mode: the state state[bh][k][c] (c < 68) is the sum of the write CTAs' own
+// states agg[bh][s][c][k] (column-major, s = 0 .. P-1), added in the order of s by one thread per
+// element; grid (ceil(68 Kp / 128), B*H).  The pad columns 65 .. 67 are written as zero.
+__global__ void __launch_bounds__(128, 16) tc_state_sum_kernel(const float* agg, int P, int Kp, float* state) {
+  dep_wait();         // the per-CTA states are complete
+  dep_launch_next();  // the read sets itself up meanwhile and waits for this grid before reading
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;  // c * Kp + k
+  if (e >= kStRow * Kp) return;
+  const int c = e / Kp, k = e - c * Kp;
+  const float* src = agg + (size_t)blockIdx.y * P * kStCols * Kp + e;
+  float s = 0.f;
+  if (c <= kDv)
+    for (int q = 0; q < P; ++q) s += __ldcg(src + (size_t)q * kStCols * Kp);
+  state[((size_t)blockIdx.y * Kp + k) * kStRow + c] = s;
+}
+
 // Public causal state [B*H][K][dv + 1] from the write accumulator [B*H][Kp][68] (columns 0..64).
 __global__ void tc_state_export_kernel(const float* __restrict__ acc, int K, int Kp, size_t n, float* __restrict__ out) {
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
@@ -1975,10 +1992,29 @@ gma_status_t tc_launch(const gma_problem_t& p, gma_op_t op, int Nk, const TcPlan
     aw.splits = plk.splits;
     if (!make_map(&mk, K, BH, Nk) || !make_map(&mv, V, BH, Nk)) return GMA_ERR_CUDA;
     const uint32_t smem_w = smem_bytes(write_layout(pl.Kp).total);
-    if (set_smem_optin((const void*)tc_write_kernel<true, NC>, (int)smem_w, 0) != GMA_OK) return GMA_ERR_CUDA;
-    GMA_LAUNCH_DEPENDENT("tc_bidir_write", (tc_write_kernel<true, NC>), dim3(plk.splits, BH), kThreadsTc, smem_w, st,
-                         mk, mv, aw);
-    if (gma_status_t e = check_launch("launch tc_bidir_write", (const void*)tc_write_kernel<true, NC>)) return e;
+    if (pl.det) {
+      // deterministic: every write CTA stores its own state, then one fixed-order sum per element; at
+      // most one wave of CTAs (max(152, B*H) states in all, whatever the key length)
+      const int cap = std::max(1, kTargetCtas / BH);
+      if (aw.splits > cap) {
+        aw.seg_tiles = cdiv(aw.tiles, cap);
+        aw.splits = cdiv(aw.tiles, aw.seg_tiles);
+      }
+      aw.state = (float*)((char*)ws + pl.off_agg);
+      if (set_smem_optin((const void*)tc_write_kernel<false, NC>, (int)smem_w, 0) != GMA_OK) return GMA_ERR_CUDA;
+      GMA_LAUNCH_DEPENDENT("tc_bidir_write", (tc_write_kernel<false, NC>), dim3(aw.splits, BH), kThreadsTc, smem_w,
+                           st, mk, mv, aw);
+      if (gma_status_t e = check_launch("launch tc_bidir_write", (const void*)tc_write_kernel<false, NC>)) return e;
+      if (set_carveout_max((const void*)tc_state_sum_kernel) != GMA_OK) return GMA_ERR_CUDA;
+      GMA_LAUNCH_DEPENDENT("tc_state_sum", tc_state_sum_kernel, dim3(cdiv(kStRow * pl.Kp, 128), BH), 128, 0, st,
+                           (const float*)aw.state, aw.splits, pl.Kp, a.state);
+      if (gma_status_t e = check_launch("launch tc_state_sum", (const void*)tc_state_sum_kernel)) return e;
+    } else {
+      if (set_smem_optin((const void*)tc_write_kernel<true, NC>, (int)smem_w, 0) != GMA_OK) return GMA_ERR_CUDA;
+      GMA_LAUNCH_DEPENDENT("tc_bidir_write", (tc_write_kernel<true, NC>), dim3(plk.splits, BH), kThreadsTc, smem_w,
+                           st, mk, mv, aw);
+      if (gma_status_t e = check_launch("launch tc_bidir_write", (const void*)tc_write_kernel<true, NC>)) return e;
+    }
   }
   if (op == GMA_OP_CAUSAL_STATE) return GMA_OK;  // the state alone
   a.fault = 0;
@@ -1995,8 +2031,9 @@ std::mutex g_fault_mu;
 
 }  // namespace
 
-TcPlan tc_plan(const gma_problem_t& p, gma_op_t op) {
+TcPlan tc_plan(const gma_problem_t& p, gma_op_t op, bool det) {
   TcPlan t{};
+  t.det = det;
   const int BH = p.B * p.H;
   t.Kp = p.K <= 64 ? 64 : (p.K <= 128 ? 128 : 256);  // = 4 NC: every row thread's logit columns are written
   t.tiles = cdiv(p.N, kTile);
@@ -2010,14 +2047,19 @@ TcPlan tc_plan(const gma_problem_t& p, gma_op_t op) {
   size_t st = 0;
   if (op == GMA_OP_BIDIR || op == GMA_OP_CROSS || op == GMA_OP_CAUSAL_STATE) st = (size_t)BH * t.Kp * kStRow * 4;
   if (op == GMA_OP_CAUSAL) st = (size_t)BH * t.splits * t.Kp * kStCols * 4;  // segment aggregates
-  t.total = align_up(t.off_state + st);
+  t.off_agg = align_up(t.off_state + st);
+  size_t agg = 0;
+  // the deterministic write makes at most max(152, B*H) CTAs over any key length
+  if (det && (op == GMA_OP_BIDIR || op == GMA_OP_CROSS || op == GMA_OP_CAUSAL_STATE))
+    agg = (size_t)std::max(kTargetCtas, BH) * t.Kp * kStCols * 4;
+  t.total = align_up(t.off_agg + agg);
   return t;
 }
 
 gma_status_t tc_run(const gma_problem_t& p, gma_op_t op, int Nk, const void* Q, const void* K, const void* V,
                     const float* mu, const float* sigma2, const float* log_pi, void* out, void* ws,
-                    cudaStream_t st, bool clear_err) {
-  const TcPlan pl = tc_plan(p, op);
+                    cudaStream_t st, bool clear_err, bool det) {
+  const TcPlan pl = tc_plan(p, op, det);
   const int BH = p.B * p.H;
   char* base = (char*)ws;
   TcArgs a{};
@@ -2038,6 +2080,14 @@ gma_status_t tc_run(const gma_problem_t& p, gma_op_t op, int Nk, const void* Q, 
   a.wait_ns = wait_limit_ns();
   if (op == GMA_OP_BIDIR) {
     std::lock_guard<std::mutex> lock(g_fault_mu);
+    // GMA_FAULT_INJECT, read at the first bidirectional call of the process: a value other than "" or "0"
+    // arms the withheld-load hook for that call
+    static bool env_seen = false;
+    if (!env_seen) {
+      env_seen = true;
+      const char* e = std::getenv("GMA_FAULT_INJECT");
+      if (e && *e && !(e[0] == '0' && e[1] == 0)) g_fault_next |= 1u;
+    }
     a.fault = g_fault_next;
     g_fault_next = 0;
   }

@@ -23,7 +23,8 @@ EXPORTED = ("gma_workspace_bytes", "gma_responsibilities", "gma_forward_bidir", 
             "gma_forward_projected",
             "gma_check_device_error", "gma_status_string", "gma_version", "gma_last_error", "gma_launch_count", "gma_profile_enable",
             "gma_profile_read", "gma_forward_bidir_static_ws", "gma_static_ws_capacity", "gma_static_ws_check_error",
-            "gma_debug_withhold_first_load", "gma_probe_ex2_rate", "gma_set_wait_limit_ns", "gma_get_wait_limit_ns")
+            "gma_debug_withhold_first_load", "gma_probe_ex2_rate", "gma_set_wait_limit_ns", "gma_get_wait_limit_ns",
+            "gma_set_deterministic", "gma_get_deterministic")
 
 
 class GmaError(RuntimeError):
@@ -109,6 +110,10 @@ def lib():
     L.gma_set_wait_limit_ns.restype = ctypes.c_int
     L.gma_get_wait_limit_ns.argtypes = []
     L.gma_get_wait_limit_ns.restype = ctypes.c_uint64
+    L.gma_set_deterministic.argtypes = [ctypes.c_int]
+    L.gma_set_deterministic.restype = ctypes.c_int
+    L.gma_get_deterministic.argtypes = []
+    L.gma_get_deterministic.restype = ctypes.c_int
     L.gma_launch_count.argtypes = []
     L.gma_launch_count.restype = ctypes.c_ulonglong
     L.gma_profile_enable.argtypes = [ctypes.c_int]
@@ -454,6 +459,20 @@ def set_wait_limit_ns(ns: int) -> None:
 
 def wait_limit_ns() -> int:
     return int(lib().gma_get_wait_limit_ns())
+
+
+def set_deterministic(mode: int) -> None:
+    """Process-wide deterministic reduction mode: 1 on, 0 off, -1 the default (GMA_DETERMINISTIC).
+
+    With it on, sums across CTAs are taken in a fixed order and repeated calls give bitwise-equal
+    outputs; workspaces grow, so a workspace sized before the switch may be too small."""
+    st = int(lib().gma_set_deterministic(int(mode)))
+    if st != GMA_OK:
+        raise GmaError(st, "gma_set_deterministic")
+
+
+def deterministic() -> bool:
+    return bool(lib().gma_get_deterministic())
 
 
 def launch_count() -> int:

@@ -336,6 +336,34 @@ GMA_API gma_status_t gma_check_device_error(void *ws, void *stream);
 GMA_API gma_status_t gma_set_wait_limit_ns(uint64_t ns);
 GMA_API uint64_t gma_get_wait_limit_ns(void);
 
+/*
+ * Deterministic reduction mode, process-wide.  By default the bidirectional
+ * write (gma_forward_bidir / gma_forward_cross / gma_causal_state and the
+ * projected bidirectional form) adds the partial states of its CTAs into one
+ * [K][dv + 1] state per head with float32 atomic (bf16 path: bulk reduce-add)
+ * operations, and the backward pass does the same for the state gradient and
+ * the parameter sums, so repeated calls agree within rounding but not bit for
+ * bit.  The pages fix no summation order: every order computes the same sums of
+ * the write (the linear-time form of "Latent memory routing").  With the mode
+ * on, each CTA stores its partial in the workspace and one thread per element
+ * adds them up in CTA order, and the float32 projection's library GEMM uses no
+ * split-K reduction, so repeated calls with the same inputs, workspace size
+ * and device give bitwise-equal outputs.  The causal forward, the
+ * responsibilities and the decode already sum in a fixed order in both modes.
+ * The mode enlarges the workspaces of the affected calls (query
+ * gma_workspace_bytes() after setting it): by max(152, B*H) x Kp x 80 floats
+ * (bf16 forward, whose write then runs at most one CTA per SM; Kp = K rounded
+ * up to 64, 128 or 256), (304 + B*H) x K x 65 floats (float32 forward), or the
+ * backward's partials.  A call whose
+ * workspace was sized with the mode off fails with GMA_ERR_WORKSPACE when the
+ * mode is on.  mode: 1 on, 0 off, -1 the default, which is on when the
+ * environment variable GMA_DETERMINISTIC (read once) is set to anything but
+ * "" or "0".  Other values: GMA_ERR_INVALID_ARG.  gma_get_deterministic()
+ * returns 1 if the next call will use the mode, else 0.
+ */
+GMA_API gma_status_t gma_set_deterministic(int mode);
+GMA_API int gma_get_deterministic(void);
+
 /* Static, NUL-terminated description of a status code. */
 GMA_API const char *gma_status_string(gma_status_t s);
 

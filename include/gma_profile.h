@@ -47,6 +47,8 @@ GMA_API gma_status_t gma_probe_ex2_rate(void *stream, double *exps_per_second);
  * after their limit (about one second), the kernel records the timeout in the workspace error word
  * and every CTA exits normally, releasing its tensor memory.  gma_check_device_error() on that
  * workspace then returns GMA_ERR_TIMEOUT.  Nothing traps or faults; the context stays usable.
+ * Setting the environment variable GMA_FAULT_INJECT (to anything but "" or "0") before the first
+ * bf16 bidirectional call of the process has the same effect on that call.
  */
 GMA_API void gma_debug_withhold_first_load(void);
 

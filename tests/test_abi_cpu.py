@@ -399,3 +399,58 @@ def test_wait_limit_environment_variable():
                              timeout=120)
         assert out.returncode == 0, out.stderr
         assert int(out.stdout.strip().splitlines()[-1]) == want, ms
+
+
+def _align(x, a=256):
+    return -(-x // a) * a
+
+
+def test_deterministic_mode_setter_and_workspace(L):
+    """The deterministic reduction mode: 1 / 0 / -1 (the default), others refused; with it on, the
+    workspaces of the calls whose sums cross CTAs grow by their documented partials and the others
+    do not change."""
+    assert L.gma_set_deterministic(-1) == gma.GMA_OK
+    default = L.gma_get_deterministic()
+    env = os.environ.get("GMA_DETERMINISTIC", "")
+    assert default == (1 if env not in ("", "0") else 0)
+    try:
+        assert L.gma_set_deterministic(0) == gma.GMA_OK
+        off = {(op, dt): gma.workspace_bytes(P(B=2, H=3, N=4096, K=100, dtype=dt), op)
+               for op in range(9) for dt in (gma.GMA_F32, gma.GMA_BF16)}
+        assert L.gma_set_deterministic(1) == gma.GMA_OK
+        assert L.gma_get_deterministic() == 1 and gma.deterministic()
+        on = {(op, dt): gma.workspace_bytes(P(B=2, H=3, N=4096, K=100, dtype=dt), op)
+              for op in range(9) for dt in (gma.GMA_F32, gma.GMA_BF16)}
+        BH, K, kp = 6, 100, 128
+        for op in (gma.OP_BIDIR, gma.OP_CROSS, gma.OP_CAUSAL_STATE):
+            # bf16: one 80-column state per write CTA, at most max(152, B*H) CTAs
+            assert on[op, gma.GMA_BF16] == _align(off[op, gma.GMA_BF16]) + _align(max(152, BH) * kp * 80 * 4)
+            # float32: one 65-column state per write CTA, at most 304 + B*H CTAs
+            assert on[op, gma.GMA_F32] == _align(off[op, gma.GMA_F32]) + _align((304 + BH) * K * 65 * 4)
+        for dt in (gma.GMA_F32, gma.GMA_BF16):
+            for op in (gma.OP_RESPONSIBILITIES, gma.OP_CAUSAL, gma.OP_CAUSAL_DECODE):
+                assert on[op, dt] == off[op, dt], op
+            for op in (gma.OP_BACKWARD_BIDIR, gma.OP_BACKWARD_CAUSAL, gma.OP_PROJECTED_BIDIR):
+                assert on[op, dt] > off[op, dt], op
+        # the key length does not enter the deterministic workspace either
+        assert gma.workspace_bytes(P(N=1 << 20), gma.OP_BIDIR) == gma.workspace_bytes(P(N=128), gma.OP_BIDIR)
+        for bad in (2, -2, 100):
+            assert L.gma_set_deterministic(bad) == gma.GMA_ERR_INVALID_ARG
+        assert L.gma_get_deterministic() == 1
+        with pytest.raises(gma.GmaError):
+            gma.set_deterministic(5)
+    finally:
+        assert L.gma_set_deterministic(-1) == gma.GMA_OK
+    assert L.gma_get_deterministic() == default
+
+
+def test_deterministic_environment_variable():
+    """GMA_DETERMINISTIC sets the default of a fresh process: anything but "" or "0" turns it on."""
+    code = ("from gaussian_mixture_sequence_gma_gb300 import gma; print(int(gma.deterministic()))")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    for val, want in (("1", 1), ("yes", 1), ("0", 0), ("", 0)):
+        env = dict(os.environ, GMA_DETERMINISTIC=val)
+        out = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True, text=True,
+                             timeout=120)
+        assert out.returncode == 0, out.stderr
+        assert int(out.stdout.strip().splitlines()[-1]) == want, val

@@ -6,6 +6,9 @@ limit (about a second), record GMA_ERR_TIMEOUT in the workspace error word, and 
 through the common exit that releases its tensor memory.  Nothing traps or faults, so the context
 stays usable: the next call on the same workspace runs normally and passes parity.
 """
+import os
+import subprocess
+import sys
 import time
 
 import numpy as np
@@ -67,3 +70,34 @@ def test_short_wait_limit_reports_sooner():
     assert gma.check_device_error(ws) == gma.GMA_OK
     ref = orc.forward(inp["Q"], inp["K"], inp["V"], inp["mu"], inp["sigma2"], inp["log_pi"], 1e-6)
     assert rel_err(O, ref) <= TOL["bf16"]
+
+
+def test_fault_inject_environment_variable():
+    """GMA_FAULT_INJECT arms the withheld load for the first bf16 bidirectional call of a fresh process:
+    that call reports GMA_ERR_TIMEOUT (20 ms wait limit), the next one is normal and passes parity."""
+    code = """
+import numpy as np, torch
+from gaussian_mixture_sequence_gma_gb300 import gma
+from gaussian_mixture_sequence_gma_gb300.inputs import make_inputs
+from oracle import oracle as orc
+from tests.helpers import rel_err, to_device
+inp = make_inputs(1, 2, 512, 64, dtype="bf16", seed=23)
+t = to_device(inp)
+args = (t["Q"], t["K"], t["V"], t["mu"], t["sigma2"], t["log_pi"])
+ws = gma.alloc_workspace(gma.problem(1, 2, 512, 64, torch.bfloat16, 1e-6), gma.OP_BIDIR, "cuda")
+gma.forward_bidir(*args, workspace=ws)
+first = gma.check_device_error(ws)
+O = gma.forward_bidir(*args, workspace=ws).float().cpu().numpy()
+second = gma.check_device_error(ws)
+ref = orc.forward(inp["Q"], inp["K"], inp["V"], inp["mu"], inp["sigma2"], inp["log_pi"], 1e-6)
+print(first, second, rel_err(O, ref))
+"""
+    from gaussian_mixture_sequence_gma_gb300 import gma
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, GMA_FAULT_INJECT="1", GMA_WAIT_LIMIT_MS="20")
+    out = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True, text=True, timeout=300)
+    assert out.returncode == 0, out.stderr[-2000:]
+    first, second, err = out.stdout.strip().splitlines()[-1].split()
+    assert int(first) == gma.GMA_ERR_TIMEOUT
+    assert int(second) == gma.GMA_OK
+    assert float(err) <= TOL["bf16"]
