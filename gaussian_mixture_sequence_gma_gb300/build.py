@@ -17,6 +17,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libgma.so")
+# bounds-check debug build: the same sources with -DGMA_BOUNDS_CHECK (see gma_debug_bounds_read)
+LIB_CHECKED = os.path.join(OUT_DIR, "libgma_checked.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "-I", INCLUDE, "-I", CSRC]
@@ -40,11 +42,14 @@ def _stale(out: str, deps: list[str]) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False, checked: bool = False) -> str:
+    """libgma.so, or (checked) its bounds-check debug variant libgma_checked.so."""
     srcs = sources()
     headers = glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh")) + \
         glob.glob(os.path.join(INCLUDE, "*.h"))
-    obj_dir = os.path.join(OUT_DIR, "obj")
+    obj_dir = os.path.join(OUT_DIR, "obj_checked" if checked else "obj")
+    lib = LIB_CHECKED if checked else LIB
+    extra = ["-DGMA_BOUNDS_CHECK"] if checked else []
     os.makedirs(obj_dir, exist_ok=True)
     procs = []
     objs = []
@@ -52,7 +57,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
         o = os.path.join(obj_dir, os.path.basename(s)[:-3] + ".o")
         objs.append(o)
         if force or _stale(o, [s] + headers + [__file__]):
-            cmd = [nvcc()] + ARCH + FLAGS + (["-Xptxas", "-v"] if ptxas_info else []) + ["-c", s, "-o", o]
+            cmd = [nvcc()] + ARCH + FLAGS + extra + (["-Xptxas", "-v"] if ptxas_info else []) + ["-c", s, "-o", o]
             procs.append((s, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)))
     failed = []
     for s, p in procs:
@@ -63,16 +68,25 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
             failed.append(s)
     if failed:
         raise RuntimeError("nvcc failed for: " + ", ".join(failed))
-    if force or procs or _stale(LIB, objs):
-        tmp = LIB + ".tmp%d" % os.getpid()
+    if force or procs or _stale(lib, objs):
+        tmp = lib + ".tmp%d" % os.getpid()
         # shared cudart: the library joins the CUDA runtime the host process (e.g. torch) already uses,
         # so the current device and stream handles are the same on both sides of the ABI
         cmd = [nvcc()] + ARCH + ["-shared", "-cudart", "shared", "-Xlinker", "-rpath=/usr/local/cuda/lib64",
                                  "-o", tmp] + objs + ["-lcublasLt"]
         subprocess.run(cmd, check=True)
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
+
+
+def build_all(force: bool = False) -> list[str]:
+    """libgma.so and libgma_checked.so, their translation units compiled concurrently."""
+    import concurrent.futures as cf
+    with cf.ThreadPoolExecutor(2) as ex:
+        futs = [ex.submit(build, force, False, False, checked) for checked in (False, True)]
+        return [f.result() for f in futs]
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv,
+                checked="--checked" in sys.argv))

@@ -105,6 +105,13 @@ gma_status_t proj_run(const gma_problem_t& p, int dm, const void* X, const void*
 // (anything but "" or "0") sets it for the first bidirectional call of the process.
 void tc_set_fault_injection(uint32_t mask);
 
+// Bounds-check debug build (-DGMA_BOUNDS_CHECK): the per-translation-unit records of failed checks
+// (first site, its index and extent, failures), copied to h[4] and optionally cleared, and a kernel that
+// fails one check on purpose without touching memory.  GMA_ERR_UNSUPPORTED in the normal build.
+gma_status_t tc_bounds_io(unsigned long long* h, bool clear);
+gma_status_t simt_bounds_io(unsigned long long* h, bool clear);
+gma_status_t bounds_selftest(cudaStream_t st);
+
 // NVTX range for the lifetime of the object (one per C-ABI call).
 struct NvtxScope {
   explicit NvtxScope(const char* name);

@@ -129,6 +129,26 @@ gma_status_t gma_profile_enable(int on) {
   return GMA_OK;
 }
 
+gma_status_t gma_debug_bounds_read(unsigned long long* out) {
+  if (!out) return GMA_ERR_INVALID_ARG;
+  unsigned long long rec[2][4] = {};
+  if (gma_status_t e = gma::tc_bounds_io(rec[0], false)) return e;
+  if (gma_status_t e = gma::simt_bounds_io(rec[1], false)) return e;
+  const unsigned long long* first = rec[0][0] ? rec[0] : rec[1];
+  out[0] = first[0];
+  out[1] = first[1];
+  out[2] = first[2];
+  out[3] = rec[0][3] + rec[1][3];
+  return GMA_OK;
+}
+
+gma_status_t gma_debug_bounds_clear(void) {
+  if (gma_status_t e = gma::tc_bounds_io(nullptr, true)) return e;
+  return gma::simt_bounds_io(nullptr, true);
+}
+
+gma_status_t gma_debug_bounds_selftest(void* stream) { return gma::bounds_selftest((cudaStream_t)stream); }
+
 int gma_profile_read(char* buf, size_t len) {
   std::lock_guard<std::mutex> lock(g_mu);
   std::map<std::string, std::pair<int, double>> agg;

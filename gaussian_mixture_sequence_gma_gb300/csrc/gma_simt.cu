@@ -13,6 +13,8 @@
 // cancels in the softmax.
 #include <cuda_bf16.h>
 
+#include <climits>
+
 #include "gma_internal.h"
 #include "gma_tc_common.cuh"
 
@@ -86,12 +88,12 @@ __global__ void simt_prep_kernel(const float* __restrict__ mu, const float* __re
 }
 
 // Loads `n` valid rows (of 64) starting at row `r0` of a [rows][64] matrix into smem as float32;
-// rows past `n` are zero.
+// rows past `n` are zero.  rows: the matrix's row count, checked in the bounds-check build.
 template <typename IO>
-__device__ __forceinline__ void load_rows(const IO* __restrict__ src, int r0, int n, float* dst) {
+__device__ __forceinline__ void load_rows(const IO* __restrict__ src, int r0, int n, float* dst, int rows = INT_MAX) {
   for (int i = threadIdx.x; i < T * kD; i += blockDim.x) {
     const int r = i / kD;
-    dst[i] = r < n ? ld_io<IO>(src + (size_t)(r0 + r) * kD + (i % kD)) : 0.f;
+    dst[i] = r < n && GMA_INB(r0 + r, rows, 201) ? ld_io<IO>(src + (size_t)(r0 + r) * kD + (i % kD)) : 0.f;
   }
 }
 
@@ -286,14 +288,17 @@ __device__ __forceinline__ void load_tile_rows(const float* src, int nvalid, int
 }
 
 // Writes (or adds, atomic != 0) the register blocks of accumulate_gt into a [K][dv + 1] state at dst.
+// off, lim (checked in the bounds-check build): dst's offset in its buffer, and the buffer's extent.
 template <int KC>
-__device__ __forceinline__ void store_gt(float* dst, int K, const float (&acc)[KC / 8][2], float z, int atomic) {
+__device__ __forceinline__ void store_gt(float* dst, int K, const float (&acc)[KC / 8][2], float z, int atomic,
+                                         size_t off = 0, size_t lim = ~(size_t)0) {
   constexpr int KW = KC / 8;
   const int lane = threadIdx.x & 31, k0 = (threadIdx.x >> 5) * KW;
 #pragma unroll
   for (int q = 0; q < KW; ++q) {
     if (k0 + q >= K) break;
     float* row = dst + (size_t)(k0 + q) * kStateCols;
+    if (!GMA_INB(off + (size_t)(k0 + q + 1) * kStateCols - 1, lim, 210)) continue;
     if (atomic) {
       atomicAdd(row + lane, acc[q][0]);
       atomicAdd(row + 32 + lane, acc[q][1]);
@@ -302,7 +307,7 @@ __device__ __forceinline__ void store_gt(float* dst, int K, const float (&acc)[K
       row[32 + lane] = acc[q][1];
     }
   }
-  if (lane < KW && k0 + lane < K) {
+  if (lane < KW && k0 + lane < K && GMA_INB(off + (size_t)(k0 + lane) * kStateCols + kDv, lim, 210)) {
     float* zp = dst + (size_t)(k0 + lane) * kStateCols + kDv;
     if (atomic) atomicAdd(zp, z); else *zp = z;
   }
@@ -320,11 +325,12 @@ __global__ void __launch_bounds__(kThreads) simt_resp_kernel(const IO* __restric
   const int t0 = blockIdx.x * T;
   const int nvalid = min(T, N - t0);
   const SimtParams P = params_at(params, H, K);
-  load_rows<IO>(X + (size_t)unit * N * kD, t0, nvalid, xs);
+  load_rows<IO>(X + (size_t)unit * N * kD, t0, nvalid, xs, N);
   __syncthreads();
   gamma_tile(xs, nvalid, P, h, K, G);
   float* out = gamma + ((size_t)unit * N + t0) * K;
-  for (int i = threadIdx.x; i < nvalid * K; i += blockDim.x) out[i] = G[i];
+  for (int i = threadIdx.x; i < nvalid * K; i += blockDim.x)
+    if (GMA_INB(((size_t)unit * N + t0) * K + i, (size_t)gridDim.y * N * K, 213)) out[i] = G[i];
 }
 
 // Eight consecutive elements of a row as float32 (one 16-byte load for bf16, two for float32).
@@ -349,11 +355,11 @@ __device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* __rest
 // A tile's share of one thread of 256: row r = tid / 8, elements 8 (tid % 8) .. + 7 of rows [r0, r0 + n)
 // of a [rows][64] matrix (zero past n), and its store into a [T][64] shared-memory tile.
 template <typename IO>
-__device__ __forceinline__ void fetch_tile8(const IO* __restrict__ src, int r0, int n, float (&v)[8]) {
+__device__ __forceinline__ void fetch_tile8(const IO* __restrict__ src, int r0, int n, float (&v)[8], int rows = INT_MAX) {
   const int r = threadIdx.x >> 3, c = 8 * (threadIdx.x & 7);
 #pragma unroll
   for (int t = 0; t < 8; ++t) v[t] = 0.f;
-  if (r < n) load8<IO>(src + (size_t)(r0 + r) * kD + c, v);
+  if (r < n && GMA_INB(r0 + r, rows, 202)) load8<IO>(src + (size_t)(r0 + r) * kD + c, v);
 }
 __device__ __forceinline__ void put_tile8(float* dst, const float (&v)[8]) {
   float* d = dst + (threadIdx.x >> 3) * kD + 8 * (threadIdx.x & 7);
@@ -368,7 +374,8 @@ __device__ __forceinline__ void put_tile8(float* dst, const float (&v)[8]) {
 template <typename IO, int KC>
 __global__ void __launch_bounds__(kThreads, KC <= 128 ? 2 : 1) simt_write_kernel(const IO* __restrict__ Kx, const IO* __restrict__ V,
                                                               float* params, int H, int N, int K, int seg_tiles,
-                                                              int splits, float* state, int atomic, float* gout) {
+                                                              int splits, float* state, int atomic, float* gout,
+                                                              size_t state_lim) {
   extern __shared__ float sm[];
   float* xs = sm;           // [T][64]
   float* vs = xs + T * kD;  // [T][64]
@@ -384,8 +391,8 @@ __global__ void __launch_bounds__(kThreads, KC <= 128 ? 2 : 1) simt_write_kernel
   const IO* vb = V + (size_t)unit * N * kDv;
   float xk[8], xv[8];  // the next tile's key and value rows, loaded while the current one is worked on
   if (tb < te) {
-    fetch_tile8<IO>(kb, tb * T, min(T, N - tb * T), xk);
-    fetch_tile8<IO>(vb, tb * T, min(T, N - tb * T), xv);
+    fetch_tile8<IO>(kb, tb * T, min(T, N - tb * T), xk, N);
+    fetch_tile8<IO>(vb, tb * T, min(T, N - tb * T), xv, N);
   }
   for (int t = tb; t < te; ++t) {
     const int t0 = t * T, nvalid = min(T, N - t0);
@@ -393,8 +400,8 @@ __global__ void __launch_bounds__(kThreads, KC <= 128 ? 2 : 1) simt_write_kernel
     put_tile8(vs, xv);
     __syncthreads();
     if (t + 1 < te) {
-      fetch_tile8<IO>(kb, t0 + T, min(T, N - t0 - T), xk);
-      fetch_tile8<IO>(vb, t0 + T, min(T, N - t0 - T), xv);
+      fetch_tile8<IO>(kb, t0 + T, min(T, N - t0 - T), xk, N);
+      fetch_tile8<IO>(vb, t0 + T, min(T, N - t0 - T), xv, N);
     }
     gamma_tile_kc<KC>(xs, nvalid, P, h, K, G);
     accumulate_gt<KC>(G, vs, kDv, nullptr, acc, z);
@@ -402,15 +409,15 @@ __global__ void __launch_bounds__(kThreads, KC <= 128 ? 2 : 1) simt_write_kernel
     __syncthreads();
   }
   const size_t npairs = (size_t)K * kStateCols;
-  store_gt<KC>(atomic ? state + (size_t)unit * npairs : state + ((size_t)unit * splits + split) * npairs, K, acc, z,
-               atomic);
+  const size_t off = atomic ? (size_t)unit * npairs : ((size_t)unit * splits + split) * npairs;
+  store_gt<KC>(state + off, K, acc, z, atomic, off, state_lim);
 }
 
 // Read phase (bidirectional): grid (tiles, B*H).
 template <typename IO>
 __global__ void __launch_bounds__(kThreads) simt_read_kernel(const IO* __restrict__ Q, float* params, int H, int N,
                                                              int K, const float* __restrict__ state, float eps,
-                                                             IO* __restrict__ O) {
+                                                             IO* __restrict__ O, size_t state_lim) {
   extern __shared__ float sm[];
   float* xs = sm;
   float* G = xs + T * kD;
@@ -418,44 +425,50 @@ __global__ void __launch_bounds__(kThreads) simt_read_kernel(const IO* __restric
   const int unit = blockIdx.y, h = unit % H;
   const int t0 = blockIdx.x * T, nvalid = min(T, N - t0);
   const SimtParams P = params_at(params, H, K);
-  load_rows<IO>(Q + (size_t)unit * N * kD, t0, nvalid, xs);
+  load_rows<IO>(Q + (size_t)unit * N * kD, t0, nvalid, xs, N);
   __syncthreads();
   gamma_tile(xs, nvalid, P, h, K, G);
   const float* S = state + (size_t)unit * K * kStateCols;
   for (int p = threadIdx.x; p < T * kStateCols; p += blockDim.x) {
     const int i = p / kStateCols, c = p % kStateCols;
     float s = 0.f;
-    for (int k = 0; k < K; ++k) s = fmaf(G[i * K + k], __ldg(S + k * kStateCols + c), s);
+    for (int k = 0; k < K; ++k)
+      if (GMA_INB((size_t)unit * K * kStateCols + k * kStateCols + c, state_lim, 211))
+        s = fmaf(G[i * K + k], __ldg(S + k * kStateCols + c), s);
     num[p] = s;
   }
   __syncthreads();
   IO* out = O + ((size_t)unit * N + t0) * kDv;
   for (int p = threadIdx.x; p < nvalid * kDv; p += blockDim.x) {
     const int i = p / kDv, c = p % kDv;
-    st_io<IO>(out + p, num[i * kStateCols + c] / (num[i * kStateCols + kDv] + eps));
+    if (GMA_INB(((size_t)unit * N + t0) * kDv + p, (size_t)gridDim.y * N * kDv, 212))
+      st_io<IO>(out + p, num[i * kStateCols + c] / (num[i * kStateCols + kDv] + eps));
   }
 }
 
 // Deterministic reduction mode: state[unit][e] = sum over p = 0 .. P-1 of part[unit][p][e], added in the
 // order of p.  grid (ceil(npairs / 256), B*H).
-__global__ void simt_state_sum_kernel(const float* __restrict__ part, int P, int npairs, float* __restrict__ state) {
+__global__ void simt_state_sum_kernel(const float* __restrict__ part, int P, int npairs, float* __restrict__ state,
+                                      size_t part_lim, size_t state_lim) {
   const int unit = blockIdx.y;
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= npairs) return;
   const float* src = part + (size_t)unit * P * npairs + e;
   float s = 0.f;
-  for (int p = 0; p < P; ++p) s += src[(size_t)p * npairs];
-  state[(size_t)unit * npairs + e] = s;
+  for (int p = 0; p < P; ++p)
+    if (GMA_INB(((size_t)unit * P + p) * npairs + e, part_lim, 215)) s += src[(size_t)p * npairs];
+  if (GMA_INB((size_t)unit * npairs + e, state_lim, 216)) state[(size_t)unit * npairs + e] = s;
 }
 
 // Exclusive scan over segments: agg[unit][p][e] <- sum_{p' < p} agg[unit][p'][e].  grid (ceil(K*65/256), B*H).
-__global__ void simt_scan_kernel(float* agg, int P, int npairs) {
+__global__ void simt_scan_kernel(float* agg, int P, int npairs, size_t lim) {
   const int unit = blockIdx.y;
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= npairs) return;
   float* base = agg + (size_t)unit * P * npairs + e;
   float run = 0.f;
   for (int p = 0; p < P; ++p) {
+    if (!GMA_INB(((size_t)unit * P + p) * npairs + e, lim, 214)) continue;
     const float t = base[(size_t)p * npairs];
     base[(size_t)p * npairs] = run;
     run += t;
@@ -469,7 +482,7 @@ template <typename IO>
 __global__ void __launch_bounds__(kThreads) simt_causal_kernel(const IO* __restrict__ Q, const IO* __restrict__ Kx,
                                                                const IO* __restrict__ V, float* params, int H, int N,
                                                                int K, int seg_tiles, int P, const float* agg,
-                                                               float eps, IO* __restrict__ O) {
+                                                               float eps, IO* __restrict__ O, size_t agg_lim) {
   extern __shared__ float sm[];
   const int npairs = K * kStateCols;
   float* S = sm;                 // [K][65]
@@ -482,17 +495,18 @@ __global__ void __launch_bounds__(kThreads) simt_causal_kernel(const IO* __restr
   const int unit = blockIdx.y, h = unit % H, seg = blockIdx.x;
   const SimtParams Pp = params_at(params, H, K);
   const float* S0 = agg + ((size_t)unit * P + seg) * npairs;
-  for (int p = threadIdx.x; p < npairs; p += blockDim.x) S[p] = S0[p];
+  for (int p = threadIdx.x; p < npairs; p += blockDim.x)
+    S[p] = GMA_INB(((size_t)unit * P + seg) * npairs + p, agg_lim, 217) ? S0[p] : 0.f;
   const int tiles = (N + T - 1) / T;
   const int tb = seg * seg_tiles, te = min(tiles, tb + seg_tiles);
   for (int t = tb; t < te; ++t) {
     const int t0 = t * T, nvalid = min(T, N - t0);
     __syncthreads();
-    load_rows<IO>(Q + (size_t)unit * N * kD, t0, nvalid, xs);
+    load_rows<IO>(Q + (size_t)unit * N * kD, t0, nvalid, xs, N);
     __syncthreads();
     gamma_tile(xs, nvalid, Pp, h, K, GQ);
-    load_rows<IO>(Kx + (size_t)unit * N * kD, t0, nvalid, xs);
-    load_rows<IO>(V + (size_t)unit * N * kDv, t0, nvalid, vs);
+    load_rows<IO>(Kx + (size_t)unit * N * kD, t0, nvalid, xs, N);
+    load_rows<IO>(V + (size_t)unit * N * kDv, t0, nvalid, vs, N);
     __syncthreads();
     gamma_tile(xs, nvalid, Pp, h, K, GK);
     // masked intra-tile affinity, j <= i inclusive
@@ -519,7 +533,8 @@ __global__ void __launch_bounds__(kThreads) simt_causal_kernel(const IO* __restr
     IO* out = O + ((size_t)unit * N + t0) * kDv;
     for (int p = threadIdx.x; p < nvalid * kDv; p += blockDim.x) {
       const int i = p / kDv, c = p % kDv;
-      st_io<IO>(out + p, num[i * kStateCols + c] / (num[i * kStateCols + kDv] + eps));
+      if (GMA_INB(((size_t)unit * N + t0) * kDv + p, (size_t)gridDim.y * N * kDv, 218))
+        st_io<IO>(out + p, num[i * kStateCols + c] / (num[i * kStateCols + kDv] + eps));
     }
     for (int p = threadIdx.x; p < npairs; p += blockDim.x) {
       const int k = p / kStateCols, c = p % kStateCols;
@@ -1562,23 +1577,26 @@ gma_status_t fill_splits(const void* func, size_t smem, int BH, int tiles, int* 
 // Write phase / segment aggregates (simt_write_kernel) for the KC class of K.
 template <typename IO, int KC>
 gma_status_t launch_write_kc(int splits, int BH, cudaStream_t st, const IO* Kx, const IO* V, float* params, int H,
-                             int N, int K, int seg_tiles, float* state, int atomic, float* gout = nullptr) {
+                             int N, int K, int seg_tiles, float* state, int atomic, float* gout = nullptr,
+                             size_t state_lim = ~(size_t)0) {
   const size_t sm = (size_t)(T * kD + T * kDv + T * KC) * sizeof(float);
   const auto kfn = simt_write_kernel<IO, KC>;
   if (set_smem_optin((const void*)kfn, (int)sm, 1) != GMA_OK) return GMA_ERR_CUDA;
   GMA_LAUNCH("simt_write", kfn, dim3(splits, BH), kThreads, sm, st, Kx, V, params, H, N, K, seg_tiles, splits,
-             state, atomic, gout);
+             state, atomic, gout, state_lim);
   return check_launch("launch simt_write", (const void*)kfn);
 }
 
 template <typename IO>
 gma_status_t launch_write(int splits, int BH, cudaStream_t st, const IO* Kx, const IO* V, float* params, int H, int N,
-                          int K, int seg_tiles, float* state, int atomic) {
+                          int K, int seg_tiles, float* state, int atomic, size_t lim) {
   switch (kc_class(K)) {
-    case 32: return launch_write_kc<IO, 32>(splits, BH, st, Kx, V, params, H, N, K, seg_tiles, state, atomic);
-    case 64: return launch_write_kc<IO, 64>(splits, BH, st, Kx, V, params, H, N, K, seg_tiles, state, atomic);
-    case 128: return launch_write_kc<IO, 128>(splits, BH, st, Kx, V, params, H, N, K, seg_tiles, state, atomic);
-    default: return launch_write_kc<IO, 256>(splits, BH, st, Kx, V, params, H, N, K, seg_tiles, state, atomic);
+    case 32: return launch_write_kc<IO, 32>(splits, BH, st, Kx, V, params, H, N, K, seg_tiles, state, atomic, nullptr, lim);
+    case 64: return launch_write_kc<IO, 64>(splits, BH, st, Kx, V, params, H, N, K, seg_tiles, state, atomic, nullptr, lim);
+    case 128:
+      return launch_write_kc<IO, 128>(splits, BH, st, Kx, V, params, H, N, K, seg_tiles, state, atomic, nullptr, lim);
+    default:
+      return launch_write_kc<IO, 256>(splits, BH, st, Kx, V, params, H, N, K, seg_tiles, state, atomic, nullptr, lim);
   }
 }
 
@@ -1599,7 +1617,7 @@ gma_status_t backward_bidir_kc(const gma_problem_t& p, const BwdPlan& b, const I
                                                  dlk))
       return e;
     GMA_LAUNCH("simt_state_sum", simt_state_sum_kernel, dim3(cdiv(npairs, 256), BH), 256, 0, st, part, b.splits,
-               npairs, state);
+               npairs, state, ~(size_t)0, ~(size_t)0);
     if (gma_status_t e = check_launch("launch simt_state_sum", (const void*)simt_state_sum_kernel)) return e;
   } else {
     if (gma_status_t e = fill_splits((const void*)wfn, sm_w, BH, tiles, &splits, &seg)) return e;
@@ -1620,7 +1638,7 @@ gma_status_t backward_bidir_kc(const gma_problem_t& p, const BwdPlan& b, const I
   if (gma_status_t e = check_launch("launch simt_bwd_query", (const void*)qfn)) return e;
   if (part) {
     GMA_LAUNCH("simt_state_sum", simt_state_sum_kernel, dim3(cdiv(npairs, 256), BH), 256, 0, st, part, splits, npairs,
-               dstate);
+               dstate, ~(size_t)0, ~(size_t)0);
     if (gma_status_t e = check_launch("launch simt_state_sum", (const void*)simt_state_sum_kernel)) return e;
   }
   const size_t sm_k = (size_t)(KC * kSP + KC + T * kD + T * kDv + T * KC) * sizeof(float);
@@ -1643,7 +1661,8 @@ gma_status_t backward_causal_kc(const gma_problem_t& p, const BwdPlan& b, const 
   if (gma_status_t e = launch_write_kc<IO, KC>(b.splits, BH, st, Kx, V, params, p.H, p.N, K, b.seg_tiles, state, 0,
                                                dlk))
     return e;
-  GMA_LAUNCH("simt_scan", simt_scan_kernel, dim3(cdiv(npairs, 256), BH), 256, 0, st, state, b.splits, npairs);
+  GMA_LAUNCH("simt_scan", simt_scan_kernel, dim3(cdiv(npairs, 256), BH), 256, 0, st, state, b.splits, npairs,
+             ~(size_t)0);
   if (gma_status_t e = check_launch("launch simt_scan", (const void*)simt_scan_kernel)) return e;
   const size_t sm_q =
       (size_t)(KC * kSP + KC + T * kD + T * kDv + 2 * T * kSP + T + T * KC + T * KG + 2 * T * T) * sizeof(float);
@@ -1840,6 +1859,8 @@ gma_status_t run_typed(const gma_problem_t& p, gma_op_t op, int Nk, const IO* Q,
                        cudaStream_t st, bool det) {
   const SimtPlan pl = simt_plan(p, op, det);
   char* base = (char*)ws;
+  // extents of the state section and of the partial states (checked by the bounds-check build)
+  const size_t state_lim = (pl.off_agg - pl.off_state) / sizeof(float), part_lim = (pl.total - pl.off_agg) / sizeof(float);
   Ctrl* ctrl = (Ctrl*)base;
   float* params = (float*)(base + pl.off_params);
   float* state = (float*)(base + pl.off_state);
@@ -1866,13 +1887,14 @@ gma_status_t run_typed(const gma_problem_t& p, gma_op_t op, int Nk, const IO* Q,
       const SimtPlan plk = simt_plan(pk, op);
       if (pl.det) {  // each write CTA stores its own state; one fixed-order sum per element
         float* part = (float*)(base + pl.off_agg);
-        if (gma_status_t e = launch_write<IO>(plk.splits, BH, st, Kx, V, params, p.H, Nk, K, plk.seg_tiles, part, 0))
+        if (gma_status_t e =
+                launch_write<IO>(plk.splits, BH, st, Kx, V, params, p.H, Nk, K, plk.seg_tiles, part, 0, part_lim))
           return e;
         GMA_LAUNCH("simt_state_sum", simt_state_sum_kernel, dim3(cdiv(npairs, 256), BH), 256, 0, st, part, plk.splits,
-                   npairs, state);
+                   npairs, state, part_lim, state_lim);
         if (gma_status_t e = check_launch("launch simt_state_sum", (const void*)simt_state_sum_kernel)) return e;
       } else if (gma_status_t e = launch_write<IO>(plk.splits, BH, st, Kx, V, params, p.H, Nk, K, plk.seg_tiles,
-                                                   state, 1)) {
+                                                   state, 1, state_lim)) {
         return e;
       }
     }
@@ -1883,24 +1905,29 @@ gma_status_t run_typed(const gma_problem_t& p, gma_op_t op, int Nk, const IO* Q,
     }
     const size_t sm_read = (size_t)(T * kD + T * K + T * kStateCols) * sizeof(float);
     if (set_smem_optin((const void*)simt_read_kernel<IO>, (int)sm_read, 2) != GMA_OK) return GMA_ERR_CUDA;
-    GMA_LAUNCH("simt_read", simt_read_kernel<IO>, dim3(pl.tiles, BH), kThreads, sm_read, st, Q, params, p.H, p.N, K, state, p.eps,
-                                                                        (IO*)out);
+    GMA_LAUNCH("simt_read", simt_read_kernel<IO>, dim3(pl.tiles, BH), kThreads, sm_read, st, Q, params, p.H, p.N, K,
+               state, p.eps, (IO*)out, state_lim);
     return cudaGetLastError() == cudaSuccess ? GMA_OK : GMA_ERR_CUDA;
   }
   // causal
-  if (gma_status_t e = launch_write<IO>(pl.splits, BH, st, Kx, V, params, p.H, p.N, K, pl.seg_tiles, state, 0))
+  if (gma_status_t e = launch_write<IO>(pl.splits, BH, st, Kx, V, params, p.H, p.N, K, pl.seg_tiles, state, 0, state_lim))
     return e;
-  GMA_LAUNCH("simt_scan", simt_scan_kernel, dim3(cdiv(npairs, 256), BH), 256, 0, st, state, pl.splits, npairs);
+  GMA_LAUNCH("simt_scan", simt_scan_kernel, dim3(cdiv(npairs, 256), BH), 256, 0, st, state, pl.splits, npairs, state_lim);
   if (cudaGetLastError() != cudaSuccess) return GMA_ERR_CUDA;
   const size_t sm_causal = (size_t)(npairs + T * kD + T * kDv + 2 * T * K + T * T + T * kStateCols) * sizeof(float);
   if (set_smem_optin((const void*)simt_causal_kernel<IO>, (int)sm_causal, 3) != GMA_OK) return GMA_ERR_CUDA;
-  GMA_LAUNCH("simt_causal", simt_causal_kernel<IO>, dim3(pl.splits, BH), kThreads, sm_causal, st, Q, Kx, V, params, p.H, p.N, K,
-                                                                           pl.seg_tiles, pl.splits, state, p.eps,
-                                                                           (IO*)out);
+  GMA_LAUNCH("simt_causal", simt_causal_kernel<IO>, dim3(pl.splits, BH), kThreads, sm_causal, st, Q, Kx, V, params, p.H,
+             p.N, K, pl.seg_tiles, pl.splits, state, p.eps, (IO*)out, state_lim);
   return cudaGetLastError() == cudaSuccess ? GMA_OK : GMA_ERR_CUDA;
 }
 
 }  // namespace
+
+#ifdef GMA_BOUNDS_CHECK
+gma_status_t simt_bounds_io(unsigned long long* h, bool clear) { return bounds_record_io(h, clear); }
+#else
+gma_status_t simt_bounds_io(unsigned long long*, bool) { return GMA_ERR_UNSUPPORTED; }
+#endif
 
 SimtPlan simt_plan(const gma_problem_t& p, gma_op_t op, bool det) {
   SimtPlan pl{};

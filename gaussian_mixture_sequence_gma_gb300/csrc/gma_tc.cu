@@ -111,6 +111,12 @@ struct Bars {
   Abort ab;
 };
 
+// Extents of the workspace sections and the output, as planned on the host (checked by the bounds-check
+// debug build only): state / out / c in floats, w in bytes, flags in words.
+struct TcLimits {
+  size_t state, out, w, c, flags;
+};
+
 struct TcArgs {
   const uint8_t* w_img;  // [H][w_head_bytes(Kp)] swizzled fp16 B operand of the log-density contraction
   const float* cbias;    // [H][256] c'_k (log2 domain); -inf past K
@@ -122,6 +128,9 @@ struct TcArgs {
   float eps;
   uint64_t wait_ns;
   uint32_t fault;  // bit 0: the producer never loads the first X tile (bounded-wait test hook)
+#ifdef GMA_BOUNDS_CHECK
+  TcLimits lim;  // only the checked build carries (and reads) the extents
+#endif
 };
 
 // ----------------------------------------------------------------------------------------------- prep
@@ -134,7 +143,8 @@ struct TcArgs {
 __global__ void __launch_bounds__(128, 16) tc_prep_kernel(const float* __restrict__ mu, const float* __restrict__ sigma2,
                                                       const float* __restrict__ log_pi, int H, int K, int Kp,
                                                       uint8_t* w_img, float* cbias, Ctrl* ctrl, float* zero,
-                                                      size_t zero_n, uint32_t* range_flags, int clear_err) {
+                                                      size_t zero_n, uint32_t* range_flags, int clear_err,
+                                                      TcLimits lim) {
   // Launched as a dependent of whatever precedes it on the stream: nothing is read or written before that
   // grid has completed (it may produce the parameters, or still read the previous call's W image).  The
   // 32-register bound lets a CTA of this grid sit beside a running tensor-core CTA meanwhile.
@@ -179,7 +189,8 @@ __global__ void __launch_bounds__(128, 16) tc_prep_kernel(const float* __restric
       if (!isfinite(val[2 * i]) || !isfinite(val[2 * i + 1])) bad = 1;
     }
   }
-  if (k < Kp)
+  if (k < Kp &&
+      GMA_INB((size_t)h * w_head_bytes(Kp) + sw128_off(k, 8 * q, (uint32_t)Kp * 128) + 15, lim.w, 101))
     *reinterpret_cast<uint4*>(w_img + (size_t)h * w_head_bytes(Kp) + sw128_off(k, 8 * q, (uint32_t)Kp * 128)) =
         make_uint4(w[0], w[1], w[2], w[3]);
   // c'_k = log pi_k log2(e) + sum_d a mu'^2 - 1/2 log2(e) sum_d log sigma2 (the two partial sums above, kept
@@ -191,8 +202,10 @@ __global__ void __launch_bounds__(128, 16) tc_prep_kernel(const float* __restric
     qsum += __shfl_xor_sync(0xffffffffu, qsum, o);
   }
   const float cprime = k < K ? log_pi[(size_t)h * K + k] * kLog2e + qsum - 0.5f * kLog2e * lsum : -INFINITY;
-  if (q == 0 && k < kCTable) cbias[(size_t)h * kCTable + k] = cprime;
-  if (q == 0 && k < Kp) {
+  if (q == 0 && k < kCTable && GMA_INB((size_t)h * kCTable + k, lim.c, 102)) cbias[(size_t)h * kCTable + k] = cprime;
+  if (q == 0 && k < Kp &&
+      GMA_INB((size_t)h * w_head_bytes(Kp) + (size_t)Kp * 256 + (size_t)max(sw32_chunk(k, 0), sw32_chunk(k, 1)) + 15,
+              lim.w, 103)) {
     // constant step of the contraction: [256 | 1] . [fp16(c'/256) | fp16(c' - 256 fp16(c'/256))] = c' to
     // about 2^-22 |c'| (-inf past K, so the padding components never win the row maximum)
     const __half hi = __float2half_rn(k < K ? cprime * (1.0f / 256.0f) : -INFINITY);
@@ -210,10 +223,12 @@ __global__ void __launch_bounds__(128, 16) tc_prep_kernel(const float* __restric
   // one flag per block, rewritten every call (so nothing needs clearing); the next kernel turns it
   // into the error word after this grid has completed
   const int any_bad = __syncthreads_or(bad);
-  if (threadIdx.x == 0) range_flags[blockIdx.y * gridDim.x + blockIdx.x] = any_bad ? 1u : 0u;
+  if (threadIdx.x == 0 && GMA_INB(blockIdx.y * gridDim.x + blockIdx.x, lim.flags, 104))
+    range_flags[blockIdx.y * gridDim.x + blockIdx.x] = any_bad ? 1u : 0u;
   const size_t tid = ((size_t)blockIdx.y * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x;
   const size_t nth = (size_t)gridDim.x * gridDim.y * blockDim.x;
-  for (size_t i = tid; i < zero_n; i += nth) zero[i] = 0.f;
+  for (size_t i = tid; i < zero_n; i += nth)
+    if (GMA_INB(i, lim.state, 105)) zero[i] = 0.f;
   if (threadIdx.x == 0) GMA_SPAN_AT(9);
 }
 
@@ -465,11 +480,13 @@ __device__ __forceinline__ void producer(const TcArgs& a, const CUtensorMap* tmX
   const int h = bh % a.H;
   // the parameter fold of this head (complete: this grid waited for it) flagged an fp16 overflow
   uint32_t bad = 0;
-  for (int i = 0; i < kCTable / 8; ++i) bad |= a.range_flags[h * (kCTable / 8) + i];
+  for (int i = 0; i < kCTable / 8; ++i)
+    if (GMA_INB(h * (kCTable / 8) + i, a.lim.flags, 110)) bad |= a.range_flags[h * (kCTable / 8) + i];
   if (bad) atomicCAS(&a.ctrl->err, kErrNone, kErrRange);
   mbar_expect_tx(&B->w_full, wbytes);
   for (uint32_t o = 0; o < wbytes; o += 32768)
-    bulk_load(smem + L.w + o, a.w_img + (size_t)h * wbytes + o, min(32768u, wbytes - o), &B->w_full);
+    if (GMA_INB((size_t)h * wbytes + o + min(32768u, wbytes - o) - 1, a.lim.w, 111))
+      bulk_load(smem + L.w + o, a.w_img + (size_t)h * wbytes + o, min(32768u, wbytes - o), &B->w_full);
   int issued[2] = {-1, -1};  // parity of the last phase armed on x_full[0], x_full[1]
   for (int u = 0; u <= T; ++u) {
     const int s = u & 1;
@@ -775,8 +792,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         if (threadIdx.x == 32 * kRowWarp0 && ok) {
           const uint32_t bytes = (uint32_t)a.Kp * kStRow * 4u, chunk = bytes / 4u;  // 16-byte multiples
           float* dst = a.state + (size_t)bh * a.Kp * kStRow;
-          for (uint32_t o = 0; o < bytes; o += chunk)
-            bulk_reduce_add_f32(reinterpret_cast<uint8_t*>(dst) + o, stage + o, chunk);
+          if (GMA_INB(((size_t)bh + 1) * a.Kp * kStRow - 1, a.lim.state, 112))
+            for (uint32_t o = 0; o < bytes; o += chunk)
+              bulk_reduce_add_f32(reinterpret_cast<uint8_t*>(dst) + o, stage + o, chunk);
           bulk_commit();
           bulk_wait_read_all();
         }
@@ -790,9 +808,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         for (int c = 0; c < 5; ++c) tmem_ld16(tmem + rc.lane_base + kColAcc + kStCols * rc.part + 16 * c, r + 16 * c);
         tmem_ld_wait();
         if (comp < a.Kp) {  // segment aggregate, column-major agg[bh][split][80][Kp]: each store covers 32 components
-          float* dst = a.state + ((size_t)bh * a.splits + split) * kStCols * a.Kp + comp;
+          const size_t i0 = ((size_t)bh * a.splits + split) * kStCols * a.Kp + comp;
+          float* dst = a.state + i0;
 #pragma unroll
-          for (int c = 0; c < kStCols; ++c) dst[(size_t)c * a.Kp] = __uint_as_float(r[c]);
+          for (int c = 0; c < kStCols; ++c)
+            if (GMA_INB(i0 + (size_t)c * a.Kp, a.lim.state, 113)) dst[(size_t)c * a.Kp] = __uint_as_float(r[c]);
         }
       }
     }
@@ -901,11 +921,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_resp_kernel(const __grid_con
       const float sum = xchg_sum(rc, 4, sp);
       if (ok && tok < a.N) {
         const float r = 1.0f / sum;
-        float* dst = reinterpret_cast<float*>(a.out) + ((size_t)bh * a.N + tok) * a.K + NC * rc.part;
+        const size_t i0 = ((size_t)bh * a.N + tok) * a.K + NC * rc.part;
+        float* dst = reinterpret_cast<float*>(a.out) + i0;
         const int nk = min(max(a.K - NC * rc.part, 0), NC);
 #pragma unroll
         for (int k = 0; k < NC; ++k)
-          if (k < nk) dst[k] = v[k] * r;
+          if (k < nk && GMA_INB(i0 + k, a.lim.out, 120)) dst[k] = v[k] * r;
       }
     }
   }
@@ -996,7 +1017,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     const uint32_t wbytes = w_head_bytes(a.Kp);
     mbar_expect_tx(&B.w_full, wbytes);
     for (uint32_t o = 0; o < wbytes; o += 32768)
-      bulk_load(smem + L.w + o, a.w_img + (size_t)(bh % a.H) * wbytes + o, min(32768u, wbytes - o), &B.w_full);
+      if (GMA_INB((size_t)(bh % a.H) * wbytes + o + min(32768u, wbytes - o) - 1, a.lim.w, 130))
+        bulk_load(smem + L.w + o, a.w_img + (size_t)(bh % a.H) * wbytes + o, min(32768u, wbytes - o), &B.w_full);
     for (int t = 0; t < 2 && t < T; ++t) {
       mbar_expect_tx(&B.x_full[t], 16384);
       tma_load_3d(smem + L.a0 + 32768 * t + 16384, &tmQ, 0, (tile0 + t) * kTile, bh, &B.x_full[t]);
@@ -1021,7 +1043,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const int it = i0 + u * nt, n = it % kStCols, c8 = it / kStCols;
         if (it < items) {
 #pragma unroll
-          for (int j = 0; j < 8; ++j) f[u][j] = n <= kDv ? __ldg(src + (size_t)(8 * c8 + j) * kStRow + n) : 0.f;
+          for (int j = 0; j < 8; ++j)
+            f[u][j] = n <= kDv && GMA_INB((size_t)bh * a.Kp * kStRow + (size_t)(8 * c8 + j) * kStRow + n, a.lim.state, 131)
+                          ? __ldg(src + (size_t)(8 * c8 + j) * kStRow + n)
+                          : 0.f;
         }
       }
 #pragma unroll
@@ -1435,8 +1460,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       const int h = bh % a.H;
       mbar_expect_tx(&B.w_full, wbytes + cbytes);
       for (uint32_t o = 0; o < wbytes; o += 32768)
-        bulk_load(smem + L.w + o, a.w_img + (size_t)h * w_head_bytes(a.Kp) + o, min(32768u, wbytes - o), &B.w_full);
-      bulk_load(smem + L.c, a.cbias + (size_t)h * kCTable, cbytes, &B.w_full);
+        if (GMA_INB((size_t)h * w_head_bytes(a.Kp) + o + min(32768u, wbytes - o) - 1, a.lim.w, 140))
+          bulk_load(smem + L.w + o, a.w_img + (size_t)h * w_head_bytes(a.Kp) + o, min(32768u, wbytes - o), &B.w_full);
+      if (GMA_INB((size_t)h * kCTable + kCTable - 1, a.lim.c, 141))
+        bulk_load(smem + L.c, a.cbias + (size_t)h * kCTable, cbytes, &B.w_full);
       int issued[3] = {-1, -1, -1};  // parity of the last load armed on xk_full, xq_full, v_full
       for (int t = 0; t < T; ++t) {
         const uint32_t pe = (t & 1) ^ 1;
@@ -1606,7 +1633,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         uint32_t r[48];
 #pragma unroll
         for (int i = 0; i < 48; ++i)
-          if (i < 16 * nc) r[i] = comp < a.Kp ? __float_as_uint(__ldg(pre + (size_t)(16 * c0 + i) * a.Kp)) : 0u;
+          if (i < 16 * nc)
+            r[i] = comp < a.Kp && GMA_INB(((size_t)bh * a.splits + seg) * kStCols * a.Kp + comp + (size_t)(16 * c0 + i) * a.Kp,
+                                          a.lim.state, 142)
+                       ? __float_as_uint(__ldg(pre + (size_t)(16 * c0 + i) * a.Kp))
+                       : 0u;
 #pragma unroll
         for (int c = 0; c < 3; ++c) {
           if (c < nc) {
@@ -1798,7 +1829,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 // Each thread has all loads of up to 32 segments in flight before the first store.
 // 128 threads of at most 32 registers, so that its CTAs fit beside a running aggregate CTA and start the
 // moment that grid completes.
-__global__ void __launch_bounds__(128, 16) tc_scan_kernel(float* agg, int P, int n) {
+__global__ void __launch_bounds__(128, 16) tc_scan_kernel(float* agg, int P, int n, size_t lim) {
   dep_wait();         // the aggregates are complete
   dep_launch_next();  // the sweep sets itself up meanwhile and waits for this grid before reading
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
@@ -1808,10 +1839,14 @@ __global__ void __launch_bounds__(128, 16) tc_scan_kernel(float* agg, int P, int
   for (int p0 = 0; p0 < P; p0 += 8) {
     float x[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) x[j] = (p0 + j < P) ? __ldcg(base + (size_t)(p0 + j) * n) : 0.f;
+    for (int j = 0; j < 8; ++j)
+      x[j] = (p0 + j < P) && GMA_INB(((size_t)blockIdx.y * P + p0 + j) * n + e, lim, 150)
+                 ? __ldcg(base + (size_t)(p0 + j) * n)
+                 : 0.f;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      if (p0 + j < P) __stcg(base + (size_t)(p0 + j) * n, run);
+      if (p0 + j < P && GMA_INB(((size_t)blockIdx.y * P + p0 + j) * n + e, lim, 150))
+        __stcg(base + (size_t)(p0 + j) * n, run);
       run += x[j];
     }
   }
@@ -1820,7 +1855,8 @@ __global__ void __launch_bounds__(128, 16) tc_scan_kernel(float* agg, int P, int
 // Deterministic reduction mode: the state state[bh][k][c] (c < 68) is the sum of the write CTAs' own
 // states agg[bh][s][c][k] (column-major, s = 0 .. P-1), added in the order of s by one thread per
 // element; grid (ceil(68 Kp / 128), B*H).  The pad columns 65 .. 67 are written as zero.
-__global__ void __launch_bounds__(128, 16) tc_state_sum_kernel(const float* agg, int P, int Kp, float* state) {
+__global__ void __launch_bounds__(128, 16) tc_state_sum_kernel(const float* agg, int P, int Kp, float* state,
+                                                               size_t lim_agg, size_t lim_state) {
   dep_wait();         // the per-CTA states are complete
   dep_launch_next();  // the read sets itself up meanwhile and waits for this grid before reading
   const int e = blockIdx.x * blockDim.x + threadIdx.x;  // c * Kp + k
@@ -1829,18 +1865,22 @@ __global__ void __launch_bounds__(128, 16) tc_state_sum_kernel(const float* agg,
   const float* src = agg + (size_t)blockIdx.y * P * kStCols * Kp + e;
   float s = 0.f;
   if (c <= kDv)
-    for (int q = 0; q < P; ++q) s += __ldcg(src + (size_t)q * kStCols * Kp);
-  state[((size_t)blockIdx.y * Kp + k) * kStRow + c] = s;
+    for (int q = 0; q < P; ++q)
+      if (GMA_INB((size_t)blockIdx.y * P * kStCols * Kp + e + (size_t)q * kStCols * Kp, lim_agg, 151))
+        s += __ldcg(src + (size_t)q * kStCols * Kp);
+  if (GMA_INB(((size_t)blockIdx.y * Kp + k) * kStRow + c, lim_state, 152))
+    state[((size_t)blockIdx.y * Kp + k) * kStRow + c] = s;
 }
 
 // Public causal state [B*H][K][dv + 1] from the write accumulator [B*H][Kp][68] (columns 0..64).
-__global__ void tc_state_export_kernel(const float* __restrict__ acc, int K, int Kp, size_t n, float* __restrict__ out) {
+__global__ void tc_state_export_kernel(const float* __restrict__ acc, int K, int Kp, size_t n, float* __restrict__ out,
+                                       size_t lim_acc) {
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
     const int c = (int)(i % (kDv + 1));
     const size_t rk = i / (kDv + 1);  // bh * K + k
     const int k = (int)(rk % K);
     const size_t bh = rk / K;
-    out[i] = acc[(bh * Kp + k) * kStRow + c];
+    if (GMA_INB((bh * Kp + k) * kStRow + c, lim_acc, 153)) out[i] = acc[(bh * Kp + k) * kStRow + c];
   }
 }
 
@@ -1971,7 +2011,8 @@ gma_status_t tc_launch(const gma_problem_t& p, gma_op_t op, int Nk, const TcPlan
     a.fault = 0;
     const int n = pl.Kp * kStCols;
     if (set_carveout_max((const void*)tc_scan_kernel) != GMA_OK) return GMA_ERR_CUDA;
-    GMA_LAUNCH_DEPENDENT("tc_causal_scan", tc_scan_kernel, dim3(cdiv(n, 128), BH), 128, 0, st, a.state, pl.splits, n);
+    GMA_LAUNCH_DEPENDENT("tc_causal_scan", tc_scan_kernel, dim3(cdiv(n, 128), BH), 128, 0, st, a.state, pl.splits, n,
+                         (pl.off_agg - pl.off_state) / 4);
     if (gma_status_t e = check_launch("launch tc_causal_scan", (const void*)tc_scan_kernel)) return e;
     const uint32_t smem_c = smem_bytes(causal_layout(pl.Kp).total);
     if (set_smem_optin((const void*)tc_causal_kernel<NC>, (int)smem_c, 0) != GMA_OK) return GMA_ERR_CUDA;
@@ -2001,13 +2042,17 @@ gma_status_t tc_launch(const gma_problem_t& p, gma_op_t op, int Nk, const TcPlan
         aw.splits = cdiv(aw.tiles, aw.seg_tiles);
       }
       aw.state = (float*)((char*)ws + pl.off_agg);
+      const size_t agg_lim = (pl.total - pl.off_agg) / 4;
+#ifdef GMA_BOUNDS_CHECK
+      aw.lim.state = agg_lim;
+#endif
       if (set_smem_optin((const void*)tc_write_kernel<false, NC>, (int)smem_w, 0) != GMA_OK) return GMA_ERR_CUDA;
       GMA_LAUNCH_DEPENDENT("tc_bidir_write", (tc_write_kernel<false, NC>), dim3(aw.splits, BH), kThreadsTc, smem_w,
                            st, mk, mv, aw);
       if (gma_status_t e = check_launch("launch tc_bidir_write", (const void*)tc_write_kernel<false, NC>)) return e;
       if (set_carveout_max((const void*)tc_state_sum_kernel) != GMA_OK) return GMA_ERR_CUDA;
       GMA_LAUNCH_DEPENDENT("tc_state_sum", tc_state_sum_kernel, dim3(cdiv(kStRow * pl.Kp, 128), BH), 128, 0, st,
-                           (const float*)aw.state, aw.splits, pl.Kp, a.state);
+                           (const float*)aw.state, aw.splits, pl.Kp, a.state, agg_lim, (pl.off_agg - pl.off_state) / 4);
       if (gma_status_t e = check_launch("launch tc_state_sum", (const void*)tc_state_sum_kernel)) return e;
     } else {
       if (set_smem_optin((const void*)tc_write_kernel<true, NC>, (int)smem_w, 0) != GMA_OK) return GMA_ERR_CUDA;
@@ -2078,6 +2123,15 @@ gma_status_t tc_run(const gma_problem_t& p, gma_op_t op, int Nk, const void* Q, 
   a.splits = pl.splits;
   a.eps = p.eps;
   a.wait_ns = wait_limit_ns();
+  TcLimits lim;
+  lim.state = (pl.off_agg - pl.off_state) / 4;
+  lim.out = op == GMA_OP_RESPONSIBILITIES ? (size_t)BH * p.N * p.K : 0;
+  lim.w = pl.off_c - pl.off_w;
+  lim.c = (pl.off_flags - pl.off_c) / 4;
+  lim.flags = (pl.off_state - pl.off_flags) / 4;
+#ifdef GMA_BOUNDS_CHECK
+  a.lim = lim;
+#endif
   if (op == GMA_OP_BIDIR) {
     std::lock_guard<std::mutex> lock(g_fault_mu);
     // GMA_FAULT_INJECT, read at the first bidirectional call of the process: a value other than "" or "0"
@@ -2095,7 +2149,8 @@ gma_status_t tc_run(const gma_problem_t& p, gma_op_t op, int Nk, const void* Q, 
   const size_t zero_n = with_state ? (size_t)BH * pl.Kp * kStRow : 0;
   if (set_carveout_max((const void*)tc_prep_kernel) != GMA_OK) return GMA_ERR_CUDA;
   GMA_LAUNCH_DEPENDENT("tc_prep", tc_prep_kernel, dim3(kCTable / 8, p.H), 128, 0, st, mu, sigma2, log_pi, p.H, p.K, pl.Kp,
-             (uint8_t*)a.w_img, (float*)a.cbias, a.ctrl, a.state, zero_n, (uint32_t*)a.range_flags, clear_err ? 1 : 0);
+             (uint8_t*)a.w_img, (float*)a.cbias, a.ctrl, a.state, zero_n, (uint32_t*)a.range_flags, clear_err ? 1 : 0,
+             lim);
   if (gma_status_t e = check_launch("launch tc_prep", (const void*)tc_prep_kernel)) return e;
   const int nc = pl.Kp <= 64 ? 16 : (pl.Kp <= 128 ? 32 : 64);  // components per row thread (4 per row)
   gma_status_t e = nc == 16   ? tc_launch<16>(p, op, Nk, pl, a, Q, K, V, ws, st)
@@ -2104,11 +2159,28 @@ gma_status_t tc_run(const gma_problem_t& p, gma_op_t op, int Nk, const void* Q, 
   if (e != GMA_OK || op != GMA_OP_CAUSAL_STATE) return e;
   const size_t n = (size_t)BH * p.K * (kDv + 1);
   GMA_LAUNCH("tc_state_export", tc_state_export_kernel, (unsigned)std::min<size_t>((n + 255) / 256, 4096), 256, 0, st,
-             a.state, p.K, pl.Kp, n, (float*)out);
+             a.state, p.K, pl.Kp, n, (float*)out, lim.state);
   return check_launch("launch tc_state_export", (const void*)tc_state_export_kernel);
 }
 
 bool tc_available() { return encode_fn() != nullptr; }
+
+#ifdef GMA_BOUNDS_CHECK
+namespace {
+// An index one past an extent of three, checked and skipped: no memory is touched.
+__global__ void bounds_selftest_kernel() {
+  if (GMA_INB(threadIdx.x + 3, 3, 999)) asm volatile("" ::: "memory");
+}
+}  // namespace
+gma_status_t tc_bounds_io(unsigned long long* h, bool clear) { return bounds_record_io(h, clear); }
+gma_status_t bounds_selftest(cudaStream_t st) {
+  GMA_LAUNCH("bounds_selftest", bounds_selftest_kernel, 1, 1, 0, st);
+  return check_launch("launch bounds_selftest", (const void*)bounds_selftest_kernel);
+}
+#else
+gma_status_t tc_bounds_io(unsigned long long*, bool) { return GMA_ERR_UNSUPPORTED; }
+gma_status_t bounds_selftest(cudaStream_t) { return GMA_ERR_UNSUPPORTED; }
+#endif
 
 void tc_set_fault_injection(uint32_t mask) {
   std::lock_guard<std::mutex> lock(g_fault_mu);

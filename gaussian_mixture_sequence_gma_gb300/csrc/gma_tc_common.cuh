@@ -18,6 +18,41 @@
 #define GMA_WAIT_SLEEP_NS 64
 #endif
 
+// ---------------------------------------------------------------------------------------------- bounds checks
+// Debug build (-DGMA_BOUNDS_CHECK): GMA_INB(i, n, site) is false when the element index i is not below n,
+// the extent the host planned for the buffer it indexes, and the caller then skips the access.  The first
+// failing site, its index and extent, and the number of failures go to this translation unit's record
+// (g_bounds), which gma_debug_bounds_read() collects; nothing traps.  In the normal build it is true.
+#ifdef GMA_BOUNDS_CHECK
+namespace gma {
+namespace {
+__device__ unsigned long long g_bounds[4];  // first site, its index, its extent; failures
+
+__device__ __noinline__ bool bounds_fail(unsigned long long i, unsigned long long n, unsigned site) {
+  if (atomicCAS(&g_bounds[0], 0ull, (unsigned long long)site) == 0ull) {
+    g_bounds[1] = i;
+    g_bounds[2] = n;
+  }
+  atomicAdd(&g_bounds[3], 1ull);
+  return false;
+}
+
+// Host side: copies this translation unit's record to h[4] (clear: then zeroes it).
+inline gma_status_t bounds_record_io(unsigned long long* h, bool clear) {
+  if (h && cudaMemcpyFromSymbol(h, g_bounds, sizeof g_bounds) != cudaSuccess) return GMA_ERR_CUDA;
+  static const unsigned long long zero[4] = {0, 0, 0, 0};
+  if (clear && cudaMemcpyToSymbol(g_bounds, zero, sizeof zero) != cudaSuccess) return GMA_ERR_CUDA;
+  return GMA_OK;
+}
+}  // namespace
+}  // namespace gma
+#define GMA_INB(i, n, site)                                        \
+  ((unsigned long long)(i) < (unsigned long long)(n) ||            \
+   ::gma::bounds_fail((unsigned long long)(i), (unsigned long long)(n), (site)))
+#else
+#define GMA_INB(i, n, site) true
+#endif
+
 namespace gma {
 namespace tc {
 

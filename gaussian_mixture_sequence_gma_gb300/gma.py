@@ -12,7 +12,9 @@ import os
 
 import torch
 
-_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libgma.so")
+# GMA_LIBRARY=checked loads the bounds-check debug build (libgma_checked.so) instead
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib",
+                         "libgma_checked.so" if os.environ.get("GMA_LIBRARY") == "checked" else "libgma.so")
 
 GMA_OK, GMA_ERR_INVALID_ARG, GMA_ERR_UNSUPPORTED, GMA_ERR_WORKSPACE, GMA_ERR_CUDA, GMA_ERR_TIMEOUT, GMA_ERR_RANGE = range(7)
 GMA_F32, GMA_BF16 = 0, 1
@@ -24,7 +26,8 @@ EXPORTED = ("gma_workspace_bytes", "gma_responsibilities", "gma_forward_bidir", 
             "gma_check_device_error", "gma_status_string", "gma_version", "gma_last_error", "gma_launch_count", "gma_profile_enable",
             "gma_profile_read", "gma_forward_bidir_static_ws", "gma_static_ws_capacity", "gma_static_ws_check_error",
             "gma_debug_withhold_first_load", "gma_probe_ex2_rate", "gma_set_wait_limit_ns", "gma_get_wait_limit_ns",
-            "gma_set_deterministic", "gma_get_deterministic")
+            "gma_set_deterministic", "gma_get_deterministic",
+            "gma_debug_bounds_read", "gma_debug_bounds_clear", "gma_debug_bounds_selftest")
 
 
 class GmaError(RuntimeError):
@@ -110,6 +113,12 @@ def lib():
     L.gma_set_wait_limit_ns.restype = ctypes.c_int
     L.gma_get_wait_limit_ns.argtypes = []
     L.gma_get_wait_limit_ns.restype = ctypes.c_uint64
+    L.gma_debug_bounds_read.argtypes = [ctypes.POINTER(ctypes.c_ulonglong)]
+    L.gma_debug_bounds_read.restype = ctypes.c_int
+    L.gma_debug_bounds_clear.argtypes = []
+    L.gma_debug_bounds_clear.restype = ctypes.c_int
+    L.gma_debug_bounds_selftest.argtypes = [ctypes.c_void_p]
+    L.gma_debug_bounds_selftest.restype = ctypes.c_int
     L.gma_set_deterministic.argtypes = [ctypes.c_int]
     L.gma_set_deterministic.restype = ctypes.c_int
     L.gma_get_deterministic.argtypes = []
@@ -459,6 +468,18 @@ def set_wait_limit_ns(ns: int) -> None:
 
 def wait_limit_ns() -> int:
     return int(lib().gma_get_wait_limit_ns())
+
+
+def bounds_record() -> tuple[int, int, int, int] | None:
+    """Bounds-check debug build: (first failing site, its index, its extent, failures); None in the
+    normal build."""
+    out = (ctypes.c_ulonglong * 4)()
+    st = int(lib().gma_debug_bounds_read(out))
+    if st == GMA_ERR_UNSUPPORTED:
+        return None
+    if st != GMA_OK:
+        raise GmaError(st, "gma_debug_bounds_read")
+    return tuple(int(v) for v in out)
 
 
 def set_deterministic(mode: int) -> None:

@@ -52,6 +52,21 @@ GMA_API gma_status_t gma_probe_ex2_rate(void *stream, double *exps_per_second);
  */
 GMA_API void gma_debug_withhold_first_load(void);
 
+/*
+ * Bounds-check debug build (libgma_checked.so, compiled with -DGMA_BOUNDS_CHECK).  In that build every
+ * computed global-memory index of the forward kernels (both paths: workspace sections, outputs, the
+ * float32 path's input rows) is compared with the extent the host planned for its buffer; a failed
+ * check skips the access and is recorded, nothing traps.  gma_debug_bounds_read() copies the record to
+ * out[4]: the first failing site (0: none), its index, its extent, and the number of failed checks
+ * since the last gma_debug_bounds_clear(); read it after the kernels have completed (for instance
+ * after cudaDeviceSynchronize()).  gma_debug_bounds_selftest()
+ * enqueues one kernel that fails one check on purpose (site 999, index 3, extent 3) without touching
+ * memory.  In the normal build all three return GMA_ERR_UNSUPPORTED.
+ */
+GMA_API gma_status_t gma_debug_bounds_read(unsigned long long *out);
+GMA_API gma_status_t gma_debug_bounds_clear(void);
+GMA_API gma_status_t gma_debug_bounds_selftest(void *stream);
+
 #ifdef __cplusplus
 }
 #endif

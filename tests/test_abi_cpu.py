@@ -454,3 +454,13 @@ def test_deterministic_environment_variable():
                              timeout=120)
         assert out.returncode == 0, out.stderr
         assert int(out.stdout.strip().splitlines()[-1]) == want, val
+
+
+def test_bounds_record_is_absent_from_the_normal_build(L):
+    """The bounds-check entry points exist in every build and answer GMA_ERR_UNSUPPORTED in the normal one."""
+    buf = (ctypes.c_ulonglong * 4)()
+    assert L.gma_debug_bounds_read(buf) == gma.GMA_ERR_UNSUPPORTED
+    assert L.gma_debug_bounds_clear() == gma.GMA_ERR_UNSUPPORTED
+    assert L.gma_debug_bounds_selftest(None) == gma.GMA_ERR_UNSUPPORTED
+    assert gma.bounds_record() is None
+    assert gma.lib_path().endswith("libgma.so")
