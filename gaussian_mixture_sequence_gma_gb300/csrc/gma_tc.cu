@@ -429,9 +429,11 @@ __device__ __forceinline__ void scale_pack_store(const float* v, float inv, uint
 // Fused pass for a TMEM-resident operand: e = 2^(v - m) packed to bf16 pairs and stored over this thread's
 // NC/2 columns starting at taddr (8 words per store).  The caller waits for the stores.
 template <int NC>
-__device__ __forceinline__ void exp_pack_tmem(const float* v, float m, uint32_t taddr) {
+__device__ __forceinline__ void exp_pack_tmem(const float* v, float m, uint32_t taddr, int c0 = 0,
+                                              int c1 = NC / 16) {
 #pragma unroll
   for (int c = 0; c < NC / 16; ++c) {
+    if (c < c0 || c >= c1) continue;
     uint32_t w[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -1360,7 +1362,8 @@ __host__ __device__ inline CausalLayout causal_layout(int Kp) {
 
 struct CBars {
   uint64_t w_full, xk_full, xk_empty, xq_full, xq_empty, v_full, v_empty;
-  uint64_t ak_full, ax_full, lk_full, lq_full, gk_full, gk_empty, gq_full, sb_full, s_done, p_full, pb_full, o_full;
+  uint64_t ak_full, ax_full, lk_full, lq_full, gk_full, gk_empty, gq_half, gq_full, sb_full, s_done, p_full, pb_full,
+      o_full;
   uint64_t o_staged, o_stored;
   uint64_t done[3];
   uint32_t tmem_base;
@@ -1427,6 +1430,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     mbar_init(&B.lq_full, 1);
     mbar_init(&B.gk_full, kRowWarps);
     mbar_init(&B.gk_empty, 2);   // the state update and P read Gamma_K
+    mbar_init(&B.gq_half, kRowWarps);
     mbar_init(&B.gq_full, kRowWarps);
     mbar_init(&B.sb_full, kRowWarps);
     mbar_init(&B.s_done, 1);
@@ -1554,7 +1558,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       bool ok = true;
       for (int t = 0; ok && t < T; ++t) {
         const uint32_t ph = t & 1;
-        if (!(ok = wait_bounded_bo(&B.gq_full, ph, &B.ab, a.ctrl, 87, a.wait_ns) &&
+        // the K-steps of the first chunks of every row part once those are written (gq_half), then the
+        // rest (as for P)
+        constexpr int kCpp = NC / 16, kHalf = kCpp > 1 ? kCpp / 2 : 1;
+        constexpr int kRest = kCpp - kHalf > 0 ? kCpp - kHalf : 1;
+        if (!(ok = wait_bounded_bo(&B.gq_half, ph, &B.ab, a.ctrl, 98, a.wait_ns) &&
                    wait_bounded_bo(&B.sb_full, ph, &B.ab, a.ctrl, 88, a.wait_ns)))
           break;
         GMA_TRACE_AT(30, t);
@@ -1562,8 +1570,17 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         // (the issuing thread waits ~100 cycles per instruction here, so a rolled loop costs nothing and
         // keeps this role's register footprint small)
 #pragma unroll 1
-        for (int ks = 0; ks < KS; ++ks)
-          mma_ts_off(tmem + kCColO, tmem + kColLog + 8 * ks, d_sb, (uint32_t)(512 * ks) >> 4, id_c80, ks > 0);
+        for (int i = 0; i < KS / kCpp * kHalf; ++i) {
+          const int ks = (i / kHalf) * kCpp + i % kHalf;
+          mma_ts_off(tmem + kCColO, tmem + kColLog + 8 * ks, d_sb, (uint32_t)(512 * ks) >> 4, id_c80, i > 0);
+        }
+        if (!(ok = wait_bounded_bo(&B.gq_full, ph, &B.ab, a.ctrl, 87, a.wait_ns))) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int i = 0; i < KS / kCpp * (kCpp - kHalf); ++i) {
+          const int ks = (i / kRest) * kCpp + kHalf + i % kRest;
+          mma_ts_off(tmem + kCColO, tmem + kColLog + 8 * ks, d_sb, (uint32_t)(512 * ks) >> 4, id_c80, 1u);
+        }
         mma_commit(&B.p_full);
         GMA_TRACE_AT(31, t);
         if (!(ok = wait_bounded_bo(&B.pb_full, ph, &B.ab, a.ctrl, 89, a.wait_ns) &&
@@ -1590,15 +1607,29 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       bool ok = true;
       for (int t = 0; ok && t < T; ++t) {
         const uint32_t ph = t & 1;
-        if (!(ok = wait_bounded_bo(&B.gq_full, ph, &B.ab, a.ctrl, 91, a.wait_ns) &&
+        // K-step ks reads chunk ks % (NC / 16) of row part ks / (NC / 16): the first chunks of every part
+        // are issued once the row warps have written them (gq_half), the rest after gq_full
+        constexpr int kCpp = NC / 16, kHalf = kCpp > 1 ? kCpp / 2 : 1;
+        if (!(ok = wait_bounded_bo(&B.gq_half, ph, &B.ab, a.ctrl, 97, a.wait_ns) &&
                    wait_bounded_bo(&B.gk_full, ph, &B.ab, a.ctrl, 92, a.wait_ns)))
           break;
         GMA_TRACE_AT(40, t);
         tc_fence_after();
 #pragma unroll 1
-        for (int ks = 0; ks < KS; ++ks)
+        for (int i = 0; i < KS / kCpp * kHalf; ++i) {
+          const int ks = (i / kHalf) * kCpp + i % kHalf;
           mma_ts_off(tmem + kCColP, tmem + kColLog + 8 * ks, d_gk_k, (uint32_t)((ks >> 2) * 16384 + (ks & 3) * 32) >> 4,
-                     id_p, ks > 0);
+                     id_p, i > 0);
+        }
+        constexpr int kRest = kCpp - kHalf > 0 ? kCpp - kHalf : 1;  // the loop below is empty when kCpp == 1
+        if (!(ok = wait_bounded_bo(&B.gq_full, ph, &B.ab, a.ctrl, 91, a.wait_ns))) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int i = 0; i < KS / kCpp * (kCpp - kHalf); ++i) {
+          const int ks = (i / kRest) * kCpp + kHalf + i % kRest;
+          mma_ts_off(tmem + kCColP, tmem + kColLog + 8 * ks, d_gk_k, (uint32_t)((ks >> 2) * 16384 + (ks & 3) * 32) >> 4,
+                     id_p, 1u);
+        }
         mma_commit(&B.p_full);
         mma_commit(&B.gk_empty);
         GMA_TRACE_AT(41, t);
@@ -1728,7 +1759,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       const float m_q = xchg_max(rc, s0, mq);
       if (warp == kRowWarp0) GMA_TRACE_AT(11, t);
       if (ok) {
-        exp_pack_tmem<NC>(v, m_q, tmem + rc.lane_base + kColLog + (NC / 2) * rc.part);
+        // in two halves of this thread's chunks: P starts on the K-steps of the first half meanwhile
+        constexpr int kHalf = NC / 16 > 1 ? NC / 32 : 1;
+        const uint32_t tq = tmem + rc.lane_base + kColLog + (NC / 2) * rc.part;
+        exp_pack_tmem<NC>(v, m_q, tq, 0, kHalf);
+        tmem_st_wait();
+        tc_fence_before();
+        warp_arrive(&B.gq_half);
+        exp_pack_tmem<NC>(v, m_q, tq, kHalf, NC / 16);
         tmem_st_wait();
         tc_fence_before();
         warp_arrive(&B.gq_full);
