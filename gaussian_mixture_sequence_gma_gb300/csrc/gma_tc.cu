@@ -1863,8 +1863,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   }
 }
 
-// Exclusive scan over segments: agg[bh][p][e] <- sum_{p' < p} agg[bh][p'][e].  grid (ceil(n / 256), B*H).
-// Each thread has all loads of up to 32 segments in flight before the first store.
+// Exclusive scan over segments: agg[bh][p][e] <- sum_{p' < p} agg[bh][p'][e].  grid (ceil(n / 128), B*H),
+// one thread per element.  Its loads go in batches of eight segments, all eight in flight; a batch's
+// stores may alias the next batch's loads, so each batch is one round trip to L2.
 // 128 threads of at most 32 registers, so that its CTAs fit beside a running aggregate CTA and start the
 // moment that grid completes.
 __global__ void __launch_bounds__(128, 16) tc_scan_kernel(float* agg, int P, int n, size_t lim) {
