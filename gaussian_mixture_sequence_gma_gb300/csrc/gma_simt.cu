@@ -1156,10 +1156,15 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_causal_key_kernel(
 // Parameter-gradient sums: grid (ceil(K / 32), H, ctas).  The rows of head h (queries then keys of every
 // batch entry, 2 B N in all) are split into ranges of rows_per_cta; a CTA walks its range in tiles of at
 // most T rows that stay within one (side, batch entry) and loads the next tile into registers while it
-// works on the current one.  Thread (k within a block of 32, group of 8 dims) sums dl_k (x_d - mu_kd)
-// and dl_k (x_d - mu_kd)^2 and adds them into pacc[h][k][d][2] (and b_k into pb[h][k]); with zstride > 0
-// (the deterministic reduction mode) it stores them instead into the slice of its row range, at
-// pacc + blockIdx.z * zstride (and pb + blockIdx.z * zstride).
+// works on the current one.  The sums are taken in the expanded form, so that one thread's row loads
+// serve several components: thread (half, kq, dg) accumulates, for components 4 kq .. 4 kq + 3 of the
+// block and dims 4 dg .. 4 dg + 3, sum dl_k x_d, sum dl_k x_d^2 and sum dl_k over the rows of its half
+// (even or odd rows of each tile).  The halves are added in a fixed order at the end, and then
+//   sum dl_k (x_d - mu_kd)   = sum dl_k x_d - mu_kd sum dl_k,
+//   sum dl_k (x_d - mu_kd)^2 = sum dl_k x_d^2 - 2 mu_kd sum dl_k x_d + mu_kd^2 sum dl_k,
+// added into pacc[h][k][d][2] (and sum dl_k into pb[h][k]); with zstride > 0 (the deterministic reduction
+// mode) stored instead into the slice of its row range, at pacc + blockIdx.z * zstride (and pb + ...).
+// In float32 the expansion loses at most about (|x| / |x - mu|)^2 ulps to cancellation.
 template <typename IO>
 __global__ void __launch_bounds__(kThreads) simt_bwd_param_kernel(const IO* __restrict__ Q, const IO* __restrict__ Kx,
                                                                   const float* __restrict__ mu, const float* dlq,
@@ -1167,19 +1172,19 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_param_kernel(const IO* __re
                                                                   long long rows_per_cta, float* pacc, float* pb,
                                                                   size_t zstride) {
   __shared__ __align__(16) float xs[T * kD];
-  __shared__ float ds[T * 32];
+  __shared__ __align__(16) float ds[T * 32];
+  __shared__ float part[128 * 36];  // the odd-row half's sums, handed to the even-row half
   const int h = blockIdx.y, k0 = blockIdx.x * 32;
-  const int kl = threadIdx.x & 31, dg = threadIdx.x >> 5;  // 8 groups of 8 dims
-  const int k = k0 + kl;
+  const int dg = threadIdx.x & 15, kq = (threadIdx.x >> 4) & 7, half = threadIdx.x >> 7;
   const int fi = threadIdx.x >> 3, fc = threadIdx.x & 7;  // fetch: row fi, dims 8 fc .. 8 fc + 7, dl 4 fc .. 4 fc + 3
   const long long total = 2LL * B * N;
   const long long r0 = (long long)blockIdx.z * rows_per_cta, r1 = min(total, r0 + rows_per_cta);
-  float m[8], a1[8], a2[8], bsum = 0.f;
+  float a1[4][4], a2[4][4], bs[4];
 #pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    m[q] = k < K ? __ldg(mu + ((size_t)h * K + k) * kD + dg * 8 + q) : 0.f;
-    a1[q] = 0.f;
-    a2[q] = 0.f;
+  for (int j = 0; j < 4; ++j) {
+    bs[j] = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) a1[j][q] = a2[j][q] = 0.f;
   }
   // the tile starting at virtual row rb: its row count, and this thread's share of x and dl
   auto fetch = [&](long long rb, int& n, float (&xv)[8], float (&dv)[4]) {
@@ -1206,41 +1211,78 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_param_kernel(const IO* __re
     __syncthreads();  // the previous tile's readers are done
     *reinterpret_cast<float4*>(xs + fi * kD + 8 * fc) = make_float4(xv[0], xv[1], xv[2], xv[3]);
     *reinterpret_cast<float4*>(xs + fi * kD + 8 * fc + 4) = make_float4(xv[4], xv[5], xv[6], xv[7]);
-#pragma unroll
-    for (int t = 0; t < 4; ++t) ds[fi * 32 + 4 * fc + t] = dv[t];
+    *reinterpret_cast<float4*>(ds + fi * 32 + 4 * fc) = make_float4(dv[0], dv[1], dv[2], dv[3]);
     __syncthreads();
     rb += ncur;
     if (rb < r1) fetch(rb, n, xv, dv);  // in flight while this tile is summed
-#pragma unroll 4
-    for (int i = 0; i < ncur; ++i) {
-      const float dl = ds[i * 32 + kl];
-      bsum += dl;
-      const float4 x0 = *reinterpret_cast<const float4*>(xs + i * kD + dg * 8);
-      const float4 x1 = *reinterpret_cast<const float4*>(xs + i * kD + dg * 8 + 4);
-      const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll 2
+    for (int i = half; i < ncur; i += 2) {
+      const float4 x4 = *reinterpret_cast<const float4*>(xs + i * kD + 4 * dg);
+      const float4 d4 = *reinterpret_cast<const float4*>(ds + i * 32 + 4 * kq);
+      const float x[4] = {x4.x, x4.y, x4.z, x4.w}, d[4] = {d4.x, d4.y, d4.z, d4.w};
+      float x2[4];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float diff = x[q] - m[q];
-        const float t = dl * diff;
-        a1[q] += t;
-        a2[q] = fmaf(t, diff, a2[q]);
+      for (int q = 0; q < 4; ++q) x2[q] = x[q] * x[q];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        bs[j] += d[j];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          a1[j][q] = fmaf(d[j], x[q], a1[j][q]);
+          a2[j][q] = fmaf(d[j], x2[q], a2[j][q]);
+        }
       }
     }
   }
-  if (k < K && zstride > 0) {
-    const size_t zo = (size_t)blockIdx.z * zstride;
+  // the odd-row half hands its sums over; the even-row half adds them (a fixed order) and finishes
+  const int slot = threadIdx.x & 127;
+  if (half == 1) {
 #pragma unroll
-    for (int q = 0; q < 8; ++q)
-      *reinterpret_cast<float2*>(pacc + zo + (((size_t)h * K + k) * kD + dg * 8 + q) * 2) = make_float2(a1[q], a2[q]);
-    if (dg == 0) pb[zo + (size_t)h * K + k] = bsum;
-  } else if (k < K) {
+    for (int j = 0; j < 4; ++j) {
+      part[(j * 9) * 128 + slot] = bs[j];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      float* dst = pacc + (((size_t)h * K + k) * kD + dg * 8 + q) * 2;
-      atomicAdd(dst, a1[q]);
-      atomicAdd(dst + 1, a2[q]);
+      for (int q = 0; q < 4; ++q) {
+        part[(j * 9 + 1 + q) * 128 + slot] = a1[j][q];
+        part[(j * 9 + 5 + q) * 128 + slot] = a2[j][q];
+      }
     }
-    if (dg == 0) atomicAdd(pb + (size_t)h * K + k, bsum);
+  }
+  __syncthreads();
+  if (half == 1) return;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    bs[j] += part[(j * 9) * 128 + slot];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      a1[j][q] += part[(j * 9 + 1 + q) * 128 + slot];
+      a2[j][q] += part[(j * 9 + 5 + q) * 128 + slot];
+    }
+  }
+  const size_t zo = zstride > 0 ? (size_t)blockIdx.z * zstride : 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int k = k0 + 4 * kq + j;
+    if (k >= K) break;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int d = 4 * dg + q;
+      const float m = __ldg(mu + ((size_t)h * K + k) * kD + d);
+      const float c1 = fmaf(-m, bs[j], a1[j][q]);                        // sum dl (x - mu)
+      const float c2 = fmaf(m * m, bs[j], fmaf(-2.f * m, a1[j][q], a2[j][q]));  // sum dl (x - mu)^2
+      float* dst = pacc + zo + (((size_t)h * K + k) * kD + d) * 2;
+      if (zstride > 0) {
+        *reinterpret_cast<float2*>(dst) = make_float2(c1, c2);
+      } else {
+        atomicAdd(dst, c1);
+        atomicAdd(dst + 1, c2);
+      }
+    }
+    if (dg == 0) {
+      if (zstride > 0)
+        pb[zo + (size_t)h * K + k] = bs[j];
+      else
+        atomicAdd(pb + (size_t)h * K + k, bs[j]);
+    }
   }
 }
 
