@@ -573,7 +573,7 @@ def run_gma(args, world, rank, local):
             "frac_of_bf16_peak": (gemm_flop + gma_flop) / t_p / 1e12 / peaks["bf16"],
             "note": "projection = one tcgen05 GEMM with bias and layout in its epilogue (bf16 Q, K, V round-trip HBM)"}
         del tp, wsp, outp, qkv
-        # backward pass of the bidirectional form (float32 CUDA-core kernels) on the bidir bf16 workload shape
+        # backward pass of the bidirectional form on the bidir bf16 workload shape
         wb = workloads()["bidir_bf16_B4H8N4096K128"]
         bi = to_dev(make_workload(wb), dev)
         gO = torch.randn((wb.B, wb.H, wb.N, 64), device=dev).to(torch.bfloat16)
@@ -590,7 +590,7 @@ def run_gma(args, world, rank, local):
         extensions["backward_bidir_bf16_B4H8N4096K128"] = {
             "ms": mb / 5, "tok_heads_per_s": wb.B * wb.H * wb.N / (mb / 5 * 1e-3), "forward_ms": mf / 5,
             "backward_over_forward": mb / mf, "workspace_bytes": wsb.numel(),
-            "note": "float32 CUDA-core kernels (no tensor cores yet)"}
+            "note": "state and key responsibilities by the tensor-core forward kernels; query, key and parameter passes in float32 on the CUDA cores"}
         del wsb
         pbc = gma.problem(wb.B, wb.H, wb.N, wb.K, torch.bfloat16, wb.eps)
         wsc = gma.alloc_workspace(pbc, gma.OP_BACKWARD_CAUSAL, dev)
@@ -605,7 +605,7 @@ def run_gma(args, world, rank, local):
         extensions["backward_causal_bf16_B4H8N4096K128"] = {
             "ms": mc / 3, "tok_heads_per_s": wb.B * wb.H * wb.N / (mc / 3 * 1e-3), "forward_ms": mfc / 5,
             "backward_over_forward": (mc / 3) / (mfc / 5), "workspace_bytes": wsc.numel(),
-            "note": "float32 CUDA-core kernels (no tensor cores yet)"}
+            "note": "float32 CUDA-core kernels"}
         del bi, gO, wsc
 
     # CPU baseline: the oracle as it stands on a bounded sample of the same workload (rank 0 only).

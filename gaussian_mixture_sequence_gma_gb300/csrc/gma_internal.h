@@ -65,9 +65,10 @@ struct TcPlan {
 TcPlan tc_plan(const gma_problem_t& p, gma_op_t op, bool det = false);
 // clear_err: the parameter fold clears the workspace error word first (false when an earlier kernel of
 // the same call, the tcgen05 projection, has already cleared it and may have reported into it).
+// ctrl: the control block the kernels report into (null: the one at the start of ws).
 gma_status_t tc_run(const gma_problem_t& p, gma_op_t op, int Nk, const void* Q, const void* K, const void* V,
                     const float* mu, const float* sigma2, const float* log_pi, void* out, void* ws,
-                    cudaStream_t stream, bool clear_err = true, bool det = false);
+                    cudaStream_t stream, bool clear_err = true, bool det = false, Ctrl* ctrl = nullptr);
 bool tc_available();
 // Tensor map over a row-major bf16 matrix [rows][cols]: boxes of box_cols x box_rows, 128-byte swizzle,
 // zero fill outside (a 3-D map with a unit outer dimension, read with 3-D tensor loads).

@@ -1554,11 +1554,13 @@ __global__ void __launch_bounds__(kDecodeThreads) simt_decode_kernel(const IO* _
 // only; one area, used by the two in turn) and pz slices of the parameter sums (pacc then pb, one slice
 // per range of rows).
 constexpr int kParamSlices = 16;
+// bf16 I/O, bidirectional: last, the workspace of the tensor-core state write and responsibilities
+// (off_tc), which compute the state and every key's gamma_K in place of the float32 write pass.
 struct BwdPlan {
   size_t off_params, off_state, off_dstate, off_pacc, off_pb, off_u, off_dlq, off_dlk, off_wpair, off_gq;
-  size_t off_part, off_ppart, pstride, total;  // pstride: floats per slice of the parameter sums
+  size_t off_part, off_ppart, pstride, off_tc, total;  // pstride: floats per slice of the parameter sums
   int splits, seg_tiles, tiles, pz;
-  bool det;
+  bool det, tc_front;
 };
 BwdPlan bwd_plan(const gma_problem_t& p, bool causal, bool det) {
   BwdPlan b{};
@@ -1597,6 +1599,11 @@ BwdPlan bwd_plan(const gma_problem_t& p, bool causal, bool det) {
     b.pz = (int)std::max(1LL, std::min<long long>(kParamSlices, (rows + T - 1) / T));
     b.total = align_up(b.off_ppart + (size_t)b.pz * b.pstride * sizeof(float));
   }
+  b.tc_front = p.dtype == GMA_BF16 && !causal && p.N > 0 && tc_available();
+  b.off_tc = b.total;
+  if (b.tc_front)
+    b.total = align_up(b.off_tc + std::max(tc_plan(p, GMA_OP_CAUSAL_STATE, det).total,
+                                           tc_plan(p, GMA_OP_RESPONSIBILITIES, det).total));
   return b;
 }
 
@@ -1650,11 +1657,13 @@ template <typename IO, int KC>
 gma_status_t backward_bidir_kc(const gma_problem_t& p, const BwdPlan& b, const IO* Q, const IO* Kx, const IO* V,
                                const IO* dO, IO* dQ, IO* dK, IO* dV, float* params, const float2* wpair, float* state,
                                float* dstate, float* dlq, float* dlk, float* part, cudaStream_t st) {
+  const bool write = !b.tc_front;  // else the state and gamma_K are already in place
   const int BH = p.B * p.H, K = p.K, tiles = cdiv(p.N, T), npairs = K * kStateCols;
   int splits = 1, seg = 1;
   const size_t sm_w = (size_t)(T * kD + T * kDv + T * KC) * sizeof(float);
   const auto wfn = simt_write_kernel<IO, KC>;
-  if (part) {
+  if (!write) {
+  } else if (part) {
     if (gma_status_t e = launch_write_kc<IO, KC>(b.splits, BH, st, Kx, V, params, p.H, p.N, K, b.seg_tiles, part, 0,
                                                  dlk))
       return e;
@@ -1750,6 +1759,17 @@ gma_status_t backward_typed(const gma_problem_t& p, bool causal, const IO* Q, co
   GMA_LAUNCH("simt_prep", simt_prep_kernel, 148, 256, 0, st, mu, sigma2, log_pi, p.H, K, params, (Ctrl*)base, zero,
              zero_n, wpair);
   if (gma_status_t e = check_launch("launch simt_prep", (const void*)simt_prep_kernel)) return e;
+  if (b.tc_front) {
+    // bf16 I/O, bidirectional: the tensor-core kernels write the state [B*H][K][65] and every key's
+    // gamma_K [B*H][N][K] (where the key side expects them), reporting into this workspace's error word
+    void* tws = base + b.off_tc;
+    if (gma_status_t e = tc_run(p, GMA_OP_CAUSAL_STATE, p.N, nullptr, Kx, V, mu, sigma2, log_pi, state, tws, st, false,
+                                det, (Ctrl*)base))
+      return e;
+    if (gma_status_t e = tc_run(p, GMA_OP_RESPONSIBILITIES, p.N, Kx, nullptr, nullptr, mu, sigma2, log_pi, dlk, tws, st,
+                                false, det, (Ctrl*)base))
+      return e;
+  }
   int pz_used = 1;  // slices of the parameter sums the finish adds up (1: the zeroed or atomic sums)
   if (p.N > 0) {
     if (causal) {

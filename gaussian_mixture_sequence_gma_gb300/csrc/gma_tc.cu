@@ -926,9 +926,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1) tc_resp_kernel(const __grid_con
         const size_t i0 = ((size_t)bh * a.N + tok) * a.K + NC * rc.part;
         float* dst = reinterpret_cast<float*>(a.out) + i0;
         const int nk = min(max(a.K - NC * rc.part, 0), NC);
+        if ((a.K & 3) == 0) {  // 16-byte aligned row segments (nk a multiple of 4 too): vector stores
 #pragma unroll
-        for (int k = 0; k < NC; ++k)
-          if (k < nk && GMA_INB(i0 + k, a.lim.out, 120)) dst[k] = v[k] * r;
+          for (int k = 0; k < NC; k += 4)
+            if (k < nk && GMA_INB(i0 + k + 3, a.lim.out, 120))
+              *reinterpret_cast<float4*>(dst + k) = make_float4(v[k] * r, v[k + 1] * r, v[k + 2] * r, v[k + 3] * r);
+        } else {
+#pragma unroll
+          for (int k = 0; k < NC; ++k)
+            if (k < nk && GMA_INB(i0 + k, a.lim.out, 120)) dst[k] = v[k] * r;
+        }
       }
     }
   }
@@ -2142,7 +2149,7 @@ TcPlan tc_plan(const gma_problem_t& p, gma_op_t op, bool det) {
 
 gma_status_t tc_run(const gma_problem_t& p, gma_op_t op, int Nk, const void* Q, const void* K, const void* V,
                     const float* mu, const float* sigma2, const float* log_pi, void* out, void* ws,
-                    cudaStream_t st, bool clear_err, bool det) {
+                    cudaStream_t st, bool clear_err, bool det, Ctrl* ctrl) {
   const TcPlan pl = tc_plan(p, op, det);
   const int BH = p.B * p.H;
   char* base = (char*)ws;
@@ -2151,7 +2158,7 @@ gma_status_t tc_run(const gma_problem_t& p, gma_op_t op, int Nk, const void* Q, 
   a.cbias = (const float*)(base + pl.off_c);
   a.range_flags = (const uint32_t*)(base + pl.off_flags);
   a.state = (float*)(base + pl.off_state);
-  a.ctrl = (Ctrl*)base;
+  a.ctrl = ctrl ? ctrl : (Ctrl*)base;
   a.out = out;
   a.H = p.H;
   a.N = p.N;
