@@ -723,7 +723,7 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_query_kernel(const IO* __re
                                                                   int H, int N, int K, int seg_tiles,
                                                                   const float* __restrict__ state, float eps,
                                                                   float* dstate, int dsplits, float* dlq,
-                                                                  IO* __restrict__ dQ) {
+                                                                  IO* __restrict__ dQ, int gpre) {
   constexpr int RK = KC / 32;
   extern __shared__ float sm[];
   float* S = sm;            // [KC][kSP]  Vt image
@@ -748,8 +748,13 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_query_kernel(const IO* __re
     __syncthreads();
     load_rows<IO>(Q + (size_t)unit * N * kD, t0, nvalid, xs);
     load_rows<IO>(dO + (size_t)unit * N * kDv, t0, nvalid, gs);
+    // gamma_Q: recomputed, or (gpre) the rows the tensor-core responsibilities kernel left in dlq, which
+    // this tile overwrites with dl_Q below
+    if (gpre)
+      load_tile_rows<KC>(dlq + ((size_t)unit * N + t0) * K, nvalid, K, G);
     __syncthreads();
-    gamma_tile_kc<KC, 2>(xs, nvalid, P, h, K, G);
+    if (!gpre) gamma_tile_kc<KC, 2>(xs, nvalid, P, h, K, G);
+    __syncthreads();
     {  // numerators and denominators of the warp's rows, then dn | dd (rows past N: zero)
       float a[4][2], dp[4] = {0.f, 0.f, 0.f, 0.f};
       rows_times_image<KC>(G, S, i0, a);
@@ -1685,7 +1690,7 @@ gma_status_t backward_bidir_kc(const gma_problem_t& p, const BwdPlan& b, const I
     return e;
   }
   GMA_LAUNCH("simt_bwd_query", qfn, dim3(splits, BH), kThreads, sm_q, st, Q, dO, params, wpair, p.H, p.N, K, seg,
-             state, p.eps, part ? part : dstate, part ? splits : 0, dlq, dQ);
+             state, p.eps, part ? part : dstate, part ? splits : 0, dlq, dQ, b.tc_front ? 1 : 0);
   if (gma_status_t e = check_launch("launch simt_bwd_query", (const void*)qfn)) return e;
   if (part) {
     GMA_LAUNCH("simt_state_sum", simt_state_sum_kernel, dim3(cdiv(npairs, 256), BH), 256, 0, st, part, splits, npairs,
@@ -1768,6 +1773,9 @@ gma_status_t backward_typed(const gma_problem_t& p, bool causal, const IO* Q, co
       return e;
     if (gma_status_t e = tc_run(p, GMA_OP_RESPONSIBILITIES, p.N, Kx, nullptr, nullptr, mu, sigma2, log_pi, dlk, tws, st,
                                 false, det, (Ctrl*)base))
+      return e;
+    if (gma_status_t e = tc_run(p, GMA_OP_RESPONSIBILITIES, p.N, Q, nullptr, nullptr, mu, sigma2, log_pi, dlq, tws, st,
+                                false, det, (Ctrl*)base))  // gamma_Q, read by the query side
       return e;
   }
   int pz_used = 1;  // slices of the parameter sums the finish adds up (1: the zeroed or atomic sums)
