@@ -590,7 +590,7 @@ def run_gma(args, world, rank, local):
         extensions["backward_bidir_bf16_B4H8N4096K128"] = {
             "ms": mb / 5, "tok_heads_per_s": wb.B * wb.H * wb.N / (mb / 5 * 1e-3), "forward_ms": mf / 5,
             "backward_over_forward": mb / mf, "workspace_bytes": wsb.numel(),
-            "note": "state and key responsibilities by the tensor-core forward kernels; query, key and parameter passes in float32 on the CUDA cores"}
+            "note": "state and responsibilities by the tensor-core forward kernels; query, key and parameter passes in float32 on the CUDA cores"}
         del wsb
         pbc = gma.problem(wb.B, wb.H, wb.N, wb.K, torch.bfloat16, wb.eps)
         wsc = gma.alloc_workspace(pbc, gma.OP_BACKWARD_CAUSAL, dev)

@@ -262,7 +262,7 @@ GMA_API gma_status_t gma_causal_decode_prepared(const gma_problem_t *p, const vo
  * (softplus, log-softmax) applies its own chain rule on top.
  *   Q, K, V, mu, sigma2, log_pi, eps: as gma_forward_bidir;  dO [B,H,N,dv] in p->dtype.
  * Computed in float32 on the CUDA cores; with bf16 I/O the state Gamma_K^T [V | 1] and every key's
- * gamma_K come from the tensor-core forward kernels (so the parameter-range check of the bf16 forward,
+ * and query's gamma come from the tensor-core forward kernels (so the parameter-range check of the bf16 forward,
  * GMA_ERR_RANGE, applies).  The workspace, gma_workspace_bytes(p, GMA_OP_BACKWARD_BIDIR), grows with N
  * (it holds the per-row softmax gradients, 8 B*H*N*K bytes, and with bf16 I/O the tensor-core
  * kernels' workspace).
