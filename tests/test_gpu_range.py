@@ -130,3 +130,27 @@ def test_fp16_overflow_reports_range_status(gma, op):
     out = call(t).float().cpu().numpy()
     assert gma.check_device_error(ws) == gma.GMA_OK
     assert np.isfinite(out).all()
+
+
+def test_bf16_backward_reports_range_status_and_recovers(gma):
+    """The bf16 bidirectional backward takes its state and responsibilities from the tensor-core kernels,
+    so a parameter beyond fp16 is reported as GMA_ERR_RANGE in its workspace; a following call with
+    valid parameters on the same workspace reports nothing and its gradients match a fresh call's (up to
+    the rounding order of the atomic reductions: a bf16 ulp here and there)."""
+    import torch
+    inp = make_inputs(1, 2, 300, 64, dtype="bf16", seed=71)
+    bad = dict(inp)
+    bad["sigma2"] = inp["sigma2"].copy()
+    bad["sigma2"][0, 3, 11] = 1e-6
+    t, tb = to_device(inp), to_device(bad)
+    dO = torch.randn(t["V"].shape, device="cuda").to(torch.bfloat16)
+    prob = gma.problem(1, 2, 300, 64, torch.bfloat16, 1e-6)
+    ws = gma.alloc_workspace(prob, gma.OP_BACKWARD_BIDIR, "cuda")
+    args = lambda x: (x["Q"], x["K"], x["V"], x["mu"], x["sigma2"], x["log_pi"], dO)
+    gma.backward_bidir(*args(tb), workspace=ws)
+    assert gma.check_device_error(ws) == gma.GMA_ERR_RANGE
+    got = gma.backward_bidir(*args(t), workspace=ws)
+    assert gma.check_device_error(ws) == gma.GMA_OK
+    ref = gma.backward_bidir(*args(t))
+    for a, b in zip(got, ref):
+        assert rel_err(a.float().cpu().numpy(), b.float().cpu().numpy()) <= 1e-3
